@@ -1,0 +1,193 @@
+// fp64 CPU oracle for fp8 paged decode attention.
+//
+// TEST INFRASTRUCTURE ONLY. This file is the parity reference for the CUDA
+// decode path and shares no code, header, table or helper with it. Only the
+// test suite, the smoke check and the benchmark's CPU-baseline leg may load it.
+//
+// What it computes (the plain definition, no splitting, no blocking):
+//   for every sequence s and query head h, with kv = h / g (g = H / Hk) and
+//   L = seq_lens[s]:
+//     k_t[d] = E4M3(K byte of token t, dim d) * k_scale
+//     v_t[d] = E4M3(V byte of token t, dim d) * v_scale
+//     z_t    = scale * sum_d q[s][h][d] * k_t[d]                 (t < L)
+//     out[s][h][d] = sum_t exp(z_t - max z) v_t[d] / sum_t exp(z_t - max z)
+//   all in IEEE binary64. L = 0 gives a zero row.
+//
+// Sources for each part:
+//  * single-query paged attention over seq_lens / block_table with a softmax
+//    scale and K/V descale factors: vLLM API page
+//    "vllm.v1.attention.backends.rocm_aiter_unified_attn",
+//    RocmAiterUnifiedAttentionImpl.forward (the unified_attention call with
+//    q, k, v, seqused_k, softmax_scale, block_table, k_descale, v_descale).
+//  * page layout of an fp8 cache: vLLM pull request lishuoshuo-amd/vllm#3,
+//    section "Details", item "Layout": K as [blocks, kv_heads, head_size/16,
+//    16, 16] and V as [blocks, kv_heads, head_size, 16] for 16-token blocks.
+//    The K intra-page order [dim/16][token][dim%16] follows the same API
+//    page's _shuffle_kv_views (K viewed as (nb, nkv, hd//x, bs, x) with
+//    x = 16 one-byte elements). For block sizes above 16 the V page is read
+//    as [head_size][block_size], the direct generalisation of the item above.
+//  * per-tensor scales broadcast to every slot: same pull request, section
+//    "Details", item "Scale tables".
+//  * fp8 flavour: OCP FP8 E4M3 ("e4m3fn": bias 7, no infinities, S.1111.111
+//    is NaN, largest finite 448), the format the API page lists as fp8_e4m3.
+//  * consecutive query heads share a kv head (h / g): the API page's forward
+//    passes num_kv_heads K/V heads for num_heads query heads; the grouping
+//    rule itself is not printed there, and h / g is the reading taken.
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+namespace {
+
+// OCP FP8 E4M3 decode from the format's definition: sign bit, 4-bit
+// exponent with bias 7, 3-bit mantissa; exponent 0 is subnormal
+// (2^-6 * m/8); exponent 15 with mantissa 7 is NaN (no infinities).
+double e4m3_value(uint8_t code) {
+  const int sign = (code >> 7) & 1;
+  const int expo = (code >> 3) & 0xF;
+  const int mant = code & 0x7;
+  double mag;
+  if (expo == 0xF && mant == 0x7) {
+    return std::nan("");
+  } else if (expo == 0) {
+    mag = std::ldexp(static_cast<double>(mant) / 8.0, -6);
+  } else {
+    mag = std::ldexp(1.0 + static_cast<double>(mant) / 8.0, expo - 7);
+  }
+  return sign ? -mag : mag;
+}
+
+// bfloat16 is the upper half of an IEEE binary32: widen and reinterpret.
+double bf16_value(uint16_t bits) {
+  const uint32_t u = static_cast<uint32_t>(bits) << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return static_cast<double>(f);
+}
+
+}  // namespace
+
+extern "C" {
+
+// Status codes returned by the oracle entry points.
+enum {
+  PDA_ORACLE_OK = 0,
+  PDA_ORACLE_BAD_SHAPE = -1,      // non-positive sizes, H % Hk != 0, D % 16 != 0
+  PDA_ORACLE_BAD_SEQ_LEN = -2,    // seq_lens[s] < 0 or > max_num_blocks_per_seq * block_size
+  PDA_ORACLE_BAD_BLOCK_ID = -3,   // a block id a sequence uses is outside [0, num_blocks)
+  PDA_ORACLE_BAD_SEQ_ID = -4,     // a requested sequence index is outside [0, num_seqs)
+};
+
+double pda_oracle_e4m3_value(uint8_t code) { return e4m3_value(code); }
+double pda_oracle_bf16_value(uint16_t bits) { return bf16_value(bits); }
+
+// Decode attention for the sequences listed in seq_ids (all of them when
+// seq_ids is NULL). out is [n_out][num_heads][head_size] binary64 with
+// n_out = n_ids (or num_seqs). Layouts (all row-major, unpadded):
+//   q            [num_seqs][num_heads][head_size] bfloat16 bit patterns
+//   k_cache      [num_blocks][num_kv_heads][head_size/16][block_size][16] e4m3 bytes
+//   v_cache      [num_blocks][num_kv_heads][head_size][block_size] e4m3 bytes
+//   block_tables [num_seqs][max_num_blocks_per_seq] int32 physical block ids
+//   seq_lens     [num_seqs] int32
+// Only the first ceil(seq_lens[s] / block_size) entries of a table row are
+// read; only token slots t < seq_lens[s] are read from a page.
+int pda_oracle_decode(double* out, const uint16_t* q, const uint8_t* k_cache,
+                      const uint8_t* v_cache, const int32_t* block_tables,
+                      const int32_t* seq_lens, int num_seqs, int num_heads,
+                      int num_kv_heads, int head_size, int block_size,
+                      int max_num_blocks_per_seq, long long num_blocks,
+                      double scale, double k_scale, double v_scale,
+                      const int32_t* seq_ids, int n_ids, int num_threads) {
+  if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_size <= 0 ||
+      block_size <= 0 || max_num_blocks_per_seq < 0 || num_blocks < 0 ||
+      num_heads % num_kv_heads != 0 || head_size % 16 != 0) {
+    return PDA_ORACLE_BAD_SHAPE;
+  }
+  const int n_out = seq_ids ? n_ids : num_seqs;
+  const int g = num_heads / num_kv_heads;
+  const int D = head_size;
+  const long long bs = block_size;
+  const long long MB = max_num_blocks_per_seq;
+
+  // Validate every sequence the call will read before any work.
+  for (int i = 0; i < n_out; ++i) {
+    const int s = seq_ids ? seq_ids[i] : i;
+    if (s < 0 || s >= num_seqs) return PDA_ORACLE_BAD_SEQ_ID;
+    const long long L = seq_lens[s];
+    if (L < 0 || L > MB * bs) return PDA_ORACLE_BAD_SEQ_LEN;
+    const long long pages = (L + bs - 1) / bs;
+    for (long long j = 0; j < pages; ++j) {
+      const long long b = block_tables[s * MB + j];
+      if (b < 0 || b >= num_blocks) return PDA_ORACLE_BAD_BLOCK_ID;
+    }
+  }
+
+  const long long rows = static_cast<long long>(n_out) * num_heads;
+#ifdef _OPENMP
+  const int nt = num_threads > 0 ? num_threads : omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
+#endif
+  for (long long r = 0; r < rows; ++r) {
+    const int i = static_cast<int>(r / num_heads);
+    const int h = static_cast<int>(r % num_heads);
+    const int s = seq_ids ? seq_ids[i] : i;
+    const int kv = h / g;
+    const long long L = seq_lens[s];
+    double* o = out + r * D;
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    if (L == 0) continue;
+
+    std::vector<double> qd(D);
+    for (int d = 0; d < D; ++d) qd[d] = bf16_value(q[(static_cast<long long>(s) * num_heads + h) * D + d]);
+
+    // Logits z_t = scale * q . k_t.
+    std::vector<double> z(L);
+    for (long long t = 0; t < L; ++t) {
+      const long long b = block_tables[s * MB + t / bs];
+      const long long slot = t % bs;
+      const uint8_t* kpage = k_cache + (b * num_kv_heads + kv) * static_cast<long long>(D) * bs;
+      double acc = 0.0;
+      for (int d = 0; d < D; ++d) {
+        const uint8_t code = kpage[(static_cast<long long>(d / 16) * bs + slot) * 16 + (d % 16)];
+        acc += qd[d] * (e4m3_value(code) * k_scale);
+      }
+      z[t] = scale * acc;
+    }
+
+    // softmax(z) . V
+    double zmax = z[0];
+    for (long long t = 1; t < L; ++t) zmax = z[t] > zmax ? z[t] : zmax;
+    double denom = 0.0;
+    std::vector<double> w(L);
+    for (long long t = 0; t < L; ++t) {
+      w[t] = std::exp(z[t] - zmax);
+      denom += w[t];
+    }
+    for (long long t = 0; t < L; ++t) {
+      const long long b = block_tables[s * MB + t / bs];
+      const long long slot = t % bs;
+      const uint8_t* vpage = v_cache + (b * num_kv_heads + kv) * static_cast<long long>(D) * bs;
+      const double wt = w[t] / denom;
+      for (int d = 0; d < D; ++d) {
+        o[d] += wt * (e4m3_value(vpage[static_cast<long long>(d) * bs + slot]) * v_scale);
+      }
+    }
+  }
+  return PDA_ORACLE_OK;
+}
+
+int pda_oracle_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+}  // extern "C"

@@ -1,0 +1,283 @@
+"""Pins that tie the fp64 oracle to something other than itself.
+
+Each ``pin_*`` function takes an oracle library handle and raises
+``AssertionError`` when the oracle disagrees with the independent fact it
+checks. They are shared by ``test_oracle.py`` (the real oracle must pass all
+of them) and ``test_oracle_mutants.py`` (each planted mistake must fail at
+least one of them).
+
+Independent facts used:
+* PyTorch's own float8_e4m3fn -> float64 conversion and the OCP E4M3 spot
+  values under ``tests/golden/``;
+* dense attention on contiguous, unpaged tensors computed with torch fp64
+  ``softmax`` and ``einsum`` (library routines), with the paged cache built
+  from the dense tensors by this module's own scatter that follows the page
+  layout statement (K as [blocks, kv_heads, head_size/16, 16, 16], V as
+  [blocks, kv_heads, head_size, block_size]);
+* closed forms: constant V, a single token, K == 0 (uniform weights);
+* invariances: physical-block permutation, poisoned tail slots.
+"""
+
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def load_spot_values():
+    rows = []
+    with open(os.path.join(GOLDEN, "e4m3_spot_values.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            code, val = line.split()
+            rows.append((int(code, 16), float(val)))
+    return rows
+
+
+def torch_e4m3(codes: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(codes.astype(np.uint8)))
+    return t.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+# ----------------------------------------------------------------- inputs
+
+def dense_case(S, Hq, Hk, lens, D=128, seed=0, code_lo=None):
+    """Random dense q (bf16 bits) and K/V e4m3 codes [S, Hk, Lmax, D]."""
+    rng = np.random.default_rng(seed)
+    Lmax = max(max(lens), 1)
+    q = torch.from_numpy(rng.standard_normal((S, Hq, D)).astype(np.float32)).to(torch.bfloat16)
+    qbits = q.view(torch.int16).numpy().view(np.uint16).copy()
+
+    def codes(shape):
+        x = torch.from_numpy((rng.standard_normal(shape) / 0.05).clip(-448, 448).astype(np.float32))
+        return x.to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
+
+    return qbits, codes((S, Hk, Lmax, D)), codes((S, Hk, Lmax, D))
+
+
+def scatter_pages(Kc, Vc, lens, bs, *, seed=0, pool_factor=1.5, extra_cols=0, fill=None):
+    """Lay dense codes out as a paged cache with a shuffled block table.
+
+    K page of block b, kv head k: bytes [d/16][slot][d%16]; V page: [d][slot].
+    Slots past a sequence's length and unused blocks get random codes (or
+    ``fill`` when given).
+    """
+    rng = np.random.default_rng(seed + 1000)
+    S, Hk, Lmax, D = Kc.shape
+    pages = [(L + bs - 1) // bs for L in lens]
+    NB = max(1, int(math.ceil(pool_factor * max(1, sum(pages)))))
+    MB = max(1, max(pages)) + extra_cols
+    if fill is None:
+        k_cache = rng.integers(0, 256, size=(NB, Hk, D // 16, bs, 16), dtype=np.uint8)
+        v_cache = rng.integers(0, 256, size=(NB, Hk, D, bs), dtype=np.uint8)
+    else:
+        k_cache = np.full((NB, Hk, D // 16, bs, 16), fill, dtype=np.uint8)
+        v_cache = np.full((NB, Hk, D, bs), fill, dtype=np.uint8)
+    perm = rng.permutation(NB).astype(np.int32)
+    tables = np.zeros((S, MB), dtype=np.int32)
+    off = 0
+    for s in range(S):
+        for j in range(pages[s]):
+            b = perm[off]
+            off += 1
+            tables[s, j] = b
+            n = min(bs, lens[s] - j * bs)
+            kp = Kc[s, :, j * bs:j * bs + n, :]            # [Hk, n, D]
+            vp = Vc[s, :, j * bs:j * bs + n, :]
+            k_cache[b, :, :, :n, :] = kp.reshape(Hk, n, D // 16, 16).transpose(0, 2, 1, 3)
+            v_cache[b, :, :, :n] = vp.transpose(0, 2, 1)
+    return k_cache, v_cache, tables, np.asarray(lens, dtype=np.int32)
+
+
+def dense_reference(qbits, Kc, Vc, lens, scale, k_scale, v_scale):
+    """softmax(q K^T * scale) V on contiguous tensors, torch fp64."""
+    q = torch.from_numpy(qbits.view(np.int16)).view(torch.bfloat16).to(torch.float64)
+    Kd = torch.from_numpy(torch_e4m3(Kc)) * k_scale
+    Vd = torch.from_numpy(torch_e4m3(Vc)) * v_scale
+    S, H, D = q.shape
+    Hk = Kd.shape[1]
+    g = H // Hk
+    out = torch.zeros(S, H, D, dtype=torch.float64)
+    for s in range(S):
+        L = int(lens[s])
+        if L == 0:
+            continue
+        Kh = Kd[s, :, :L].repeat_interleave(g, dim=0)   # [H, L, D]
+        Vh = Vd[s, :, :L].repeat_interleave(g, dim=0)
+        z = torch.einsum("hld,hd->hl", Kh, q[s]) * scale
+        p = torch.softmax(z, dim=-1)
+        out[s] = torch.einsum("hl,hld->hd", p, Vh)
+    return out.numpy()
+
+
+def run(lib, qbits, k_cache, v_cache, tables, lens, scale, k_scale, v_scale, **kw):
+    return oracle.decode(qbits, k_cache, v_cache, tables, lens, scale=scale, k_scale=k_scale,
+                         v_scale=v_scale, lib=lib, **kw)
+
+
+# ------------------------------------------------------------------- pins
+
+def pin_e4m3_table(lib):
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch_e4m3(codes)
+    got = np.array([lib.pda_oracle_e4m3_value(int(c)) for c in codes])
+    nan_ref, nan_got = np.isnan(ref), np.isnan(got)
+    assert np.array_equal(nan_ref, nan_got), "NaN codes differ"
+    assert np.array_equal(ref[~nan_ref], got[~nan_got]), "finite e4m3 values differ from torch"
+    assert np.array_equal(np.signbit(ref[~nan_ref]), np.signbit(got[~nan_got])), "signed zero differs"
+    for code, val in load_spot_values():
+        g = lib.pda_oracle_e4m3_value(code)
+        if math.isnan(val):
+            assert math.isnan(g), hex(code)
+        else:
+            assert g == val and math.copysign(1, g) == math.copysign(1, val), (hex(code), g, val)
+
+
+def pin_bf16(lib):
+    rng = np.random.default_rng(3)
+    x = torch.from_numpy(rng.standard_normal(4096).astype(np.float32) * 10).to(torch.bfloat16)
+    bits = x.view(torch.int16).numpy().view(np.uint16)
+    ref = x.to(torch.float64).numpy()
+    got = np.array([lib.pda_oracle_bf16_value(int(b)) for b in bits])
+    assert np.array_equal(ref, got)
+
+
+DENSE_CASES = [
+    # (S, Hq, Hk, lens, bs, scale, k_scale, v_scale, extra table columns)
+    (1, 1, 1, [1], 16, 0.3, 0.05, 0.05, 0),
+    (2, 4, 4, [16, 17], 16, 1 / math.sqrt(128), 0.05, 0.07, 1),
+    (3, 8, 2, [5, 40, 33], 16, 1 / math.sqrt(128), 0.04, 0.05, 2),
+    (2, 5, 1, [31, 16], 16, 0.2, 0.05, 0.05, 0),
+    (2, 16, 2, [70, 64], 64, 1 / math.sqrt(128), 0.05, 0.03, 1),
+    (3, 8, 8, [1, 2, 129], 64, 0.1, 0.06, 0.05, 3),
+]
+
+
+def pin_dense(lib, cases=DENSE_CASES, tol=1e-12):
+    for i, (S, Hq, Hk, lens, bs, scale, ks, vs, extra) in enumerate(cases):
+        qbits, Kc, Vc = dense_case(S, Hq, Hk, lens, seed=10 + i)
+        kc, vc, tb, ln = scatter_pages(Kc, Vc, lens, bs, seed=i, extra_cols=extra)
+        got = run(lib, qbits, kc, vc, tb, ln, scale, ks, vs)
+        ref = dense_reference(qbits, Kc, Vc, lens, scale, ks, vs)
+        err = np.max(np.abs(got - ref)) if got.size else 0.0
+        assert np.all(np.isfinite(got)), "non-finite oracle output (case %d)" % i
+        assert err <= tol * max(1.0, np.max(np.abs(ref))), "case %d: max |oracle - dense| = %g" % (i, err)
+
+
+def pin_large_logits(lib):
+    """Logits of magnitude ~1e3 (exp overflows binary64 past ~709) need the max shift."""
+    lens = [20, 3]
+    qbits, Kc, Vc = dense_case(2, 4, 2, lens, seed=77)
+    kc, vc, tb, ln = scatter_pages(Kc, Vc, lens, 16, seed=5)
+    scale = 150.0
+    got = run(lib, qbits, kc, vc, tb, ln, scale, 0.05, 0.05)
+    ref = dense_reference(qbits, Kc, Vc, lens, scale, 0.05, 0.05)
+    assert np.all(np.isfinite(got)), "non-finite output for large logits"
+    assert np.max(np.abs(got - ref)) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
+
+
+def pin_permutation_invariance(lib):
+    lens = [37, 80, 16]
+    qbits, Kc, Vc = dense_case(3, 8, 2, lens, seed=21)
+    a = scatter_pages(Kc, Vc, lens, 16, seed=1)
+    b = scatter_pages(Kc, Vc, lens, 16, seed=2)
+    assert not np.array_equal(a[2], b[2])
+    oa = run(lib, qbits, *a, 0.09, 0.05, 0.05)
+    ob = run(lib, qbits, *b, 0.09, 0.05, 0.05)
+    assert np.array_equal(oa, ob), "output depends on physical block placement"
+
+
+def pin_constant_v(lib):
+    lens = [45, 7]
+    qbits, Kc, Vc = dense_case(2, 8, 2, lens, seed=31)
+    rng = np.random.default_rng(9)
+    col = rng.integers(0, 0x7E, size=(2, 2, 1, 128), dtype=np.uint8)   # finite codes
+    Vc = np.broadcast_to(col, Vc.shape).copy()
+    kc, vc, tb, ln = scatter_pages(Kc, Vc, lens, 16, seed=3)
+    vs = 0.05
+    got = run(lib, qbits, kc, vc, tb, ln, 0.088, 0.05, vs)
+    val = torch_e4m3(col[:, :, 0, :]) * vs     # [S, Hk, D]
+    want = np.repeat(val, 4, axis=1)            # g = 4
+    assert np.max(np.abs(got - want)) <= 1e-12 * max(1.0, np.max(np.abs(want)))
+
+
+def pin_single_token(lib):
+    lens = [1, 1]
+    qbits, Kc, Vc = dense_case(2, 4, 2, lens, seed=41)
+    kc, vc, tb, ln = scatter_pages(Kc, Vc, lens, 16, seed=4)
+    vs = 0.05
+    got = run(lib, qbits, kc, vc, tb, ln, 0.088, 0.05, vs)
+    want = np.repeat(torch_e4m3(Vc[:, :, 0, :]) * vs, 2, axis=1)
+    assert np.array_equal(got, want), "one-token context must return v_0 exactly"
+
+
+def pin_zero_k(lib):
+    lens = [33, 64]
+    qbits, Kc, Vc = dense_case(2, 8, 2, lens, seed=51)
+    Kc[:] = 0
+    kc, vc, tb, ln = scatter_pages(Kc, Vc, lens, 16, seed=6)
+    vs = 0.05
+    got = run(lib, qbits, kc, vc, tb, ln, 0.088, 0.05, vs)
+    Vd = torch_e4m3(Vc) * vs
+    want = np.zeros_like(got)
+    for s, L in enumerate(lens):
+        want[s] = np.repeat(Vd[s, :, :L, :].mean(axis=1), 4, axis=0)
+    assert np.max(np.abs(got - want)) <= 1e-12
+
+
+def pin_tail_poison(lib):
+    """Slots past seq_len and table entries past the last page are never read."""
+    lens = [19, 50, 16]
+    qbits, Kc, Vc = dense_case(3, 4, 2, lens, seed=61)
+    kc, vc, tb, ln = scatter_pages(Kc, Vc, lens, 16, seed=7, extra_cols=2)
+    base = run(lib, qbits, kc, vc, tb, ln, 0.088, 0.05, 0.05)
+    for code in (0x7F, 0x7E, 0xFE):
+        kc2, vc2 = kc.copy(), vc.copy()
+        for s, L in enumerate(lens):
+            P = (L + 15) // 16
+            n = L - (P - 1) * 16
+            b = tb[s, P - 1]
+            kc2[b, :, :, n:, :] = code
+            vc2[b, :, :, n:] = code
+        tb2 = tb.copy()
+        for s, L in enumerate(lens):
+            tb2[s, (L + 15) // 16:] = -1     # never dereferenced
+        got = run(lib, qbits, kc2, vc2, tb2, ln, 0.088, 0.05, 0.05)
+        assert np.array_equal(got, base), "tail slot contents leaked into the output (code %#x)" % code
+
+
+def pin_gqa_is_repeated_mha(lib):
+    """g query heads per kv head == MHA on K/V heads repeated g times."""
+    lens = [23, 48]
+    qbits, Kc, Vc = dense_case(2, 8, 2, lens, seed=71)
+    g = 4
+    kc, vc, tb, ln = scatter_pages(Kc, Vc, lens, 16, seed=8)
+    got = run(lib, qbits, kc, vc, tb, ln, 0.1, 0.05, 0.05)
+    kc_m = np.repeat(kc, g, axis=1)
+    vc_m = np.repeat(vc, g, axis=1)
+    mha = run(lib, qbits, kc_m, vc_m, tb, ln, 0.1, 0.05, 0.05)
+    assert np.array_equal(got, mha)
+
+
+def pin_zero_length(lib):
+    lens = [0, 5]
+    qbits, Kc, Vc = dense_case(2, 4, 1, lens, seed=81)
+    kc, vc, tb, ln = scatter_pages(Kc, Vc, lens, 16, seed=9)
+    got = run(lib, qbits, kc, vc, tb, ln, 0.1, 0.05, 0.05)
+    assert np.all(got[0] == 0.0)
+    ref = dense_reference(qbits, Kc, Vc, lens, 0.1, 0.05, 0.05)
+    assert np.max(np.abs(got - ref)) <= 1e-12
+
+
+ALL_PINS = [pin_e4m3_table, pin_bf16, pin_dense, pin_large_logits, pin_permutation_invariance,
+            pin_constant_v, pin_single_token, pin_zero_k, pin_tail_poison, pin_gqa_is_repeated_mha,
+            pin_zero_length]

@@ -1,0 +1,62 @@
+"""Planted mistakes in a copy of the oracle must each fail a pin (CPU only).
+
+Every mutant is a one-line textual change to ``oracle/pda_oracle.cpp``
+compiled into a temporary library; the real source is never modified. This
+shows the pins in ``oracle_pins.py`` are strong enough to catch a dropped
+term, a wrong sign or index, or a transposed operand.
+"""
+
+import os
+
+import pytest
+
+import oracle
+from tests import oracle_pins as P
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "pda_oracle.cpp")
+
+MUTANTS = {
+    "dropped_k_scale": ("acc += qd[d] * (e4m3_value(code) * k_scale);", "acc += qd[d] * e4m3_value(code);"),
+    "dropped_v_scale": ("(e4m3_value(vpage[static_cast<long long>(d) * bs + slot]) * v_scale)",
+                        "e4m3_value(vpage[static_cast<long long>(d) * bs + slot])"),
+    "dropped_softmax_scale": ("z[t] = scale * acc;", "z[t] = acc;"),
+    "wrong_sign": ("z[t] = scale * acc;", "z[t] = -scale * acc;"),
+    "k_page_token_major": ("kpage[(static_cast<long long>(d / 16) * bs + slot) * 16 + (d % 16)]",
+                           "kpage[(slot * (D / 16) + d / 16) * 16 + (d % 16)]"),
+    "v_page_token_major": ("vpage[static_cast<long long>(d) * bs + slot]", "vpage[slot * D + d]"),
+    "gqa_modulo": ("const int kv = h / g;", "const int kv = h % num_kv_heads;"),
+    "e4m3_bias_8": ("mag = std::ldexp(1.0 + static_cast<double>(mant) / 8.0, expo - 7);",
+                    "mag = std::ldexp(1.0 + static_cast<double>(mant) / 8.0, expo - 8);"),
+    "e4m3_subnormal_as_normal": ("mag = std::ldexp(static_cast<double>(mant) / 8.0, -6);",
+                                 "mag = std::ldexp(1.0 + static_cast<double>(mant) / 8.0, -7);"),
+    "no_max_shift": ("w[t] = std::exp(z[t] - zmax);", "w[t] = std::exp(z[t]);"),
+    "table_row_stride_pages": ("const long long b = block_tables[s * MB + t / bs];\n      const long long slot = t % bs;\n      const uint8_t* kpage",
+                               "const long long b = block_tables[s * ((L + bs - 1) / bs) + t / bs];\n      const long long slot = t % bs;\n      const uint8_t* kpage"),
+    "one_token_short": ("std::vector<double> z(L);\n    for (long long t = 0; t < L; ++t) {",
+                        "std::vector<double> z(L);\n    z[L - 1] = -1e300;\n    for (long long t = 0; t + 1 < L; ++t) {"),
+}
+
+
+@pytest.fixture(scope="module")
+def src_text():
+    with open(SRC) as f:
+        return f.read()
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, src_text, tmp_path):
+    old, new = MUTANTS[name]
+    assert src_text.count(old) >= 1, "mutation anchor not found: %s" % name
+    mutated = src_text.replace(old, new, 1)
+    src = tmp_path / "mutant.cpp"
+    src.write_text(mutated)
+    lib_path = str(tmp_path / "libmutant.so")
+    oracle.build(force=True, src=str(src), out=lib_path)
+    lib = oracle.load(lib_path)
+    caught = []
+    for pin in P.ALL_PINS:
+        try:
+            pin(lib)
+        except (AssertionError, oracle.OracleError):
+            caught.append(pin.__name__)
+    assert caught, "mutant %s passed every pin" % name
