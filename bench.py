@@ -1,0 +1,441 @@
+"""Benchmark: fp8 paged decode attention on GB300, one JSON line on stdout.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config NAME]
+
+A step is one ``pda_decode`` call (split plan, page gather, dequant, QK^T,
+online softmax, PV, CTA merge, partial store / LSE merge) over one batch of
+synthetic input already resident in HBM. Steps are captured in CUDA graphs
+(the pages time "impl.forward in a CUDA graph, us per call") and replayed;
+the timed region is bracketed by a barrier and device synchronisation and
+timed with CUDA events on the replay stream. Under torchrun every rank is an
+independent replica on its own GPU (decode attention has no exchange step):
+the value is the bytes all ranks moved over the slowest rank's time.
+
+``--impl reference`` times the fp64 CPU oracle (the parity reference) on the
+host cores instead, on bounded samples of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "µs/call and achieved HBM GB/s (% of GB300 peak) for fp8 paged decode attention"
+UNIT = "GB/s"
+# The pages' own figure for the same workload (32/8 heads, ctx 4096, 256
+# sequences, fp8 cache, 16-token blocks): 362.53 us/call for the asm kernel
+# on AMD MI355X, i.e. this many GB/s for the same byte count. Context only.
+PAGES_GBS_SAME_WORKLOAD = 2_151_941_120 / 362.53e-6 / 1e9
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=workloads.HEADLINE, choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_decode_pda_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it is for this kernel source."""
+    p = os.path.join(ROOT, "profiles", "decode_kernel_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("source_sha") != kernel_source_sha():
+        return None
+    ent = d.get("per_workload", {}).get(workload)
+    if not ent:
+        return None
+    return float(ent["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling around the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="pda_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        load = [x for x, p in zip(sm, pw)] if sm else []
+        return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None, "samples": len(rows), "reasons": sorted(reasons)}
+
+
+def oracle_sample_rate(batch, budget_s: float, max_seqs: int | None = None):
+    """Time the fp64 oracle on the first n sequences of the batch, n grown
+    until about budget_s of wall time; returns (GB/s, description, cores)."""
+    import oracle
+
+    cfg = batch.cfg
+    raw = batch.raw()
+    threads = oracle.max_threads()
+    n = 1
+    S = cfg.num_seqs if max_seqs is None else min(cfg.num_seqs, max_seqs)
+    while True:
+        ids = list(range(n))
+        t0 = time.perf_counter()
+        oracle.decode(**raw, scale=cfg.scale, k_scale=cfg.k_scale, v_scale=cfg.v_scale, seq_ids=ids)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s or n >= S:
+            break
+        n = min(S, max(n + 1, int(n * min(8.0, budget_s / max(dt, 1e-3)))))
+    lens = [batch.seq_lens_host[i] for i in ids]
+    sub = workloads.algorithmic_bytes(cfg.with_(num_seqs=n), lens)
+    desc = "%d of %d sequences (all %d heads, their full contexts), %.2f s, %d OpenMP threads" % (
+        n, cfg.num_seqs, cfg.num_heads, dt, threads)
+    return sub / dt / 1e9, desc, threads, n, dt
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, ws, rank, local):
+    import paged_kv_decode_pda_gb300 as pda
+    from paged_kv_decode_pda_gb300 import build
+
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    build.build()
+    pda.load()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    cfg = workloads.CONFIGS[args.config]
+    batch = workloads.make_batch(cfg, device=dev, seed=cfg.seed + rank)
+    bytes_per_call = workloads.algorithmic_bytes(cfg, batch.seq_lens_host)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    kv_bytes = batch.k_cache.numel() + batch.v_cache.numel()
+    replicas = max(1, math.ceil(3 * l2 / kv_bytes))
+    caches = [(batch.k_cache, batch.v_cache)] + [(batch.k_cache.clone(), batch.v_cache.clone())
+                                                 for _ in range(replicas - 1)]
+    nsplit = pda.plan_splits(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq,
+                             cfg.block_size)
+    kernels_per_call = 1 + (1 if nsplit > 1 else 0)
+    stream = torch.cuda.Stream(device=dev)
+    out = torch.empty_like(batch.q)
+    pda.reserve(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq, cfg.block_size,
+                stream=stream)
+
+    def call(i):
+        kc, vc = caches[i % replicas]
+        pda.decode(batch.q, kc, vc, batch.block_tables, batch.seq_lens, cfg.scale, cfg.k_scale, cfg.v_scale,
+                   out=out, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            call(i)
+    stream.synchronize()
+    assert pda.query_device_status(stream) == 0
+
+    # Graphs: one of `chunk` calls (each bracketed by its own kernel events), one for the remainder.
+    K = args.steps
+    chunk = min(K, 100)
+    ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(chunk)]
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                if n == chunk:
+                    pda.set_profile_events(*ev_pairs[i])
+                call(i)
+                pda.set_profile_events(None, None)
+        return g
+
+    g_main = capture(chunk)
+    rem = K % chunk
+    g_rem = capture(rem) if rem else None
+    with torch.cuda.stream(stream):
+        g_main.replay()
+    stream.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for _ in range(K // chunk):
+            g_main.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        t_end.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    kern_ms = [a.elapsed_time(b) for a, b in ev_pairs]
+    assert pda.query_device_status(stream) == 0
+
+    if ws > 1:
+        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    # ---- end to end through the public API from pinned host buffers
+    e2e = None
+    if args.e2e_steps > 0:
+        host = {k: v.detach().cpu().pin_memory() for k, v in
+                dict(q=batch.q, k=batch.k_cache, v=batch.v_cache, t=batch.block_tables, l=batch.seq_lens).items()}
+        dev_bufs = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+        out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+
+        def e2e_step():
+            for k in host:
+                dev_bufs[k].copy_(host[k], non_blocking=True)
+            pda.decode(dev_bufs["q"], dev_bufs["k"], dev_bufs["v"], dev_bufs["t"], dev_bufs["l"], cfg.scale,
+                       cfg.k_scale, cfg.v_scale, out=out, stream=stream)
+            out_host.copy_(out, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            e2e_step()
+        stream.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(args.e2e_steps):
+                e2e_step()
+            e1.record(stream)
+        stream.synchronize()
+        e2e_ms = e0.elapsed_time(e1)
+        if ws > 1:
+            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": ws * bytes_per_call * args.e2e_steps / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms / args.e2e_steps,
+               "path": "pinned host -> cudaMemcpyAsync -> pda_decode -> cudaMemcpyAsync -> pinned host"}
+        del dev_bufs, host
+
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    peak, peak_kind = peaks()
+    kern_mean_ms = statistics.fmean(kern_ms)
+    achieved = bytes_per_call / (kern_mean_ms * 1e-3) / 1e9
+    traffic = ncu_traffic(cfg.name)
+    value = ws * bytes_per_call * K / (elapsed_ms * 1e-3) / 1e9
+    us_per_call = elapsed_ms * 1e3 / K
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        rate, desc, cores, _, _ = oracle_sample_rate(batch, budget_s=10.0)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": ws,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / K,
+        "us_per_call": us_per_call,
+        "frac_of_peak_hbm": value / ws / peak,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": value / ws / PAGES_GBS_SAME_WORKLOAD,
+        "vs_baseline_note": "pages' asm kernel on AMD MI355X, 362.53 us/call for this workload (context only)",
+        "dtype": "e4m3 KV / bf16 q -> f16 MMA, fp32 accumulate, bf16 out",
+        "data": "synthetic (seeded N(0,1) q; K/V N(0,1) quantised to e4m3 with scale 0.05; shuffled block tables)",
+        "config": {"workload": cfg.name, "num_seqs": cfg.num_seqs, "num_heads": cfg.num_heads,
+                   "num_kv_heads": cfg.num_kv_heads, "head_size": cfg.head_size, "block_size": cfg.block_size,
+                   "ctx": cfg.ctx if cfg.ctx else list(cfg.ctx_range), "kv_splits": nsplit,
+                   "bytes_per_call": bytes_per_call,
+                   "l2": "KV pool %.2f GB x %d replica(s) >= 3x L2 (%d MB); no flush needed" % (
+                       kv_bytes / 1e9, replicas, l2 >> 20),
+                   "timing": "CUDA graphs of %d calls replayed; events on the replay stream" % chunk,
+                   "parallelism": "replicas x%d" % ws},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
+                     "kernel": "pda_split_decode_kernel", "kernel_us_mean": kern_mean_ms * 1e3,
+                     "kernel_launches_timed": len(kern_ms), "algorithmic_bytes_per_launch": bytes_per_call},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": clocks,
+        "gpu_launches": K * kernels_per_call,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ---------------------------------------------------------- reference arm
+
+def run_reference(args, ws, rank, local):
+    if rank != 0:
+        return
+    import oracle
+
+    cfg = workloads.CONFIGS[args.config]
+    batch = workloads.make_batch(cfg, device="cpu")
+    raw = batch.raw()
+    # Size each step so the whole run stays within about three minutes.
+    budget_total = 180.0
+    per_step = max(0.02, budget_total / max(1, args.steps + args.warmup))
+    _, _, cores, n, dt = oracle_sample_rate(batch, budget_s=per_step)
+    ids = list(range(n))
+    lens = [batch.seq_lens_host[i] for i in ids]
+    sample_bytes = workloads.algorithmic_bytes(cfg.with_(num_seqs=n), lens)
+
+    def step():
+        oracle.decode(**raw, scale=cfg.scale, k_scale=cfg.k_scale, v_scale=cfg.v_scale, seq_ids=ids)
+
+    for _ in range(args.warmup):
+        step()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        step()
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = sample_bytes * args.steps / total / 1e9
+    desc = "%d of %d sequences (all %d heads, full contexts) per step, %d OpenMP threads" % (
+        n, cfg.num_seqs, cfg.num_heads, cores)
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total * 1e3 / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (same generator and seed as the CUDA arm)",
+        "config": {"workload": cfg.name, "sample": desc},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, ws, rank, local)
+    else:
+        run_ours(args, ws, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,182 @@
+/*
+ * pda.h -- fp8 paged decode attention for NVIDIA GB300 (sm_103a), C ABI.
+ *
+ * One call computes single-query ("decode") attention for a batch of
+ * sequences whose keys and values sit in a paged fp8 cache:
+ *
+ *   out[s][h][:] = softmax_t( scale * q[s][h] . k_t ) . v_t ,  t < seq_lens[s]
+ *
+ * with k_t, v_t the e4m3 cache bytes of token t times k_scale / v_scale,
+ * gathered page by page through block_tables, and query head h reading kv
+ * head h / (num_heads / num_kv_heads).
+ *
+ * Sources. What the call computes and its argument roles follow the vLLM API
+ * page "vllm.v1.attention.backends.rocm_aiter_unified_attn"
+ * (RocmAiterUnifiedAttentionImpl.forward: q, k, v, out, seqused_k,
+ * softmax_scale, block_table, k_descale, v_descale). The cache layout follows
+ * vLLM pull request lishuoshuo-amd/vllm#3 ("Details", item "Layout"): for an
+ * fp8 cache, K as [blocks, kv_heads, head_size/16, 16, 16] and V as
+ * [blocks, kv_heads, head_size, 16] with 16-token blocks, pages addressed by
+ * a dense page stride. The K intra-page order (token-major inside each
+ * 16-dimension chunk) is the one the API page's _shuffle_kv_views gives
+ * (K viewed as (nb, nkv, hd//x, bs, x), x = 16 bytes). Per-tensor scales
+ * follow the pull request's "Scale tables" item (a table filled with the
+ * per-tensor scale); block sizes that are multiples of 16 follow the API
+ * page's supports_block_size / customize_spec; GQA ratios up to 8 follow the
+ * pull request's "Claims" and "Cut and precision" items.
+ *
+ * Threading and ordering. Every entry point is thread-safe. pda_decode is
+ * stream-ordered: it validates on the host, enqueues its kernels on `stream`
+ * and returns without synchronising the host, reading device memory from the
+ * host, or allocating (once the workspace is large enough), so it can be
+ * captured in a CUDA graph. Errors detected on the host return before any
+ * launch; nothing is written to `out` then.
+ */
+#ifndef PDA_H_
+#define PDA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same opaque handle types as the CUDA runtime's (identical typedefs). */
+typedef struct CUstream_st* cudaStream_t;
+typedef struct CUevent_st* cudaEvent_t;
+
+typedef enum pda_status {
+  PDA_OK = 0,
+  PDA_ERR_INVALID_ARG = 1,     /* null / misaligned pointer, negative size, H % Hk != 0 */
+  PDA_ERR_UNSUPPORTED = 2,     /* valid but outside the supported set (see pda_decode) */
+  PDA_ERR_WORKSPACE = 3,       /* workspace must grow while the stream is being captured */
+  PDA_ERR_CUDA = 4,            /* a CUDA runtime call or kernel launch failed */
+  PDA_ERR_DEVICE_TIMEOUT = 5   /* a kernel gave up on a bounded wait (pda_query_device_status) */
+} pda_status;
+
+/*
+ * pda_decode -- decode attention over a paged fp8 KV cache.
+ *
+ * Device pointers (all on the device that is current for the calling thread
+ * and that owns `stream`; each 16-byte aligned; row-major, unpadded):
+ *   out           bf16  [num_seqs][num_heads][head_size]          written
+ *   q             bf16  [num_seqs][num_heads][head_size]          read
+ *   k_cache       e4m3  [num_blocks][num_kv_heads][head_size/16][block_size][16]  read
+ *   v_cache       e4m3  [num_blocks][num_kv_heads][head_size][block_size]          read
+ *   block_tables  int32 [num_seqs][max_num_blocks_per_seq]        read
+ *   seq_lens      int32 [num_seqs]                                read
+ * e4m3 is OCP FP8 E4M3 (torch.float8_e4m3fn). Sequence s reads the first
+ * ceil(seq_lens[s] / block_size) entries of its table row and, in its last
+ * page, only the slots below seq_lens[s]; other slots and entries may hold
+ * anything. A sequence with seq_lens[s] == 0 gets a zero output row.
+ *
+ * Scalars: scale is the softmax scale (1/sqrt(head_size) for plain
+ * attention); k_scale and v_scale multiply the e4m3 values on dequantisation
+ * (value = e4m3 * scale), i.e. the k/v "descale" of the API page.
+ *
+ * max_num_blocks_per_seq is the row stride of block_tables. It is not in the
+ * argument list the method states; it is required to index a [S, MB] table
+ * and gives the host an upper bound on context length without reading
+ * seq_lens back from the device (which would synchronise).
+ *
+ * Supported set: head_size == 128; block_size a multiple of 16, 16..128;
+ * num_heads % num_kv_heads == 0 with a ratio of 1..8; num_seqs >= 0
+ * (0 returns PDA_OK with no launch); seq_lens[s] <= max_num_blocks_per_seq *
+ * block_size and every used block id in [0, num_blocks) are the caller's
+ * contract (the kernel never reads past a table row and clamps lengths to
+ * the row's capacity; it does not know num_blocks).
+ *
+ * Ownership: the caller owns every buffer. The library owns an internal
+ * per-(device, stream) workspace for split partials; it grows with
+ * cudaMallocAsync on `stream` when a call needs more and the stream is not
+ * capturing (PDA_ERR_WORKSPACE if it is; size it first with pda_reserve).
+ *
+ * Determinism: for fixed inputs and a fixed split count the result is
+ * bitwise reproducible. The split count depends on num_seqs * num_kv_heads
+ * and max_num_blocks_per_seq, so a sequence's result may change in the last
+ * bits with the batch it shares a call with.
+ *
+ * Returns PDA_OK, PDA_ERR_INVALID_ARG, PDA_ERR_UNSUPPORTED,
+ * PDA_ERR_WORKSPACE or PDA_ERR_CUDA (launch failure).
+ */
+pda_status pda_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                      int num_heads, int num_kv_heads, int head_size, int block_size,
+                      int max_num_blocks_per_seq, float scale, float k_scale, float v_scale,
+                      cudaStream_t stream);
+
+/* Static text for a status code; never NULL. */
+const char* pda_status_string(int status);
+
+/*
+ * pda_choose_splits -- the split-count heuristic (pure, host only).
+ *
+ * Returns how many KV splits each (sequence, kv head) work unit is cut into
+ * for a batch of num_seqs * num_kv_heads units with at most
+ * max_num_blocks_per_seq pages of block_size tokens, on a device with
+ * sm_count SMs that hold ctas_per_sm decode CTAs each. The cut mirrors the
+ * pull request's dispatch rule ("Claims": work units compared with twice the
+ * compute-unit count): split only while the units alone leave SMs idle,
+ * never below a minimum page count per split. Result in
+ * [1, max(1, max_num_blocks_per_seq)]. Invalid arguments return 1.
+ */
+int pda_choose_splits(int num_seqs, int num_kv_heads, int max_num_blocks_per_seq, int block_size,
+                      int sm_count, int ctas_per_sm);
+
+/*
+ * pda_plan_splits -- the split count pda_decode would use on the current
+ * device for these sizes (heuristic or override). Returns < 1 on error.
+ */
+int pda_plan_splits(int num_seqs, int num_heads, int num_kv_heads, int max_num_blocks_per_seq,
+                    int block_size);
+
+/*
+ * pda_set_split_override -- force the split count of later pda_decode calls
+ * (process-wide; 0 restores the heuristic). For tests and measurements.
+ * Values above the table row length are clamped at call time.
+ */
+void pda_set_split_override(int num_splits);
+
+/*
+ * pda_reserve -- size the workspace of (current device, stream) for calls up
+ * to these sizes, so later calls (for example under stream capture) need no
+ * allocation. Stream-ordered; returns PDA_OK or PDA_ERR_CUDA.
+ */
+pda_status pda_reserve(int num_seqs, int num_heads, int num_kv_heads, int max_num_blocks_per_seq,
+                       int block_size, cudaStream_t stream);
+
+/* pda_release -- free every workspace the library holds (synchronises each device used). */
+pda_status pda_release(void);
+
+/*
+ * pda_query_device_status -- synchronise `stream`, then read and clear the
+ * device status word of the current device. *code receives 0 when every
+ * kernel since the last query finished normally, or a nonzero code when a
+ * kernel gave up on a bounded wait (its output is then undefined). Returns
+ * PDA_ERR_DEVICE_TIMEOUT when *code != 0. Test / debug call: it blocks.
+ */
+pda_status pda_query_device_status(cudaStream_t stream, int* code);
+
+/*
+ * pda_set_profile_events -- when both events are non-NULL, later pda_decode
+ * calls record `before` immediately before and `after` immediately after the
+ * split-KV decode kernel on their stream (capturable). NULL, NULL turns it
+ * off. Process-wide; for measurement only.
+ */
+void pda_set_profile_events(cudaEvent_t before, cudaEvent_t after);
+
+/*
+ * pda_test_bounded_wait -- launch one CTA that waits on a barrier nothing
+ * will complete, with a limit of timeout_us microseconds, on `stream`. The
+ * kernel gives up, records PDA timeout code in the device status word and
+ * returns (no trap, no fault); pda_query_device_status then reports it.
+ * Exercises the bounded-wait error path of the decode kernel's barriers.
+ * timeout_us must be in [1, 2000000].
+ */
+pda_status pda_test_bounded_wait(int timeout_us, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PDA_H_ */

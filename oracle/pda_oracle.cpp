@@ -128,6 +128,10 @@ int pda_oracle_decode(double* out, const uint16_t* q, const uint8_t* k_cache,
     }
   }
 
+  // The 256 possible byte values, decoded once (same values as e4m3_value).
+  double e4m3[256];
+  for (int c = 0; c < 256; ++c) e4m3[c] = e4m3_value(static_cast<uint8_t>(c));
+
   const long long rows = static_cast<long long>(n_out) * num_heads;
 #ifdef _OPENMP
   const int nt = num_threads > 0 ? num_threads : omp_get_max_threads();
@@ -155,7 +159,7 @@ int pda_oracle_decode(double* out, const uint16_t* q, const uint8_t* k_cache,
       double acc = 0.0;
       for (int d = 0; d < D; ++d) {
         const uint8_t code = kpage[(static_cast<long long>(d / 16) * bs + slot) * 16 + (d % 16)];
-        acc += qd[d] * (e4m3_value(code) * k_scale);
+        acc += qd[d] * (e4m3[code] * k_scale);
       }
       z[t] = scale * acc;
     }
@@ -175,7 +179,7 @@ int pda_oracle_decode(double* out, const uint16_t* q, const uint8_t* k_cache,
       const uint8_t* vpage = v_cache + (b * num_kv_heads + kv) * static_cast<long long>(D) * bs;
       const double wt = w[t] / denom;
       for (int d = 0; d < D; ++d) {
-        o[d] += wt * (e4m3_value(vpage[static_cast<long long>(d) * bs + slot]) * v_scale);
+        o[d] += wt * (e4m3[vpage[static_cast<long long>(d) * bs + slot]] * v_scale);
       }
     }
   }

@@ -1,0 +1,31 @@
+"""fp8 paged decode attention for NVIDIA GB300 (sm_103a).
+
+Single-query attention over a paged fp8-e4m3 KV cache (16-token-multiple
+blocks, per-sequence block tables, GQA up to 8) as a C-ABI library
+(``include/pda.h``, ``libpda.so``) with hand-written sm_103a kernels: a
+split-KV decode kernel, a log-sum-exp merge kernel and a host split-count
+heuristic. This package is a thin ctypes binding; it performs no compute.
+"""
+
+from ._binding import (  # noqa: F401
+    LIB_PATH,
+    PDA_ERR_CUDA,
+    PDA_ERR_DEVICE_TIMEOUT,
+    PDA_ERR_INVALID_ARG,
+    PDA_ERR_UNSUPPORTED,
+    PDA_ERR_WORKSPACE,
+    PDA_OK,
+    PdaError,
+    choose_splits,
+    decode,
+    decode_raw,
+    load,
+    plan_splits,
+    query_device_status,
+    release,
+    reserve,
+    set_profile_events,
+    set_split_override,
+    status_string,
+    bounded_wait_check,
+)

@@ -1,0 +1,187 @@
+"""ctypes binding of the C ABI declared in ``include/pda.h``.
+
+Argument marshalling only: tensors become device pointers and sizes, and
+every step of the computation runs in the library's CUDA kernels. The shared
+library ``libpda.so`` is built in-tree (``paged_kv_decode_pda_gb300.build``);
+if it is missing the first call raises ``PdaError`` -- there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpda.so")
+
+PDA_OK = 0
+PDA_ERR_INVALID_ARG = 1
+PDA_ERR_UNSUPPORTED = 2
+PDA_ERR_WORKSPACE = 3
+PDA_ERR_CUDA = 4
+PDA_ERR_DEVICE_TIMEOUT = 5
+
+# Functions (name -> (restype, argtypes)) the header declares.
+_P, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+SIGNATURES = {
+    "pda_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _F, _P]),
+    "pda_status_string": (ctypes.c_char_p, [_I]),
+    "pda_choose_splits": (_I, [_I, _I, _I, _I, _I, _I]),
+    "pda_plan_splits": (_I, [_I, _I, _I, _I, _I]),
+    "pda_set_split_override": (None, [_I]),
+    "pda_reserve": (_I, [_I, _I, _I, _I, _I, _P]),
+    "pda_release": (_I, []),
+    "pda_query_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_int)]),
+    "pda_set_profile_events": (None, [_P, _P]),
+    "pda_test_bounded_wait": (_I, [_I, _P]),
+}
+
+_lock = threading.RLock()
+_lib = None
+
+
+class PdaError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (what or "pda", status_string(status), status))
+
+
+def load(path: str | None = None):
+    """Load libpda.so (once) and bind every declared entry point."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise PdaError(PDA_ERR_CUDA, "libpda.so not built at %s (run paged_kv_decode_pda_gb300.build.build())" % p)
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    if _lib is None:
+        return _STATUS_TEXT.get(int(status), "unknown status")
+    return _lib.pda_status_string(int(status)).decode()
+
+
+_STATUS_TEXT = {PDA_OK: "ok", PDA_ERR_INVALID_ARG: "invalid argument", PDA_ERR_UNSUPPORTED: "unsupported configuration",
+                PDA_ERR_WORKSPACE: "workspace must grow during stream capture", PDA_ERR_CUDA: "CUDA runtime error",
+                PDA_ERR_DEVICE_TIMEOUT: "a kernel gave up on a bounded wait"}
+
+
+def _check(status: int, what: str):
+    if status != PDA_OK:
+        raise PdaError(status, what)
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return int(stream.cuda_stream)
+    return int(stream)
+
+
+def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+           seq_lens: torch.Tensor, scale: float, k_scale: float, v_scale: float, *,
+           out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Decode attention over a paged fp8 cache (``pda_decode``).
+
+    q ``[S, H, 128]`` bf16; k_cache ``[NB, Hk, 8, bs, 16]`` and v_cache
+    ``[NB, Hk, 128, bs]`` float8_e4m3fn (or uint8 bytes); block_tables
+    ``[S, MB]`` int32; seq_lens ``[S]`` int32; all contiguous on one CUDA
+    device. Returns ``out`` (allocated like q when not given).
+    """
+    lib = load()
+    if q.dim() != 3 or k_cache.dim() != 5 or v_cache.dim() != 4 or block_tables.dim() != 2 or seq_lens.dim() != 1:
+        raise PdaError(PDA_ERR_INVALID_ARG, "decode: tensor ranks")
+    if q.dtype != torch.bfloat16 or block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise PdaError(PDA_ERR_INVALID_ARG, "decode: dtypes (q bf16, tables/seq_lens int32)")
+    for t in (k_cache, v_cache):
+        if t.dtype not in (torch.float8_e4m3fn, torch.uint8):
+            raise PdaError(PDA_ERR_INVALID_ARG, "decode: cache dtype must be float8_e4m3fn")
+    ts = [q, k_cache, v_cache, block_tables, seq_lens]
+    if not all(t.is_cuda and t.is_contiguous() for t in ts):
+        raise PdaError(PDA_ERR_INVALID_ARG, "decode: tensors must be contiguous CUDA tensors")
+    S, H, D = q.shape
+    NB, Hk, D16, bs, sixteen = k_cache.shape
+    if (sixteen != 16 or D16 * 16 != D or tuple(v_cache.shape) != (NB, Hk, D, bs)
+            or block_tables.shape[0] != S or seq_lens.shape[0] != S):
+        raise PdaError(PDA_ERR_INVALID_ARG, "decode: shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous() or not out.is_cuda:
+        raise PdaError(PDA_ERR_INVALID_ARG, "decode: out")
+    st = lib.pda_decode(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                        block_tables.data_ptr(), seq_lens.data_ptr(), S, H, Hk, D, bs,
+                        int(block_tables.shape[1]), float(scale), float(k_scale), float(v_scale),
+                        _stream_ptr(stream))
+    _check(st, "pda_decode")
+    return out
+
+
+def decode_raw(out_ptr: int, q_ptr: int, k_ptr: int, v_ptr: int, tables_ptr: int, lens_ptr: int, num_seqs: int,
+               num_heads: int, num_kv_heads: int, head_size: int, block_size: int, max_num_blocks_per_seq: int,
+               scale: float, k_scale: float, v_scale: float, stream_ptr: int = 0) -> int:
+    """``pda_decode`` on raw device addresses; returns the status code."""
+    return load().pda_decode(out_ptr, q_ptr, k_ptr, v_ptr, tables_ptr, lens_ptr, num_seqs, num_heads,
+                             num_kv_heads, head_size, block_size, max_num_blocks_per_seq, float(scale),
+                             float(k_scale), float(v_scale), stream_ptr)
+
+
+def choose_splits(num_seqs, num_kv_heads, max_num_blocks_per_seq, block_size, sm_count, ctas_per_sm) -> int:
+    return load().pda_choose_splits(num_seqs, num_kv_heads, max_num_blocks_per_seq, block_size, sm_count,
+                                    ctas_per_sm)
+
+
+def plan_splits(num_seqs, num_heads, num_kv_heads, max_num_blocks_per_seq, block_size) -> int:
+    n = load().pda_plan_splits(num_seqs, num_heads, num_kv_heads, max_num_blocks_per_seq, block_size)
+    if n < 1:
+        raise PdaError(PDA_ERR_CUDA, "pda_plan_splits")
+    return n
+
+
+def set_split_override(n: int) -> None:
+    load().pda_set_split_override(int(n))
+
+
+def reserve(num_seqs, num_heads, num_kv_heads, max_num_blocks_per_seq, block_size, stream=None) -> None:
+    _check(load().pda_reserve(num_seqs, num_heads, num_kv_heads, max_num_blocks_per_seq, block_size,
+                              _stream_ptr(stream)), "pda_reserve")
+
+
+def release() -> None:
+    _check(load().pda_release(), "pda_release")
+
+
+def query_device_status(stream=None) -> int:
+    code = ctypes.c_int(0)
+    st = load().pda_query_device_status(_stream_ptr(stream), ctypes.byref(code))
+    if st not in (PDA_OK, PDA_ERR_DEVICE_TIMEOUT):
+        raise PdaError(st, "pda_query_device_status")
+    return int(code.value)
+
+
+def set_profile_events(before, after) -> None:
+    """Record two torch.cuda.Event around the decode kernel (None, None: off)."""
+    if before is None or after is None:
+        load().pda_set_profile_events(None, None)
+    else:
+        for e in (before, after):
+            if int(e.cuda_event) == 0:   # torch creates the event on its first record
+                e.record()
+        load().pda_set_profile_events(int(before.cuda_event), int(after.cuda_event))
+
+
+def bounded_wait_check(timeout_us: int, stream=None) -> None:
+    _check(load().pda_test_bounded_wait(int(timeout_us), _stream_ptr(stream)), "pda_test_bounded_wait")

@@ -1,0 +1,333 @@
+// C ABI of the fp8 paged decode attention library (see include/pda.h):
+// argument validation, the split-count heuristic, the per-stream workspace,
+// and the launches of the split-KV decode and merge kernels.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/pda.h"
+#include "pda_kernels.cuh"
+
+namespace {
+
+using pda::kHeadDim;
+
+std::atomic<int> g_split_override{0};
+std::atomic<cudaEvent_t> g_prof_before{nullptr};
+std::atomic<cudaEvent_t> g_prof_after{nullptr};
+
+struct DeviceInfo {
+  int sm_count = 0;
+  int ctas_per_sm_by_bs[9] = {0};  // index bs/16 (1..8)
+  bool smem_attr_set = false;
+};
+std::mutex g_dev_mu;
+std::map<int, DeviceInfo> g_devices;
+
+struct Workspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::mutex g_ws_mu;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+// Ring geometry for a block size: a stage holds max(64, bs) tokens of K and
+// V (whole pages); about 64 KiB of stages per CTA.
+struct RingShape {
+  int pages_per_stage;
+  int num_stages;
+  uint32_t stage_bytes;
+  size_t smem_bytes;
+};
+
+RingShape ring_shape(int bs) {
+  RingShape r;
+  r.pages_per_stage = bs < pda::kStageTokensMin ? pda::kStageTokensMin / bs : 1;
+  r.stage_bytes = 2u * (uint32_t)r.pages_per_stage * (uint32_t)(kHeadDim * bs);
+  r.num_stages = (int)(65536u / r.stage_bytes);
+  if (r.num_stages < 2) r.num_stages = 2;
+  size_t ring = (size_t)r.num_stages * r.stage_bytes;
+  size_t merge = (size_t)pda::kConsumerWarps * pda::kMaxGqa * (pda::kMergeStride + 2) * sizeof(float);
+  if (ring < merge) ring = merge;
+  r.smem_bytes = ring + 2 * 8 * (size_t)r.num_stages + 16;
+  return r;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+pda_status validate(const void* out, const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, const int32_t* seq_lens, int num_seqs, int num_heads,
+                    int num_kv_heads, int head_size, int block_size, int max_blocks, float scale,
+                    float k_scale, float v_scale) {
+  if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 ||
+      max_blocks < 0)
+    return PDA_ERR_INVALID_ARG;
+  if (num_heads % num_kv_heads != 0) return PDA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale)) return PDA_ERR_INVALID_ARG;
+  if (head_size != kHeadDim) return PDA_ERR_UNSUPPORTED;
+  if (block_size % 16 != 0 || block_size > 128) return PDA_ERR_UNSUPPORTED;
+  const int g = num_heads / num_kv_heads;
+  if (g > pda::kMaxGqa) return PDA_ERR_UNSUPPORTED;
+  if (num_seqs > 65535 || num_kv_heads > 65535) return PDA_ERR_UNSUPPORTED;
+  if ((long long)max_blocks * block_size > (long long)INT32_MAX / 2) return PDA_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PDA_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens) return PDA_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return PDA_ERR_INVALID_ARG;
+  return PDA_OK;
+}
+
+pda_status device_info(int dev, int bs, int* sm_count, int* ctas_per_sm) {
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& di = g_devices[dev];
+  if (di.sm_count == 0) {
+    if (cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      di.sm_count = 0;
+      return PDA_ERR_CUDA;
+    }
+  }
+  if (!di.smem_attr_set) {
+    // Opt in to the largest ring any block size uses.
+    size_t mx = 0;
+    for (int b = 16; b <= 128; b += 16) {
+      size_t s = ring_shape(b).smem_bytes;
+      mx = s > mx ? s : mx;
+    }
+    if (cudaFuncSetAttribute(pda::pda_split_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)mx) != cudaSuccess)
+      return PDA_ERR_CUDA;
+    di.smem_attr_set = true;
+  }
+  int& occ = di.ctas_per_sm_by_bs[bs / 16];
+  if (occ == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pda::pda_split_decode_kernel, pda::kThreads,
+                                                      ring_shape(bs).smem_bytes) != cudaSuccess)
+      return PDA_ERR_CUDA;
+    occ = n > 0 ? n : 1;
+  }
+  *sm_count = di.sm_count;
+  *ctas_per_sm = occ;
+  return PDA_OK;
+}
+
+int resolve_splits(int num_seqs, int num_kv_heads, int max_blocks, int bs, int sm_count, int ctas_per_sm) {
+  int n = g_split_override.load();
+  if (n <= 0) n = pda_choose_splits(num_seqs, num_kv_heads, max_blocks, bs, sm_count, ctas_per_sm);
+  const int cap = max_blocks > 0 ? max_blocks : 1;
+  if (n > cap) n = cap;
+  if (n < 1) n = 1;
+  return n;
+}
+
+size_t workspace_bytes(int num_seqs, int num_heads, int nsplit) {
+  if (nsplit <= 1) return 0;
+  const size_t rows = (size_t)num_seqs * num_heads * nsplit;
+  const size_t o = rows * kHeadDim * sizeof(float);
+  return o + rows * 2 * sizeof(float);
+}
+
+// Returns the workspace pointer for (device, stream), growing it with
+// stream-ordered allocation when not capturing.
+pda_status get_workspace(int dev, cudaStream_t stream, size_t bytes, void** out) {
+  *out = nullptr;
+  if (bytes == 0) return PDA_OK;
+  std::lock_guard<std::mutex> lk(g_ws_mu);
+  Workspace& ws = g_ws[{dev, stream}];
+  if (ws.bytes >= bytes) {
+    *out = ws.ptr;
+    return PDA_OK;
+  }
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return PDA_ERR_CUDA;
+  if (cs != cudaStreamCaptureStatusNone) return PDA_ERR_WORKSPACE;
+  size_t want = bytes + (bytes >> 3);
+  want = (want + 255) & ~(size_t)255;
+  void* p = nullptr;
+  if (cudaMallocAsync(&p, want, stream) != cudaSuccess) return PDA_ERR_CUDA;
+  if (ws.ptr) cudaFreeAsync(ws.ptr, stream);
+  ws.ptr = p;
+  ws.bytes = want;
+  *out = p;
+  return PDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pda_status_string(int status) {
+  switch (status) {
+    case PDA_OK: return "ok";
+    case PDA_ERR_INVALID_ARG: return "invalid argument";
+    case PDA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PDA_ERR_WORKSPACE: return "workspace must grow during stream capture (call pda_reserve first)";
+    case PDA_ERR_CUDA: return "CUDA runtime error";
+    case PDA_ERR_DEVICE_TIMEOUT: return "a kernel gave up on a bounded wait";
+    default: return "unknown status";
+  }
+}
+
+int pda_choose_splits(int num_seqs, int num_kv_heads, int max_num_blocks_per_seq, int block_size, int sm_count,
+                      int ctas_per_sm) {
+  if (num_seqs <= 0 || num_kv_heads <= 0 || max_num_blocks_per_seq <= 0 || block_size <= 0 || sm_count <= 0 ||
+      ctas_per_sm <= 0)
+    return 1;
+  const long long units = (long long)num_seqs * num_kv_heads;
+  const long long slots = (long long)sm_count * ctas_per_sm;
+  // Split only while the work units alone cannot fill two waves of CTAs,
+  // and keep at least kMinSplitTokens tokens of streaming per split so the
+  // page ring pays for its fill and the partials stay small next to K/V.
+  const long long kMinSplitTokens = 256;
+  long long want = (2 * slots + units - 1) / units;
+  const long long min_pages = (kMinSplitTokens + block_size - 1) / block_size;
+  long long cap = max_num_blocks_per_seq / min_pages;
+  if (cap < 1) cap = 1;
+  if (want > cap) want = cap;
+  if (want < 1) want = 1;
+  return (int)want;
+}
+
+void pda_set_split_override(int num_splits) { g_split_override.store(num_splits > 0 ? num_splits : 0); }
+
+int pda_plan_splits(int num_seqs, int num_heads, int num_kv_heads, int max_num_blocks_per_seq, int block_size) {
+  (void)num_heads;
+  if (block_size <= 0 || block_size % 16 != 0 || block_size > 128) return -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  int sms = 0, occ = 0;
+  if (device_info(dev, block_size, &sms, &occ) != PDA_OK) return -1;
+  return resolve_splits(num_seqs, num_kv_heads, max_num_blocks_per_seq, block_size, sms, occ);
+}
+
+void pda_set_profile_events(cudaEvent_t before, cudaEvent_t after) {
+  if (before && after) {
+    g_prof_before.store(before);
+    g_prof_after.store(after);
+  } else {
+    g_prof_before.store(nullptr);
+    g_prof_after.store(nullptr);
+  }
+}
+
+pda_status pda_reserve(int num_seqs, int num_heads, int num_kv_heads, int max_num_blocks_per_seq, int block_size,
+                       cudaStream_t stream) {
+  if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || max_num_blocks_per_seq < 0 || block_size <= 0 ||
+      block_size % 16 != 0 || block_size > 128)
+    return PDA_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PDA_ERR_CUDA;
+  int sms = 0, occ = 0;
+  pda_status st = device_info(dev, block_size, &sms, &occ);
+  if (st != PDA_OK) return st;
+  const int nsplit = resolve_splits(num_seqs, num_kv_heads, max_num_blocks_per_seq, block_size, sms, occ);
+  void* ws = nullptr;
+  return get_workspace(dev, stream, workspace_bytes(num_seqs, num_heads, nsplit), &ws);
+}
+
+pda_status pda_release(void) {
+  std::lock_guard<std::mutex> lk(g_ws_mu);
+  int prev = 0;
+  cudaGetDevice(&prev);
+  pda_status st = PDA_OK;
+  for (auto& kv : g_ws) {
+    if (!kv.second.ptr) continue;
+    if (cudaSetDevice(kv.first.first) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess ||
+        cudaFree(kv.second.ptr) != cudaSuccess)
+      st = PDA_ERR_CUDA;
+  }
+  g_ws.clear();
+  cudaSetDevice(prev);
+  return st;
+}
+
+pda_status pda_query_device_status(cudaStream_t stream, int* code) {
+  if (!code) return PDA_ERR_INVALID_ARG;
+  *code = 0;
+  unsigned int v = 0, zero = 0;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return PDA_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(&v, pda::g_status, sizeof v) != cudaSuccess) return PDA_ERR_CUDA;
+  if (cudaMemcpyToSymbol(pda::g_status, &zero, sizeof zero) != cudaSuccess) return PDA_ERR_CUDA;
+  *code = (int)v;
+  return v ? PDA_ERR_DEVICE_TIMEOUT : PDA_OK;
+}
+
+pda_status pda_test_bounded_wait(int timeout_us, cudaStream_t stream) {
+  if (timeout_us < 1 || timeout_us > 2000000) return PDA_ERR_INVALID_ARG;
+  pda::pda_bounded_wait_test_kernel<<<1, 32, 0, stream>>>((unsigned long long)timeout_us * 1000ull);
+  return cudaGetLastError() == cudaSuccess ? PDA_OK : PDA_ERR_CUDA;
+}
+
+pda_status pda_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, const int32_t* seq_lens, int num_seqs, int num_heads,
+                      int num_kv_heads, int head_size, int block_size, int max_num_blocks_per_seq, float scale,
+                      float k_scale, float v_scale, cudaStream_t stream) {
+  pda_status st = validate(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_heads, num_kv_heads,
+                           head_size, block_size, max_num_blocks_per_seq, scale, k_scale, v_scale);
+  if (st != PDA_OK || num_seqs == 0) return st;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PDA_ERR_CUDA;
+  int sms = 0, occ = 0;
+  st = device_info(dev, block_size, &sms, &occ);
+  if (st != PDA_OK) return st;
+  const int MB = max_num_blocks_per_seq > 0 ? max_num_blocks_per_seq : 1;
+  const int nsplit = resolve_splits(num_seqs, num_kv_heads, MB, block_size, sms, occ);
+  void* ws = nullptr;
+  st = get_workspace(dev, stream, workspace_bytes(num_seqs, num_heads, nsplit), &ws);
+  if (st != PDA_OK) return st;
+
+  const RingShape rs = ring_shape(block_size);
+  pda::DecodeParams p;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k_cache = static_cast<const uint8_t*>(k_cache);
+  p.v_cache = static_cast<const uint8_t*>(v_cache);
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.part_o = static_cast<float*>(ws);
+  p.part_ml = ws ? static_cast<float*>(ws) + (size_t)num_seqs * num_heads * nsplit * kHeadDim : nullptr;
+  p.num_heads = num_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.gqa = num_heads / num_kv_heads;
+  p.block_size = block_size;
+  p.max_blocks = max_num_blocks_per_seq;
+  p.nsplit = nsplit;
+  p.pages_per_stage = rs.pages_per_stage;
+  p.num_stages = rs.num_stages;
+  p.stage_bytes = rs.stage_bytes;
+  p.logit_scale_log2 = (float)((double)scale * (double)k_scale * 1.4426950408889634);
+  p.v_scale = v_scale;
+
+  cudaEvent_t eb = g_prof_before.load(), ea = g_prof_after.load();
+  if (eb && ea && cudaEventRecord(eb, stream) != cudaSuccess) return PDA_ERR_CUDA;
+  dim3 grid((unsigned)nsplit, (unsigned)num_kv_heads, (unsigned)num_seqs);
+  pda::pda_split_decode_kernel<<<grid, pda::kThreads, rs.smem_bytes, stream>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
+  if (eb && ea && cudaEventRecord(ea, stream) != cudaSuccess) return PDA_ERR_CUDA;
+
+  if (nsplit > 1) {
+    pda::MergeParams mp;
+    mp.out = p.out;
+    mp.part_o = p.part_o;
+    mp.part_ml = p.part_ml;
+    mp.seq_lens = seq_lens;
+    mp.num_heads = num_heads;
+    mp.block_size = block_size;
+    mp.max_blocks = max_num_blocks_per_seq;
+    mp.nsplit = nsplit;
+    mp.v_scale = v_scale;
+    pda::pda_merge_kernel<<<dim3((unsigned)num_heads, (unsigned)num_seqs), kHeadDim, 0, stream>>>(mp);
+    if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
+  }
+  return PDA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,452 @@
+// Split-KV fp8 paged decode kernel and log-sum-exp merge kernel (sm_103a).
+//
+// Work unit: one (sequence, kv head, KV split). One CTA per unit:
+//   * warp kConsumerWarps (the producer) gathers the split's pages through
+//     the block table and streams them with 1-D bulk (TMA) copies into a
+//     ring of shared-memory stages, one mbarrier pair per stage;
+//   * warps 0..kConsumerWarps-1 (the consumers) each take 16-token tiles of
+//     a stage and run, for all query heads of the GQA group at once,
+//       S^T = K_tile (16 tok x 128) * Q^T (128 x 8 heads)     (warp MMA)
+//       online softmax over tokens in fp32 (exp2 domain)
+//       O^T += V_tile^T (128 x 16 tok) * P^T (16 tok x 8 heads)
+//     with K and V dequantised exactly from e4m3 to f16 in registers, once
+//     per tile for every head of the group;
+//   * the consumers merge their (m, l, O) through shared memory and either
+//     write bf16 output (one split) or an fp32 partial (several splits) that
+//     the merge kernel combines by log-sum-exp.
+//
+// The pages give the cache layout (K [blocks, kv_heads, head_size/16, bs, 16],
+// V [blocks, kv_heads, head_size, bs]; vLLM pull request
+// lishuoshuo-amd/vllm#3, "Details" -> "Layout") and what the call computes
+// (vLLM API page vllm.v1.attention.backends.rocm_aiter_unified_attn,
+// RocmAiterUnifiedAttentionImpl.forward). The kernel design is this
+// library's own.
+#pragma once
+
+#include "pda_device.cuh"
+
+namespace pda {
+
+constexpr int kHeadDim = 128;
+constexpr int kChunks = kHeadDim / 16;       // 16-dim chunks of a K page
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStageTokensMin = 64;          // a stage holds >= 64 tokens of K and V
+constexpr int kMaxGqa = 8;                   // MMA N dimension: query heads of a group
+constexpr int kMergeStride = kHeadDim + 4;   // padded fp32 row of the CTA merge area
+
+struct DecodeParams {
+  __nv_bfloat16* out;           // [S][H][D]
+  const __nv_bfloat16* q;       // [S][H][D]
+  const uint8_t* k_cache;       // [NB][Hk][D/16][bs][16]
+  const uint8_t* v_cache;       // [NB][Hk][D][bs]
+  const int32_t* block_tables;  // [S][MB]
+  const int32_t* seq_lens;      // [S]
+  float* part_o;                // [S][H][nsplit][D]   (nsplit > 1)
+  float* part_ml;               // [S][H][nsplit][2]   (nsplit > 1): m (log2 units), l
+  int num_heads;
+  int num_kv_heads;
+  int gqa;
+  int block_size;
+  int max_blocks;               // block table row stride
+  int nsplit;
+  int pages_per_stage;
+  int num_stages;
+  uint32_t stage_bytes;
+  float logit_scale_log2;       // scale * k_scale * log2(e)
+  float v_scale;
+};
+
+// Token order of the 16 MMA rows of a K tile. Row r of the QK accumulator
+// holds token row_token(r); the order is chosen so that, after the P
+// fragment is transposed with movmatrix, each lane holds the probabilities
+// of exactly the tokens whose V bytes ldmatrix hands it (4 consecutive
+// tokens, with the two halves swapped for lanes whose tig >= 2), and so that
+// both 8-row K ldmatrix groups hit 8 distinct 16-byte bank groups.
+// Rows 0..7 -> tokens 0,1,4,5,10,11,14,15; rows 8..15 -> 2,3,6,7,8,9,12,13.
+__device__ __forceinline__ int row_token(int r) {
+  const int hi = r >> 3;            // which 8-row half
+  const int t = (r >> 1) & 3;       // lane quad index the row pair maps to
+  const int e = r & 1;
+  const int swap = (t >= 2) ? 1 : 0;
+  return 4 * t + 2 * (hi ^ swap) + e;
+}
+
+// Pages [first, end) of split `split` for a sequence with `pages` pages.
+__device__ __forceinline__ void split_range(int pages, int nsplit, int split, int& first, int& end) {
+  const int per = (pages + nsplit - 1) / nsplit;
+  first = split * per;
+  end = min(pages, first + per);
+}
+
+__device__ __forceinline__ float warp_max_over_gid(float v) {
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+  return v;
+}
+__device__ __forceinline__ float warp_sum_over_gid(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 4);
+  v += __shfl_xor_sync(0xffffffffu, v, 8);
+  v += __shfl_xor_sync(0xffffffffu, v, 16);
+  return v;
+}
+
+__global__ void __launch_bounds__(kThreads) pda_split_decode_kernel(const DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int split = blockIdx.x;
+  const int kvh = blockIdx.y;
+  const int s = blockIdx.z;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bs = p.block_size;
+  const int H = p.num_heads;
+  const int g = p.gqa;
+
+  int L = __ldg(p.seq_lens + s);
+  L = max(0, min(L, p.max_blocks * bs));
+  const int pages = (L + bs - 1) / bs;
+  int pg_first, pg_end;
+  split_range(pages, p.nsplit, split, pg_first, pg_end);
+
+  if (pg_first >= pg_end) {
+    // No tokens for this split. With one split the row is all-zero output;
+    // with several, the merge kernel skips empty splits by the same rule.
+    if (p.nsplit == 1) {
+      for (int i = threadIdx.x; i < g * kHeadDim; i += blockDim.x) {
+        const int h = kvh * g + i / kHeadDim;
+        p.out[((size_t)s * H + h) * kHeadDim + (i % kHeadDim)] = __float2bfloat16_rn(0.f);
+      }
+    }
+    return;
+  }
+
+  const int NS = p.num_stages;
+  const int PPS = p.pages_per_stage;
+  uint8_t* ring = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)NS * p.stage_bytes);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * NS);
+  const uint32_t ring_u32 = smem_u32(ring);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8u * NS;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(full0 + 8u * i, 1);
+      mbar_init(empty0 + 8u * i, kConsumerWarps);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  const int n_pages = pg_end - pg_first;
+  const int n_fills = (n_pages + PPS - 1) / PPS;
+  const uint32_t page_bytes = (uint32_t)(kHeadDim * bs);
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    const int32_t* row = p.block_tables + (size_t)s * p.max_blocks;
+    const size_t head_stride = (size_t)page_bytes;
+    const size_t block_stride = (size_t)p.num_kv_heads * page_bytes;
+    int fill = 0;
+    bool ok = true;
+    for (int base = 0; base < n_pages && ok; base += 32) {
+      const int my_idx = base + lane;
+      const int my_block = my_idx < n_pages ? __ldg(row + pg_first + my_idx) : 0;
+      const int chunk_pages = min(32, n_pages - base);
+      for (int j = 0; j < chunk_pages; j += PPS, ++fill) {
+        const int stage = fill % NS;
+        const uint32_t round = (uint32_t)(fill / NS);
+        int blk[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) blk[t] = __shfl_sync(0xffffffffu, my_block, (j + t) & 31);
+        const int np = min(PPS, chunk_pages - j);
+        const bool got = mbar_wait_bounded(empty0 + 8u * stage, (round & 1u) ^ 1u, abort_flag, kWaitLimitNs);
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) {
+            atomicOr(&g_status, kStatusEmptyWaitTimeout);
+            *abort_flag = 1;
+          }
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t sbase = ring_u32 + (uint32_t)stage * p.stage_bytes;
+          const uint32_t bar = full0 + 8u * stage;
+          mbar_arrive_expect_tx(bar, 2u * page_bytes * (uint32_t)np);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            if (t < np) {
+              const size_t off = (size_t)blk[t] * block_stride + (size_t)kvh * head_stride;
+              bulk_g2s(sbase + (uint32_t)t * page_bytes, p.k_cache + off, page_bytes, bar);
+              bulk_g2s(sbase + (uint32_t)(PPS + t) * page_bytes, p.v_cache + off, page_bytes, bar);
+            }
+          }
+        }
+        __syncwarp();
+      }
+    }
+    // Drain: never leave the CTA with copies still landing in its smem.
+    const int issued = fill;
+    for (int f = max(0, issued - NS); f < issued; ++f) {
+      const int stage = f % NS;
+      if (!mbar_wait_bounded(full0 + 8u * stage, (uint32_t)(f / NS) & 1u, nullptr, kWaitLimitNs)) {
+        if (lane == 0) atomicOr(&g_status, kStatusDrainTimeout);
+        break;
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int gid = lane >> 2;
+  const int tig = lane & 3;
+
+  // Q^T fragments (B operand, 16 dims x 8 heads per chunk) in f16. Chunk c
+  // k-slots (2tig, 2tig+1) <- dims 16c+4tig+{0,1}; (2tig+8, 2tig+9) <- dims
+  // 16c+4tig+{2,3}; this matches how K bytes land in the A fragments below.
+  uint32_t qf[kChunks][2];
+  {
+    const bool live = gid < g;
+    const __nv_bfloat16* qrow = p.q + ((size_t)s * H + (size_t)kvh * g + (live ? gid : 0)) * kHeadDim;
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+      uint2 v = live ? ld_nc_v2(qrow + 16 * c + 4 * tig) : make_uint2(0u, 0u);
+      qf[c][0] = pack_f16x2(bf16lo_f32(v.x), bf16hi_f32(v.x));
+      qf[c][1] = pack_f16x2(bf16lo_f32(v.y), bf16hi_f32(v.y));
+    }
+  }
+
+  // ldmatrix row assignment. K: lane l supplies token row_token(l & 15) of
+  // chunk (2kk + (l >> 4)). V: lane l supplies dim (32mp + l).
+  const uint32_t k_lane_off = (uint32_t)(row_token(lane & 15) * 16) + (uint32_t)((lane >> 4) * bs * 16);
+  const uint32_t v_lane_off = (uint32_t)(lane * bs);
+  const uint32_t v_swap_sel = tig >= 2 ? 0x1032u : 0x3210u;
+  const int tokA = row_token(gid);
+  const int tokB = row_token(gid + 8);
+
+  float m0 = -INFINITY, m1 = -INFINITY;   // running max (log2 units), heads 2tig, 2tig+1
+  float l0 = 0.f, l1 = 0.f;               // running partial sums over this lane's tokens
+  float o[kChunks][4];                    // O^T: m-tile mt = dims 16mt.. ; cols heads 2tig, 2tig+1
+#pragma unroll
+  for (int i = 0; i < kChunks; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+  const float lsc = p.logit_scale_log2;
+  const int tiles_per_page = bs / 16;
+
+  for (int fill = 0; fill < n_fills; ++fill) {
+    const int stage = fill % NS;
+    const uint32_t round = (uint32_t)(fill / NS);
+    const bool got = mbar_wait_bounded(full0 + 8u * stage, round & 1u, abort_flag, kWaitLimitNs);
+    if (!__all_sync(0xffffffffu, got)) {
+      if (lane == 0) {
+        atomicOr(&g_status, kStatusFullWaitTimeout);
+        *abort_flag = 1;
+      }
+      break;
+    }
+    const int fill_first_page = pg_first + fill * PPS;
+    const int np = min(PPS, pg_end - fill_first_page);
+    const int n_tiles = np * tiles_per_page;
+    const uint32_t sbase = ring_u32 + (uint32_t)stage * p.stage_bytes;
+
+    for (int tile = warp; tile < n_tiles; tile += kConsumerWarps) {
+      const int pg = tile / tiles_per_page;
+      const int sub = tile % tiles_per_page;
+      const int tok0 = (fill_first_page + pg) * bs + sub * 16;
+      if (tok0 >= L) continue;
+      const uint32_t kbase = sbase + (uint32_t)pg * page_bytes + (uint32_t)(sub * 256);
+      const uint32_t vbase = sbase + (uint32_t)(PPS + pg) * page_bytes + (uint32_t)(sub * 16);
+
+      // ---- S^T = K_tile * Q^T
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < kChunks / 2; ++kk) {
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4(kbase + k_lane_off + (uint32_t)(2 * kk * bs * 16), r0, r1, r2, r3);
+        mma_f16(sc, e4m3x2_lo_to_f16x2(r0), e4m3x2_lo_to_f16x2(r1), e4m3x2_hi_to_f16x2(r0),
+                e4m3x2_hi_to_f16x2(r1), qf[2 * kk][0], qf[2 * kk][1]);
+        mma_f16(sc, e4m3x2_lo_to_f16x2(r2), e4m3x2_lo_to_f16x2(r3), e4m3x2_hi_to_f16x2(r2),
+                e4m3x2_hi_to_f16x2(r3), qf[2 * kk + 1][0], qf[2 * kk + 1][1]);
+      }
+
+      // ---- online softmax (exp2 domain); tokens >= L are masked
+      const bool vA = tok0 + tokA < L;
+      const bool vB = tok0 + tokB < L;
+      const float s0 = vA ? sc[0] * lsc : -INFINITY;
+      const float s1 = vA ? sc[1] * lsc : -INFINITY;
+      const float s2 = vB ? sc[2] * lsc : -INFINITY;
+      const float s3 = vB ? sc[3] * lsc : -INFINITY;
+      const float mx0 = warp_max_over_gid(fmaxf(s0, s2));
+      const float mx1 = warp_max_over_gid(fmaxf(s1, s3));
+      const float mn0 = fmaxf(m0, mx0);
+      const float mn1 = fmaxf(m1, mx1);
+      const float c0 = fast_exp2(m0 - mn0);
+      const float c1 = fast_exp2(m1 - mn1);
+      m0 = mn0;
+      m1 = mn1;
+      const float p0 = fast_exp2(s0 - mn0);
+      const float p1 = fast_exp2(s1 - mn1);
+      const float p2 = fast_exp2(s2 - mn0);
+      const float p3 = fast_exp2(s3 - mn1);
+      l0 = l0 * c0 + (p0 + p2);
+      l1 = l1 * c1 + (p1 + p3);
+#pragma unroll
+      for (int mt = 0; mt < kChunks; ++mt) {
+        o[mt][0] *= c0;
+        o[mt][1] *= c1;
+        o[mt][2] *= c0;
+        o[mt][3] *= c1;
+      }
+      // P^T fragment: transpose (token rows x head cols) to (head rows x token cols).
+      const uint32_t pb0 = movmatrix_trans(pack_f16x2(p0, p1));
+      const uint32_t pb1 = movmatrix_trans(pack_f16x2(p2, p3));
+
+      // ---- O^T += V_tile^T * P^T
+      const int n_valid = L - tok0;
+      uint32_t vmask = 0xFFFFFFFFu;
+      if (n_valid < 16) {
+        // Zero the V bytes of tokens >= L (their e4m3 codes may be NaN and
+        // 0 * NaN would poison the accumulator). Lane holds tokens 4tig..4tig+3.
+        const int k = min(max(n_valid - 4 * tig, 0), 4);
+        vmask = k >= 4 ? 0xFFFFFFFFu : ((1u << (8 * k)) - 1u);
+      }
+#pragma unroll
+      for (int mp = 0; mp < kChunks / 2; ++mp) {
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4(vbase + v_lane_off + (uint32_t)(32 * mp * bs), r0, r1, r2, r3);
+        r0 = __byte_perm(r0 & vmask, 0, v_swap_sel);
+        r1 = __byte_perm(r1 & vmask, 0, v_swap_sel);
+        r2 = __byte_perm(r2 & vmask, 0, v_swap_sel);
+        r3 = __byte_perm(r3 & vmask, 0, v_swap_sel);
+        mma_f16(o[2 * mp], e4m3x2_lo_to_f16x2(r0), e4m3x2_lo_to_f16x2(r1), e4m3x2_hi_to_f16x2(r0),
+                e4m3x2_hi_to_f16x2(r1), pb0, pb1);
+        mma_f16(o[2 * mp + 1], e4m3x2_lo_to_f16x2(r2), e4m3x2_lo_to_f16x2(r3), e4m3x2_hi_to_f16x2(r2),
+                e4m3x2_hi_to_f16x2(r3), pb0, pb1);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8u * stage);
+  }
+
+  // ------------------------------------------------ merge the consumer warps
+  l0 = warp_sum_over_gid(l0);
+  l1 = warp_sum_over_gid(l1);
+  // All consumer warps are past their last ring read once they pass this
+  // barrier; the abort decision is the same for all of them.
+  if (named_barrier_or(1, kConsumerWarps * 32, *abort_flag)) return;
+
+  float* mo = reinterpret_cast<float*>(smem);                       // [w][head][kMergeStride]
+  float* mml = mo + kConsumerWarps * kMaxGqa * kMergeStride;        // [w][head][2]
+  {
+    float* mw = mo + warp * kMaxGqa * kMergeStride;
+#pragma unroll
+    for (int mt = 0; mt < kChunks; ++mt) {
+      const int d0 = 16 * mt + gid;
+      mw[(2 * tig) * kMergeStride + d0] = o[mt][0];
+      mw[(2 * tig + 1) * kMergeStride + d0] = o[mt][1];
+      mw[(2 * tig) * kMergeStride + d0 + 8] = o[mt][2];
+      mw[(2 * tig + 1) * kMergeStride + d0 + 8] = o[mt][3];
+    }
+    if (gid == 0) {
+      float* ml = mml + warp * kMaxGqa * 2;
+      ml[(2 * tig) * 2 + 0] = m0;
+      ml[(2 * tig) * 2 + 1] = l0;
+      ml[(2 * tig + 1) * 2 + 0] = m1;
+      ml[(2 * tig + 1) * 2 + 1] = l1;
+    }
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+
+  const int d = threadIdx.x;  // 0..127: one output dim per consumer thread
+  for (int hh = 0; hh < g; ++hh) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mml[(w * kMaxGqa + hh) * 2]);
+    float acc = 0.f, den = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float mw = mml[(w * kMaxGqa + hh) * 2];
+        const float f = fast_exp2(mw - M);
+        acc += f * mo[(w * kMaxGqa + hh) * kMergeStride + d];
+        den += f * mml[(w * kMaxGqa + hh) * 2 + 1];
+      }
+    }
+    const int h = kvh * g + hh;
+    if (p.nsplit == 1) {
+      const float r = den > 0.f ? acc * (p.v_scale / den) : 0.f;
+      p.out[((size_t)s * H + h) * kHeadDim + d] = __float2bfloat16_rn(r);
+    } else {
+      const size_t prow = ((size_t)s * H + h) * p.nsplit + split;
+      p.part_o[prow * kHeadDim + d] = acc;
+      if (d == 0) {
+        p.part_ml[prow * 2 + 0] = M;
+        p.part_ml[prow * 2 + 1] = den;
+      }
+    }
+  }
+}
+
+// Log-sum-exp merge of the per-split partials of one (sequence, head) per
+// 128-thread block (one output dim per thread):
+//   M = max_i m_i,  out = v_scale * sum_i 2^(m_i - M) O_i / sum_i 2^(m_i - M) l_i
+// Splits with no pages were never written and are skipped by the same page
+// rule the decode kernel uses; a zero-length sequence gets zeros.
+struct MergeParams {
+  __nv_bfloat16* out;
+  const float* part_o;
+  const float* part_ml;
+  const int32_t* seq_lens;
+  int num_heads;
+  int block_size;
+  int max_blocks;
+  int nsplit;
+  float v_scale;
+};
+
+__global__ void __launch_bounds__(kHeadDim) pda_merge_kernel(const MergeParams p) {
+  const int h = blockIdx.x;
+  const int s = blockIdx.y;
+  const int d = threadIdx.x;
+  int L = __ldg(p.seq_lens + s);
+  L = max(0, min(L, p.max_blocks * p.block_size));
+  const int pages = (L + p.block_size - 1) / p.block_size;
+  int active = 0;
+  if (pages > 0) {
+    const int per = (pages + p.nsplit - 1) / p.nsplit;
+    active = (pages + per - 1) / per;
+  }
+  const size_t prow0 = ((size_t)s * p.num_heads + h) * p.nsplit;
+  float M = -INFINITY;
+  for (int i = 0; i < active; ++i) M = fmaxf(M, __ldg(p.part_ml + (prow0 + i) * 2));
+  float acc = 0.f, den = 0.f;
+  if (M != -INFINITY) {
+    for (int i = 0; i < active; ++i) {
+      const float f = fast_exp2(__ldg(p.part_ml + (prow0 + i) * 2) - M);
+      acc += f * __ldg(p.part_o + (prow0 + i) * kHeadDim + d);
+      den += f * __ldg(p.part_ml + (prow0 + i) * 2 + 1);
+    }
+  }
+  const float r = den > 0.f ? acc * (p.v_scale / den) : 0.f;
+  p.out[((size_t)s * p.num_heads + h) * kHeadDim + d] = __float2bfloat16_rn(r);
+}
+
+// One CTA waits on an mbarrier that nothing completes, with a short limit,
+// then records kStatusTestWaitTimeout and returns. Exercises the bounded
+// wait used by the decode kernel without faulting or hanging anything.
+__global__ void pda_bounded_wait_test_kernel(unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (!mbar_wait_bounded(b, 0u, nullptr, limit_ns)) atomicOr(&g_status, kStatusTestWaitTimeout);
+  }
+}
+
+}  // namespace pda

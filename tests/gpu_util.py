@@ -1,0 +1,58 @@
+"""Shared helpers for the GPU parity tests: run the CUDA path, compare with the oracle.
+
+Tolerances (on the bf16 output, against the binary64 oracle):
+  * max |gpu - oracle| <= 8e-3 and mean |gpu - oracle| <= 2e-4 per batch;
+  * an element whose exact value has |o| >= 4 cannot be stored in bf16 within
+    8e-3 (its rounding step is 2^-5 or more), so its bound is 8e-3 plus half
+    a bf16 step at |o|; such elements are counted and reported.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import paged_kv_decode_pda_gb300 as pda
+
+MAX_ABS = 8e-3
+MEAN_ABS = 2e-4
+
+
+def run_cuda(batch, out=None, stream=None) -> torch.Tensor:
+    cfg = batch.cfg
+    return pda.decode(batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.seq_lens, cfg.scale,
+                      cfg.k_scale, cfg.v_scale, out=out, stream=stream)
+
+
+def run_oracle(batch, seq_ids=None) -> np.ndarray:
+    cfg = batch.cfg
+    return oracle.decode(**batch.raw(), scale=cfg.scale, k_scale=cfg.k_scale, v_scale=cfg.v_scale,
+                         seq_ids=seq_ids)
+
+
+def bf16_half_step(x: np.ndarray) -> np.ndarray:
+    """Half the spacing of bf16 numbers around |x| (8 significant bits)."""
+    ax = np.maximum(np.abs(x), np.finfo(np.float32).tiny)
+    e = np.floor(np.log2(ax))
+    return np.ldexp(1.0, (e - 8).astype(np.int64))
+
+
+def compare(got_bf16: torch.Tensor, ref: np.ndarray, label: str = "") -> dict:
+    got = got_bf16.detach().float().cpu().numpy().astype(np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.isfinite(got).all(), "%s: non-finite output" % label
+    err = np.abs(got - ref)
+    big = np.abs(ref) >= 4.0
+    bound = np.where(big, MAX_ABS + bf16_half_step(ref), MAX_ABS)
+    worst = float(err.max()) if err.size else 0.0
+    mean = float(err.mean()) if err.size else 0.0
+    # error beyond the unavoidable bf16 rounding of the exact value
+    rounded = ref.astype(np.float32)
+    rounded = torch.from_numpy(rounded).to(torch.bfloat16).float().numpy().astype(np.float64)
+    stats = dict(max_abs=worst, mean_abs=mean, max_abs_vs_bf16_oracle=float(np.abs(got - rounded).max()),
+                 max_abs_out=float(np.abs(ref).max()) if ref.size else 0.0, n_bf16_limited=int(big.sum()))
+    assert (err <= bound).all(), "%s: max abs err %g (bound %g) at %s" % (
+        label, worst, MAX_ABS, np.unravel_index(np.argmax(err - bound), err.shape))
+    assert mean <= MEAN_ABS, "%s: mean abs err %g > %g" % (label, mean, MEAN_ABS)
+    return stats

@@ -1,0 +1,154 @@
+"""C-ABI surface on the CPU: symbols, status strings, heuristic, host validation.
+
+No test here launches a kernel or needs a GPU: every pda_decode call below is
+rejected by host-side validation before any CUDA call.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_decode_pda_gb300 as pda
+from paged_kv_decode_pda_gb300 import _binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return pda.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pda_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("pda_decode", "pda_status_string", "pda_choose_splits", "pda_reserve", "pda_release",
+                 "pda_query_device_status"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) == set(_binding.SIGNATURES), "binding and header disagree"
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        s = lib.pda_status_string(code)
+        assert s and s != b"unknown status"
+    assert lib.pda_status_string(99) == b"unknown status"
+
+
+# --------------------------------------------------------------- heuristic
+
+SM, OCC = 152, 3
+
+
+@pytest.mark.parametrize("S,Hk,MB,bs,expect", [
+    (16, 8, 64, 16, 4),       # 128 units, 1024-token contexts: capped by the 256-token minimum split
+    (64, 8, 64, 16, 2),       # 512 units < 2 waves of 456 CTAs
+    (256, 8, 256, 16, 1),     # 2048 units fill the GPU
+    (256, 8, 250, 16, 1),
+    (128, 8, 128, 64, 1),     # 1024 units, 64-token blocks
+    (1, 8, 256, 16, 16),      # a single long sequence splits to the cap
+    (1, 1, 2, 16, 1),         # too short to split
+])
+def test_choose_splits_table(lib, S, Hk, MB, bs, expect):
+    assert lib.pda_choose_splits(S, Hk, MB, bs, SM, OCC) == expect
+
+
+def test_choose_splits_bounds_and_monotonicity(lib):
+    for bs in (16, 32, 64, 128):
+        for MB in (1, 2, 7, 64, 255, 1000):
+            prev = None
+            for S in (1, 2, 3, 8, 16, 64, 256, 1024):
+                n = lib.pda_choose_splits(S, 8, MB, bs, SM, OCC)
+                assert 1 <= n <= max(1, MB)
+                # enough tokens per split
+                if n > 1:
+                    assert MB * bs // n >= 256
+                if prev is not None:
+                    assert n <= prev, "more sequences must never mean more splits"
+                prev = n
+
+
+def test_choose_splits_invalid_inputs_return_one(lib):
+    for args in [(0, 8, 64, 16, SM, OCC), (16, 0, 64, 16, SM, OCC), (16, 8, 0, 16, SM, OCC),
+                 (16, 8, 64, 0, SM, OCC), (16, 8, 64, 16, 0, OCC), (16, 8, 64, 16, SM, 0), (-1, 8, 64, 16, SM, OCC)]:
+        assert lib.pda_choose_splits(*args) == 1
+
+
+# -------------------------------------------------------- host validation
+
+A = 1 << 20  # a 16-byte-aligned fake address (never dereferenced: validation fails first)
+
+
+def call(lib, **kw):
+    a = dict(out=A, q=A, k=A, v=A, tables=A, lens=A, S=2, H=8, Hk=2, D=128, bs=16, MB=4, scale=0.1, ks=0.05,
+             vs=0.05, stream=None)
+    a.update(kw)
+    return lib.pda_decode(a["out"], a["q"], a["k"], a["v"], a["tables"], a["lens"], a["S"], a["H"], a["Hk"],
+                          a["D"], a["bs"], a["MB"], a["scale"], a["ks"], a["vs"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=64), pda.PDA_ERR_UNSUPPORTED),
+    (dict(D=256), pda.PDA_ERR_UNSUPPORTED),
+    (dict(bs=8), pda.PDA_ERR_UNSUPPORTED),
+    (dict(bs=24), pda.PDA_ERR_UNSUPPORTED),
+    (dict(bs=144), pda.PDA_ERR_UNSUPPORTED),
+    (dict(H=18, Hk=2), pda.PDA_ERR_UNSUPPORTED),   # GQA 9 > 8
+    (dict(H=7, Hk=2), pda.PDA_ERR_INVALID_ARG),     # not a multiple
+    (dict(S=-1), pda.PDA_ERR_INVALID_ARG),
+    (dict(H=0), pda.PDA_ERR_INVALID_ARG),
+    (dict(Hk=0), pda.PDA_ERR_INVALID_ARG),
+    (dict(MB=-1), pda.PDA_ERR_INVALID_ARG),
+    (dict(out=None), pda.PDA_ERR_INVALID_ARG),
+    (dict(q=None), pda.PDA_ERR_INVALID_ARG),
+    (dict(k=None), pda.PDA_ERR_INVALID_ARG),
+    (dict(v=None), pda.PDA_ERR_INVALID_ARG),
+    (dict(tables=None), pda.PDA_ERR_INVALID_ARG),
+    (dict(lens=None), pda.PDA_ERR_INVALID_ARG),
+    (dict(q=A + 8), pda.PDA_ERR_INVALID_ARG),       # misaligned
+    (dict(k=A + 4), pda.PDA_ERR_INVALID_ARG),
+    (dict(out=A + 2), pda.PDA_ERR_INVALID_ARG),
+    (dict(tables=A + 2), pda.PDA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), pda.PDA_ERR_INVALID_ARG),
+    (dict(ks=float("inf")), pda.PDA_ERR_INVALID_ARG),
+    (dict(S=70000), pda.PDA_ERR_UNSUPPORTED),
+])
+def test_decode_rejects_before_launch(lib, kw, status):
+    assert call(lib, **kw) == status
+
+
+def test_decode_zero_sequences_is_a_noop(lib):
+    assert call(lib, S=0, out=None, q=None, k=None, v=None, tables=None, lens=None) == pda.PDA_OK
+
+
+def test_bounded_wait_rejects_bad_limits(lib):
+    assert lib.pda_test_bounded_wait(0, None) == pda.PDA_ERR_INVALID_ARG
+    assert lib.pda_test_bounded_wait(2000001, None) == pda.PDA_ERR_INVALID_ARG
+
+
+def test_query_status_null_pointer(lib):
+    assert lib.pda_query_device_status(None, ctypes.POINTER(ctypes.c_int)()) == pda.PDA_ERR_INVALID_ARG
+
+
+def test_reserve_rejects_bad_args(lib):
+    assert lib.pda_reserve(4, 8, 2, 16, 24, None) == pda.PDA_ERR_INVALID_ARG
+    assert lib.pda_reserve(-1, 8, 2, 16, 16, None) == pda.PDA_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(pda.PdaError, match="not built"):
+        _binding.load(str(tmp_path / "missing.so"))

@@ -1,0 +1,256 @@
+"""GPU parity of the CUDA decode path (through the C ABI) against the fp64 oracle."""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_decode_pda_gb300 as pda
+import workloads
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    torch.cuda.set_device(0)
+    from paged_kv_decode_pda_gb300 import build
+    build.build()
+    pda.load()
+    pda.set_split_override(0)
+    yield
+    pda.set_split_override(0)
+    assert pda.query_device_status() == 0
+
+
+# ------------------------------------------------------------ full configs
+
+@pytest.mark.parametrize("name", [workloads.SMALL, "40q8kv-64seq-ctx1024-bs16"])
+def test_config_full_parity(name):
+    batch = workloads.make_batch(workloads.CONFIGS[name], device=DEV)
+    out = U.run_cuda(batch)
+    torch.cuda.synchronize()
+    stats = U.compare(out, U.run_oracle(batch), name)
+    print(name, stats)
+
+
+@pytest.mark.parametrize("name,n_sample", [
+    ("32q8kv-256seq-ctx4096-bs16", 24),
+    ("40q8kv-256seq-ctx1to4000-bs16", 48),
+    ("64q8kv-128seq-ctx8192-bs64", 12),
+])
+def test_config_full_size_sampled(name, n_sample):
+    """Full-size batch in the benchmark's launch configuration; sampled rows vs the oracle."""
+    cfg = workloads.CONFIGS[name]
+    batch = workloads.make_batch(cfg, device=DEV)
+    out = U.run_cuda(batch)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(123)
+    ids = set(rng.choice(cfg.num_seqs, size=n_sample, replace=False).tolist())
+    lens = batch.seq_lens_host
+    ids |= {int(np.argmin(lens)), int(np.argmax(lens)), 0, cfg.num_seqs - 1}
+    ids = sorted(ids)
+    ref = U.run_oracle(batch, seq_ids=ids)
+    stats = U.compare(out[ids], ref, name)
+    print(name, "splits", pda.plan_splits(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads,
+                                          cfg.max_num_blocks_per_seq, cfg.block_size), stats)
+
+
+# -------------------------------------------------------------- edge cases
+
+EDGE = [
+    # (num_seqs, H, Hk, seq_lens, block_size)
+    (1, 8, 8, [1], 16),
+    (3, 8, 1, [15, 16, 17], 16),
+    (4, 12, 4, [0, 1, 31, 33], 16),
+    (2, 16, 2, [63, 64], 64),
+    (3, 40, 8, [65, 1, 200], 64),
+    (2, 6, 2, [257, 5], 32),
+    (2, 14, 2, [100, 47], 48),
+    (2, 7, 1, [129, 128], 128),
+    (5, 64, 8, [3, 700, 16, 17, 1024], 16),
+    (2, 4, 4, [0, 0], 16),
+]
+
+
+@pytest.mark.parametrize("case", EDGE, ids=lambda c: "S%d_H%d_Hk%d_bs%d" % (c[0], c[1], c[2], c[4]))
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_edge_cases(case, splits):
+    S, H, Hk, lens, bs = case
+    batch = workloads.make_custom(S, H, Hk, lens, block_size=bs, pool_factor=1.5, seed=sum(lens) + H,
+                                  device=DEV)
+    pda.set_split_override(splits)
+    try:
+        out = U.run_cuda(batch)
+        torch.cuda.synchronize()
+    finally:
+        pda.set_split_override(0)
+    U.compare(out, U.run_oracle(batch), str(case))
+    for s, L in enumerate(lens):
+        if L == 0:
+            assert torch.all(out[s] == 0)
+
+
+def test_extra_table_columns_and_unused_pool_blocks():
+    batch = workloads.make_custom(3, 8, 2, [40, 200, 17], block_size=16, pool_factor=2.0, seed=5, device=DEV,
+                                  max_num_blocks_per_seq=40)
+    out = U.run_cuda(batch)
+    U.compare(out, U.run_oracle(batch), "wide table")
+
+
+# ---------------------------------------------------------- split behaviour
+
+def test_split_counts_agree():
+    batch = workloads.make_custom(4, 32, 8, [1000, 513, 77, 1024], block_size=16, seed=9, device=DEV)
+    ref = U.run_oracle(batch)
+    outs = {}
+    for n in (1, 2, 3, 7, 64):
+        pda.set_split_override(n)
+        try:
+            outs[n] = U.run_cuda(batch).float()
+            torch.cuda.synchronize()
+        finally:
+            pda.set_split_override(0)
+        U.compare(outs[n], ref, "splits=%d" % n)
+    for n in outs:
+        assert (outs[n] - outs[1]).abs().max().item() <= 8e-3
+
+
+def test_split_deterministic():
+    batch = workloads.make_custom(8, 40, 8, [300] * 8, seed=4, device=DEV)
+    for n in (1, 4):
+        pda.set_split_override(n)
+        try:
+            a = U.run_cuda(batch)
+            b = U.run_cuda(batch)
+            torch.cuda.synchronize()
+        finally:
+            pda.set_split_override(0)
+        assert torch.equal(a, b)
+
+
+# --------------------------------------------------- gather / tail handling
+
+def _permute_blocks(batch, seed):
+    """Same logical cache, different physical placement."""
+    NB = batch.num_blocks
+    g = torch.Generator().manual_seed(seed)
+    perm = torch.randperm(NB, generator=g)           # new_id = perm[old_id]
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(NB)
+    k2 = batch.k_cache[inv.to(batch.k_cache.device)].contiguous()
+    v2 = batch.v_cache[inv.to(batch.v_cache.device)].contiguous()
+    t2 = perm.to(torch.int32).to(batch.block_tables.device)[batch.block_tables.long()].contiguous()
+    return workloads.Batch(batch.cfg, batch.q, k2, v2, t2, batch.seq_lens, batch.seq_lens_host)
+
+
+@pytest.mark.parametrize("bs", [16, 64])
+def test_gather_is_exact_under_block_permutation(bs):
+    batch = workloads.make_custom(6, 32, 8, [1, 100, 513, 64, 1000, 17], block_size=bs, pool_factor=1.7, seed=11,
+                                  device=DEV)
+    for n in (1, 3):
+        pda.set_split_override(n)
+        try:
+            a = U.run_cuda(batch)
+            b = U.run_cuda(_permute_blocks(batch, 1))
+            c = U.run_cuda(_permute_blocks(batch, 2))
+            torch.cuda.synchronize()
+        finally:
+            pda.set_split_override(0)
+        assert torch.equal(a, b) and torch.equal(a, c), "output depends on physical block ids"
+
+
+@pytest.mark.parametrize("code", [0x7F, 0x7E, 0xFE])
+def test_tail_slots_and_table_padding_are_ignored(code):
+    lens = [19, 50, 16, 1, 33]
+    batch = workloads.make_custom(5, 16, 4, lens, block_size=16, pool_factor=1.0, seed=12, device=DEV,
+                                  max_num_blocks_per_seq=6)
+    base = U.run_cuda(batch).clone()
+    k2, v2, t2 = batch.k_cache.clone(), batch.v_cache.clone(), batch.block_tables.clone()
+    kb, vb = k2.view(torch.uint8), v2.view(torch.uint8)
+    for s, L in enumerate(lens):
+        P = (L + 15) // 16
+        n = L - (P - 1) * 16
+        b = int(batch.block_tables[s, P - 1])
+        kb[b, :, :, n:, :] = code
+        vb[b, :, :, n:] = code
+        t2[s, P:] = -1
+    poisoned = workloads.Batch(batch.cfg, batch.q, k2, v2, t2, batch.seq_lens, batch.seq_lens_host)
+    for n in (1, 2):
+        pda.set_split_override(n)
+        try:
+            got = U.run_cuda(poisoned)
+            ref = U.run_cuda(batch)
+            torch.cuda.synchronize()
+        finally:
+            pda.set_split_override(0)
+        assert torch.equal(got, ref)
+    assert torch.equal(U.run_cuda(poisoned), base)
+
+
+# -------------------------------------------------- streams, graphs, status
+
+def test_side_stream_and_graph_capture():
+    batch = workloads.make_custom(16, 32, 8, [1024] * 16, seed=13, device=DEV)
+    cfg = batch.cfg
+    eager = U.run_cuda(batch).clone()
+    s = torch.cuda.Stream()
+    pda.reserve(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq, cfg.block_size,
+                stream=s)
+    out = torch.empty_like(batch.q)
+    with torch.cuda.stream(s):
+        U.run_cuda(batch, out=out, stream=s)
+    s.synchronize()
+    assert torch.equal(out, eager)
+    g = torch.cuda.CUDAGraph()
+    out2 = torch.zeros_like(batch.q)
+    with torch.cuda.graph(g, stream=s):
+        U.run_cuda(batch, out=out2, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out2, eager)
+
+
+def test_workspace_growth_during_capture_is_refused():
+    pda.release()
+    batch = workloads.make_custom(2, 8, 2, [2048, 2048], seed=14, device=DEV)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    err = None
+    try:
+        with torch.cuda.graph(g, stream=s):
+            try:
+                U.run_cuda(batch, stream=s)
+            except pda.PdaError as e:
+                err = e
+    except Exception:
+        pass
+    assert err is not None and err.status == pda.PDA_ERR_WORKSPACE
+
+
+def test_bounded_wait_reports_and_context_survives():
+    assert pda.query_device_status() == 0
+    pda.bounded_wait_check(2000)
+    code = pda.query_device_status()
+    assert code != 0
+    assert pda.query_device_status() == 0
+    batch = workloads.make_custom(2, 8, 2, [40, 7], seed=15, device=DEV)
+    U.compare(U.run_cuda(batch), U.run_oracle(batch), "after timeout")
+
+
+def test_profile_events():
+    batch = workloads.make_custom(4, 8, 2, [512] * 4, seed=16, device=DEV)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pda.set_profile_events(a, b)
+    try:
+        U.run_cuda(batch)
+        b.synchronize()
+        assert a.elapsed_time(b) > 0
+    finally:
+        pda.set_profile_events(None, None)

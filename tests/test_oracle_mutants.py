@@ -16,9 +16,9 @@ from tests import oracle_pins as P
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "pda_oracle.cpp")
 
 MUTANTS = {
-    "dropped_k_scale": ("acc += qd[d] * (e4m3_value(code) * k_scale);", "acc += qd[d] * e4m3_value(code);"),
-    "dropped_v_scale": ("(e4m3_value(vpage[static_cast<long long>(d) * bs + slot]) * v_scale)",
-                        "e4m3_value(vpage[static_cast<long long>(d) * bs + slot])"),
+    "dropped_k_scale": ("acc += qd[d] * (e4m3[code] * k_scale);", "acc += qd[d] * e4m3[code];"),
+    "dropped_v_scale": ("(e4m3[vpage[static_cast<long long>(d) * bs + slot]] * v_scale)",
+                        "e4m3[vpage[static_cast<long long>(d) * bs + slot]]"),
     "dropped_softmax_scale": ("z[t] = scale * acc;", "z[t] = acc;"),
     "wrong_sign": ("z[t] = scale * acc;", "z[t] = -scale * acc;"),
     "k_page_token_major": ("kpage[(static_cast<long long>(d / 16) * bs + slot) * 16 + (d % 16)]",
