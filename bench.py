@@ -64,6 +64,22 @@ def dist_env():
     return ws, rank, local
 
 
+def reduce_max(x: float, ws: int, device) -> float:
+    """Max of a per-rank scalar over all ranks (the slowest replica's time)."""
+    if ws <= 1:
+        return float(x)
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(bytes_per_step_local: int, steps: int, elapsed_ms_local: float, ws: int, device):
+    """Whole-job GB/s: bytes all ranks moved (equal work per replica) over the slowest rank's time."""
+    ms = reduce_max(elapsed_ms_local, ws, device)
+    return ws * bytes_per_step_local * steps / (ms * 1e-3) / 1e9, ms
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -274,10 +290,7 @@ def run_ours(args, ws, rank, local):
     kern_ms = [a.elapsed_time(b) for a, b in ev_pairs]
     assert pda.query_device_status(stream) == 0
 
-    if ws > 1:
-        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    value, elapsed_ms = aggregate_throughput(bytes_per_call, K, elapsed_ms, ws, dev)
 
     # ---- end to end through the public API from pinned host buffers
     e2e = None
@@ -308,12 +321,8 @@ def run_ours(args, ws, rank, local):
                 e2e_step()
             e1.record(stream)
         stream.synchronize()
-        e2e_ms = e0.elapsed_time(e1)
-        if ws > 1:
-            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": ws * bytes_per_call * args.e2e_steps / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+        e2e_value, e2e_ms = aggregate_throughput(bytes_per_call, args.e2e_steps, e0.elapsed_time(e1), ws, dev)
+        e2e = {"value": e2e_value, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms / args.e2e_steps,
                "path": "pinned host -> cudaMemcpyAsync -> pda_decode -> cudaMemcpyAsync -> pinned host"}
@@ -328,7 +337,6 @@ def run_ours(args, ws, rank, local):
     kern_mean_ms = statistics.fmean(kern_ms)
     achieved = bytes_per_call / (kern_mean_ms * 1e-3) / 1e9
     traffic = ncu_traffic(cfg.name)
-    value = ws * bytes_per_call * K / (elapsed_ms * 1e-3) / 1e9
     us_per_call = elapsed_ms * 1e3 / K
 
     cpu = None

@@ -80,6 +80,11 @@ def _bind(lib):
     lib.pda_oracle_e4m3_value.argtypes = [ctypes.c_uint8]
     lib.pda_oracle_bf16_value.restype = f64
     lib.pda_oracle_bf16_value.argtypes = [ctypes.c_uint16]
+    lib.pda_oracle_e4m3_encode.restype = ctypes.c_uint8
+    lib.pda_oracle_e4m3_encode.argtypes = [f64]
+    lib.pda_oracle_reshape_and_cache.restype = i32
+    lib.pda_oracle_reshape_and_cache.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i64, ctypes.c_float,
+                                                 ctypes.c_float]
     lib.pda_oracle_max_threads.restype = i32
     lib.pda_oracle_max_threads.argtypes = []
     return lib
@@ -141,3 +146,32 @@ def decode(q, k_cache, v_cache, block_tables, seq_lens, *, scale: float, k_scale
     if rc != 0:
         raise OracleError("oracle rejected the inputs: %s (%d)" % (STATUS.get(rc, "?"), rc))
     return out
+
+
+def e4m3_encode(x: float, lib=None) -> int:
+    return (lib or load()).pda_oracle_e4m3_encode(float(x))
+
+
+def reshape_and_cache(k_cache, v_cache, key, value, slot_mapping, *, k_scale: float, v_scale: float,
+                      lib=None) -> None:
+    """Quantise and scatter new tokens into the paged caches, in place.
+
+    key / value: uint16 bf16 bits ``[T, Hk, D]``; slot_mapping: int64 ``[T]``
+    (negative = skip); caches: uint8 arrays as for ``decode`` (modified).
+    """
+    for a, dt in ((k_cache, np.uint8), (v_cache, np.uint8)):
+        if a.dtype != dt or not a.flags["C_CONTIGUOUS"]:
+            raise TypeError("caches must be C-contiguous uint8 arrays")
+    key = _c(key, np.uint16)
+    value = _c(value, np.uint16)
+    slot_mapping = _c(slot_mapping, np.int64)
+    T, Hk, D = key.shape
+    NB, Hk2, D16, bs, sixteen = k_cache.shape
+    if value.shape != key.shape or Hk2 != Hk or D16 * 16 != D or v_cache.shape != (NB, Hk, D, bs):
+        raise OracleError("shapes do not match")
+    L = lib if lib is not None else load()
+    rc = L.pda_oracle_reshape_and_cache(k_cache.ctypes.data, v_cache.ctypes.data, key.ctypes.data,
+                                        value.ctypes.data, slot_mapping.ctypes.data, T, Hk, D, bs, NB,
+                                        float(k_scale), float(v_scale))
+    if rc != 0:
+        raise OracleError("oracle rejected the inputs: %s (%d)" % (STATUS.get(rc, "?"), rc))

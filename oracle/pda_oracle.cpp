@@ -71,6 +71,26 @@ double bf16_value(uint16_t bits) {
   return static_cast<double>(f);
 }
 
+// Nearest OCP E4M3 code to x by exhaustive search over the finite
+// non-negative codes: ties go to the even code (even mantissa), magnitudes
+// past 448 saturate to 448, the sign is kept (so -0 and tiny negatives give
+// 0x80), NaN gives the NaN code with x's sign.
+uint8_t e4m3_encode(double x) {
+  if (std::isnan(x)) return std::signbit(x) ? 0xFF : 0x7F;
+  const uint8_t sign = std::signbit(x) ? 0x80 : 0x00;
+  const double a = std::fabs(x);
+  int best = 0;
+  double best_d = INFINITY;
+  for (int c = 0; c <= 0x7E; ++c) {
+    const double d = std::fabs(a - e4m3_value(static_cast<uint8_t>(c)));
+    if (d < best_d || (d == best_d && (c & 1) == 0)) {
+      best = c;
+      best_d = d;
+    }
+  }
+  return static_cast<uint8_t>(sign | best);
+}
+
 }  // namespace
 
 extern "C" {
@@ -180,6 +200,53 @@ int pda_oracle_decode(double* out, const uint16_t* q, const uint8_t* k_cache,
       const double wt = w[t] / denom;
       for (int d = 0; d < D; ++d) {
         o[d] += wt * (e4m3[vpage[static_cast<long long>(d) * bs + slot]] * v_scale);
+      }
+    }
+  }
+  return PDA_ORACLE_OK;
+}
+
+uint8_t pda_oracle_e4m3_encode(double x) { return e4m3_encode(x); }
+
+// KV-cache write: quantise new keys / values and scatter them into the
+// paged cache (vLLM API page "vllm.v1.attention.backends.rocm_aiter_unified_attn",
+// RocmAiterUnifiedAttentionImpl.do_kv_cache_update -> reshape_and_cache with
+// key, value, key_cache, value_cache, slot_mapping, k_scale, v_scale).
+// For token t with slot = slot_mapping[t] >= 0, block b = slot / block_size,
+// offset o = slot % block_size, kv head k and dim d:
+//   k_cache[b][k][d/16][o][d%16] = E4M3( float(key[t][k][d]) / k_scale )
+//   v_cache[b][k][d][o]          = E4M3( float(value[t][k][d]) / v_scale )
+// The quotient is the binary32 quotient (the cache stores what a binary32
+// division produces before rounding to e4m3); E4M3 is e4m3_encode. Negative
+// slots are skipped (padding). key / value are bf16 bit patterns
+// [num_tokens][num_kv_heads][head_size]. Returns PDA_ORACLE_BAD_SHAPE or
+// PDA_ORACLE_BAD_BLOCK_ID (a slot past the pool) without writing anything.
+int pda_oracle_reshape_and_cache(uint8_t* k_cache, uint8_t* v_cache, const uint16_t* key,
+                                 const uint16_t* value, const int64_t* slot_mapping, int num_tokens,
+                                 int num_kv_heads, int head_size, int block_size, long long num_blocks,
+                                 float k_scale, float v_scale) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_size <= 0 || head_size % 16 != 0 ||
+      block_size <= 0 || num_blocks < 0) {
+    return PDA_ORACLE_BAD_SHAPE;
+  }
+  const long long bs = block_size;
+  const long long D = head_size;
+  for (int t = 0; t < num_tokens; ++t) {
+    if (slot_mapping[t] >= num_blocks * bs) return PDA_ORACLE_BAD_BLOCK_ID;
+  }
+  for (int t = 0; t < num_tokens; ++t) {
+    const long long slot = slot_mapping[t];
+    if (slot < 0) continue;
+    const long long b = slot / bs;
+    const long long o = slot % bs;
+    for (int k = 0; k < num_kv_heads; ++k) {
+      for (long long d = 0; d < D; ++d) {
+        const long long src = (static_cast<long long>(t) * num_kv_heads + k) * D + d;
+        const float xk = static_cast<float>(bf16_value(key[src])) / k_scale;
+        const float xv = static_cast<float>(bf16_value(value[src])) / v_scale;
+        const long long page = (b * num_kv_heads + k) * D * bs;
+        k_cache[page + ((d / 16) * bs + o) * 16 + (d % 16)] = e4m3_encode(xk);
+        v_cache[page + d * bs + o] = e4m3_encode(xv);
       }
     }
   }

@@ -37,8 +37,8 @@ struct Workspace {
 std::mutex g_ws_mu;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
 
-// Ring geometry for a block size: a stage holds max(64, bs) tokens of K and
-// V (whole pages); about 64 KiB of stages per CTA.
+// Ring geometry for a block size: a stage holds max(16 * consumer warps, bs)
+// tokens of K and V (whole pages); about kRingBytes of stages per CTA.
 struct RingShape {
   int pages_per_stage;
   int num_stages;
@@ -50,7 +50,7 @@ RingShape ring_shape(int bs) {
   RingShape r;
   r.pages_per_stage = bs < pda::kStageTokensMin ? pda::kStageTokensMin / bs : 1;
   r.stage_bytes = 2u * (uint32_t)r.pages_per_stage * (uint32_t)(kHeadDim * bs);
-  r.num_stages = (int)(65536u / r.stage_bytes);
+  r.num_stages = (int)((uint32_t)pda::kRingBytes / r.stage_bytes);
   if (r.num_stages < 2) r.num_stages = 2;
   size_t ring = (size_t)r.num_stages * r.stage_bytes;
   size_t merge = (size_t)pda::kConsumerWarps * pda::kMaxGqa * (pda::kMergeStride + 2) * sizeof(float);

@@ -27,11 +27,23 @@
 
 namespace pda {
 
+// Compile-time tuning: consumer warps per CTA and shared-memory ring bytes.
+#ifndef PDA_CONSUMER_WARPS
+#define PDA_CONSUMER_WARPS 4
+#endif
+#ifndef PDA_RING_BYTES
+#define PDA_RING_BYTES 65536
+#endif
+
 constexpr int kHeadDim = 128;
 constexpr int kChunks = kHeadDim / 16;       // 16-dim chunks of a K page
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStageTokensMin = 64;          // a stage holds >= 64 tokens of K and V
+constexpr int kConsumerWarps = PDA_CONSUMER_WARPS;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 32;
+constexpr int kStageTokensMin = 16 * kConsumerWarps;  // one 16-token tile per consumer warp per stage
+constexpr int kRingBytes = PDA_RING_BYTES;
+constexpr int kMaxPagesPerStage = kStageTokensMin / 16;  // 16-token pages; divides 32
+static_assert(32 % kMaxPagesPerStage == 0, "stage pages must tile a 32-entry table chunk");
 constexpr int kMaxGqa = 8;                   // MMA N dimension: query heads of a group
 constexpr int kMergeStride = kHeadDim + 4;   // padded fp32 row of the CTA merge area
 
@@ -158,9 +170,9 @@ __global__ void __launch_bounds__(kThreads) pda_split_decode_kernel(const Decode
       for (int j = 0; j < chunk_pages; j += PPS, ++fill) {
         const int stage = fill % NS;
         const uint32_t round = (uint32_t)(fill / NS);
-        int blk[4];
+        int blk[kMaxPagesPerStage];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) blk[t] = __shfl_sync(0xffffffffu, my_block, (j + t) & 31);
+        for (int t = 0; t < kMaxPagesPerStage; ++t) blk[t] = __shfl_sync(0xffffffffu, my_block, (j + t) & 31);
         const int np = min(PPS, chunk_pages - j);
         const bool got = mbar_wait_bounded(empty0 + 8u * stage, (round & 1u) ^ 1u, abort_flag, kWaitLimitNs);
         if (!__all_sync(0xffffffffu, got)) {
@@ -176,7 +188,7 @@ __global__ void __launch_bounds__(kThreads) pda_split_decode_kernel(const Decode
           const uint32_t bar = full0 + 8u * stage;
           mbar_arrive_expect_tx(bar, 2u * page_bytes * (uint32_t)np);
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
+          for (int t = 0; t < kMaxPagesPerStage; ++t) {
             if (t < np) {
               const size_t off = (size_t)blk[t] * block_stride + (size_t)kvh * head_stride;
               bulk_g2s(sbase + (uint32_t)t * page_bytes, p.k_cache + off, page_bytes, bar);
@@ -335,7 +347,7 @@ __global__ void __launch_bounds__(kThreads) pda_split_decode_kernel(const Decode
   l1 = warp_sum_over_gid(l1);
   // All consumer warps are past their last ring read once they pass this
   // barrier; the abort decision is the same for all of them.
-  if (named_barrier_or(1, kConsumerWarps * 32, *abort_flag)) return;
+  if (named_barrier_or(1, kConsumerThreads, *abort_flag)) return;
 
   float* mo = reinterpret_cast<float*>(smem);                       // [w][head][kMergeStride]
   float* mml = mo + kConsumerWarps * kMaxGqa * kMergeStride;        // [w][head][2]
@@ -357,10 +369,11 @@ __global__ void __launch_bounds__(kThreads) pda_split_decode_kernel(const Decode
       ml[(2 * tig + 1) * 2 + 1] = l1;
     }
   }
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
 
-  const int d = threadIdx.x;  // 0..127: one output dim per consumer thread
-  for (int hh = 0; hh < g; ++hh) {
+  for (int i = threadIdx.x; i < g * kHeadDim; i += kConsumerThreads) {
+    const int hh = i / kHeadDim;
+    const int d = i % kHeadDim;
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mml[(w * kMaxGqa + hh) * 2]);

@@ -278,6 +278,101 @@ def pin_zero_length(lib):
     assert np.max(np.abs(got - ref)) <= 1e-12
 
 
+# ------------------------------------------------------- KV-cache write pins
+
+def torch_quantise(bits_u16: np.ndarray, scale: float) -> np.ndarray:
+    """bf16 bits -> fp32 -> / scale (binary32) -> clamp +-448 -> e4m3 (torch, RNE) codes."""
+    x = torch.from_numpy(bits_u16.view(np.int16)).view(torch.bfloat16).float()
+    q = (x / torch.tensor(scale, dtype=torch.float32)).clamp(-448.0, 448.0)
+    return q.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def pin_e4m3_encode(lib):
+    enc = lambda x: int(lib.pda_oracle_e4m3_encode(float(x)))
+    vals = torch_e4m3(np.arange(256, dtype=np.uint8))
+    for c in range(256):
+        if (c & 0x7F) == 0x7F:
+            continue
+        assert enc(vals[c]) == c, "code %#x does not round-trip" % c
+    pos = np.sort(vals[:0x7F])
+    mids = (pos[:-1] + pos[1:]) / 2                      # exact in binary64
+    ref = torch.from_numpy(mids.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert all(mids.astype(np.float32) == mids)
+    got = np.array([enc(m) for m in mids])
+    assert np.array_equal(got, ref), "ties must round to the even code"
+    rng = np.random.default_rng(17)
+    for sigma in (1e-3, 0.05, 1.0, 30.0, 300.0):
+        x = np.clip(rng.standard_normal(4000) * sigma, -448, 448).astype(np.float32)
+        ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        got = np.array([enc(v) for v in x])
+        assert np.array_equal(got, ref), "sigma %g" % sigma
+    for x, c in ((449.0, 0x7E), (464.0, 0x7E), (1e30, 0x7E), (math.inf, 0x7E), (-500.0, 0xFE), (-math.inf, 0xFE),
+                 (-0.0, 0x80), (0.0, 0x00), (-1e-9, 0x80)):
+        assert enc(x) == c, (x, hex(enc(x)), hex(c))
+    assert (enc(math.nan) & 0x7F) == 0x7F
+
+
+def _scatter_expected(k_cache, v_cache, kq, vq, slots, bs):
+    """Independent scatter of quantised codes [T, Hk, D] following the page layout."""
+    kc, vc = k_cache.copy(), v_cache.copy()
+    T, Hk, D = kq.shape
+    for t in range(T):
+        s = int(slots[t])
+        if s < 0:
+            continue
+        b, o = divmod(s, bs)
+        kc[b, :, :, o, :] = kq[t].reshape(Hk, D // 16, 16)
+        vc[b, :, :, o] = vq[t]
+    return kc, vc
+
+
+def pin_reshape_and_cache(lib):
+    rng = np.random.default_rng(23)
+    for (T, Hk, bs, NB, ks, vs) in ((5, 2, 16, 4, 0.05, 0.07), (37, 8, 64, 3, 0.05, 0.05), (9, 1, 32, 5, 0.3, 0.01)):
+        D = 128
+        key = torch.from_numpy(rng.standard_normal((T, Hk, D)).astype(np.float32)).to(torch.bfloat16)
+        val = torch.from_numpy((rng.standard_normal((T, Hk, D)) * 3).astype(np.float32)).to(torch.bfloat16)
+        kb = key.view(torch.int16).numpy().view(np.uint16).copy()
+        vb = val.view(torch.int16).numpy().view(np.uint16).copy()
+        slots = rng.permutation(NB * bs)[:T].astype(np.int64)
+        slots[rng.random(T) < 0.2] = -1
+        kc0 = rng.integers(0, 256, size=(NB, Hk, D // 16, bs, 16), dtype=np.uint8)
+        vc0 = rng.integers(0, 256, size=(NB, Hk, D, bs), dtype=np.uint8)
+        want_k, want_v = _scatter_expected(kc0, vc0, torch_quantise(kb, ks), torch_quantise(vb, vs), slots, bs)
+        kc, vc = kc0.copy(), vc0.copy()
+        oracle.reshape_and_cache(kc, vc, kb, vb, slots, k_scale=ks, v_scale=vs, lib=lib)
+        assert np.array_equal(kc, want_k), "K cache bytes differ"
+        assert np.array_equal(vc, want_v), "V cache bytes differ"
+
+
+def pin_quantise_in_binary32(lib):
+    """The code is decided on the binary32 quotient, not the exact one."""
+    rng = np.random.default_rng(29)
+    found = 0
+    for scale in (0.05, 0.07, 0.3, 0.011):
+        bits = rng.integers(0x3000, 0x4400, size=20000, dtype=np.uint16)   # positive bf16, 2^-31 .. 2^9
+        x = bits.astype(np.uint32) << 16
+        xf = x.view(np.float32).astype(np.float64)
+        q32 = (xf.astype(np.float32) / np.float32(scale)).astype(np.float64)
+        q64 = xf / float(np.float32(scale))
+        c32 = torch.from_numpy(np.clip(q32, -448, 448).astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        for i in range(len(bits)):
+            e32 = int(lib.pda_oracle_e4m3_encode(q32[i]))
+            e64 = int(lib.pda_oracle_e4m3_encode(q64[i]))
+            if e32 != e64:
+                found += 1
+                kc = np.zeros((1, 1, 8, 16, 16), dtype=np.uint8)
+                vc = np.zeros((1, 1, 128, 16), dtype=np.uint8)
+                kb = np.zeros((1, 1, 128), dtype=np.uint16)
+                kb[0, 0, 0] = bits[i]
+                oracle.reshape_and_cache(kc, vc, kb, kb.copy(), np.array([0], dtype=np.int64), k_scale=scale,
+                                         v_scale=scale, lib=lib)
+                assert kc[0, 0, 0, 0, 0] == e32 == c32[i], "cache code must follow the binary32 quotient"
+                if found >= 3:
+                    return
+    assert found > 0, "no binary32/exact decision difference found to pin"
+
+
 ALL_PINS = [pin_e4m3_table, pin_bf16, pin_dense, pin_large_logits, pin_permutation_invariance,
             pin_constant_v, pin_single_token, pin_zero_k, pin_tail_poison, pin_gqa_is_repeated_mha,
-            pin_zero_length]
+            pin_zero_length, pin_e4m3_encode, pin_reshape_and_cache, pin_quantise_in_binary32]

@@ -34,6 +34,15 @@ MUTANTS = {
                                "const long long b = block_tables[s * ((L + bs - 1) / bs) + t / bs];\n      const long long slot = t % bs;\n      const uint8_t* kpage"),
     "one_token_short": ("std::vector<double> z(L);\n    for (long long t = 0; t < L; ++t) {",
                         "std::vector<double> z(L);\n    z[L - 1] = -1e300;\n    for (long long t = 0; t + 1 < L; ++t) {"),
+    "encode_ties_to_odd": ("(d == best_d && (c & 1) == 0)", "(d == best_d && (c & 1) == 1)"),
+    "encode_ties_away": ("(d == best_d && (c & 1) == 0)", "(d == best_d)"),
+    "cache_write_divides_in_binary64": ("const float xk = static_cast<float>(bf16_value(key[src])) / k_scale;",
+                                        "const double xk = bf16_value(key[src]) / static_cast<double>(k_scale);"),
+    "cache_write_multiplies_scale": ("const float xv = static_cast<float>(bf16_value(value[src])) / v_scale;",
+                                     "const float xv = static_cast<float>(bf16_value(value[src])) * v_scale;"),
+    "cache_write_k_token_major": ("k_cache[page + ((d / 16) * bs + o) * 16 + (d % 16)]",
+                                  "k_cache[page + (o * (D / 16) + d / 16) * 16 + (d % 16)]"),
+    "cache_write_v_token_major": ("v_cache[page + d * bs + o]", "v_cache[page + o * D + d]"),
 }
 
 
