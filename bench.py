@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--config", default=workloads.HEADLINE, choices=sorted(workloads.CONFIGS))
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", type=int, default=0, metavar="N",
+                    help="profiling mode: N plain pda_decode calls on the config, no timing, no JSON metric")
     return ap.parse_args()
 
 
@@ -436,9 +438,36 @@ def run_reference(args, ws, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_profile(args):
+    """N plain calls of the decode path (what an ncu capture of this command sees)."""
+    import paged_kv_decode_pda_gb300 as pda
+    from paged_kv_decode_pda_gb300 import build
+
+    torch.cuda.set_device(0)
+    build.build()
+    cfg = workloads.CONFIGS[args.config]
+    batch = workloads.make_batch(cfg, device="cuda:0")
+    out = torch.empty_like(batch.q)
+    for _ in range(args.profile):
+        pda.decode(batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.seq_lens, cfg.scale,
+                   cfg.k_scale, cfg.v_scale, out=out)
+    torch.cuda.synchronize()
+    code = pda.query_device_status()
+    nsplit = pda.plan_splits(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq,
+                             cfg.block_size)
+    print(json.dumps({"profile_calls": args.profile, "workload": cfg.name, "kv_splits": nsplit,
+                      "bytes_per_call": workloads.algorithmic_bytes(cfg, batch.seq_lens_host),
+                      "device_status": code}))
+    if code:
+        raise SystemExit(1)
+
+
 def main():
     args = parse()
     ws, rank, local = dist_env()
+    if args.profile:
+        run_profile(args)
+        return
     if args.impl == "reference":
         run_reference(args, ws, rank, local)
     else:

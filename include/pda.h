@@ -51,7 +51,7 @@ typedef enum pda_status {
   PDA_ERR_UNSUPPORTED = 2,     /* valid but outside the supported set (see pda_decode) */
   PDA_ERR_WORKSPACE = 3,       /* workspace must grow while the stream is being captured */
   PDA_ERR_CUDA = 4,            /* a CUDA runtime call or kernel launch failed */
-  PDA_ERR_DEVICE_TIMEOUT = 5   /* a kernel gave up on a bounded wait (pda_query_device_status) */
+  PDA_ERR_DEVICE_TIMEOUT = 5   /* a kernel reported a device-side error (pda_query_device_status) */
 } pda_status;
 
 /*
@@ -104,6 +104,36 @@ pda_status pda_decode(void* out, const void* q, const void* k_cache, const void*
                       int num_heads, int num_kv_heads, int head_size, int block_size,
                       int max_num_blocks_per_seq, float scale, float k_scale, float v_scale,
                       cudaStream_t stream);
+
+/*
+ * pda_reshape_and_cache -- KV-cache write: quantise new keys and values to
+ * e4m3 with the per-tensor scales and scatter them into the paged cache.
+ *
+ * Source: vLLM API page "vllm.v1.attention.backends.rocm_aiter_unified_attn",
+ * RocmAiterUnifiedAttentionImpl.do_kv_cache_update, which hands key, value,
+ * key_cache, value_cache, slot_mapping, k_scale and v_scale to the cache
+ * writer before attention runs; the page layout is pda_decode's.
+ *
+ *   key, value    bf16  [num_tokens][num_kv_heads][head_size]   read
+ *   k_cache       e4m3  [num_blocks][num_kv_heads][head_size/16][block_size][16]  written
+ *   v_cache       e4m3  [num_blocks][num_kv_heads][head_size][block_size]          written
+ *   slot_mapping  int64 [num_tokens]: slot = block * block_size + offset;
+ *                 negative = padding (skipped)
+ *
+ * Token t goes to block slot/block_size, offset slot%block_size; byte d of
+ * kv head k is E4M3(float(x) / scale), the IEEE binary32 quotient rounded to
+ * the nearest e4m3 value (ties to even), saturating at +-448 (infinities
+ * included), NaN kept. Slots >= num_blocks * block_size are not written and
+ * set a code in the device status word (see pda_query_device_status).
+ * Slots must be distinct (two tokens writing one slot leave either value).
+ * Pointers 16-byte aligned (slot_mapping 8-byte), all on the current device.
+ * Supported: head_size 128, block_size a multiple of 16 up to 128. Scales
+ * must be finite and nonzero. Stream-ordered, no host sync, capturable.
+ */
+pda_status pda_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                                 const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_size,
+                                 int block_size, long long num_blocks, float k_scale, float v_scale,
+                                 cudaStream_t stream);
 
 /* Static text for a status code; never NULL. */
 const char* pda_status_string(int status);

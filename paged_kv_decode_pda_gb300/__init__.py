@@ -24,6 +24,7 @@ from ._binding import (  # noqa: F401
     query_device_status,
     release,
     reserve,
+    reshape_and_cache,
     set_profile_events,
     set_split_override,
     status_string,

@@ -37,6 +37,7 @@ SIGNATURES = {
     "pda_query_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_int)]),
     "pda_set_profile_events": (None, [_P, _P]),
     "pda_test_bounded_wait": (_I, [_I, _P]),
+    "pda_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_longlong, _F, _F, _P]),
 }
 
 _lock = threading.RLock()
@@ -185,3 +186,30 @@ def set_profile_events(before, after) -> None:
 
 def bounded_wait_check(timeout_us: int, stream=None) -> None:
     _check(load().pda_test_bounded_wait(int(timeout_us), _stream_ptr(stream)), "pda_test_bounded_wait")
+
+
+def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      slot_mapping: torch.Tensor, k_scale: float, v_scale: float, *, stream=None) -> None:
+    """Quantise and scatter new tokens into the paged fp8 cache (``pda_reshape_and_cache``).
+
+    key / value ``[T, Hk, 128]`` bf16; slot_mapping ``[T]`` int64 (negative =
+    skip); caches as for ``decode`` (written in place).
+    """
+    lib = load()
+    if key.dim() != 3 or value.shape != key.shape or key.dtype != torch.bfloat16 or value.dtype != torch.bfloat16:
+        raise PdaError(PDA_ERR_INVALID_ARG, "reshape_and_cache: key/value")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.shape != (key.shape[0],):
+        raise PdaError(PDA_ERR_INVALID_ARG, "reshape_and_cache: slot_mapping")
+    for t in (k_cache, v_cache):
+        if t.dtype not in (torch.float8_e4m3fn, torch.uint8):
+            raise PdaError(PDA_ERR_INVALID_ARG, "reshape_and_cache: cache dtype")
+    ts = [key, value, k_cache, v_cache, slot_mapping]
+    if not all(t.is_cuda and t.is_contiguous() for t in ts):
+        raise PdaError(PDA_ERR_INVALID_ARG, "reshape_and_cache: tensors must be contiguous CUDA tensors")
+    T, Hk, D = key.shape
+    NB, Hk2, D16, bs, sixteen = k_cache.shape
+    if Hk2 != Hk or D16 * 16 != D or sixteen != 16 or tuple(v_cache.shape) != (NB, Hk, D, bs):
+        raise PdaError(PDA_ERR_INVALID_ARG, "reshape_and_cache: shapes")
+    _check(lib.pda_reshape_and_cache(key.data_ptr(), value.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                     slot_mapping.data_ptr(), T, Hk, D, bs, NB, float(k_scale), float(v_scale),
+                                     _stream_ptr(stream)), "pda_reshape_and_cache")

@@ -265,6 +265,40 @@ pda_status pda_test_bounded_wait(int timeout_us, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? PDA_OK : PDA_ERR_CUDA;
 }
 
+pda_status pda_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                                 const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_size,
+                                 int block_size, long long num_blocks, float k_scale, float v_scale,
+                                 cudaStream_t stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 || num_blocks < 0)
+    return PDA_ERR_INVALID_ARG;
+  if (!std::isfinite(k_scale) || !std::isfinite(v_scale) || k_scale == 0.f || v_scale == 0.f)
+    return PDA_ERR_INVALID_ARG;
+  if (head_size != kHeadDim) return PDA_ERR_UNSUPPORTED;
+  if (block_size % 16 != 0 || block_size > 128) return PDA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PDA_OK;
+  if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PDA_ERR_INVALID_ARG;
+  if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return PDA_ERR_INVALID_ARG;
+  pda::CacheWriteParams p;
+  p.key = static_cast<const __nv_bfloat16*>(key);
+  p.value = static_cast<const __nv_bfloat16*>(value);
+  p.k_cache = static_cast<uint8_t*>(k_cache);
+  p.v_cache = static_cast<uint8_t*>(v_cache);
+  p.slot_mapping = slot_mapping;
+  p.num_tokens = num_tokens;
+  p.num_kv_heads = num_kv_heads;
+  p.block_size = block_size;
+  p.num_slots = num_blocks * (long long)block_size;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  const long long items = (long long)num_tokens * num_kv_heads;
+  const long long blocks = (items + pda::kCacheWriteWarps - 1) / pda::kCacheWriteWarps;
+  if (blocks > 0x7FFFFFFFLL) return PDA_ERR_UNSUPPORTED;
+  pda::pda_reshape_and_cache_kernel<<<(unsigned)blocks, pda::kCacheWriteWarps * 32, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? PDA_OK : PDA_ERR_CUDA;
+}
+
 pda_status pda_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
                       const int32_t* block_tables, const int32_t* seq_lens, int num_seqs, int num_heads,
                       int num_kv_heads, int head_size, int block_size, int max_num_blocks_per_seq, float scale,

@@ -19,6 +19,7 @@ enum : unsigned int {
   kStatusEmptyWaitTimeout = 1u << 1,  // producer waited too long for a free ring slot
   kStatusDrainTimeout = 1u << 2,      // copies still in flight at exit after the limit
   kStatusTestWaitTimeout = 1u << 3,   // pda_test_bounded_wait gave up (expected)
+  kStatusBadSlot = 1u << 4,           // reshape_and_cache saw a slot past the pool (skipped)
 };
 
 // Limit on any single barrier wait. Healthy waits last microseconds; the
@@ -152,6 +153,14 @@ __device__ __forceinline__ uint32_t e4m3x2_hi_to_f16x2(uint32_t x) {
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two fp32 -> e4m3x2 (hi in the upper byte), round to nearest even,
+// saturating finite (|x| > 448 and infinities give +-448; NaN stays NaN).
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
 

@@ -72,9 +72,9 @@ struct DecodeParams {
 // Token order of the 16 MMA rows of a K tile. Row r of the QK accumulator
 // holds token row_token(r); the order is chosen so that, after the P
 // fragment is transposed with movmatrix, each lane holds the probabilities
-// of exactly the tokens whose V bytes ldmatrix hands it (4 consecutive
-// tokens, with the two halves swapped for lanes whose tig >= 2), and so that
-// both 8-row K ldmatrix groups hit 8 distinct 16-byte bank groups.
+// of exactly the 4 consecutive tokens whose V bytes ldmatrix hands it (as
+// two pairs, in swapped order for lanes whose tig >= 2), and so that both
+// 8-row K ldmatrix groups hit 8 distinct 16-byte bank groups.
 // Rows 0..7 -> tokens 0,1,4,5,10,11,14,15; rows 8..15 -> 2,3,6,7,8,9,12,13.
 __device__ __forceinline__ int row_token(int r) {
   const int hi = r >> 3;            // which 8-row half
@@ -104,7 +104,7 @@ __device__ __forceinline__ float warp_sum_over_gid(float v) {
   return v;
 }
 
-__global__ void __launch_bounds__(kThreads) pda_split_decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, 3) pda_split_decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int split = blockIdx.x;
   const int kvh = blockIdx.y;
@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(kThreads) pda_split_decode_kernel(const Decode
   // chunk (2kk + (l >> 4)). V: lane l supplies dim (32mp + l).
   const uint32_t k_lane_off = (uint32_t)(row_token(lane & 15) * 16) + (uint32_t)((lane >> 4) * bs * 16);
   const uint32_t v_lane_off = (uint32_t)(lane * bs);
-  const uint32_t v_swap_sel = tig >= 2 ? 0x1032u : 0x3210u;
+  const bool low_quad = tig < 2;
   const int tokA = row_token(gid);
   const int tokB = row_token(gid + 8);
 
@@ -271,17 +271,20 @@ __global__ void __launch_bounds__(kThreads) pda_split_decode_kernel(const Decode
       const uint32_t kbase = sbase + (uint32_t)pg * page_bytes + (uint32_t)(sub * 256);
       const uint32_t vbase = sbase + (uint32_t)(PPS + pg) * page_bytes + (uint32_t)(sub * 16);
 
-      // ---- S^T = K_tile * Q^T
+      // ---- S^T = K_tile * Q^T (two independent accumulator chains)
       float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      float sd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int kk = 0; kk < kChunks / 2; ++kk) {
         uint32_t r0, r1, r2, r3;
         ldsm_x4(kbase + k_lane_off + (uint32_t)(2 * kk * bs * 16), r0, r1, r2, r3);
         mma_f16(sc, e4m3x2_lo_to_f16x2(r0), e4m3x2_lo_to_f16x2(r1), e4m3x2_hi_to_f16x2(r0),
                 e4m3x2_hi_to_f16x2(r1), qf[2 * kk][0], qf[2 * kk][1]);
-        mma_f16(sc, e4m3x2_lo_to_f16x2(r2), e4m3x2_lo_to_f16x2(r3), e4m3x2_hi_to_f16x2(r2),
+        mma_f16(sd, e4m3x2_lo_to_f16x2(r2), e4m3x2_lo_to_f16x2(r3), e4m3x2_hi_to_f16x2(r2),
                 e4m3x2_hi_to_f16x2(r3), qf[2 * kk + 1][0], qf[2 * kk + 1][1]);
       }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sc[i] += sd[i];
 
       // ---- online softmax (exp2 domain); tokens >= L are masked
       const bool vA = tok0 + tokA < L;
@@ -304,38 +307,45 @@ __global__ void __launch_bounds__(kThreads) pda_split_decode_kernel(const Decode
       const float p3 = fast_exp2(s3 - mn1);
       l0 = l0 * c0 + (p0 + p2);
       l1 = l1 * c1 + (p1 + p3);
+      if (__any_sync(0xffffffffu, (c0 != 1.f) | (c1 != 1.f))) {  // a running max moved
 #pragma unroll
-      for (int mt = 0; mt < kChunks; ++mt) {
-        o[mt][0] *= c0;
-        o[mt][1] *= c1;
-        o[mt][2] *= c0;
-        o[mt][3] *= c1;
+        for (int mt = 0; mt < kChunks; ++mt) {
+          o[mt][0] *= c0;
+          o[mt][1] *= c1;
+          o[mt][2] *= c0;
+          o[mt][3] *= c1;
+        }
       }
-      // P^T fragment: transpose (token rows x head cols) to (head rows x token cols).
-      const uint32_t pb0 = movmatrix_trans(pack_f16x2(p0, p1));
-      const uint32_t pb1 = movmatrix_trans(pack_f16x2(p2, p3));
+      // P^T fragment: transpose (token rows x head cols) to (head rows x token
+      // cols). Lane quads 2 and 3 hold their two token pairs in the other
+      // order (row_token), so they swap the two halves of the B fragment.
+      const uint32_t t0 = movmatrix_trans(pack_f16x2(p0, p1));
+      const uint32_t t1 = movmatrix_trans(pack_f16x2(p2, p3));
+      const uint32_t pb0 = low_quad ? t0 : t1;
+      const uint32_t pb1 = low_quad ? t1 : t0;
 
-      // ---- O^T += V_tile^T * P^T
+      // ---- O^T += V_tile^T * P^T; lane holds V bytes of tokens 4tig..4tig+3
+      uint32_t vr[kChunks / 2][4];
+#pragma unroll
+      for (int mp = 0; mp < kChunks / 2; ++mp)
+        ldsm_x4(vbase + v_lane_off + (uint32_t)(32 * mp * bs), vr[mp][0], vr[mp][1], vr[mp][2], vr[mp][3]);
       const int n_valid = L - tok0;
-      uint32_t vmask = 0xFFFFFFFFu;
       if (n_valid < 16) {
-        // Zero the V bytes of tokens >= L (their e4m3 codes may be NaN and
-        // 0 * NaN would poison the accumulator). Lane holds tokens 4tig..4tig+3.
+        // Zero the V bytes of tokens >= L: their e4m3 codes may be NaN and
+        // 0 * NaN would poison the accumulator.
         const int k = min(max(n_valid - 4 * tig, 0), 4);
-        vmask = k >= 4 ? 0xFFFFFFFFu : ((1u << (8 * k)) - 1u);
+        const uint32_t vmask = k >= 4 ? 0xFFFFFFFFu : ((1u << (8 * k)) - 1u);
+#pragma unroll
+        for (int mp = 0; mp < kChunks / 2; ++mp)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) vr[mp][i] &= vmask;
       }
 #pragma unroll
       for (int mp = 0; mp < kChunks / 2; ++mp) {
-        uint32_t r0, r1, r2, r3;
-        ldsm_x4(vbase + v_lane_off + (uint32_t)(32 * mp * bs), r0, r1, r2, r3);
-        r0 = __byte_perm(r0 & vmask, 0, v_swap_sel);
-        r1 = __byte_perm(r1 & vmask, 0, v_swap_sel);
-        r2 = __byte_perm(r2 & vmask, 0, v_swap_sel);
-        r3 = __byte_perm(r3 & vmask, 0, v_swap_sel);
-        mma_f16(o[2 * mp], e4m3x2_lo_to_f16x2(r0), e4m3x2_lo_to_f16x2(r1), e4m3x2_hi_to_f16x2(r0),
-                e4m3x2_hi_to_f16x2(r1), pb0, pb1);
-        mma_f16(o[2 * mp + 1], e4m3x2_lo_to_f16x2(r2), e4m3x2_lo_to_f16x2(r3), e4m3x2_hi_to_f16x2(r2),
-                e4m3x2_hi_to_f16x2(r3), pb0, pb1);
+        mma_f16(o[2 * mp], e4m3x2_lo_to_f16x2(vr[mp][0]), e4m3x2_lo_to_f16x2(vr[mp][1]),
+                e4m3x2_hi_to_f16x2(vr[mp][0]), e4m3x2_hi_to_f16x2(vr[mp][1]), pb0, pb1);
+        mma_f16(o[2 * mp + 1], e4m3x2_lo_to_f16x2(vr[mp][2]), e4m3x2_lo_to_f16x2(vr[mp][3]),
+                e4m3x2_hi_to_f16x2(vr[mp][2]), e4m3x2_hi_to_f16x2(vr[mp][3]), pb0, pb1);
       }
     }
     __syncwarp();
@@ -460,6 +470,61 @@ __global__ void pda_bounded_wait_test_kernel(unsigned long long limit_ns) {
   if (threadIdx.x == 0) {
     if (!mbar_wait_bounded(b, 0u, nullptr, limit_ns)) atomicOr(&g_status, kStatusTestWaitTimeout);
   }
+}
+
+// KV-cache write: quantise new keys / values to e4m3 with the per-tensor
+// scales and scatter them into the paged cache (vLLM API page
+// vllm.v1.attention.backends.rocm_aiter_unified_attn, do_kv_cache_update ->
+// reshape_and_cache). One warp per (token, kv head), 4 dims per lane:
+//   K bytes -> k_cache[b][k][d/16][o][d%16]   (one 4-byte store per lane)
+//   V bytes -> v_cache[b][k][d][o]            (four byte stores per lane)
+// with b = slot / bs, o = slot % bs. The code is decided on the IEEE binary32
+// quotient x / scale. Negative slots are padding; slots past the pool are
+// skipped and flagged in the status word.
+struct CacheWriteParams {
+  const __nv_bfloat16* key;      // [T][Hk][128]
+  const __nv_bfloat16* value;    // [T][Hk][128]
+  uint8_t* k_cache;
+  uint8_t* v_cache;
+  const int64_t* slot_mapping;   // [T]
+  int num_tokens;
+  int num_kv_heads;
+  int block_size;
+  long long num_slots;           // num_blocks * block_size
+  float k_scale;
+  float v_scale;
+};
+
+constexpr int kCacheWriteWarps = 8;
+
+__global__ void __launch_bounds__(kCacheWriteWarps * 32) pda_reshape_and_cache_kernel(const CacheWriteParams p) {
+  const long long item = (long long)blockIdx.x * kCacheWriteWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (item >= (long long)p.num_tokens * p.num_kv_heads) return;
+  const int t = (int)(item / p.num_kv_heads);
+  const int k = (int)(item % p.num_kv_heads);
+  const long long slot = __ldg(p.slot_mapping + t);
+  if (slot < 0) return;
+  if (slot >= p.num_slots) {
+    if (lane == 0) atomicOr(&g_status, kStatusBadSlot);
+    return;
+  }
+  const long long b = slot / p.block_size;
+  const int o = (int)(slot % p.block_size);
+  const size_t src = ((size_t)t * p.num_kv_heads + k) * kHeadDim + 4 * lane;
+  const uint2 kx = ld_nc_v2(p.key + src);
+  const uint2 vx = ld_nc_v2(p.value + src);
+  const float ks = p.k_scale, vs = p.v_scale;
+  const uint32_t kq = f32x2_to_e4m3x2(__fdiv_rn(bf16lo_f32(kx.x), ks), __fdiv_rn(bf16hi_f32(kx.x), ks)) |
+                      (f32x2_to_e4m3x2(__fdiv_rn(bf16lo_f32(kx.y), ks), __fdiv_rn(bf16hi_f32(kx.y), ks)) << 16);
+  const uint32_t vq = f32x2_to_e4m3x2(__fdiv_rn(bf16lo_f32(vx.x), vs), __fdiv_rn(bf16hi_f32(vx.x), vs)) |
+                      (f32x2_to_e4m3x2(__fdiv_rn(bf16lo_f32(vx.y), vs), __fdiv_rn(bf16hi_f32(vx.y), vs)) << 16);
+  const size_t page = ((size_t)b * p.num_kv_heads + k) * (size_t)kHeadDim * p.block_size;
+  const int d0 = 4 * lane;
+  *reinterpret_cast<uint32_t*>(p.k_cache + page + ((size_t)(d0 / 16) * p.block_size + o) * 16 + (d0 % 16)) = kq;
+  uint8_t* vrow = p.v_cache + page + (size_t)d0 * p.block_size + o;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) vrow[(size_t)i * p.block_size] = (uint8_t)(vq >> (8 * i));
 }
 
 }  // namespace pda

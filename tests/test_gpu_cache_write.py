@@ -1,0 +1,75 @@
+"""GPU KV-cache write (pda_reshape_and_cache) against the oracle: cache bytes must match exactly."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_decode_pda_gb300 as pda
+from tests import gpu_util as U
+import workloads
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _case(T, Hk, bs, NB, seed, scale_k=0.05, scale_v=0.07, pad_frac=0.2, special=False):
+    g = torch.Generator().manual_seed(seed)
+    key = torch.randn(T, Hk, 128, generator=g) * 2
+    val = torch.randn(T, Hk, 128, generator=g) * 30
+    if special:
+        key[0, 0, :8] = torch.tensor([float("inf"), -float("inf"), float("nan"), 1e6, -1e6, 0.0, -0.0, 1e-30])
+    key, val = key.to(torch.bfloat16), val.to(torch.bfloat16)
+    slots = torch.randperm(NB * bs, generator=g)[:T].to(torch.int64)
+    slots[torch.rand(T, generator=g) < pad_frac] = -1
+    kc = torch.randint(0, 256, (NB, Hk, 8, bs, 16), generator=g, dtype=torch.uint8)
+    vc = torch.randint(0, 256, (NB, Hk, 128, bs), generator=g, dtype=torch.uint8)
+    return key, val, slots, kc, vc, scale_k, scale_v
+
+
+@pytest.mark.parametrize("T,Hk,bs,NB,seed,special", [
+    (1, 1, 16, 1, 0, False), (7, 8, 16, 4, 1, True), (256, 8, 16, 300, 2, False), (100, 4, 64, 5, 3, False),
+    (33, 2, 32, 4, 4, True), (513, 8, 128, 9, 5, False),
+])
+def test_cache_write_bit_exact(T, Hk, bs, NB, seed, special):
+    key, val, slots, kc, vc, ks, vs = _case(T, Hk, bs, NB, seed, special=special)
+    kc_ref, vc_ref = kc.numpy().copy(), vc.numpy().copy()
+    oracle.reshape_and_cache(kc_ref, vc_ref, key.view(torch.int16).numpy().view(np.uint16),
+                             val.view(torch.int16).numpy().view(np.uint16), slots.numpy(), k_scale=ks, v_scale=vs)
+    kd, vd = kc.to(DEV), vc.to(DEV)
+    pda.reshape_and_cache(key.to(DEV), val.to(DEV), kd, vd, slots.to(DEV), ks, vs)
+    torch.cuda.synchronize()
+    assert pda.query_device_status() == 0
+    assert np.array_equal(kd.cpu().numpy(), kc_ref), "K cache bytes differ from the oracle"
+    assert np.array_equal(vd.cpu().numpy(), vc_ref), "V cache bytes differ from the oracle"
+
+
+def test_cache_write_out_of_pool_slot_is_skipped_and_flagged():
+    key, val, slots, kc, vc, ks, vs = _case(4, 2, 16, 2, 7, pad_frac=0.0)
+    slots[1] = 2 * 16 + 5       # past the pool
+    kd, vd = kc.to(DEV), vc.to(DEV)
+    pda.reshape_and_cache(key.to(DEV), val.to(DEV), kd, vd, slots.to(DEV), ks, vs)
+    assert pda.query_device_status() != 0
+    good = slots.clone()
+    good[1] = -1
+    kc_ref, vc_ref = kc.numpy().copy(), vc.numpy().copy()
+    oracle.reshape_and_cache(kc_ref, vc_ref, key.view(torch.int16).numpy().view(np.uint16),
+                             val.view(torch.int16).numpy().view(np.uint16), good.numpy(), k_scale=ks, v_scale=vs)
+    assert np.array_equal(kd.cpu().numpy(), kc_ref) and np.array_equal(vd.cpu().numpy(), vc_ref)
+
+
+def test_write_then_decode_matches_oracle():
+    """Fill a cache token by token through the GPU writer, then decode it."""
+    S, H, Hk, bs = 3, 16, 4, 16
+    lens = [40, 17, 64]
+    batch = workloads.make_custom(S, H, Hk, lens, block_size=bs, seed=8, device=DEV)
+    g = torch.Generator().manual_seed(9)
+    for s, L in enumerate(lens):
+        key = torch.randn(L, Hk, 128, generator=g).to(torch.bfloat16).to(DEV)
+        val = torch.randn(L, Hk, 128, generator=g).to(torch.bfloat16).to(DEV)
+        row = batch.block_tables[s].long()
+        t = torch.arange(L, device=DEV)
+        slots = row[t // bs] * bs + t % bs
+        pda.reshape_and_cache(key, val, batch.k_cache, batch.v_cache, slots, batch.cfg.k_scale, batch.cfg.v_scale)
+    out = U.run_cuda(batch)
+    U.compare(out, U.run_oracle(batch), "write-then-decode")
