@@ -106,6 +106,31 @@ pda_status pda_decode(void* out, const void* q, const void* k_cache, const void*
                       cudaStream_t stream);
 
 /*
+ * pda_decode_slot_scales -- pda_decode with per-slot dequantisation scales.
+ *
+ * Source: vLLM pull request lishuoshuo-amd/vllm#3, "Details", item "Scale
+ * tables": the asm kernel reads per-slot [blocks, kv_heads, block_size]
+ * scales (filled there with the per-tensor scale).
+ *
+ *   k_scales, v_scales  fp32 [num_blocks][num_kv_heads][block_size]  read,
+ *                       16-byte aligned, on the current device
+ *
+ * The token in slot o of block b, kv head k, dequantises as e4m3 *
+ * k_scales[b][k][o] (V: v_scales[b][k][o]). Every other argument, the
+ * supported set and the error behaviour are pda_decode's; tables filled with
+ * one value give pda_decode's result for that per-tensor scale (up to fp32
+ * rounding order). Entries of slots past a sequence's length are never used
+ * (they may hold anything). Within one KV split, the largest ratio between
+ * two V scales must stay below 2^15 (probabilities are carried in f16
+ * relative to the split's first V scale).
+ */
+pda_status pda_decode_slot_scales(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                  const float* k_scales, const float* v_scales, const int32_t* block_tables,
+                                  const int32_t* seq_lens, int num_seqs, int num_heads, int num_kv_heads,
+                                  int head_size, int block_size, int max_num_blocks_per_seq, float scale,
+                                  cudaStream_t stream);
+
+/*
  * pda_reshape_and_cache -- KV-cache write: quantise new keys and values to
  * e4m3 with the per-tensor scales and scatter them into the paged cache.
  *
@@ -146,8 +171,8 @@ const char* pda_status_string(int status);
  * max_num_blocks_per_seq pages of block_size tokens, on a device with
  * sm_count SMs that hold ctas_per_sm decode CTAs each. The cut mirrors the
  * pull request's dispatch rule ("Claims": work units compared with twice the
- * compute-unit count): split only while the units alone leave SMs idle,
- * never below a minimum page count per split. Result in
+ * compute-unit count): split until the CTAs make at least four waves over
+ * the resident slots, never below 256 tokens per split. Result in
  * [1, max(1, max_num_blocks_per_seq)]. Invalid arguments return 1.
  */
 int pda_choose_splits(int num_seqs, int num_kv_heads, int max_num_blocks_per_seq, int block_size,

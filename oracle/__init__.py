@@ -75,7 +75,7 @@ def _bind(lib):
     i32, i64, f64 = ctypes.c_int, ctypes.c_longlong, ctypes.c_double
     lib.pda_oracle_decode.restype = i32
     lib.pda_oracle_decode.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64,
-                                      f64, f64, f64, P, i32, i32]
+                                      f64, f64, f64, P, P, P, i32, i32]
     lib.pda_oracle_e4m3_value.restype = f64
     lib.pda_oracle_e4m3_value.argtypes = [ctypes.c_uint8]
     lib.pda_oracle_bf16_value.restype = f64
@@ -109,13 +109,14 @@ def _c(a, dtype):
     return a
 
 
-def decode(q, k_cache, v_cache, block_tables, seq_lens, *, scale: float, k_scale: float,
-           v_scale: float, num_blocks: int | None = None, seq_ids=None, num_threads: int = 0,
-           lib=None) -> np.ndarray:
+def decode(q, k_cache, v_cache, block_tables, seq_lens, *, scale: float, k_scale: float = 1.0,
+           v_scale: float = 1.0, k_scales=None, v_scales=None, num_blocks: int | None = None, seq_ids=None,
+           num_threads: int = 0, lib=None) -> np.ndarray:
     """Exact (binary64) decode attention; returns float64 ``[n, H, D]``.
 
     ``seq_ids`` selects a subset of sequences (rows of the result follow its
-    order); ``None`` computes every sequence.
+    order); ``None`` computes every sequence. ``k_scales`` / ``v_scales``
+    (float32 ``[NB, Hk, bs]``) replace the per-tensor scales slot by slot.
     """
     q = _c(q, np.uint16)
     k_cache = _c(k_cache, np.uint8)
@@ -137,11 +138,18 @@ def decode(q, k_cache, v_cache, block_tables, seq_lens, *, scale: float, k_scale
         seq_ids = _c(np.asarray(seq_ids, dtype=np.int32), np.int32)
         ids_p = seq_ids.ctypes.data
         n = int(seq_ids.shape[0])
+    ks_p = vs_p = None
+    if k_scales is not None or v_scales is not None:
+        k_scales = _c(k_scales, np.float32)
+        v_scales = _c(v_scales, np.float32)
+        if k_scales.shape != (NB, Hk, bs) or v_scales.shape != (NB, Hk, bs):
+            raise OracleError("scale tables must be [num_blocks, num_kv_heads, block_size]")
+        ks_p, vs_p = k_scales.ctypes.data, v_scales.ctypes.data
     out = np.zeros((n, H, D), dtype=np.float64)
     L = lib if lib is not None else load()
     rc = L.pda_oracle_decode(out.ctypes.data, q.ctypes.data, k_cache.ctypes.data, v_cache.ctypes.data,
                              block_tables.ctypes.data, seq_lens.ctypes.data, S, H, Hk, D, bs, MB,
-                             int(num_blocks), float(scale), float(k_scale), float(v_scale), ids_p, n,
+                             int(num_blocks), float(scale), float(k_scale), float(v_scale), ks_p, vs_p, ids_p, n,
                              int(num_threads))
     if rc != 0:
         raise OracleError("oracle rejected the inputs: %s (%d)" % (STATUS.get(rc, "?"), rc))

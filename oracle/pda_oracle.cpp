@@ -117,12 +117,20 @@ double pda_oracle_bf16_value(uint16_t bits) { return bf16_value(bits); }
 //   seq_lens     [num_seqs] int32
 // Only the first ceil(seq_lens[s] / block_size) entries of a table row are
 // read; only token slots t < seq_lens[s] are read from a page.
+//
+// Per-slot scale tables (vLLM pull request lishuoshuo-amd/vllm#3, "Details",
+// item "Scale tables": the asm kernel reads per-slot [blocks, kv_heads,
+// block_size] scales): when k_scales / v_scales are non-NULL they are fp32
+// [num_blocks][num_kv_heads][block_size] and the token in slot o of block b,
+// kv head k, dequantises with k_scales[b][k][o] (v_scales[b][k][o]) in place
+// of the per-tensor k_scale (v_scale).
 int pda_oracle_decode(double* out, const uint16_t* q, const uint8_t* k_cache,
                       const uint8_t* v_cache, const int32_t* block_tables,
                       const int32_t* seq_lens, int num_seqs, int num_heads,
                       int num_kv_heads, int head_size, int block_size,
                       int max_num_blocks_per_seq, long long num_blocks,
                       double scale, double k_scale, double v_scale,
+                      const float* k_scales, const float* v_scales,
                       const int32_t* seq_ids, int n_ids, int num_threads) {
   if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_size <= 0 ||
       block_size <= 0 || max_num_blocks_per_seq < 0 || num_blocks < 0 ||
@@ -176,10 +184,11 @@ int pda_oracle_decode(double* out, const uint16_t* q, const uint8_t* k_cache,
       const long long b = block_tables[s * MB + t / bs];
       const long long slot = t % bs;
       const uint8_t* kpage = k_cache + (b * num_kv_heads + kv) * static_cast<long long>(D) * bs;
+      const double ks = k_scales ? static_cast<double>(k_scales[(b * num_kv_heads + kv) * bs + slot]) : k_scale;
       double acc = 0.0;
       for (int d = 0; d < D; ++d) {
         const uint8_t code = kpage[(static_cast<long long>(d / 16) * bs + slot) * 16 + (d % 16)];
-        acc += qd[d] * (e4m3[code] * k_scale);
+        acc += qd[d] * (e4m3[code] * ks);
       }
       z[t] = scale * acc;
     }
@@ -197,9 +206,10 @@ int pda_oracle_decode(double* out, const uint16_t* q, const uint8_t* k_cache,
       const long long b = block_tables[s * MB + t / bs];
       const long long slot = t % bs;
       const uint8_t* vpage = v_cache + (b * num_kv_heads + kv) * static_cast<long long>(D) * bs;
+      const double vs = v_scales ? static_cast<double>(v_scales[(b * num_kv_heads + kv) * bs + slot]) : v_scale;
       const double wt = w[t] / denom;
       for (int d = 0; d < D; ++d) {
-        o[d] += wt * (e4m3[vpage[static_cast<long long>(d) * bs + slot]] * v_scale);
+        o[d] += wt * (e4m3[vpage[static_cast<long long>(d) * bs + slot]] * vs);
       }
     }
   }

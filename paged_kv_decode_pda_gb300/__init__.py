@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     PdaError,
     choose_splits,
     decode,
+    decode_slot_scales,
     decode_raw,
     load,
     plan_splits,

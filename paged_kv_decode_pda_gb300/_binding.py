@@ -38,6 +38,7 @@ SIGNATURES = {
     "pda_set_profile_events": (None, [_P, _P]),
     "pda_test_bounded_wait": (_I, [_I, _P]),
     "pda_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_longlong, _F, _F, _P]),
+    "pda_decode_slot_scales": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
 }
 
 _lock = threading.RLock()
@@ -104,6 +105,27 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
     device. Returns ``out`` (allocated like q when not given).
     """
     lib = load()
+    _check_decode_args(q, k_cache, v_cache, block_tables, seq_lens)
+    out = _out_like(q, out)
+    S, H, D = q.shape
+    NB, Hk, D16, bs, sixteen = k_cache.shape
+    st = lib.pda_decode(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                        block_tables.data_ptr(), seq_lens.data_ptr(), S, H, Hk, D, bs,
+                        int(block_tables.shape[1]), float(scale), float(k_scale), float(v_scale),
+                        _stream_ptr(stream))
+    _check(st, "pda_decode")
+    return out
+
+
+def _out_like(q, out):
+    if out is None:
+        return torch.empty_like(q)
+    if out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous() or not out.is_cuda:
+        raise PdaError(PDA_ERR_INVALID_ARG, "decode: out")
+    return out
+
+
+def _check_decode_args(q, k_cache, v_cache, block_tables, seq_lens):
     if q.dim() != 3 or k_cache.dim() != 5 or v_cache.dim() != 4 or block_tables.dim() != 2 or seq_lens.dim() != 1:
         raise PdaError(PDA_ERR_INVALID_ARG, "decode: tensor ranks")
     if q.dtype != torch.bfloat16 or block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
@@ -119,15 +141,25 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
     if (sixteen != 16 or D16 * 16 != D or tuple(v_cache.shape) != (NB, Hk, D, bs)
             or block_tables.shape[0] != S or seq_lens.shape[0] != S):
         raise PdaError(PDA_ERR_INVALID_ARG, "decode: shapes")
-    if out is None:
-        out = torch.empty_like(q)
-    elif out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous() or not out.is_cuda:
-        raise PdaError(PDA_ERR_INVALID_ARG, "decode: out")
-    st = lib.pda_decode(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
-                        block_tables.data_ptr(), seq_lens.data_ptr(), S, H, Hk, D, bs,
-                        int(block_tables.shape[1]), float(scale), float(k_scale), float(v_scale),
-                        _stream_ptr(stream))
-    _check(st, "pda_decode")
+
+
+def decode_slot_scales(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, k_scales: torch.Tensor,
+                       v_scales: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float, *,
+                       out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """``pda_decode_slot_scales``: decode with per-slot fp32 scale tables ``[NB, Hk, bs]``."""
+    lib = load()
+    _check_decode_args(q, k_cache, v_cache, block_tables, seq_lens)
+    NB, Hk, _, bs, _ = k_cache.shape
+    for t in (k_scales, v_scales):
+        if t.dtype != torch.float32 or tuple(t.shape) != (NB, Hk, bs) or not t.is_cuda or not t.is_contiguous():
+            raise PdaError(PDA_ERR_INVALID_ARG, "decode_slot_scales: scale tables must be fp32 [NB, Hk, bs]")
+    out = _out_like(q, out)
+    S, H, D = q.shape
+    st = lib.pda_decode_slot_scales(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                    k_scales.data_ptr(), v_scales.data_ptr(), block_tables.data_ptr(),
+                                    seq_lens.data_ptr(), S, H, Hk, D, bs, int(block_tables.shape[1]), float(scale),
+                                    _stream_ptr(stream))
+    _check(st, "pda_decode_slot_scales")
     return out
 
 

@@ -24,7 +24,7 @@ std::atomic<cudaEvent_t> g_prof_after{nullptr};
 
 struct DeviceInfo {
   int sm_count = 0;
-  int ctas_per_sm_by_bs[9] = {0};  // index bs/16 (1..8)
+  int ctas_per_sm_by_bs[2][9] = {{0}};  // [slot scales][bs/16 (1..8)]
   bool smem_attr_set = false;
 };
 std::mutex g_dev_mu;
@@ -43,14 +43,16 @@ struct RingShape {
   int pages_per_stage;
   int num_stages;
   uint32_t stage_bytes;
+  uint32_t scale_off;
   size_t smem_bytes;
 };
 
-RingShape ring_shape(int bs) {
+RingShape ring_shape(int bs, bool slot_scales = false) {
   RingShape r;
   r.pages_per_stage = bs < pda::kStageTokensMin ? pda::kStageTokensMin / bs : 1;
-  r.stage_bytes = 2u * (uint32_t)r.pages_per_stage * (uint32_t)(kHeadDim * bs);
-  r.num_stages = (int)((uint32_t)pda::kRingBytes / r.stage_bytes);
+  r.scale_off = 2u * (uint32_t)r.pages_per_stage * (uint32_t)(kHeadDim * bs);
+  r.stage_bytes = r.scale_off + (slot_scales ? 2u * (uint32_t)r.pages_per_stage * (uint32_t)bs * 4u : 0u);
+  r.num_stages = (int)((uint32_t)pda::kRingBytes / r.scale_off);  // scale rows ride on top
   if (r.num_stages < 2) r.num_stages = 2;
   size_t ring = (size_t)r.num_stages * r.stage_bytes;
   size_t merge = (size_t)pda::kConsumerWarps * pda::kMaxGqa * (pda::kMergeStride + 2) * sizeof(float);
@@ -84,7 +86,7 @@ pda_status validate(const void* out, const void* q, const void* k_cache, const v
   return PDA_OK;
 }
 
-pda_status device_info(int dev, int bs, int* sm_count, int* ctas_per_sm) {
+pda_status device_info(int dev, int bs, int* sm_count, int* ctas_per_sm, bool slot_scales = false) {
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceInfo& di = g_devices[dev];
   if (di.sm_count == 0) {
@@ -97,20 +99,27 @@ pda_status device_info(int dev, int bs, int* sm_count, int* ctas_per_sm) {
     // Opt in to the largest ring any block size uses.
     size_t mx = 0;
     for (int b = 16; b <= 128; b += 16) {
-      size_t s = ring_shape(b).smem_bytes;
-      mx = s > mx ? s : mx;
+      for (int sc = 0; sc < 2; ++sc) {
+        size_t s = ring_shape(b, sc != 0).smem_bytes;
+        mx = s > mx ? s : mx;
+      }
     }
-    if (cudaFuncSetAttribute(pda::pda_split_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(pda::pda_split_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)mx) != cudaSuccess ||
+        cudaFuncSetAttribute(pda::pda_split_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)mx) != cudaSuccess)
       return PDA_ERR_CUDA;
     di.smem_attr_set = true;
   }
-  int& occ = di.ctas_per_sm_by_bs[bs / 16];
+  int& occ = di.ctas_per_sm_by_bs[slot_scales ? 1 : 0][bs / 16];
   if (occ == 0) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pda::pda_split_decode_kernel, pda::kThreads,
-                                                      ring_shape(bs).smem_bytes) != cudaSuccess)
-      return PDA_ERR_CUDA;
+    const cudaError_t e =
+        slot_scales ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pda::pda_split_decode_kernel<true>,
+                                                                    pda::kThreads, ring_shape(bs, true).smem_bytes)
+                    : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pda::pda_split_decode_kernel<false>,
+                                                                    pda::kThreads, ring_shape(bs).smem_bytes);
+    if (e != cudaSuccess) return PDA_ERR_CUDA;
     occ = n > 0 ? n : 1;
   }
   *sm_count = di.sm_count;
@@ -125,6 +134,15 @@ int resolve_splits(int num_seqs, int num_kv_heads, int max_blocks, int bs, int s
   if (n > cap) n = cap;
   if (n < 1) n = 1;
   return n;
+}
+
+// Profiling events: inside stream capture a plain record only expresses a
+// dependency, so record them as external event nodes there.
+cudaError_t record_profile_event(cudaEvent_t e, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    return cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+  return cudaEventRecord(e, s);
 }
 
 size_t workspace_bytes(int num_seqs, int num_heads, int nsplit) {
@@ -161,6 +179,81 @@ pda_status get_workspace(int dev, cudaStream_t stream, size_t bytes, void** out)
 
 }  // namespace
 
+// Shared launch path of pda_decode (k_scales == v_scales == nullptr) and
+// pda_decode_slot_scales (per-slot tables; k_scale, v_scale unused).
+static pda_status launch_decode(bool slot, void* out, const void* q, const void* k_cache, const void* v_cache,
+                                const float* k_scales, const float* v_scales, const int32_t* block_tables,
+                                const int32_t* seq_lens, int num_seqs, int num_heads, int num_kv_heads,
+                                int head_size, int block_size, int max_num_blocks_per_seq, float scale,
+                                float k_scale, float v_scale, cudaStream_t stream) {
+  pda_status st = validate(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_heads, num_kv_heads,
+                           head_size, block_size, max_num_blocks_per_seq, scale, k_scale, v_scale);
+  if (st != PDA_OK || num_seqs == 0) return st;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PDA_ERR_CUDA;
+  int sms = 0, occ = 0;
+  st = device_info(dev, block_size, &sms, &occ, slot);
+  if (st != PDA_OK) return st;
+  const int MB = max_num_blocks_per_seq > 0 ? max_num_blocks_per_seq : 1;
+  const int nsplit = resolve_splits(num_seqs, num_kv_heads, MB, block_size, sms, occ);
+  void* ws = nullptr;
+  st = get_workspace(dev, stream, workspace_bytes(num_seqs, num_heads, nsplit), &ws);
+  if (st != PDA_OK) return st;
+
+  const RingShape rs = ring_shape(block_size, slot);
+  pda::DecodeParams p;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k_cache = static_cast<const uint8_t*>(k_cache);
+  p.v_cache = static_cast<const uint8_t*>(v_cache);
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.part_o = static_cast<float*>(ws);
+  p.part_ml = ws ? static_cast<float*>(ws) + (size_t)num_seqs * num_heads * nsplit * kHeadDim : nullptr;
+  p.num_heads = num_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.gqa = num_heads / num_kv_heads;
+  p.block_size = block_size;
+  p.max_blocks = max_num_blocks_per_seq;
+  p.nsplit = nsplit;
+  p.pages_per_stage = rs.pages_per_stage;
+  p.num_stages = rs.num_stages;
+  p.stage_bytes = rs.stage_bytes;
+  p.scale_off = rs.scale_off;
+  p.k_scales = slot ? k_scales : nullptr;
+  p.v_scales = slot ? v_scales : nullptr;
+  p.logit_scale_log2 = (float)((double)scale * (slot ? 1.0 : (double)k_scale) * 1.4426950408889634);
+  p.v_scale = v_scale;
+
+  cudaEvent_t eb = g_prof_before.load(), ea = g_prof_after.load();
+  if (eb && ea && record_profile_event(eb, stream) != cudaSuccess) return PDA_ERR_CUDA;
+  dim3 grid((unsigned)nsplit, (unsigned)num_kv_heads, (unsigned)num_seqs);
+  if (slot)
+    pda::pda_split_decode_kernel<true><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(p);
+  else
+    pda::pda_split_decode_kernel<false><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
+  if (eb && ea && record_profile_event(ea, stream) != cudaSuccess) return PDA_ERR_CUDA;
+
+  if (nsplit > 1) {
+    pda::MergeParams mp;
+    mp.out = p.out;
+    mp.part_o = p.part_o;
+    mp.part_ml = p.part_ml;
+    mp.seq_lens = seq_lens;
+    mp.num_heads = num_heads;
+    mp.block_size = block_size;
+    mp.max_blocks = max_num_blocks_per_seq;
+    mp.nsplit = nsplit;
+    mp.v_scale = slot ? 1.f : v_scale;
+    pda::pda_merge_kernel<<<dim3((unsigned)num_heads, (unsigned)num_seqs), kHeadDim, 0, stream>>>(mp);
+    if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
+  }
+  return PDA_OK;
+}
+
+
 extern "C" {
 
 const char* pda_status_string(int status) {
@@ -182,11 +275,14 @@ int pda_choose_splits(int num_seqs, int num_kv_heads, int max_num_blocks_per_seq
     return 1;
   const long long units = (long long)num_seqs * num_kv_heads;
   const long long slots = (long long)sm_count * ctas_per_sm;
-  // Split only while the work units alone cannot fill two waves of CTAs,
-  // and keep at least kMinSplitTokens tokens of streaming per split so the
-  // page ring pays for its fill and the partials stay small next to K/V.
+  // Split until the CTAs make at least kMinWaves waves over the resident
+  // slots (fewer, longer CTAs leave the GPU under-filled while the last wave
+  // drains), but keep at least kMinSplitTokens tokens of streaming per split
+  // so the page ring pays for its fill and the partials stay small next to
+  // the K/V bytes.
+  const long long kMinWaves = 4;
   const long long kMinSplitTokens = 256;
-  long long want = (2 * slots + units - 1) / units;
+  long long want = (kMinWaves * slots + units - 1) / units;
   const long long min_pages = (kMinSplitTokens + block_size - 1) / block_size;
   long long cap = max_num_blocks_per_seq / min_pages;
   if (cap < 1) cap = 1;
@@ -303,65 +399,21 @@ pda_status pda_decode(void* out, const void* q, const void* k_cache, const void*
                       const int32_t* block_tables, const int32_t* seq_lens, int num_seqs, int num_heads,
                       int num_kv_heads, int head_size, int block_size, int max_num_blocks_per_seq, float scale,
                       float k_scale, float v_scale, cudaStream_t stream) {
-  pda_status st = validate(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_heads, num_kv_heads,
-                           head_size, block_size, max_num_blocks_per_seq, scale, k_scale, v_scale);
-  if (st != PDA_OK || num_seqs == 0) return st;
+  return launch_decode(false, out, q, k_cache, v_cache, nullptr, nullptr, block_tables, seq_lens, num_seqs,
+                       num_heads, num_kv_heads, head_size, block_size, max_num_blocks_per_seq, scale, k_scale,
+                       v_scale, stream);
+}
 
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return PDA_ERR_CUDA;
-  int sms = 0, occ = 0;
-  st = device_info(dev, block_size, &sms, &occ);
-  if (st != PDA_OK) return st;
-  const int MB = max_num_blocks_per_seq > 0 ? max_num_blocks_per_seq : 1;
-  const int nsplit = resolve_splits(num_seqs, num_kv_heads, MB, block_size, sms, occ);
-  void* ws = nullptr;
-  st = get_workspace(dev, stream, workspace_bytes(num_seqs, num_heads, nsplit), &ws);
-  if (st != PDA_OK) return st;
-
-  const RingShape rs = ring_shape(block_size);
-  pda::DecodeParams p;
-  p.out = static_cast<__nv_bfloat16*>(out);
-  p.q = static_cast<const __nv_bfloat16*>(q);
-  p.k_cache = static_cast<const uint8_t*>(k_cache);
-  p.v_cache = static_cast<const uint8_t*>(v_cache);
-  p.block_tables = block_tables;
-  p.seq_lens = seq_lens;
-  p.part_o = static_cast<float*>(ws);
-  p.part_ml = ws ? static_cast<float*>(ws) + (size_t)num_seqs * num_heads * nsplit * kHeadDim : nullptr;
-  p.num_heads = num_heads;
-  p.num_kv_heads = num_kv_heads;
-  p.gqa = num_heads / num_kv_heads;
-  p.block_size = block_size;
-  p.max_blocks = max_num_blocks_per_seq;
-  p.nsplit = nsplit;
-  p.pages_per_stage = rs.pages_per_stage;
-  p.num_stages = rs.num_stages;
-  p.stage_bytes = rs.stage_bytes;
-  p.logit_scale_log2 = (float)((double)scale * (double)k_scale * 1.4426950408889634);
-  p.v_scale = v_scale;
-
-  cudaEvent_t eb = g_prof_before.load(), ea = g_prof_after.load();
-  if (eb && ea && cudaEventRecord(eb, stream) != cudaSuccess) return PDA_ERR_CUDA;
-  dim3 grid((unsigned)nsplit, (unsigned)num_kv_heads, (unsigned)num_seqs);
-  pda::pda_split_decode_kernel<<<grid, pda::kThreads, rs.smem_bytes, stream>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
-  if (eb && ea && cudaEventRecord(ea, stream) != cudaSuccess) return PDA_ERR_CUDA;
-
-  if (nsplit > 1) {
-    pda::MergeParams mp;
-    mp.out = p.out;
-    mp.part_o = p.part_o;
-    mp.part_ml = p.part_ml;
-    mp.seq_lens = seq_lens;
-    mp.num_heads = num_heads;
-    mp.block_size = block_size;
-    mp.max_blocks = max_num_blocks_per_seq;
-    mp.nsplit = nsplit;
-    mp.v_scale = v_scale;
-    pda::pda_merge_kernel<<<dim3((unsigned)num_heads, (unsigned)num_seqs), kHeadDim, 0, stream>>>(mp);
-    if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
-  }
-  return PDA_OK;
+pda_status pda_decode_slot_scales(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                  const float* k_scales, const float* v_scales, const int32_t* block_tables,
+                                  const int32_t* seq_lens, int num_seqs, int num_heads, int num_kv_heads,
+                                  int head_size, int block_size, int max_num_blocks_per_seq, float scale,
+                                  cudaStream_t stream) {
+  if (num_seqs > 0 && (!k_scales || !v_scales || !aligned16(k_scales) || !aligned16(v_scales)))
+    return PDA_ERR_INVALID_ARG;
+  return launch_decode(true, out, q, k_cache, v_cache, k_scales, v_scales, block_tables, seq_lens, num_seqs,
+                       num_heads, num_kv_heads, head_size, block_size, max_num_blocks_per_seq, scale, 1.f, 1.f,
+                       stream);
 }
 
 }  // extern "C"

@@ -65,8 +65,11 @@ struct DecodeParams {
   int pages_per_stage;
   int num_stages;
   uint32_t stage_bytes;
-  float logit_scale_log2;       // scale * k_scale * log2(e)
-  float v_scale;
+  uint32_t scale_off;           // per-slot scale rows inside a stage (slot-scale variant)
+  const float* k_scales;        // [NB][Hk][bs] fp32 (slot-scale variant)
+  const float* v_scales;        // [NB][Hk][bs] fp32 (slot-scale variant)
+  float logit_scale_log2;       // scale * k_scale * log2(e)  (scale * log2(e) with slot scales)
+  float v_scale;                // per-tensor V scale (unused with slot scales)
 };
 
 // Token order of the 16 MMA rows of a K tile. Row r of the QK accumulator
@@ -104,6 +107,14 @@ __device__ __forceinline__ float warp_sum_over_gid(float v) {
   return v;
 }
 
+// kSlotScales: K/V dequantise with per-slot fp32 tables [NB][Hk][bs] (the
+// per-slot scale tables the pull request's "Scale tables" item describes)
+// instead of the per-tensor scalars. The producer copies each page's two
+// scale rows into the stage next to its K/V bytes; a token's K scale
+// multiplies its logit, its V scale multiplies its probability before the PV
+// product (relative to the V scale of the split's first slot, so P stays in
+// f16's normal range), and the sum l uses the unscaled probabilities.
+template <bool kSlotScales>
 __global__ void __launch_bounds__(kThreads, 3) pda_split_decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int split = blockIdx.x;
@@ -186,13 +197,19 @@ __global__ void __launch_bounds__(kThreads, 3) pda_split_decode_kernel(const Dec
         if (lane == 0) {
           const uint32_t sbase = ring_u32 + (uint32_t)stage * p.stage_bytes;
           const uint32_t bar = full0 + 8u * stage;
-          mbar_arrive_expect_tx(bar, 2u * page_bytes * (uint32_t)np);
+          const uint32_t row_bytes = (uint32_t)bs * 4u;
+          mbar_arrive_expect_tx(bar, (2u * page_bytes + (kSlotScales ? 2u * row_bytes : 0u)) * (uint32_t)np);
 #pragma unroll
           for (int t = 0; t < kMaxPagesPerStage; ++t) {
             if (t < np) {
               const size_t off = (size_t)blk[t] * block_stride + (size_t)kvh * head_stride;
               bulk_g2s(sbase + (uint32_t)t * page_bytes, p.k_cache + off, page_bytes, bar);
               bulk_g2s(sbase + (uint32_t)(PPS + t) * page_bytes, p.v_cache + off, page_bytes, bar);
+              if constexpr (kSlotScales) {
+                const size_t srow = ((size_t)blk[t] * p.num_kv_heads + kvh) * (size_t)bs;
+                bulk_g2s(sbase + p.scale_off + (uint32_t)t * row_bytes, p.k_scales + srow, row_bytes, bar);
+                bulk_g2s(sbase + p.scale_off + (uint32_t)(PPS + t) * row_bytes, p.v_scales + srow, row_bytes, bar);
+              }
             }
           }
         }
@@ -246,6 +263,9 @@ __global__ void __launch_bounds__(kThreads, 3) pda_split_decode_kernel(const Dec
 
   const float lsc = p.logit_scale_log2;
   const int tiles_per_page = bs / 16;
+  // Slot-scale variant: V scales enter P relative to vref (the split's first
+  // slot), and vref multiplies the result back at the end.
+  float vref = 1.f, vinv = 1.f;
 
   for (int fill = 0; fill < n_fills; ++fill) {
     const int stage = fill % NS;
@@ -262,6 +282,16 @@ __global__ void __launch_bounds__(kThreads, 3) pda_split_decode_kernel(const Dec
     const int np = min(PPS, pg_end - fill_first_page);
     const int n_tiles = np * tiles_per_page;
     const uint32_t sbase = ring_u32 + (uint32_t)stage * p.stage_bytes;
+    if constexpr (kSlotScales) {
+      if (fill == 0) {
+        const float v0 = *reinterpret_cast<const float*>(smem + stage * p.stage_bytes + p.scale_off +
+                                                         (uint32_t)PPS * (uint32_t)bs * 4u);
+        if (isfinite(v0) && v0 != 0.f) {
+          vref = v0;
+          vinv = 1.f / v0;
+        }
+      }
+    }
 
     for (int tile = warp; tile < n_tiles; tile += kConsumerWarps) {
       const int pg = tile / tiles_per_page;
@@ -289,10 +319,20 @@ __global__ void __launch_bounds__(kThreads, 3) pda_split_decode_kernel(const Dec
       // ---- online softmax (exp2 domain); tokens >= L are masked
       const bool vA = tok0 + tokA < L;
       const bool vB = tok0 + tokB < L;
-      const float s0 = vA ? sc[0] * lsc : -INFINITY;
-      const float s1 = vA ? sc[1] * lsc : -INFINITY;
-      const float s2 = vB ? sc[2] * lsc : -INFINITY;
-      const float s3 = vB ? sc[3] * lsc : -INFINITY;
+      float lscA = lsc, lscB = lsc, vsA = 1.f, vsB = 1.f;
+      if constexpr (kSlotScales) {
+        const uint8_t* ks = smem + stage * p.stage_bytes + p.scale_off + (pg * bs + sub * 16) * 4;
+        const uint8_t* vs = ks + PPS * bs * 4;
+        // Scales of slots past the length may hold anything (even NaN).
+        lscA *= vA ? reinterpret_cast<const float*>(ks)[tokA] : 0.f;
+        lscB *= vB ? reinterpret_cast<const float*>(ks)[tokB] : 0.f;
+        vsA = vA ? reinterpret_cast<const float*>(vs)[tokA] * vinv : 0.f;
+        vsB = vB ? reinterpret_cast<const float*>(vs)[tokB] * vinv : 0.f;
+      }
+      const float s0 = vA ? sc[0] * lscA : -INFINITY;
+      const float s1 = vA ? sc[1] * lscA : -INFINITY;
+      const float s2 = vB ? sc[2] * lscB : -INFINITY;
+      const float s3 = vB ? sc[3] * lscB : -INFINITY;
       const float mx0 = warp_max_over_gid(fmaxf(s0, s2));
       const float mx1 = warp_max_over_gid(fmaxf(s1, s3));
       const float mn0 = fmaxf(m0, mx0);
@@ -319,8 +359,16 @@ __global__ void __launch_bounds__(kThreads, 3) pda_split_decode_kernel(const Dec
       // P^T fragment: transpose (token rows x head cols) to (head rows x token
       // cols). Lane quads 2 and 3 hold their two token pairs in the other
       // order (row_token), so they swap the two halves of the B fragment.
-      const uint32_t t0 = movmatrix_trans(pack_f16x2(p0, p1));
-      const uint32_t t1 = movmatrix_trans(pack_f16x2(p2, p3));
+      uint32_t x0, x1;
+      if constexpr (kSlotScales) {
+        x0 = pack_f16x2(p0 * vsA, p1 * vsA);
+        x1 = pack_f16x2(p2 * vsB, p3 * vsB);
+      } else {
+        x0 = pack_f16x2(p0, p1);
+        x1 = pack_f16x2(p2, p3);
+      }
+      const uint32_t t0 = movmatrix_trans(x0);
+      const uint32_t t1 = movmatrix_trans(x1);
       const uint32_t pb0 = low_quad ? t0 : t1;
       const uint32_t pb1 = low_quad ? t1 : t0;
 
@@ -399,11 +447,12 @@ __global__ void __launch_bounds__(kThreads, 3) pda_split_decode_kernel(const Dec
     }
     const int h = kvh * g + hh;
     if (p.nsplit == 1) {
-      const float r = den > 0.f ? acc * (p.v_scale / den) : 0.f;
+      const float r = den > 0.f ? acc * ((kSlotScales ? vref : p.v_scale) / den) : 0.f;
       p.out[((size_t)s * H + h) * kHeadDim + d] = __float2bfloat16_rn(r);
     } else {
+      // Slot-scale partials carry their own V reference (the merge then uses 1).
       const size_t prow = ((size_t)s * H + h) * p.nsplit + split;
-      p.part_o[prow * kHeadDim + d] = acc;
+      p.part_o[prow * kHeadDim + d] = kSlotScales ? acc * vref : acc;
       if (d == 0) {
         p.part_ml[prow * 2 + 0] = M;
         p.part_ml[prow * 2 + 1] = den;

@@ -1,10 +1,16 @@
 """Shared helpers for the GPU parity tests: run the CUDA path, compare with the oracle.
 
 Tolerances (on the bf16 output, against the binary64 oracle):
-  * max |gpu - oracle| <= 8e-3 and mean |gpu - oracle| <= 2e-4 per batch;
+  * max |gpu - oracle| <= 8e-3 and mean |gpu - oracle| <= 2e-4 per batch,
+    literally, on the benchmark-shaped batches (the workloads the bar is
+    quoted on: long contexts, so |o| is an average of many values);
   * an element whose exact value has |o| >= 4 cannot be stored in bf16 within
     8e-3 (its rounding step is 2^-5 or more), so its bound is 8e-3 plus half
-    a bf16 step at |o|; such elements are counted and reported.
+    a bf16 step at |o|; such elements are counted and reported;
+  * on edge-case batches with a few tokens, |o| is O(1) and rounding the
+    exact value to bf16 alone costs about |o|/1000 on average, more than
+    2e-4; there the mean bar is 2e-4 on top of that unavoidable rounding
+    error (mean |bf16(oracle) - oracle|), which is computed and reported.
 """
 
 from __future__ import annotations
@@ -38,7 +44,7 @@ def bf16_half_step(x: np.ndarray) -> np.ndarray:
     return np.ldexp(1.0, (e - 8).astype(np.int64))
 
 
-def compare(got_bf16: torch.Tensor, ref: np.ndarray, label: str = "") -> dict:
+def compare(got_bf16: torch.Tensor, ref: np.ndarray, label: str = "", literal: bool = False) -> dict:
     got = got_bf16.detach().float().cpu().numpy().astype(np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
     assert np.isfinite(got).all(), "%s: non-finite output" % label
@@ -50,9 +56,13 @@ def compare(got_bf16: torch.Tensor, ref: np.ndarray, label: str = "") -> dict:
     # error beyond the unavoidable bf16 rounding of the exact value
     rounded = ref.astype(np.float32)
     rounded = torch.from_numpy(rounded).to(torch.bfloat16).float().numpy().astype(np.float64)
+    repr_err = float(np.abs(rounded - ref).mean()) if ref.size else 0.0
     stats = dict(max_abs=worst, mean_abs=mean, max_abs_vs_bf16_oracle=float(np.abs(got - rounded).max()),
+                 mean_abs_bf16_rounding_of_oracle=repr_err,
                  max_abs_out=float(np.abs(ref).max()) if ref.size else 0.0, n_bf16_limited=int(big.sum()))
     assert (err <= bound).all(), "%s: max abs err %g (bound %g) at %s" % (
         label, worst, MAX_ABS, np.unravel_index(np.argmax(err - bound), err.shape))
-    assert mean <= MEAN_ABS, "%s: mean abs err %g > %g" % (label, mean, MEAN_ABS)
+    mean_bar = MEAN_ABS if literal else MEAN_ABS + repr_err
+    assert mean <= mean_bar, "%s: mean abs err %g > %g (bf16 rounding of the exact value alone: %g)" % (
+        label, mean, mean_bar, repr_err)
     return stats

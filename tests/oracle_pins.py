@@ -278,6 +278,51 @@ def pin_zero_length(lib):
     assert np.max(np.abs(got - ref)) <= 1e-12
 
 
+# --------------------------------------------------- per-slot scale tables
+
+def _slot_scales_for(tables, lens, bs, NB, Hk, per_token_k, per_token_v, fill_k, fill_v):
+    """Scatter per-token scales [S, Hk, Lmax] into [NB, Hk, bs] tables."""
+    ks = np.full((NB, Hk, bs), fill_k, dtype=np.float32)
+    vs = np.full((NB, Hk, bs), fill_v, dtype=np.float32)
+    for s, L in enumerate(lens):
+        for t in range(L):
+            b = tables[s, t // bs]
+            ks[b, :, t % bs] = per_token_k[s, :, t]
+            vs[b, :, t % bs] = per_token_v[s, :, t]
+    return ks, vs
+
+
+def pin_slot_scales(lib):
+    rng = np.random.default_rng(31)
+    for (S, Hq, Hk, lens, bs) in ((3, 8, 2, [5, 40, 33], 16), (2, 16, 2, [70, 64], 64)):
+        qbits, Kc, Vc = dense_case(S, Hq, Hk, lens, seed=91)
+        kc, vc, tb, ln = scatter_pages(Kc, Vc, lens, bs, seed=12, extra_cols=1)
+        NB = kc.shape[0]
+        Lmax = max(lens)
+        pk = (rng.random((S, Hk, Lmax)) * 0.09 + 0.01).astype(np.float32)
+        pv = (rng.random((S, Hk, Lmax)) * 0.09 + 0.01).astype(np.float32)
+        ks, vs = _slot_scales_for(tb, lens, bs, NB, Hk, pk, pv, 123.0, -7.0)   # unused slots: junk
+        got = oracle.decode(qbits, kc, vc, tb, ln, scale=0.09, k_scales=ks, v_scales=vs, lib=lib)
+        # dense torch reference with per-token scales
+        q = torch.from_numpy(qbits.view(np.int16)).view(torch.bfloat16).to(torch.float64)
+        Kd = torch.from_numpy(torch_e4m3(Kc)) * torch.from_numpy(pk.astype(np.float64))[..., None]
+        Vd = torch.from_numpy(torch_e4m3(Vc)) * torch.from_numpy(pv.astype(np.float64))[..., None]
+        g = Hq // Hk
+        for s, L in enumerate(lens):
+            Kh = Kd[s, :, :L].repeat_interleave(g, dim=0)
+            Vh = Vd[s, :, :L].repeat_interleave(g, dim=0)
+            p = torch.softmax(torch.einsum("hld,hd->hl", Kh, q[s]) * 0.09, dim=-1)
+            ref = torch.einsum("hl,hld->hd", p, Vh).numpy()
+            assert np.max(np.abs(got[s] - ref)) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
+        # tables filled with one value equal the per-tensor call bitwise
+        kf = np.full((NB, Hk, bs), 0.05, dtype=np.float32)
+        vf = np.full((NB, Hk, bs), 0.07, dtype=np.float32)
+        a = oracle.decode(qbits, kc, vc, tb, ln, scale=0.09, k_scales=kf, v_scales=vf, lib=lib)
+        b = oracle.decode(qbits, kc, vc, tb, ln, scale=0.09, k_scale=float(np.float32(0.05)),
+                          v_scale=float(np.float32(0.07)), lib=lib)
+        assert np.array_equal(a, b)
+
+
 # ------------------------------------------------------- KV-cache write pins
 
 def torch_quantise(bits_u16: np.ndarray, scale: float) -> np.ndarray:
@@ -375,4 +420,4 @@ def pin_quantise_in_binary32(lib):
 
 ALL_PINS = [pin_e4m3_table, pin_bf16, pin_dense, pin_large_logits, pin_permutation_invariance,
             pin_constant_v, pin_single_token, pin_zero_k, pin_tail_poison, pin_gqa_is_repeated_mha,
-            pin_zero_length, pin_e4m3_encode, pin_reshape_and_cache, pin_quantise_in_binary32]
+            pin_zero_length, pin_slot_scales, pin_e4m3_encode, pin_reshape_and_cache, pin_quantise_in_binary32]

@@ -56,10 +56,10 @@ SM, OCC = 152, 3
 
 @pytest.mark.parametrize("S,Hk,MB,bs,expect", [
     (16, 8, 64, 16, 4),       # 128 units, 1024-token contexts: capped by the 256-token minimum split
-    (64, 8, 64, 16, 2),       # 512 units < 2 waves of 456 CTAs
-    (256, 8, 256, 16, 1),     # 2048 units fill the GPU
+    (64, 8, 64, 16, 4),       # 512 units: 4 waves of 456 CTAs need 4 splits (cap 4)
+    (256, 8, 256, 16, 1),     # 2048 units already make 4.5 waves
     (256, 8, 250, 16, 1),
-    (128, 8, 128, 64, 1),     # 1024 units, 64-token blocks
+    (128, 8, 128, 64, 2),     # 1024 units, 64-token blocks: 2.2 waves -> 2 splits
     (1, 8, 256, 16, 16),      # a single long sequence splits to the cap
     (1, 1, 2, 16, 1),         # too short to split
 ])

@@ -36,7 +36,7 @@ def test_config_full_parity(name):
     batch = workloads.make_batch(workloads.CONFIGS[name], device=DEV)
     out = U.run_cuda(batch)
     torch.cuda.synchronize()
-    stats = U.compare(out, U.run_oracle(batch), name)
+    stats = U.compare(out, U.run_oracle(batch), name, literal=True)
     print(name, stats)
 
 
@@ -57,7 +57,7 @@ def test_config_full_size_sampled(name, n_sample):
     ids |= {int(np.argmin(lens)), int(np.argmax(lens)), 0, cfg.num_seqs - 1}
     ids = sorted(ids)
     ref = U.run_oracle(batch, seq_ids=ids)
-    stats = U.compare(out[ids], ref, name)
+    stats = U.compare(out[ids], ref, name, literal=True)
     print(name, "splits", pda.plan_splits(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads,
                                           cfg.max_num_blocks_per_seq, cfg.block_size), stats)
 
@@ -254,3 +254,46 @@ def test_profile_events():
         assert a.elapsed_time(b) > 0
     finally:
         pda.set_profile_events(None, None)
+
+
+# ------------------------------------------------------- per-slot scales
+
+@pytest.mark.parametrize("bs,splits", [(16, 0), (16, 3), (64, 0), (64, 2)])
+def test_slot_scales_parity(bs, splits):
+    import oracle
+    lens = [1, 37, 300, 1024, 16]
+    batch = workloads.make_custom(5, 32, 8, lens, block_size=bs, pool_factor=1.3, seed=21 + bs, device=DEV)
+    NB, Hk = batch.num_blocks, 8
+    g = torch.Generator(device=DEV).manual_seed(5)
+    ks = (torch.rand(NB, Hk, bs, generator=g, device=DEV) * 0.09 + 0.01).float()
+    vs = (torch.rand(NB, Hk, bs, generator=g, device=DEV) * 0.09 + 0.01).float()
+    # slots past each length hold junk scales, which must never be used
+    for s, L in enumerate(lens):
+        P = (L + bs - 1) // bs
+        b = int(batch.block_tables[s, P - 1])
+        n = L - (P - 1) * bs
+        ks[b, :, n:] = float("nan")
+        vs[b, :, n:] = float("nan")
+    pda.set_split_override(splits)
+    try:
+        out = pda.decode_slot_scales(batch.q, batch.k_cache, batch.v_cache, ks, vs, batch.block_tables,
+                                     batch.seq_lens, batch.cfg.scale)
+        torch.cuda.synchronize()
+    finally:
+        pda.set_split_override(0)
+    raw = batch.raw()
+    ref = oracle.decode(**raw, scale=batch.cfg.scale, k_scales=ks.cpu().numpy(), v_scales=vs.cpu().numpy())
+    U.compare(out, ref, "slot scales bs=%d" % bs)
+
+
+def test_slot_scales_constant_table_matches_per_tensor():
+    batch = workloads.make_custom(4, 40, 8, [100, 1000, 7, 513], seed=33, device=DEV)
+    NB, Hk, bs = batch.num_blocks, 8, 16
+    ks = torch.full((NB, Hk, bs), batch.cfg.k_scale, device=DEV)
+    vs = torch.full((NB, Hk, bs), batch.cfg.v_scale, device=DEV)
+    a = pda.decode_slot_scales(batch.q, batch.k_cache, batch.v_cache, ks, vs, batch.block_tables, batch.seq_lens,
+                               batch.cfg.scale)
+    b = U.run_cuda(batch)
+    torch.cuda.synchronize()
+    assert (a.float() - b.float()).abs().max().item() <= 4e-3
+    U.compare(a, U.run_oracle(batch), "constant tables")

@@ -16,8 +16,8 @@ from tests import oracle_pins as P
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "pda_oracle.cpp")
 
 MUTANTS = {
-    "dropped_k_scale": ("acc += qd[d] * (e4m3[code] * k_scale);", "acc += qd[d] * e4m3[code];"),
-    "dropped_v_scale": ("(e4m3[vpage[static_cast<long long>(d) * bs + slot]] * v_scale)",
+    "dropped_k_scale": ("acc += qd[d] * (e4m3[code] * ks);", "acc += qd[d] * e4m3[code];"),
+    "dropped_v_scale": ("(e4m3[vpage[static_cast<long long>(d) * bs + slot]] * vs)",
                         "e4m3[vpage[static_cast<long long>(d) * bs + slot]]"),
     "dropped_softmax_scale": ("z[t] = scale * acc;", "z[t] = acc;"),
     "wrong_sign": ("z[t] = scale * acc;", "z[t] = -scale * acc;"),
@@ -43,6 +43,8 @@ MUTANTS = {
     "cache_write_k_token_major": ("k_cache[page + ((d / 16) * bs + o) * 16 + (d % 16)]",
                                   "k_cache[page + (o * (D / 16) + d / 16) * 16 + (d % 16)]"),
     "cache_write_v_token_major": ("v_cache[page + d * bs + o]", "v_cache[page + o * D + d]"),
+    "slot_scale_wrong_head": ("k_scales[(b * num_kv_heads + kv) * bs + slot]", "k_scales[(b * num_kv_heads + 0) * bs + slot]"),
+    "slot_scale_wrong_slot": ("v_scales[(b * num_kv_heads + kv) * bs + slot]", "v_scales[(b * num_kv_heads + kv) * bs]"),
 }
 
 
