@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--config", default=workloads.HEADLINE, choices=sorted(workloads.CONFIGS))
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=["decode", "cache_write"], default="decode",
+                    help="cache_write: time pda_reshape_and_cache on --tokens new tokens of the config's kv heads")
+    ap.add_argument("--tokens", type=int, default=65536)
     ap.add_argument("--profile", type=int, default=0, metavar="N",
                     help="profiling mode: N plain pda_decode calls on the config, no timing, no JSON metric")
     return ap.parse_args()
@@ -486,11 +489,66 @@ def run_profile(args):
         raise SystemExit(1)
 
 
+def run_cache_write(args):
+    """Time the KV-cache write (quantise + scatter) on one GPU; one JSON line."""
+    import paged_kv_decode_pda_gb300 as pda
+    from paged_kv_decode_pda_gb300 import build
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    cfg = workloads.CONFIGS[args.config]
+    T, Hk, bs = args.tokens, cfg.num_kv_heads, cfg.block_size
+    g = torch.Generator(device=dev).manual_seed(cfg.seed)
+    NB = max(1, (T + bs - 1) // bs) * 2
+    key = torch.randn(T, Hk, 128, generator=g, device=dev).to(torch.bfloat16)
+    val = torch.randn(T, Hk, 128, generator=g, device=dev).to(torch.bfloat16)
+    slots = torch.randperm(NB * bs, generator=g, device=dev)[:T].to(torch.int64)
+    kc = torch.zeros(NB, Hk, 8, bs, 16, dtype=torch.uint8, device=dev)
+    vc = torch.zeros(NB, Hk, 128, bs, dtype=torch.uint8, device=dev)
+    nbytes = T * Hk * 128 * (2 + 2 + 1 + 1) + T * 8
+    stream = torch.cuda.Stream(device=dev)
+
+    def call():
+        pda.reshape_and_cache(key, val, kc, vc, slots, cfg.k_scale, cfg.v_scale, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            call()
+    stream.synchronize()
+    K = args.steps
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        for _ in range(min(K, 100)):
+            call()
+    reps = max(1, K // min(K, 100))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            gr.replay()
+        e1.record(stream)
+    stream.synchronize()
+    n_calls = reps * min(K, 100)
+    us = e0.elapsed_time(e1) * 1e3 / n_calls
+    assert pda.query_device_status(stream) == 0
+    peak, kind = peaks()
+    print(json.dumps({"op": "cache_write", "metric": "us/call and GB/s of pda_reshape_and_cache", "value": nbytes / us / 1e3,
+                      "unit": "GB/s", "us_per_call": us, "calls": n_calls, "tokens": T, "num_kv_heads": Hk,
+                      "block_size": bs, "bytes_per_call": nbytes,
+                      "roofline": {"bound": "hbm", "achieved": nbytes / us / 1e3, "peak": peak, "unit": "GB/s",
+                                   "frac": nbytes / us / 1e3 / peak, "peak_source": kind}}), flush=True)
+
+
 def main():
     args = parse()
     ws, rank, local = dist_env()
     if args.profile:
         run_profile(args)
+        return
+    if args.op == "cache_write":
+        if rank == 0:
+            run_cache_write(args)
         return
     if args.impl == "reference":
         run_reference(args, ws, rank, local)
