@@ -60,8 +60,10 @@ def compare(got_bf16: torch.Tensor, ref: np.ndarray, label: str = "", literal: b
     stats = dict(max_abs=worst, mean_abs=mean, max_abs_vs_bf16_oracle=float(np.abs(got - rounded).max()),
                  mean_abs_bf16_rounding_of_oracle=repr_err,
                  max_abs_out=float(np.abs(ref).max()) if ref.size else 0.0, n_bf16_limited=int(big.sum()))
-    assert (err <= bound).all(), "%s: max abs err %g (bound %g) at %s" % (
-        label, worst, MAX_ABS, np.unravel_index(np.argmax(err - bound), err.shape))
+    if not (err <= bound).all():
+        at = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError("%s: max abs err %g (bound %g) at %s: gpu %r oracle %r" % (
+            label, worst, float(bound[at]), at, float(got[at]), float(ref[at])))
     mean_bar = MEAN_ABS if literal else MEAN_ABS + repr_err
     assert mean <= mean_bar, "%s: mean abs err %g > %g (bf16 rounding of the exact value alone: %g)" % (
         label, mean, mean_bar, repr_err)

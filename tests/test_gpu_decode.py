@@ -264,9 +264,12 @@ def test_slot_scales_parity(bs, splits):
     lens = [1, 37, 300, 1024, 16]
     batch = workloads.make_custom(5, 32, 8, lens, block_size=bs, pool_factor=1.3, seed=21 + bs, device=DEV)
     NB, Hk = batch.num_blocks, 8
+    # Per-slot scales within +-20 % of the scale the codes were made with (the
+    # spread per-token quantisation of N(0,1) data gives), so values keep the
+    # configs' range; P is carried in f16, so the error scales with |v|.
     g = torch.Generator(device=DEV).manual_seed(5)
-    ks = (torch.rand(NB, Hk, bs, generator=g, device=DEV) * 0.09 + 0.01).float()
-    vs = (torch.rand(NB, Hk, bs, generator=g, device=DEV) * 0.09 + 0.01).float()
+    ks = (torch.rand(NB, Hk, bs, generator=g, device=DEV) * 0.02 + 0.04).float()
+    vs = (torch.rand(NB, Hk, bs, generator=g, device=DEV) * 0.02 + 0.04).float()
     # slots past each length hold junk scales, which must never be used
     for s, L in enumerate(lens):
         P = (L + bs - 1) // bs
