@@ -51,7 +51,8 @@ typedef enum pda_status {
   PDA_ERR_UNSUPPORTED = 2,     /* valid but outside the supported set (see pda_decode) */
   PDA_ERR_WORKSPACE = 3,       /* workspace must grow while the stream is being captured */
   PDA_ERR_CUDA = 4,            /* a CUDA runtime call or kernel launch failed */
-  PDA_ERR_DEVICE_TIMEOUT = 5   /* a kernel reported a device-side error (pda_query_device_status) */
+  PDA_ERR_DEVICE_TIMEOUT = 5,  /* a kernel reported a device-side error (pda_query_device_status) */
+  PDA_ERR_NOALLOC_CAPACITY = 6 /* pda_decode_noalloc: the call needs more scratch than its static buffer */
 } pda_status;
 
 /*
@@ -159,6 +160,43 @@ pda_status pda_reshape_and_cache(const void* key, const void* value, void* k_cac
                                  const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_size,
                                  int block_size, long long num_blocks, float k_scale, float v_scale,
                                  cudaStream_t stream);
+
+/*
+ * pda_decode_noalloc -- pda_decode for callers that cannot allocate device
+ * memory. No counterpart in the paper: this is an interface convenience of
+ * this library.
+ *
+ * pda_decode keeps its split partials in a workspace it grows with
+ * cudaMallocAsync. Some callers cannot allow that: a serving process that
+ * reserved all device memory for its own pool at start-up, code that must
+ * not add to the device's allocation (for example under a strict memory
+ * budget or an allocator that must see every byte), or a caller whose first
+ * use of a shape would otherwise trigger an allocation at a bad moment. This
+ * entry point computes exactly what pda_decode computes, with the same
+ * kernels, split count and results, but its partials live in a fixed 16 MiB
+ * array compiled into the library: every GPU that loads the library holds
+ * that array until the process exits. It calls no cudaMalloc, cudaFree or
+ * other allocating routine.
+ *
+ * Arguments, layouts, supported set and ordering are pda_decode's. Limit:
+ * num_seqs * num_heads * splits * 520 bytes must fit in 16 MiB (splits is
+ * the split count pda_plan_splits reports; a call that needs one split uses
+ * no scratch at all); larger calls return PDA_ERR_NOALLOC_CAPACITY before
+ * launching anything. The first call on each device also looks up the
+ * array's device address and the device's properties (no allocation); make
+ * that first call outside any stream capture. All calls on a device share
+ * the one array: nothing in it needs to start at zero (each call writes the
+ * partials it reads), but two calls whose kernels can run at the same time
+ * on the GPU (on two streams with no ordering between them, from two host
+ * threads, or from two libraries' copies in one process sharing a stream
+ * order they do not control) race on it and give wrong results; order them
+ * on one stream or with events. Profiling events
+ * (pda_set_profile_events) are not recorded by this entry point.
+ */
+pda_status pda_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, const int32_t* seq_lens, int num_seqs, int num_heads,
+                              int num_kv_heads, int head_size, int block_size, int max_num_blocks_per_seq,
+                              float scale, float k_scale, float v_scale, cudaStream_t stream);
 
 /* Static text for a status code; never NULL. */
 const char* pda_status_string(int status);

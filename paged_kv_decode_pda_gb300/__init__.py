@@ -12,12 +12,14 @@ from ._binding import (  # noqa: F401
     PDA_ERR_CUDA,
     PDA_ERR_DEVICE_TIMEOUT,
     PDA_ERR_INVALID_ARG,
+    PDA_ERR_NOALLOC_CAPACITY,
     PDA_ERR_UNSUPPORTED,
     PDA_ERR_WORKSPACE,
     PDA_OK,
     PdaError,
     choose_splits,
     decode,
+    decode_noalloc,
     decode_slot_scales,
     decode_raw,
     load,

@@ -23,6 +23,7 @@ PDA_ERR_UNSUPPORTED = 2
 PDA_ERR_WORKSPACE = 3
 PDA_ERR_CUDA = 4
 PDA_ERR_DEVICE_TIMEOUT = 5
+PDA_ERR_NOALLOC_CAPACITY = 6
 
 # Functions (name -> (restype, argtypes)) the header declares.
 _P, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
@@ -39,6 +40,7 @@ SIGNATURES = {
     "pda_test_bounded_wait": (_I, [_I, _P]),
     "pda_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_longlong, _F, _F, _P]),
     "pda_decode_slot_scales": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "pda_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _F, _P]),
 }
 
 _lock = threading.RLock()
@@ -78,7 +80,8 @@ def status_string(status: int) -> str:
 
 _STATUS_TEXT = {PDA_OK: "ok", PDA_ERR_INVALID_ARG: "invalid argument", PDA_ERR_UNSUPPORTED: "unsupported configuration",
                 PDA_ERR_WORKSPACE: "workspace must grow during stream capture", PDA_ERR_CUDA: "CUDA runtime error",
-                PDA_ERR_DEVICE_TIMEOUT: "a kernel gave up on a bounded wait"}
+                PDA_ERR_DEVICE_TIMEOUT: "a kernel gave up on a bounded wait",
+                PDA_ERR_NOALLOC_CAPACITY: "the call needs more split scratch than the static buffer holds"}
 
 
 def _check(status: int, what: str):
@@ -160,6 +163,29 @@ def decode_slot_scales(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Te
                                     seq_lens.data_ptr(), S, H, Hk, D, bs, int(block_tables.shape[1]), float(scale),
                                     _stream_ptr(stream))
     _check(st, "pda_decode_slot_scales")
+    return out
+
+
+def decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                   seq_lens: torch.Tensor, scale: float, k_scale: float, v_scale: float, *, out: torch.Tensor,
+                   stream=None) -> torch.Tensor:
+    """``pda_decode_noalloc``: ``decode`` without any device allocation.
+
+    The output buffer must be given (nothing is allocated here either); the
+    library keeps split partials in its fixed 16 MiB device array.
+    """
+    lib = load()
+    _check_decode_args(q, k_cache, v_cache, block_tables, seq_lens)
+    if out is None:
+        raise PdaError(PDA_ERR_INVALID_ARG, "decode_noalloc: out must be given")
+    out = _out_like(q, out)
+    S, H, D = q.shape
+    NB, Hk, _, bs, _ = k_cache.shape
+    st = lib.pda_decode_noalloc(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                block_tables.data_ptr(), seq_lens.data_ptr(), S, H, Hk, D, bs,
+                                int(block_tables.shape[1]), float(scale), float(k_scale), float(v_scale),
+                                _stream_ptr(stream))
+    _check(st, "pda_decode_noalloc")
     return out
 
 

@@ -264,6 +264,8 @@ const char* pda_status_string(int status) {
     case PDA_ERR_WORKSPACE: return "workspace must grow during stream capture (call pda_reserve first)";
     case PDA_ERR_CUDA: return "CUDA runtime error";
     case PDA_ERR_DEVICE_TIMEOUT: return "a kernel gave up on a bounded wait";
+    case PDA_ERR_NOALLOC_CAPACITY:
+      return "the call needs more split scratch than pda_decode_noalloc's static buffer holds";
     default: return "unknown status";
   }
 }
@@ -417,3 +419,128 @@ pda_status pda_decode_slot_scales(void* out, const void* q, const void* k_cache,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// pda_decode_noalloc: the split-KV decode path with its split partials in a
+// fixed device array that is part of the loaded library, for callers that
+// must not allocate device memory (see include/pda.h). Nothing below touches
+// the workspace, the host containers or any allocator.
+
+namespace {
+
+// Room for num_seqs * num_heads * splits <= 32,264 partial rows of 520 bytes.
+constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;  // 16 MiB per device
+
+// The partials' storage. Host code may not use this name as an address (on
+// the host it is only a stand-in); each device's address comes from
+// cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+struct NoAllocDevice {
+  bool ready;
+  void* scratch;      // device address of g_noalloc_scratch on this device
+  int sm_count;
+  int occ[9];         // resident decode CTAs per SM, by block_size / 16
+};
+std::mutex g_noalloc_mu;
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+
+// One-time set-up for `dev` (which must be current): the scratch address,
+// the SM count and the decode kernel's shared-memory opt-in. No allocation.
+pda_status noalloc_setup(int dev, int bs, NoAllocDevice* out) {
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return PDA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  NoAllocDevice& d = g_noalloc_dev[dev];
+  if (!d.ready) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return PDA_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return PDA_ERR_CUDA;
+    size_t mx = 0;
+    for (int b = 16; b <= 128; b += 16) {
+      const size_t sb = ring_shape(b).smem_bytes;
+      mx = sb > mx ? sb : mx;
+    }
+    if (cudaFuncSetAttribute(pda::pda_split_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)mx) != cudaSuccess)
+      return PDA_ERR_CUDA;
+    d.scratch = ptr;
+    d.sm_count = sms;
+    d.ready = true;
+  }
+  int& occ = d.occ[bs / 16];
+  if (occ == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pda::pda_split_decode_kernel<false>, pda::kThreads,
+                                                      ring_shape(bs).smem_bytes) != cudaSuccess)
+      return PDA_ERR_CUDA;
+    occ = n > 0 ? n : 1;
+  }
+  *out = d;
+  return PDA_OK;
+}
+
+}  // namespace
+
+extern "C" pda_status pda_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                                         int num_heads, int num_kv_heads, int head_size, int block_size,
+                                         int max_num_blocks_per_seq, float scale, float k_scale, float v_scale,
+                                         cudaStream_t stream) {
+  pda_status st = validate(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_heads, num_kv_heads,
+                           head_size, block_size, max_num_blocks_per_seq, scale, k_scale, v_scale);
+  if (st != PDA_OK || num_seqs == 0) return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PDA_ERR_CUDA;
+  NoAllocDevice d;
+  st = noalloc_setup(dev, block_size, &d);
+  if (st != PDA_OK) return st;
+  const int MB = max_num_blocks_per_seq > 0 ? max_num_blocks_per_seq : 1;
+  const int nsplit = resolve_splits(num_seqs, num_kv_heads, MB, block_size, d.sm_count, d.occ[block_size / 16]);
+  if (workspace_bytes(num_seqs, num_heads, nsplit) > kNoAllocScratchBytes) return PDA_ERR_NOALLOC_CAPACITY;
+
+  const RingShape rs = ring_shape(block_size);
+  float* scratch = static_cast<float*>(d.scratch);
+  pda::DecodeParams p;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k_cache = static_cast<const uint8_t*>(k_cache);
+  p.v_cache = static_cast<const uint8_t*>(v_cache);
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.part_o = scratch;
+  p.part_ml = scratch + (size_t)num_seqs * num_heads * nsplit * kHeadDim;
+  p.num_heads = num_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.gqa = num_heads / num_kv_heads;
+  p.block_size = block_size;
+  p.max_blocks = max_num_blocks_per_seq;
+  p.nsplit = nsplit;
+  p.pages_per_stage = rs.pages_per_stage;
+  p.num_stages = rs.num_stages;
+  p.stage_bytes = rs.stage_bytes;
+  p.scale_off = rs.scale_off;
+  p.k_scales = nullptr;
+  p.v_scales = nullptr;
+  p.logit_scale_log2 = (float)((double)scale * (double)k_scale * 1.4426950408889634);
+  p.v_scale = v_scale;
+  dim3 grid((unsigned)nsplit, (unsigned)num_kv_heads, (unsigned)num_seqs);
+  pda::pda_split_decode_kernel<false><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
+  if (nsplit > 1) {
+    pda::MergeParams mp;
+    mp.out = p.out;
+    mp.part_o = p.part_o;
+    mp.part_ml = p.part_ml;
+    mp.seq_lens = seq_lens;
+    mp.num_heads = num_heads;
+    mp.block_size = block_size;
+    mp.max_blocks = max_num_blocks_per_seq;
+    mp.nsplit = nsplit;
+    mp.v_scale = v_scale;
+    pda::pda_merge_kernel<<<dim3((unsigned)num_heads, (unsigned)num_seqs), kHeadDim, 0, stream>>>(mp);
+    if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
+  }
+  return PDA_OK;
+}

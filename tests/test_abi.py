@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(6):
+    for code in range(7):
         s = lib.pda_status_string(code)
         assert s and s != b"unknown status"
     assert lib.pda_status_string(99) == b"unknown status"
