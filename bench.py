@@ -96,10 +96,11 @@ def peaks():
 
 
 def kernel_source_sha() -> str:
+    """Hash of the device sources the decode kernel is compiled from (host code excluded)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_pda_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
+        if name.endswith(".cuh"):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
