@@ -207,10 +207,12 @@ const char* pda_status_string(int status);
  * Returns how many KV splits each (sequence, kv head) work unit is cut into
  * for a batch of num_seqs * num_kv_heads units with at most
  * max_num_blocks_per_seq pages of block_size tokens, on a device with
- * sm_count SMs that hold ctas_per_sm decode CTAs each. The cut mirrors the
- * pull request's dispatch rule ("Claims": work units compared with twice the
- * compute-unit count): split until the CTAs make at least four waves over
- * the resident slots, never below 256 tokens per split. Result in
+ * sm_count SMs that hold ctas_per_sm decode CTAs each. Like the pull
+ * request's dispatch rule ("Claims": work units compared with the
+ * compute-unit count), it compares work units with the resident CTA slots:
+ * a unit is split when its K/V bytes (at max_num_blocks_per_seq pages)
+ * exceed 1 MiB, or when the units fill less than one wave of slots (then up
+ * to one wave), never below 256 tokens per split. Result in
  * [1, max(1, max_num_blocks_per_seq)]. Invalid arguments return 1.
  */
 int pda_choose_splits(int num_seqs, int num_kv_heads, int max_num_blocks_per_seq, int block_size,

@@ -277,14 +277,20 @@ int pda_choose_splits(int num_seqs, int num_kv_heads, int max_num_blocks_per_seq
     return 1;
   const long long units = (long long)num_seqs * num_kv_heads;
   const long long slots = (long long)sm_count * ctas_per_sm;
-  // Split until the CTAs make at least kMinWaves waves over the resident
-  // slots (fewer, longer CTAs leave the GPU under-filled while the last wave
-  // drains), but keep at least kMinSplitTokens tokens of streaming per split
-  // so the page ring pays for its fill and the partials stay small next to
-  // the K/V bytes.
-  const long long kMinWaves = 4;
+  // Two reasons to split a (sequence, kv head) unit, measured on GB300:
+  //  * a unit's K/V bytes exceed kMaxSplitBytes: a few long CTAs leave most
+  //    resident slots idle while the last wave drains;
+  //  * the units fill less than one wave of resident CTAs: split up to one
+  //    wave (more splits only add partial traffic and the merge launch).
+  // Never below kMinSplitTokens tokens per split.
+  const long long kMaxSplitBytes = 1LL << 20;
   const long long kMinSplitTokens = 256;
-  long long want = (kMinWaves * slots + units - 1) / units;
+  const long long unit_bytes = (long long)max_num_blocks_per_seq * block_size * 128 * 2;
+  long long want = (unit_bytes + kMaxSplitBytes - 1) / kMaxSplitBytes;
+  if (units < slots) {
+    const long long fill = slots / units;
+    if (fill > want) want = fill;
+  }
   const long long min_pages = (kMinSplitTokens + block_size - 1) / block_size;
   long long cap = max_num_blocks_per_seq / min_pages;
   if (cap < 1) cap = 1;

@@ -55,13 +55,14 @@ SM, OCC = 152, 3
 
 
 @pytest.mark.parametrize("S,Hk,MB,bs,expect", [
-    (16, 8, 64, 16, 4),       # 128 units, 1024-token contexts: capped by the 256-token minimum split
-    (64, 8, 64, 16, 4),       # 512 units: 4 waves of 456 CTAs need 4 splits (cap 4)
-    (256, 8, 256, 16, 1),     # 2048 units already make 4.5 waves
+    (16, 8, 64, 16, 3),       # 128 units < 456 slots: split to fill one wave (3 x 128 <= 456)
+    (64, 8, 64, 16, 1),       # 512 units already fill a wave; 256 KiB per unit
+    (256, 8, 256, 16, 1),     # 1 MiB per unit, 2048 units
     (256, 8, 250, 16, 1),
-    (128, 8, 128, 64, 2),     # 1024 units, 64-token blocks: 2.2 waves -> 2 splits
-    (1, 8, 256, 16, 16),      # a single long sequence splits to the cap
+    (128, 8, 128, 64, 2),     # 64-token blocks: 2 MiB per unit -> two 1 MiB splits
+    (1, 8, 256, 16, 16),      # a single long sequence splits to the 256-token cap
     (1, 1, 2, 16, 1),         # too short to split
+    (4, 8, 2048, 16, 14),     # 32 units of 8 MiB: one wave needs 14 splits (cap 128)
 ])
 def test_choose_splits_table(lib, S, Hk, MB, bs, expect):
     assert lib.pda_choose_splits(S, Hk, MB, bs, SM, OCC) == expect
@@ -80,6 +81,8 @@ def test_choose_splits_bounds_and_monotonicity(lib):
                 if prev is not None:
                     assert n <= prev, "more sequences must never mean more splits"
                 prev = n
+                if S * 8 >= SM * OCC and MB * bs * 256 <= (1 << 20):
+                    assert n == 1, "a full wave of small units needs no split"
 
 
 def test_choose_splits_invalid_inputs_return_one(lib):
