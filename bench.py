@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--config", default=workloads.HEADLINE, choices=sorted(workloads.CONFIGS))
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--variant", choices=["plain", "slot_scales", "ex"], default="plain",
+                    help="decode entry point: pda_decode, pda_decode_slot_scales (per-slot tables), or "
+                         "pda_decode_ex with per-head sinks and e4m3 output")
     ap.add_argument("--op", choices=["decode", "cache_write"], default="decode",
                     help="cache_write: time pda_reshape_and_cache on --tokens new tokens of the config's kv heads")
     ap.add_argument("--tokens", type=int, default=65536)
@@ -241,10 +244,29 @@ def run_ours(args, ws, rank, local):
     pda.reserve(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq, cfg.block_size,
                 stream=stream)
 
+    if args.variant == "slot_scales":
+        # per-slot tables filled with the per-tensor scales (the pages' use)
+        ks_t = torch.full((batch.num_blocks, cfg.num_kv_heads, cfg.block_size), cfg.k_scale, device=dev)
+        vs_t = torch.full_like(ks_t, cfg.v_scale)
+        pages_used = batch.pages_used()
+        bytes_per_call += 2 * pages_used * cfg.block_size * 4 * cfg.num_kv_heads
+    elif args.variant == "ex":
+        sinks = torch.randn(cfg.num_heads, generator=torch.Generator().manual_seed(3)).float().to(dev)
+        out = torch.empty(batch.q.shape, dtype=torch.float8_e4m3fn, device=dev)
+        bytes_per_call -= out.numel()   # 1-byte instead of 2-byte output
+        bytes_per_call += cfg.num_heads * 4
+
     def call(i):
         kc, vc = caches[i % replicas]
-        pda.decode(batch.q, kc, vc, batch.block_tables, batch.seq_lens, cfg.scale, cfg.k_scale, cfg.v_scale,
-                   out=out, stream=stream)
+        if args.variant == "slot_scales":
+            pda.decode_slot_scales(batch.q, kc, vc, ks_t, vs_t, batch.block_tables, batch.seq_lens, cfg.scale,
+                                   out=out, stream=stream)
+        elif args.variant == "ex":
+            pda.decode_ex(batch.q, kc, vc, batch.block_tables, batch.seq_lens, cfg.scale, cfg.k_scale, cfg.v_scale,
+                          sinks=sinks, output_scale=0.0075, out=out, stream=stream)
+        else:
+            pda.decode(batch.q, kc, vc, batch.block_tables, batch.seq_lens, cfg.scale, cfg.k_scale, cfg.v_scale,
+                       out=out, stream=stream)
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -323,7 +345,7 @@ def run_ours(args, ws, rank, local):
 
     # ---- end to end through the public API from pinned host buffers
     e2e = None
-    if args.e2e_steps > 0:
+    if args.e2e_steps > 0 and args.variant == "plain":
         host = {k: v.detach().cpu().pin_memory() for k, v in
                 dict(q=batch.q, k=batch.k_cache, v=batch.v_cache, t=batch.block_tables, l=batch.seq_lens).items()}
         dev_bufs = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
@@ -365,7 +387,7 @@ def run_ours(args, ws, rank, local):
     peak, peak_kind = peaks()
     kern_mean_ms = statistics.fmean(kern_ms)
     achieved = bytes_per_call / (kern_mean_ms * 1e-3) / 1e9
-    traffic = ncu_traffic(cfg.name)
+    traffic = ncu_traffic(cfg.name) if args.variant == "plain" else None
     us_per_call = elapsed_ms * 1e3 / K
 
     cpu = None
@@ -389,7 +411,7 @@ def run_ours(args, ws, rank, local):
         "vs_baseline_note": "pages' asm kernel on AMD MI355X, 362.53 us/call for this workload (context only)",
         "dtype": "e4m3 KV / bf16 q -> f16 MMA, fp32 accumulate, bf16 out",
         "data": "synthetic (seeded N(0,1) q; K/V N(0,1) quantised to e4m3 with scale 0.05; shuffled block tables)",
-        "config": {"workload": cfg.name, "num_seqs": cfg.num_seqs, "num_heads": cfg.num_heads,
+        "config": {"workload": cfg.name, "variant": args.variant, "num_seqs": cfg.num_seqs, "num_heads": cfg.num_heads,
                    "num_kv_heads": cfg.num_kv_heads, "head_size": cfg.head_size, "block_size": cfg.block_size,
                    "ctx": cfg.ctx if cfg.ctx else list(cfg.ctx_range), "kv_splits": nsplit,
                    "bytes_per_call": bytes_per_call,

@@ -106,6 +106,42 @@ pda_status pda_decode(void* out, const void* q, const void* k_cache, const void*
                       int max_num_blocks_per_seq, float scale, float k_scale, float v_scale,
                       cudaStream_t stream);
 
+/* Output element type of pda_decode_ex. */
+typedef enum pda_out_dtype {
+  PDA_OUT_BF16 = 0,  /* bf16 [num_seqs][num_heads][head_size] */
+  PDA_OUT_E4M3 = 1   /* e4m3 bytes [num_seqs][num_heads][head_size]: E4M3(o / output_scale) */
+} pda_out_dtype;
+
+/*
+ * pda_decode_ex -- pda_decode with attention sinks and fused fp8 output.
+ *
+ * Source: the vLLM API page "vllm.v1.attention.backends.rocm_aiter_unified_attn"
+ * passes sinks= and output_scale= to the attention call (its backend reports
+ * supports_sink, and fused output quantisation for kFp8StaticTensorSym, one
+ * static symmetric per-tensor scale). The page does not print either
+ * computation; this library takes the plain reading of each:
+ *
+ *   sinks        fp32 [num_heads] on the device, or NULL. sinks[h] is a
+ *                logit of query head h in the units of scale * q . k that
+ *                joins the softmax normaliser and carries no value:
+ *                out = sum_t e^(z_t) v_t / (sum_t e^(z_t) + e^(sinks[h])).
+ *                A zero-length sequence still gives zeros.
+ *   out_dtype    PDA_OUT_BF16 (as pda_decode) or PDA_OUT_E4M3: out holds
+ *                e4m3 bytes E4M3(o / output_scale), the binary32 quotient
+ *                rounded to the nearest e4m3 value (ties to even),
+ *                saturating at +-448.
+ *   output_scale finite and > 0 when out_dtype is PDA_OUT_E4M3 (ignored
+ *                otherwise).
+ *
+ * Everything else is pda_decode's. Returns PDA_ERR_INVALID_ARG for an
+ * unknown out_dtype, a bad output_scale or a misaligned sinks pointer.
+ */
+pda_status pda_decode_ex(void* out, const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* block_tables, const int32_t* seq_lens, int num_seqs, int num_heads,
+                         int num_kv_heads, int head_size, int block_size, int max_num_blocks_per_seq, float scale,
+                         float k_scale, float v_scale, const float* sinks, int out_dtype, float output_scale,
+                         cudaStream_t stream);
+
 /*
  * pda_decode_slot_scales -- pda_decode with per-slot dequantisation scales.
  *

@@ -75,7 +75,9 @@ def _bind(lib):
     i32, i64, f64 = ctypes.c_int, ctypes.c_longlong, ctypes.c_double
     lib.pda_oracle_decode.restype = i32
     lib.pda_oracle_decode.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64,
-                                      f64, f64, f64, P, P, P, i32, i32]
+                                      f64, f64, f64, P, P, P, P, i32, i32]
+    lib.pda_oracle_quantize_e4m3.restype = None
+    lib.pda_oracle_quantize_e4m3.argtypes = [P, P, i64, f64]
     lib.pda_oracle_e4m3_value.restype = f64
     lib.pda_oracle_e4m3_value.argtypes = [ctypes.c_uint8]
     lib.pda_oracle_bf16_value.restype = f64
@@ -110,13 +112,15 @@ def _c(a, dtype):
 
 
 def decode(q, k_cache, v_cache, block_tables, seq_lens, *, scale: float, k_scale: float = 1.0,
-           v_scale: float = 1.0, k_scales=None, v_scales=None, num_blocks: int | None = None, seq_ids=None,
-           num_threads: int = 0, lib=None) -> np.ndarray:
+           v_scale: float = 1.0, k_scales=None, v_scales=None, sinks=None, num_blocks: int | None = None,
+           seq_ids=None, num_threads: int = 0, lib=None) -> np.ndarray:
     """Exact (binary64) decode attention; returns float64 ``[n, H, D]``.
 
     ``seq_ids`` selects a subset of sequences (rows of the result follow its
     order); ``None`` computes every sequence. ``k_scales`` / ``v_scales``
     (float32 ``[NB, Hk, bs]``) replace the per-tensor scales slot by slot.
+    ``sinks`` (float32 ``[H]``) adds one value-less logit per head to the
+    softmax normaliser.
     """
     q = _c(q, np.uint16)
     k_cache = _c(k_cache, np.uint8)
@@ -145,12 +149,18 @@ def decode(q, k_cache, v_cache, block_tables, seq_lens, *, scale: float, k_scale
         if k_scales.shape != (NB, Hk, bs) or v_scales.shape != (NB, Hk, bs):
             raise OracleError("scale tables must be [num_blocks, num_kv_heads, block_size]")
         ks_p, vs_p = k_scales.ctypes.data, v_scales.ctypes.data
+    sk_p = None
+    if sinks is not None:
+        sinks = _c(np.asarray(sinks, dtype=np.float32), np.float32)
+        if sinks.shape != (H,):
+            raise OracleError("sinks must be float32 [num_heads]")
+        sk_p = sinks.ctypes.data
     out = np.zeros((n, H, D), dtype=np.float64)
     L = lib if lib is not None else load()
     rc = L.pda_oracle_decode(out.ctypes.data, q.ctypes.data, k_cache.ctypes.data, v_cache.ctypes.data,
                              block_tables.ctypes.data, seq_lens.ctypes.data, S, H, Hk, D, bs, MB,
-                             int(num_blocks), float(scale), float(k_scale), float(v_scale), ks_p, vs_p, ids_p, n,
-                             int(num_threads))
+                             int(num_blocks), float(scale), float(k_scale), float(v_scale), ks_p, vs_p, sk_p,
+                             ids_p, n, int(num_threads))
     if rc != 0:
         raise OracleError("oracle rejected the inputs: %s (%d)" % (STATUS.get(rc, "?"), rc))
     return out
@@ -183,3 +193,11 @@ def reshape_and_cache(k_cache, v_cache, key, value, slot_mapping, *, k_scale: fl
                                         float(k_scale), float(v_scale))
     if rc != 0:
         raise OracleError("oracle rejected the inputs: %s (%d)" % (STATUS.get(rc, "?"), rc))
+
+
+def quantize_e4m3(x, output_scale: float, lib=None) -> np.ndarray:
+    """Static per-tensor fp8 output quantisation: E4M3(x / output_scale) codes (uint8)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    codes = np.zeros(x.shape, dtype=np.uint8)
+    (lib or load()).pda_oracle_quantize_e4m3(x.ctypes.data, codes.ctypes.data, x.size, float(output_scale))
+    return codes

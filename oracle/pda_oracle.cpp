@@ -118,6 +118,13 @@ double pda_oracle_bf16_value(uint16_t bits) { return bf16_value(bits); }
 // Only the first ceil(seq_lens[s] / block_size) entries of a table row are
 // read; only token slots t < seq_lens[s] are read from a page.
 //
+// Attention sinks (the API page passes sinks= to unified_attention and its
+// backend reports supports_sink; the arithmetic is not printed there): when
+// sinks is non-NULL, sinks[h] is a logit of query head h, in the same units
+// as scale * q . k, that joins the softmax normaliser but carries no value:
+//   out = sum_t e^(z_t - M) v_t / (sum_t e^(z_t - M) + e^(sink_h - M)),
+//   M = max(max_t z_t, sink_h); a zero-length sequence still gives zeros.
+//
 // Per-slot scale tables (vLLM pull request lishuoshuo-amd/vllm#3, "Details",
 // item "Scale tables": the asm kernel reads per-slot [blocks, kv_heads,
 // block_size] scales): when k_scales / v_scales are non-NULL they are fp32
@@ -130,7 +137,7 @@ int pda_oracle_decode(double* out, const uint16_t* q, const uint8_t* k_cache,
                       int num_kv_heads, int head_size, int block_size,
                       int max_num_blocks_per_seq, long long num_blocks,
                       double scale, double k_scale, double v_scale,
-                      const float* k_scales, const float* v_scales,
+                      const float* k_scales, const float* v_scales, const float* sinks,
                       const int32_t* seq_ids, int n_ids, int num_threads) {
   if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_size <= 0 ||
       block_size <= 0 || max_num_blocks_per_seq < 0 || num_blocks < 0 ||
@@ -193,10 +200,12 @@ int pda_oracle_decode(double* out, const uint16_t* q, const uint8_t* k_cache,
       z[t] = scale * acc;
     }
 
-    // softmax(z) . V
+    // softmax(z) . V (with the sink, if any, in the normaliser only)
     double zmax = z[0];
     for (long long t = 1; t < L; ++t) zmax = z[t] > zmax ? z[t] : zmax;
-    double denom = 0.0;
+    const double zs = sinks ? static_cast<double>(sinks[h]) : -INFINITY;
+    if (zs > zmax) zmax = zs;
+    double denom = sinks ? std::exp(zs - zmax) : 0.0;
     std::vector<double> w(L);
     for (long long t = 0; t < L; ++t) {
       w[t] = std::exp(z[t] - zmax);
@@ -217,6 +226,14 @@ int pda_oracle_decode(double* out, const uint16_t* q, const uint8_t* k_cache,
 }
 
 uint8_t pda_oracle_e4m3_encode(double x) { return e4m3_encode(x); }
+
+// Static per-tensor fp8 output quantisation (the API page's fused output
+// quantisation, kFp8StaticTensorSym: one scale, symmetric): code =
+// E4M3(x / output_scale), nearest e4m3 value of the exact quotient, ties to
+// even, saturating at +-448.
+void pda_oracle_quantize_e4m3(const double* x, uint8_t* codes, long long n, double output_scale) {
+  for (long long i = 0; i < n; ++i) codes[i] = e4m3_encode(x[i] / output_scale);
+}
 
 // KV-cache write: quantise new keys / values and scatter them into the
 // paged cache (vLLM API page "vllm.v1.attention.backends.rocm_aiter_unified_attn",

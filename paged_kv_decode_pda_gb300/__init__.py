@@ -16,9 +16,12 @@ from ._binding import (  # noqa: F401
     PDA_ERR_UNSUPPORTED,
     PDA_ERR_WORKSPACE,
     PDA_OK,
+    PDA_OUT_BF16,
+    PDA_OUT_E4M3,
     PdaError,
     choose_splits,
     decode,
+    decode_ex,
     decode_noalloc,
     decode_slot_scales,
     decode_raw,

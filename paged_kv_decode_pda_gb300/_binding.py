@@ -41,7 +41,11 @@ SIGNATURES = {
     "pda_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_longlong, _F, _F, _P]),
     "pda_decode_slot_scales": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "pda_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _F, _P]),
+    "pda_decode_ex": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _F, _P, _I, _F, _P]),
 }
+
+PDA_OUT_BF16 = 0
+PDA_OUT_E4M3 = 1
 
 _lock = threading.RLock()
 _lib = None
@@ -163,6 +167,32 @@ def decode_slot_scales(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Te
                                     seq_lens.data_ptr(), S, H, Hk, D, bs, int(block_tables.shape[1]), float(scale),
                                     _stream_ptr(stream))
     _check(st, "pda_decode_slot_scales")
+    return out
+
+
+def decode_ex(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+              seq_lens: torch.Tensor, scale: float, k_scale: float, v_scale: float, *, sinks=None,
+              output_scale: float | None = None, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """``pda_decode_ex``: decode with optional per-head sinks (fp32 ``[H]``) and,
+    when ``output_scale`` is given, e4m3 output ``E4M3(o / output_scale)``."""
+    lib = load()
+    _check_decode_args(q, k_cache, v_cache, block_tables, seq_lens)
+    S, H, D = q.shape
+    NB, Hk, _, bs, _ = k_cache.shape
+    if sinks is not None and (sinks.dtype != torch.float32 or tuple(sinks.shape) != (H,) or not sinks.is_cuda):
+        raise PdaError(PDA_ERR_INVALID_ARG, "decode_ex: sinks must be a CUDA float32 [num_heads] tensor")
+    fp8 = output_scale is not None
+    want = torch.float8_e4m3fn if fp8 else torch.bfloat16
+    if out is None:
+        out = torch.empty(q.shape, dtype=want, device=q.device)
+    elif out.shape != q.shape or out.dtype not in ((want, torch.uint8) if fp8 else (want,)) or not out.is_contiguous():
+        raise PdaError(PDA_ERR_INVALID_ARG, "decode_ex: out")
+    st = lib.pda_decode_ex(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                           block_tables.data_ptr(), seq_lens.data_ptr(), S, H, Hk, D, bs, int(block_tables.shape[1]),
+                           float(scale), float(k_scale), float(v_scale), sinks.data_ptr() if sinks is not None else None,
+                           PDA_OUT_E4M3 if fp8 else PDA_OUT_BF16, float(output_scale) if fp8 else 1.0,
+                           _stream_ptr(stream))
+    _check(st, "pda_decode_ex")
     return out
 
 

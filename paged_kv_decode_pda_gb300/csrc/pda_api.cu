@@ -185,7 +185,8 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
                                 const float* k_scales, const float* v_scales, const int32_t* block_tables,
                                 const int32_t* seq_lens, int num_seqs, int num_heads, int num_kv_heads,
                                 int head_size, int block_size, int max_num_blocks_per_seq, float scale,
-                                float k_scale, float v_scale, cudaStream_t stream) {
+                                float k_scale, float v_scale, cudaStream_t stream, const float* sinks = nullptr,
+                                int out_fp8 = 0, float out_scale = 1.f) {
   pda_status st = validate(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_heads, num_kv_heads,
                            head_size, block_size, max_num_blocks_per_seq, scale, k_scale, v_scale);
   if (st != PDA_OK || num_seqs == 0) return st;
@@ -203,7 +204,7 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
 
   const RingShape rs = ring_shape(block_size, slot);
   pda::DecodeParams p;
-  p.out = static_cast<__nv_bfloat16*>(out);
+  p.out = out;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k_cache = static_cast<const uint8_t*>(k_cache);
   p.v_cache = static_cast<const uint8_t*>(v_cache);
@@ -225,6 +226,9 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
   p.v_scales = slot ? v_scales : nullptr;
   p.logit_scale_log2 = (float)((double)scale * (slot ? 1.0 : (double)k_scale) * 1.4426950408889634);
   p.v_scale = v_scale;
+  p.sinks = sinks;
+  p.out_fp8 = out_fp8;
+  p.out_scale = out_scale;
 
   cudaEvent_t eb = g_prof_before.load(), ea = g_prof_after.load();
   if (eb && ea && record_profile_event(eb, stream) != cudaSuccess) return PDA_ERR_CUDA;
@@ -247,6 +251,9 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
     mp.max_blocks = max_num_blocks_per_seq;
     mp.nsplit = nsplit;
     mp.v_scale = slot ? 1.f : v_scale;
+    mp.sinks = sinks;
+    mp.out_fp8 = out_fp8;
+    mp.out_scale = out_scale;
     pda::pda_merge_kernel<<<dim3((unsigned)num_heads, (unsigned)num_seqs), kHeadDim, 0, stream>>>(mp);
     if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
   }
@@ -412,6 +419,20 @@ pda_status pda_decode(void* out, const void* q, const void* k_cache, const void*
                        v_scale, stream);
 }
 
+pda_status pda_decode_ex(void* out, const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* block_tables, const int32_t* seq_lens, int num_seqs, int num_heads,
+                         int num_kv_heads, int head_size, int block_size, int max_num_blocks_per_seq, float scale,
+                         float k_scale, float v_scale, const float* sinks, int out_dtype, float output_scale,
+                         cudaStream_t stream) {
+  if (out_dtype != PDA_OUT_BF16 && out_dtype != PDA_OUT_E4M3) return PDA_ERR_INVALID_ARG;
+  if (out_dtype == PDA_OUT_E4M3 && !(std::isfinite(output_scale) && output_scale > 0.f)) return PDA_ERR_INVALID_ARG;
+  if (sinks && (reinterpret_cast<uintptr_t>(sinks) & 3u)) return PDA_ERR_INVALID_ARG;
+  return launch_decode(false, out, q, k_cache, v_cache, nullptr, nullptr, block_tables, seq_lens, num_seqs,
+                       num_heads, num_kv_heads, head_size, block_size, max_num_blocks_per_seq, scale, k_scale,
+                       v_scale, stream, sinks, out_dtype == PDA_OUT_E4M3 ? 1 : 0,
+                       out_dtype == PDA_OUT_E4M3 ? output_scale : 1.f);
+}
+
 pda_status pda_decode_slot_scales(void* out, const void* q, const void* k_cache, const void* v_cache,
                                   const float* k_scales, const float* v_scales, const int32_t* block_tables,
                                   const int32_t* seq_lens, int num_seqs, int num_heads, int num_kv_heads,
@@ -509,7 +530,7 @@ extern "C" pda_status pda_decode_noalloc(void* out, const void* q, const void* k
   const RingShape rs = ring_shape(block_size);
   float* scratch = static_cast<float*>(d.scratch);
   pda::DecodeParams p;
-  p.out = static_cast<__nv_bfloat16*>(out);
+  p.out = out;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k_cache = static_cast<const uint8_t*>(k_cache);
   p.v_cache = static_cast<const uint8_t*>(v_cache);

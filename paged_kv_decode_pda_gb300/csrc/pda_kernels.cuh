@@ -48,7 +48,7 @@ constexpr int kMaxGqa = 8;                   // MMA N dimension: query heads of 
 constexpr int kMergeStride = kHeadDim + 4;   // padded fp32 row of the CTA merge area
 
 struct DecodeParams {
-  __nv_bfloat16* out;           // [S][H][D]
+  void* out;                    // [S][H][D] bf16, or e4m3 bytes when out_fp8
   const __nv_bfloat16* q;       // [S][H][D]
   const uint8_t* k_cache;       // [NB][Hk][D/16][bs][16]
   const uint8_t* v_cache;       // [NB][Hk][D][bs]
@@ -70,7 +70,33 @@ struct DecodeParams {
   const float* v_scales;        // [NB][Hk][bs] fp32 (slot-scale variant)
   float logit_scale_log2;       // scale * k_scale * log2(e)  (scale * log2(e) with slot scales)
   float v_scale;                // per-tensor V scale (unused with slot scales)
+  const float* sinks = nullptr; // [H] per-head sink logits (scale * q.k units), or none
+  int out_fp8 = 0;              // 1: out holds E4M3(o / out_scale) bytes
+  float out_scale = 1.f;
 };
+
+// Final normalisation shared by the decode kernel (one split) and the merge
+// kernel: a sink logit zs (log2 units, -inf for none) joins the normaliser
+// only; M is the running max of the numerator terms.
+__device__ __forceinline__ float finish(float acc, float den, float M, float zs, float vfac) {
+  if (zs != -INFINITY) {
+    const float Mn = fmaxf(M, zs);
+    const float f = (M == -INFINITY) ? 0.f : fast_exp2(M - Mn);
+    acc *= f;
+    den = den * f + fast_exp2(zs - Mn);
+  }
+  return den > 0.f ? acc * (vfac / den) : 0.f;
+}
+
+// Store one output element: bf16, or the e4m3 code of x / out_scale (IEEE
+// binary32 quotient, round to nearest even, saturating at +-448).
+__device__ __forceinline__ void store_out(void* out, size_t idx, float x, int out_fp8, float out_scale) {
+  if (out_fp8) {
+    static_cast<uint8_t*>(out)[idx] = (uint8_t)(f32x2_to_e4m3x2(__fdiv_rn(x, out_scale), 0.f) & 0xFFu);
+  } else {
+    static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(x);
+  }
+}
 
 // Token order of the 16 MMA rows of a K tile. Row r of the QK accumulator
 // holds token row_token(r); the order is chosen so that, after the P
@@ -138,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 3) pda_split_decode_kernel(const Dec
     if (p.nsplit == 1) {
       for (int i = threadIdx.x; i < g * kHeadDim; i += blockDim.x) {
         const int h = kvh * g + i / kHeadDim;
-        p.out[((size_t)s * H + h) * kHeadDim + (i % kHeadDim)] = __float2bfloat16_rn(0.f);
+        store_out(p.out, ((size_t)s * H + h) * kHeadDim + (i % kHeadDim), 0.f, p.out_fp8, p.out_scale);
       }
     }
     return;
@@ -447,8 +473,9 @@ __global__ void __launch_bounds__(kThreads, 3) pda_split_decode_kernel(const Dec
     }
     const int h = kvh * g + hh;
     if (p.nsplit == 1) {
-      const float r = den > 0.f ? acc * ((kSlotScales ? vref : p.v_scale) / den) : 0.f;
-      p.out[((size_t)s * H + h) * kHeadDim + d] = __float2bfloat16_rn(r);
+      const float zs = p.sinks ? __ldg(p.sinks + h) * 1.4426950408889634f : -INFINITY;
+      const float r = finish(acc, den, M, zs, kSlotScales ? vref : p.v_scale);
+      store_out(p.out, ((size_t)s * H + h) * kHeadDim + d, r, p.out_fp8, p.out_scale);
     } else {
       // Slot-scale partials carry their own V reference (the merge then uses 1).
       const size_t prow = ((size_t)s * H + h) * p.nsplit + split;
@@ -464,10 +491,11 @@ __global__ void __launch_bounds__(kThreads, 3) pda_split_decode_kernel(const Dec
 // Log-sum-exp merge of the per-split partials of one (sequence, head) per
 // 128-thread block (one output dim per thread):
 //   M = max_i m_i,  out = v_scale * sum_i 2^(m_i - M) O_i / sum_i 2^(m_i - M) l_i
+// with a sink logit, if any, added to the denominator (finish()).
 // Splits with no pages were never written and are skipped by the same page
 // rule the decode kernel uses; a zero-length sequence gets zeros.
 struct MergeParams {
-  __nv_bfloat16* out;
+  void* out;
   const float* part_o;
   const float* part_ml;
   const int32_t* seq_lens;
@@ -476,6 +504,9 @@ struct MergeParams {
   int max_blocks;
   int nsplit;
   float v_scale;
+  const float* sinks = nullptr;
+  int out_fp8 = 0;
+  float out_scale = 1.f;
 };
 
 __global__ void __launch_bounds__(kHeadDim) pda_merge_kernel(const MergeParams p) {
@@ -501,8 +532,9 @@ __global__ void __launch_bounds__(kHeadDim) pda_merge_kernel(const MergeParams p
       den += f * __ldg(p.part_ml + (prow0 + i) * 2 + 1);
     }
   }
-  const float r = den > 0.f ? acc * (p.v_scale / den) : 0.f;
-  p.out[((size_t)s * p.num_heads + h) * kHeadDim + d] = __float2bfloat16_rn(r);
+  const float zs = p.sinks ? __ldg(p.sinks + h) * 1.4426950408889634f : -INFINITY;
+  const float r = (pages > 0) ? finish(acc, den, M, zs, p.v_scale) : 0.f;
+  store_out(p.out, ((size_t)s * p.num_heads + h) * kHeadDim + d, r, p.out_fp8, p.out_scale);
 }
 
 // One CTA waits on an mbarrier that nothing completes, with a short limit,

@@ -323,6 +323,60 @@ def pin_slot_scales(lib):
         assert np.array_equal(a, b)
 
 
+# ----------------------------------------------------- sinks, fp8 output
+
+def pin_sinks(lib):
+    lens = [1, 5, 40, 33, 0]
+    qbits, Kc, Vc = dense_case(5, 8, 2, lens, seed=101)
+    kc, vc, tb, ln = scatter_pages(Kc, Vc, lens, 16, seed=13)
+    rng = np.random.default_rng(103)
+    sinks = (rng.standard_normal(8) * 2).astype(np.float32)
+    got = oracle.decode(qbits, kc, vc, tb, ln, scale=0.09, k_scale=0.05, v_scale=0.05, sinks=sinks, lib=lib)
+    # dense reference: softmax over [z_0..z_{L-1}, sink], the sink's weight dropped
+    q = torch.from_numpy(qbits.view(np.int16)).view(torch.bfloat16).to(torch.float64)
+    Kd = torch.from_numpy(torch_e4m3(Kc)) * 0.05
+    Vd = torch.from_numpy(torch_e4m3(Vc)) * 0.05
+    for s, L in enumerate(lens):
+        if L == 0:
+            assert np.all(got[s] == 0)
+            continue
+        Kh = Kd[s, :, :L].repeat_interleave(4, dim=0)
+        Vh = Vd[s, :, :L].repeat_interleave(4, dim=0)
+        z = torch.einsum("hld,hd->hl", Kh, q[s]) * 0.09
+        zz = torch.cat([z, torch.from_numpy(sinks.astype(np.float64))[:, None]], dim=1)
+        p = torch.softmax(zz, dim=-1)[:, :L]
+        ref = torch.einsum("hl,hld->hd", p, Vh).numpy()
+        assert np.max(np.abs(got[s] - ref)) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
+    # closed form: K = 0 makes every logit 0, so out = L / (L + e^sink) * mean(v)
+    Kc[:] = 0
+    kc, vc, tb, ln = scatter_pages(Kc, Vc, lens, 16, seed=13)
+    got = oracle.decode(qbits, kc, vc, tb, ln, scale=0.09, k_scale=0.05, v_scale=0.05, sinks=sinks, lib=lib)
+    for s, L in enumerate(lens):
+        if L == 0:
+            continue
+        for h in range(8):
+            want = L / (L + math.exp(float(sinks[h]))) * Vd[s, h // 4, :L].mean(0).numpy()
+            assert np.max(np.abs(got[s, h] - want)) <= 1e-12
+    # a sink at -inf is no sink
+    none = oracle.decode(qbits, kc, vc, tb, ln, scale=0.09, k_scale=0.05, v_scale=0.05, lib=lib)
+    neg = oracle.decode(qbits, kc, vc, tb, ln, scale=0.09, k_scale=0.05, v_scale=0.05,
+                        sinks=np.full(8, -np.inf, dtype=np.float32), lib=lib)
+    assert np.array_equal(none, neg)
+
+
+def pin_quantize_output(lib):
+    rng = np.random.default_rng(107)
+    x = np.concatenate([rng.standard_normal(5000) * 0.3, [0.0, -0.0, 1e9, -1e9, 1e-12]])
+    for sc in (0.01, 0.0173, 0.5):
+        got = oracle.quantize_e4m3(x, sc, lib=lib)
+        ref = torch.from_numpy(np.clip(x / sc, -448, 448).astype(np.float32)).to(torch.float8_e4m3fn)
+        ref = ref.view(torch.uint8).numpy()
+        # the binary64 quotient rounded to binary32 first can only move a
+        # result that sits within a binary32 ulp of a midpoint
+        diff = got != ref
+        assert diff.sum() <= 2, "fp8 output codes differ from torch on %d values" % diff.sum()
+
+
 # ------------------------------------------------------- KV-cache write pins
 
 def torch_quantise(bits_u16: np.ndarray, scale: float) -> np.ndarray:
@@ -420,4 +474,4 @@ def pin_quantise_in_binary32(lib):
 
 ALL_PINS = [pin_e4m3_table, pin_bf16, pin_dense, pin_large_logits, pin_permutation_invariance,
             pin_constant_v, pin_single_token, pin_zero_k, pin_tail_poison, pin_gqa_is_repeated_mha,
-            pin_zero_length, pin_slot_scales, pin_e4m3_encode, pin_reshape_and_cache, pin_quantise_in_binary32]
+            pin_zero_length, pin_slot_scales, pin_sinks, pin_quantize_output, pin_e4m3_encode, pin_reshape_and_cache, pin_quantise_in_binary32]

@@ -1,0 +1,115 @@
+"""pda_decode_ex on GPU: attention sinks and fused e4m3 output against the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_decode_pda_gb300 as pda
+import workloads
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    torch.cuda.set_device(0)
+    from paged_kv_decode_pda_gb300 import build
+    build.build()
+    pda.load()
+    pda.set_split_override(0)
+    yield
+    pda.set_split_override(0)
+    assert pda.query_device_status() == 0
+
+
+def _batch(seed=41):
+    return workloads.make_custom(6, 40, 8, [0, 1, 17, 300, 1024, 777], block_size=16, pool_factor=1.2, seed=seed,
+                                 device=DEV)
+
+
+def _sinks(H, seed):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(H, generator=g) * 2).float()
+
+
+@pytest.mark.parametrize("splits", [1, 3, 12])
+def test_sinks_parity(splits):
+    batch = _batch()
+    cfg = batch.cfg
+    sinks = _sinks(cfg.num_heads, 1)
+    pda.set_split_override(splits)
+    try:
+        out = pda.decode_ex(batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.seq_lens, cfg.scale,
+                            cfg.k_scale, cfg.v_scale, sinks=sinks.to(DEV))
+        torch.cuda.synchronize()
+    finally:
+        pda.set_split_override(0)
+    ref = oracle.decode(**batch.raw(), scale=cfg.scale, k_scale=cfg.k_scale, v_scale=cfg.v_scale,
+                        sinks=sinks.numpy())
+    U.compare(out, ref, "sinks, splits=%d" % splits)
+    assert torch.all(out[0] == 0), "zero-length sequence must stay zero with a sink"
+
+
+def test_ex_without_options_equals_decode():
+    batch = _batch(43)
+    cfg = batch.cfg
+    a = pda.decode_ex(batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.seq_lens, cfg.scale,
+                      cfg.k_scale, cfg.v_scale)
+    b = U.run_cuda(batch)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("splits,with_sinks", [(1, False), (3, True), (12, False), (12, True)])
+def test_fp8_output(splits, with_sinks):
+    batch = _batch(47)
+    cfg = batch.cfg
+    sinks = _sinks(cfg.num_heads, 2) if with_sinks else None
+    out_scale = 0.0075   # |o| up to ~3.4 -> codes up to 448
+    pda.set_split_override(splits)
+    try:
+        out = pda.decode_ex(batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.seq_lens, cfg.scale,
+                            cfg.k_scale, cfg.v_scale, sinks=sinks.to(DEV) if with_sinks else None,
+                            output_scale=out_scale)
+        torch.cuda.synchronize()
+    finally:
+        pda.set_split_override(0)
+    exact = oracle.decode(**batch.raw(), scale=cfg.scale, k_scale=cfg.k_scale, v_scale=cfg.v_scale,
+                          sinks=sinks.numpy() if with_sinks else None)
+    want = oracle.quantize_e4m3(exact, out_scale)
+    got = out.view(torch.uint8).cpu().numpy()
+    vg = torch.from_numpy(got).view(torch.float8_e4m3fn).double().numpy() * out_scale
+    vw = torch.from_numpy(want).view(torch.float8_e4m3fn).double().numpy() * out_scale
+    # The code is decided on the kernel's fp32 result, the oracle's on the
+    # exact one. Bound per element: half an e4m3 step at |o| (the rounding
+    # any e4m3 output has) plus the bf16 path's 8e-3 bar for the kernel's own
+    # error; on average the kernel may add at most the 2e-4 mean bar to the
+    # unavoidable e4m3 rounding error of the exact values.
+    # Saturation: values past 448 * scale store as +-448 on both sides.
+    target = np.clip(exact, -448.0 * out_scale, 448.0 * out_scale)
+    q = np.abs(target) / out_scale
+    expo = np.floor(np.log2(np.maximum(q, 2.0 ** -6)))
+    half_step = np.ldexp(1.0, (expo - 4).astype(np.int64)) * out_scale
+    err = np.abs(vg - target)
+    assert np.all(err <= half_step + U.MAX_ABS), "max excess %g" % float(np.max(err - half_step))
+    assert err.mean() <= np.abs(vw - target).mean() + U.MEAN_ABS, (err.mean(), np.abs(vw - target).mean())
+    frac_equal = float(np.mean(got == want))
+    assert frac_equal >= 0.9, "only %.4f of fp8 codes equal the exact result's code" % frac_equal
+    assert np.all(got[0] == 0)
+
+
+def test_ex_rejects_bad_options():
+    lib = pda.load()
+    batch = _batch(49)
+    cfg = batch.cfg
+    args = [batch.q.data_ptr(), batch.q.data_ptr(), batch.k_cache.data_ptr(), batch.v_cache.data_ptr(),
+            batch.block_tables.data_ptr(), batch.seq_lens.data_ptr(), cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads,
+            128, 16, int(batch.block_tables.shape[1]), cfg.scale, cfg.k_scale, cfg.v_scale]
+    assert lib.pda_decode_ex(*args, None, 7, 1.0, None) == pda.PDA_ERR_INVALID_ARG
+    assert lib.pda_decode_ex(*args, None, pda.PDA_OUT_E4M3, 0.0, None) == pda.PDA_ERR_INVALID_ARG
+    assert lib.pda_decode_ex(*args, None, pda.PDA_OUT_E4M3, float("nan"), None) == pda.PDA_ERR_INVALID_ARG

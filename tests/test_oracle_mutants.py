@@ -45,6 +45,7 @@ MUTANTS = {
     "cache_write_v_token_major": ("v_cache[page + d * bs + o]", "v_cache[page + o * D + d]"),
     "slot_scale_wrong_head": ("k_scales[(b * num_kv_heads + kv) * bs + slot]", "k_scales[(b * num_kv_heads + 0) * bs + slot]"),
     "slot_scale_wrong_slot": ("v_scales[(b * num_kv_heads + kv) * bs + slot]", "v_scales[(b * num_kv_heads + kv) * bs]"),
+    "sink_carries_value": ("double denom = sinks ? std::exp(zs - zmax) : 0.0;", "double denom = 0.0;"),
 }
 
 
