@@ -54,9 +54,10 @@ def parse():
     ap.add_argument("--config", default=workloads.HEADLINE, choices=sorted(workloads.CONFIGS))
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--variant", choices=["plain", "slot_scales", "ex"], default="plain",
-                    help="decode entry point: pda_decode, pda_decode_slot_scales (per-slot tables), or "
-                         "pda_decode_ex with per-head sinks and e4m3 output")
+    ap.add_argument("--variant", choices=["plain", "slot_scales", "ex", "shuffled_v"], default="plain",
+                    help="decode entry point: pda_decode, pda_decode_slot_scales (per-slot tables), "
+                         "pda_decode_ex with per-head sinks and e4m3 output, or pda_decode_ex on the "
+                         "shuffled V layout")
     ap.add_argument("--op", choices=["decode", "cache_write"], default="decode",
                     help="cache_write: time pda_reshape_and_cache on --tokens new tokens of the config's kv heads")
     ap.add_argument("--tokens", type=int, default=65536)
@@ -256,9 +257,18 @@ def run_ours(args, ws, rank, local):
         bytes_per_call -= out.numel()   # 1-byte instead of 2-byte output
         bytes_per_call += cfg.num_heads * 4
 
+    elif args.variant == "shuffled_v":
+        def shuffle(v):
+            NB, Hk, D, bs = v.shape
+            return v.reshape(NB, Hk, D, bs // 16, 16).permute(0, 1, 3, 2, 4).contiguous()
+        caches = [(k, shuffle(v)) for k, v in caches]
+
     def call(i):
         kc, vc = caches[i % replicas]
-        if args.variant == "slot_scales":
+        if args.variant == "shuffled_v":
+            pda.decode_ex(batch.q, kc, vc, batch.block_tables, batch.seq_lens, cfg.scale, cfg.k_scale, cfg.v_scale,
+                          v_shuffled=True, out=out, stream=stream)
+        elif args.variant == "slot_scales":
             pda.decode_slot_scales(batch.q, kc, vc, ks_t, vs_t, batch.block_tables, batch.seq_lens, cfg.scale,
                                    out=out, stream=stream)
         elif args.variant == "ex":

@@ -106,6 +106,20 @@ pda_status pda_decode(void* out, const void* q, const void* k_cache, const void*
                       int max_num_blocks_per_seq, float scale, float k_scale, float v_scale,
                       cudaStream_t stream);
 
+/*
+ * KV cache layouts (pda_decode_ex, pda_reshape_and_cache). K is always
+ * [num_blocks][num_kv_heads][head_size/16][block_size][16].
+ *   PDA_KV_NATIVE      V [num_blocks][num_kv_heads][head_size][block_size]
+ *   PDA_KV_SHUFFLED_V  V [num_blocks][num_kv_heads][block_size/16][head_size][16]
+ * The shuffled V is AITER's layout; at block_size 16 the two are the same
+ * bytes (vLLM pull request lishuoshuo-amd/vllm#3, "Details", item "Layout";
+ * the API page's _shuffle_kv_views views V as (nb, nkv, bs//x, hd, x)).
+ */
+typedef enum pda_kv_layout {
+  PDA_KV_NATIVE = 0,
+  PDA_KV_SHUFFLED_V = 1
+} pda_kv_layout;
+
 /* Output element type of pda_decode_ex. */
 typedef enum pda_out_dtype {
   PDA_OUT_BF16 = 0,  /* bf16 [num_seqs][num_heads][head_size] */
@@ -133,14 +147,17 @@ typedef enum pda_out_dtype {
  *   output_scale finite and > 0 when out_dtype is PDA_OUT_E4M3 (ignored
  *                otherwise).
  *
+ *   kv_layout    PDA_KV_NATIVE (pda_decode's layout) or PDA_KV_SHUFFLED_V.
+ *
  * Everything else is pda_decode's. Returns PDA_ERR_INVALID_ARG for an
- * unknown out_dtype, a bad output_scale or a misaligned sinks pointer.
+ * unknown kv_layout or out_dtype, a bad output_scale or a misaligned sinks
+ * pointer.
  */
 pda_status pda_decode_ex(void* out, const void* q, const void* k_cache, const void* v_cache,
                          const int32_t* block_tables, const int32_t* seq_lens, int num_seqs, int num_heads,
                          int num_kv_heads, int head_size, int block_size, int max_num_blocks_per_seq, float scale,
-                         float k_scale, float v_scale, const float* sinks, int out_dtype, float output_scale,
-                         cudaStream_t stream);
+                         float k_scale, float v_scale, int kv_layout, const float* sinks, int out_dtype,
+                         float output_scale, cudaStream_t stream);
 
 /*
  * pda_decode_slot_scales -- pda_decode with per-slot dequantisation scales.
@@ -178,7 +195,9 @@ pda_status pda_decode_slot_scales(void* out, const void* q, const void* k_cache,
  *
  *   key, value    bf16  [num_tokens][num_kv_heads][head_size]   read
  *   k_cache       e4m3  [num_blocks][num_kv_heads][head_size/16][block_size][16]  written
- *   v_cache       e4m3  [num_blocks][num_kv_heads][head_size][block_size]          written
+ *   v_cache       e4m3  as kv_layout says (PDA_KV_NATIVE: [num_blocks][num_kv_heads]
+ *                 [head_size][block_size]; PDA_KV_SHUFFLED_V: [num_blocks]
+ *                 [num_kv_heads][block_size/16][head_size][16])           written
  *   slot_mapping  int64 [num_tokens]: slot = block * block_size + offset;
  *                 negative = padding (skipped)
  *
@@ -194,7 +213,7 @@ pda_status pda_decode_slot_scales(void* out, const void* q, const void* k_cache,
  */
 pda_status pda_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
                                  const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_size,
-                                 int block_size, long long num_blocks, float k_scale, float v_scale,
+                                 int block_size, long long num_blocks, float k_scale, float v_scale, int kv_layout,
                                  cudaStream_t stream);
 
 /*

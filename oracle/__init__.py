@@ -75,7 +75,7 @@ def _bind(lib):
     i32, i64, f64 = ctypes.c_int, ctypes.c_longlong, ctypes.c_double
     lib.pda_oracle_decode.restype = i32
     lib.pda_oracle_decode.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64,
-                                      f64, f64, f64, P, P, P, P, i32, i32]
+                                      f64, f64, f64, P, P, P, i32, P, i32, i32]
     lib.pda_oracle_quantize_e4m3.restype = None
     lib.pda_oracle_quantize_e4m3.argtypes = [P, P, i64, f64]
     lib.pda_oracle_e4m3_value.restype = f64
@@ -86,7 +86,7 @@ def _bind(lib):
     lib.pda_oracle_e4m3_encode.argtypes = [f64]
     lib.pda_oracle_reshape_and_cache.restype = i32
     lib.pda_oracle_reshape_and_cache.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i64, ctypes.c_float,
-                                                 ctypes.c_float]
+                                                 ctypes.c_float, i32]
     lib.pda_oracle_max_threads.restype = i32
     lib.pda_oracle_max_threads.argtypes = []
     return lib
@@ -112,15 +112,15 @@ def _c(a, dtype):
 
 
 def decode(q, k_cache, v_cache, block_tables, seq_lens, *, scale: float, k_scale: float = 1.0,
-           v_scale: float = 1.0, k_scales=None, v_scales=None, sinks=None, num_blocks: int | None = None,
-           seq_ids=None, num_threads: int = 0, lib=None) -> np.ndarray:
+           v_scale: float = 1.0, k_scales=None, v_scales=None, sinks=None, v_shuffled: bool = False,
+           num_blocks: int | None = None, seq_ids=None, num_threads: int = 0, lib=None) -> np.ndarray:
     """Exact (binary64) decode attention; returns float64 ``[n, H, D]``.
 
     ``seq_ids`` selects a subset of sequences (rows of the result follow its
     order); ``None`` computes every sequence. ``k_scales`` / ``v_scales``
     (float32 ``[NB, Hk, bs]``) replace the per-tensor scales slot by slot.
     ``sinks`` (float32 ``[H]``) adds one value-less logit per head to the
-    softmax normaliser.
+    softmax normaliser. ``v_shuffled``: ``v_cache`` is ``[NB, Hk, bs/16, D, 16]``.
     """
     q = _c(q, np.uint16)
     k_cache = _c(k_cache, np.uint8)
@@ -129,7 +129,8 @@ def decode(q, k_cache, v_cache, block_tables, seq_lens, *, scale: float, k_scale
     seq_lens = _c(seq_lens, np.int32)
     S, H, D = q.shape
     NB, Hk, D16, bs, sixteen = k_cache.shape
-    if sixteen != 16 or D16 * 16 != D or v_cache.shape != (NB, Hk, D, bs):
+    v_want = (NB, Hk, bs // 16, D, 16) if v_shuffled else (NB, Hk, D, bs)
+    if sixteen != 16 or D16 * 16 != D or v_cache.shape != v_want:
         raise OracleError("cache shapes do not match q: k %s v %s q %s" % (k_cache.shape, v_cache.shape, q.shape))
     if block_tables.ndim != 2 or block_tables.shape[0] != S or seq_lens.shape != (S,):
         raise OracleError("table shapes do not match q")
@@ -160,7 +161,7 @@ def decode(q, k_cache, v_cache, block_tables, seq_lens, *, scale: float, k_scale
     rc = L.pda_oracle_decode(out.ctypes.data, q.ctypes.data, k_cache.ctypes.data, v_cache.ctypes.data,
                              block_tables.ctypes.data, seq_lens.ctypes.data, S, H, Hk, D, bs, MB,
                              int(num_blocks), float(scale), float(k_scale), float(v_scale), ks_p, vs_p, sk_p,
-                             ids_p, n, int(num_threads))
+                             1 if v_shuffled else 0, ids_p, n, int(num_threads))
     if rc != 0:
         raise OracleError("oracle rejected the inputs: %s (%d)" % (STATUS.get(rc, "?"), rc))
     return out
@@ -171,7 +172,7 @@ def e4m3_encode(x: float, lib=None) -> int:
 
 
 def reshape_and_cache(k_cache, v_cache, key, value, slot_mapping, *, k_scale: float, v_scale: float,
-                      lib=None) -> None:
+                      v_shuffled: bool = False, lib=None) -> None:
     """Quantise and scatter new tokens into the paged caches, in place.
 
     key / value: uint16 bf16 bits ``[T, Hk, D]``; slot_mapping: int64 ``[T]``
@@ -185,12 +186,13 @@ def reshape_and_cache(k_cache, v_cache, key, value, slot_mapping, *, k_scale: fl
     slot_mapping = _c(slot_mapping, np.int64)
     T, Hk, D = key.shape
     NB, Hk2, D16, bs, sixteen = k_cache.shape
-    if value.shape != key.shape or Hk2 != Hk or D16 * 16 != D or v_cache.shape != (NB, Hk, D, bs):
+    v_want = (NB, Hk, bs // 16, D, 16) if v_shuffled else (NB, Hk, D, bs)
+    if value.shape != key.shape or Hk2 != Hk or D16 * 16 != D or v_cache.shape != v_want:
         raise OracleError("shapes do not match")
     L = lib if lib is not None else load()
     rc = L.pda_oracle_reshape_and_cache(k_cache.ctypes.data, v_cache.ctypes.data, key.ctypes.data,
                                         value.ctypes.data, slot_mapping.ctypes.data, T, Hk, D, bs, NB,
-                                        float(k_scale), float(v_scale))
+                                        float(k_scale), float(v_scale), 1 if v_shuffled else 0)
     if rc != 0:
         raise OracleError("oracle rejected the inputs: %s (%d)" % (STATUS.get(rc, "?"), rc))
 

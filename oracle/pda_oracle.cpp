@@ -118,6 +118,12 @@ double pda_oracle_bf16_value(uint16_t bits) { return bf16_value(bits); }
 // Only the first ceil(seq_lens[s] / block_size) entries of a table row are
 // read; only token slots t < seq_lens[s] are read from a page.
 //
+// V layout: v_shuffled == 0 reads V pages as [head_size][block_size];
+// v_shuffled == 1 reads AITER's shuffled V, [block_size/16][head_size][16]
+// per (block, kv head) (vLLM pull request lishuoshuo-amd/vllm#3, "Details",
+// item "Layout"; the API page's _shuffle_kv_views, V viewed as
+// (nb, nkv, bs//x, hd, x)). The two coincide at block_size 16.
+//
 // Attention sinks (the API page passes sinks= to unified_attention and its
 // backend reports supports_sink; the arithmetic is not printed there): when
 // sinks is non-NULL, sinks[h] is a logit of query head h, in the same units
@@ -138,7 +144,7 @@ int pda_oracle_decode(double* out, const uint16_t* q, const uint8_t* k_cache,
                       int max_num_blocks_per_seq, long long num_blocks,
                       double scale, double k_scale, double v_scale,
                       const float* k_scales, const float* v_scales, const float* sinks,
-                      const int32_t* seq_ids, int n_ids, int num_threads) {
+                      int v_shuffled, const int32_t* seq_ids, int n_ids, int num_threads) {
   if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_size <= 0 ||
       block_size <= 0 || max_num_blocks_per_seq < 0 || num_blocks < 0 ||
       num_heads % num_kv_heads != 0 || head_size % 16 != 0) {
@@ -218,7 +224,9 @@ int pda_oracle_decode(double* out, const uint16_t* q, const uint8_t* k_cache,
       const double vs = v_scales ? static_cast<double>(v_scales[(b * num_kv_heads + kv) * bs + slot]) : v_scale;
       const double wt = w[t] / denom;
       for (int d = 0; d < D; ++d) {
-        o[d] += wt * (e4m3[vpage[static_cast<long long>(d) * bs + slot]] * vs);
+        const long long vi = v_shuffled ? ((slot / 16) * D + d) * 16 + (slot % 16)
+                                        : static_cast<long long>(d) * bs + slot;
+        o[d] += wt * (e4m3[vpage[vi]] * vs);
       }
     }
   }
@@ -243,6 +251,7 @@ void pda_oracle_quantize_e4m3(const double* x, uint8_t* codes, long long n, doub
 // offset o = slot % block_size, kv head k and dim d:
 //   k_cache[b][k][d/16][o][d%16] = E4M3( float(key[t][k][d]) / k_scale )
 //   v_cache[b][k][d][o]          = E4M3( float(value[t][k][d]) / v_scale )
+// (v_shuffled = 1: v_cache[b][k][o/16][d][o%16], the shuffled V layout.)
 // The quotient is the binary32 quotient (the cache stores what a binary32
 // division produces before rounding to e4m3); E4M3 is e4m3_encode. Negative
 // slots are skipped (padding). key / value are bf16 bit patterns
@@ -251,7 +260,7 @@ void pda_oracle_quantize_e4m3(const double* x, uint8_t* codes, long long n, doub
 int pda_oracle_reshape_and_cache(uint8_t* k_cache, uint8_t* v_cache, const uint16_t* key,
                                  const uint16_t* value, const int64_t* slot_mapping, int num_tokens,
                                  int num_kv_heads, int head_size, int block_size, long long num_blocks,
-                                 float k_scale, float v_scale) {
+                                 float k_scale, float v_scale, int v_shuffled) {
   if (num_tokens < 0 || num_kv_heads <= 0 || head_size <= 0 || head_size % 16 != 0 ||
       block_size <= 0 || num_blocks < 0) {
     return PDA_ORACLE_BAD_SHAPE;
@@ -273,7 +282,8 @@ int pda_oracle_reshape_and_cache(uint8_t* k_cache, uint8_t* v_cache, const uint1
         const float xv = static_cast<float>(bf16_value(value[src])) / v_scale;
         const long long page = (b * num_kv_heads + k) * D * bs;
         k_cache[page + ((d / 16) * bs + o) * 16 + (d % 16)] = e4m3_encode(xk);
-        v_cache[page + d * bs + o] = e4m3_encode(xv);
+        const long long vi = v_shuffled ? ((o / 16) * D + d) * 16 + (o % 16) : d * bs + o;
+        v_cache[page + vi] = e4m3_encode(xv);
       }
     }
   }

@@ -15,6 +15,8 @@ from ._binding import (  # noqa: F401
     PDA_ERR_NOALLOC_CAPACITY,
     PDA_ERR_UNSUPPORTED,
     PDA_ERR_WORKSPACE,
+    PDA_KV_NATIVE,
+    PDA_KV_SHUFFLED_V,
     PDA_OK,
     PDA_OUT_BF16,
     PDA_OUT_E4M3,

@@ -38,14 +38,16 @@ SIGNATURES = {
     "pda_query_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_int)]),
     "pda_set_profile_events": (None, [_P, _P]),
     "pda_test_bounded_wait": (_I, [_I, _P]),
-    "pda_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_longlong, _F, _F, _P]),
+    "pda_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_longlong, _F, _F, _I, _P]),
     "pda_decode_slot_scales": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "pda_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _F, _P]),
-    "pda_decode_ex": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _F, _P, _I, _F, _P]),
+    "pda_decode_ex": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _F, _I, _P, _I, _F, _P]),
 }
 
 PDA_OUT_BF16 = 0
 PDA_OUT_E4M3 = 1
+PDA_KV_NATIVE = 0
+PDA_KV_SHUFFLED_V = 1
 
 _lock = threading.RLock()
 _lib = None
@@ -132,8 +134,9 @@ def _out_like(q, out):
     return out
 
 
-def _check_decode_args(q, k_cache, v_cache, block_tables, seq_lens):
-    if q.dim() != 3 or k_cache.dim() != 5 or v_cache.dim() != 4 or block_tables.dim() != 2 or seq_lens.dim() != 1:
+def _check_decode_args(q, k_cache, v_cache, block_tables, seq_lens, v_shuffled=False):
+    if (q.dim() != 3 or k_cache.dim() != 5 or v_cache.dim() != (5 if v_shuffled else 4) or block_tables.dim() != 2
+            or seq_lens.dim() != 1):
         raise PdaError(PDA_ERR_INVALID_ARG, "decode: tensor ranks")
     if q.dtype != torch.bfloat16 or block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
         raise PdaError(PDA_ERR_INVALID_ARG, "decode: dtypes (q bf16, tables/seq_lens int32)")
@@ -145,7 +148,8 @@ def _check_decode_args(q, k_cache, v_cache, block_tables, seq_lens):
         raise PdaError(PDA_ERR_INVALID_ARG, "decode: tensors must be contiguous CUDA tensors")
     S, H, D = q.shape
     NB, Hk, D16, bs, sixteen = k_cache.shape
-    if (sixteen != 16 or D16 * 16 != D or tuple(v_cache.shape) != (NB, Hk, D, bs)
+    v_want = (NB, Hk, bs // 16, D, 16) if v_shuffled else (NB, Hk, D, bs)
+    if (sixteen != 16 or D16 * 16 != D or tuple(v_cache.shape) != v_want
             or block_tables.shape[0] != S or seq_lens.shape[0] != S):
         raise PdaError(PDA_ERR_INVALID_ARG, "decode: shapes")
 
@@ -172,11 +176,13 @@ def decode_slot_scales(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Te
 
 def decode_ex(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
               seq_lens: torch.Tensor, scale: float, k_scale: float, v_scale: float, *, sinks=None,
-              output_scale: float | None = None, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """``pda_decode_ex``: decode with optional per-head sinks (fp32 ``[H]``) and,
-    when ``output_scale`` is given, e4m3 output ``E4M3(o / output_scale)``."""
+              output_scale: float | None = None, v_shuffled: bool = False, out: torch.Tensor | None = None,
+              stream=None) -> torch.Tensor:
+    """``pda_decode_ex``: decode with optional per-head sinks (fp32 ``[H]``),
+    e4m3 output ``E4M3(o / output_scale)`` when ``output_scale`` is given, and
+    the shuffled V layout ``[NB, Hk, bs/16, 128, 16]`` when ``v_shuffled``."""
     lib = load()
-    _check_decode_args(q, k_cache, v_cache, block_tables, seq_lens)
+    _check_decode_args(q, k_cache, v_cache, block_tables, seq_lens, v_shuffled)
     S, H, D = q.shape
     NB, Hk, _, bs, _ = k_cache.shape
     if sinks is not None and (sinks.dtype != torch.float32 or tuple(sinks.shape) != (H,) or not sinks.is_cuda):
@@ -189,7 +195,9 @@ def decode_ex(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, blo
         raise PdaError(PDA_ERR_INVALID_ARG, "decode_ex: out")
     st = lib.pda_decode_ex(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
                            block_tables.data_ptr(), seq_lens.data_ptr(), S, H, Hk, D, bs, int(block_tables.shape[1]),
-                           float(scale), float(k_scale), float(v_scale), sinks.data_ptr() if sinks is not None else None,
+                           float(scale), float(k_scale), float(v_scale),
+                           PDA_KV_SHUFFLED_V if v_shuffled else PDA_KV_NATIVE,
+                           sinks.data_ptr() if sinks is not None else None,
                            PDA_OUT_E4M3 if fp8 else PDA_OUT_BF16, float(output_scale) if fp8 else 1.0,
                            _stream_ptr(stream))
     _check(st, "pda_decode_ex")
@@ -277,7 +285,8 @@ def bounded_wait_check(timeout_us: int, stream=None) -> None:
 
 
 def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
-                      slot_mapping: torch.Tensor, k_scale: float, v_scale: float, *, stream=None) -> None:
+                      slot_mapping: torch.Tensor, k_scale: float, v_scale: float, *, v_shuffled: bool = False,
+                      stream=None) -> None:
     """Quantise and scatter new tokens into the paged fp8 cache (``pda_reshape_and_cache``).
 
     key / value ``[T, Hk, 128]`` bf16; slot_mapping ``[T]`` int64 (negative =
@@ -296,8 +305,10 @@ def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Ten
         raise PdaError(PDA_ERR_INVALID_ARG, "reshape_and_cache: tensors must be contiguous CUDA tensors")
     T, Hk, D = key.shape
     NB, Hk2, D16, bs, sixteen = k_cache.shape
-    if Hk2 != Hk or D16 * 16 != D or sixteen != 16 or tuple(v_cache.shape) != (NB, Hk, D, bs):
+    v_want = (NB, Hk, bs // 16, D, 16) if v_shuffled else (NB, Hk, D, bs)
+    if Hk2 != Hk or D16 * 16 != D or sixteen != 16 or tuple(v_cache.shape) != v_want:
         raise PdaError(PDA_ERR_INVALID_ARG, "reshape_and_cache: shapes")
     _check(lib.pda_reshape_and_cache(key.data_ptr(), value.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
                                      slot_mapping.data_ptr(), T, Hk, D, bs, NB, float(k_scale), float(v_scale),
-                                     _stream_ptr(stream)), "pda_reshape_and_cache")
+                                     PDA_KV_SHUFFLED_V if v_shuffled else PDA_KV_NATIVE, _stream_ptr(stream)),
+           "pda_reshape_and_cache")

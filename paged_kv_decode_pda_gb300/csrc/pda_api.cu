@@ -186,7 +186,7 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
                                 const int32_t* seq_lens, int num_seqs, int num_heads, int num_kv_heads,
                                 int head_size, int block_size, int max_num_blocks_per_seq, float scale,
                                 float k_scale, float v_scale, cudaStream_t stream, const float* sinks = nullptr,
-                                int out_fp8 = 0, float out_scale = 1.f) {
+                                int out_fp8 = 0, float out_scale = 1.f, int v_shuffled = 0) {
   pda_status st = validate(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_heads, num_kv_heads,
                            head_size, block_size, max_num_blocks_per_seq, scale, k_scale, v_scale);
   if (st != PDA_OK || num_seqs == 0) return st;
@@ -229,6 +229,7 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
   p.sinks = sinks;
   p.out_fp8 = out_fp8;
   p.out_scale = out_scale;
+  p.v_shuffled = v_shuffled;
 
   cudaEvent_t eb = g_prof_before.load(), ea = g_prof_after.load();
   if (eb && ea && record_profile_event(eb, stream) != cudaSuccess) return PDA_ERR_CUDA;
@@ -378,10 +379,11 @@ pda_status pda_test_bounded_wait(int timeout_us, cudaStream_t stream) {
 
 pda_status pda_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
                                  const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_size,
-                                 int block_size, long long num_blocks, float k_scale, float v_scale,
+                                 int block_size, long long num_blocks, float k_scale, float v_scale, int kv_layout,
                                  cudaStream_t stream) {
   if (num_tokens < 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 || num_blocks < 0)
     return PDA_ERR_INVALID_ARG;
+  if (kv_layout != PDA_KV_NATIVE && kv_layout != PDA_KV_SHUFFLED_V) return PDA_ERR_INVALID_ARG;
   if (!std::isfinite(k_scale) || !std::isfinite(v_scale) || k_scale == 0.f || v_scale == 0.f)
     return PDA_ERR_INVALID_ARG;
   if (head_size != kHeadDim) return PDA_ERR_UNSUPPORTED;
@@ -403,6 +405,7 @@ pda_status pda_reshape_and_cache(const void* key, const void* value, void* k_cac
   p.num_slots = num_blocks * (long long)block_size;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
+  p.v_shuffled = kv_layout == PDA_KV_SHUFFLED_V ? 1 : 0;
   const long long items = (long long)num_tokens * num_kv_heads;
   const long long blocks = (items + pda::kCacheWriteWarps - 1) / pda::kCacheWriteWarps;
   if (blocks > 0x7FFFFFFFLL) return PDA_ERR_UNSUPPORTED;
@@ -422,15 +425,16 @@ pda_status pda_decode(void* out, const void* q, const void* k_cache, const void*
 pda_status pda_decode_ex(void* out, const void* q, const void* k_cache, const void* v_cache,
                          const int32_t* block_tables, const int32_t* seq_lens, int num_seqs, int num_heads,
                          int num_kv_heads, int head_size, int block_size, int max_num_blocks_per_seq, float scale,
-                         float k_scale, float v_scale, const float* sinks, int out_dtype, float output_scale,
-                         cudaStream_t stream) {
+                         float k_scale, float v_scale, int kv_layout, const float* sinks, int out_dtype,
+                         float output_scale, cudaStream_t stream) {
+  if (kv_layout != PDA_KV_NATIVE && kv_layout != PDA_KV_SHUFFLED_V) return PDA_ERR_INVALID_ARG;
   if (out_dtype != PDA_OUT_BF16 && out_dtype != PDA_OUT_E4M3) return PDA_ERR_INVALID_ARG;
   if (out_dtype == PDA_OUT_E4M3 && !(std::isfinite(output_scale) && output_scale > 0.f)) return PDA_ERR_INVALID_ARG;
   if (sinks && (reinterpret_cast<uintptr_t>(sinks) & 3u)) return PDA_ERR_INVALID_ARG;
   return launch_decode(false, out, q, k_cache, v_cache, nullptr, nullptr, block_tables, seq_lens, num_seqs,
                        num_heads, num_kv_heads, head_size, block_size, max_num_blocks_per_seq, scale, k_scale,
                        v_scale, stream, sinks, out_dtype == PDA_OUT_E4M3 ? 1 : 0,
-                       out_dtype == PDA_OUT_E4M3 ? output_scale : 1.f);
+                       out_dtype == PDA_OUT_E4M3 ? output_scale : 1.f, kv_layout == PDA_KV_SHUFFLED_V ? 1 : 0);
 }
 
 pda_status pda_decode_slot_scales(void* out, const void* q, const void* k_cache, const void* v_cache,

@@ -70,6 +70,7 @@ struct DecodeParams {
   const float* v_scales;        // [NB][Hk][bs] fp32 (slot-scale variant)
   float logit_scale_log2;       // scale * k_scale * log2(e)  (scale * log2(e) with slot scales)
   float v_scale;                // per-tensor V scale (unused with slot scales)
+  int v_shuffled = 0;           // 1: V pages are [bs/16][D][16] (AITER shuffled), else [D][bs]
   const float* sinks = nullptr; // [H] per-head sink logits (scale * q.k units), or none
   int out_fp8 = 0;              // 1: out holds E4M3(o / out_scale) bytes
   float out_scale = 1.f;
@@ -276,7 +277,12 @@ __global__ void __launch_bounds__(kThreads, 3) pda_split_decode_kernel(const Dec
   // ldmatrix row assignment. K: lane l supplies token row_token(l & 15) of
   // chunk (2kk + (l >> 4)). V: lane l supplies dim (32mp + l).
   const uint32_t k_lane_off = (uint32_t)(row_token(lane & 15) * 16) + (uint32_t)((lane >> 4) * bs * 16);
-  const uint32_t v_lane_off = (uint32_t)(lane * bs);
+  // V: a 16-token tile is 128 rows of 16 bytes at stride v_row (bs for
+  // [D][bs] pages; 16 for shuffled [bs/16][D][16] pages, whose tiles are
+  // contiguous and so bank-conflict free for any block size).
+  const uint32_t v_row = p.v_shuffled ? 16u : (uint32_t)bs;
+  const uint32_t v_sub = p.v_shuffled ? (uint32_t)(kHeadDim * 16) : 16u;
+  const uint32_t v_lane_off = (uint32_t)lane * v_row;
   const bool low_quad = tig < 2;
   const int tokA = row_token(gid);
   const int tokB = row_token(gid + 8);
@@ -325,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 3) pda_split_decode_kernel(const Dec
       const int tok0 = (fill_first_page + pg) * bs + sub * 16;
       if (tok0 >= L) continue;
       const uint32_t kbase = sbase + (uint32_t)pg * page_bytes + (uint32_t)(sub * 256);
-      const uint32_t vbase = sbase + (uint32_t)(PPS + pg) * page_bytes + (uint32_t)(sub * 16);
+      const uint32_t vbase = sbase + (uint32_t)(PPS + pg) * page_bytes + (uint32_t)sub * v_sub;
 
       // ---- S^T = K_tile * Q^T (two independent accumulator chains)
       float sc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -402,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 3) pda_split_decode_kernel(const Dec
       uint32_t vr[kChunks / 2][4];
 #pragma unroll
       for (int mp = 0; mp < kChunks / 2; ++mp)
-        ldsm_x4(vbase + v_lane_off + (uint32_t)(32 * mp * bs), vr[mp][0], vr[mp][1], vr[mp][2], vr[mp][3]);
+        ldsm_x4(vbase + v_lane_off + (uint32_t)(32 * mp) * v_row, vr[mp][0], vr[mp][1], vr[mp][2], vr[mp][3]);
       const int n_valid = L - tok0;
       if (n_valid < 16) {
         // Zero the V bytes of tokens >= L: their e4m3 codes may be NaN and
@@ -558,7 +564,8 @@ __global__ void pda_bounded_wait_test_kernel(unsigned long long limit_ns) {
 // vllm.v1.attention.backends.rocm_aiter_unified_attn, do_kv_cache_update ->
 // reshape_and_cache). One warp per (token, kv head), 4 dims per lane:
 //   K bytes -> k_cache[b][k][d/16][o][d%16]   (one 4-byte store per lane)
-//   V bytes -> v_cache[b][k][d][o]            (four byte stores per lane)
+//   V bytes -> v_cache[b][k][d][o]            (four byte stores per lane), or
+//              v_cache[b][k][o/16][d][o%16]   for the shuffled V layout
 // with b = slot / bs, o = slot % bs. The code is decided on the IEEE binary32
 // quotient x / scale. Negative slots are padding; slots past the pool are
 // skipped and flagged in the status word.
@@ -574,6 +581,7 @@ struct CacheWriteParams {
   long long num_slots;           // num_blocks * block_size
   float k_scale;
   float v_scale;
+  int v_shuffled = 0;            // 1: V pages are [bs/16][D][16]
 };
 
 constexpr int kCacheWriteWarps = 8;
@@ -603,9 +611,11 @@ __global__ void __launch_bounds__(kCacheWriteWarps * 32) pda_reshape_and_cache_k
   const size_t page = ((size_t)b * p.num_kv_heads + k) * (size_t)kHeadDim * p.block_size;
   const int d0 = 4 * lane;
   *reinterpret_cast<uint32_t*>(p.k_cache + page + ((size_t)(d0 / 16) * p.block_size + o) * 16 + (d0 % 16)) = kq;
-  uint8_t* vrow = p.v_cache + page + (size_t)d0 * p.block_size + o;
+  const size_t vstride = p.v_shuffled ? 16 : (size_t)p.block_size;
+  uint8_t* vrow = p.v_cache + page +
+                  (p.v_shuffled ? ((size_t)(o / 16) * kHeadDim + d0) * 16 + (o % 16) : (size_t)d0 * p.block_size + o);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) vrow[(size_t)i * p.block_size] = (uint8_t)(vq >> (8 * i));
+  for (int i = 0; i < 4; ++i) vrow[(size_t)i * vstride] = (uint8_t)(vq >> (8 * i));
 }
 
 }  // namespace pda

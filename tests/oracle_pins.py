@@ -323,6 +323,38 @@ def pin_slot_scales(lib):
         assert np.array_equal(a, b)
 
 
+# ------------------------------------------------------- shuffled V layout
+
+def shuffle_v(v_native: np.ndarray) -> np.ndarray:
+    """[NB, Hk, D, bs] -> AITER-shuffled [NB, Hk, bs/16, D, 16] (same bytes at bs 16)."""
+    NB, Hk, D, bs = v_native.shape
+    return np.ascontiguousarray(v_native.reshape(NB, Hk, D, bs // 16, 16).transpose(0, 1, 3, 2, 4))
+
+
+def pin_shuffled_v(lib):
+    for (S, Hq, Hk, lens, bs) in ((3, 8, 2, [5, 40, 33], 16), (2, 16, 2, [70, 64], 64), (2, 8, 8, [129, 1], 32)):
+        qbits, Kc, Vc = dense_case(S, Hq, Hk, lens, seed=111)
+        kc, vc, tb, ln = scatter_pages(Kc, Vc, lens, bs, seed=17, extra_cols=1)
+        a = run(lib, qbits, kc, vc, tb, ln, 0.09, 0.05, 0.05)
+        b = oracle.decode(qbits, kc, shuffle_v(vc), tb, ln, scale=0.09, k_scale=0.05, v_scale=0.05,
+                          v_shuffled=True, lib=lib)
+        assert np.array_equal(a, b), "shuffled V must read the same values as native V"
+        ref = dense_reference(qbits, Kc, Vc, lens, 0.09, 0.05, 0.05)
+        assert np.max(np.abs(b - ref)) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
+    # the cache writer lays out the same bytes in both layouts
+    rng = np.random.default_rng(113)
+    T, Hk, bs, NB = 40, 2, 64, 2
+    key = torch.from_numpy(rng.standard_normal((T, Hk, 128)).astype(np.float32)).to(torch.bfloat16)
+    kb = key.view(torch.int16).numpy().view(np.uint16).copy()
+    slots = rng.permutation(NB * bs)[:T].astype(np.int64)
+    kc = np.zeros((NB, Hk, 8, bs, 16), dtype=np.uint8)
+    v1 = np.zeros((NB, Hk, 128, bs), dtype=np.uint8)
+    v2 = np.zeros((NB, Hk, bs // 16, 128, 16), dtype=np.uint8)
+    oracle.reshape_and_cache(kc, v1, kb, kb, slots, k_scale=0.05, v_scale=0.05, lib=lib)
+    oracle.reshape_and_cache(kc.copy(), v2, kb, kb, slots, k_scale=0.05, v_scale=0.05, v_shuffled=True, lib=lib)
+    assert np.array_equal(shuffle_v(v1), v2)
+
+
 # ----------------------------------------------------- sinks, fp8 output
 
 def pin_sinks(lib):
@@ -474,4 +506,4 @@ def pin_quantise_in_binary32(lib):
 
 ALL_PINS = [pin_e4m3_table, pin_bf16, pin_dense, pin_large_logits, pin_permutation_invariance,
             pin_constant_v, pin_single_token, pin_zero_k, pin_tail_poison, pin_gqa_is_repeated_mha,
-            pin_zero_length, pin_slot_scales, pin_sinks, pin_quantize_output, pin_e4m3_encode, pin_reshape_and_cache, pin_quantise_in_binary32]
+            pin_zero_length, pin_slot_scales, pin_shuffled_v, pin_sinks, pin_quantize_output, pin_e4m3_encode, pin_reshape_and_cache, pin_quantise_in_binary32]

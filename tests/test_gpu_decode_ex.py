@@ -110,6 +110,54 @@ def test_ex_rejects_bad_options():
     args = [batch.q.data_ptr(), batch.q.data_ptr(), batch.k_cache.data_ptr(), batch.v_cache.data_ptr(),
             batch.block_tables.data_ptr(), batch.seq_lens.data_ptr(), cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads,
             128, 16, int(batch.block_tables.shape[1]), cfg.scale, cfg.k_scale, cfg.v_scale]
-    assert lib.pda_decode_ex(*args, None, 7, 1.0, None) == pda.PDA_ERR_INVALID_ARG
-    assert lib.pda_decode_ex(*args, None, pda.PDA_OUT_E4M3, 0.0, None) == pda.PDA_ERR_INVALID_ARG
-    assert lib.pda_decode_ex(*args, None, pda.PDA_OUT_E4M3, float("nan"), None) == pda.PDA_ERR_INVALID_ARG
+    assert lib.pda_decode_ex(*args, 0, None, 7, 1.0, None) == pda.PDA_ERR_INVALID_ARG
+    assert lib.pda_decode_ex(*args, 0, None, pda.PDA_OUT_E4M3, 0.0, None) == pda.PDA_ERR_INVALID_ARG
+    assert lib.pda_decode_ex(*args, 0, None, pda.PDA_OUT_E4M3, float("nan"), None) == pda.PDA_ERR_INVALID_ARG
+    assert lib.pda_decode_ex(*args, 5, None, pda.PDA_OUT_BF16, 1.0, None) == pda.PDA_ERR_INVALID_ARG
+
+
+# ------------------------------------------------------- shuffled V layout
+
+def _shuffle_v(v):
+    NB, Hk, D, bs = v.shape
+    return v.reshape(NB, Hk, D, bs // 16, 16).permute(0, 1, 3, 2, 4).contiguous()
+
+
+@pytest.mark.parametrize("bs,splits", [(16, 0), (32, 3), (64, 0), (64, 12), (128, 2)])
+def test_shuffled_v_parity_and_equal_to_native(bs, splits):
+    batch = workloads.make_custom(5, 32, 8, [1, 77, 1024, 513, 300], block_size=bs, pool_factor=1.3, seed=53 + bs,
+                                  device=DEV)
+    cfg = batch.cfg
+    v_sh = _shuffle_v(batch.v_cache)
+    pda.set_split_override(splits)
+    try:
+        a = pda.decode_ex(batch.q, batch.k_cache, v_sh, batch.block_tables, batch.seq_lens, cfg.scale, cfg.k_scale,
+                          cfg.v_scale, v_shuffled=True)
+        b = U.run_cuda(batch)
+        torch.cuda.synchronize()
+    finally:
+        pda.set_split_override(0)
+    assert torch.equal(a, b), "the two V layouts hold the same values"
+    raw = batch.raw()
+    raw["v_cache"] = v_sh.cpu().contiguous().view(torch.uint8).numpy()
+    ref = oracle.decode(**raw, scale=cfg.scale, k_scale=cfg.k_scale, v_scale=cfg.v_scale, v_shuffled=True)
+    U.compare(a, ref, "shuffled V bs=%d" % bs)
+
+
+@pytest.mark.parametrize("bs", [16, 64])
+def test_cache_write_shuffled_v_bit_exact(bs):
+    g = torch.Generator().manual_seed(bs)
+    T, Hk, NB = 100, 4, 8
+    key = (torch.randn(T, Hk, 128, generator=g) * 2).to(torch.bfloat16)
+    val = (torch.randn(T, Hk, 128, generator=g) * 2).to(torch.bfloat16)
+    slots = torch.randperm(NB * bs, generator=g)[:T].to(torch.int64)
+    kc = torch.randint(0, 256, (NB, Hk, 8, bs, 16), generator=g, dtype=torch.uint8)
+    vc = torch.randint(0, 256, (NB, Hk, bs // 16, 128, 16), generator=g, dtype=torch.uint8)
+    kr, vr = kc.numpy().copy(), vc.numpy().copy()
+    oracle.reshape_and_cache(kr, vr, key.view(torch.int16).numpy().view(np.uint16),
+                             val.view(torch.int16).numpy().view(np.uint16), slots.numpy(), k_scale=0.05,
+                             v_scale=0.05, v_shuffled=True)
+    kd, vd = kc.to(DEV), vc.to(DEV)
+    pda.reshape_and_cache(key.to(DEV), val.to(DEV), kd, vd, slots.to(DEV), 0.05, 0.05, v_shuffled=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(kd.cpu().numpy(), kr) and np.array_equal(vd.cpu().numpy(), vr)

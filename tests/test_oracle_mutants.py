@@ -17,13 +17,12 @@ SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), 
 
 MUTANTS = {
     "dropped_k_scale": ("acc += qd[d] * (e4m3[code] * ks);", "acc += qd[d] * e4m3[code];"),
-    "dropped_v_scale": ("(e4m3[vpage[static_cast<long long>(d) * bs + slot]] * vs)",
-                        "e4m3[vpage[static_cast<long long>(d) * bs + slot]]"),
+    "dropped_v_scale": ("o[d] += wt * (e4m3[vpage[vi]] * vs);", "o[d] += wt * e4m3[vpage[vi]];"),
     "dropped_softmax_scale": ("z[t] = scale * acc;", "z[t] = acc;"),
     "wrong_sign": ("z[t] = scale * acc;", "z[t] = -scale * acc;"),
     "k_page_token_major": ("kpage[(static_cast<long long>(d / 16) * bs + slot) * 16 + (d % 16)]",
                            "kpage[(slot * (D / 16) + d / 16) * 16 + (d % 16)]"),
-    "v_page_token_major": ("vpage[static_cast<long long>(d) * bs + slot]", "vpage[slot * D + d]"),
+    "v_page_token_major": (": static_cast<long long>(d) * bs + slot;", ": slot * D + d;"),
     "gqa_modulo": ("const int kv = h / g;", "const int kv = h % num_kv_heads;"),
     "e4m3_bias_8": ("mag = std::ldexp(1.0 + static_cast<double>(mant) / 8.0, expo - 7);",
                     "mag = std::ldexp(1.0 + static_cast<double>(mant) / 8.0, expo - 8);"),
@@ -42,9 +41,11 @@ MUTANTS = {
                                      "const float xv = static_cast<float>(bf16_value(value[src])) * v_scale;"),
     "cache_write_k_token_major": ("k_cache[page + ((d / 16) * bs + o) * 16 + (d % 16)]",
                                   "k_cache[page + (o * (D / 16) + d / 16) * 16 + (d % 16)]"),
-    "cache_write_v_token_major": ("v_cache[page + d * bs + o]", "v_cache[page + o * D + d]"),
+    "cache_write_v_token_major": (": d * bs + o;", ": o * D + d;"),
     "slot_scale_wrong_head": ("k_scales[(b * num_kv_heads + kv) * bs + slot]", "k_scales[(b * num_kv_heads + 0) * bs + slot]"),
     "slot_scale_wrong_slot": ("v_scales[(b * num_kv_heads + kv) * bs + slot]", "v_scales[(b * num_kv_heads + kv) * bs]"),
+    "shuffled_v_dim_token_swapped": ("const long long vi = v_shuffled ? ((slot / 16) * D + d) * 16 + (slot % 16)",
+                                      "const long long vi = v_shuffled ? ((slot / 16) * D + (slot % 16)) * 16 + d % 16"),
     "sink_carries_value": ("double denom = sinks ? std::exp(zs - zmax) : 0.0;", "double denom = 0.0;"),
 }
 
