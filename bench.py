@@ -54,10 +54,10 @@ def parse():
     ap.add_argument("--config", default=workloads.HEADLINE, choices=sorted(workloads.CONFIGS))
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--variant", choices=["plain", "slot_scales", "ex", "shuffled_v"], default="plain",
+    ap.add_argument("--variant", choices=["plain", "slot_scales", "ex", "shuffled_v", "strided_nhd"], default="plain",
                     help="decode entry point: pda_decode, pda_decode_slot_scales (per-slot tables), "
-                         "pda_decode_ex with per-head sinks and e4m3 output, or pda_decode_ex on the "
-                         "shuffled V layout")
+                         "pda_decode_ex with per-head sinks and e4m3 output, pda_decode_ex on the "
+                         "shuffled V layout, or pda_decode_strided on [NB, bs, Hk, 128] K and V")
     ap.add_argument("--op", choices=["decode", "cache_write"], default="decode",
                     help="cache_write: time pda_reshape_and_cache on --tokens new tokens of the config's kv heads")
     ap.add_argument("--tokens", type=int, default=65536)
@@ -263,9 +263,24 @@ def run_ours(args, ws, rank, local):
             return v.reshape(NB, Hk, D, bs // 16, 16).permute(0, 1, 3, 2, 4).contiguous()
         caches = [(k, shuffle(v)) for k, v in caches]
 
+    elif args.variant == "strided_nhd":
+        def nhd(k, v):
+            NB, Hk, C, bs, _ = k.shape
+            kt = k.view(torch.uint8).permute(0, 3, 1, 2, 4).reshape(NB, bs, Hk, 128).contiguous()
+            vt = v.view(torch.uint8).permute(0, 3, 1, 2).contiguous()
+            return kt, vt
+        caches = [nhd(k, v) for k, v in caches]
+        hk, bsz = cfg.num_kv_heads, cfg.block_size
+        nhd_strides = (bsz * hk * 128, hk * 128, 128)
+
     def call(i):
         kc, vc = caches[i % replicas]
-        if args.variant == "shuffled_v":
+        if args.variant == "strided_nhd":
+            pda.decode_strided(batch.q, kc.data_ptr(), vc.data_ptr(), batch.block_tables, batch.seq_lens, cfg.scale,
+                               cfg.k_scale, cfg.v_scale, num_kv_heads=hk, block_size=bsz,
+                               num_blocks=batch.num_blocks, k_strides=nhd_strides, v_strides=nhd_strides, out=out,
+                               stream=stream)
+        elif args.variant == "shuffled_v":
             pda.decode_ex(batch.q, kc, vc, batch.block_tables, batch.seq_lens, cfg.scale, cfg.k_scale, cfg.v_scale,
                           v_shuffled=True, out=out, stream=stream)
         elif args.variant == "slot_scales":
@@ -455,7 +470,7 @@ def run_reference(args, ws, rank, local):
     batch = workloads.make_batch(cfg, device="cpu")
     raw = batch.raw()
     # Size each step so the whole run stays within about three minutes.
-    budget_total = 180.0
+    budget_total = 120.0
     per_step = max(0.02, budget_total / max(1, args.steps + args.warmup))
     _, _, cores, n, dt = oracle_sample_rate(batch, budget_s=per_step)
     ids = list(range(n))

@@ -160,6 +160,44 @@ pda_status pda_decode_ex(void* out, const void* q, const void* k_cache, const vo
                          float output_scale, cudaStream_t stream);
 
 /*
+ * pda_decode_strided -- pda_decode on token-major ("flash" / NHD family)
+ * caches given by byte strides.
+ *
+ * Source: the vLLM API page "vllm.v1.attention.backends.rocm_aiter_unified_attn":
+ * the backend's kv_cache is documented as [num_blocks, 2, block_size,
+ * num_kv_heads, head_size], its _split_kv_cache turns a (blocks, heads,
+ * tokens, 2*head_size) tensor into K and V views of shape (blocks, tokens,
+ * heads, head_size) ("keep K and V packed in the content dim"), and it
+ * supports the LBHNC and LHBNC layouts. In all of these the head_size bytes
+ * of one (block, token, kv head) are contiguous and everything else is a
+ * stride, so one entry point covers them:
+ *
+ *   K row of (block b, token t, kv head h) = k_cache + b*k_block_stride
+ *                                           + t*k_token_stride + h*k_head_stride
+ *   (V likewise with v_cache and the v_* strides), head_size = 128 bytes, e4m3.
+ *
+ * Examples (bytes; D = 128):
+ *   [NB, bs, Hk, D] for K and for V:  block bs*Hk*D, token Hk*D, head D
+ *   [NB, 2, bs, Hk, D]:               K = base, V = base + bs*Hk*D;
+ *                                     block 2*bs*Hk*D, token Hk*D, head D
+ *   [NB, Hk, bs, 2*D] (K|V packed):   K = base, V = base + D;
+ *                                     block Hk*bs*2*D, token 2*D, head bs*2*D
+ *
+ * num_blocks bounds the block index (pages are read through TMA tensor maps
+ * built from these strides; a block id outside [0, num_blocks) reads zeros).
+ * Strides must be positive multiples of 16 that nest without overlap once
+ * sorted (smallest >= 128), and K and V must sort in the same order; else
+ * PDA_ERR_UNSUPPORTED. Everything else is pda_decode's.
+ */
+pda_status pda_decode_strided(void* out, const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, const int32_t* seq_lens, int num_seqs, int num_heads,
+                              int num_kv_heads, int head_size, int block_size, int max_num_blocks_per_seq,
+                              long long num_blocks, long long k_block_stride, long long k_token_stride,
+                              long long k_head_stride, long long v_block_stride, long long v_token_stride,
+                              long long v_head_stride, float scale, float k_scale, float v_scale,
+                              cudaStream_t stream);
+
+/*
  * pda_decode_slot_scales -- pda_decode with per-slot dequantisation scales.
  *
  * Source: vLLM pull request lishuoshuo-amd/vllm#3, "Details", item "Scale

@@ -26,6 +26,7 @@ from ._binding import (  # noqa: F401
     decode_ex,
     decode_noalloc,
     decode_slot_scales,
+    decode_strided,
     decode_raw,
     load,
     plan_splits,

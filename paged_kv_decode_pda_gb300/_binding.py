@@ -42,6 +42,8 @@ SIGNATURES = {
     "pda_decode_slot_scales": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "pda_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _F, _P]),
     "pda_decode_ex": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _F, _I, _P, _I, _F, _P]),
+    "pda_decode_strided": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I] + [ctypes.c_longlong] * 7
+                           + [_F, _F, _F, _P]),
 }
 
 PDA_OUT_BF16 = 0
@@ -201,6 +203,33 @@ def decode_ex(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, blo
                            PDA_OUT_E4M3 if fp8 else PDA_OUT_BF16, float(output_scale) if fp8 else 1.0,
                            _stream_ptr(stream))
     _check(st, "pda_decode_ex")
+    return out
+
+
+def decode_strided(q: torch.Tensor, k_rows_base: int, v_rows_base: int, block_tables: torch.Tensor,
+                   seq_lens: torch.Tensor, scale: float, k_scale: float, v_scale: float, *, num_kv_heads: int,
+                   block_size: int, num_blocks: int, k_strides, v_strides, out: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    """``pda_decode_strided``: decode on a token-major fp8 cache.
+
+    ``k_rows_base`` / ``v_rows_base`` are device addresses of the (block 0,
+    token 0, head 0) rows; ``k_strides`` / ``v_strides`` are byte strides
+    (block, token, kv head); every row holds 128 contiguous e4m3 bytes.
+    """
+    lib = load()
+    if q.dim() != 3 or q.dtype != torch.bfloat16 or not q.is_cuda or not q.is_contiguous():
+        raise PdaError(PDA_ERR_INVALID_ARG, "decode_strided: q")
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise PdaError(PDA_ERR_INVALID_ARG, "decode_strided: tables / seq_lens dtype")
+    out = _out_like(q, out)
+    S, H, D = q.shape
+    kb, kt, kh = (int(x) for x in k_strides)
+    vb, vt, vh = (int(x) for x in v_strides)
+    st = lib.pda_decode_strided(out.data_ptr(), q.data_ptr(), int(k_rows_base), int(v_rows_base),
+                                block_tables.data_ptr(), seq_lens.data_ptr(), S, H, int(num_kv_heads), D,
+                                int(block_size), int(block_tables.shape[1]), int(num_blocks), kb, kt, kh, vb, vt, vh,
+                                float(scale), float(k_scale), float(v_scale), _stream_ptr(stream))
+    _check(st, "pda_decode_strided")
     return out
 
 

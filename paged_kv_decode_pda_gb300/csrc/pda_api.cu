@@ -1,6 +1,7 @@
 // C ABI of the fp8 paged decode attention library (see include/pda.h):
 // argument validation, the split-count heuristic, the per-stream workspace,
 // and the launches of the split-KV decode and merge kernels.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -57,11 +58,85 @@ RingShape ring_shape(int bs, bool slot_scales = false) {
   size_t ring = (size_t)r.num_stages * r.stage_bytes;
   size_t merge = (size_t)pda::kConsumerWarps * pda::kMaxGqa * (pda::kMergeStride + 2) * sizeof(float);
   if (ring < merge) ring = merge;
-  r.smem_bytes = ring + 2 * 8 * (size_t)r.num_stages + 16;
+  // + 1 KiB so the kernel can align the ring to 1024 bytes (128-byte swizzle).
+  r.smem_bytes = ring + 2 * 8 * (size_t)r.num_stages + 16 + 1024;
   return r;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Placeholder tensor maps for the page-major kernels (never dereferenced).
+const CUtensorMap g_no_map = {};
+
+// ---- token-major (strided) caches: tensor maps built on the host per call.
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver, looked up once (no libcuda link).
+EncodeTiledFn encode_tiled() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+struct TokenMajorMaps {
+  CUtensorMap k;
+  CUtensorMap v;
+  int dim_token, dim_head, dim_block;  // positions 1..3 in both maps
+};
+
+// One 4-D map over a cache whose row of 128 bytes for (block b, token t,
+// kv head h) starts at base + b*sb + t*st + h*sh. Dimension 0 is the row's
+// bytes; dimensions 1..3 are token, head and block sorted by stride, which
+// must nest without overlap. The box is one page: all bs tokens of one
+// (block, head), landing as [bs][128] with 128-byte swizzle.
+pda_status make_token_major_map(const void* base, long long nb, int hk, int bs, long long sb, long long st,
+                                long long sh, CUtensorMap* map, int* pos_token, int* pos_head, int* pos_block) {
+  struct D {
+    long long stride, extent;
+    int what;  // 0 token, 1 head, 2 block
+  } d[3] = {{st, bs, 0}, {sh, hk, 1}, {sb, nb, 2}};
+  for (auto& x : d)
+    if (x.stride <= 0 || (x.stride & 15) != 0 || x.extent <= 0 || x.extent > (1LL << 32) || x.stride >= (1LL << 40))
+      return PDA_ERR_INVALID_ARG;
+  for (int i = 0; i < 3; ++i)
+    for (int j = i + 1; j < 3; ++j)
+      if (d[j].stride < d[i].stride) std::swap(d[i], d[j]);
+  if (d[0].stride < kHeadDim || d[1].stride < d[0].stride * d[0].extent || d[2].stride < d[1].stride * d[1].extent)
+    return PDA_ERR_UNSUPPORTED;  // rows overlap: not a layout a tensor map can describe
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return PDA_ERR_CUDA;
+  cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)d[0].extent, (cuuint64_t)d[1].extent,
+                        (cuuint64_t)d[2].extent};
+  cuuint64_t strides[3] = {(cuuint64_t)d[0].stride, (cuuint64_t)d[1].stride, (cuuint64_t)d[2].stride};
+  cuuint32_t box[4] = {(cuuint32_t)kHeadDim, 1, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  for (int i = 0; i < 3; ++i) {
+    if (d[i].what == 0) {
+      box[1 + i] = (cuuint32_t)bs;
+      *pos_token = 1 + i;
+    } else if (d[i].what == 1) {
+      *pos_head = 1 + i;
+    } else {
+      *pos_block = 1 + i;
+    }
+  }
+  if (enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return PDA_ERR_INVALID_ARG;
+  return PDA_OK;
+}
 
 pda_status validate(const void* out, const void* q, const void* k_cache, const void* v_cache,
                     const int32_t* block_tables, const int32_t* seq_lens, int num_seqs, int num_heads,
@@ -104,9 +179,11 @@ pda_status device_info(int dev, int bs, int* sm_count, int* ctas_per_sm, bool sl
         mx = s > mx ? s : mx;
       }
     }
-    if (cudaFuncSetAttribute(pda::pda_split_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(pda::pda_split_decode_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)mx) != cudaSuccess ||
-        cudaFuncSetAttribute(pda::pda_split_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(pda::pda_split_decode_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)mx) != cudaSuccess ||
+        cudaFuncSetAttribute(pda::pda_split_decode_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)mx) != cudaSuccess)
       return PDA_ERR_CUDA;
     di.smem_attr_set = true;
@@ -115,9 +192,9 @@ pda_status device_info(int dev, int bs, int* sm_count, int* ctas_per_sm, bool sl
   if (occ == 0) {
     int n = 0;
     const cudaError_t e =
-        slot_scales ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pda::pda_split_decode_kernel<true>,
+        slot_scales ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pda::pda_split_decode_kernel<true, false>,
                                                                     pda::kThreads, ring_shape(bs, true).smem_bytes)
-                    : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pda::pda_split_decode_kernel<false>,
+                    : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pda::pda_split_decode_kernel<false, false>,
                                                                     pda::kThreads, ring_shape(bs).smem_bytes);
     if (e != cudaSuccess) return PDA_ERR_CUDA;
     occ = n > 0 ? n : 1;
@@ -186,7 +263,8 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
                                 const int32_t* seq_lens, int num_seqs, int num_heads, int num_kv_heads,
                                 int head_size, int block_size, int max_num_blocks_per_seq, float scale,
                                 float k_scale, float v_scale, cudaStream_t stream, const float* sinks = nullptr,
-                                int out_fp8 = 0, float out_scale = 1.f, int v_shuffled = 0) {
+                                int out_fp8 = 0, float out_scale = 1.f, int v_shuffled = 0,
+                                const TokenMajorMaps* tm = nullptr) {
   pda_status st = validate(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_heads, num_kv_heads,
                            head_size, block_size, max_num_blocks_per_seq, scale, k_scale, v_scale);
   if (st != PDA_OK || num_seqs == 0) return st;
@@ -230,14 +308,21 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
   p.out_fp8 = out_fp8;
   p.out_scale = out_scale;
   p.v_shuffled = v_shuffled;
+  if (tm) {
+    p.tm_dim_token = tm->dim_token;
+    p.tm_dim_head = tm->dim_head;
+    p.tm_dim_block = tm->dim_block;
+  }
 
   cudaEvent_t eb = g_prof_before.load(), ea = g_prof_after.load();
   if (eb && ea && record_profile_event(eb, stream) != cudaSuccess) return PDA_ERR_CUDA;
   dim3 grid((unsigned)nsplit, (unsigned)num_kv_heads, (unsigned)num_seqs);
-  if (slot)
-    pda::pda_split_decode_kernel<true><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(p);
+  if (tm)
+    pda::pda_split_decode_kernel<false, true><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(p, tm->k, tm->v);
+  else if (slot)
+    pda::pda_split_decode_kernel<true, false><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(p, g_no_map, g_no_map);
   else
-    pda::pda_split_decode_kernel<false><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(p);
+    pda::pda_split_decode_kernel<false, false><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(p, g_no_map, g_no_map);
   if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
   if (eb && ea && record_profile_event(ea, stream) != cudaSuccess) return PDA_ERR_CUDA;
 
@@ -437,6 +522,31 @@ pda_status pda_decode_ex(void* out, const void* q, const void* k_cache, const vo
                        out_dtype == PDA_OUT_E4M3 ? output_scale : 1.f, kv_layout == PDA_KV_SHUFFLED_V ? 1 : 0);
 }
 
+pda_status pda_decode_strided(void* out, const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, const int32_t* seq_lens, int num_seqs, int num_heads,
+                              int num_kv_heads, int head_size, int block_size, int max_num_blocks_per_seq,
+                              long long num_blocks, long long k_block_stride, long long k_token_stride,
+                              long long k_head_stride, long long v_block_stride, long long v_token_stride,
+                              long long v_head_stride, float scale, float k_scale, float v_scale,
+                              cudaStream_t stream) {
+  pda_status st = validate(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_heads, num_kv_heads,
+                           head_size, block_size, max_num_blocks_per_seq, scale, k_scale, v_scale);
+  if (st != PDA_OK || num_seqs == 0) return st;
+  if (num_blocks <= 0) return PDA_ERR_INVALID_ARG;
+  TokenMajorMaps tm;
+  int vt = 0, vh = 0, vb = 0;
+  st = make_token_major_map(k_cache, num_blocks, num_kv_heads, block_size, k_block_stride, k_token_stride,
+                            k_head_stride, &tm.k, &tm.dim_token, &tm.dim_head, &tm.dim_block);
+  if (st != PDA_OK) return st;
+  st = make_token_major_map(v_cache, num_blocks, num_kv_heads, block_size, v_block_stride, v_token_stride,
+                            v_head_stride, &tm.v, &vt, &vh, &vb);
+  if (st != PDA_OK) return st;
+  if (vt != tm.dim_token || vh != tm.dim_head || vb != tm.dim_block) return PDA_ERR_UNSUPPORTED;
+  return launch_decode(false, out, q, k_cache, v_cache, nullptr, nullptr, block_tables, seq_lens, num_seqs,
+                       num_heads, num_kv_heads, head_size, block_size, max_num_blocks_per_seq, scale, k_scale,
+                       v_scale, stream, nullptr, 0, 1.f, 0, &tm);
+}
+
 pda_status pda_decode_slot_scales(void* out, const void* q, const void* k_cache, const void* v_cache,
                                   const float* k_scales, const float* v_scales, const int32_t* block_tables,
                                   const int32_t* seq_lens, int num_seqs, int num_heads, int num_kv_heads,
@@ -493,7 +603,7 @@ pda_status noalloc_setup(int dev, int bs, NoAllocDevice* out) {
       const size_t sb = ring_shape(b).smem_bytes;
       mx = sb > mx ? sb : mx;
     }
-    if (cudaFuncSetAttribute(pda::pda_split_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(pda::pda_split_decode_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)mx) != cudaSuccess)
       return PDA_ERR_CUDA;
     d.scratch = ptr;
@@ -503,7 +613,7 @@ pda_status noalloc_setup(int dev, int bs, NoAllocDevice* out) {
   int& occ = d.occ[bs / 16];
   if (occ == 0) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pda::pda_split_decode_kernel<false>, pda::kThreads,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pda::pda_split_decode_kernel<false, false>, pda::kThreads,
                                                       ring_shape(bs).smem_bytes) != cudaSuccess)
       return PDA_ERR_CUDA;
     occ = n > 0 ? n : 1;
@@ -557,7 +667,7 @@ extern "C" pda_status pda_decode_noalloc(void* out, const void* q, const void* k
   p.logit_scale_log2 = (float)((double)scale * (double)k_scale * 1.4426950408889634);
   p.v_scale = v_scale;
   dim3 grid((unsigned)nsplit, (unsigned)num_kv_heads, (unsigned)num_seqs);
-  pda::pda_split_decode_kernel<false><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(p);
+  pda::pda_split_decode_kernel<false, false><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(p, g_no_map, g_no_map);
   if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
   if (nsplit > 1) {
     pda::MergeParams mp;

@@ -71,6 +71,11 @@ struct DecodeParams {
   float logit_scale_log2;       // scale * k_scale * log2(e)  (scale * log2(e) with slot scales)
   float v_scale;                // per-tensor V scale (unused with slot scales)
   int v_shuffled = 0;           // 1: V pages are [bs/16][D][16] (AITER shuffled), else [D][bs]
+  // Token-major variant: position (1..3) of the token, kv-head and block
+  // dimensions in the 4-D tensor maps (dimension 0 is the 128 bytes of a row).
+  int tm_dim_token = 1;
+  int tm_dim_head = 2;
+  int tm_dim_block = 3;
   const float* sinks = nullptr; // [H] per-head sink logits (scale * q.k units), or none
   int out_fp8 = 0;              // 1: out holds E4M3(o / out_scale) bytes
   float out_scale = 1.f;
@@ -141,8 +146,19 @@ __device__ __forceinline__ float warp_sum_over_gid(float v) {
 // multiplies its logit, its V scale multiplies its probability before the PV
 // product (relative to the V scale of the split's first slot, so P stays in
 // f16's normal range), and the sum l uses the unscaled probabilities.
-template <bool kSlotScales>
-__global__ void __launch_bounds__(kThreads, 3) pda_split_decode_kernel(const DecodeParams p) {
+//
+// kTokenMajor: K and V pages are token-major rows of 128 bytes reached
+// through strided tensor maps (the flash / NHD family of layouts). Each page
+// lands in shared memory as [bs][128] with 128-byte swizzle (16-byte chunk c
+// of row t at c ^ (t & 7)); QK^T reads K rows with ldmatrix in natural token
+// order, PV reads V with ldmatrix.trans, whose b16 transpose hands each lane
+// 2 tokens x 2 dims per register, split into an even-dim and an odd-dim
+// fragment row by one byte permute. Output row gid of m-tile mt is then dim
+// 16mt + 2gid and row gid + 8 is dim 16mt + 2gid + 1.
+template <bool kSlotScales, bool kTokenMajor>
+__global__ void __launch_bounds__(kThreads, 3)
+    pda_split_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_v) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int split = blockIdx.x;
   const int kvh = blockIdx.y;
@@ -173,8 +189,9 @@ __global__ void __launch_bounds__(kThreads, 3) pda_split_decode_kernel(const Dec
 
   const int NS = p.num_stages;
   const int PPS = p.pages_per_stage;
-  uint8_t* ring = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)NS * p.stage_bytes);
+  // Ring base aligned to 1024 bytes (the 128-byte swizzle repeats every 1 KiB).
+  uint8_t* ring = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + (size_t)NS * p.stage_bytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * NS);
   const uint32_t ring_u32 = smem_u32(ring);
   const uint32_t full0 = smem_u32(bars);
@@ -229,9 +246,19 @@ __global__ void __launch_bounds__(kThreads, 3) pda_split_decode_kernel(const Dec
 #pragma unroll
           for (int t = 0; t < kMaxPagesPerStage; ++t) {
             if (t < np) {
-              const size_t off = (size_t)blk[t] * block_stride + (size_t)kvh * head_stride;
-              bulk_g2s(sbase + (uint32_t)t * page_bytes, p.k_cache + off, page_bytes, bar);
-              bulk_g2s(sbase + (uint32_t)(PPS + t) * page_bytes, p.v_cache + off, page_bytes, bar);
+              if constexpr (kTokenMajor) {
+                // coordinates: 0 for the row bytes and the token dim, kvh and
+                // the block id in the head and block dims
+                const int c1 = p.tm_dim_head == 1 ? kvh : (p.tm_dim_block == 1 ? blk[t] : 0);
+                const int c2 = p.tm_dim_head == 2 ? kvh : (p.tm_dim_block == 2 ? blk[t] : 0);
+                const int c3 = p.tm_dim_head == 3 ? kvh : (p.tm_dim_block == 3 ? blk[t] : 0);
+                tma_load_4d(sbase + (uint32_t)t * page_bytes, &tm_k, 0, c1, c2, c3, bar);
+                tma_load_4d(sbase + (uint32_t)(PPS + t) * page_bytes, &tm_v, 0, c1, c2, c3, bar);
+              } else {
+                const size_t off = (size_t)blk[t] * block_stride + (size_t)kvh * head_stride;
+                bulk_g2s(sbase + (uint32_t)t * page_bytes, p.k_cache + off, page_bytes, bar);
+                bulk_g2s(sbase + (uint32_t)(PPS + t) * page_bytes, p.v_cache + off, page_bytes, bar);
+              }
               if constexpr (kSlotScales) {
                 const size_t srow = ((size_t)blk[t] * p.num_kv_heads + kvh) * (size_t)bs;
                 bulk_g2s(sbase + p.scale_off + (uint32_t)t * row_bytes, p.k_scales + srow, row_bytes, bar);
@@ -277,15 +304,20 @@ __global__ void __launch_bounds__(kThreads, 3) pda_split_decode_kernel(const Dec
   // ldmatrix row assignment. K: lane l supplies token row_token(l & 15) of
   // chunk (2kk + (l >> 4)). V: lane l supplies dim (32mp + l).
   const uint32_t k_lane_off = (uint32_t)(row_token(lane & 15) * 16) + (uint32_t)((lane >> 4) * bs * 16);
+  // Token-major tiles: lane l addresses token row (l & 15), chunk (2j + (l >> 4)),
+  // swizzled by the row's low 3 bits.
+  const uint32_t tm_row = (uint32_t)(lane & 15) * 128u;
+  const uint32_t tm_xor = (uint32_t)(lane & 7);
+  const uint32_t tm_hi = (uint32_t)(lane >> 4);
   // V: a 16-token tile is 128 rows of 16 bytes at stride v_row (bs for
   // [D][bs] pages; 16 for shuffled [bs/16][D][16] pages, whose tiles are
   // contiguous and so bank-conflict free for any block size).
   const uint32_t v_row = p.v_shuffled ? 16u : (uint32_t)bs;
   const uint32_t v_sub = p.v_shuffled ? (uint32_t)(kHeadDim * 16) : 16u;
   const uint32_t v_lane_off = (uint32_t)lane * v_row;
-  const bool low_quad = tig < 2;
-  const int tokA = row_token(gid);
-  const int tokB = row_token(gid + 8);
+  const bool low_quad = kTokenMajor ? true : tig < 2;
+  const int tokA = kTokenMajor ? gid : row_token(gid);
+  const int tokB = kTokenMajor ? gid + 8 : row_token(gid + 8);
 
   float m0 = -INFINITY, m1 = -INFINITY;   // running max (log2 units), heads 2tig, 2tig+1
   float l0 = 0.f, l1 = 0.f;               // running partial sums over this lane's tokens
@@ -330,8 +362,10 @@ __global__ void __launch_bounds__(kThreads, 3) pda_split_decode_kernel(const Dec
       const int sub = tile % tiles_per_page;
       const int tok0 = (fill_first_page + pg) * bs + sub * 16;
       if (tok0 >= L) continue;
-      const uint32_t kbase = sbase + (uint32_t)pg * page_bytes + (uint32_t)(sub * 256);
-      const uint32_t vbase = sbase + (uint32_t)(PPS + pg) * page_bytes + (uint32_t)sub * v_sub;
+      const uint32_t kbase = kTokenMajor ? sbase + (uint32_t)pg * page_bytes + (uint32_t)sub * 2048u
+                                         : sbase + (uint32_t)pg * page_bytes + (uint32_t)(sub * 256);
+      const uint32_t vbase = kTokenMajor ? sbase + (uint32_t)(PPS + pg) * page_bytes + (uint32_t)sub * 2048u
+                                         : sbase + (uint32_t)(PPS + pg) * page_bytes + (uint32_t)sub * v_sub;
 
       // ---- S^T = K_tile * Q^T (two independent accumulator chains)
       float sc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -339,7 +373,10 @@ __global__ void __launch_bounds__(kThreads, 3) pda_split_decode_kernel(const Dec
 #pragma unroll
       for (int kk = 0; kk < kChunks / 2; ++kk) {
         uint32_t r0, r1, r2, r3;
-        ldsm_x4(kbase + k_lane_off + (uint32_t)(2 * kk * bs * 16), r0, r1, r2, r3);
+        if constexpr (kTokenMajor)
+          ldsm_x4(kbase + tm_row + ((((uint32_t)(2 * kk) + tm_hi) ^ tm_xor) << 4), r0, r1, r2, r3);
+        else
+          ldsm_x4(kbase + k_lane_off + (uint32_t)(2 * kk * bs * 16), r0, r1, r2, r3);
         mma_f16(sc, e4m3x2_lo_to_f16x2(r0), e4m3x2_lo_to_f16x2(r1), e4m3x2_hi_to_f16x2(r0),
                 e4m3x2_hi_to_f16x2(r1), qf[2 * kk][0], qf[2 * kk][1]);
         mma_f16(sd, e4m3x2_lo_to_f16x2(r2), e4m3x2_lo_to_f16x2(r3), e4m3x2_hi_to_f16x2(r2),
@@ -404,28 +441,60 @@ __global__ void __launch_bounds__(kThreads, 3) pda_split_decode_kernel(const Dec
       const uint32_t pb0 = low_quad ? t0 : t1;
       const uint32_t pb1 = low_quad ? t1 : t0;
 
-      // ---- O^T += V_tile^T * P^T; lane holds V bytes of tokens 4tig..4tig+3
+      // ---- O^T += V_tile^T * P^T
+      // Page-major V: lane holds V bytes of tokens 4tig..4tig+3 of one dim.
+      // Token-major V (ldmatrix.trans): a register holds tokens (2tig, 2tig+1)
+      // x dims (2gid, 2gid+1) of a chunk; registers 0/2 tokens 0-7, 1/3 8-15.
       uint32_t vr[kChunks / 2][4];
 #pragma unroll
-      for (int mp = 0; mp < kChunks / 2; ++mp)
-        ldsm_x4(vbase + v_lane_off + (uint32_t)(32 * mp) * v_row, vr[mp][0], vr[mp][1], vr[mp][2], vr[mp][3]);
+      for (int mp = 0; mp < kChunks / 2; ++mp) {
+        if constexpr (kTokenMajor)
+          ldsm_x4_trans(vbase + tm_row + ((((uint32_t)(2 * mp) + tm_hi) ^ tm_xor) << 4), vr[mp][0], vr[mp][1],
+                        vr[mp][2], vr[mp][3]);
+        else
+          ldsm_x4(vbase + v_lane_off + (uint32_t)(32 * mp) * v_row, vr[mp][0], vr[mp][1], vr[mp][2], vr[mp][3]);
+      }
       const int n_valid = L - tok0;
       if (n_valid < 16) {
         // Zero the V bytes of tokens >= L: their e4m3 codes may be NaN and
         // 0 * NaN would poison the accumulator.
-        const int k = min(max(n_valid - 4 * tig, 0), 4);
-        const uint32_t vmask = k >= 4 ? 0xFFFFFFFFu : ((1u << (8 * k)) - 1u);
+        if constexpr (kTokenMajor) {
+          const uint32_t m_lo = (2 * tig < n_valid ? 0x0000FFFFu : 0u) | (2 * tig + 1 < n_valid ? 0xFFFF0000u : 0u);
+          const uint32_t m_hi =
+              (8 + 2 * tig < n_valid ? 0x0000FFFFu : 0u) | (9 + 2 * tig < n_valid ? 0xFFFF0000u : 0u);
 #pragma unroll
-        for (int mp = 0; mp < kChunks / 2; ++mp)
+          for (int mp = 0; mp < kChunks / 2; ++mp) {
+            vr[mp][0] &= m_lo;
+            vr[mp][1] &= m_hi;
+            vr[mp][2] &= m_lo;
+            vr[mp][3] &= m_hi;
+          }
+        } else {
+          const int k = min(max(n_valid - 4 * tig, 0), 4);
+          const uint32_t vmask = k >= 4 ? 0xFFFFFFFFu : ((1u << (8 * k)) - 1u);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) vr[mp][i] &= vmask;
+          for (int mp = 0; mp < kChunks / 2; ++mp)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) vr[mp][i] &= vmask;
+        }
       }
 #pragma unroll
       for (int mp = 0; mp < kChunks / 2; ++mp) {
-        mma_f16(o[2 * mp], e4m3x2_lo_to_f16x2(vr[mp][0]), e4m3x2_lo_to_f16x2(vr[mp][1]),
-                e4m3x2_hi_to_f16x2(vr[mp][0]), e4m3x2_hi_to_f16x2(vr[mp][1]), pb0, pb1);
-        mma_f16(o[2 * mp + 1], e4m3x2_lo_to_f16x2(vr[mp][2]), e4m3x2_lo_to_f16x2(vr[mp][3]),
-                e4m3x2_hi_to_f16x2(vr[mp][2]), e4m3x2_hi_to_f16x2(vr[mp][3]), pb0, pb1);
+        if constexpr (kTokenMajor) {
+          // bytes (t,d0) (t,d1) (t',d0) (t',d1) -> (t,d0) (t',d0) | (t,d1) (t',d1)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t ya = __byte_perm(vr[mp][2 * h], 0, 0x3120);
+            const uint32_t yb = __byte_perm(vr[mp][2 * h + 1], 0, 0x3120);
+            mma_f16(o[2 * mp + h], e4m3x2_lo_to_f16x2(ya), e4m3x2_hi_to_f16x2(ya), e4m3x2_lo_to_f16x2(yb),
+                    e4m3x2_hi_to_f16x2(yb), pb0, pb1);
+          }
+        } else {
+          mma_f16(o[2 * mp], e4m3x2_lo_to_f16x2(vr[mp][0]), e4m3x2_lo_to_f16x2(vr[mp][1]),
+                  e4m3x2_hi_to_f16x2(vr[mp][0]), e4m3x2_hi_to_f16x2(vr[mp][1]), pb0, pb1);
+          mma_f16(o[2 * mp + 1], e4m3x2_lo_to_f16x2(vr[mp][2]), e4m3x2_lo_to_f16x2(vr[mp][3]),
+                  e4m3x2_hi_to_f16x2(vr[mp][2]), e4m3x2_hi_to_f16x2(vr[mp][3]), pb0, pb1);
+        }
       }
     }
     __syncwarp();
@@ -445,11 +514,13 @@ __global__ void __launch_bounds__(kThreads, 3) pda_split_decode_kernel(const Dec
     float* mw = mo + warp * kMaxGqa * kMergeStride;
 #pragma unroll
     for (int mt = 0; mt < kChunks; ++mt) {
-      const int d0 = 16 * mt + gid;
+      // accumulator rows gid / gid + 8 of m-tile mt hold these two dims
+      const int d0 = kTokenMajor ? 16 * mt + 2 * gid : 16 * mt + gid;
+      const int d1 = kTokenMajor ? d0 + 1 : d0 + 8;
       mw[(2 * tig) * kMergeStride + d0] = o[mt][0];
       mw[(2 * tig + 1) * kMergeStride + d0] = o[mt][1];
-      mw[(2 * tig) * kMergeStride + d0 + 8] = o[mt][2];
-      mw[(2 * tig + 1) * kMergeStride + d0 + 8] = o[mt][3];
+      mw[(2 * tig) * kMergeStride + d1] = o[mt][2];
+      mw[(2 * tig + 1) * kMergeStride + d1] = o[mt][3];
     }
     if (gid == 0) {
       float* ml = mml + warp * kMaxGqa * 2;
