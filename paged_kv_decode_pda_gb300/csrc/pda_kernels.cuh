@@ -633,13 +633,18 @@ __global__ void pda_bounded_wait_test_kernel(unsigned long long limit_ns) {
 // KV-cache write: quantise new keys / values to e4m3 with the per-tensor
 // scales and scatter them into the paged cache (vLLM API page
 // vllm.v1.attention.backends.rocm_aiter_unified_attn, do_kv_cache_update ->
-// reshape_and_cache). One warp per (token, kv head), 4 dims per lane:
-//   K bytes -> k_cache[b][k][d/16][o][d%16]   (one 4-byte store per lane)
-//   V bytes -> v_cache[b][k][d][o]            (four byte stores per lane), or
-//              v_cache[b][k][o/16][d][o%16]   for the shuffled V layout
-// with b = slot / bs, o = slot % bs. The code is decided on the IEEE binary32
-// quotient x / scale. Negative slots are padding; slots past the pool are
-// skipped and flagged in the status word.
+// reshape_and_cache), for slot = b * bs + o:
+//   K bytes -> k_cache[b][k][d/16][o][d%16]
+//   V bytes -> v_cache[b][k][d][o], or v_cache[b][k][o/16][d][o%16] (shuffled V)
+// The code is decided on the IEEE binary32 quotient x / scale. Negative slots
+// are padding; slots past the pool are skipped and flagged in the status word.
+//
+// One 128-thread CTA per (16 consecutive tokens, kv head); thread (j, c)
+// owns token j and the 16 dims of chunk c. Its 16 K codes are one 16-byte
+// K row, stored directly for any slot. V rows run over tokens, so when the
+// 16 slots form one aligned run of a block (a prefill writing whole groups)
+// the codes are transposed through shared memory and each dim's 16 tokens
+// leave as one 16-byte store; otherwise each thread stores its 16 V bytes.
 struct CacheWriteParams {
   const __nv_bfloat16* key;      // [T][Hk][128]
   const __nv_bfloat16* value;    // [T][Hk][128]
@@ -655,10 +660,93 @@ struct CacheWriteParams {
   int v_shuffled = 0;            // 1: V pages are [bs/16][D][16]
 };
 
-constexpr int kCacheWriteWarps = 8;
+constexpr int kCacheWriteThreads = 128;   // 16 tokens x 8 chunks of 16 dims
+constexpr int kCacheWriteWarpsPerCta = 8;  // scattered writer: one warp per (token, kv head)
 
-__global__ void __launch_bounds__(kCacheWriteWarps * 32) pda_reshape_and_cache_kernel(const CacheWriteParams p) {
-  const long long item = (long long)blockIdx.x * kCacheWriteWarps + (threadIdx.x >> 5);
+// Scattered writer for small batches (a decode step: one token per
+// sequence, at slots all over the pool): one warp per (token, kv head), 4
+// dims per lane, so every byte store has its own lane.
+__global__ void __launch_bounds__(kCacheWriteWarpsPerCta * 32)
+    pda_reshape_and_cache_scatter_kernel(const struct CacheWriteParams p);
+
+__device__ __forceinline__ uint4 quantize16(const __nv_bfloat16* src, float scale) {
+  const uint4 a = __ldg(reinterpret_cast<const uint4*>(src));
+  const uint4 b = __ldg(reinterpret_cast<const uint4*>(src) + 1);
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t q[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(bf16lo_f32(w[2 * i]), scale), __fdiv_rn(bf16hi_f32(w[2 * i]), scale));
+    const uint32_t hi =
+        f32x2_to_e4m3x2(__fdiv_rn(bf16lo_f32(w[2 * i + 1]), scale), __fdiv_rn(bf16hi_f32(w[2 * i + 1]), scale));
+    q[i] = lo | (hi << 16);
+  }
+  return make_uint4(q[0], q[1], q[2], q[3]);
+}
+
+__global__ void __launch_bounds__(kCacheWriteThreads) pda_reshape_and_cache_kernel(const CacheWriteParams p) {
+  __shared__ __align__(16) uint8_t vt[16][kHeadDim];   // V codes [token][dim] for the transpose
+  const int tid = threadIdx.x;
+  const int j = tid >> 3;
+  const int c = tid & 7;
+  const int k = blockIdx.y;
+  const int t0 = blockIdx.x * 16;
+  const int t = t0 + j;
+  const int bs = p.block_size;
+
+  long long slot = -1;
+  if (t < p.num_tokens) slot = __ldg(p.slot_mapping + t);
+  const bool in_pool = slot < p.num_slots;
+  if (slot >= 0 && !in_pool && c == 0) atomicOr(&g_status, kStatusBadSlot);
+  const bool valid = slot >= 0 && in_pool;
+
+  uint4 kq = make_uint4(0, 0, 0, 0), vq = make_uint4(0, 0, 0, 0);
+  if (valid) {
+    const size_t src = ((size_t)t * p.num_kv_heads + k) * kHeadDim + 16 * c;
+    kq = quantize16(p.key + src, p.k_scale);
+    vq = quantize16(p.value + src, p.v_scale);
+  }
+  const long long b = valid ? slot / bs : 0;
+  const int o = valid ? (int)(slot % bs) : 0;
+  const size_t page = ((size_t)b * p.num_kv_heads + k) * (size_t)kHeadDim * bs;
+  if (valid) *reinterpret_cast<uint4*>(p.k_cache + page + ((size_t)c * bs + o) * 16) = kq;
+
+  // One aligned run of 16 slots in one block? (uniform over the CTA)
+  __shared__ long long first_slot;
+  if (tid == 0) first_slot = slot;
+  __syncthreads();
+  const bool run = valid && (first_slot % 16 == 0) && (slot == first_slot + j);
+  const int fast = __syncthreads_and(run ? 1 : 0);
+  if (fast) {
+    *reinterpret_cast<uint4*>(&vt[j][16 * c]) = vq;
+    __syncthreads();
+    // thread d gathers dim d of the 16 tokens: one V row of the run
+    const int d = tid;
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      w[i] = (uint32_t)vt[4 * i][d] | ((uint32_t)vt[4 * i + 1][d] << 8) | ((uint32_t)vt[4 * i + 2][d] << 16) |
+             ((uint32_t)vt[4 * i + 3][d] << 24);
+    const long long b0 = first_slot / bs;
+    const int o0 = (int)(first_slot % bs);
+    const size_t page0 = ((size_t)b0 * p.num_kv_heads + k) * (size_t)kHeadDim * bs;
+    const size_t off = p.v_shuffled ? ((size_t)(o0 / 16) * kHeadDim + d) * 16 : (size_t)d * bs + o0;
+    *reinterpret_cast<uint4*>(p.v_cache + page0 + off) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else if (valid) {
+    const uint32_t vw[4] = {vq.x, vq.y, vq.z, vq.w};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int d = 16 * c + i;
+      const size_t off = p.v_shuffled ? ((size_t)(o / 16) * kHeadDim + d) * 16 + (o % 16) : (size_t)d * bs + o;
+      p.v_cache[page + off] = (uint8_t)(vw[i >> 2] >> (8 * (i & 3)));
+    }
+  }
+}
+
+// Definition of the scattered writer declared above.
+__global__ void __launch_bounds__(kCacheWriteWarpsPerCta * 32)
+    pda_reshape_and_cache_scatter_kernel(const CacheWriteParams p) {
+  const long long item = (long long)blockIdx.x * kCacheWriteWarpsPerCta + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (item >= (long long)p.num_tokens * p.num_kv_heads) return;
   const int t = (int)(item / p.num_kv_heads);
@@ -669,8 +757,9 @@ __global__ void __launch_bounds__(kCacheWriteWarps * 32) pda_reshape_and_cache_k
     if (lane == 0) atomicOr(&g_status, kStatusBadSlot);
     return;
   }
-  const long long b = slot / p.block_size;
-  const int o = (int)(slot % p.block_size);
+  const int bs = p.block_size;
+  const long long b = slot / bs;
+  const int o = (int)(slot % bs);
   const size_t src = ((size_t)t * p.num_kv_heads + k) * kHeadDim + 4 * lane;
   const uint2 kx = ld_nc_v2(p.key + src);
   const uint2 vx = ld_nc_v2(p.value + src);
@@ -679,12 +768,12 @@ __global__ void __launch_bounds__(kCacheWriteWarps * 32) pda_reshape_and_cache_k
                       (f32x2_to_e4m3x2(__fdiv_rn(bf16lo_f32(kx.y), ks), __fdiv_rn(bf16hi_f32(kx.y), ks)) << 16);
   const uint32_t vq = f32x2_to_e4m3x2(__fdiv_rn(bf16lo_f32(vx.x), vs), __fdiv_rn(bf16hi_f32(vx.x), vs)) |
                       (f32x2_to_e4m3x2(__fdiv_rn(bf16lo_f32(vx.y), vs), __fdiv_rn(bf16hi_f32(vx.y), vs)) << 16);
-  const size_t page = ((size_t)b * p.num_kv_heads + k) * (size_t)kHeadDim * p.block_size;
+  const size_t page = ((size_t)b * p.num_kv_heads + k) * (size_t)kHeadDim * bs;
   const int d0 = 4 * lane;
-  *reinterpret_cast<uint32_t*>(p.k_cache + page + ((size_t)(d0 / 16) * p.block_size + o) * 16 + (d0 % 16)) = kq;
-  const size_t vstride = p.v_shuffled ? 16 : (size_t)p.block_size;
-  uint8_t* vrow = p.v_cache + page +
-                  (p.v_shuffled ? ((size_t)(o / 16) * kHeadDim + d0) * 16 + (o % 16) : (size_t)d0 * p.block_size + o);
+  *reinterpret_cast<uint32_t*>(p.k_cache + page + ((size_t)(d0 / 16) * bs + o) * 16 + (d0 % 16)) = kq;
+  const size_t vstride = p.v_shuffled ? 16 : (size_t)bs;
+  uint8_t* vrow =
+      p.v_cache + page + (p.v_shuffled ? ((size_t)(o / 16) * kHeadDim + d0) * 16 + (o % 16) : (size_t)d0 * bs + o);
 #pragma unroll
   for (int i = 0; i < 4; ++i) vrow[(size_t)i * vstride] = (uint8_t)(vq >> (8 * i));
 }

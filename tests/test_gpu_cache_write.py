@@ -30,6 +30,7 @@ def _case(T, Hk, bs, NB, seed, scale_k=0.05, scale_v=0.07, pad_frac=0.2, special
 @pytest.mark.parametrize("T,Hk,bs,NB,seed,special", [
     (1, 1, 16, 1, 0, False), (7, 8, 16, 4, 1, True), (256, 8, 16, 300, 2, False), (100, 4, 64, 5, 3, False),
     (33, 2, 32, 4, 4, True), (513, 8, 128, 9, 5, False),
+    (5000, 8, 16, 400, 6, True),     # above the scattered writer's limit: run writer with random slots
 ])
 def test_cache_write_bit_exact(T, Hk, bs, NB, seed, special):
     key, val, slots, kc, vc, ks, vs = _case(T, Hk, bs, NB, seed, special=special)
@@ -73,3 +74,44 @@ def test_write_then_decode_matches_oracle():
         pda.reshape_and_cache(key, val, batch.k_cache, batch.v_cache, slots, batch.cfg.k_scale, batch.cfg.v_scale)
     out = U.run_cuda(batch)
     U.compare(out, U.run_oracle(batch), "write-then-decode")
+
+
+@pytest.mark.parametrize("bs,shuffled", [(16, False), (64, False), (64, True), (32, True)])
+def test_cache_write_runs_bit_exact(bs, shuffled):
+    """Prefill-like slots: whole aligned 16-slot runs (coalesced path) mixed
+    with a misaligned run and a run broken by padding (per-token path)."""
+    g = torch.Generator().manual_seed(100 + bs)
+    Hk = 8
+    n_whole = 4800 // bs                      # > 32768 (token, head) items: the run writer
+    NB = n_whole + 6
+    blocks = torch.randperm(NB, generator=g)
+    slots = []
+    for b in blocks[:n_whole].tolist():       # whole blocks, in token order
+        slots += list(range(b * bs, (b + 1) * bs))
+    blocks = blocks[n_whole - 6:]             # keep the indices below as they were
+    b = int(blocks[6])
+    slots += list(range(b * bs + 3, b * bs + min(bs, 3 + 16)))   # misaligned run inside one block
+    b = int(blocks[7])
+    run = list(range(b * bs, b * bs + 16))
+    run[5] = -1                                          # padding inside a run
+    slots += run
+    slots += [int(blocks[8]) * bs + 7]                   # ragged tail
+    T = len(slots)
+    used = [x for x in slots if x >= 0]
+    assert len(set(used)) == len(used), "slots must be distinct"
+    slots_t = torch.tensor(slots, dtype=torch.int64)
+    key = (torch.randn(T, Hk, 128, generator=g) * 3).to(torch.bfloat16)
+    val = (torch.randn(T, Hk, 128, generator=g) * 3).to(torch.bfloat16)
+    kc = torch.randint(0, 256, (NB, Hk, 8, bs, 16), generator=g, dtype=torch.uint8)
+    vshape = (NB, Hk, bs // 16, 128, 16) if shuffled else (NB, Hk, 128, bs)
+    vc = torch.randint(0, 256, vshape, generator=g, dtype=torch.uint8)
+    kr, vr = kc.numpy().copy(), vc.numpy().copy()
+    oracle.reshape_and_cache(kr, vr, key.view(torch.int16).numpy().view(np.uint16),
+                             val.view(torch.int16).numpy().view(np.uint16), slots_t.numpy(), k_scale=0.05,
+                             v_scale=0.07, v_shuffled=shuffled)
+    kd, vd = kc.to(DEV), vc.to(DEV)
+    pda.reshape_and_cache(key.to(DEV), val.to(DEV), kd, vd, slots_t.to(DEV), 0.05, 0.07, v_shuffled=shuffled)
+    torch.cuda.synchronize()
+    assert pda.query_device_status() == 0
+    assert np.array_equal(kd.cpu().numpy(), kr), "K bytes differ"
+    assert np.array_equal(vd.cpu().numpy(), vr), "V bytes differ"
