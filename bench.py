@@ -248,53 +248,7 @@ def run_ours(args, ws, rank, local):
     pda.reserve(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq, cfg.block_size,
                 stream=stream)
 
-    if args.variant == "slot_scales":
-        # per-slot tables filled with the per-tensor scales (the pages' use)
-        ks_t = torch.full((batch.num_blocks, cfg.num_kv_heads, cfg.block_size), cfg.k_scale, device=dev)
-        vs_t = torch.full_like(ks_t, cfg.v_scale)
-        pages_used = batch.pages_used()
-        bytes_per_call += 2 * pages_used * cfg.block_size * 4 * cfg.num_kv_heads
-    elif args.variant == "ex":
-        sinks = torch.randn(cfg.num_heads, generator=torch.Generator().manual_seed(3)).float().to(dev)
-        out = torch.empty(batch.q.shape, dtype=torch.float8_e4m3fn, device=dev)
-        bytes_per_call -= out.numel()   # 1-byte instead of 2-byte output
-        bytes_per_call += cfg.num_heads * 4
-
-    elif args.variant == "shuffled_v":
-        def shuffle(v):
-            NB, Hk, D, bs = v.shape
-            return v.reshape(NB, Hk, D, bs // 16, 16).permute(0, 1, 3, 2, 4).contiguous()
-        caches = [(k, shuffle(v)) for k, v in caches]
-
-    elif args.variant == "strided_nhd":
-        def nhd(k, v):
-            NB, Hk, C, bs, _ = k.shape
-            kt = k.view(torch.uint8).permute(0, 3, 1, 2, 4).reshape(NB, bs, Hk, 128).contiguous()
-            vt = v.view(torch.uint8).permute(0, 3, 1, 2).contiguous()
-            return kt, vt
-        caches = [nhd(k, v) for k, v in caches]
-        hk, bsz = cfg.num_kv_heads, cfg.block_size
-        nhd_strides = (bsz * hk * 128, hk * 128, 128)
-
-    def call(i):
-        kc, vc = caches[i % replicas]
-        if args.variant == "strided_nhd":
-            pda.decode_strided(batch.q, kc.data_ptr(), vc.data_ptr(), batch.block_tables, batch.seq_lens, cfg.scale,
-                               cfg.k_scale, cfg.v_scale, num_kv_heads=hk, block_size=bsz,
-                               num_blocks=batch.num_blocks, k_strides=nhd_strides, v_strides=nhd_strides, out=out,
-                               stream=stream)
-        elif args.variant == "shuffled_v":
-            pda.decode_ex(batch.q, kc, vc, batch.block_tables, batch.seq_lens, cfg.scale, cfg.k_scale, cfg.v_scale,
-                          v_shuffled=True, out=out, stream=stream)
-        elif args.variant == "slot_scales":
-            pda.decode_slot_scales(batch.q, kc, vc, ks_t, vs_t, batch.block_tables, batch.seq_lens, cfg.scale,
-                                   out=out, stream=stream)
-        elif args.variant == "ex":
-            pda.decode_ex(batch.q, kc, vc, batch.block_tables, batch.seq_lens, cfg.scale, cfg.k_scale, cfg.v_scale,
-                          sinks=sinks, output_scale=0.0075, out=out, stream=stream)
-        else:
-            pda.decode(batch.q, kc, vc, batch.block_tables, batch.seq_lens, cfg.scale, cfg.k_scale, cfg.v_scale,
-                       out=out, stream=stream)
+    call, out, bytes_per_call = make_variant_call(args.variant, cfg, batch, caches, out, bytes_per_call, stream)
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -516,8 +470,67 @@ def run_reference(args, ws, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def make_variant_call(variant, cfg, batch, caches, out, bytes_per_call, stream):
+    """The per-call closure for one decode variant, its output and its algorithmic bytes per call.
+
+    ``caches`` is a list of (K, V) replicas in the native layout; call(i)
+    reads replica i mod len(caches).
+    """
+    import paged_kv_decode_pda_gb300 as pda
+
+    dev = batch.q.device
+    replicas = len(caches)
+    if variant == "slot_scales":
+        # per-slot tables filled with the per-tensor scales (the pages' use)
+        ks_t = torch.full((batch.num_blocks, cfg.num_kv_heads, cfg.block_size), cfg.k_scale, device=dev)
+        vs_t = torch.full_like(ks_t, cfg.v_scale)
+        pages_used = batch.pages_used()
+        bytes_per_call += 2 * pages_used * cfg.block_size * 4 * cfg.num_kv_heads
+    elif variant == "ex":
+        sinks = torch.randn(cfg.num_heads, generator=torch.Generator().manual_seed(3)).float().to(dev)
+        out = torch.empty(batch.q.shape, dtype=torch.float8_e4m3fn, device=dev)
+        bytes_per_call -= out.numel()   # 1-byte instead of 2-byte output
+        bytes_per_call += cfg.num_heads * 4
+    elif variant == "shuffled_v":
+        def shuffle(v):
+            NB, Hk, D, bs = v.shape
+            return v.reshape(NB, Hk, D, bs // 16, 16).permute(0, 1, 3, 2, 4).contiguous()
+        caches = [(k, shuffle(v)) for k, v in caches]
+    elif variant == "strided_nhd":
+        def nhd(k, v):
+            NB, Hk, C, bs, _ = k.shape
+            kt = k.view(torch.uint8).permute(0, 3, 1, 2, 4).reshape(NB, bs, Hk, 128).contiguous()
+            vt = v.view(torch.uint8).permute(0, 3, 1, 2).contiguous()
+            return kt, vt
+        caches = [nhd(k, v) for k, v in caches]
+        hk, bsz = cfg.num_kv_heads, cfg.block_size
+        nhd_strides = (bsz * hk * 128, hk * 128, 128)
+
+    def call(i):
+        kc, vc = caches[i % replicas]
+        if variant == "strided_nhd":
+            pda.decode_strided(batch.q, kc.data_ptr(), vc.data_ptr(), batch.block_tables, batch.seq_lens, cfg.scale,
+                               cfg.k_scale, cfg.v_scale, num_kv_heads=hk, block_size=bsz,
+                               num_blocks=batch.num_blocks, k_strides=nhd_strides, v_strides=nhd_strides, out=out,
+                               stream=stream)
+        elif variant == "shuffled_v":
+            pda.decode_ex(batch.q, kc, vc, batch.block_tables, batch.seq_lens, cfg.scale, cfg.k_scale, cfg.v_scale,
+                          v_shuffled=True, out=out, stream=stream)
+        elif variant == "slot_scales":
+            pda.decode_slot_scales(batch.q, kc, vc, ks_t, vs_t, batch.block_tables, batch.seq_lens, cfg.scale,
+                                   out=out, stream=stream)
+        elif variant == "ex":
+            pda.decode_ex(batch.q, kc, vc, batch.block_tables, batch.seq_lens, cfg.scale, cfg.k_scale, cfg.v_scale,
+                          sinks=sinks, output_scale=0.0075, out=out, stream=stream)
+        else:
+            pda.decode(batch.q, kc, vc, batch.block_tables, batch.seq_lens, cfg.scale, cfg.k_scale, cfg.v_scale,
+                       out=out, stream=stream)
+
+    return call, out, bytes_per_call
+
+
 def run_profile(args):
-    """N plain calls of the decode path (what an ncu capture of this command sees)."""
+    """N calls of one decode variant, untimed (what an ncu capture of this command sees)."""
     import paged_kv_decode_pda_gb300 as pda
     from paged_kv_decode_pda_gb300 import build
 
@@ -525,16 +538,18 @@ def run_profile(args):
     build.build()
     cfg = workloads.CONFIGS[args.config]
     batch = workloads.make_batch(cfg, device="cuda:0")
-    out = torch.empty_like(batch.q)
-    for _ in range(args.profile):
-        pda.decode(batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.seq_lens, cfg.scale,
-                   cfg.k_scale, cfg.v_scale, out=out)
+    stream = torch.cuda.current_stream()
+    call, out, bytes_per_call = make_variant_call(args.variant, cfg, batch, [(batch.k_cache, batch.v_cache)],
+                                                  torch.empty_like(batch.q),
+                                                  workloads.algorithmic_bytes(cfg, batch.seq_lens_host), stream)
+    for i in range(args.profile):
+        call(i)
     torch.cuda.synchronize()
     code = pda.query_device_status()
     nsplit = pda.plan_splits(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq,
                              cfg.block_size)
-    print(json.dumps({"profile_calls": args.profile, "workload": cfg.name, "kv_splits": nsplit,
-                      "bytes_per_call": workloads.algorithmic_bytes(cfg, batch.seq_lens_host),
+    print(json.dumps({"profile_calls": args.profile, "workload": cfg.name, "variant": args.variant,
+                      "kv_splits": nsplit, "bytes_per_call": bytes_per_call,
                       "device_status": code}))
     if code:
         raise SystemExit(1)

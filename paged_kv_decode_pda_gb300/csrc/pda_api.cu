@@ -23,9 +23,12 @@ std::atomic<int> g_split_override{0};
 std::atomic<cudaEvent_t> g_prof_before{nullptr};
 std::atomic<cudaEvent_t> g_prof_after{nullptr};
 
+// Decode kernel instances the library launches.
+enum KernelKind { kPlainWide = 0, kPlainDense, kSlotWide, kTokenWide, kTokenDense, kNumKinds };
+
 struct DeviceInfo {
   int sm_count = 0;
-  int ctas_per_sm_by_bs[2][9] = {{0}};  // [slot scales][bs/16 (1..8)]
+  int ctas_per_sm[kNumKinds][9] = {{0}};  // [instance][bs/16 (1..8)]
   bool smem_attr_set = false;
 };
 std::mutex g_dev_mu;
@@ -48,12 +51,12 @@ struct RingShape {
   size_t smem_bytes;
 };
 
-RingShape ring_shape(int bs, bool slot_scales = false) {
+RingShape ring_shape(int bs, bool slot_scales = false, int ring_bytes = pda::kRingBytes) {
   RingShape r;
   r.pages_per_stage = bs < pda::kStageTokensMin ? pda::kStageTokensMin / bs : 1;
   r.scale_off = 2u * (uint32_t)r.pages_per_stage * (uint32_t)(kHeadDim * bs);
   r.stage_bytes = r.scale_off + (slot_scales ? 2u * (uint32_t)r.pages_per_stage * (uint32_t)bs * 4u : 0u);
-  r.num_stages = (int)((uint32_t)pda::kRingBytes / r.scale_off);  // scale rows ride on top
+  r.num_stages = (int)((uint32_t)ring_bytes / r.scale_off);  // scale rows ride on top
   if (r.num_stages < 2) r.num_stages = 2;
   size_t ring = (size_t)r.num_stages * r.stage_bytes;
   size_t merge = (size_t)pda::kConsumerWarps * pda::kMaxGqa * (pda::kMergeStride + 2) * sizeof(float);
@@ -167,7 +170,25 @@ pda_status validate(const void* out, const void* q, const void* k_cache, const v
   return PDA_OK;
 }
 
-pda_status device_info(int dev, int bs, int* sm_count, int* ctas_per_sm, bool slot_scales = false) {
+bool is_dense(KernelKind k) { return k == kPlainDense || k == kTokenDense; }
+bool is_slot(KernelKind k) { return k == kSlotWide; }
+
+RingShape ring_for(KernelKind k, int bs) {
+  return ring_shape(bs, is_slot(k), is_dense(k) ? pda::kDenseRingBytes : pda::kRingBytes);
+}
+
+const void* kernel_fn(KernelKind k) {
+  switch (k) {
+    case kPlainWide: return (const void*)pda::pda_split_decode_kernel<false, false, pda::kWideCtasPerSm>;
+    case kPlainDense: return (const void*)pda::pda_split_decode_kernel<false, false, pda::kDenseCtasPerSm>;
+    case kSlotWide: return (const void*)pda::pda_split_decode_kernel<true, false, pda::kWideCtasPerSm>;
+    case kTokenWide: return (const void*)pda::pda_split_decode_kernel<false, true, pda::kWideCtasPerSm>;
+    default: return (const void*)pda::pda_split_decode_kernel<false, true, pda::kDenseCtasPerSm>;
+  }
+}
+
+// SM count and resident CTAs per SM of instance `kind` for block size bs.
+pda_status device_info(int dev, int bs, int* sm_count, int* ctas_per_sm, KernelKind kind = kPlainWide) {
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceInfo& di = g_devices[dev];
   if (di.sm_count == 0) {
@@ -177,32 +198,25 @@ pda_status device_info(int dev, int bs, int* sm_count, int* ctas_per_sm, bool sl
     }
   }
   if (!di.smem_attr_set) {
-    // Opt in to the largest ring any block size uses.
+    // Opt every instance in to the largest ring any block size uses.
     size_t mx = 0;
-    for (int b = 16; b <= 128; b += 16) {
-      for (int sc = 0; sc < 2; ++sc) {
-        size_t s = ring_shape(b, sc != 0).smem_bytes;
-        mx = s > mx ? s : mx;
+    for (int b = 16; b <= 128; b += 16)
+      for (int k = 0; k < kNumKinds; ++k) {
+        const size_t sb = ring_for((KernelKind)k, b).smem_bytes;
+        mx = sb > mx ? sb : mx;
       }
-    }
-    if (cudaFuncSetAttribute(pda::pda_split_decode_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)mx) != cudaSuccess ||
-        cudaFuncSetAttribute(pda::pda_split_decode_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)mx) != cudaSuccess ||
-        cudaFuncSetAttribute(pda::pda_split_decode_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)mx) != cudaSuccess)
-      return PDA_ERR_CUDA;
+    for (int k = 0; k < kNumKinds; ++k)
+      if (cudaFuncSetAttribute(kernel_fn((KernelKind)k), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx) !=
+          cudaSuccess)
+        return PDA_ERR_CUDA;
     di.smem_attr_set = true;
   }
-  int& occ = di.ctas_per_sm_by_bs[slot_scales ? 1 : 0][bs / 16];
+  int& occ = di.ctas_per_sm[kind][bs / 16];
   if (occ == 0) {
     int n = 0;
-    const cudaError_t e =
-        slot_scales ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pda::pda_split_decode_kernel<true, false>,
-                                                                    pda::kThreads, ring_shape(bs, true).smem_bytes)
-                    : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pda::pda_split_decode_kernel<false, false>,
-                                                                    pda::kThreads, ring_shape(bs).smem_bytes);
-    if (e != cudaSuccess) return PDA_ERR_CUDA;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel_fn(kind), pda::kThreads,
+                                                      ring_for(kind, bs).smem_bytes) != cudaSuccess)
+      return PDA_ERR_CUDA;
     occ = n > 0 ? n : 1;
   }
   *sm_count = di.sm_count;
@@ -217,6 +231,37 @@ int resolve_splits(int num_seqs, int num_kv_heads, int max_blocks, int bs, int s
   if (n > cap) n = cap;
   if (n < 1) n = 1;
   return n;
+}
+
+// Split count and kernel instance for a call: the wide instance (3 CTAs per
+// SM, 64 KiB ring) unless its planned grid fits one wave of the dense
+// instance (4 CTAs per SM, 48 KiB ring), which then runs the whole batch at
+// once (measured on GB300: 64 x 1K-token batch 27.6 us dense vs 37.3 us wide;
+// large and ragged batches are faster wide).
+struct Plan {
+  KernelKind kind;
+  int nsplit;
+};
+
+pda_status plan_call(int dev, int num_seqs, int num_kv_heads, int max_blocks, int bs, KernelKind wide,
+                     KernelKind dense, Plan* out) {
+  int sms = 0, occ = 0;
+  pda_status st = device_info(dev, bs, &sms, &occ, wide);
+  if (st != PDA_OK) return st;
+  const int MB = max_blocks > 0 ? max_blocks : 1;
+  out->kind = wide;
+  out->nsplit = resolve_splits(num_seqs, num_kv_heads, MB, bs, sms, occ);
+  if (dense != wide) {
+    int occ_d = 0;
+    st = device_info(dev, bs, &sms, &occ_d, dense);
+    if (st != PDA_OK) return st;
+    const long long ctas = (long long)num_seqs * num_kv_heads * out->nsplit;
+    if (occ_d > occ && ctas <= (long long)sms * occ_d) {
+      out->kind = dense;
+      out->nsplit = resolve_splits(num_seqs, num_kv_heads, MB, bs, sms, occ_d);
+    }
+  }
+  return PDA_OK;
 }
 
 // Profiling events: inside stream capture a plain record only expresses a
@@ -277,16 +322,17 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PDA_ERR_CUDA;
-  int sms = 0, occ = 0;
-  st = device_info(dev, block_size, &sms, &occ, slot);
+  const KernelKind wide = slot ? kSlotWide : (tm ? kTokenWide : kPlainWide);
+  const KernelKind dense = slot ? kSlotWide : (tm ? kTokenDense : kPlainDense);
+  Plan pl;
+  st = plan_call(dev, num_seqs, num_kv_heads, max_num_blocks_per_seq, block_size, wide, dense, &pl);
   if (st != PDA_OK) return st;
-  const int MB = max_num_blocks_per_seq > 0 ? max_num_blocks_per_seq : 1;
-  const int nsplit = resolve_splits(num_seqs, num_kv_heads, MB, block_size, sms, occ);
+  const int nsplit = pl.nsplit;
   void* ws = nullptr;
   st = get_workspace(dev, stream, workspace_bytes(num_seqs, num_heads, nsplit), &ws);
   if (st != PDA_OK) return st;
 
-  const RingShape rs = ring_shape(block_size, slot);
+  const RingShape rs = ring_for(pl.kind, block_size);
   pda::DecodeParams p;
   p.out = out;
   p.q = static_cast<const __nv_bfloat16*>(q);
@@ -323,12 +369,30 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
   cudaEvent_t eb = g_prof_before.load(), ea = g_prof_after.load();
   if (eb && ea && record_profile_event(eb, stream) != cudaSuccess) return PDA_ERR_CUDA;
   dim3 grid((unsigned)nsplit, (unsigned)num_kv_heads, (unsigned)num_seqs);
-  if (tm)
-    pda::pda_split_decode_kernel<false, true><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(p, tm->k, tm->v);
-  else if (slot)
-    pda::pda_split_decode_kernel<true, false><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(p, g_no_map, g_no_map);
-  else
-    pda::pda_split_decode_kernel<false, false><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(p, g_no_map, g_no_map);
+  const CUtensorMap& mk = tm ? tm->k : g_no_map;
+  const CUtensorMap& mv = tm ? tm->v : g_no_map;
+  switch (pl.kind) {
+    case kPlainWide:
+      pda::pda_split_decode_kernel<false, false, pda::kWideCtasPerSm><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(
+          p, mk, mv);
+      break;
+    case kPlainDense:
+      pda::pda_split_decode_kernel<false, false, pda::kDenseCtasPerSm><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(
+          p, mk, mv);
+      break;
+    case kSlotWide:
+      pda::pda_split_decode_kernel<true, false, pda::kWideCtasPerSm><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(
+          p, mk, mv);
+      break;
+    case kTokenWide:
+      pda::pda_split_decode_kernel<false, true, pda::kWideCtasPerSm><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(
+          p, mk, mv);
+      break;
+    default:
+      pda::pda_split_decode_kernel<false, true, pda::kDenseCtasPerSm><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(
+          p, mk, mv);
+      break;
+  }
   if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
   if (eb && ea && record_profile_event(ea, stream) != cudaSuccess) return PDA_ERR_CUDA;
 
@@ -405,9 +469,11 @@ int pda_plan_splits(int num_seqs, int num_heads, int num_kv_heads, int max_num_b
   if (block_size <= 0 || block_size % 16 != 0 || block_size > 128) return -1;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
-  int sms = 0, occ = 0;
-  if (device_info(dev, block_size, &sms, &occ) != PDA_OK) return -1;
-  return resolve_splits(num_seqs, num_kv_heads, max_num_blocks_per_seq, block_size, sms, occ);
+  Plan pl;
+  if (plan_call(dev, num_seqs, num_kv_heads, max_num_blocks_per_seq, block_size, kPlainWide, kPlainDense, &pl) !=
+      PDA_OK)
+    return -1;
+  return pl.nsplit;
 }
 
 void pda_set_profile_events(cudaEvent_t before, cudaEvent_t after) {
@@ -427,12 +493,18 @@ pda_status pda_reserve(int num_seqs, int num_heads, int num_kv_heads, int max_nu
     return PDA_ERR_INVALID_ARG;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PDA_ERR_CUDA;
-  int sms = 0, occ = 0;
-  pda_status st = device_info(dev, block_size, &sms, &occ);
-  if (st != PDA_OK) return st;
-  const int nsplit = resolve_splits(num_seqs, num_kv_heads, max_num_blocks_per_seq, block_size, sms, occ);
+  // Size for the largest plan any entry point makes for these sizes.
+  size_t bytes = 0;
+  const KernelKind pairs[3][2] = {{kPlainWide, kPlainDense}, {kSlotWide, kSlotWide}, {kTokenWide, kTokenDense}};
+  for (const auto& pr : pairs) {
+    Plan pl;
+    pda_status st = plan_call(dev, num_seqs, num_kv_heads, max_num_blocks_per_seq, block_size, pr[0], pr[1], &pl);
+    if (st != PDA_OK) return st;
+    const size_t b = workspace_bytes(num_seqs, num_heads, pl.nsplit);
+    bytes = b > bytes ? b : bytes;
+  }
   void* ws = nullptr;
-  return get_workspace(dev, stream, workspace_bytes(num_seqs, num_heads, nsplit), &ws);
+  return get_workspace(dev, stream, bytes, &ws);
 }
 
 pda_status pda_release(void) {
@@ -617,8 +689,8 @@ pda_status noalloc_setup(int dev, int bs, NoAllocDevice* out) {
       const size_t sb = ring_shape(b).smem_bytes;
       mx = sb > mx ? sb : mx;
     }
-    if (cudaFuncSetAttribute(pda::pda_split_decode_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)mx) != cudaSuccess)
+    if (cudaFuncSetAttribute(pda::pda_split_decode_kernel<false, false, pda::kWideCtasPerSm>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx) != cudaSuccess)
       return PDA_ERR_CUDA;
     d.scratch = ptr;
     d.sm_count = sms;
@@ -627,8 +699,8 @@ pda_status noalloc_setup(int dev, int bs, NoAllocDevice* out) {
   int& occ = d.occ[bs / 16];
   if (occ == 0) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pda::pda_split_decode_kernel<false, false>, pda::kThreads,
-                                                      ring_shape(bs).smem_bytes) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pda::pda_split_decode_kernel<false, false, pda::kWideCtasPerSm>,
+                                                      pda::kThreads, ring_shape(bs).smem_bytes) != cudaSuccess)
       return PDA_ERR_CUDA;
     occ = n > 0 ? n : 1;
   }
@@ -681,7 +753,7 @@ extern "C" pda_status pda_decode_noalloc(void* out, const void* q, const void* k
   p.logit_scale_log2 = (float)((double)scale * (double)k_scale * 1.4426950408889634);
   p.v_scale = v_scale;
   dim3 grid((unsigned)nsplit, (unsigned)num_kv_heads, (unsigned)num_seqs);
-  pda::pda_split_decode_kernel<false, false><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(p, g_no_map, g_no_map);
+  pda::pda_split_decode_kernel<false, false, pda::kWideCtasPerSm><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(p, g_no_map, g_no_map);
   if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
   if (nsplit > 1) {
     pda::MergeParams mp;

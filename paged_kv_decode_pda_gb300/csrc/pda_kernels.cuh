@@ -34,6 +34,12 @@ namespace pda {
 #ifndef PDA_RING_BYTES
 #define PDA_RING_BYTES 65536
 #endif
+// Two residency targets for the decode kernel, chosen per call: 3 CTAs per
+// SM with the full ring for large batches, 4 CTAs per SM with a 48 KiB ring
+// (registers capped by the launch bounds) when the whole grid fits one wave.
+constexpr int kWideCtasPerSm = 3;
+constexpr int kDenseCtasPerSm = 4;
+constexpr int kDenseRingBytes = 49152;
 
 constexpr int kHeadDim = 128;
 constexpr int kChunks = kHeadDim / 16;       // 16-dim chunks of a K page
@@ -155,8 +161,8 @@ __device__ __forceinline__ float warp_sum_over_gid(float v) {
 // 2 tokens x 2 dims per register, split into an even-dim and an odd-dim
 // fragment row by one byte permute. Output row gid of m-tile mt is then dim
 // 16mt + 2gid and row gid + 8 is dim 16mt + 2gid + 1.
-template <bool kSlotScales, bool kTokenMajor>
-__global__ void __launch_bounds__(kThreads, 3)
+template <bool kSlotScales, bool kTokenMajor, int kMinCtasPerSm>
+__global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
     pda_split_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v) {
   extern __shared__ __align__(128) uint8_t smem[];
