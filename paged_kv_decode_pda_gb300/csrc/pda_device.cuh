@@ -113,6 +113,18 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only, both addresses 16-byte
+// aligned), tracked by cp_async_arrive_noinc.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// One arrival on `bar` once every cp.async this thread issued has landed.
+// .noinc: the arrival is part of the count the barrier was initialised with.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // 4-D tiled tensor copy global -> shared through a tensor map in kernel
 // parameter space, completing its bytes on `bar`.
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,

@@ -205,7 +205,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
-      mbar_init(full0 + 8u * i, 1);
+      // slot scales: one more arrival per producer lane (its scale copies)
+      mbar_init(full0 + 8u * i, kSlotScales ? 33u : 1u);
       mbar_init(empty0 + 8u * i, kConsumerWarps);
     }
     *abort_flag = 0;
@@ -247,8 +248,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
         if (lane == 0) {
           const uint32_t sbase = ring_u32 + (uint32_t)stage * p.stage_bytes;
           const uint32_t bar = full0 + 8u * stage;
-          const uint32_t row_bytes = (uint32_t)bs * 4u;
-          mbar_arrive_expect_tx(bar, (2u * page_bytes + (kSlotScales ? 2u * row_bytes : 0u)) * (uint32_t)np);
+          mbar_arrive_expect_tx(bar, 2u * page_bytes * (uint32_t)np);
 #pragma unroll
           for (int t = 0; t < kMaxPagesPerStage; ++t) {
             if (t < np) {
@@ -265,13 +265,31 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
                 bulk_g2s(sbase + (uint32_t)t * page_bytes, p.k_cache + off, page_bytes, bar);
                 bulk_g2s(sbase + (uint32_t)(PPS + t) * page_bytes, p.v_cache + off, page_bytes, bar);
               }
-              if constexpr (kSlotScales) {
-                const size_t srow = ((size_t)blk[t] * p.num_kv_heads + kvh) * (size_t)bs;
-                bulk_g2s(sbase + p.scale_off + (uint32_t)t * row_bytes, p.k_scales + srow, row_bytes, bar);
-                bulk_g2s(sbase + p.scale_off + (uint32_t)(PPS + t) * row_bytes, p.v_scales + srow, row_bytes, bar);
-              }
             }
           }
+        }
+        if constexpr (kSlotScales) {
+          // The stage's K and V scale rows (np pages x bs floats each) as
+          // 16-byte cp.async pieces spread over the warp: tiny rows would
+          // cost a bulk-copy operation each. Every lane then arrives once on
+          // the full barrier when its pieces have landed.
+          const int per_row = bs / 4;
+          const int per_table = np * per_row;
+          for (int c0 = 0; c0 < 2 * per_table; c0 += 32) {  // warp-uniform trip count
+            const int c = min(c0 + lane, 2 * per_table - 1);
+            const int table = c / per_table;
+            const int t = (c % per_table) / per_row;
+            const int piece = c % per_row;
+            const int b = __shfl_sync(0xffffffffu, my_block, (j + t) & 31);
+            if (c0 + lane < 2 * per_table) {
+              const float* src =
+                  (table ? p.v_scales : p.k_scales) + ((size_t)b * p.num_kv_heads + kvh) * (size_t)bs + 4 * piece;
+              cp_async_16(ring_u32 + (uint32_t)stage * p.stage_bytes + p.scale_off +
+                              (uint32_t)((table * PPS + t) * bs * 4 + piece * 16),
+                          src);
+            }
+          }
+          cp_async_arrive_noinc(full0 + 8u * stage);
         }
         __syncwarp();
       }
@@ -354,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
     const uint32_t sbase = ring_u32 + (uint32_t)stage * p.stage_bytes;
     if constexpr (kSlotScales) {
       if (fill == 0) {
-        const float v0 = *reinterpret_cast<const float*>(smem + stage * p.stage_bytes + p.scale_off +
+        const float v0 = *reinterpret_cast<const float*>(ring + stage * p.stage_bytes + p.scale_off +
                                                          (uint32_t)PPS * (uint32_t)bs * 4u);
         if (isfinite(v0) && v0 != 0.f) {
           vref = v0;
@@ -396,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
       const bool vB = tok0 + tokB < L;
       float lscA = lsc, lscB = lsc, vsA = 1.f, vsB = 1.f;
       if constexpr (kSlotScales) {
-        const uint8_t* ks = smem + stage * p.stage_bytes + p.scale_off + (pg * bs + sub * 16) * 4;
+        const uint8_t* ks = ring + stage * p.stage_bytes + p.scale_off + (pg * bs + sub * 16) * 4;
         const uint8_t* vs = ks + PPS * bs * 4;
         // Scales of slots past the length may hold anything (even NaN).
         lscA *= vA ? reinterpret_cast<const float*>(ks)[tokA] : 0.f;

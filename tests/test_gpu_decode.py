@@ -258,7 +258,7 @@ def test_profile_events():
 
 # ------------------------------------------------------- per-slot scales
 
-@pytest.mark.parametrize("bs,splits", [(16, 0), (16, 3), (64, 0), (64, 2)])
+@pytest.mark.parametrize("bs,splits", [(16, 0), (16, 3), (32, 0), (64, 0), (64, 2), (128, 0), (128, 2)])
 def test_slot_scales_parity(bs, splits):
     import oracle
     lens = [1, 37, 300, 1024, 16]
