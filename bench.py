@@ -22,6 +22,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -191,20 +192,41 @@ class ClockSampler:
                 "power_w_max": max(pw) if pw else None, "samples": len(rows), "reasons": sorted(reasons)}
 
 
-def oracle_sample_rate(batch, budget_s: float, max_seqs: int | None = None):
+def host_cpu_name() -> str:
+    """The host CPU model as the OS reports it (x86 'model name'; on Arm the
+    implementer/part codes when no name is given), with the online core count."""
+    name = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        for key in ("model name", "Model", "CPU part"):
+            for line in info.splitlines():
+                if line.startswith(key):
+                    name = line.split(":", 1)[1].strip()
+                    break
+            if name:
+                break
+    except OSError:
+        pass
+    return "%s (%d cores online)" % (name or platform.machine(), os.cpu_count() or 0)
+
+
+def oracle_sample_rate(batch, budget_s: float, max_seqs: int | None = None, threads: int = 0):
     """Time the fp64 oracle on the first n sequences of the batch, n grown
-    until about budget_s of wall time; returns (GB/s, description, cores)."""
+    until about budget_s of wall time, on `threads` OpenMP threads (0: all);
+    returns (GB/s, description, threads, n, seconds)."""
     import oracle
 
     cfg = batch.cfg
     raw = batch.raw()
-    threads = oracle.max_threads()
+    threads = threads or oracle.max_threads()
     n = 1
     S = cfg.num_seqs if max_seqs is None else min(cfg.num_seqs, max_seqs)
     while True:
         ids = list(range(n))
         t0 = time.perf_counter()
-        oracle.decode(**raw, scale=cfg.scale, k_scale=cfg.k_scale, v_scale=cfg.v_scale, seq_ids=ids)
+        oracle.decode(**raw, scale=cfg.scale, k_scale=cfg.k_scale, v_scale=cfg.v_scale, seq_ids=ids,
+                      num_threads=threads)
         dt = time.perf_counter() - t0
         if dt >= budget_s or n >= S:
             break
@@ -242,7 +264,13 @@ def run_ours(args, ws, rank, local):
                                                  for _ in range(replicas - 1)]
     nsplit = pda.plan_splits(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq,
                              cfg.block_size)
-    kernels_per_call = 1 + (1 if nsplit > 1 else 0)
+    if args.variant in ("plain", "ex", "shuffled_v"):
+        kernels_per_call = pda.plan_launches(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads,
+                                             cfg.max_num_blocks_per_seq, cfg.block_size)
+    else:   # per-unit kernel (+ merge)
+        kernels_per_call = 1 + (1 if nsplit > 1 else 0)
+    kernel_kind = pda.KERNEL_NAMES[pda.plan_kernel(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads,
+                                                   cfg.max_num_blocks_per_seq, cfg.block_size)]
     stream = torch.cuda.Stream(device=dev)
     out = torch.empty_like(batch.q)
     pda.reserve(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq, cfg.block_size,
@@ -375,7 +403,9 @@ def run_ours(args, ws, rank, local):
     cpu = None
     if not args.no_cpu_baseline:
         rate, desc, cores, _, _ = oracle_sample_rate(batch, budget_s=10.0)
-        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+        rate1, desc1, _, _, _ = oracle_sample_rate(batch, budget_s=4.0, threads=1)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
+               "one_core": {"value": rate1, "sample": desc1}, "host_cpu": host_cpu_name()}
 
     line = {
         "metric": METRIC,
@@ -395,7 +425,7 @@ def run_ours(args, ws, rank, local):
         "data": "synthetic (seeded N(0,1) q; K/V N(0,1) quantised to e4m3 with scale 0.05; shuffled block tables)",
         "config": {"workload": cfg.name, "variant": args.variant, "num_seqs": cfg.num_seqs, "num_heads": cfg.num_heads,
                    "num_kv_heads": cfg.num_kv_heads, "head_size": cfg.head_size, "block_size": cfg.block_size,
-                   "ctx": cfg.ctx if cfg.ctx else list(cfg.ctx_range), "kv_splits": nsplit,
+                   "ctx": cfg.ctx if cfg.ctx else list(cfg.ctx_range), "kv_splits": nsplit, "decode_kernel": kernel_kind if args.variant in ("plain", "ex", "shuffled_v") else None,
                    "bytes_per_call": bytes_per_call,
                    "l2": "KV pool %.2f GB x %d replica(s) >= 3x L2 (%d MB); no flush needed" % (
                        kv_bytes / 1e9, replicas, l2 >> 20),
@@ -435,7 +465,8 @@ def run_reference(args, ws, rank, local):
     sample_bytes = workloads.algorithmic_bytes(cfg.with_(num_seqs=n), lens)
 
     def step():
-        oracle.decode(**raw, scale=cfg.scale, k_scale=cfg.k_scale, v_scale=cfg.v_scale, seq_ids=ids)
+        oracle.decode(**raw, scale=cfg.scale, k_scale=cfg.k_scale, v_scale=cfg.v_scale, seq_ids=ids,
+                      num_threads=threads)
 
     for _ in range(args.warmup):
         step()

@@ -265,16 +265,20 @@ pda_status pda_reshape_and_cache(const void* key, const void* value, void* k_cac
  * not add to the device's allocation (for example under a strict memory
  * budget or an allocator that must see every byte), or a caller whose first
  * use of a shape would otherwise trigger an allocation at a bad moment. This
- * entry point computes exactly what pda_decode computes, with the same
- * kernels, split count and results, but its partials live in a fixed 16 MiB
- * array compiled into the library: every GPU that loads the library holds
- * that array until the process exits. It calls no cudaMalloc, cudaFree or
- * other allocating routine.
+ * entry point computes what pda_decode computes, with the same per-unit
+ * arithmetic, but always on the per-unit decode kernel with 3 CTAs per SM
+ * and the split count pda_choose_splits gives for that residency; its
+ * partials live in a fixed 16 MiB array compiled into the library: every
+ * GPU that loads the library holds that array until the process exits. It
+ * calls no cudaMalloc, cudaFree or other allocating routine. Where
+ * pda_decode plans the same split count (every batch that does not fit one
+ * wave of 4 CTAs per SM) the results are bitwise equal; otherwise they
+ * agree to rounding.
  *
  * Arguments, layouts, supported set and ordering are pda_decode's. Limit:
  * num_seqs * num_heads * splits * 520 bytes must fit in 16 MiB (splits is
- * the split count pda_plan_splits reports; a call that needs one split uses
- * no scratch at all); larger calls return PDA_ERR_NOALLOC_CAPACITY before
+ * the split count above; a call that needs one split uses no scratch at
+ * all); larger calls return PDA_ERR_NOALLOC_CAPACITY before
  * launching anything. The first call on each device also looks up the
  * array's device address and the device's properties (no allocation); make
  * that first call outside any stream capture. All calls on a device share
@@ -318,6 +322,32 @@ int pda_choose_splits(int num_seqs, int num_kv_heads, int max_num_blocks_per_seq
 int pda_plan_splits(int num_seqs, int num_heads, int num_kv_heads, int max_num_blocks_per_seq,
                     int block_size);
 
+/* Decode kernel instances (pda_plan_kernel). */
+typedef enum {
+  PDA_KERNEL_PER_UNIT = 0,       /* one CTA per work unit, 3 CTAs per SM, 64 KiB page ring */
+  PDA_KERNEL_PER_UNIT_DENSE = 1, /* one CTA per work unit, 4 CTAs per SM, 48 KiB page ring */
+  PDA_KERNEL_PERSISTENT = 2      /* one CTA per resident slot working through a queue of units */
+} pda_kernel;
+
+/*
+ * pda_plan_kernel -- the decode kernel instance pda_decode (and pda_decode_ex)
+ * would launch on the current device for these sizes: the dense per-unit
+ * instance when the planned grid fits one wave of 4 CTAs per SM, else the
+ * persistent kernel. A call captured into a CUDA graph without a prior
+ * pda_reserve (so with no workspace for the persistent kernel's queue) runs
+ * the 3-CTA per-unit instance instead. Diagnostic; returns < 0 on error.
+ */
+int pda_plan_kernel(int num_seqs, int num_heads, int num_kv_heads, int max_num_blocks_per_seq, int block_size);
+
+/*
+ * pda_plan_launches -- kernels one pda_decode call launches for these sizes
+ * on the current device: the decode kernel, plus the unit-order kernel when
+ * the persistent kernel has more units than resident CTAs (up to 16384
+ * units), plus the merge kernel when the call splits. 0 for num_seqs == 0;
+ * < 0 on error. Diagnostic (counts graph nodes, profiler launches).
+ */
+int pda_plan_launches(int num_seqs, int num_heads, int num_kv_heads, int max_num_blocks_per_seq, int block_size);
+
 /*
  * pda_set_split_override -- force the split count of later pda_decode calls
  * (process-wide; 0 restores the heuristic). For tests and measurements.
@@ -348,8 +378,9 @@ pda_status pda_query_device_status(cudaStream_t stream, int* code);
 /*
  * pda_set_profile_events -- when both events are non-NULL, later pda_decode
  * calls record `before` immediately before and `after` immediately after the
- * split-KV decode kernel on their stream (capturable). NULL, NULL turns it
- * off. Process-wide; for measurement only.
+ * split-KV decode kernel on their stream (capturable); with the persistent
+ * kernel's unit-order kernel, `before` precedes that one too (the two run
+ * overlapped). NULL, NULL turns it off. Process-wide; for measurement only.
  */
 void pda_set_profile_events(cudaEvent_t before, cudaEvent_t after);
 

@@ -15,6 +15,10 @@ from ._binding import (  # noqa: F401
     PDA_ERR_NOALLOC_CAPACITY,
     PDA_ERR_UNSUPPORTED,
     PDA_ERR_WORKSPACE,
+    KERNEL_NAMES,
+    PDA_KERNEL_PER_UNIT,
+    PDA_KERNEL_PER_UNIT_DENSE,
+    PDA_KERNEL_PERSISTENT,
     PDA_KV_NATIVE,
     PDA_KV_SHUFFLED_V,
     PDA_OK,
@@ -29,6 +33,8 @@ from ._binding import (  # noqa: F401
     decode_strided,
     decode_raw,
     load,
+    plan_kernel,
+    plan_launches,
     plan_splits,
     query_device_status,
     release,

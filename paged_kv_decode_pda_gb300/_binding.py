@@ -32,6 +32,8 @@ SIGNATURES = {
     "pda_status_string": (ctypes.c_char_p, [_I]),
     "pda_choose_splits": (_I, [_I, _I, _I, _I, _I, _I]),
     "pda_plan_splits": (_I, [_I, _I, _I, _I, _I]),
+    "pda_plan_kernel": (_I, [_I, _I, _I, _I, _I]),
+    "pda_plan_launches": (_I, [_I, _I, _I, _I, _I]),
     "pda_set_split_override": (None, [_I]),
     "pda_reserve": (_I, [_I, _I, _I, _I, _I, _P]),
     "pda_release": (_I, []),
@@ -274,6 +276,27 @@ def plan_splits(num_seqs, num_heads, num_kv_heads, max_num_blocks_per_seq, block
     n = load().pda_plan_splits(num_seqs, num_heads, num_kv_heads, max_num_blocks_per_seq, block_size)
     if n < 1:
         raise PdaError(PDA_ERR_CUDA, "pda_plan_splits")
+    return n
+
+
+PDA_KERNEL_PER_UNIT, PDA_KERNEL_PER_UNIT_DENSE, PDA_KERNEL_PERSISTENT = 0, 1, 2
+KERNEL_NAMES = {PDA_KERNEL_PER_UNIT: "per-unit (3 CTAs/SM)", PDA_KERNEL_PER_UNIT_DENSE: "per-unit dense (4 CTAs/SM)",
+                PDA_KERNEL_PERSISTENT: "persistent"}
+
+
+def plan_kernel(num_seqs, num_heads, num_kv_heads, max_num_blocks_per_seq, block_size) -> int:
+    """The decode kernel instance (PDA_KERNEL_*) pda_decode would launch for these sizes."""
+    k = load().pda_plan_kernel(num_seqs, num_heads, num_kv_heads, max_num_blocks_per_seq, block_size)
+    if k < 0:
+        raise PdaError(PDA_ERR_CUDA, "pda_plan_kernel")
+    return k
+
+
+def plan_launches(num_seqs, num_heads, num_kv_heads, max_num_blocks_per_seq, block_size) -> int:
+    """Kernels one pda_decode call launches for these sizes."""
+    n = load().pda_plan_launches(num_seqs, num_heads, num_kv_heads, max_num_blocks_per_seq, block_size)
+    if n < 0:
+        raise PdaError(PDA_ERR_CUDA, "pda_plan_launches")
     return n
 
 

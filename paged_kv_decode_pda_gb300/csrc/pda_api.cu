@@ -24,7 +24,7 @@ std::atomic<cudaEvent_t> g_prof_before{nullptr};
 std::atomic<cudaEvent_t> g_prof_after{nullptr};
 
 // Decode kernel instances the library launches.
-enum KernelKind { kPlainWide = 0, kPlainDense, kSlotWide, kTokenWide, kTokenDense, kNumKinds };
+enum KernelKind { kPlainWide = 0, kPlainDense, kSlotWide, kTokenWide, kTokenDense, kPersistWide, kNumKinds };
 
 struct DeviceInfo {
   int sm_count = 0;
@@ -48,6 +48,8 @@ struct RingShape {
   int num_stages;
   uint32_t stage_bytes;
   uint32_t scale_off;
+  uint32_t q_off = 0;    // persistent kernel: the unit's query rows
+  uint32_t hdr_off = 0;  // persistent kernel: the stage header
   size_t smem_bytes;
 };
 
@@ -63,6 +65,21 @@ RingShape ring_shape(int bs, bool slot_scales = false, int ring_bytes = pda::kRi
   if (ring < merge) ring = merge;
   // + 1 KiB so the kernel can align the ring to 1024 bytes (128-byte swizzle).
   r.smem_bytes = ring + 2 * 8 * (size_t)r.num_stages + 16 + 1024;
+  return r;
+}
+
+// Persistent-kernel stage: K and V pages, then the unit's query rows, then
+// the header; at least the CTA merge area (a unit's last stage holds its
+// merge). Barriers: full and empty per stage plus one consumer barrier.
+RingShape persistent_ring_shape(int bs) {
+  RingShape r = ring_shape(bs);
+  const uint32_t kv = r.scale_off;
+  r.q_off = kv;
+  uint32_t h = kv + pda::kStageQBytes;
+  if (h < pda::kMergeBytes) h = pda::kMergeBytes;
+  r.hdr_off = (h + 15u) & ~15u;
+  r.stage_bytes = r.hdr_off + pda::kStageHeaderBytes;
+  r.smem_bytes = (size_t)r.num_stages * r.stage_bytes + 8 * (2 * (size_t)r.num_stages + 1) + 16 + 1024;
   return r;
 }
 
@@ -174,6 +191,7 @@ bool is_dense(KernelKind k) { return k == kPlainDense || k == kTokenDense; }
 bool is_slot(KernelKind k) { return k == kSlotWide; }
 
 RingShape ring_for(KernelKind k, int bs) {
+  if (k == kPersistWide) return persistent_ring_shape(bs);
   return ring_shape(bs, is_slot(k), is_dense(k) ? pda::kDenseRingBytes : pda::kRingBytes);
 }
 
@@ -183,6 +201,7 @@ const void* kernel_fn(KernelKind k) {
     case kPlainDense: return (const void*)pda::pda_split_decode_kernel<false, false, pda::kDenseCtasPerSm>;
     case kSlotWide: return (const void*)pda::pda_split_decode_kernel<true, false, pda::kWideCtasPerSm>;
     case kTokenWide: return (const void*)pda::pda_split_decode_kernel<false, true, pda::kWideCtasPerSm>;
+    case kPersistWide: return (const void*)pda::pda_persistent_decode_kernel<pda::kWideCtasPerSm>;
     default: return (const void*)pda::pda_split_decode_kernel<false, true, pda::kDenseCtasPerSm>;
   }
 }
@@ -233,6 +252,13 @@ int resolve_splits(int num_seqs, int num_kv_heads, int max_blocks, int bs, int s
   return n;
 }
 
+// The wide instance of plain calls: the persistent kernel unless built out.
+#ifdef PDA_DISABLE_PERSISTENT
+constexpr KernelKind kWidePlain = kPlainWide;
+#else
+constexpr KernelKind kWidePlain = kPersistWide;
+#endif
+
 // Split count and kernel instance for a call: the wide instance (3 CTAs per
 // SM, 64 KiB ring) unless its planned grid fits one wave of the dense
 // instance (4 CTAs per SM, 48 KiB ring), which then runs the whole batch at
@@ -241,7 +267,14 @@ int resolve_splits(int num_seqs, int num_kv_heads, int max_blocks, int bs, int s
 struct Plan {
   KernelKind kind;
   int nsplit;
+  unsigned grid = 0;         // persistent kernel: CTAs (resident slots, at most one per unit)
+  long long ordered = 0;     // persistent kernel: units handed out longest first (0: ticket order)
 };
+
+// Largest batch (in work units) whose units the persistent kernel takes in
+// longest-first order: the order kernel is one CTA, so its time grows with
+// the units, and it must finish while the CTAs work on their first units.
+constexpr long long kMaxOrderedUnits = 16384;
 
 pda_status plan_call(int dev, int num_seqs, int num_kv_heads, int max_blocks, int bs, KernelKind wide,
                      KernelKind dense, Plan* out) {
@@ -261,6 +294,12 @@ pda_status plan_call(int dev, int num_seqs, int num_kv_heads, int max_blocks, in
       out->nsplit = resolve_splits(num_seqs, num_kv_heads, MB, bs, sms, occ_d);
     }
   }
+  if (out->kind == kPersistWide) {
+    const long long units = (long long)num_seqs * num_kv_heads * out->nsplit;
+    const long long slots = (long long)sms * occ;
+    out->grid = (unsigned)(units < slots ? units : slots);
+    out->ordered = (units > slots && units <= kMaxOrderedUnits) ? units - slots : 0;
+  }
   return PDA_OK;
 }
 
@@ -273,11 +312,33 @@ cudaError_t record_profile_event(cudaEvent_t e, cudaStream_t s) {
   return cudaEventRecord(e, s);
 }
 
-size_t workspace_bytes(int num_seqs, int num_heads, int nsplit) {
+// Workspace of one (device, stream): kQueueBytes of work-queue counters for
+// the persistent kernel (zeroed when allocated; each launch leaves them at
+// zero), the persistent kernel's unit order, then the split partials
+// O [S][H][nsplit][D] and (m, l) [S][H][nsplit][2].
+constexpr size_t kQueueBytes = 256;
+
+// Bytes of the split partials (0 for one split).
+size_t partial_bytes(int num_seqs, int num_heads, int nsplit) {
   if (nsplit <= 1) return 0;
   const size_t rows = (size_t)num_seqs * num_heads * nsplit;
-  const size_t o = rows * kHeadDim * sizeof(float);
-  return o + rows * 2 * sizeof(float);
+  return rows * kHeadDim * sizeof(float) + rows * 2 * sizeof(float);
+}
+
+struct WsLayout {
+  size_t order_off = 0;
+  size_t part_off = 0;
+  size_t bytes = 0;
+};
+
+WsLayout ws_layout(int num_seqs, int num_heads, const Plan& pl) {
+  WsLayout w;
+  const size_t part = partial_bytes(num_seqs, num_heads, pl.nsplit);
+  if (pl.kind != kPersistWide && part == 0) return w;
+  w.order_off = kQueueBytes;
+  w.part_off = w.order_off + (((size_t)pl.ordered * sizeof(int) + 255) & ~(size_t)255);
+  w.bytes = w.part_off + part;
+  return w;
 }
 
 // Returns the workspace pointer for (device, stream), growing it with
@@ -298,6 +359,10 @@ pda_status get_workspace(int dev, cudaStream_t stream, size_t bytes, void** out)
   want = (want + 255) & ~(size_t)255;
   void* p = nullptr;
   if (cudaMallocAsync(&p, want, stream) != cudaSuccess) return PDA_ERR_CUDA;
+  if (cudaMemsetAsync(p, 0, kQueueBytes, stream) != cudaSuccess) {
+    cudaFreeAsync(p, stream);
+    return PDA_ERR_CUDA;
+  }
   if (ws.ptr) cudaFreeAsync(ws.ptr, stream);
   ws.ptr = p;
   ws.bytes = want;
@@ -322,14 +387,21 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PDA_ERR_CUDA;
-  const KernelKind wide = slot ? kSlotWide : (tm ? kTokenWide : kPlainWide);
+  const KernelKind wide = slot ? kSlotWide : (tm ? kTokenWide : kWidePlain);
   const KernelKind dense = slot ? kSlotWide : (tm ? kTokenDense : kPlainDense);
   Plan pl;
   st = plan_call(dev, num_seqs, num_kv_heads, max_num_blocks_per_seq, block_size, wide, dense, &pl);
   if (st != PDA_OK) return st;
   const int nsplit = pl.nsplit;
   void* ws = nullptr;
-  st = get_workspace(dev, stream, workspace_bytes(num_seqs, num_heads, nsplit), &ws);
+  WsLayout wl = ws_layout(num_seqs, num_heads, pl);
+  st = get_workspace(dev, stream, wl.bytes, &ws);
+  if (st == PDA_ERR_WORKSPACE && pl.kind == kPersistWide && nsplit == 1) {
+    // Captured without pda_reserve: the per-unit kernel needs no workspace.
+    pl.kind = kPlainWide;
+    wl = WsLayout();
+    st = PDA_OK;
+  }
   if (st != PDA_OK) return st;
 
   const RingShape rs = ring_for(pl.kind, block_size);
@@ -340,8 +412,9 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
   p.v_cache = static_cast<const uint8_t*>(v_cache);
   p.block_tables = block_tables;
   p.seq_lens = seq_lens;
-  p.part_o = static_cast<float*>(ws);
-  p.part_ml = ws ? static_cast<float*>(ws) + (size_t)num_seqs * num_heads * nsplit * kHeadDim : nullptr;
+  unsigned* queue = static_cast<unsigned*>(ws);
+  p.part_o = nsplit > 1 ? reinterpret_cast<float*>(static_cast<char*>(ws) + wl.part_off) : nullptr;
+  p.part_ml = nsplit > 1 ? p.part_o + (size_t)num_seqs * num_heads * nsplit * kHeadDim : nullptr;
   p.num_heads = num_heads;
   p.num_kv_heads = num_kv_heads;
   p.gqa = num_heads / num_kv_heads;
@@ -352,6 +425,8 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
   p.num_stages = rs.num_stages;
   p.stage_bytes = rs.stage_bytes;
   p.scale_off = rs.scale_off;
+  p.q_off = rs.q_off;
+  p.hdr_off = rs.hdr_off;
   p.k_scales = slot ? k_scales : nullptr;
   p.v_scales = slot ? v_scales : nullptr;
   p.logit_scale_log2 = (float)((double)scale * (slot ? 1.0 : (double)k_scale) * 1.4426950408889634);
@@ -372,6 +447,44 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
   const CUtensorMap& mk = tm ? tm->k : g_no_map;
   const CUtensorMap& mv = tm ? tm->v : g_no_map;
   switch (pl.kind) {
+    case kPersistWide: {
+      const int units = num_seqs * num_kv_heads * nsplit;
+      if (pl.ordered > 0) {
+        // The order kernel, then the decode kernel as its programmatic
+        // dependent: the decode CTAs start on their first units at once and
+        // wait for the order only before taking a second one.
+        pda::OrderParams op;
+        op.seq_lens = seq_lens;
+        op.order = reinterpret_cast<int*>(static_cast<char*>(ws) + wl.order_off);
+        op.first = (int)pl.grid;
+        op.num_units = units;
+        op.num_kv_heads = num_kv_heads;
+        op.nsplit = nsplit;
+        op.block_size = block_size;
+        op.max_blocks = max_num_blocks_per_seq;
+        op.max_split_pages = (max_num_blocks_per_seq + nsplit - 1) / nsplit;
+        pda::pda_order_units_kernel<<<1, pda::kOrderThreads, 0, stream>>>(op);
+        if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
+        p.unit_order = op.order;
+        cudaLaunchConfig_t lc = {};
+        lc.gridDim = dim3(pl.grid);
+        lc.blockDim = dim3(pda::kThreads);
+        lc.dynamicSmemBytes = rs.smem_bytes;
+        lc.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        lc.attrs = attr;
+        lc.numAttrs = 1;
+        if (cudaLaunchKernelEx(&lc, pda::pda_persistent_decode_kernel<pda::kWideCtasPerSm>, p, queue, units) !=
+            cudaSuccess)
+          return PDA_ERR_CUDA;
+      } else {
+        pda::pda_persistent_decode_kernel<pda::kWideCtasPerSm><<<pl.grid, pda::kThreads, rs.smem_bytes, stream>>>(
+            p, queue, units);
+      }
+      break;
+    }
     case kPlainWide:
       pda::pda_split_decode_kernel<false, false, pda::kWideCtasPerSm><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(
           p, mk, mv);
@@ -470,10 +583,39 @@ int pda_plan_splits(int num_seqs, int num_heads, int num_kv_heads, int max_num_b
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
   Plan pl;
-  if (plan_call(dev, num_seqs, num_kv_heads, max_num_blocks_per_seq, block_size, kPlainWide, kPlainDense, &pl) !=
+  if (plan_call(dev, num_seqs, num_kv_heads, max_num_blocks_per_seq, block_size, kWidePlain, kPlainDense, &pl) !=
       PDA_OK)
     return -1;
   return pl.nsplit;
+}
+
+int pda_plan_kernel(int num_seqs, int num_heads, int num_kv_heads, int max_num_blocks_per_seq, int block_size) {
+  (void)num_heads;
+  if (block_size <= 0 || block_size % 16 != 0 || block_size > 128) return -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  Plan pl;
+  if (plan_call(dev, num_seqs, num_kv_heads, max_num_blocks_per_seq, block_size, kWidePlain, kPlainDense, &pl) !=
+      PDA_OK)
+    return -1;
+  switch (pl.kind) {
+    case kPlainDense: return PDA_KERNEL_PER_UNIT_DENSE;
+    case kPersistWide: return PDA_KERNEL_PERSISTENT;
+    default: return PDA_KERNEL_PER_UNIT;
+  }
+}
+
+int pda_plan_launches(int num_seqs, int num_heads, int num_kv_heads, int max_num_blocks_per_seq, int block_size) {
+  (void)num_heads;
+  if (num_seqs == 0) return 0;
+  if (block_size <= 0 || block_size % 16 != 0 || block_size > 128) return -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  Plan pl;
+  if (plan_call(dev, num_seqs, num_kv_heads, max_num_blocks_per_seq, block_size, kWidePlain, kPlainDense, &pl) !=
+      PDA_OK)
+    return -1;
+  return 1 + (pl.ordered > 0 ? 1 : 0) + (pl.nsplit > 1 ? 1 : 0);
 }
 
 void pda_set_profile_events(cudaEvent_t before, cudaEvent_t after) {
@@ -495,12 +637,12 @@ pda_status pda_reserve(int num_seqs, int num_heads, int num_kv_heads, int max_nu
   if (cudaGetDevice(&dev) != cudaSuccess) return PDA_ERR_CUDA;
   // Size for the largest plan any entry point makes for these sizes.
   size_t bytes = 0;
-  const KernelKind pairs[3][2] = {{kPlainWide, kPlainDense}, {kSlotWide, kSlotWide}, {kTokenWide, kTokenDense}};
+  const KernelKind pairs[3][2] = {{kWidePlain, kPlainDense}, {kSlotWide, kSlotWide}, {kTokenWide, kTokenDense}};
   for (const auto& pr : pairs) {
     Plan pl;
     pda_status st = plan_call(dev, num_seqs, num_kv_heads, max_num_blocks_per_seq, block_size, pr[0], pr[1], &pl);
     if (st != PDA_OK) return st;
-    const size_t b = workspace_bytes(num_seqs, num_heads, pl.nsplit);
+    const size_t b = ws_layout(num_seqs, num_heads, pl).bytes;
     bytes = b > bytes ? b : bytes;
   }
   void* ws = nullptr;
@@ -725,7 +867,7 @@ extern "C" pda_status pda_decode_noalloc(void* out, const void* q, const void* k
   if (st != PDA_OK) return st;
   const int MB = max_num_blocks_per_seq > 0 ? max_num_blocks_per_seq : 1;
   const int nsplit = resolve_splits(num_seqs, num_kv_heads, MB, block_size, d.sm_count, d.occ[block_size / 16]);
-  if (workspace_bytes(num_seqs, num_heads, nsplit) > kNoAllocScratchBytes) return PDA_ERR_NOALLOC_CAPACITY;
+  if (partial_bytes(num_seqs, num_heads, nsplit) > kNoAllocScratchBytes) return PDA_ERR_NOALLOC_CAPACITY;
 
   const RingShape rs = ring_shape(block_size);
   float* scratch = static_cast<float*>(d.scratch);

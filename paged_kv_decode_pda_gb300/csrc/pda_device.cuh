@@ -21,6 +21,7 @@ enum : unsigned int {
   kStatusDrainTimeout = 1u << 2,      // copies still in flight at exit after the limit
   kStatusTestWaitTimeout = 1u << 3,   // pda_test_bounded_wait gave up (expected)
   kStatusBadSlot = 1u << 4,           // reshape_and_cache saw a slot past the pool (skipped)
+  kStatusMergeWaitTimeout = 1u << 5,  // persistent decode: consumer warps never met to merge a unit
 };
 
 // Limit on any single barrier wait. Healthy waits last microseconds; the
@@ -200,6 +201,22 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float r;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
+}
+
+// Programmatic dependent launch: a kernel launched as the programmatic
+// dependent of the previous one waits here until that kernel has finished
+// and its memory writes are visible; the previous kernel lets it launch
+// early with grid_dependents_launch().
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// 8-byte shared-memory load (8-byte aligned address).
+__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
 }
 
 __device__ __forceinline__ uint2 ld_nc_v2(const void* p) {

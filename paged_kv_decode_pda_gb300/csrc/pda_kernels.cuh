@@ -85,6 +85,13 @@ struct DecodeParams {
   const float* sinks = nullptr; // [H] per-head sink logits (scale * q.k units), or none
   int out_fp8 = 0;              // 1: out holds E4M3(o / out_scale) bytes
   float out_scale = 1.f;
+  // Persistent kernel: stage offsets of the unit's query rows and of the
+  // stage header.
+  uint32_t q_off = 0;
+  uint32_t hdr_off = 0;
+  // Persistent kernel: unit of ticket gridDim.x + i is unit_order[i]
+  // (longest first, written by pda_order_units_kernel), or ticket order.
+  const int* unit_order = nullptr;
 };
 
 // Final normalisation shared by the decode kernel (one split) and the merge
@@ -143,6 +150,272 @@ __device__ __forceinline__ float warp_sum_over_gid(float v) {
   v += __shfl_xor_sync(0xffffffffu, v, 8);
   v += __shfl_xor_sync(0xffffffffu, v, 16);
   return v;
+}
+
+// One consumer warp's share of a work unit: the GQA group's Q^T fragments
+// and the running softmax state (m, l, O^T) of the unit, updated one
+// 16-token tile at a time (the template flags are those of the kernels).
+template <bool kSlotScales, bool kTokenMajor>
+struct TileWorker {
+  int gid, tig;
+  uint32_t k_lane_off;   // page-major K: ldmatrix row of this lane
+  uint32_t tm_row, tm_xor, tm_hi;  // token-major tiles: row, swizzle and chunk half
+  uint32_t v_row, v_lane_off;
+  bool low_quad;
+  int tokA, tokB;        // tokens of accumulator rows gid and gid + 8
+  uint32_t qf[kChunks][2];
+  float m0, m1;          // running max (log2 units), heads 2tig, 2tig+1
+  float l0, l1;          // running partial sums over this lane's tokens
+  float o[kChunks][4];   // O^T: m-tile mt = dims 16mt.. ; cols heads 2tig, 2tig+1
+
+  __device__ __forceinline__ void setup(int lane, int bs, int v_shuffled) {
+    gid = lane >> 2;
+    tig = lane & 3;
+    // ldmatrix row assignment. K: lane l supplies token row_token(l & 15) of
+    // chunk (2kk + (l >> 4)). V: lane l supplies dim (32mp + l).
+    k_lane_off = (uint32_t)(row_token(lane & 15) * 16) + (uint32_t)((lane >> 4) * bs * 16);
+    // Token-major tiles: lane l addresses token row (l & 15), chunk (2j + (l >> 4)),
+    // swizzled by the row's low 3 bits.
+    tm_row = (uint32_t)(lane & 15) * 128u;
+    tm_xor = (uint32_t)(lane & 7);
+    tm_hi = (uint32_t)(lane >> 4);
+    // V: a 16-token tile is 128 rows of 16 bytes at stride v_row (bs for
+    // [D][bs] pages; 16 for shuffled [bs/16][D][16] pages, whose tiles are
+    // contiguous and so bank-conflict free for any block size).
+    v_row = v_shuffled ? 16u : (uint32_t)bs;
+    v_lane_off = (uint32_t)lane * v_row;
+    low_quad = kTokenMajor ? true : tig < 2;
+    tokA = kTokenMajor ? gid : row_token(gid);
+    tokB = kTokenMajor ? gid + 8 : row_token(gid + 8);
+  }
+
+  __device__ __forceinline__ void reset() {
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < kChunks; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  }
+
+  // Q^T fragments (B operand, 16 dims x 8 heads per chunk) in f16 from the
+  // bf16 query row of head `gid` (zeros when gid is past the group). Chunk c
+  // k-slots (2tig, 2tig+1) <- dims 16c+4tig+{0,1}; (2tig+8, 2tig+9) <- dims
+  // 16c+4tig+{2,3}; this matches how K bytes land in the A fragments below.
+  __device__ __forceinline__ void set_q_chunk(int c, uint2 v) {
+    qf[c][0] = pack_f16x2(bf16lo_f32(v.x), bf16hi_f32(v.x));
+    qf[c][1] = pack_f16x2(bf16lo_f32(v.y), bf16hi_f32(v.y));
+  }
+  __device__ __forceinline__ void load_q_global(const __nv_bfloat16* qrow, bool live) {
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) set_q_chunk(c, live ? ld_nc_v2(qrow + 16 * c + 4 * tig) : make_uint2(0u, 0u));
+  }
+  __device__ __forceinline__ void load_q_shared(uint32_t qrow, bool live) {
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c)
+      set_q_chunk(c, live ? ld_shared_v2(qrow + (uint32_t)(16 * c + 4 * tig) * 2u) : make_uint2(0u, 0u));
+  }
+
+  // One 16-token tile: K bytes at kbase, V bytes at vbase (shared), the first
+  // n_valid (>= 1) tokens real. Slot scales: ks / vs point at the tile's 16
+  // K and V scales, vinv is 1 / (the reference V scale).
+  __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int bs, int n_valid, float lsc,
+                                       const float* ks, const float* vs, float vinv) {
+    // ---- S^T = K_tile * Q^T (two independent accumulator chains)
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+    float sd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < kChunks / 2; ++kk) {
+      uint32_t r0, r1, r2, r3;
+      if constexpr (kTokenMajor)
+        ldsm_x4(kbase + tm_row + ((((uint32_t)(2 * kk) + tm_hi) ^ tm_xor) << 4), r0, r1, r2, r3);
+      else
+        ldsm_x4(kbase + k_lane_off + (uint32_t)(2 * kk * bs * 16), r0, r1, r2, r3);
+      mma_f16(sc, e4m3x2_lo_to_f16x2(r0), e4m3x2_lo_to_f16x2(r1), e4m3x2_hi_to_f16x2(r0),
+              e4m3x2_hi_to_f16x2(r1), qf[2 * kk][0], qf[2 * kk][1]);
+      mma_f16(sd, e4m3x2_lo_to_f16x2(r2), e4m3x2_lo_to_f16x2(r3), e4m3x2_hi_to_f16x2(r2),
+              e4m3x2_hi_to_f16x2(r3), qf[2 * kk + 1][0], qf[2 * kk + 1][1]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sc[i] += sd[i];
+
+    // ---- online softmax (exp2 domain); tokens >= n_valid are masked
+    const bool vA = tokA < n_valid;
+    const bool vB = tokB < n_valid;
+    float lscA = lsc, lscB = lsc, vsA = 1.f, vsB = 1.f;
+    if constexpr (kSlotScales) {
+      // Scales of slots past the length may hold anything (even NaN).
+      lscA *= vA ? ks[tokA] : 0.f;
+      lscB *= vB ? ks[tokB] : 0.f;
+      vsA = vA ? vs[tokA] * vinv : 0.f;
+      vsB = vB ? vs[tokB] * vinv : 0.f;
+    }
+    const float s0 = vA ? sc[0] * lscA : -INFINITY;
+    const float s1 = vA ? sc[1] * lscA : -INFINITY;
+    const float s2 = vB ? sc[2] * lscB : -INFINITY;
+    const float s3 = vB ? sc[3] * lscB : -INFINITY;
+    const float mx0 = warp_max_over_gid(fmaxf(s0, s2));
+    const float mx1 = warp_max_over_gid(fmaxf(s1, s3));
+    const float mn0 = fmaxf(m0, mx0);
+    const float mn1 = fmaxf(m1, mx1);
+    const float c0 = fast_exp2(m0 - mn0);
+    const float c1 = fast_exp2(m1 - mn1);
+    m0 = mn0;
+    m1 = mn1;
+    const float p0 = fast_exp2(s0 - mn0);
+    const float p1 = fast_exp2(s1 - mn1);
+    const float p2 = fast_exp2(s2 - mn0);
+    const float p3 = fast_exp2(s3 - mn1);
+    l0 = l0 * c0 + (p0 + p2);
+    l1 = l1 * c1 + (p1 + p3);
+    if (__any_sync(0xffffffffu, (c0 != 1.f) | (c1 != 1.f))) {  // a running max moved
+#pragma unroll
+      for (int mt = 0; mt < kChunks; ++mt) {
+        o[mt][0] *= c0;
+        o[mt][1] *= c1;
+        o[mt][2] *= c0;
+        o[mt][3] *= c1;
+      }
+    }
+    // P^T fragment: transpose (token rows x head cols) to (head rows x token
+    // cols). Lane quads 2 and 3 hold their two token pairs in the other
+    // order (row_token), so they swap the two halves of the B fragment.
+    uint32_t x0, x1;
+    if constexpr (kSlotScales) {
+      x0 = pack_f16x2(p0 * vsA, p1 * vsA);
+      x1 = pack_f16x2(p2 * vsB, p3 * vsB);
+    } else {
+      x0 = pack_f16x2(p0, p1);
+      x1 = pack_f16x2(p2, p3);
+    }
+    const uint32_t t0 = movmatrix_trans(x0);
+    const uint32_t t1 = movmatrix_trans(x1);
+    const uint32_t pb0 = low_quad ? t0 : t1;
+    const uint32_t pb1 = low_quad ? t1 : t0;
+
+    // ---- O^T += V_tile^T * P^T
+    // Page-major V: lane holds V bytes of tokens 4tig..4tig+3 of one dim.
+    // Token-major V (ldmatrix.trans): a register holds tokens (2tig, 2tig+1)
+    // x dims (2gid, 2gid+1) of a chunk; registers 0/2 tokens 0-7, 1/3 8-15.
+    uint32_t vr[kChunks / 2][4];
+#pragma unroll
+    for (int mp = 0; mp < kChunks / 2; ++mp) {
+      if constexpr (kTokenMajor)
+        ldsm_x4_trans(vbase + tm_row + ((((uint32_t)(2 * mp) + tm_hi) ^ tm_xor) << 4), vr[mp][0], vr[mp][1],
+                      vr[mp][2], vr[mp][3]);
+      else
+        ldsm_x4(vbase + v_lane_off + (uint32_t)(32 * mp) * v_row, vr[mp][0], vr[mp][1], vr[mp][2], vr[mp][3]);
+    }
+    if (n_valid < 16) {
+      // Zero the V bytes of tokens >= n_valid: their e4m3 codes may be NaN
+      // and 0 * NaN would poison the accumulator.
+      if constexpr (kTokenMajor) {
+        const uint32_t m_lo = (2 * tig < n_valid ? 0x0000FFFFu : 0u) | (2 * tig + 1 < n_valid ? 0xFFFF0000u : 0u);
+        const uint32_t m_hi =
+            (8 + 2 * tig < n_valid ? 0x0000FFFFu : 0u) | (9 + 2 * tig < n_valid ? 0xFFFF0000u : 0u);
+#pragma unroll
+        for (int mp = 0; mp < kChunks / 2; ++mp) {
+          vr[mp][0] &= m_lo;
+          vr[mp][1] &= m_hi;
+          vr[mp][2] &= m_lo;
+          vr[mp][3] &= m_hi;
+        }
+      } else {
+        const int k = min(max(n_valid - 4 * tig, 0), 4);
+        const uint32_t vmask = k >= 4 ? 0xFFFFFFFFu : ((1u << (8 * k)) - 1u);
+#pragma unroll
+        for (int mp = 0; mp < kChunks / 2; ++mp)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) vr[mp][i] &= vmask;
+      }
+    }
+#pragma unroll
+    for (int mp = 0; mp < kChunks / 2; ++mp) {
+      if constexpr (kTokenMajor) {
+        // bytes (t,d0) (t,d1) (t',d0) (t',d1) -> (t,d0) (t',d0) | (t,d1) (t',d1)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t ya = __byte_perm(vr[mp][2 * h], 0, 0x3120);
+          const uint32_t yb = __byte_perm(vr[mp][2 * h + 1], 0, 0x3120);
+          mma_f16(o[2 * mp + h], e4m3x2_lo_to_f16x2(ya), e4m3x2_hi_to_f16x2(ya), e4m3x2_lo_to_f16x2(yb),
+                  e4m3x2_hi_to_f16x2(yb), pb0, pb1);
+        }
+      } else {
+        mma_f16(o[2 * mp], e4m3x2_lo_to_f16x2(vr[mp][0]), e4m3x2_lo_to_f16x2(vr[mp][1]),
+                e4m3x2_hi_to_f16x2(vr[mp][0]), e4m3x2_hi_to_f16x2(vr[mp][1]), pb0, pb1);
+        mma_f16(o[2 * mp + 1], e4m3x2_lo_to_f16x2(vr[mp][2]), e4m3x2_lo_to_f16x2(vr[mp][3]),
+                e4m3x2_hi_to_f16x2(vr[mp][2]), e4m3x2_hi_to_f16x2(vr[mp][3]), pb0, pb1);
+      }
+    }
+  }
+
+  // This warp's (m, l, O) into the CTA merge area: mo [w][head][kMergeStride],
+  // mml [w][head][2].
+  __device__ __forceinline__ void store_merge(float* mo, float* mml, int warp) {
+    l0 = warp_sum_over_gid(l0);
+    l1 = warp_sum_over_gid(l1);
+    float* mw = mo + warp * kMaxGqa * kMergeStride;
+#pragma unroll
+    for (int mt = 0; mt < kChunks; ++mt) {
+      // accumulator rows gid / gid + 8 of m-tile mt hold these two dims
+      const int d0 = kTokenMajor ? 16 * mt + 2 * gid : 16 * mt + gid;
+      const int d1 = kTokenMajor ? d0 + 1 : d0 + 8;
+      mw[(2 * tig) * kMergeStride + d0] = o[mt][0];
+      mw[(2 * tig + 1) * kMergeStride + d0] = o[mt][1];
+      mw[(2 * tig) * kMergeStride + d1] = o[mt][2];
+      mw[(2 * tig + 1) * kMergeStride + d1] = o[mt][3];
+    }
+    if (gid == 0) {
+      float* ml = mml + warp * kMaxGqa * 2;
+      ml[(2 * tig) * 2 + 0] = m0;
+      ml[(2 * tig) * 2 + 1] = l0;
+      ml[(2 * tig + 1) * 2 + 0] = m1;
+      ml[(2 * tig + 1) * 2 + 1] = l1;
+    }
+  }
+};
+
+// Bytes of the CTA merge area (per-warp O rows and (m, l) pairs).
+constexpr uint32_t kMergeBytes = (uint32_t)(kConsumerWarps * kMaxGqa * (kMergeStride + 2) * sizeof(float));
+
+// Combine the consumer warps' (m, l, O) of unit (s, kvh, split) from the
+// merge area and store the bf16 / e4m3 output (one split) or the fp32
+// partial (several splits). Consumer thread `tid` of kConsumerThreads.
+// vref: the slot-scale variant's reference V scale (1 otherwise).
+template <bool kSlotScales>
+__device__ __forceinline__ void reduce_store(const DecodeParams& p, const float* mo, const float* mml, int tid, int s,
+                                             int kvh, int split, float vref) {
+  const int g = p.gqa;
+  const int H = p.num_heads;
+  for (int i = tid; i < g * kHeadDim; i += kConsumerThreads) {
+    const int hh = i / kHeadDim;
+    const int d = i % kHeadDim;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mml[(w * kMaxGqa + hh) * 2]);
+    float acc = 0.f, den = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float mw = mml[(w * kMaxGqa + hh) * 2];
+        const float f = fast_exp2(mw - M);
+        acc += f * mo[(w * kMaxGqa + hh) * kMergeStride + d];
+        den += f * mml[(w * kMaxGqa + hh) * 2 + 1];
+      }
+    }
+    const int h = kvh * g + hh;
+    if (p.nsplit == 1) {
+      const float zs = p.sinks ? __ldg(p.sinks + h) * 1.4426950408889634f : -INFINITY;
+      const float r = finish(acc, den, M, zs, kSlotScales ? vref : p.v_scale);
+      store_out(p.out, ((size_t)s * H + h) * kHeadDim + d, r, p.out_fp8, p.out_scale);
+    } else {
+      // Slot-scale partials carry their own V reference (the merge then uses 1).
+      const size_t prow = ((size_t)s * H + h) * p.nsplit + split;
+      p.part_o[prow * kHeadDim + d] = kSlotScales ? acc * vref : acc;
+      if (d == 0) {
+        p.part_ml[prow * 2 + 0] = M;
+        p.part_ml[prow * 2 + 1] = den;
+      }
+    }
+  }
 }
 
 // kSlotScales: K/V dequantise with per-slot fp32 tables [NB][Hk][bs] (the
@@ -307,50 +580,17 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
   }
 
   // -------------------------------------------------------------- consumers
-  const int gid = lane >> 2;
-  const int tig = lane & 3;
-
-  // Q^T fragments (B operand, 16 dims x 8 heads per chunk) in f16. Chunk c
-  // k-slots (2tig, 2tig+1) <- dims 16c+4tig+{0,1}; (2tig+8, 2tig+9) <- dims
-  // 16c+4tig+{2,3}; this matches how K bytes land in the A fragments below.
-  uint32_t qf[kChunks][2];
+  TileWorker<kSlotScales, kTokenMajor> w;
+  w.setup(lane, bs, p.v_shuffled);
   {
-    const bool live = gid < g;
-    const __nv_bfloat16* qrow = p.q + ((size_t)s * H + (size_t)kvh * g + (live ? gid : 0)) * kHeadDim;
-#pragma unroll
-    for (int c = 0; c < kChunks; ++c) {
-      uint2 v = live ? ld_nc_v2(qrow + 16 * c + 4 * tig) : make_uint2(0u, 0u);
-      qf[c][0] = pack_f16x2(bf16lo_f32(v.x), bf16hi_f32(v.x));
-      qf[c][1] = pack_f16x2(bf16lo_f32(v.y), bf16hi_f32(v.y));
-    }
+    const bool live = w.gid < g;
+    w.load_q_global(p.q + ((size_t)s * H + (size_t)kvh * g + (live ? w.gid : 0)) * kHeadDim, live);
   }
-
-  // ldmatrix row assignment. K: lane l supplies token row_token(l & 15) of
-  // chunk (2kk + (l >> 4)). V: lane l supplies dim (32mp + l).
-  const uint32_t k_lane_off = (uint32_t)(row_token(lane & 15) * 16) + (uint32_t)((lane >> 4) * bs * 16);
-  // Token-major tiles: lane l addresses token row (l & 15), chunk (2j + (l >> 4)),
-  // swizzled by the row's low 3 bits.
-  const uint32_t tm_row = (uint32_t)(lane & 15) * 128u;
-  const uint32_t tm_xor = (uint32_t)(lane & 7);
-  const uint32_t tm_hi = (uint32_t)(lane >> 4);
-  // V: a 16-token tile is 128 rows of 16 bytes at stride v_row (bs for
-  // [D][bs] pages; 16 for shuffled [bs/16][D][16] pages, whose tiles are
-  // contiguous and so bank-conflict free for any block size).
-  const uint32_t v_row = p.v_shuffled ? 16u : (uint32_t)bs;
-  const uint32_t v_sub = p.v_shuffled ? (uint32_t)(kHeadDim * 16) : 16u;
-  const uint32_t v_lane_off = (uint32_t)lane * v_row;
-  const bool low_quad = kTokenMajor ? true : tig < 2;
-  const int tokA = kTokenMajor ? gid : row_token(gid);
-  const int tokB = kTokenMajor ? gid + 8 : row_token(gid + 8);
-
-  float m0 = -INFINITY, m1 = -INFINITY;   // running max (log2 units), heads 2tig, 2tig+1
-  float l0 = 0.f, l1 = 0.f;               // running partial sums over this lane's tokens
-  float o[kChunks][4];                    // O^T: m-tile mt = dims 16mt.. ; cols heads 2tig, 2tig+1
-#pragma unroll
-  for (int i = 0; i < kChunks; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  w.reset();
 
   const float lsc = p.logit_scale_log2;
   const int tiles_per_page = bs / 16;
+  const uint32_t v_sub = p.v_shuffled ? (uint32_t)(kHeadDim * 16) : 16u;
   // Slot-scale variant: V scales enter P relative to vref (the split's first
   // slot), and vref multiplies the result back at the end.
   float vref = 1.f, vinv = 1.f;
@@ -370,10 +610,11 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
     const int np = min(PPS, pg_end - fill_first_page);
     const int n_tiles = np * tiles_per_page;
     const uint32_t sbase = ring_u32 + (uint32_t)stage * p.stage_bytes;
+    // slot scales of the stage: K rows of its pages, then V rows
+    const float* srow = reinterpret_cast<const float*>(ring + stage * p.stage_bytes + p.scale_off);
     if constexpr (kSlotScales) {
       if (fill == 0) {
-        const float v0 = *reinterpret_cast<const float*>(ring + stage * p.stage_bytes + p.scale_off +
-                                                         (uint32_t)PPS * (uint32_t)bs * 4u);
+        const float v0 = srow[PPS * bs];
         if (isfinite(v0) && v0 != 0.f) {
           vref = v0;
           vinv = 1.f / v0;
@@ -390,203 +631,384 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
                                          : sbase + (uint32_t)pg * page_bytes + (uint32_t)(sub * 256);
       const uint32_t vbase = kTokenMajor ? sbase + (uint32_t)(PPS + pg) * page_bytes + (uint32_t)sub * 2048u
                                          : sbase + (uint32_t)(PPS + pg) * page_bytes + (uint32_t)sub * v_sub;
-
-      // ---- S^T = K_tile * Q^T (two independent accumulator chains)
-      float sc[4] = {0.f, 0.f, 0.f, 0.f};
-      float sd[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int kk = 0; kk < kChunks / 2; ++kk) {
-        uint32_t r0, r1, r2, r3;
-        if constexpr (kTokenMajor)
-          ldsm_x4(kbase + tm_row + ((((uint32_t)(2 * kk) + tm_hi) ^ tm_xor) << 4), r0, r1, r2, r3);
-        else
-          ldsm_x4(kbase + k_lane_off + (uint32_t)(2 * kk * bs * 16), r0, r1, r2, r3);
-        mma_f16(sc, e4m3x2_lo_to_f16x2(r0), e4m3x2_lo_to_f16x2(r1), e4m3x2_hi_to_f16x2(r0),
-                e4m3x2_hi_to_f16x2(r1), qf[2 * kk][0], qf[2 * kk][1]);
-        mma_f16(sd, e4m3x2_lo_to_f16x2(r2), e4m3x2_lo_to_f16x2(r3), e4m3x2_hi_to_f16x2(r2),
-                e4m3x2_hi_to_f16x2(r3), qf[2 * kk + 1][0], qf[2 * kk + 1][1]);
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) sc[i] += sd[i];
-
-      // ---- online softmax (exp2 domain); tokens >= L are masked
-      const bool vA = tok0 + tokA < L;
-      const bool vB = tok0 + tokB < L;
-      float lscA = lsc, lscB = lsc, vsA = 1.f, vsB = 1.f;
-      if constexpr (kSlotScales) {
-        const uint8_t* ks = ring + stage * p.stage_bytes + p.scale_off + (pg * bs + sub * 16) * 4;
-        const uint8_t* vs = ks + PPS * bs * 4;
-        // Scales of slots past the length may hold anything (even NaN).
-        lscA *= vA ? reinterpret_cast<const float*>(ks)[tokA] : 0.f;
-        lscB *= vB ? reinterpret_cast<const float*>(ks)[tokB] : 0.f;
-        vsA = vA ? reinterpret_cast<const float*>(vs)[tokA] * vinv : 0.f;
-        vsB = vB ? reinterpret_cast<const float*>(vs)[tokB] * vinv : 0.f;
-      }
-      const float s0 = vA ? sc[0] * lscA : -INFINITY;
-      const float s1 = vA ? sc[1] * lscA : -INFINITY;
-      const float s2 = vB ? sc[2] * lscB : -INFINITY;
-      const float s3 = vB ? sc[3] * lscB : -INFINITY;
-      const float mx0 = warp_max_over_gid(fmaxf(s0, s2));
-      const float mx1 = warp_max_over_gid(fmaxf(s1, s3));
-      const float mn0 = fmaxf(m0, mx0);
-      const float mn1 = fmaxf(m1, mx1);
-      const float c0 = fast_exp2(m0 - mn0);
-      const float c1 = fast_exp2(m1 - mn1);
-      m0 = mn0;
-      m1 = mn1;
-      const float p0 = fast_exp2(s0 - mn0);
-      const float p1 = fast_exp2(s1 - mn1);
-      const float p2 = fast_exp2(s2 - mn0);
-      const float p3 = fast_exp2(s3 - mn1);
-      l0 = l0 * c0 + (p0 + p2);
-      l1 = l1 * c1 + (p1 + p3);
-      if (__any_sync(0xffffffffu, (c0 != 1.f) | (c1 != 1.f))) {  // a running max moved
-#pragma unroll
-        for (int mt = 0; mt < kChunks; ++mt) {
-          o[mt][0] *= c0;
-          o[mt][1] *= c1;
-          o[mt][2] *= c0;
-          o[mt][3] *= c1;
-        }
-      }
-      // P^T fragment: transpose (token rows x head cols) to (head rows x token
-      // cols). Lane quads 2 and 3 hold their two token pairs in the other
-      // order (row_token), so they swap the two halves of the B fragment.
-      uint32_t x0, x1;
-      if constexpr (kSlotScales) {
-        x0 = pack_f16x2(p0 * vsA, p1 * vsA);
-        x1 = pack_f16x2(p2 * vsB, p3 * vsB);
-      } else {
-        x0 = pack_f16x2(p0, p1);
-        x1 = pack_f16x2(p2, p3);
-      }
-      const uint32_t t0 = movmatrix_trans(x0);
-      const uint32_t t1 = movmatrix_trans(x1);
-      const uint32_t pb0 = low_quad ? t0 : t1;
-      const uint32_t pb1 = low_quad ? t1 : t0;
-
-      // ---- O^T += V_tile^T * P^T
-      // Page-major V: lane holds V bytes of tokens 4tig..4tig+3 of one dim.
-      // Token-major V (ldmatrix.trans): a register holds tokens (2tig, 2tig+1)
-      // x dims (2gid, 2gid+1) of a chunk; registers 0/2 tokens 0-7, 1/3 8-15.
-      uint32_t vr[kChunks / 2][4];
-#pragma unroll
-      for (int mp = 0; mp < kChunks / 2; ++mp) {
-        if constexpr (kTokenMajor)
-          ldsm_x4_trans(vbase + tm_row + ((((uint32_t)(2 * mp) + tm_hi) ^ tm_xor) << 4), vr[mp][0], vr[mp][1],
-                        vr[mp][2], vr[mp][3]);
-        else
-          ldsm_x4(vbase + v_lane_off + (uint32_t)(32 * mp) * v_row, vr[mp][0], vr[mp][1], vr[mp][2], vr[mp][3]);
-      }
-      const int n_valid = L - tok0;
-      if (n_valid < 16) {
-        // Zero the V bytes of tokens >= L: their e4m3 codes may be NaN and
-        // 0 * NaN would poison the accumulator.
-        if constexpr (kTokenMajor) {
-          const uint32_t m_lo = (2 * tig < n_valid ? 0x0000FFFFu : 0u) | (2 * tig + 1 < n_valid ? 0xFFFF0000u : 0u);
-          const uint32_t m_hi =
-              (8 + 2 * tig < n_valid ? 0x0000FFFFu : 0u) | (9 + 2 * tig < n_valid ? 0xFFFF0000u : 0u);
-#pragma unroll
-          for (int mp = 0; mp < kChunks / 2; ++mp) {
-            vr[mp][0] &= m_lo;
-            vr[mp][1] &= m_hi;
-            vr[mp][2] &= m_lo;
-            vr[mp][3] &= m_hi;
-          }
-        } else {
-          const int k = min(max(n_valid - 4 * tig, 0), 4);
-          const uint32_t vmask = k >= 4 ? 0xFFFFFFFFu : ((1u << (8 * k)) - 1u);
-#pragma unroll
-          for (int mp = 0; mp < kChunks / 2; ++mp)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) vr[mp][i] &= vmask;
-        }
-      }
-#pragma unroll
-      for (int mp = 0; mp < kChunks / 2; ++mp) {
-        if constexpr (kTokenMajor) {
-          // bytes (t,d0) (t,d1) (t',d0) (t',d1) -> (t,d0) (t',d0) | (t,d1) (t',d1)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t ya = __byte_perm(vr[mp][2 * h], 0, 0x3120);
-            const uint32_t yb = __byte_perm(vr[mp][2 * h + 1], 0, 0x3120);
-            mma_f16(o[2 * mp + h], e4m3x2_lo_to_f16x2(ya), e4m3x2_hi_to_f16x2(ya), e4m3x2_lo_to_f16x2(yb),
-                    e4m3x2_hi_to_f16x2(yb), pb0, pb1);
-          }
-        } else {
-          mma_f16(o[2 * mp], e4m3x2_lo_to_f16x2(vr[mp][0]), e4m3x2_lo_to_f16x2(vr[mp][1]),
-                  e4m3x2_hi_to_f16x2(vr[mp][0]), e4m3x2_hi_to_f16x2(vr[mp][1]), pb0, pb1);
-          mma_f16(o[2 * mp + 1], e4m3x2_lo_to_f16x2(vr[mp][2]), e4m3x2_lo_to_f16x2(vr[mp][3]),
-                  e4m3x2_hi_to_f16x2(vr[mp][2]), e4m3x2_hi_to_f16x2(vr[mp][3]), pb0, pb1);
-        }
-      }
+      w.tile(kbase, vbase, bs, L - tok0, lsc, srow + pg * bs + sub * 16, srow + (PPS + pg) * bs + sub * 16, vinv);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8u * stage);
   }
 
   // ------------------------------------------------ merge the consumer warps
-  l0 = warp_sum_over_gid(l0);
-  l1 = warp_sum_over_gid(l1);
   // All consumer warps are past their last ring read once they pass this
   // barrier; the abort decision is the same for all of them.
   if (named_barrier_or(1, kConsumerThreads, *abort_flag)) return;
 
   float* mo = reinterpret_cast<float*>(smem);                       // [w][head][kMergeStride]
   float* mml = mo + kConsumerWarps * kMaxGqa * kMergeStride;        // [w][head][2]
-  {
-    float* mw = mo + warp * kMaxGqa * kMergeStride;
-#pragma unroll
-    for (int mt = 0; mt < kChunks; ++mt) {
-      // accumulator rows gid / gid + 8 of m-tile mt hold these two dims
-      const int d0 = kTokenMajor ? 16 * mt + 2 * gid : 16 * mt + gid;
-      const int d1 = kTokenMajor ? d0 + 1 : d0 + 8;
-      mw[(2 * tig) * kMergeStride + d0] = o[mt][0];
-      mw[(2 * tig + 1) * kMergeStride + d0] = o[mt][1];
-      mw[(2 * tig) * kMergeStride + d1] = o[mt][2];
-      mw[(2 * tig + 1) * kMergeStride + d1] = o[mt][3];
-    }
-    if (gid == 0) {
-      float* ml = mml + warp * kMaxGqa * 2;
-      ml[(2 * tig) * 2 + 0] = m0;
-      ml[(2 * tig) * 2 + 1] = l0;
-      ml[(2 * tig + 1) * 2 + 0] = m1;
-      ml[(2 * tig + 1) * 2 + 1] = l1;
-    }
-  }
+  w.store_merge(mo, mml, warp);
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+  reduce_store<kSlotScales>(p, mo, mml, threadIdx.x, s, kvh, split, vref);
+}
 
-  for (int i = threadIdx.x; i < g * kHeadDim; i += kConsumerThreads) {
-    const int hh = i / kHeadDim;
-    const int d = i % kHeadDim;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mml[(w * kMaxGqa + hh) * 2]);
-    float acc = 0.f, den = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float mw = mml[(w * kMaxGqa + hh) * 2];
-        const float f = fast_exp2(mw - M);
-        acc += f * mo[(w * kMaxGqa + hh) * kMergeStride + d];
-        den += f * mml[(w * kMaxGqa + hh) * 2 + 1];
-      }
-    }
-    const int h = kvh * g + hh;
-    if (p.nsplit == 1) {
-      const float zs = p.sinks ? __ldg(p.sinks + h) * 1.4426950408889634f : -INFINITY;
-      const float r = finish(acc, den, M, zs, kSlotScales ? vref : p.v_scale);
-      store_out(p.out, ((size_t)s * H + h) * kHeadDim + d, r, p.out_fp8, p.out_scale);
-    } else {
-      // Slot-scale partials carry their own V reference (the merge then uses 1).
-      const size_t prow = ((size_t)s * H + h) * p.nsplit + split;
-      p.part_o[prow * kHeadDim + d] = kSlotScales ? acc * vref : acc;
-      if (d == 0) {
-        p.part_ml[prow * 2 + 0] = M;
-        p.part_ml[prow * 2 + 1] = den;
-      }
-    }
+// --------------------------------------------------------------------------
+// Persistent variant (per-tensor scales, page-major K and V, either V page
+// order): the grid is the resident CTA slots, and each CTA works through a
+// queue of work units. Its producer warp takes the next unit from an atomic
+// ticket counter as soon as the previous unit's pages are issued, so the
+// ring keeps streaming across unit boundaries instead of filling and
+// draining once per unit, and free CTAs pick up work dynamically. Each stage
+// carries a header naming its unit; the unit's first stage also carries the
+// unit's query rows (copied with its pages). The consumer warps finish a
+// unit on its last stage: they merge their (m, l, O) in that stage's memory
+// and only then release it to the producer.
+//
+// Unit u is (s, kvh, split) = (u / (Hk nsplit), (u / nsplit) % Hk, u % nsplit),
+// the order of the per-unit grid. CTA b starts with unit b; its later
+// tickets are gridDim.x + the counter's previous value, taken when the
+// producer reaches the last stage of its current unit (so a CTA claims work
+// only shortly before it can start it), and ticket gridDim.x + i is unit
+// unit_order[i] when an order is given: longest units first, so that the
+// last units to start are the short ones. That order comes from a kernel
+// launched just before this one as its programmatic dependency; only the
+// second ticket waits for it. queue[0] is the counter and queue[1] counts
+// finished CTAs: the last CTA to finish zeroes both, so every launch finds
+// them at zero (the workspace starts zeroed).
+struct StageHeader {
+  int s, kvh, split, L;
+  int first_page;  // page index (in the sequence) of the stage's first page
+  int np;          // pages in the stage (0: a zero-length sequence)
+  int flags;       // kHdrFirst / kHdrLast / kHdrEnd
+  int pad;
+};
+constexpr int kHdrFirst = 1;
+constexpr int kHdrLast = 2;
+constexpr int kHdrEnd = 4;
+constexpr uint32_t kStageQBytes = kMaxGqa * kHeadDim * 2;
+constexpr uint32_t kStageHeaderBytes = sizeof(StageHeader);
+
+// Bounded barrier of the consumer warps on an mbarrier (count kConsumerWarps):
+// false (with the status bit and the abort flag raised) after the wait
+// limit, or when the CTA is aborting.
+__device__ __forceinline__ bool consumer_sync(uint32_t bar, uint32_t& phase, int lane, volatile int* abort_flag) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+  const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar, phase & 1u, abort_flag, kWaitLimitNs));
+  ++phase;
+  if (!ok && lane == 0) {
+    atomicOr(&g_status, kStatusMergeWaitTimeout);
+    *abort_flag = 1;
   }
+  return ok;
+}
+
+template <int kMinCtasPerSm>
+__global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
+    pda_persistent_decode_kernel(const DecodeParams p, unsigned* queue, int num_units) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bs = p.block_size;
+  const int g = p.gqa;
+  const int NS = p.num_stages;
+  const int PPS = p.pages_per_stage;
+
+  uint8_t* ring = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + (size_t)NS * p.stage_bytes);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * NS + 1);
+  const uint32_t ring_u32 = smem_u32(ring);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8u * NS;
+  const uint32_t cons_bar = full0 + 16u * NS;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(full0 + 8u * i, 1);
+      mbar_init(empty0 + 8u * i, kConsumerWarps);
+    }
+    mbar_init(cons_bar, kConsumerWarps);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  const uint32_t page_bytes = (uint32_t)(kHeadDim * bs);
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    const size_t head_stride = (size_t)page_bytes;
+    const size_t block_stride = (size_t)p.num_kv_heads * page_bytes;
+    const int per_seq = p.num_kv_heads * p.nsplit;
+    int fill = 0;
+    bool ok = true;
+    unsigned t = blockIdx.x;  // ticket
+    unsigned unit = t;
+    bool order_ready = false;
+    while (ok && t < (unsigned)num_units) {
+      const int s = (int)(unit / (unsigned)per_seq);
+      const int kvh = (int)((unit / (unsigned)p.nsplit) % (unsigned)p.num_kv_heads);
+      const int split = (int)(unit % (unsigned)p.nsplit);
+      int L = __ldg(p.seq_lens + s);
+      L = max(0, min(L, p.max_blocks * bs));
+      const int pages = (L + bs - 1) / bs;
+      int pg_first, pg_end;
+      split_range(pages, p.nsplit, split, pg_first, pg_end);
+      bool skip = false;
+      if (pg_first >= pg_end) {
+        // An empty split writes nothing (the merge kernel skips it); a
+        // zero-length sequence gets one header-only stage so that the
+        // consumers store its zero output.
+        if (p.nsplit > 1) skip = true;
+        pg_first = pg_end = 0;
+      }
+      unsigned t_next = 0;
+      bool fetched = false;
+      const int n_pages = pg_end - pg_first;
+      const int n_st = skip ? 0 : (n_pages > 0 ? (n_pages + PPS - 1) / PPS : 1);
+      const int32_t* row = p.block_tables + (size_t)s * p.max_blocks + pg_first;
+      int my_block = 0;
+      for (int k = 0; k < n_st; ++k, ++fill) {
+        const int j = k * PPS;  // page offset in the unit; stages never straddle a 32-page chunk
+        if ((j & 31) == 0) my_block = (j + lane < n_pages) ? __ldg(row + j + lane) : 0;
+        int blk[kMaxPagesPerStage];
+#pragma unroll
+        for (int u = 0; u < kMaxPagesPerStage; ++u) blk[u] = __shfl_sync(0xffffffffu, my_block, (j + u) & 31);
+        const int np = max(0, min(PPS, n_pages - j));
+        if (k == n_st - 1) {
+          // next ticket: its latency overlaps the wait for this stage's slot
+          if (lane == 0) t_next = gridDim.x + atomicAdd(queue, 1u);
+          fetched = true;
+        }
+        const int stage = fill % NS;
+        const uint32_t round = (uint32_t)(fill / NS);
+        const bool got = mbar_wait_bounded(empty0 + 8u * stage, (round & 1u) ^ 1u, abort_flag, kWaitLimitNs);
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) {
+            atomicOr(&g_status, kStatusEmptyWaitTimeout);
+            *abort_flag = 1;
+          }
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t sbase = ring_u32 + (uint32_t)stage * p.stage_bytes;
+          const uint32_t bar = full0 + 8u * stage;
+          StageHeader* hd = reinterpret_cast<StageHeader*>(ring + (size_t)stage * p.stage_bytes + p.hdr_off);
+          hd->s = s;
+          hd->kvh = kvh;
+          hd->split = split;
+          hd->L = L;
+          hd->first_page = pg_first + j;
+          hd->np = np;
+          hd->flags = (k == 0 ? kHdrFirst : 0) | (k == n_st - 1 ? kHdrLast : 0);
+          const bool with_q = (k == 0) && (np > 0);
+          const uint32_t q_bytes = with_q ? (uint32_t)g * kHeadDim * 2u : 0u;
+          const uint32_t bytes = 2u * page_bytes * (uint32_t)np + q_bytes;
+          if (bytes == 0) {
+            mbar_arrive(bar);  // release-orders the header for the consumers
+          } else {
+            mbar_arrive_expect_tx(bar, bytes);
+            if (with_q)
+              bulk_g2s(sbase + p.q_off, p.q + ((size_t)s * p.num_heads + (size_t)kvh * g) * kHeadDim, q_bytes, bar);
+#pragma unroll
+            for (int u = 0; u < kMaxPagesPerStage; ++u) {
+              if (u < np) {
+                const size_t off = (size_t)blk[u] * block_stride + (size_t)kvh * head_stride;
+                bulk_g2s(sbase + (uint32_t)u * page_bytes, p.k_cache + off, page_bytes, bar);
+                bulk_g2s(sbase + (uint32_t)(PPS + u) * page_bytes, p.v_cache + off, page_bytes, bar);
+              }
+            }
+          }
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (!fetched && lane == 0) t_next = gridDim.x + atomicAdd(queue, 1u);
+      t = __shfl_sync(0xffffffffu, t_next, 0);
+      unit = t;
+      if (p.unit_order != nullptr && t < (unsigned)num_units) {
+        if (!order_ready) {
+          grid_dependency_wait();  // the order kernel has finished and its writes are visible
+          order_ready = true;
+        }
+        unsigned u = 0;
+        if (lane == 0) u = (unsigned)__ldcg(p.unit_order + (t - gridDim.x));
+        unit = __shfl_sync(0xffffffffu, u, 0);
+      }
+    }
+    if (ok) {
+      // End marker: a header-only stage that stops the consumers.
+      const int stage = fill % NS;
+      const uint32_t round = (uint32_t)(fill / NS);
+      const bool got = mbar_wait_bounded(empty0 + 8u * stage, (round & 1u) ^ 1u, abort_flag, kWaitLimitNs);
+      if (__all_sync(0xffffffffu, got)) {
+        if (lane == 0) {
+          StageHeader* hd = reinterpret_cast<StageHeader*>(ring + (size_t)stage * p.stage_bytes + p.hdr_off);
+          hd->flags = kHdrEnd;
+          mbar_arrive(full0 + 8u * stage);
+        }
+        ++fill;
+      } else if (lane == 0) {
+        atomicOr(&g_status, kStatusEmptyWaitTimeout);
+        *abort_flag = 1;
+      }
+      __syncwarp();
+    }
+    // Drain: never leave the CTA with copies still landing in its smem.
+    for (int f = max(0, fill - NS); f < fill; ++f) {
+      if (!mbar_wait_bounded(full0 + 8u * (f % NS), (uint32_t)(f / NS) & 1u, nullptr, kWaitLimitNs)) {
+        if (lane == 0) atomicOr(&g_status, kStatusDrainTimeout);
+        break;
+      }
+    }
+    // Queue bookkeeping: this CTA takes no more tickets.
+    if (lane == 0) {
+      __threadfence();
+      if (atomicAdd(queue + 1, 1u) == gridDim.x - 1) {
+        atomicExch(queue, 0u);
+        atomicExch(queue + 1, 0u);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  TileWorker<false, false> w;
+  w.setup(lane, bs, p.v_shuffled);
+  w.reset();
+  const float lsc = p.logit_scale_log2;
+  const int tiles_per_page = bs / 16;
+  const uint32_t v_sub = p.v_shuffled ? (uint32_t)(kHeadDim * 16) : 16u;
+  uint32_t cons_phase = 0;
+
+  for (int fill = 0;; ++fill) {
+    const int stage = fill % NS;
+    const uint32_t round = (uint32_t)(fill / NS);
+    const bool got = mbar_wait_bounded(full0 + 8u * stage, round & 1u, abort_flag, kWaitLimitNs);
+    if (!__all_sync(0xffffffffu, got)) {
+      if (lane == 0) {
+        atomicOr(&g_status, kStatusFullWaitTimeout);
+        *abort_flag = 1;
+      }
+      break;
+    }
+    const StageHeader hd = *reinterpret_cast<const StageHeader*>(ring + (size_t)stage * p.stage_bytes + p.hdr_off);
+    if (hd.flags & kHdrEnd) break;
+    const uint32_t sbase = ring_u32 + (uint32_t)stage * p.stage_bytes;
+    if (hd.flags & kHdrFirst) {
+      w.reset();
+      if (hd.np > 0) {
+        const bool live = w.gid < g;
+        w.load_q_shared(sbase + p.q_off + (uint32_t)(live ? w.gid : 0) * (uint32_t)(kHeadDim * 2), live);
+      }
+    }
+    const int n_tiles = hd.np * tiles_per_page;
+    for (int tile = warp; tile < n_tiles; tile += kConsumerWarps) {
+      const int pg = tile / tiles_per_page;
+      const int sub = tile % tiles_per_page;
+      const int tok0 = (hd.first_page + pg) * bs + sub * 16;
+      if (tok0 >= hd.L) continue;
+      const uint32_t kbase = sbase + (uint32_t)pg * page_bytes + (uint32_t)(sub * 256);
+      const uint32_t vbase = sbase + (uint32_t)(PPS + pg) * page_bytes + (uint32_t)sub * v_sub;
+      w.tile(kbase, vbase, bs, hd.L - tok0, lsc, nullptr, nullptr, 1.f);
+    }
+    if (hd.flags & kHdrLast) {
+      // Every consumer warp is done with this stage's pages: its memory
+      // becomes the merge area until the stage is released below.
+      if (!consumer_sync(cons_bar, cons_phase, lane, abort_flag)) break;
+      float* mo = reinterpret_cast<float*>(ring + (size_t)stage * p.stage_bytes);
+      float* mml = mo + kConsumerWarps * kMaxGqa * kMergeStride;
+      w.store_merge(mo, mml, warp);
+      if (!consumer_sync(cons_bar, cons_phase, lane, abort_flag)) break;
+      reduce_store<false>(p, mo, mml, threadIdx.x, hd.s, hd.kvh, hd.split, 1.f);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8u * stage);
+  }
+  // A consumer that leaves on a failed wait raises the abort flag; the
+  // others then fail their next bounded wait and leave too.
+}
+
+// Longest-first order of the work units the persistent kernel hands out
+// after each CTA's first one (units first .. num_units-1): a counting sort of
+// the units by the number of pages of their split, in buckets of equal page
+// count (of equal page-count ranges when a split can hold more than
+// kOrderBuckets - 1 pages). Units in one bucket keep no particular order;
+// the order only decides which CTA computes a unit and when, never the
+// unit's result. One CTA; it lets the persistent kernel launch at once.
+constexpr int kOrderThreads = 1024;
+constexpr int kOrderBuckets = 4096;
+
+struct OrderParams {
+  const int32_t* seq_lens;
+  int* order;           // [num_units - first]
+  int first;            // units below this are taken by block index
+  int num_units;
+  int num_kv_heads;
+  int nsplit;
+  int block_size;
+  int max_blocks;
+  int max_split_pages;  // ceil(max_blocks / nsplit): largest page count of a split
+};
+
+__device__ __forceinline__ int order_key(const OrderParams& p, int u) {
+  const int s = u / (p.num_kv_heads * p.nsplit);
+  const int split = u % p.nsplit;
+  int L = __ldg(p.seq_lens + s);
+  L = max(0, min(L, p.max_blocks * p.block_size));
+  int first, end;
+  split_range((L + p.block_size - 1) / p.block_size, p.nsplit, split, first, end);
+  const int n = max(0, end - first);
+  const int k = p.max_split_pages < kOrderBuckets
+                    ? n
+                    : (int)((long long)n * (kOrderBuckets - 1) / (long long)p.max_split_pages);
+  return kOrderBuckets - 1 - min(k, kOrderBuckets - 1);  // longest first
+}
+
+__global__ void __launch_bounds__(kOrderThreads) pda_order_units_kernel(const OrderParams p) {
+  grid_dependents_launch();
+  __shared__ unsigned count[kOrderBuckets];
+  __shared__ unsigned warp_sum[kOrderThreads / 32];
+  const int tid = threadIdx.x;
+  for (int i = tid; i < kOrderBuckets; i += kOrderThreads) count[i] = 0u;
+  __syncthreads();
+  for (int u = p.first + tid; u < p.num_units; u += kOrderThreads) atomicAdd(&count[order_key(p, u)], 1u);
+  __syncthreads();
+  // exclusive prefix sum over the buckets: thread t owns buckets 4t .. 4t+3
+  constexpr int kPer = kOrderBuckets / kOrderThreads;
+  unsigned own[kPer];
+  unsigned sum = 0;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    own[j] = count[kPer * tid + j];
+    sum += own[j];
+  }
+  const int lane = tid & 31, warp = tid >> 5;
+  unsigned incl = sum;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const unsigned v = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned w = warp_sum[lane];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const unsigned v = __shfl_up_sync(0xffffffffu, w, d);
+      if (lane >= d) w += v;
+    }
+    warp_sum[lane] = w - warp_sum[lane];  // exclusive over warps
+  }
+  __syncthreads();
+  unsigned base = warp_sum[warp] + incl - sum;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    count[kPer * tid + j] = base;
+    base += own[j];
+  }
+  __syncthreads();
+  for (int u = p.first + tid; u < p.num_units; u += kOrderThreads)
+    p.order[atomicAdd(&count[order_key(p, u)], 1u)] = u;
 }
 
 // Log-sum-exp merge of the per-split partials of one (sequence, head) per

@@ -1,0 +1,186 @@
+"""GPU parity of the persistent decode kernel against the fp64 oracle.
+
+A batch whose grid does not fit one wave of 4 CTAs per SM runs on the
+persistent kernel: one CTA per resident slot, work units taken from an
+atomic queue, pages streamed across unit boundaries, each unit's query rows
+and header carried in its first stage, the consumer warps' merge done in the
+unit's last stage. The batches here have many short, ragged sequences
+(zero lengths, partial pages, one-token contexts), so every CTA runs many
+units back to back and the oracle still finishes in seconds.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_decode_pda_gb300 as pda
+import workloads
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    torch.cuda.set_device(0)
+    from paged_kv_decode_pda_gb300 import build
+    build.build()
+    pda.load()
+    pda.set_split_override(0)
+    yield
+    pda.set_split_override(0)
+    assert pda.query_device_status() == 0
+
+
+def _many(S, bs, seed, max_len=300, H=32, Hk=8):
+    """S ragged sequences in [0, max_len): every 13th empty, some of one token."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(1, max_len, S)
+    lens[::13] = 0
+    lens[5::17] = 1
+    return workloads.make_custom(S, H, Hk, lens.tolist(), block_size=bs, pool_factor=1.2, seed=seed, device=DEV)
+
+
+def _kernel(batch):
+    cfg = batch.cfg
+    return pda.plan_kernel(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq,
+                           cfg.block_size)
+
+
+@pytest.mark.parametrize("bs,splits", [(16, 0), (16, 2), (16, 5), (32, 0), (32, 3), (48, 0), (64, 0), (64, 2),
+                                       (128, 0), (128, 2)])
+def test_persistent_parity(bs, splits):
+    batch = _many(160, bs, seed=100 + bs + splits)
+    pda.set_split_override(splits)
+    try:
+        assert _kernel(batch) == pda.PDA_KERNEL_PERSISTENT
+        out = U.run_cuda(batch)
+        torch.cuda.synchronize()
+    finally:
+        pda.set_split_override(0)
+    stats = U.compare(out, U.run_oracle(batch), "persistent bs=%d splits=%d" % (bs, splits))
+    lens = batch.seq_lens_host
+    assert all(torch.all(out[s] == 0) for s in range(len(lens)) if lens[s] == 0), "empty sequences give zeros"
+    print(bs, splits, stats)
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_persistent_bitwise_equals_per_unit_kernel(splits):
+    # pda_decode_noalloc always runs the per-unit kernel; with the same split
+    # count the per-unit arithmetic (stages, tiles, warp merge) is identical.
+    batch = _many(200, 16, seed=7, max_len=700)
+    cfg = batch.cfg
+    pda.set_split_override(splits)
+    try:
+        assert _kernel(batch) == pda.PDA_KERNEL_PERSISTENT
+        a = U.run_cuda(batch)
+        b = torch.empty_like(batch.q)
+        pda.decode_noalloc(batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.seq_lens, cfg.scale,
+                           cfg.k_scale, cfg.v_scale, out=b)
+        torch.cuda.synchronize()
+    finally:
+        pda.set_split_override(0)
+    assert torch.equal(a, b)
+
+
+def test_launch_counts():
+    # units beyond the resident slots are handed out longest first (one more
+    # launch, up to 16384 units); a split adds the merge launch
+    batch = _many(160, 16, seed=3)
+    cfg = batch.cfg
+    args = (cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq, cfg.block_size)
+    assert pda.plan_launches(*args) == 2
+    pda.set_split_override(3)
+    try:
+        assert pda.plan_launches(*args) == 3
+    finally:
+        pda.set_split_override(0)
+    assert pda.plan_launches(2200, 32, 8, 8, 16) == 1   # 17600 units: ticket order
+    assert pda.plan_launches(0, 32, 8, 8, 16) == 0
+
+
+def test_ticket_order_beyond_the_ordered_limit():
+    # 2200 sequences x 8 kv heads = 17600 units: no order kernel, tickets in unit order
+    batch = _many(2200, 16, seed=19, max_len=90)
+    cfg = batch.cfg
+    assert _kernel(batch) == pda.PDA_KERNEL_PERSISTENT
+    assert pda.plan_launches(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq,
+                             cfg.block_size) == 1
+    out = U.run_cuda(batch)
+    b = torch.empty_like(batch.q)
+    pda.decode_noalloc(batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.seq_lens, cfg.scale,
+                       cfg.k_scale, cfg.v_scale, out=b)
+    torch.cuda.synchronize()
+    assert torch.equal(out, b)
+    U.compare(out, U.run_oracle(batch), "persistent, 17600 units")
+
+
+def test_queue_resets_between_calls_and_graph_replays():
+    # The work queue lives in the stream's workspace and each launch leaves
+    # it at zero: calls of different sizes back to back, then graph replays.
+    s = torch.cuda.Stream()
+    batches = [_many(S, 16, seed=S) for S in (120, 300, 97)]
+    for b in batches:
+        assert _kernel(b) == pda.PDA_KERNEL_PERSISTENT
+    first = []
+    with torch.cuda.stream(s):
+        for b in batches:
+            first.append(U.run_cuda(b, stream=s).clone())
+        again = [U.run_cuda(b, stream=s).clone() for b in reversed(batches)][::-1]
+    s.synchronize()
+    for x, y in zip(first, again):
+        assert torch.equal(x, y)
+    b = batches[1]
+    cfg = b.cfg
+    pda.reserve(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq, cfg.block_size,
+                stream=s)
+    out = torch.zeros_like(b.q)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        U.run_cuda(b, out=out, stream=s)
+    for _ in range(5):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, first[1])
+    U.compare(first[1], U.run_oracle(b), "persistent, 300 sequences")
+
+
+def test_persistent_sinks_fp8_and_shuffled_v():
+    batch = _many(150, 32, seed=61, H=40)
+    cfg = batch.cfg
+    assert _kernel(batch) == pda.PDA_KERNEL_PERSISTENT
+    g = torch.Generator().manual_seed(9)
+    sinks = (torch.randn(cfg.num_heads, generator=g) * 2).float()
+    NB, Hk, D, bs = batch.v_cache.shape
+    v_sh = batch.v_cache.reshape(NB, Hk, D, bs // 16, 16).permute(0, 1, 3, 2, 4).contiguous()
+    a = pda.decode_ex(batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.seq_lens, cfg.scale,
+                      cfg.k_scale, cfg.v_scale, sinks=sinks.to(DEV))
+    b = pda.decode_ex(batch.q, batch.k_cache, v_sh, batch.block_tables, batch.seq_lens, cfg.scale, cfg.k_scale,
+                      cfg.v_scale, sinks=sinks.to(DEV), v_shuffled=True)
+    out_scale = 0.0075
+    c = pda.decode_ex(batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.seq_lens, cfg.scale,
+                      cfg.k_scale, cfg.v_scale, sinks=sinks.to(DEV), output_scale=out_scale)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b), "the two V layouts hold the same values"
+    exact = oracle.decode(**batch.raw(), scale=cfg.scale, k_scale=cfg.k_scale, v_scale=cfg.v_scale,
+                          sinks=sinks.numpy())
+    U.compare(a, exact, "persistent with sinks")
+    # e4m3 output: each stored code's value lies within half an e4m3 step of
+    # the exact result (clipped to the e4m3 range) plus the 8e-3 bar, and
+    # most codes equal the code of the exact result.
+    got = c.view(torch.uint8).cpu().numpy()
+    vg = torch.from_numpy(got).view(torch.float8_e4m3fn).double().numpy() * out_scale
+    target = np.clip(exact, -448.0 * out_scale, 448.0 * out_scale)
+    q = np.abs(target) / out_scale
+    expo = np.floor(np.log2(np.maximum(q, 2.0 ** -6)))
+    half_step = np.ldexp(1.0, (expo - 4).astype(np.int64)) * out_scale
+    assert np.all(np.abs(vg - target) <= half_step + U.MAX_ABS)
+    want = oracle.quantize_e4m3(exact, out_scale)
+    assert float(np.mean(got == want)) >= 0.9
