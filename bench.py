@@ -103,6 +103,14 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# One call in this many inside the timed region carries kernel events.
+EVENT_STRIDE = 10
+
+# Kernel function behind each decode instance name the library reports.
+KERNEL_FUNCTION = {"per-unit (3 CTAs/SM)": "pda_split_decode_kernel", "per-unit dense (4 CTAs/SM)":
+                   "pda_split_decode_kernel", "persistent": "pda_persistent_decode_kernel"}
+
+
 def kernel_source_sha() -> str:
     """Hash of the device sources the decode kernel is compiled from (host code excluded)."""
     h = hashlib.sha256()
@@ -284,17 +292,20 @@ def run_ours(args, ws, rank, local):
     stream.synchronize()
     assert pda.query_device_status(stream) == 0
 
-    # Graphs: one of `chunk` calls (each bracketed by its own kernel events), one for the remainder.
+    # Graphs: one of `chunk` calls, every EVENT_STRIDE-th of them bracketed by
+    # kernel events (an event node costs microseconds, too much to put around
+    # every call of a small batch), and one graph for the remainder.
     K = args.steps
     chunk = min(K, 100)
-    ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(chunk)]
+    n_ev = (chunk + EVENT_STRIDE - 1) // EVENT_STRIDE
+    ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
 
     def capture(n, with_events):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for i in range(n):
-                if with_events:
-                    pda.set_profile_events(*ev_pairs[i])
+                if with_events and i % EVENT_STRIDE == 0:
+                    pda.set_profile_events(*ev_pairs[i // EVENT_STRIDE])
                 call(i)
                 pda.set_profile_events(None, None)
         return g
@@ -334,13 +345,14 @@ def run_ours(args, ws, rank, local):
                 g_rem.replay()
         else:
             # host enqueue (~10 us) stays far below the kernel time, so the
-            # stream never drains; the last `chunk` calls carry kernel events
+            # stream never drains; every EVENT_STRIDE-th of the last `chunk`
+            # calls carries kernel events
             for i in range(K):
                 j = i - (K - chunk)
-                if j >= 0:
-                    pda.set_profile_events(*ev_pairs[j])
+                if j >= 0 and j % EVENT_STRIDE == 0:
+                    pda.set_profile_events(*ev_pairs[j // EVENT_STRIDE])
                 call(i)
-            pda.set_profile_events(None, None)
+                pda.set_profile_events(None, None)
         t_end.record(stream)
     stream.synchronize()
     torch.cuda.synchronize()
@@ -434,7 +446,12 @@ def run_ours(args, ws, rank, local):
                    "parallelism": "replicas x%d" % ws},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
-                     "kernel": "pda_split_decode_kernel", "kernel_us_mean": kern_mean_ms * 1e3,
+                     "kernel": KERNEL_FUNCTION[kernel_kind] if args.variant in ("plain", "ex", "shuffled_v")
+                     else "pda_split_decode_kernel",
+                     "timed_span": "profile events around the decode kernel (with the unit-order kernel that "
+                                   "precedes the persistent kernel) of every %dth call in the timed region"
+                                   % EVENT_STRIDE,
+                     "kernel_us_mean": kern_mean_ms * 1e3,
                      "kernel_launches_timed": len(kern_ms), "algorithmic_bytes_per_launch": bytes_per_call},
         "cpu_baseline": cpu,
         "e2e": e2e,
