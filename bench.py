@@ -272,7 +272,7 @@ def run_ours(args, ws, rank, local):
                                                  for _ in range(replicas - 1)]
     nsplit = pda.plan_splits(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq,
                              cfg.block_size)
-    if args.variant in ("plain", "ex", "shuffled_v"):
+    if args.variant != "slot_scales":   # token-major caches plan like page-major ones
         kernels_per_call = pda.plan_launches(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads,
                                              cfg.max_num_blocks_per_seq, cfg.block_size)
     else:   # per-unit kernel (+ merge)
@@ -437,7 +437,7 @@ def run_ours(args, ws, rank, local):
         "data": "synthetic (seeded N(0,1) q; K/V N(0,1) quantised to e4m3 with scale 0.05; shuffled block tables)",
         "config": {"workload": cfg.name, "variant": args.variant, "num_seqs": cfg.num_seqs, "num_heads": cfg.num_heads,
                    "num_kv_heads": cfg.num_kv_heads, "head_size": cfg.head_size, "block_size": cfg.block_size,
-                   "ctx": cfg.ctx if cfg.ctx else list(cfg.ctx_range), "kv_splits": nsplit, "decode_kernel": kernel_kind if args.variant in ("plain", "ex", "shuffled_v") else None,
+                   "ctx": cfg.ctx if cfg.ctx else list(cfg.ctx_range), "kv_splits": nsplit, "decode_kernel": kernel_kind if args.variant != "slot_scales" else None,
                    "bytes_per_call": bytes_per_call,
                    "l2": "KV pool %.2f GB x %d replica(s) >= 3x L2 (%d MB); no flush needed" % (
                        kv_bytes / 1e9, replicas, l2 >> 20),
@@ -446,7 +446,7 @@ def run_ours(args, ws, rank, local):
                    "parallelism": "replicas x%d" % ws},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
-                     "kernel": KERNEL_FUNCTION[kernel_kind] if args.variant in ("plain", "ex", "shuffled_v")
+                     "kernel": KERNEL_FUNCTION[kernel_kind] if args.variant != "slot_scales"
                      else "pda_split_decode_kernel",
                      "timed_span": "profile events around the decode kernel (with the unit-order kernel that "
                                    "precedes the persistent kernel) of every %dth call in the timed region"

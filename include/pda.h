@@ -330,8 +330,9 @@ typedef enum {
 } pda_kernel;
 
 /*
- * pda_plan_kernel -- the decode kernel instance pda_decode (and pda_decode_ex)
- * would launch on the current device for these sizes: the dense per-unit
+ * pda_plan_kernel -- the decode kernel instance pda_decode (and pda_decode_ex,
+ * and pda_decode_strided with token-major pages) would launch on the current
+ * device for these sizes: the dense per-unit
  * instance when the planned grid fits one wave of 4 CTAs per SM, else the
  * persistent kernel. A call captured into a CUDA graph without a prior
  * pda_reserve (so with no workspace for the persistent kernel's queue) runs

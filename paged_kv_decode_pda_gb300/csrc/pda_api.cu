@@ -24,7 +24,17 @@ std::atomic<cudaEvent_t> g_prof_before{nullptr};
 std::atomic<cudaEvent_t> g_prof_after{nullptr};
 
 // Decode kernel instances the library launches.
-enum KernelKind { kPlainWide = 0, kPlainDense, kSlotWide, kTokenWide, kTokenDense, kPersistWide, kNumKinds };
+enum KernelKind {
+  kPlainWide = 0,
+  kPlainDense,
+  kSlotWide,
+  kTokenWide,
+  kTokenDense,
+  kPersistWide,   // persistent, page-major pages
+  kPersistToken,  // persistent, token-major pages through tensor maps
+  kNumKinds
+};
+bool is_persistent(int k) { return k == kPersistWide || k == kPersistToken; }
 
 struct DeviceInfo {
   int sm_count = 0;
@@ -48,8 +58,6 @@ struct RingShape {
   int num_stages;
   uint32_t stage_bytes;
   uint32_t scale_off;
-  uint32_t q_off = 0;    // persistent kernel: the unit's query rows
-  uint32_t hdr_off = 0;  // persistent kernel: the stage header
   size_t smem_bytes;
 };
 
@@ -68,18 +76,19 @@ RingShape ring_shape(int bs, bool slot_scales = false, int ring_bytes = pda::kRi
   return r;
 }
 
-// Persistent-kernel stage: K and V pages, then the unit's query rows, then
-// the header; at least the CTA merge area (a unit's last stage holds its
-// merge). Barriers: full and empty per stage plus one consumer barrier.
+// Persistent-kernel ring: stages of K and V pages, each a multiple of 1 KiB
+// (swizzled tensor-map pages need 1 KiB alignment) and at least the merge
+// rows; then one side entry per stage (query rows, merge (m, l), header);
+// then full and empty barriers per stage plus one consumer barrier.
 RingShape persistent_ring_shape(int bs) {
   RingShape r = ring_shape(bs);
   const uint32_t kv = r.scale_off;
-  r.q_off = kv;
-  uint32_t h = kv + pda::kStageQBytes;
-  if (h < pda::kMergeBytes) h = pda::kMergeBytes;
-  r.hdr_off = (h + 15u) & ~15u;
-  r.stage_bytes = r.hdr_off + pda::kStageHeaderBytes;
-  r.smem_bytes = (size_t)r.num_stages * r.stage_bytes + 8 * (2 * (size_t)r.num_stages + 1) + 16 + 1024;
+  uint32_t st = kv > pda::kPersistMergeBytes ? kv : pda::kPersistMergeBytes;
+  st = (st + 1023u) & ~1023u;
+  r.stage_bytes = st;
+  r.num_stages = (int)((uint32_t)pda::kRingBytes / st);
+  if (r.num_stages < 2) r.num_stages = 2;
+  r.smem_bytes = (size_t)r.num_stages * (st + pda::kAuxBytes) + 8 * (2 * (size_t)r.num_stages + 1) + 16 + 1024;
   return r;
 }
 
@@ -191,7 +200,7 @@ bool is_dense(KernelKind k) { return k == kPlainDense || k == kTokenDense; }
 bool is_slot(KernelKind k) { return k == kSlotWide; }
 
 RingShape ring_for(KernelKind k, int bs) {
-  if (k == kPersistWide) return persistent_ring_shape(bs);
+  if (is_persistent(k)) return persistent_ring_shape(bs);
   return ring_shape(bs, is_slot(k), is_dense(k) ? pda::kDenseRingBytes : pda::kRingBytes);
 }
 
@@ -201,7 +210,8 @@ const void* kernel_fn(KernelKind k) {
     case kPlainDense: return (const void*)pda::pda_split_decode_kernel<false, false, pda::kDenseCtasPerSm>;
     case kSlotWide: return (const void*)pda::pda_split_decode_kernel<true, false, pda::kWideCtasPerSm>;
     case kTokenWide: return (const void*)pda::pda_split_decode_kernel<false, true, pda::kWideCtasPerSm>;
-    case kPersistWide: return (const void*)pda::pda_persistent_decode_kernel<pda::kWideCtasPerSm>;
+    case kPersistWide: return (const void*)pda::pda_persistent_decode_kernel<false, pda::kWideCtasPerSm>;
+    case kPersistToken: return (const void*)pda::pda_persistent_decode_kernel<true, pda::kWideCtasPerSm>;
     default: return (const void*)pda::pda_split_decode_kernel<false, true, pda::kDenseCtasPerSm>;
   }
 }
@@ -252,11 +262,14 @@ int resolve_splits(int num_seqs, int num_kv_heads, int max_blocks, int bs, int s
   return n;
 }
 
-// The wide instance of plain calls: the persistent kernel unless built out.
+// The wide instances of plain and token-major calls: the persistent kernel
+// unless built out.
 #ifdef PDA_DISABLE_PERSISTENT
 constexpr KernelKind kWidePlain = kPlainWide;
+constexpr KernelKind kWideToken = kTokenWide;
 #else
 constexpr KernelKind kWidePlain = kPersistWide;
+constexpr KernelKind kWideToken = kPersistToken;
 #endif
 
 // Split count and kernel instance for a call: the wide instance (3 CTAs per
@@ -294,7 +307,7 @@ pda_status plan_call(int dev, int num_seqs, int num_kv_heads, int max_blocks, in
       out->nsplit = resolve_splits(num_seqs, num_kv_heads, MB, bs, sms, occ_d);
     }
   }
-  if (out->kind == kPersistWide) {
+  if (is_persistent(out->kind)) {
     const long long units = (long long)num_seqs * num_kv_heads * out->nsplit;
     const long long slots = (long long)sms * occ;
     out->grid = (unsigned)(units < slots ? units : slots);
@@ -334,7 +347,7 @@ struct WsLayout {
 WsLayout ws_layout(int num_seqs, int num_heads, const Plan& pl) {
   WsLayout w;
   const size_t part = partial_bytes(num_seqs, num_heads, pl.nsplit);
-  if (pl.kind != kPersistWide && part == 0) return w;
+  if (!is_persistent(pl.kind) && part == 0) return w;
   w.order_off = kQueueBytes;
   w.part_off = w.order_off + (((size_t)pl.ordered * sizeof(int) + 255) & ~(size_t)255);
   w.bytes = w.part_off + part;
@@ -387,7 +400,7 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PDA_ERR_CUDA;
-  const KernelKind wide = slot ? kSlotWide : (tm ? kTokenWide : kWidePlain);
+  const KernelKind wide = slot ? kSlotWide : (tm ? kWideToken : kWidePlain);
   const KernelKind dense = slot ? kSlotWide : (tm ? kTokenDense : kPlainDense);
   Plan pl;
   st = plan_call(dev, num_seqs, num_kv_heads, max_num_blocks_per_seq, block_size, wide, dense, &pl);
@@ -396,9 +409,9 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
   void* ws = nullptr;
   WsLayout wl = ws_layout(num_seqs, num_heads, pl);
   st = get_workspace(dev, stream, wl.bytes, &ws);
-  if (st == PDA_ERR_WORKSPACE && pl.kind == kPersistWide && nsplit == 1) {
+  if (st == PDA_ERR_WORKSPACE && is_persistent(pl.kind) && nsplit == 1) {
     // Captured without pda_reserve: the per-unit kernel needs no workspace.
-    pl.kind = kPlainWide;
+    pl.kind = pl.kind == kPersistToken ? kTokenWide : kPlainWide;
     wl = WsLayout();
     st = PDA_OK;
   }
@@ -425,8 +438,6 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
   p.num_stages = rs.num_stages;
   p.stage_bytes = rs.stage_bytes;
   p.scale_off = rs.scale_off;
-  p.q_off = rs.q_off;
-  p.hdr_off = rs.hdr_off;
   p.k_scales = slot ? k_scales : nullptr;
   p.v_scales = slot ? v_scales : nullptr;
   p.logit_scale_log2 = (float)((double)scale * (slot ? 1.0 : (double)k_scale) * 1.4426950408889634);
@@ -447,7 +458,8 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
   const CUtensorMap& mk = tm ? tm->k : g_no_map;
   const CUtensorMap& mv = tm ? tm->v : g_no_map;
   switch (pl.kind) {
-    case kPersistWide: {
+    case kPersistWide:
+    case kPersistToken: {
       const int units = num_seqs * num_kv_heads * nsplit;
       if (pl.ordered > 0) {
         // The order kernel, then the decode kernel as its programmatic
@@ -476,12 +488,19 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         lc.attrs = attr;
         lc.numAttrs = 1;
-        if (cudaLaunchKernelEx(&lc, pda::pda_persistent_decode_kernel<pda::kWideCtasPerSm>, p, queue, units) !=
-            cudaSuccess)
-          return PDA_ERR_CUDA;
+        const cudaError_t e =
+            pl.kind == kPersistToken
+                ? cudaLaunchKernelEx(&lc, pda::pda_persistent_decode_kernel<true, pda::kWideCtasPerSm>, p, queue,
+                                     units, mk, mv)
+                : cudaLaunchKernelEx(&lc, pda::pda_persistent_decode_kernel<false, pda::kWideCtasPerSm>, p, queue,
+                                     units, mk, mv);
+        if (e != cudaSuccess) return PDA_ERR_CUDA;
+      } else if (pl.kind == kPersistToken) {
+        pda::pda_persistent_decode_kernel<true, pda::kWideCtasPerSm>
+            <<<pl.grid, pda::kThreads, rs.smem_bytes, stream>>>(p, queue, units, mk, mv);
       } else {
-        pda::pda_persistent_decode_kernel<pda::kWideCtasPerSm><<<pl.grid, pda::kThreads, rs.smem_bytes, stream>>>(
-            p, queue, units);
+        pda::pda_persistent_decode_kernel<false, pda::kWideCtasPerSm>
+            <<<pl.grid, pda::kThreads, rs.smem_bytes, stream>>>(p, queue, units, mk, mv);
       }
       break;
     }
@@ -637,7 +656,7 @@ pda_status pda_reserve(int num_seqs, int num_heads, int num_kv_heads, int max_nu
   if (cudaGetDevice(&dev) != cudaSuccess) return PDA_ERR_CUDA;
   // Size for the largest plan any entry point makes for these sizes.
   size_t bytes = 0;
-  const KernelKind pairs[3][2] = {{kWidePlain, kPlainDense}, {kSlotWide, kSlotWide}, {kTokenWide, kTokenDense}};
+  const KernelKind pairs[3][2] = {{kWidePlain, kPlainDense}, {kSlotWide, kSlotWide}, {kWideToken, kTokenDense}};
   for (const auto& pr : pairs) {
     Plan pl;
     pda_status st = plan_call(dev, num_seqs, num_kv_heads, max_num_blocks_per_seq, block_size, pr[0], pr[1], &pl);

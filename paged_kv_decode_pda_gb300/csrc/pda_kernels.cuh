@@ -85,10 +85,6 @@ struct DecodeParams {
   const float* sinks = nullptr; // [H] per-head sink logits (scale * q.k units), or none
   int out_fp8 = 0;              // 1: out holds E4M3(o / out_scale) bytes
   float out_scale = 1.f;
-  // Persistent kernel: stage offsets of the unit's query rows and of the
-  // stage header.
-  uint32_t q_off = 0;
-  uint32_t hdr_off = 0;
   // Persistent kernel: unit of ticket gridDim.x + i is unit_order[i]
   // (longest first, written by pda_order_units_kernel), or ticket order.
   const int* unit_order = nullptr;
@@ -347,21 +343,22 @@ struct TileWorker {
     }
   }
 
-  // This warp's (m, l, O) into the CTA merge area: mo [w][head][kMergeStride],
+  // This warp's (m, l, O) into the CTA merge area: mo [w][head][kStride],
   // mml [w][head][2].
+  template <int kStride>
   __device__ __forceinline__ void store_merge(float* mo, float* mml, int warp) {
     l0 = warp_sum_over_gid(l0);
     l1 = warp_sum_over_gid(l1);
-    float* mw = mo + warp * kMaxGqa * kMergeStride;
+    float* mw = mo + warp * kMaxGqa * kStride;
 #pragma unroll
     for (int mt = 0; mt < kChunks; ++mt) {
       // accumulator rows gid / gid + 8 of m-tile mt hold these two dims
       const int d0 = kTokenMajor ? 16 * mt + 2 * gid : 16 * mt + gid;
       const int d1 = kTokenMajor ? d0 + 1 : d0 + 8;
-      mw[(2 * tig) * kMergeStride + d0] = o[mt][0];
-      mw[(2 * tig + 1) * kMergeStride + d0] = o[mt][1];
-      mw[(2 * tig) * kMergeStride + d1] = o[mt][2];
-      mw[(2 * tig + 1) * kMergeStride + d1] = o[mt][3];
+      mw[(2 * tig) * kStride + d0] = o[mt][0];
+      mw[(2 * tig + 1) * kStride + d0] = o[mt][1];
+      mw[(2 * tig) * kStride + d1] = o[mt][2];
+      mw[(2 * tig + 1) * kStride + d1] = o[mt][3];
     }
     if (gid == 0) {
       float* ml = mml + warp * kMaxGqa * 2;
@@ -373,14 +370,12 @@ struct TileWorker {
   }
 };
 
-// Bytes of the CTA merge area (per-warp O rows and (m, l) pairs).
-constexpr uint32_t kMergeBytes = (uint32_t)(kConsumerWarps * kMaxGqa * (kMergeStride + 2) * sizeof(float));
-
 // Combine the consumer warps' (m, l, O) of unit (s, kvh, split) from the
 // merge area and store the bf16 / e4m3 output (one split) or the fp32
 // partial (several splits). Consumer thread `tid` of kConsumerThreads.
-// vref: the slot-scale variant's reference V scale (1 otherwise).
-template <bool kSlotScales>
+// vref: the slot-scale variant's reference V scale (1 otherwise). kStride:
+// the fp32 row stride of mo.
+template <bool kSlotScales, int kStride>
 __device__ __forceinline__ void reduce_store(const DecodeParams& p, const float* mo, const float* mml, int tid, int s,
                                              int kvh, int split, float vref) {
   const int g = p.gqa;
@@ -397,7 +392,7 @@ __device__ __forceinline__ void reduce_store(const DecodeParams& p, const float*
       for (int w = 0; w < kConsumerWarps; ++w) {
         const float mw = mml[(w * kMaxGqa + hh) * 2];
         const float f = fast_exp2(mw - M);
-        acc += f * mo[(w * kMaxGqa + hh) * kMergeStride + d];
+        acc += f * mo[(w * kMaxGqa + hh) * kStride + d];
         den += f * mml[(w * kMaxGqa + hh) * 2 + 1];
       }
     }
@@ -644,22 +639,28 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
 
   float* mo = reinterpret_cast<float*>(smem);                       // [w][head][kMergeStride]
   float* mml = mo + kConsumerWarps * kMaxGqa * kMergeStride;        // [w][head][2]
-  w.store_merge(mo, mml, warp);
+  w.template store_merge<kMergeStride>(mo, mml, warp);
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
-  reduce_store<kSlotScales>(p, mo, mml, threadIdx.x, s, kvh, split, vref);
+  reduce_store<kSlotScales, kMergeStride>(p, mo, mml, threadIdx.x, s, kvh, split, vref);
 }
 
 // --------------------------------------------------------------------------
-// Persistent variant (per-tensor scales, page-major K and V, either V page
-// order): the grid is the resident CTA slots, and each CTA works through a
+// Persistent variant (per-tensor scales; page-major K and V in either V page
+// order, or token-major pages through tensor maps): the grid is the resident
+// CTA slots, and each CTA works through a
 // queue of work units. Its producer warp takes the next unit from an atomic
 // ticket counter as soon as the previous unit's pages are issued, so the
 // ring keeps streaming across unit boundaries instead of filling and
 // draining once per unit, and free CTAs pick up work dynamically. Each stage
-// carries a header naming its unit; the unit's first stage also carries the
-// unit's query rows (copied with its pages). The consumer warps finish a
-// unit on its last stage: they merge their (m, l, O) in that stage's memory
-// and only then release it to the producer.
+// has a small side entry with a header naming its unit; for the unit's first
+// stage it also holds the unit's query rows (copied with its pages). The
+// consumer warps finish a unit on its last stage: they merge their O rows in
+// that stage's page memory (and their (m, l) in its side entry) and only
+// then release it to the producer.
+//
+// Shared memory: NS stages of stage_bytes (K pages, then V pages; a multiple
+// of 1 KiB and at least the merge rows, so swizzled tensor-map pages stay
+// aligned), then NS side entries of kAuxBytes, then the barriers.
 //
 // Unit u is (s, kvh, split) = (u / (Hk nsplit), (u / nsplit) % Hk, u % nsplit),
 // the order of the per-unit grid. CTA b starts with unit b; its later
@@ -682,8 +683,13 @@ struct StageHeader {
 constexpr int kHdrFirst = 1;
 constexpr int kHdrLast = 2;
 constexpr int kHdrEnd = 4;
-constexpr uint32_t kStageQBytes = kMaxGqa * kHeadDim * 2;
-constexpr uint32_t kStageHeaderBytes = sizeof(StageHeader);
+constexpr uint32_t kAuxQ = 0;                                     // query rows, g x 256 B
+constexpr uint32_t kAuxMl = kMaxGqa * kHeadDim * 2;              // merge (m, l) [w][head][2]
+constexpr uint32_t kAuxHdr = kAuxMl + kConsumerWarps * kMaxGqa * 2 * 4;  // StageHeader
+constexpr uint32_t kAuxBytes = kAuxHdr + sizeof(StageHeader);
+constexpr int kPersistMergeStride = kHeadDim;                     // O rows fill 16 KiB exactly
+constexpr uint32_t kPersistMergeBytes = kConsumerWarps * kMaxGqa * kPersistMergeStride * 4;
+static_assert(kAuxBytes % 16 == 0, "side entries keep 16-byte alignment");
 
 // Bounded barrier of the consumer warps on an mbarrier (count kConsumerWarps):
 // false (with the status bit and the abort flag raised) after the wait
@@ -700,9 +706,10 @@ __device__ __forceinline__ bool consumer_sync(uint32_t bar, uint32_t& phase, int
   return ok;
 }
 
-template <int kMinCtasPerSm>
+template <bool kTokenMajor, int kMinCtasPerSm>
 __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
-    pda_persistent_decode_kernel(const DecodeParams p, unsigned* queue, int num_units) {
+    pda_persistent_decode_kernel(const DecodeParams p, unsigned* queue, int num_units,
+                                 const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -712,9 +719,11 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
   const int PPS = p.pages_per_stage;
 
   uint8_t* ring = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + (size_t)NS * p.stage_bytes);
+  uint8_t* aux = ring + (size_t)NS * p.stage_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(aux + (size_t)NS * kAuxBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * NS + 1);
   const uint32_t ring_u32 = smem_u32(ring);
+  const uint32_t aux_u32 = smem_u32(aux);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8u * NS;
   const uint32_t cons_bar = full0 + 16u * NS;
@@ -791,7 +800,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
         if (lane == 0) {
           const uint32_t sbase = ring_u32 + (uint32_t)stage * p.stage_bytes;
           const uint32_t bar = full0 + 8u * stage;
-          StageHeader* hd = reinterpret_cast<StageHeader*>(ring + (size_t)stage * p.stage_bytes + p.hdr_off);
+          StageHeader* hd = reinterpret_cast<StageHeader*>(aux + (size_t)stage * kAuxBytes + kAuxHdr);
           hd->s = s;
           hd->kvh = kvh;
           hd->split = split;
@@ -807,13 +816,24 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
           } else {
             mbar_arrive_expect_tx(bar, bytes);
             if (with_q)
-              bulk_g2s(sbase + p.q_off, p.q + ((size_t)s * p.num_heads + (size_t)kvh * g) * kHeadDim, q_bytes, bar);
+              bulk_g2s(aux_u32 + (uint32_t)stage * kAuxBytes + kAuxQ,
+                       p.q + ((size_t)s * p.num_heads + (size_t)kvh * g) * kHeadDim, q_bytes, bar);
 #pragma unroll
             for (int u = 0; u < kMaxPagesPerStage; ++u) {
               if (u < np) {
-                const size_t off = (size_t)blk[u] * block_stride + (size_t)kvh * head_stride;
-                bulk_g2s(sbase + (uint32_t)u * page_bytes, p.k_cache + off, page_bytes, bar);
-                bulk_g2s(sbase + (uint32_t)(PPS + u) * page_bytes, p.v_cache + off, page_bytes, bar);
+                if constexpr (kTokenMajor) {
+                  // coordinates: 0 for the row bytes and the token dim, kvh
+                  // and the block id in the head and block dims
+                  const int c1 = p.tm_dim_head == 1 ? kvh : (p.tm_dim_block == 1 ? blk[u] : 0);
+                  const int c2 = p.tm_dim_head == 2 ? kvh : (p.tm_dim_block == 2 ? blk[u] : 0);
+                  const int c3 = p.tm_dim_head == 3 ? kvh : (p.tm_dim_block == 3 ? blk[u] : 0);
+                  tma_load_4d(sbase + (uint32_t)u * page_bytes, &tm_k, 0, c1, c2, c3, bar);
+                  tma_load_4d(sbase + (uint32_t)(PPS + u) * page_bytes, &tm_v, 0, c1, c2, c3, bar);
+                } else {
+                  const size_t off = (size_t)blk[u] * block_stride + (size_t)kvh * head_stride;
+                  bulk_g2s(sbase + (uint32_t)u * page_bytes, p.k_cache + off, page_bytes, bar);
+                  bulk_g2s(sbase + (uint32_t)(PPS + u) * page_bytes, p.v_cache + off, page_bytes, bar);
+                }
               }
             }
           }
@@ -841,7 +861,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
       const bool got = mbar_wait_bounded(empty0 + 8u * stage, (round & 1u) ^ 1u, abort_flag, kWaitLimitNs);
       if (__all_sync(0xffffffffu, got)) {
         if (lane == 0) {
-          StageHeader* hd = reinterpret_cast<StageHeader*>(ring + (size_t)stage * p.stage_bytes + p.hdr_off);
+          StageHeader* hd = reinterpret_cast<StageHeader*>(aux + (size_t)stage * kAuxBytes + kAuxHdr);
           hd->flags = kHdrEnd;
           mbar_arrive(full0 + 8u * stage);
         }
@@ -871,7 +891,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
   }
 
   // -------------------------------------------------------------- consumers
-  TileWorker<false, false> w;
+  TileWorker<false, kTokenMajor> w;
   w.setup(lane, bs, p.v_shuffled);
   w.reset();
   const float lsc = p.logit_scale_log2;
@@ -890,14 +910,15 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
       }
       break;
     }
-    const StageHeader hd = *reinterpret_cast<const StageHeader*>(ring + (size_t)stage * p.stage_bytes + p.hdr_off);
+    const StageHeader hd = *reinterpret_cast<const StageHeader*>(aux + (size_t)stage * kAuxBytes + kAuxHdr);
     if (hd.flags & kHdrEnd) break;
     const uint32_t sbase = ring_u32 + (uint32_t)stage * p.stage_bytes;
     if (hd.flags & kHdrFirst) {
       w.reset();
       if (hd.np > 0) {
         const bool live = w.gid < g;
-        w.load_q_shared(sbase + p.q_off + (uint32_t)(live ? w.gid : 0) * (uint32_t)(kHeadDim * 2), live);
+        w.load_q_shared(aux_u32 + (uint32_t)stage * kAuxBytes + kAuxQ + (uint32_t)(live ? w.gid : 0) * (kHeadDim * 2),
+                        live);
       }
     }
     const int n_tiles = hd.np * tiles_per_page;
@@ -906,8 +927,10 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
       const int sub = tile % tiles_per_page;
       const int tok0 = (hd.first_page + pg) * bs + sub * 16;
       if (tok0 >= hd.L) continue;
-      const uint32_t kbase = sbase + (uint32_t)pg * page_bytes + (uint32_t)(sub * 256);
-      const uint32_t vbase = sbase + (uint32_t)(PPS + pg) * page_bytes + (uint32_t)sub * v_sub;
+      const uint32_t kbase = kTokenMajor ? sbase + (uint32_t)pg * page_bytes + (uint32_t)sub * 2048u
+                                         : sbase + (uint32_t)pg * page_bytes + (uint32_t)(sub * 256);
+      const uint32_t vbase = kTokenMajor ? sbase + (uint32_t)(PPS + pg) * page_bytes + (uint32_t)sub * 2048u
+                                         : sbase + (uint32_t)(PPS + pg) * page_bytes + (uint32_t)sub * v_sub;
       w.tile(kbase, vbase, bs, hd.L - tok0, lsc, nullptr, nullptr, 1.f);
     }
     if (hd.flags & kHdrLast) {
@@ -915,10 +938,10 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
       // becomes the merge area until the stage is released below.
       if (!consumer_sync(cons_bar, cons_phase, lane, abort_flag)) break;
       float* mo = reinterpret_cast<float*>(ring + (size_t)stage * p.stage_bytes);
-      float* mml = mo + kConsumerWarps * kMaxGqa * kMergeStride;
-      w.store_merge(mo, mml, warp);
+      float* mml = reinterpret_cast<float*>(aux + (size_t)stage * kAuxBytes + kAuxMl);
+      w.template store_merge<kPersistMergeStride>(mo, mml, warp);
       if (!consumer_sync(cons_bar, cons_phase, lane, abort_flag)) break;
-      reduce_store<false>(p, mo, mml, threadIdx.x, hd.s, hd.kvh, hd.split, 1.f);
+      reduce_store<false, kPersistMergeStride>(p, mo, mml, threadIdx.x, hd.s, hd.kvh, hd.split, 1.f);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8u * stage);

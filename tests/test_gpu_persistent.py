@@ -152,6 +152,25 @@ def test_queue_resets_between_calls_and_graph_replays():
     U.compare(first[1], U.run_oracle(b), "persistent, 300 sequences")
 
 
+def test_two_streams_run_their_queues_side_by_side():
+    # Each stream has its own workspace, so its own work queue: two calls
+    # that can overlap on the GPU must both give the single-stream result.
+    a, b = _many(200, 16, seed=71), _many(260, 16, seed=72)
+    ref_a, ref_b = U.run_cuda(a).clone(), U.run_cuda(b).clone()
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    for _ in range(3):
+        with torch.cuda.stream(s1):
+            oa = U.run_cuda(a, stream=s1)
+        with torch.cuda.stream(s2):
+            ob = U.run_cuda(b, stream=s2)
+        outs.append((oa, ob))
+    torch.cuda.synchronize()
+    for oa, ob in outs:
+        assert torch.equal(oa, ref_a) and torch.equal(ob, ref_b)
+
+
 def test_persistent_sinks_fp8_and_shuffled_v():
     batch = _many(150, 32, seed=61, H=40)
     cfg = batch.cfg

@@ -76,6 +76,32 @@ def test_strided_parity(layout, bs, splits):
     assert (out.float() - ref_gpu.float()).abs().max().item() <= 8e-3
 
 
+@pytest.mark.parametrize("layout", ["nhd", "block_split", "packed"])
+@pytest.mark.parametrize("bs,splits", [(16, 0), (16, 2), (32, 0), (64, 3), (128, 0)])
+def test_strided_persistent_parity(layout, bs, splits):
+    # 160 ragged sequences x 8 kv heads: more units than one wave, so the
+    # persistent kernel runs them, its pages arriving through tensor maps.
+    import numpy as np
+    rng = np.random.default_rng(200 + bs)
+    lens = rng.integers(1, 300, 160)
+    lens[::13] = 0
+    lens[5::17] = 1
+    batch = workloads.make_custom(160, 32, 8, lens.tolist(), block_size=bs, pool_factor=1.2, seed=81 + bs,
+                                  device=DEV)
+    cfg = batch.cfg
+    keep, keep2, kp, vp, ks, vs = layouts(batch)[layout]
+    pda.set_split_override(splits)
+    try:
+        out = pda.decode_strided(batch.q, kp, vp, batch.block_tables, batch.seq_lens, cfg.scale, cfg.k_scale,
+                                 cfg.v_scale, num_kv_heads=cfg.num_kv_heads, block_size=bs,
+                                 num_blocks=batch.num_blocks, k_strides=ks, v_strides=vs)
+        torch.cuda.synchronize()
+    finally:
+        pda.set_split_override(0)
+    U.compare(out, U.run_oracle(batch), "strided persistent %s bs=%d splits=%d" % (layout, bs, splits))
+    assert all(torch.all(out[s] == 0) for s in range(len(lens)) if lens[s] == 0)
+
+
 def test_strided_headline_batch_full_size():
     cfg = workloads.CONFIGS[workloads.HEADLINE]
     batch = workloads.make_batch(cfg, device=DEV)
