@@ -483,7 +483,7 @@ def run_reference(args, ws, rank, local):
 
     def step():
         oracle.decode(**raw, scale=cfg.scale, k_scale=cfg.k_scale, v_scale=cfg.v_scale, seq_ids=ids,
-                      num_threads=threads)
+                      num_threads=cores)
 
     for _ in range(args.warmup):
         step()
