@@ -542,8 +542,19 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
     mp.sinks = sinks;
     mp.out_fp8 = out_fp8;
     mp.out_scale = out_scale;
-    pda::pda_merge_kernel<<<dim3((unsigned)num_heads, (unsigned)num_seqs), kHeadDim, 0, stream>>>(mp);
-    if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
+    // Programmatic dependent of the decode kernel: its launch overlaps the
+    // decode kernel's last CTAs, and it waits for the partials on the device.
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3((unsigned)num_heads, (unsigned)num_seqs);
+    lc.blockDim = dim3(kHeadDim);
+    lc.dynamicSmemBytes = 0;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    if (cudaLaunchKernelEx(&lc, pda::pda_merge_kernel, mp) != cudaSuccess) return PDA_ERR_CUDA;
   }
   return PDA_OK;
 }

@@ -434,6 +434,9 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
     pda_split_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v) {
   extern __shared__ __align__(128) uint8_t smem[];
+  // A merge kernel launched as this grid's programmatic dependent may start
+  // its launch now; it waits for this grid's results before reading them.
+  grid_dependents_launch();
   const int split = blockIdx.x;
   const int kvh = blockIdx.y;
   const int s = blockIdx.z;
@@ -711,6 +714,9 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
     pda_persistent_decode_kernel(const DecodeParams p, unsigned* queue, int num_units,
                                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   extern __shared__ __align__(128) uint8_t smem[];
+  // A merge kernel launched as this grid's programmatic dependent may start
+  // its launch now; it waits for this grid's results before reading them.
+  grid_dependents_launch();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int bs = p.block_size;
@@ -1068,14 +1074,17 @@ __global__ void __launch_bounds__(kHeadDim) pda_merge_kernel(const MergeParams p
     active = (pages + per - 1) / per;
   }
   const size_t prow0 = ((size_t)s * p.num_heads + h) * p.nsplit;
+  // Launched as the decode kernel's programmatic dependent: wait until it
+  // has finished and its partials are visible (a no-op otherwise).
+  grid_dependency_wait();
   float M = -INFINITY;
-  for (int i = 0; i < active; ++i) M = fmaxf(M, __ldg(p.part_ml + (prow0 + i) * 2));
+  for (int i = 0; i < active; ++i) M = fmaxf(M, __ldcg(p.part_ml + (prow0 + i) * 2));
   float acc = 0.f, den = 0.f;
   if (M != -INFINITY) {
     for (int i = 0; i < active; ++i) {
-      const float f = fast_exp2(__ldg(p.part_ml + (prow0 + i) * 2) - M);
-      acc += f * __ldg(p.part_o + (prow0 + i) * kHeadDim + d);
-      den += f * __ldg(p.part_ml + (prow0 + i) * 2 + 1);
+      const float f = fast_exp2(__ldcg(p.part_ml + (prow0 + i) * 2) - M);
+      acc += f * __ldcg(p.part_o + (prow0 + i) * kHeadDim + d);
+      den += f * __ldcg(p.part_ml + (prow0 + i) * 2 + 1);
     }
   }
   const float zs = p.sinks ? __ldg(p.sinks + h) * 1.4426950408889634f : -INFINITY;
