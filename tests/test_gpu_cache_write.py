@@ -45,6 +45,50 @@ def test_cache_write_bit_exact(T, Hk, bs, NB, seed, special):
     assert np.array_equal(vd.cpu().numpy(), vc_ref), "V cache bytes differ from the oracle"
 
 
+@pytest.mark.parametrize("scale", [0.05, 0.0731, 1.0 / 3.0, 2.0 ** -7, 2.0e-39])
+@pytest.mark.parametrize("slots_kind", ["blocks", "scattered"])
+def test_cache_write_every_bf16_value_bit_exact(scale, slots_kind):
+    # All 65,536 bf16 bit patterns (NaNs, infinities, subnormals, both zeros)
+    # as K and as V, through both writers: every code must equal the oracle's
+    # e4m3 code of the binary32 quotient. 2e-39 is a (subnormal) scale whose
+    # reciprocal overflows. Blocks of 16 whole slots take the run writer; 4096 scattered
+    # tokens take the scattered writer.
+    T, Hk, bs = 512, 1, 16
+    allv = torch.arange(65536, dtype=torch.int32).to(torch.int16).view(torch.bfloat16).reshape(T, Hk, 128)
+    key = allv
+    val = allv.flip(0)
+    g = torch.Generator().manual_seed(11)
+    NB = 64
+    if slots_kind == "blocks":
+        slots = torch.arange(T, dtype=torch.int64)
+    else:
+        # 4096 tokens, each row holding 16 patterns 8 times over
+        key = key.reshape(T * 8, Hk, 16).repeat_interleave(8, dim=2)
+        val = val.reshape(T * 8, Hk, 16).repeat_interleave(8, dim=2)
+        T, NB = key.shape[0], 300
+        slots = torch.randperm(NB * bs, generator=g)[:T].to(torch.int64)
+    kc = torch.zeros(NB, Hk, 8, bs, 16, dtype=torch.uint8)
+    vc = torch.zeros(NB, Hk, 128, bs, dtype=torch.uint8)
+    kc_ref, vc_ref = kc.numpy().copy(), vc.numpy().copy()
+    oracle.reshape_and_cache(kc_ref, vc_ref, key.contiguous().view(torch.int16).numpy().view(np.uint16),
+                             val.contiguous().view(torch.int16).numpy().view(np.uint16), slots.numpy(),
+                             k_scale=scale, v_scale=scale)
+    kd, vd = kc.to(DEV), vc.to(DEV)
+    pda.reshape_and_cache(key.contiguous().to(DEV), val.contiguous().to(DEV), kd, vd, slots.to(DEV), scale, scale)
+    torch.cuda.synchronize()
+    assert pda.query_device_status() == 0
+
+    # e4m3fn has two NaN codes, 0x7F and 0xFF; a NaN input may map to either
+    # (the oracle keeps the input's sign, the GPU writes 0x7F), so NaN codes
+    # compare equal. Every other code must match exactly.
+    def same_nan(a):
+        return np.where((a & 0x7F) == 0x7F, 0x7F, a)
+    kg, vg = kd.cpu().numpy(), vd.cpu().numpy()
+    assert np.array_equal(same_nan(kg), same_nan(kc_ref)), "K codes differ from the oracle"
+    assert np.array_equal(same_nan(vg), same_nan(vc_ref)), "V codes differ from the oracle"
+    assert np.count_nonzero((kg & 0x7F) == 0x7F) == np.count_nonzero((kc_ref & 0x7F) == 0x7F)
+
+
 def test_cache_write_out_of_pool_slot_is_skipped_and_flagged():
     key, val, slots, kc, vc, ks, vs = _case(4, 2, 16, 2, 7, pad_frac=0.0)
     slots[1] = 2 * 16 + 5       # past the pool
