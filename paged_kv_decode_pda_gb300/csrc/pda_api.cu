@@ -95,10 +95,11 @@ RingShape persistent_ring_shape(int bs) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Cache writes of up to this many (token, kv head) items use the scattered
-// writer (measured on GB300: 4.0 us for 256 tokens x 8 heads against 6.0 us
-// for the run writer; the run writer is 5.8x faster on a 65,536-token
-// prefill).
-constexpr long long kScatterWriteMaxItems = 32768;
+// writer (one warp per item).
+#ifndef PDA_SCATTER_WRITE_MAX_ITEMS
+#define PDA_SCATTER_WRITE_MAX_ITEMS 2048
+#endif
+constexpr long long kScatterWriteMaxItems = PDA_SCATTER_WRITE_MAX_ITEMS;
 
 // Placeholder tensor maps for the page-major kernels (never dereferenced).
 const CUtensorMap g_no_map = {};
@@ -742,15 +743,21 @@ pda_status pda_reshape_and_cache(const void* key, const void* value, void* k_cac
   p.v_scale = v_scale;
   p.v_shuffled = kv_layout == PDA_KV_SHUFFLED_V ? 1 : 0;
   if (num_kv_heads > 65535) return PDA_ERR_UNSUPPORTED;
-  // A decode step writes one token per sequence at scattered slots: use one
-  // warp per (token, kv head). Large writes (a prefill) come in runs of
-  // consecutive slots: use the run writer, which stores 16-byte rows.
+  // Small writes (a decode step's few hundred (token, kv head) items at
+  // scattered slots) take one warp per item; larger ones one CTA per 16
+  // tokens of a kv head, which stores a run of whole blocks as 16-byte V
+  // rows and scattered slots a token at a time. Measured on GB300 (µs per
+  // call, 8 kv heads, random slots / whole blocks): 256 tokens 4.1 / 4.8
+  // one warp per item against 5.6 / 3.6 per 16 tokens; 4096 tokens 28.1 /
+  // 31.4 against 33.8 / 7.4; 65,536 tokens 551 (earlier 16-token writer) /
+  // 83.8 against 424 / 83.2.
   const long long items = (long long)num_tokens * num_kv_heads;
   if (items <= kScatterWriteMaxItems) {
     const long long blocks = (items + pda::kCacheWriteWarpsPerCta - 1) / pda::kCacheWriteWarpsPerCta;
     pda::pda_reshape_and_cache_scatter_kernel<<<(unsigned)blocks, pda::kCacheWriteWarpsPerCta * 32, 0, stream>>>(p);
   } else {
-    const dim3 grid((unsigned)((num_tokens + 15) / 16), (unsigned)num_kv_heads);
+    const dim3 grid((unsigned)((num_tokens + pda::kCacheWriteTokens - 1) / pda::kCacheWriteTokens),
+                    (unsigned)num_kv_heads);
     pda::pda_reshape_and_cache_kernel<<<grid, pda::kCacheWriteThreads, 0, stream>>>(p);
   }
   return cudaGetLastError() == cudaSuccess ? PDA_OK : PDA_ERR_CUDA;

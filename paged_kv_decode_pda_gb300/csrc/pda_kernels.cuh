@@ -1117,12 +1117,15 @@ __global__ void pda_bounded_wait_test_kernel(unsigned long long limit_ns) {
 // The code is decided on the IEEE binary32 quotient x / scale. Negative slots
 // are padding; slots past the pool are skipped and flagged in the status word.
 //
-// One 128-thread CTA per (16 consecutive tokens, kv head); thread (j, c)
-// owns token j and the 16 dims of chunk c. Its 16 K codes are one 16-byte
-// K row, stored directly for any slot. V rows run over tokens, so when the
-// 16 slots form one aligned run of a block (a prefill writing whole groups)
-// the codes are transposed through shared memory and each dim's 16 tokens
-// leave as one 16-byte store; otherwise each thread stores its 16 V bytes.
+// One 128-thread CTA per (16 consecutive tokens, kv head). Thread (j, c)
+// quantises token j's 16 dims of chunk c (two 32-byte loads per tensor, so
+// many bytes are in flight) and stores its 16 K codes as one 16-byte K row.
+// The V codes go through shared memory. V rows run over tokens: when the
+// 16 slots form one aligned run of a block (a prefill writing whole
+// groups), thread d stores dim d of the 16 tokens as one 16-byte row;
+// otherwise (a decode step's slots, scattered over the pool) warp w stores
+// tokens 4w..4w+3 one at a time, its 32 lanes writing 4 bytes each into that
+// token's page, so every store instruction stays within one page.
 struct CacheWriteParams {
   const __nv_bfloat16* key;      // [T][Hk][128]
   const __nv_bfloat16* value;    // [T][Hk][128]
@@ -1138,14 +1141,9 @@ struct CacheWriteParams {
   int v_shuffled = 0;            // 1: V pages are [bs/16][D][16]
 };
 
-constexpr int kCacheWriteThreads = 128;   // 16 tokens x 8 chunks of 16 dims
+constexpr int kCacheWriteTokens = 16;   // one aligned run at most
+constexpr int kCacheWriteThreads = 128;  // 16 tokens x 8 chunks of 16 dims
 constexpr int kCacheWriteWarpsPerCta = 8;  // scattered writer: one warp per (token, kv head)
-
-// Scattered writer for small batches (a decode step: one token per
-// sequence, at slots all over the pool): one warp per (token, kv head), 4
-// dims per lane, so every byte store has its own lane.
-__global__ void __launch_bounds__(kCacheWriteWarpsPerCta * 32)
-    pda_reshape_and_cache_scatter_kernel(const struct CacheWriteParams p);
 
 __device__ __forceinline__ uint4 quantize16(const __nv_bfloat16* src, float scale) {
   const uint4 a = __ldg(reinterpret_cast<const uint4*>(src));
@@ -1163,13 +1161,13 @@ __device__ __forceinline__ uint4 quantize16(const __nv_bfloat16* src, float scal
 }
 
 __global__ void __launch_bounds__(kCacheWriteThreads) pda_reshape_and_cache_kernel(const CacheWriteParams p) {
-  __shared__ __align__(16) uint8_t vt[16][kHeadDim];   // V codes [token][dim] for the transpose
+  __shared__ __align__(16) uint8_t vt[kCacheWriteTokens][kHeadDim];  // V codes [token][dim]
+  __shared__ long long slots[kCacheWriteTokens];                      // -1: nothing to write
   const int tid = threadIdx.x;
   const int j = tid >> 3;
   const int c = tid & 7;
   const int k = blockIdx.y;
-  const int t0 = blockIdx.x * 16;
-  const int t = t0 + j;
+  const int t = blockIdx.x * kCacheWriteTokens + j;
   const int bs = p.block_size;
 
   long long slot = -1;
@@ -1178,26 +1176,23 @@ __global__ void __launch_bounds__(kCacheWriteThreads) pda_reshape_and_cache_kern
   if (slot >= 0 && !in_pool && c == 0) atomicOr(&g_status, kStatusBadSlot);
   const bool valid = slot >= 0 && in_pool;
 
-  uint4 kq = make_uint4(0, 0, 0, 0), vq = make_uint4(0, 0, 0, 0);
   if (valid) {
     const size_t src = ((size_t)t * p.num_kv_heads + k) * kHeadDim + 16 * c;
-    kq = quantize16(p.key + src, p.k_scale);
-    vq = quantize16(p.value + src, p.v_scale);
+    const uint4 kq = quantize16(p.key + src, p.k_scale);
+    const uint4 vq = quantize16(p.value + src, p.v_scale);
+    const long long b = slot / bs;
+    const int o = (int)(slot % bs);
+    const size_t page = ((size_t)b * p.num_kv_heads + k) * (size_t)kHeadDim * bs;
+    *reinterpret_cast<uint4*>(p.k_cache + page + ((size_t)c * bs + o) * 16) = kq;
+    *reinterpret_cast<uint4*>(&vt[j][16 * c]) = vq;
   }
-  const long long b = valid ? slot / bs : 0;
-  const int o = valid ? (int)(slot % bs) : 0;
-  const size_t page = ((size_t)b * p.num_kv_heads + k) * (size_t)kHeadDim * bs;
-  if (valid) *reinterpret_cast<uint4*>(p.k_cache + page + ((size_t)c * bs + o) * 16) = kq;
+  if (c == 0) slots[j] = valid ? slot : -1;
+  __syncthreads();
 
   // One aligned run of 16 slots in one block? (uniform over the CTA)
-  __shared__ long long first_slot;
-  if (tid == 0) first_slot = slot;
-  __syncthreads();
-  const bool run = valid && (first_slot % 16 == 0) && (slot == first_slot + j);
-  const int fast = __syncthreads_and(run ? 1 : 0);
-  if (fast) {
-    *reinterpret_cast<uint4*>(&vt[j][16 * c]) = vq;
-    __syncthreads();
+  const long long first = slots[0];
+  const bool run = valid && (first % kCacheWriteTokens == 0) && (slot == first + j);
+  if (__syncthreads_and(run ? 1 : 0)) {
     // thread d gathers dim d of the 16 tokens: one V row of the run
     const int d = tid;
     uint32_t w[4];
@@ -1205,23 +1200,35 @@ __global__ void __launch_bounds__(kCacheWriteThreads) pda_reshape_and_cache_kern
     for (int i = 0; i < 4; ++i)
       w[i] = (uint32_t)vt[4 * i][d] | ((uint32_t)vt[4 * i + 1][d] << 8) | ((uint32_t)vt[4 * i + 2][d] << 16) |
              ((uint32_t)vt[4 * i + 3][d] << 24);
-    const long long b0 = first_slot / bs;
-    const int o0 = (int)(first_slot % bs);
+    const long long b0 = first / bs;
+    const int o0 = (int)(first % bs);
     const size_t page0 = ((size_t)b0 * p.num_kv_heads + k) * (size_t)kHeadDim * bs;
     const size_t off = p.v_shuffled ? ((size_t)(o0 / 16) * kHeadDim + d) * 16 : (size_t)d * bs + o0;
     *reinterpret_cast<uint4*>(p.v_cache + page0 + off) = make_uint4(w[0], w[1], w[2], w[3]);
-  } else if (valid) {
-    const uint32_t vw[4] = {vq.x, vq.y, vq.z, vq.w};
+  } else {
+    // warp w writes tokens 4w..4w+3 one after the other, lane l dims 4l..4l+3
+    const int warp = tid >> 5;
+    const int d0 = 4 * (tid & 31);
+    const size_t vstride = p.v_shuffled ? 16 : (size_t)bs;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int d = 16 * c + i;
-      const size_t off = p.v_shuffled ? ((size_t)(o / 16) * kHeadDim + d) * 16 + (o % 16) : (size_t)d * bs + o;
-      p.v_cache[page + off] = (uint8_t)(vw[i >> 2] >> (8 * (i & 3)));
+    for (int i = 0; i < kCacheWriteTokens / 4; ++i) {
+      const int jj = 4 * warp + i;
+      const long long sl = slots[jj];
+      if (sl < 0) continue;
+      const long long b = sl / bs;
+      const int o = (int)(sl % bs);
+      const uint32_t v = *reinterpret_cast<const uint32_t*>(&vt[jj][d0]);
+      uint8_t* vrow = p.v_cache + ((size_t)b * p.num_kv_heads + k) * (size_t)kHeadDim * bs +
+                      (p.v_shuffled ? ((size_t)(o / 16) * kHeadDim + d0) * 16 + (o % 16) : (size_t)d0 * bs + o);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) vrow[(size_t)q * vstride] = (uint8_t)(v >> (8 * q));
     }
   }
 }
 
-// Definition of the scattered writer declared above.
+// Scattered writer for small writes (a decode step: one token per sequence,
+// at slots all over the pool): one warp per (token, kv head), 4 dims per
+// lane, no shared memory or block barrier, so a small grid finishes soonest.
 __global__ void __launch_bounds__(kCacheWriteWarpsPerCta * 32)
     pda_reshape_and_cache_scatter_kernel(const CacheWriteParams p) {
   const long long item = (long long)blockIdx.x * kCacheWriteWarpsPerCta + (threadIdx.x >> 5);

@@ -30,7 +30,7 @@ def _case(T, Hk, bs, NB, seed, scale_k=0.05, scale_v=0.07, pad_frac=0.2, special
 @pytest.mark.parametrize("T,Hk,bs,NB,seed,special", [
     (1, 1, 16, 1, 0, False), (7, 8, 16, 4, 1, True), (256, 8, 16, 300, 2, False), (100, 4, 64, 5, 3, False),
     (33, 2, 32, 4, 4, True), (513, 8, 128, 9, 5, False),
-    (5000, 8, 16, 400, 6, True),     # above the scattered writer's limit: run writer with random slots
+    (5000, 8, 16, 400, 6, True),     # many 16-token groups with random slots
 ])
 def test_cache_write_bit_exact(T, Hk, bs, NB, seed, special):
     key, val, slots, kc, vc, ks, vs = _case(T, Hk, bs, NB, seed, special=special)
@@ -46,27 +46,31 @@ def test_cache_write_bit_exact(T, Hk, bs, NB, seed, special):
 
 
 @pytest.mark.parametrize("scale", [0.05, 0.0731, 1.0 / 3.0, 2.0 ** -7, 2.0e-39])
-@pytest.mark.parametrize("slots_kind", ["blocks", "scattered"])
+@pytest.mark.parametrize("slots_kind", ["runs", "scattered", "small"])
 def test_cache_write_every_bf16_value_bit_exact(scale, slots_kind):
     # All 65,536 bf16 bit patterns (NaNs, infinities, subnormals, both zeros)
-    # as K and as V, through both writers: every code must equal the oracle's
-    # e4m3 code of the binary32 quotient. 2e-39 is a (subnormal) scale whose
-    # reciprocal overflows. Blocks of 16 whole slots take the run writer; 4096 scattered
-    # tokens take the scattered writer.
-    T, Hk, bs = 512, 1, 16
-    allv = torch.arange(65536, dtype=torch.int32).to(torch.int16).view(torch.bfloat16).reshape(T, Hk, 128)
-    key = allv
-    val = allv.flip(0)
+    # as K and as V, through every writer path: 4096 tokens in whole blocks
+    # (16-byte V rows), 4096 tokens at scattered slots (a token at a time),
+    # and 512 tokens at scattered slots (one warp per token: a small write).
+    # Every code must equal the oracle's e4m3 code of the binary32 quotient.
+    # 2e-39 is a (subnormal) scale whose reciprocal overflows.
+    Hk, bs = 1, 16
+    allv = torch.arange(65536, dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
     g = torch.Generator().manual_seed(11)
-    NB = 64
-    if slots_kind == "blocks":
-        slots = torch.arange(T, dtype=torch.int64)
+    if slots_kind == "small":
+        T, NB = 512, 64
+        key = allv.reshape(T, Hk, 128)
+        val = key.flip(0)
+        slots = torch.randperm(NB * bs, generator=g)[:T].to(torch.int64)
     else:
         # 4096 tokens, each row holding 16 patterns 8 times over
-        key = key.reshape(T * 8, Hk, 16).repeat_interleave(8, dim=2)
-        val = val.reshape(T * 8, Hk, 16).repeat_interleave(8, dim=2)
-        T, NB = key.shape[0], 300
-        slots = torch.randperm(NB * bs, generator=g)[:T].to(torch.int64)
+        T, NB = 4096, 300
+        key = allv.reshape(T, Hk, 16).repeat_interleave(8, dim=2)
+        val = key.flip(0)
+        if slots_kind == "runs":
+            slots = torch.arange(T, dtype=torch.int64)
+        else:
+            slots = torch.randperm(NB * bs, generator=g)[:T].to(torch.int64)
     kc = torch.zeros(NB, Hk, 8, bs, 16, dtype=torch.uint8)
     vc = torch.zeros(NB, Hk, 128, bs, dtype=torch.uint8)
     kc_ref, vc_ref = kc.numpy().copy(), vc.numpy().copy()
@@ -126,7 +130,7 @@ def test_cache_write_runs_bit_exact(bs, shuffled):
     with a misaligned run and a run broken by padding (per-token path)."""
     g = torch.Generator().manual_seed(100 + bs)
     Hk = 8
-    n_whole = 4800 // bs                      # > 32768 (token, head) items: the run writer
+    n_whole = 4800 // bs                      # 4800 tokens in whole blocks
     NB = n_whole + 6
     blocks = torch.randperm(NB, generator=g)
     slots = []
