@@ -152,6 +152,34 @@ def test_queue_resets_between_calls_and_graph_replays():
     U.compare(first[1], U.run_oracle(b), "persistent, 300 sequences")
 
 
+@pytest.mark.parametrize("splits", [2, 3])
+def test_split_batch_in_a_graph_matches_eager(splits):
+    # Order kernel, persistent kernel and the merge kernel (a programmatic
+    # dependent) captured together and replayed.
+    b = _many(180, 16, seed=90 + splits, max_len=600)
+    cfg = b.cfg
+    pda.set_split_override(splits)
+    try:
+        assert pda.plan_launches(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq,
+                                 cfg.block_size) == 3
+        eager = U.run_cuda(b).clone()
+        s = torch.cuda.Stream()
+        pda.reserve(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq, cfg.block_size,
+                    stream=s)
+        out = torch.zeros_like(b.q)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            U.run_cuda(b, out=out, stream=s)
+        for _ in range(3):
+            out.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(out, eager)
+    finally:
+        pda.set_split_override(0)
+    U.compare(eager, U.run_oracle(b), "persistent, %d splits" % splits)
+
+
 def test_two_streams_run_their_queues_side_by_side():
     # Each stream has its own workspace, so its own work queue: two calls
     # that can overlap on the GPU must both give the single-stream result.
