@@ -121,6 +121,42 @@ def test_ticket_order_beyond_the_ordered_limit():
     U.compare(out, U.run_oracle(batch), "persistent, 17600 units")
 
 
+def test_largest_batch_of_short_sequences():
+    # 65,535 sequences (the largest batch) x 2 kv heads = 131,070 units of
+    # 0-40 tokens: the persistent kernel in ticket order (past the ordered
+    # limit), its queue counting 131,070 tickets. Sampled rows against the
+    # oracle.
+    S = 65535
+    rng = np.random.default_rng(5)
+    lens = rng.integers(0, 41, S)
+    batch = workloads.make_custom(S, 8, 2, lens.tolist(), block_size=16, pool_factor=1.1, seed=6, device=DEV)
+    cfg = batch.cfg
+    assert _kernel(batch) == pda.PDA_KERNEL_PERSISTENT
+    out = U.run_cuda(batch)
+    torch.cuda.synchronize()
+    ids = sorted(set(rng.choice(S, 400, replace=False).tolist()) | {0, S - 1, int(np.argmax(lens))})
+    U.compare(out[ids], U.run_oracle(batch, seq_ids=ids), "65535 sequences")
+    zero = [s for s in range(S) if lens[s] == 0]
+    assert torch.all(out[zero] == 0)
+
+
+@pytest.mark.parametrize("S", [40, 400])
+def test_all_sequences_empty(S):
+    # Every sequence has length 0: the dense per-unit kernel (40 sequences)
+    # and the persistent kernel (400) must both write all-zero rows, with
+    # and without splits.
+    batch = workloads.make_custom(S, 32, 8, [0] * S, block_size=16, seed=S, device=DEV)
+    for splits in (0, 3):
+        pda.set_split_override(splits)
+        try:
+            out = torch.full_like(batch.q, 7.0)
+            U.run_cuda(batch, out=out)
+            torch.cuda.synchronize()
+        finally:
+            pda.set_split_override(0)
+        assert torch.all(out == 0), "splits %d" % splits
+
+
 def test_queue_resets_between_calls_and_graph_replays():
     # The work queue lives in the stream's workspace and each launch leaves
     # it at zero: calls of different sizes back to back, then graph replays.

@@ -162,13 +162,23 @@ def make_batch(cfg: Config, device="cpu", seed: int | None = None) -> Batch:
     v_cache = quantized_normal((NB, Hk, D, bs), cfg.v_scale, gen, device)
     perm = torch.randperm(NB, generator=gen, device=device).to(torch.int32).cpu()
 
-    tables = torch.zeros(S, MB, dtype=torch.int32)
-    off = 0
-    for s, P in enumerate(pages):
-        tables[s, :P] = perm[off:off + P]
-        off += P
+    tables = _fill_tables(S, MB, pages, perm)
     seq_lens = torch.tensor(lens_host, dtype=torch.int32)
     return Batch(cfg, q, k_cache, v_cache, tables.to(device), seq_lens.to(device), lens_host)
+
+
+def _fill_tables(S: int, MB: int, pages, perm: torch.Tensor) -> torch.Tensor:
+    """Block table [S, MB] int32: sequence s takes the next pages[s] entries of
+    perm (a permutation of the pool), in order; the rest of its row is 0."""
+    tables = torch.zeros(S, MB, dtype=torch.int32)
+    counts = torch.tensor(pages, dtype=torch.int64)
+    total = int(counts.sum())
+    if total:
+        rows = torch.repeat_interleave(torch.arange(S), counts)
+        starts = torch.cumsum(counts, 0) - counts
+        cols = torch.arange(total) - torch.repeat_interleave(starts, counts)
+        tables[rows, cols] = perm[:total]
+    return tables
 
 
 def make_custom(num_seqs, num_heads, num_kv_heads, seq_lens, *, block_size=16, head_size=128,
@@ -193,11 +203,7 @@ def make_custom(num_seqs, num_heads, num_kv_heads, seq_lens, *, block_size=16, h
     k_cache = quantized_normal((NB, Hk, D // 16, bs, 16), k_scale, gen, device)
     v_cache = quantized_normal((NB, Hk, D, bs), v_scale, gen, device)
     perm = torch.randperm(NB, generator=gen, device=device).to(torch.int32).cpu()
-    tables = torch.zeros(S, MB, dtype=torch.int32)
-    off = 0
-    for s, P in enumerate(pages):
-        tables[s, :P] = perm[off:off + P]
-        off += P
+    tables = _fill_tables(S, MB, pages, perm)
     seq_lens_t = torch.tensor(lens_host, dtype=torch.int32)
     return Batch(cfg, q, k_cache, v_cache, tables.to(device), seq_lens_t.to(device), lens_host)
 
