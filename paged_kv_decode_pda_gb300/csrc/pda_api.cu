@@ -308,6 +308,11 @@ pda_status plan_call(int dev, int num_seqs, int num_kv_heads, int max_blocks, in
       out->nsplit = resolve_splits(num_seqs, num_kv_heads, MB, bs, sms, occ_d);
     }
   }
+  if (is_persistent(out->kind) && (long long)num_seqs * num_kv_heads * out->nsplit > INT32_MAX) {
+    // The persistent kernel counts units in 32-bit tickets; the per-unit
+    // kernel's grid (splits, kv heads, sequences) has no such bound.
+    out->kind = out->kind == kPersistToken ? kTokenWide : kPlainWide;
+  }
   if (is_persistent(out->kind)) {
     const long long units = (long long)num_seqs * num_kv_heads * out->nsplit;
     const long long slots = (long long)sms * occ;
