@@ -401,6 +401,144 @@ def run_ours(args, ws, rank, local):
                "path": "pinned host -> cudaMemcpyAsync -> pda_decode -> cudaMemcpyAsync -> pinned host"}
         del dev_bufs, host
 
+    # ---- a serving decode step: the KV cache stays resident; each step ships
+    # q, one new K/V token per sequence, its slot, the tables and lengths,
+    # writes the new tokens with pda_reshape_and_cache, decodes, and reads
+    # the output back. Same metric (algorithmic decode bytes per step time).
+    e2e_step_line = None
+    if args.e2e_steps > 0 and args.variant == "plain":
+        S, Hk = cfg.num_seqs, cfg.num_kv_heads
+        g = torch.Generator().manual_seed(cfg.seed + 17)
+        lens_h = torch.tensor(batch.seq_lens_host, dtype=torch.int64)
+        last = torch.clamp(lens_h - 1, min=0)
+        tables_h = batch.block_tables.cpu().to(torch.int64)
+        slots_h = tables_h[torch.arange(S), last // cfg.block_size] * cfg.block_size + last % cfg.block_size
+        slots_h[lens_h == 0] = -1
+        parts = {"q": batch.q.detach().cpu(),
+                 "k_new": (torch.randn(S, Hk, 128, generator=g) * 2).to(torch.bfloat16),
+                 "v_new": (torch.randn(S, Hk, 128, generator=g) * 2).to(torch.bfloat16),
+                 "slots": slots_h,
+                 "t": batch.block_tables.cpu(),
+                 "l": batch.seq_lens.cpu()}
+        # One pinned host buffer and one device buffer hold all of a step's
+        # inputs (256-byte aligned parts), so a step is a single copy in.
+        offs, total = {}, 0
+        for k, v in parts.items():
+            offs[k] = total
+            total += (v.numel() * v.element_size() + 255) // 256 * 256
+        blob_h = torch.empty(total, dtype=torch.uint8).pin_memory()
+        blob_d = torch.empty(total, dtype=torch.uint8, device=dev)
+
+        def view(blob, k):
+            v = parts[k]
+            n = v.numel() * v.element_size()
+            return blob[offs[k]:offs[k] + n].view(v.dtype).view(v.shape)
+
+        for k, v in parts.items():
+            view(blob_h, k).copy_(v)
+        dev_bufs = {k: view(blob_d, k) for k in parts}
+        out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        kc, vc = caches[0]
+        h2d = total
+        d2h = out_host.numel() * out_host.element_size()
+
+        def serving_step():
+            blob_d.copy_(blob_h, non_blocking=True)
+            pda.reshape_and_cache(dev_bufs["k_new"], dev_bufs["v_new"], kc, vc, dev_bufs["slots"], cfg.k_scale,
+                                  cfg.v_scale, stream=stream)
+            pda.decode(dev_bufs["q"], kc, vc, dev_bufs["t"], dev_bufs["l"], cfg.scale, cfg.k_scale, cfg.v_scale,
+                       out=out, stream=stream)
+            out_host.copy_(out, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                serving_step()
+        stream.synchronize()
+        # A server replays its step as a CUDA graph (copies included).
+        per_graph = 10
+        step_mode = "graph"
+        try:
+            g_step = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_step, stream=stream):
+                for _ in range(per_graph):
+                    serving_step()
+            with torch.cuda.stream(stream):
+                g_step.replay()
+            stream.synchronize()
+        except Exception:
+            step_mode = "eager"
+            torch.cuda.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+        n_steps = per_graph * max(2, args.e2e_steps)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(n_steps // per_graph):
+                if step_mode == "graph":
+                    g_step.replay()
+                else:
+                    for _ in range(per_graph):
+                        serving_step()
+            e1.record(stream)
+        stream.synchronize()
+        assert pda.query_device_status(stream) == 0
+        serial_ms = e0.elapsed_time(e1) / n_steps
+
+        # Pipelined, as a server runs it: step i's inputs cross on a copy-in
+        # stream while step i-1 decodes, and step i-1's output comes back on
+        # a copy-out stream while step i decodes. Two device input buffers
+        # and two outputs; events order every reuse.
+        blob_d2 = [blob_d, torch.empty_like(blob_d)]
+        dev_bufs2 = [dev_bufs, {k: view(blob_d2[1], k) for k in parts}]
+        outs = [out, torch.empty_like(out)]
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_done = [torch.cuda.Event() for _ in range(2)]
+        ev_read = [torch.cuda.Event() for _ in range(2)]
+
+        def pipelined(n):
+            for i in range(n):
+                b = i % 2
+                if i >= 2:
+                    s_in.wait_event(ev_done[b])      # step i-2 has finished reading buffer b
+                with torch.cuda.stream(s_in):
+                    blob_d2[b].copy_(blob_h, non_blocking=True)
+                    ev_in[b].record(s_in)
+                stream.wait_event(ev_in[b])
+                if i >= 2:
+                    stream.wait_event(ev_read[b])    # step i-2's output has been read back
+                db = dev_bufs2[b]
+                pda.reshape_and_cache(db["k_new"], db["v_new"], kc, vc, db["slots"], cfg.k_scale, cfg.v_scale,
+                                      stream=stream)
+                pda.decode(db["q"], kc, vc, db["t"], db["l"], cfg.scale, cfg.k_scale, cfg.v_scale, out=outs[b],
+                           stream=stream)
+                ev_done[b].record(stream)
+                s_out.wait_event(ev_done[b])
+                with torch.cuda.stream(s_out):
+                    out_host.copy_(outs[b], non_blocking=True)
+                    ev_read[b].record(s_out)
+
+        pipelined(4)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        s_in.wait_event(e0)
+        pipelined(n_steps)
+        stream.wait_stream(s_out)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        assert pda.query_device_status(stream) == 0
+        v_step, ms_step = aggregate_throughput(bytes_per_call, n_steps, e0.elapsed_time(e1), ws, dev)
+        e2e_step_line = {"value": v_step, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                         "ms_per_step": ms_step / n_steps, "steps": n_steps, "launch": "pipelined",
+                         "serial_ms_per_step": serial_ms, "serial_launch": step_mode,
+                         "path": "pinned host -> one cudaMemcpyAsync (q, new K/V tokens, slots, tables, lengths) -> "
+                                 "pda_reshape_and_cache -> pda_decode -> cudaMemcpyAsync -> pinned host; "
+                                 "KV cache resident in HBM; pipelined: copies of neighbouring steps overlap the "
+                                 "decode on two copy streams"}
+        del dev_bufs, dev_bufs2, blob_h, blob_d, blob_d2
+
     if rank != 0:
         if ws > 1:
             torch.distributed.destroy_process_group()
@@ -455,6 +593,7 @@ def run_ours(args, ws, rank, local):
                      "kernel_launches_timed": len(kern_ms), "algorithmic_bytes_per_launch": bytes_per_call},
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "e2e_serving_step": e2e_step_line,
         "clocks": clocks,
         "gpu_launches": K * kernels_per_call,
     }
