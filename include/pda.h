@@ -88,14 +88,20 @@ typedef enum pda_status {
  * the row's capacity; it does not know num_blocks).
  *
  * Ownership: the caller owns every buffer. The library owns an internal
- * per-(device, stream) workspace for split partials; it grows with
- * cudaMallocAsync on `stream` when a call needs more and the stream is not
- * capturing (PDA_ERR_WORKSPACE if it is; size it first with pda_reserve).
+ * per-(device, stream) workspace: the persistent kernel's work-queue words
+ * and unit order, and the split partials. It grows with cudaMallocAsync on
+ * `stream` when a call needs more and the stream is not capturing. If it is
+ * capturing, a call that needs split partials returns PDA_ERR_WORKSPACE
+ * (size the workspace first with pda_reserve), and a one-split call runs the
+ * per-unit kernel, which needs none. Calls on one stream run in stream order
+ * and share its workspace; calls on different streams have their own.
  *
  * Determinism: for fixed inputs and a fixed split count the result is
- * bitwise reproducible. The split count depends on num_seqs * num_kv_heads
- * and max_num_blocks_per_seq, so a sequence's result may change in the last
- * bits with the batch it shares a call with.
+ * bitwise reproducible. Which CTA computes a work unit, and when, changes
+ * from call to call (the persistent kernel hands units out from a queue) but
+ * never changes the unit's result. The split count depends on
+ * num_seqs * num_kv_heads and max_num_blocks_per_seq, so a sequence's result
+ * may change in the last bits with the batch it shares a call with.
  *
  * Returns PDA_OK, PDA_ERR_INVALID_ARG, PDA_ERR_UNSUPPORTED,
  * PDA_ERR_WORKSPACE or PDA_ERR_CUDA (launch failure).
@@ -358,7 +364,8 @@ void pda_set_split_override(int num_splits);
 
 /*
  * pda_reserve -- size the workspace of (current device, stream) for calls up
- * to these sizes, so later calls (for example under stream capture) need no
+ * to these sizes (any entry point's plan: queue words, unit order, split
+ * partials), so later calls (for example under stream capture) need no
  * allocation. Stream-ordered; returns PDA_OK or PDA_ERR_CUDA.
  */
 pda_status pda_reserve(int num_seqs, int num_heads, int num_kv_heads, int max_num_blocks_per_seq,
