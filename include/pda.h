@@ -347,6 +347,23 @@ typedef enum {
 int pda_plan_kernel(int num_seqs, int num_heads, int num_kv_heads, int max_num_blocks_per_seq, int block_size);
 
 /*
+ * pda_choose_kernel -- the planner's choice for a pda_decode call (pure,
+ * host only, no device needed): for a batch of num_seqs * num_kv_heads
+ * units with at most max_num_blocks_per_seq pages of block_size tokens, on a
+ * device with sm_count SMs holding ctas_per_sm per-unit / persistent CTAs
+ * or ctas_per_sm_dense dense per-unit CTAs each. Returns the PDA_KERNEL_*
+ * instance and, when the pointers are non-NULL, stores the split count and
+ * the kernels launched per call. The dense per-unit instance is chosen when
+ * its grid fits one wave, else the persistent kernel (the 3-CTA per-unit
+ * kernel past 2^31 units). The split count follows pda_choose_splits with
+ * the chosen residency; the split override is not applied. Invalid
+ * arguments return -1. pda_plan_kernel / pda_plan_splits / pda_plan_launches
+ * give the same answers for the current device.
+ */
+int pda_choose_kernel(int num_seqs, int num_kv_heads, int max_num_blocks_per_seq, int block_size, int sm_count,
+                      int ctas_per_sm, int ctas_per_sm_dense, int* num_splits, int* launches);
+
+/*
  * pda_plan_launches -- kernels one pda_decode call launches for these sizes
  * on the current device: the decode kernel, plus the unit-order kernel when
  * the persistent kernel has more units than resident CTAs (up to 16384

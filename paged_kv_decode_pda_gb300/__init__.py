@@ -25,6 +25,7 @@ from ._binding import (  # noqa: F401
     PDA_OUT_BF16,
     PDA_OUT_E4M3,
     PdaError,
+    choose_kernel,
     choose_splits,
     decode,
     decode_ex,

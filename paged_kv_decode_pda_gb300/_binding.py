@@ -34,6 +34,7 @@ SIGNATURES = {
     "pda_plan_splits": (_I, [_I, _I, _I, _I, _I]),
     "pda_plan_kernel": (_I, [_I, _I, _I, _I, _I]),
     "pda_plan_launches": (_I, [_I, _I, _I, _I, _I]),
+    "pda_choose_kernel": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "pda_set_split_override": (None, [_I]),
     "pda_reserve": (_I, [_I, _I, _I, _I, _I, _P]),
     "pda_release": (_I, []),
@@ -290,6 +291,17 @@ def plan_kernel(num_seqs, num_heads, num_kv_heads, max_num_blocks_per_seq, block
     if k < 0:
         raise PdaError(PDA_ERR_CUDA, "pda_plan_kernel")
     return k
+
+
+def choose_kernel(num_seqs, num_kv_heads, max_num_blocks_per_seq, block_size, sm_count, ctas_per_sm,
+                  ctas_per_sm_dense) -> tuple[int, int, int]:
+    """The planner's pure choice: (PDA_KERNEL_* instance, split count, launches per call)."""
+    ns, nl = ctypes.c_int(0), ctypes.c_int(0)
+    k = load().pda_choose_kernel(num_seqs, num_kv_heads, max_num_blocks_per_seq, block_size, sm_count, ctas_per_sm,
+                                 ctas_per_sm_dense, ctypes.byref(ns), ctypes.byref(nl))
+    if k < 0:
+        raise PdaError(PDA_ERR_INVALID_ARG, "pda_choose_kernel")
+    return k, ns.value, nl.value
 
 
 def plan_launches(num_seqs, num_heads, num_kv_heads, max_num_blocks_per_seq, block_size) -> int:

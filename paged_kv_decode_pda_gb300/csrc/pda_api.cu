@@ -254,8 +254,9 @@ pda_status device_info(int dev, int bs, int* sm_count, int* ctas_per_sm, KernelK
   return PDA_OK;
 }
 
-int resolve_splits(int num_seqs, int num_kv_heads, int max_blocks, int bs, int sm_count, int ctas_per_sm) {
-  int n = g_split_override.load();
+int resolve_splits(int num_seqs, int num_kv_heads, int max_blocks, int bs, int sm_count, int ctas_per_sm,
+                   int override_splits) {
+  int n = override_splits;
   if (n <= 0) n = pda_choose_splits(num_seqs, num_kv_heads, max_blocks, bs, sm_count, ctas_per_sm);
   const int cap = max_blocks > 0 ? max_blocks : 1;
   if (n > cap) n = cap;
@@ -290,35 +291,51 @@ struct Plan {
 // the units, and it must finish while the CTAs work on their first units.
 constexpr long long kMaxOrderedUnits = 16384;
 
-pda_status plan_call(int dev, int num_seqs, int num_kv_heads, int max_blocks, int bs, KernelKind wide,
-                     KernelKind dense, Plan* out) {
-  int sms = 0, occ = 0;
-  pda_status st = device_info(dev, bs, &sms, &occ, wide);
-  if (st != PDA_OK) return st;
+// The plan from sizes and residency alone (host only): split count with
+// the wide instance's CTAs per SM; the dense instance when that grid fits
+// one wave of it; the per-unit kernel instead of the persistent one past
+// 2^31 units (32-bit tickets); the persistent grid and how many units it
+// hands out in longest-first order.
+Plan plan_from(int num_seqs, int num_kv_heads, int max_blocks, int bs, int sms, int occ, int occ_d, KernelKind wide,
+               KernelKind dense, int override_splits) {
+  Plan pl;
   const int MB = max_blocks > 0 ? max_blocks : 1;
-  out->kind = wide;
-  out->nsplit = resolve_splits(num_seqs, num_kv_heads, MB, bs, sms, occ);
+  pl.kind = wide;
+  pl.nsplit = resolve_splits(num_seqs, num_kv_heads, MB, bs, sms, occ, override_splits);
   if (dense != wide) {
-    int occ_d = 0;
-    st = device_info(dev, bs, &sms, &occ_d, dense);
-    if (st != PDA_OK) return st;
-    const long long ctas = (long long)num_seqs * num_kv_heads * out->nsplit;
+    const long long ctas = (long long)num_seqs * num_kv_heads * pl.nsplit;
     if (occ_d > occ && ctas <= (long long)sms * occ_d) {
-      out->kind = dense;
-      out->nsplit = resolve_splits(num_seqs, num_kv_heads, MB, bs, sms, occ_d);
+      pl.kind = dense;
+      pl.nsplit = resolve_splits(num_seqs, num_kv_heads, MB, bs, sms, occ_d, override_splits);
     }
   }
-  if (is_persistent(out->kind) && (long long)num_seqs * num_kv_heads * out->nsplit > INT32_MAX) {
+  if (is_persistent(pl.kind) && (long long)num_seqs * num_kv_heads * pl.nsplit > INT32_MAX) {
     // The persistent kernel counts units in 32-bit tickets; the per-unit
     // kernel's grid (splits, kv heads, sequences) has no such bound.
-    out->kind = out->kind == kPersistToken ? kTokenWide : kPlainWide;
+    pl.kind = pl.kind == kPersistToken ? kTokenWide : kPlainWide;
   }
-  if (is_persistent(out->kind)) {
-    const long long units = (long long)num_seqs * num_kv_heads * out->nsplit;
+  if (is_persistent(pl.kind)) {
+    const long long units = (long long)num_seqs * num_kv_heads * pl.nsplit;
     const long long slots = (long long)sms * occ;
-    out->grid = (unsigned)(units < slots ? units : slots);
-    out->ordered = (units > slots && units <= kMaxOrderedUnits) ? units - slots : 0;
+    pl.grid = (unsigned)(units < slots ? units : slots);
+    pl.ordered = (units > slots && units <= kMaxOrderedUnits) ? units - slots : 0;
   }
+  return pl;
+}
+
+// Kernels one call launches under plan pl.
+int plan_launches(const Plan& pl) { return 1 + (pl.ordered > 0 ? 1 : 0) + (pl.nsplit > 1 ? 1 : 0); }
+
+pda_status plan_call(int dev, int num_seqs, int num_kv_heads, int max_blocks, int bs, KernelKind wide,
+                     KernelKind dense, Plan* out) {
+  int sms = 0, occ = 0, occ_d = 0;
+  pda_status st = device_info(dev, bs, &sms, &occ, wide);
+  if (st != PDA_OK) return st;
+  if (dense != wide) {
+    st = device_info(dev, bs, &sms, &occ_d, dense);
+    if (st != PDA_OK) return st;
+  }
+  *out = plan_from(num_seqs, num_kv_heads, max_blocks, bs, sms, occ, occ_d, wide, dense, g_split_override.load());
   return PDA_OK;
 }
 
@@ -611,6 +628,22 @@ int pda_choose_splits(int num_seqs, int num_kv_heads, int max_num_blocks_per_seq
   return (int)want;
 }
 
+int pda_choose_kernel(int num_seqs, int num_kv_heads, int max_num_blocks_per_seq, int block_size, int sm_count,
+                      int ctas_per_sm, int ctas_per_sm_dense, int* num_splits, int* launches) {
+  if (num_seqs <= 0 || num_kv_heads <= 0 || max_num_blocks_per_seq <= 0 || block_size <= 0 || sm_count <= 0 ||
+      ctas_per_sm <= 0 || ctas_per_sm_dense <= 0)
+    return -1;
+  const Plan pl = plan_from(num_seqs, num_kv_heads, max_num_blocks_per_seq, block_size, sm_count, ctas_per_sm,
+                            ctas_per_sm_dense, kWidePlain, kPlainDense, 0);
+  if (num_splits) *num_splits = pl.nsplit;
+  if (launches) *launches = plan_launches(pl);
+  switch (pl.kind) {
+    case kPlainDense: return PDA_KERNEL_PER_UNIT_DENSE;
+    case kPersistWide: return PDA_KERNEL_PERSISTENT;
+    default: return PDA_KERNEL_PER_UNIT;
+  }
+}
+
 void pda_set_split_override(int num_splits) { g_split_override.store(num_splits > 0 ? num_splits : 0); }
 
 int pda_plan_splits(int num_seqs, int num_heads, int num_kv_heads, int max_num_blocks_per_seq, int block_size) {
@@ -651,7 +684,7 @@ int pda_plan_launches(int num_seqs, int num_heads, int num_kv_heads, int max_num
   if (plan_call(dev, num_seqs, num_kv_heads, max_num_blocks_per_seq, block_size, kWidePlain, kPlainDense, &pl) !=
       PDA_OK)
     return -1;
-  return 1 + (pl.ordered > 0 ? 1 : 0) + (pl.nsplit > 1 ? 1 : 0);
+  return plan_launches(pl);
 }
 
 void pda_set_profile_events(cudaEvent_t before, cudaEvent_t after) {
@@ -908,7 +941,8 @@ extern "C" pda_status pda_decode_noalloc(void* out, const void* q, const void* k
   st = noalloc_setup(dev, block_size, &d);
   if (st != PDA_OK) return st;
   const int MB = max_num_blocks_per_seq > 0 ? max_num_blocks_per_seq : 1;
-  const int nsplit = resolve_splits(num_seqs, num_kv_heads, MB, block_size, d.sm_count, d.occ[block_size / 16]);
+  const int nsplit =
+      resolve_splits(num_seqs, num_kv_heads, MB, block_size, d.sm_count, d.occ[block_size / 16], g_split_override.load());
   if (partial_bytes(num_seqs, num_heads, nsplit) > kNoAllocScratchBytes) return PDA_ERR_NOALLOC_CAPACITY;
 
   const RingShape rs = ring_shape(block_size);

@@ -85,6 +85,29 @@ def test_choose_splits_bounds_and_monotonicity(lib):
                     assert n == 1, "a full wave of small units needs no split"
 
 
+# GB300: 152 SMs, 3 per-unit / persistent CTAs or 4 dense per-unit CTAs per SM
+@pytest.mark.parametrize("S,Hk,MB,bs,kind,splits,launches", [
+    (16, 8, 64, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 4, 2),   # 16 x 1024: one wave of 4/SM, 4 splits + merge
+    (64, 8, 64, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 1, 1),   # 64 x 1024: 512 CTAs fit 608 slots
+    (256, 8, 256, 16, pda.PDA_KERNEL_PERSISTENT, 1, 2),     # headline: order kernel + persistent
+    (256, 8, 250, 16, pda.PDA_KERNEL_PERSISTENT, 1, 2),     # ragged up to 4000 tokens
+    (128, 8, 128, 64, pda.PDA_KERNEL_PERSISTENT, 2, 3),     # 64-token blocks: + merge
+    (2200, 8, 8, 16, pda.PDA_KERNEL_PERSISTENT, 1, 1),      # 17,600 units: ticket order, no order kernel
+    (76, 8, 8, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 1, 1),    # 608 units: exactly one dense wave
+    (77, 8, 8, 16, pda.PDA_KERNEL_PERSISTENT, 1, 2),        # 616 units: one more than a dense wave
+    (65535, 65535, 2, 16, pda.PDA_KERNEL_PER_UNIT, 1, 1),   # past 2^31 units: per-unit kernel
+])
+def test_choose_kernel_table(lib, S, Hk, MB, bs, kind, splits, launches):
+    assert pda.choose_kernel(S, Hk, MB, bs, 152, 3, 4) == (kind, splits, launches)
+
+
+def test_choose_kernel_rejects_bad_sizes(lib):
+    for args in [(0, 8, 64, 16, 152, 3, 4), (16, 0, 64, 16, 152, 3, 4), (16, 8, 0, 16, 152, 3, 4),
+                 (16, 8, 64, 16, 0, 3, 4), (16, 8, 64, 16, 152, 0, 4), (16, 8, 64, 16, 152, 3, 0)]:
+        with pytest.raises(pda.PdaError):
+            pda.choose_kernel(*args)
+
+
 def test_choose_splits_invalid_inputs_return_one(lib):
     for args in [(0, 8, 64, 16, SM, OCC), (16, 0, 64, 16, SM, OCC), (16, 8, 0, 16, SM, OCC),
                  (16, 8, 64, 0, SM, OCC), (16, 8, 64, 16, 0, OCC), (16, 8, 64, 16, SM, 0), (-1, 8, 64, 16, SM, OCC)]:

@@ -89,6 +89,19 @@ def test_persistent_bitwise_equals_per_unit_kernel(splits):
     assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("S,Hk,MB,bs", [(16, 8, 64, 16), (64, 8, 64, 16), (256, 8, 256, 16), (128, 8, 128, 64),
+                                       (77, 8, 8, 16), (2200, 8, 8, 16), (40, 4, 300, 32)])
+def test_device_plan_matches_the_pure_planner(S, Hk, MB, bs):
+    # On this device (its SM count, 3 persistent / 4 dense CTAs per SM) the
+    # device-side plan equals the host-only planner's choice.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    kind, splits, launches = pda.choose_kernel(S, Hk, MB, bs, sms, 3, 4)
+    H = 4 * Hk
+    assert pda.plan_kernel(S, H, Hk, MB, bs) == kind
+    assert pda.plan_splits(S, H, Hk, MB, bs) == splits
+    assert pda.plan_launches(S, H, Hk, MB, bs) == launches
+
+
 def test_launch_counts():
     # units beyond the resident slots are handed out longest first (one more
     # launch, up to 16384 units); a split adds the merge launch
