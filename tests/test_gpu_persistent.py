@@ -54,7 +54,7 @@ def _kernel(batch):
 
 
 @pytest.mark.parametrize("bs,splits", [(16, 0), (16, 2), (16, 5), (32, 0), (32, 3), (48, 0), (64, 0), (64, 2),
-                                       (128, 0), (128, 2)])
+                                       (80, 0), (96, 2), (112, 0), (128, 0), (128, 2)])
 def test_persistent_parity(bs, splits):
     batch = _many(160, bs, seed=100 + bs + splits)
     pda.set_split_override(splits)

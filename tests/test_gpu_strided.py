@@ -77,7 +77,7 @@ def test_strided_parity(layout, bs, splits):
 
 
 @pytest.mark.parametrize("layout", ["nhd", "block_split", "packed"])
-@pytest.mark.parametrize("bs,splits", [(16, 0), (16, 2), (32, 0), (64, 3), (128, 0)])
+@pytest.mark.parametrize("bs,splits", [(16, 0), (16, 2), (32, 0), (64, 3), (80, 0), (128, 0)])
 def test_strided_persistent_parity(layout, bs, splits):
     # 160 ragged sequences x 8 kv heads: more units than one wave, so the
     # persistent kernel runs them, its pages arriving through tensor maps.
