@@ -145,10 +145,20 @@ pda_status make_token_major_map(const void* base, long long nb, int hk, int bs, 
   for (auto& x : d)
     if (x.stride <= 0 || (x.stride & 15) != 0 || x.extent <= 0 || x.extent > (1LL << 32) || x.stride >= (1LL << 40))
       return PDA_ERR_INVALID_ARG;
+  // Sort by stride, dimensions of extent 1 (a single kv head or block,
+  // whose stride is never used) last; those then get the stride that nests
+  // exactly after the dimension before them.
+  auto before = [](const D& a, const D& b) {
+    if ((a.extent == 1) != (b.extent == 1)) return b.extent == 1;
+    return a.extent != 1 && a.stride < b.stride;
+  };
   for (int i = 0; i < 3; ++i)
     for (int j = i + 1; j < 3; ++j)
-      if (d[j].stride < d[i].stride) std::swap(d[i], d[j]);
-  if (d[0].stride < kHeadDim || d[1].stride < d[0].stride * d[0].extent || d[2].stride < d[1].stride * d[1].extent)
+      if (before(d[j], d[i])) std::swap(d[i], d[j]);
+  for (int i = 1; i < 3; ++i)
+    if (d[i].extent == 1) d[i].stride = d[i - 1].stride * d[i - 1].extent;
+  if (d[0].stride < kHeadDim || d[1].stride < d[0].stride * d[0].extent || d[2].stride < d[1].stride * d[1].extent ||
+      d[1].stride >= (1LL << 40) || d[2].stride >= (1LL << 40))
     return PDA_ERR_UNSUPPORTED;  // rows overlap: not a layout a tensor map can describe
   EncodeTiledFn enc = encode_tiled();
   if (!enc) return PDA_ERR_CUDA;

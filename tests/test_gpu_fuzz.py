@@ -1,0 +1,110 @@
+"""Randomised GPU parity over the supported shape space, against the fp64 oracle.
+
+Each case draws, from a fixed seed: the batch size, kv heads and GQA ratio
+(1-8), the block size (16-128), ragged lengths (zeros included), a table
+wider than needed, a split count (planned or forced) and an entry point
+(plain, sinks, shuffled V, token-major, per-slot scales). Contexts stay
+short so that the oracle is quick; the batch sizes reach both kernel shapes.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_decode_pda_gb300 as pda
+import workloads
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+D = 128
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    torch.cuda.set_device(0)
+    from paged_kv_decode_pda_gb300 import build
+    build.build()
+    pda.load()
+    pda.set_split_override(0)
+    yield
+    pda.set_split_override(0)
+    assert pda.query_device_status() == 0
+
+
+def _case(seed):
+    rng = np.random.default_rng(1000 + seed)
+    Hk = int(rng.choice([1, 2, 3, 4, 8]))
+    g = int(rng.integers(1, 9))
+    bs = int(rng.choice([16, 32, 48, 64, 80, 96, 112, 128]))
+    S = int(rng.choice([1, 3, 17, 60, 150, 300]))
+    max_len = int(rng.choice([1, 20, 200, 600]))
+    lens = rng.integers(0, max_len + 1, S)
+    lens[rng.random(S) < 0.1] = 0
+    pages = max(1, int((lens.max() + bs - 1) // bs))
+    MB = pages + int(rng.integers(0, 2 * pages + 1))          # tables wider than needed
+    splits = int(rng.choice([0, 0, 1, 2, 3, 7]))
+    variant = str(rng.choice(["plain", "sinks", "shuffled_v", "token_major", "slot_scales"]))
+    return dict(Hk=Hk, g=g, bs=bs, S=S, lens=lens.tolist(), MB=MB, splits=splits, variant=variant, seed=seed)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_case(seed):
+    c = _case(seed)
+    H = c["Hk"] * c["g"]
+    batch = workloads.make_custom(c["S"], H, c["Hk"], c["lens"], block_size=c["bs"], pool_factor=1.3,
+                                  seed=2000 + seed, device=DEV, max_num_blocks_per_seq=c["MB"])
+    cfg = batch.cfg
+    raw = batch.raw()
+    kw = dict(scale=cfg.scale, k_scale=cfg.k_scale, v_scale=cfg.v_scale)
+    label = "case %d %s" % (seed, c)
+    pda.set_split_override(c["splits"])
+    try:
+        v = c["variant"]
+        if v == "plain":
+            out = U.run_cuda(batch)
+            ref = oracle.decode(**raw, **kw)
+        elif v == "sinks":
+            sinks = (torch.randn(H, generator=torch.Generator().manual_seed(seed)) * 2).float()
+            out = pda.decode_ex(batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.seq_lens,
+                                cfg.scale, cfg.k_scale, cfg.v_scale, sinks=sinks.to(DEV))
+            ref = oracle.decode(**raw, **kw, sinks=sinks.numpy())
+        elif v == "shuffled_v":
+            NB, Hk, _, bs = batch.v_cache.shape
+            v_sh = batch.v_cache.reshape(NB, Hk, D, bs // 16, 16).permute(0, 1, 3, 2, 4).contiguous()
+            out = pda.decode_ex(batch.q, batch.k_cache, v_sh, batch.block_tables, batch.seq_lens, cfg.scale,
+                                cfg.k_scale, cfg.v_scale, v_shuffled=True)
+            raw_sh = dict(raw)
+            raw_sh["v_cache"] = v_sh.cpu().contiguous().view(torch.uint8).numpy()
+            ref = oracle.decode(**raw_sh, **kw, v_shuffled=True)
+        elif v == "token_major":
+            k = batch.k_cache.view(torch.uint8)
+            NB, Hk, C, bs, _ = k.shape
+            kt = k.permute(0, 3, 1, 2, 4).reshape(NB, bs, Hk, D).contiguous()
+            vt = batch.v_cache.view(torch.uint8).permute(0, 3, 1, 2).contiguous()
+            st = (bs * Hk * D, Hk * D, D)
+            out = pda.decode_strided(batch.q, kt.data_ptr(), vt.data_ptr(), batch.block_tables, batch.seq_lens,
+                                     cfg.scale, cfg.k_scale, cfg.v_scale, num_kv_heads=Hk, block_size=bs,
+                                     num_blocks=NB, k_strides=st, v_strides=st)
+            torch.cuda.synchronize()
+            del kt, vt
+            ref = oracle.decode(**raw, **kw)
+        else:
+            NB, Hk, bs = batch.num_blocks, c["Hk"], c["bs"]
+            gen = torch.Generator(device=DEV).manual_seed(seed)
+            ks = (torch.rand(NB, Hk, bs, generator=gen, device=DEV) * 0.02 + 0.04).float()
+            vs = (torch.rand(NB, Hk, bs, generator=gen, device=DEV) * 0.02 + 0.04).float()
+            out = pda.decode_slot_scales(batch.q, batch.k_cache, batch.v_cache, ks, vs, batch.block_tables,
+                                         batch.seq_lens, cfg.scale)
+            ref = oracle.decode(**raw, scale=cfg.scale, k_scales=ks.cpu().numpy(), v_scales=vs.cpu().numpy())
+        torch.cuda.synchronize()
+    finally:
+        pda.set_split_override(0)
+    U.compare(out, ref, label)
+    lens = c["lens"]
+    assert all(torch.all(out[s] == 0) for s in range(len(lens)) if lens[s] == 0), label

@@ -114,6 +114,22 @@ def test_strided_headline_batch_full_size():
     U.compare(out[ids], U.run_oracle(batch, seq_ids=ids), "strided nhd headline", literal=True)
 
 
+@pytest.mark.parametrize("layout", ["nhd", "block_split", "packed"])
+@pytest.mark.parametrize("bs", [16, 64])
+def test_strided_single_kv_head(layout, bs):
+    # One kv head: the head dimension has extent 1 and shares the token
+    # stride (NHD), so it must not be taken for an overlapping dimension.
+    batch = workloads.make_custom(3, 7, 1, [404, 0, 199], block_size=bs, pool_factor=1.3, seed=71 + bs,
+                                  device=DEV)
+    cfg = batch.cfg
+    keep, keep2, kp, vp, ks, vs = layouts(batch)[layout]
+    out = pda.decode_strided(batch.q, kp, vp, batch.block_tables, batch.seq_lens, cfg.scale, cfg.k_scale,
+                             cfg.v_scale, num_kv_heads=1, block_size=bs, num_blocks=batch.num_blocks,
+                             k_strides=ks, v_strides=vs)
+    torch.cuda.synchronize()
+    U.compare(out, U.run_oracle(batch), "strided %s, one kv head, bs=%d" % (layout, bs))
+
+
 def test_strided_rejects_bad_strides():
     batch = workloads.make_custom(2, 8, 2, [20, 5], seed=67, device=DEV)
     cfg = batch.cfg
