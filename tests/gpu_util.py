@@ -70,3 +70,33 @@ def compare(got_bf16: torch.Tensor, ref: np.ndarray, label: str = "", literal: b
     assert mean <= mean_bar, "%s: mean abs err %g > %g (bf16 rounding of the exact value alone: %g)" % (
         label, mean, mean_bar, repr_err)
     return stats
+
+
+def compare_e4m3(got_u8: torch.Tensor, exact: np.ndarray, out_scale: float, label: str = "",
+                 min_equal: float = 0.9) -> dict:
+    """Check an e4m3 output (codes of o / out_scale) against the exact result.
+
+    The kernel decides each code on its fp32 result, the oracle on the exact
+    one. Per element the stored value lies within half an e4m3 step at |o|
+    (the rounding any e4m3 output has) plus the 8e-3 bar of the bf16 path;
+    values past 448 * out_scale saturate to +-448 on both sides. On average
+    the kernel adds at most the 2e-4 mean bar to the e4m3 rounding error of
+    the exact values, and most codes equal the code of the exact result.
+    """
+    got = got_u8.view(torch.uint8).cpu().numpy()
+    want = oracle.quantize_e4m3(exact, out_scale)
+    vg = torch.from_numpy(got).view(torch.float8_e4m3fn).double().numpy() * out_scale
+    vw = torch.from_numpy(want).view(torch.float8_e4m3fn).double().numpy() * out_scale
+    target = np.clip(exact, -448.0 * out_scale, 448.0 * out_scale)
+    q = np.abs(target) / out_scale
+    expo = np.floor(np.log2(np.maximum(q, 2.0 ** -6)))
+    half_step = np.ldexp(1.0, (expo - 4).astype(np.int64)) * out_scale
+    err = np.abs(vg - target)
+    assert np.isfinite(vg).all(), "%s: non-finite e4m3 code" % label
+    assert np.all(err <= half_step + MAX_ABS), "%s: max excess %g" % (label, float(np.max(err - half_step)))
+    mean_w = float(np.abs(vw - target).mean()) if err.size else 0.0
+    assert err.mean() <= mean_w + MEAN_ABS, "%s: mean %g vs exact-code mean %g" % (label, err.mean(), mean_w)
+    frac_equal = float(np.mean(got == want)) if err.size else 1.0
+    assert frac_equal >= min_equal, "%s: only %.4f of e4m3 codes equal the exact result's code" % (
+        label, frac_equal)
+    return dict(frac_equal=frac_equal, mean=float(err.mean()) if err.size else 0.0)

@@ -3,11 +3,14 @@
 Each case draws, from a fixed seed: the batch size, kv heads and GQA ratio
 (1-8), the block size (16-128), ragged lengths (zeros included), a table
 wider than needed, a split count (planned or forced) and an entry point
-(plain, sinks, shuffled V, token-major, per-slot scales). Contexts stay
+(plain, sinks, shuffled V, token-major, per-slot scales, e4m3 output with
+sinks and either V layout, the no-allocation entry point). Contexts stay
 short so that the oracle is quick; the batch sizes reach both kernel shapes.
 """
 
 from __future__ import annotations
+
+import os
 
 import numpy as np
 import pytest
@@ -49,11 +52,13 @@ def _case(seed):
     pages = max(1, int((lens.max() + bs - 1) // bs))
     MB = pages + int(rng.integers(0, 2 * pages + 1))          # tables wider than needed
     splits = int(rng.choice([0, 0, 1, 2, 3, 7]))
-    variant = str(rng.choice(["plain", "sinks", "shuffled_v", "token_major", "slot_scales"]))
+    variant = str(rng.choice(["plain", "sinks", "shuffled_v", "token_major", "slot_scales", "e4m3_out",
+                              "noalloc"]))
     return dict(Hk=Hk, g=g, bs=bs, S=S, lens=lens.tolist(), MB=MB, splits=splits, variant=variant, seed=seed)
 
 
-@pytest.mark.parametrize("seed", range(40))
+@pytest.mark.parametrize("seed", range(int(os.environ.get("PDA_FUZZ_FIRST", "0")),
+                                  int(os.environ.get("PDA_FUZZ_FIRST", "0")) + int(os.environ.get("PDA_FUZZ_CASES", "40"))))
 def test_random_case(seed):
     c = _case(seed)
     H = c["Hk"] * c["g"]
@@ -94,6 +99,37 @@ def test_random_case(seed):
             torch.cuda.synchronize()
             del kt, vt
             ref = oracle.decode(**raw, **kw)
+        elif v == "e4m3_out":
+            sinks = (torch.randn(H, generator=torch.Generator().manual_seed(seed)) * 2).float()
+            use_sinks, shuffled = seed % 2 == 0, seed % 3 == 0
+            vc = batch.v_cache
+            if shuffled:
+                NB, Hk, _, bs = vc.shape
+                vc = vc.reshape(NB, Hk, D, bs // 16, 16).permute(0, 1, 3, 2, 4).contiguous()
+            out_scale = 0.0075
+            out = pda.decode_ex(batch.q, batch.k_cache, vc, batch.block_tables, batch.seq_lens, cfg.scale,
+                                cfg.k_scale, cfg.v_scale, sinks=sinks.to(DEV) if use_sinks else None,
+                                output_scale=out_scale, v_shuffled=shuffled)
+            torch.cuda.synchronize()
+            ref = oracle.decode(**raw, **kw, sinks=sinks.numpy() if use_sinks else None)
+        elif v == "noalloc":
+            out = torch.empty_like(batch.q)
+            try:
+                pda.decode_noalloc(batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.seq_lens,
+                                   cfg.scale, cfg.k_scale, cfg.v_scale, out=out)
+            except pda.PdaError as e:
+                # refused before any launch: only a call of two or more splits
+                # needs scratch, 520 bytes per (sequence, head, split)
+                assert e.status == pda.PDA_ERR_NOALLOC_CAPACITY, label
+                assert c["S"] * H * 2 * 520 > 16 << 20, label
+                return
+            if c["splits"]:
+                # the same split count through the allocating entry point: the
+                # per-unit arithmetic is the same whichever kernel runs it
+                again = U.run_cuda(batch)
+                torch.cuda.synchronize()
+                assert torch.equal(out, again), label
+            ref = oracle.decode(**raw, **kw)
         else:
             NB, Hk, bs = batch.num_blocks, c["Hk"], c["bs"]
             gen = torch.Generator(device=DEV).manual_seed(seed)
@@ -105,6 +141,10 @@ def test_random_case(seed):
         torch.cuda.synchronize()
     finally:
         pda.set_split_override(0)
-    U.compare(out, ref, label)
+    if c["variant"] == "e4m3_out":
+        U.compare_e4m3(out, ref, 0.0075, label, min_equal=0.85)
+        out = out.view(torch.uint8)
+    else:
+        U.compare(out, ref, label)
     lens = c["lens"]
     assert all(torch.all(out[s] == 0) for s in range(len(lens)) if lens[s] == 0), label

@@ -268,15 +268,4 @@ def test_persistent_sinks_fp8_and_shuffled_v():
     exact = oracle.decode(**batch.raw(), scale=cfg.scale, k_scale=cfg.k_scale, v_scale=cfg.v_scale,
                           sinks=sinks.numpy())
     U.compare(a, exact, "persistent with sinks")
-    # e4m3 output: each stored code's value lies within half an e4m3 step of
-    # the exact result (clipped to the e4m3 range) plus the 8e-3 bar, and
-    # most codes equal the code of the exact result.
-    got = c.view(torch.uint8).cpu().numpy()
-    vg = torch.from_numpy(got).view(torch.float8_e4m3fn).double().numpy() * out_scale
-    target = np.clip(exact, -448.0 * out_scale, 448.0 * out_scale)
-    q = np.abs(target) / out_scale
-    expo = np.floor(np.log2(np.maximum(q, 2.0 ** -6)))
-    half_step = np.ldexp(1.0, (expo - 4).astype(np.int64)) * out_scale
-    assert np.all(np.abs(vg - target) <= half_step + U.MAX_ABS)
-    want = oracle.quantize_e4m3(exact, out_scale)
-    assert float(np.mean(got == want)) >= 0.9
+    U.compare_e4m3(c, exact, out_scale, "persistent e4m3 output")
