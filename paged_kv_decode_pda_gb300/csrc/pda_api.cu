@@ -86,7 +86,7 @@ RingShape persistent_ring_shape(int bs) {
   uint32_t st = kv > pda::kPersistMergeBytes ? kv : pda::kPersistMergeBytes;
   st = (st + 1023u) & ~1023u;
   r.stage_bytes = st;
-  r.num_stages = (int)((uint32_t)pda::kRingBytes / st);
+  r.num_stages = (int)((uint32_t)pda::kPersistRingBytes / st);
   if (r.num_stages < 2) r.num_stages = 2;
   r.smem_bytes = (size_t)r.num_stages * (st + pda::kAuxBytes) + 8 * (2 * (size_t)r.num_stages + 1) + 16 + 1024;
   return r;
@@ -221,8 +221,8 @@ const void* kernel_fn(KernelKind k) {
     case kPlainDense: return (const void*)pda::pda_split_decode_kernel<false, false, pda::kDenseCtasPerSm>;
     case kSlotWide: return (const void*)pda::pda_split_decode_kernel<true, false, pda::kWideCtasPerSm>;
     case kTokenWide: return (const void*)pda::pda_split_decode_kernel<false, true, pda::kWideCtasPerSm>;
-    case kPersistWide: return (const void*)pda::pda_persistent_decode_kernel<false, pda::kWideCtasPerSm>;
-    case kPersistToken: return (const void*)pda::pda_persistent_decode_kernel<true, pda::kWideCtasPerSm>;
+    case kPersistWide: return (const void*)pda::pda_persistent_decode_kernel<false, pda::kPersistCtasPerSm>;
+    case kPersistToken: return (const void*)pda::pda_persistent_decode_kernel<true, pda::kPersistCtasPerSm>;
     default: return (const void*)pda::pda_split_decode_kernel<false, true, pda::kDenseCtasPerSm>;
   }
 }
@@ -523,16 +523,16 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
         lc.numAttrs = 1;
         const cudaError_t e =
             pl.kind == kPersistToken
-                ? cudaLaunchKernelEx(&lc, pda::pda_persistent_decode_kernel<true, pda::kWideCtasPerSm>, p, queue,
+                ? cudaLaunchKernelEx(&lc, pda::pda_persistent_decode_kernel<true, pda::kPersistCtasPerSm>, p, queue,
                                      units, mk, mv)
-                : cudaLaunchKernelEx(&lc, pda::pda_persistent_decode_kernel<false, pda::kWideCtasPerSm>, p, queue,
+                : cudaLaunchKernelEx(&lc, pda::pda_persistent_decode_kernel<false, pda::kPersistCtasPerSm>, p, queue,
                                      units, mk, mv);
         if (e != cudaSuccess) return PDA_ERR_CUDA;
       } else if (pl.kind == kPersistToken) {
-        pda::pda_persistent_decode_kernel<true, pda::kWideCtasPerSm>
+        pda::pda_persistent_decode_kernel<true, pda::kPersistCtasPerSm>
             <<<pl.grid, pda::kThreads, rs.smem_bytes, stream>>>(p, queue, units, mk, mv);
       } else {
-        pda::pda_persistent_decode_kernel<false, pda::kWideCtasPerSm>
+        pda::pda_persistent_decode_kernel<false, pda::kPersistCtasPerSm>
             <<<pl.grid, pda::kThreads, rs.smem_bytes, stream>>>(p, queue, units, mk, mv);
       }
       break;

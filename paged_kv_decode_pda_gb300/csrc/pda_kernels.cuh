@@ -40,6 +40,14 @@ namespace pda {
 constexpr int kWideCtasPerSm = 3;
 constexpr int kDenseCtasPerSm = 4;
 constexpr int kDenseRingBytes = 49152;
+#ifndef PDA_PERSIST_CTAS
+#define PDA_PERSIST_CTAS 3
+#endif
+#ifndef PDA_PERSIST_RING_BYTES
+#define PDA_PERSIST_RING_BYTES 65536
+#endif
+constexpr int kPersistCtasPerSm = PDA_PERSIST_CTAS;
+constexpr int kPersistRingBytes = PDA_PERSIST_RING_BYTES;
 
 constexpr int kHeadDim = 128;
 constexpr int kChunks = kHeadDim / 16;       // 16-dim chunks of a K page
@@ -464,6 +472,11 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
     return;
   }
 
+  const int n_pages = pg_end - pg_first;
+  // The producer's first 32 block-table entries: the load overlaps the
+  // barrier setup below.
+  const int32_t* row = p.block_tables + (size_t)s * p.max_blocks + pg_first;
+  int my_block = (warp == kConsumerWarps && lane < n_pages) ? __ldg(row + lane) : 0;
   const int NS = p.num_stages;
   const int PPS = p.pages_per_stage;
   // Ring base aligned to 1024 bytes (the 128-byte swizzle repeats every 1 KiB).
@@ -485,20 +498,18 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
   }
   __syncthreads();
 
-  const int n_pages = pg_end - pg_first;
   const int n_fills = (n_pages + PPS - 1) / PPS;
   const uint32_t page_bytes = (uint32_t)(kHeadDim * bs);
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    const int32_t* row = p.block_tables + (size_t)s * p.max_blocks;
     const size_t head_stride = (size_t)page_bytes;
     const size_t block_stride = (size_t)p.num_kv_heads * page_bytes;
     int fill = 0;
     bool ok = true;
     for (int base = 0; base < n_pages && ok; base += 32) {
-      const int my_idx = base + lane;
-      const int my_block = my_idx < n_pages ? __ldg(row + pg_first + my_idx) : 0;
+      // the next chunk's entries, loaded one chunk ahead of their use
+      const int next_block = base + 32 + lane < n_pages ? __ldg(row + base + 32 + lane) : 0;
       const int chunk_pages = min(32, n_pages - base);
       for (int j = 0; j < chunk_pages; j += PPS, ++fill) {
         const int stage = fill % NS;
@@ -564,6 +575,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
         }
         __syncwarp();
       }
+      my_block = next_block;
     }
     // Drain: never leave the CTA with copies still landing in its smem.
     const int issued = fill;
@@ -779,10 +791,15 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
       const int n_pages = pg_end - pg_first;
       const int n_st = skip ? 0 : (n_pages > 0 ? (n_pages + PPS - 1) / PPS : 1);
       const int32_t* row = p.block_tables + (size_t)s * p.max_blocks + pg_first;
-      int my_block = 0;
+      int my_block = 0, next_block = 0;
       for (int k = 0; k < n_st; ++k, ++fill) {
         const int j = k * PPS;  // page offset in the unit; stages never straddle a 32-page chunk
-        if ((j & 31) == 0) my_block = (j + lane < n_pages) ? __ldg(row + j + lane) : 0;
+        if ((j & 31) == 0) {
+          // this chunk's entries (loaded one chunk ahead, except the first)
+          // and the next chunk's
+          my_block = j == 0 ? ((lane < n_pages) ? __ldg(row + lane) : 0) : next_block;
+          next_block = (j + 32 + lane < n_pages) ? __ldg(row + j + 32 + lane) : 0;
+        }
         int blk[kMaxPagesPerStage];
 #pragma unroll
         for (int u = 0; u < kMaxPagesPerStage; ++u) blk[u] = __shfl_sync(0xffffffffu, my_block, (j + u) & 31);
