@@ -301,6 +301,44 @@ pda_status pda_decode_noalloc(void* out, const void* q, const void* k_cache, con
                               int num_kv_heads, int head_size, int block_size, int max_num_blocks_per_seq,
                               float scale, float k_scale, float v_scale, cudaStream_t stream);
 
+/*
+ * pda_decode_host -- pda_decode on inputs and output in host memory. No
+ * counterpart on the pages (whose decode call reads device tensors): an
+ * interface convenience for callers whose batch lives on the host, and the
+ * end-to-end path the benchmark times.
+ *
+ * Host pointers (layouts as pda_decode's; none needs 16-byte alignment):
+ *   out           bf16  [num_seqs][num_heads][head_size]          written
+ *   q             bf16  [num_seqs][num_heads][head_size]          read
+ *   k_cache       e4m3  [num_blocks][num_kv_heads][head_size/16][block_size][16]  read
+ *   v_cache       e4m3  [num_blocks][num_kv_heads][head_size][block_size]          read
+ *   block_tables  int32 [num_seqs][max_num_blocks_per_seq]        read
+ *   seq_lens      int32 [num_seqs]                                read
+ * num_blocks is the number of blocks in the cache arrays (their extent,
+ * which the call copies whole).
+ *
+ * Before anything is enqueued the host checks every table entry a sequence
+ * reads (the first ceil(seq_lens[s] / block_size) of row s) against
+ * [0, num_blocks) and every length against [0, max_num_blocks_per_seq *
+ * block_size]; a bad entry or length returns PDA_ERR_INVALID_ARG and nothing
+ * runs. Then, on `stream`: one cudaMemcpyAsync host -> device per input into
+ * a staging buffer the library keeps per (device, stream), pda_decode on the
+ * staged copies, and one cudaMemcpyAsync device -> host of the output. The
+ * call returns without synchronising: the caller synchronises `stream`
+ * before reading `out` and keeps every input unchanged and alive until then.
+ * Pinned host memory (cudaHostAlloc / cudaHostRegister) makes the copies
+ * asynchronous; with pageable memory they may block the calling thread.
+ *
+ * The staging buffer grows with cudaMallocAsync outside stream capture;
+ * growing it during capture returns PDA_ERR_WORKSPACE (make one call of the
+ * largest shape first). pda_release frees it. Other errors and the supported
+ * set are pda_decode's.
+ */
+pda_status pda_decode_host(void* out, const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, const int32_t* seq_lens, int num_seqs, int num_heads,
+                           int num_kv_heads, int head_size, int block_size, int max_num_blocks_per_seq,
+                           long long num_blocks, float scale, float k_scale, float v_scale, cudaStream_t stream);
+
 /* Static text for a status code; never NULL. */
 const char* pda_status_string(int status);
 

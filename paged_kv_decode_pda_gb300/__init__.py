@@ -29,6 +29,7 @@ from ._binding import (  # noqa: F401
     choose_splits,
     decode,
     decode_ex,
+    decode_host,
     decode_noalloc,
     decode_slot_scales,
     decode_strided,

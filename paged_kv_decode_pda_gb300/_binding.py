@@ -44,6 +44,7 @@ SIGNATURES = {
     "pda_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_longlong, _F, _F, _I, _P]),
     "pda_decode_slot_scales": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "pda_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _F, _P]),
+    "pda_decode_host": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_longlong, _F, _F, _F, _P]),
     "pda_decode_ex": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _F, _I, _P, _I, _F, _P]),
     "pda_decode_strided": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I] + [ctypes.c_longlong] * 7
                            + [_F, _F, _F, _P]),
@@ -256,6 +257,42 @@ def decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
                                 int(block_tables.shape[1]), float(scale), float(k_scale), float(v_scale),
                                 _stream_ptr(stream))
     _check(st, "pda_decode_noalloc")
+    return out
+
+
+def decode_host(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                seq_lens: torch.Tensor, scale: float, k_scale: float, v_scale: float, *, out: torch.Tensor,
+                stream=None) -> torch.Tensor:
+    """``pda_decode_host``: ``decode`` on CPU tensors (pinned for asynchronous copies).
+
+    Shapes and dtypes as ``decode``; every tensor, ``out`` included, is a
+    contiguous CPU tensor. The call enqueues the copies in, the decode and
+    the copy out on ``stream`` and returns: synchronise the stream before
+    reading ``out``, and keep the inputs unchanged until then.
+    """
+    lib = load()
+    if (q.dim() != 3 or k_cache.dim() != 5 or v_cache.dim() != 4 or block_tables.dim() != 2
+            or seq_lens.dim() != 1):
+        raise PdaError(PDA_ERR_INVALID_ARG, "decode_host: tensor ranks")
+    if q.dtype != torch.bfloat16 or block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise PdaError(PDA_ERR_INVALID_ARG, "decode_host: dtypes (q bf16, tables/seq_lens int32)")
+    if any(t.dtype not in (torch.float8_e4m3fn, torch.uint8) for t in (k_cache, v_cache)):
+        raise PdaError(PDA_ERR_INVALID_ARG, "decode_host: cache dtype must be float8_e4m3fn")
+    if out is None or out.shape != q.shape or out.dtype != torch.bfloat16:
+        raise PdaError(PDA_ERR_INVALID_ARG, "decode_host: out must be given, shaped and typed like q")
+    ts = [out, q, k_cache, v_cache, block_tables, seq_lens]
+    if any(t.is_cuda or not t.is_contiguous() for t in ts):
+        raise PdaError(PDA_ERR_INVALID_ARG, "decode_host: tensors must be contiguous CPU tensors")
+    S, H, D = q.shape
+    NB, Hk, D16, bs, sixteen = k_cache.shape
+    if (sixteen != 16 or D16 * 16 != D or tuple(v_cache.shape) != (NB, Hk, D, bs) or block_tables.shape[0] != S
+            or seq_lens.shape[0] != S):
+        raise PdaError(PDA_ERR_INVALID_ARG, "decode_host: shapes")
+    st = lib.pda_decode_host(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                             block_tables.data_ptr(), seq_lens.data_ptr(), S, H, Hk, D, bs,
+                             int(block_tables.shape[1]), NB, float(scale), float(k_scale), float(v_scale),
+                             _stream_ptr(stream))
+    _check(st, "pda_decode_host")
     return out
 
 

@@ -50,6 +50,8 @@ struct Workspace {
 };
 std::mutex g_ws_mu;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+// Staging buffers of pda_decode_host, per (device, stream); under g_ws_mu.
+std::map<std::pair<int, cudaStream_t>, Workspace> g_stage;
 
 // Ring geometry for a block size: a stage holds max(16 * consumer warps, bs)
 // tokens of K and V (whole pages); about kRingBytes of stages per CTA.
@@ -184,10 +186,9 @@ pda_status make_token_major_map(const void* base, long long nb, int hk, int bs, 
   return PDA_OK;
 }
 
-pda_status validate(const void* out, const void* q, const void* k_cache, const void* v_cache,
-                    const int32_t* block_tables, const int32_t* seq_lens, int num_seqs, int num_heads,
-                    int num_kv_heads, int head_size, int block_size, int max_blocks, float scale,
-                    float k_scale, float v_scale) {
+// The checks of sizes and scalars every decode entry point makes.
+pda_status validate_sizes(int num_seqs, int num_heads, int num_kv_heads, int head_size, int block_size,
+                          int max_blocks, float scale, float k_scale, float v_scale) {
   if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 ||
       max_blocks < 0)
     return PDA_ERR_INVALID_ARG;
@@ -199,7 +200,16 @@ pda_status validate(const void* out, const void* q, const void* k_cache, const v
   if (g > pda::kMaxGqa) return PDA_ERR_UNSUPPORTED;
   if (num_seqs > 65535 || num_kv_heads > 65535) return PDA_ERR_UNSUPPORTED;
   if ((long long)max_blocks * block_size > (long long)INT32_MAX / 2) return PDA_ERR_UNSUPPORTED;
-  if (num_seqs == 0) return PDA_OK;
+  return PDA_OK;
+}
+
+pda_status validate(const void* out, const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, const int32_t* seq_lens, int num_seqs, int num_heads,
+                    int num_kv_heads, int head_size, int block_size, int max_blocks, float scale,
+                    float k_scale, float v_scale) {
+  const pda_status st =
+      validate_sizes(num_seqs, num_heads, num_kv_heads, head_size, block_size, max_blocks, scale, k_scale, v_scale);
+  if (st != PDA_OK || num_seqs == 0) return st;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens) return PDA_ERR_INVALID_ARG;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
       (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
@@ -733,13 +743,16 @@ pda_status pda_release(void) {
   int prev = 0;
   cudaGetDevice(&prev);
   pda_status st = PDA_OK;
-  for (auto& kv : g_ws) {
-    if (!kv.second.ptr) continue;
-    if (cudaSetDevice(kv.first.first) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess ||
-        cudaFree(kv.second.ptr) != cudaSuccess)
-      st = PDA_ERR_CUDA;
+  for (auto* m : {&g_ws, &g_stage}) {
+    for (auto& kv : *m) {
+      if (!kv.second.ptr) continue;
+      if (cudaSetDevice(kv.first.first) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess ||
+          cudaFree(kv.second.ptr) != cudaSuccess)
+        st = PDA_ERR_CUDA;
+    }
   }
   g_ws.clear();
+  g_stage.clear();
   cudaSetDevice(prev);
   return st;
 }
@@ -818,6 +831,70 @@ pda_status pda_decode(void* out, const void* q, const void* k_cache, const void*
   return launch_decode(false, out, q, k_cache, v_cache, nullptr, nullptr, block_tables, seq_lens, num_seqs,
                        num_heads, num_kv_heads, head_size, block_size, max_num_blocks_per_seq, scale, k_scale,
                        v_scale, stream);
+}
+
+pda_status pda_decode_host(void* out, const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, const int32_t* seq_lens, int num_seqs, int num_heads,
+                           int num_kv_heads, int head_size, int block_size, int max_num_blocks_per_seq,
+                           long long num_blocks, float scale, float k_scale, float v_scale, cudaStream_t stream) {
+  // pda_decode's checks of sizes and scalars; host pointers need no
+  // particular alignment.
+  const pda_status vs = validate_sizes(num_seqs, num_heads, num_kv_heads, head_size, block_size,
+                                       max_num_blocks_per_seq, scale, k_scale, v_scale);
+  if (vs != PDA_OK || num_seqs == 0) return vs;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || num_blocks <= 0)
+    return PDA_ERR_INVALID_ARG;
+  // Every table entry and length the kernels will read.
+  const long long max_len = (long long)max_num_blocks_per_seq * block_size;
+  for (int s = 0; s < num_seqs; ++s) {
+    const int L = seq_lens[s];
+    if (L < 0 || L > max_len) return PDA_ERR_INVALID_ARG;
+    const int32_t* row = block_tables + (size_t)s * max_num_blocks_per_seq;
+    for (int i = 0, n = (L + block_size - 1) / block_size; i < n; ++i)
+      if (row[i] < 0 || row[i] >= num_blocks) return PDA_ERR_INVALID_ARG;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PDA_ERR_CUDA;
+  auto up = [](size_t b) { return (b + 255) & ~(size_t)255; };
+  const size_t q_bytes = (size_t)num_seqs * num_heads * kHeadDim * 2;
+  const size_t page_bytes = (size_t)num_blocks * num_kv_heads * kHeadDim * block_size;
+  const size_t t_bytes = (size_t)num_seqs * max_num_blocks_per_seq * sizeof(int32_t);
+  const size_t l_bytes = (size_t)num_seqs * sizeof(int32_t);
+  const size_t off_k = up(q_bytes), off_v = off_k + up(page_bytes), off_t = off_v + up(page_bytes);
+  const size_t off_l = off_t + up(t_bytes), off_o = off_l + up(l_bytes), total = off_o + up(q_bytes);
+  char* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    Workspace& sb = g_stage[{dev, stream}];
+    if (sb.bytes < total) {
+      cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+      if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return PDA_ERR_CUDA;
+      if (cs != cudaStreamCaptureStatusNone) return PDA_ERR_WORKSPACE;
+      void* p = nullptr;
+      if (cudaMallocAsync(&p, total, stream) != cudaSuccess) return PDA_ERR_CUDA;
+      if (sb.ptr) cudaFreeAsync(sb.ptr, stream);
+      sb.ptr = p;
+      sb.bytes = total;
+    }
+    base = static_cast<char*>(sb.ptr);
+  }
+  const struct {
+    size_t off;
+    const void* src;
+    size_t bytes;
+  } in[] = {{0, q, q_bytes}, {off_k, k_cache, page_bytes}, {off_v, v_cache, page_bytes},
+            {off_t, block_tables, t_bytes}, {off_l, seq_lens, l_bytes}};
+  for (const auto& c : in)
+    if (c.bytes && cudaMemcpyAsync(base + c.off, c.src, c.bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+      return PDA_ERR_CUDA;
+  pda_status st = launch_decode(false, base + off_o, base, base + off_k, base + off_v, nullptr, nullptr,
+                                reinterpret_cast<const int32_t*>(base + off_t),
+                                reinterpret_cast<const int32_t*>(base + off_l), num_seqs, num_heads, num_kv_heads,
+                                head_size, block_size, max_num_blocks_per_seq, scale, k_scale, v_scale, stream);
+  if (st != PDA_OK) return st;
+  if (cudaMemcpyAsync(out, base + off_o, q_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return PDA_ERR_CUDA;
+  return PDA_OK;
 }
 
 pda_status pda_decode_ex(void* out, const void* q, const void* k_cache, const void* v_cache,

@@ -178,3 +178,40 @@ def test_reserve_rejects_bad_args(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(pda.PdaError, match="not built"):
         _binding.load(str(tmp_path / "missing.so"))
+
+
+# ------------------------------------------- pda_decode_host: host-side checks
+
+def host_call(lib, lens, table, NB=4, H=8, Hk=2, bs=16):
+    import numpy as np
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    table = np.ascontiguousarray(table, dtype=np.int32)
+    S, MB = table.shape
+    q = np.zeros((S, H, 128), np.uint16)
+    out = np.zeros_like(q)
+    k = np.zeros((NB, Hk, 8, bs, 16), np.uint8)
+    v = np.zeros((NB, Hk, 128, bs), np.uint8)
+    return lib.pda_decode_host(out.ctypes.data, q.ctypes.data, k.ctypes.data, v.ctypes.data, table.ctypes.data,
+                               lens.ctypes.data, S, H, Hk, 128, bs, MB, NB, 0.1, 0.05, 0.05, None)
+
+
+@pytest.mark.parametrize("lens,table", [
+    ([17, 5], [[0, 4, 0], [1, 0, 0]]),       # entry 4 of a 4-block pool, read by sequence 0
+    ([17, 5], [[0, 1, 0], [-1, 0, 0]]),      # negative entry read by sequence 1
+    ([49, 0], [[0, 1, 2], [0, 0, 0]]),       # 49 tokens need 4 entries of a 3-entry row
+    ([-1, 0], [[0, 0, 0], [0, 0, 0]]),       # negative length
+])
+def test_decode_host_checks_tables_before_any_copy(lib, lens, table):
+    # Every entry a sequence reads is checked on the host against the pool;
+    # these calls return before any CUDA call (no device is needed).
+    assert host_call(lib, lens, table) == pda.PDA_ERR_INVALID_ARG
+
+
+def test_decode_host_shares_the_size_checks(lib):
+    import numpy as np
+    t = np.zeros((2, 3), np.int32)
+    assert host_call(lib, [1, 1], t, H=18, Hk=2) == pda.PDA_ERR_UNSUPPORTED      # GQA 9
+    assert host_call(lib, [1, 1], t, bs=24) == pda.PDA_ERR_UNSUPPORTED
+    assert host_call(lib, [1, 1], t, NB=0) == pda.PDA_ERR_INVALID_ARG
+    assert lib.pda_decode_host(None, None, None, None, None, None, 0, 8, 2, 128, 16, 3, 4, 0.1, 0.05, 0.05,
+                               None) == pda.PDA_OK
