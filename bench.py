@@ -703,6 +703,9 @@ def make_variant_call(variant, cfg, batch, caches, out, bytes_per_call, stream):
         caches = [nhd(k, v) for k, v in caches]
         hk, bsz = cfg.num_kv_heads, cfg.block_size
         nhd_strides = (bsz * hk * 128, hk * 128, 128)
+    # The variant inputs above were made on torch's current stream; the calls
+    # run on `stream`.
+    torch.cuda.synchronize(dev)
 
     def call(i):
         kc, vc = caches[i % replicas]

@@ -201,6 +201,7 @@ def test_side_stream_and_graph_capture():
     cfg = batch.cfg
     eager = U.run_cuda(batch).clone()
     s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())   # the batch was made on the current stream
     pda.reserve(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq, cfg.block_size,
                 stream=s)
     out = torch.empty_like(batch.q)

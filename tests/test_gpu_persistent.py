@@ -175,6 +175,7 @@ def test_queue_resets_between_calls_and_graph_replays():
     # it at zero: calls of different sizes back to back, then graph replays.
     s = torch.cuda.Stream()
     batches = [_many(S, 16, seed=S) for S in (120, 300, 97)]
+    s.wait_stream(torch.cuda.current_stream())   # the batches were made on the current stream
     for b in batches:
         assert _kernel(b) == pda.PDA_KERNEL_PERSISTENT
     first = []
