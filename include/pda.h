@@ -418,6 +418,22 @@ int pda_plan_launches(int num_seqs, int num_heads, int num_kv_heads, int max_num
 void pda_set_split_override(int num_splits);
 
 /*
+ * pda_set_block_check -- device-side check of block ids for later decode
+ * calls (process-wide). pda_decode, pda_decode_ex, pda_decode_slot_scales
+ * and pda_decode_noalloc are not given the pool size, so a table entry
+ * outside the pool would make them read outside k_cache / v_cache (the
+ * caller's error, see pda_decode). With num_blocks > 0 their kernels check
+ * every block id they read against [0, num_blocks): an id outside it sets
+ * bit 64 of the device status word (pda_query_device_status) and its page is
+ * read from block 0 instead, so that call's output is wrong but no read
+ * leaves the pool. 0 (the default) turns the check off. pda_decode_strided
+ * and pda_decode_host, which are given the pool size, bound their reads
+ * themselves. For debugging and for callers that cannot vouch for their
+ * tables; the check adds a compare per block id in the producer warp.
+ */
+void pda_set_block_check(long long num_blocks);
+
+/*
  * pda_reserve -- size the workspace of (current device, stream) for calls up
  * to these sizes (any entry point's plan: queue words, unit order, split
  * partials), so later calls (for example under stream capture) need no
@@ -433,8 +449,11 @@ pda_status pda_release(void);
  * pda_query_device_status -- synchronise `stream`, then read and clear the
  * device status word of the current device. *code receives 0 when every
  * kernel since the last query finished normally, or a nonzero code when a
- * kernel gave up on a bounded wait (its output is then undefined). Returns
- * PDA_ERR_DEVICE_TIMEOUT when *code != 0. Test / debug call: it blocks.
+ * kernel gave up on a bounded wait, or skipped or redirected an access
+ * outside the pool (a cache-write slot past the pool: bit 16; with
+ * pda_set_block_check, a block id outside the pool: bit 64); the output of
+ * that call is then undefined. Returns PDA_ERR_DEVICE_TIMEOUT when
+ * *code != 0. Test / debug call: it blocks.
  */
 pda_status pda_query_device_status(cudaStream_t stream, int* code);
 

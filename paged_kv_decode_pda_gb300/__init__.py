@@ -42,6 +42,7 @@ from ._binding import (  # noqa: F401
     release,
     reserve,
     reshape_and_cache,
+    set_block_check,
     set_profile_events,
     set_split_override,
     status_string,

@@ -36,6 +36,7 @@ SIGNATURES = {
     "pda_plan_launches": (_I, [_I, _I, _I, _I, _I]),
     "pda_choose_kernel": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "pda_set_split_override": (None, [_I]),
+    "pda_set_block_check": (None, [ctypes.c_longlong]),
     "pda_reserve": (_I, [_I, _I, _I, _I, _I, _P]),
     "pda_release": (_I, []),
     "pda_query_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_int)]),
@@ -351,6 +352,11 @@ def plan_launches(num_seqs, num_heads, num_kv_heads, max_num_blocks_per_seq, blo
 
 def set_split_override(n: int) -> None:
     load().pda_set_split_override(int(n))
+
+
+def set_block_check(num_blocks: int) -> None:
+    """``pda_set_block_check``: check decode block ids against [0, num_blocks) on the device (0 = off)."""
+    load().pda_set_block_check(int(num_blocks))
 
 
 def reserve(num_seqs, num_heads, num_kv_heads, max_num_blocks_per_seq, block_size, stream=None) -> None:

@@ -20,6 +20,9 @@ namespace {
 using pda::kHeadDim;
 
 std::atomic<int> g_split_override{0};
+// pda_set_block_check: the pool size the decode kernels check block ids
+// against (0 = no check), clamped to 2^31 (every int32 id below it).
+std::atomic<uint32_t> g_block_limit{0u};
 std::atomic<cudaEvent_t> g_prof_before{nullptr};
 std::atomic<cudaEvent_t> g_prof_after{nullptr};
 
@@ -462,6 +465,7 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
 
   const RingShape rs = ring_for(pl.kind, block_size);
   pda::DecodeParams p;
+  p.block_limit = g_block_limit.load();
   p.out = out;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k_cache = static_cast<const uint8_t*>(k_cache);
@@ -665,6 +669,10 @@ int pda_choose_kernel(int num_seqs, int num_kv_heads, int max_num_blocks_per_seq
 }
 
 void pda_set_split_override(int num_splits) { g_split_override.store(num_splits > 0 ? num_splits : 0); }
+
+void pda_set_block_check(long long num_blocks) {
+  g_block_limit.store(num_blocks <= 0 ? 0u : (num_blocks >= (1LL << 31) ? (1u << 31) : (uint32_t)num_blocks));
+}
 
 int pda_plan_splits(int num_seqs, int num_heads, int num_kv_heads, int max_num_blocks_per_seq, int block_size) {
   (void)num_heads;
@@ -1035,6 +1043,7 @@ extern "C" pda_status pda_decode_noalloc(void* out, const void* q, const void* k
   const RingShape rs = ring_shape(block_size);
   float* scratch = static_cast<float*>(d.scratch);
   pda::DecodeParams p;
+  p.block_limit = g_block_limit.load();
   p.out = out;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k_cache = static_cast<const uint8_t*>(k_cache);

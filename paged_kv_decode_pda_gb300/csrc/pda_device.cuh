@@ -22,6 +22,7 @@ enum : unsigned int {
   kStatusTestWaitTimeout = 1u << 3,   // pda_test_bounded_wait gave up (expected)
   kStatusBadSlot = 1u << 4,           // reshape_and_cache saw a slot past the pool (skipped)
   kStatusMergeWaitTimeout = 1u << 5,  // persistent decode: consumer warps never met to merge a unit
+  kStatusBadBlock = 1u << 6,          // decode with the block check on: a block id outside the pool
 };
 
 // Limit on any single barrier wait. Healthy waits last microseconds; the

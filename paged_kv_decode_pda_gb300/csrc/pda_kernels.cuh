@@ -96,7 +96,19 @@ struct DecodeParams {
   // Persistent kernel: unit of ticket gridDim.x + i is unit_order[i]
   // (longest first, written by pda_order_units_kernel), or ticket order.
   const int* unit_order = nullptr;
+  // Block check: nonzero = the pool size; a block id outside [0, block_limit)
+  // is recorded in the status word and read as block 0.
+  uint32_t block_limit = 0u;
 };
+
+// A block id the producer is about to read, checked when the block check is on.
+__device__ __forceinline__ int checked_block(int b, uint32_t limit) {
+  if (limit != 0u && (uint32_t)b >= limit) {
+    atomicOr(&g_status, kStatusBadBlock);
+    return 0;
+  }
+  return b;
+}
 
 // Final normalisation shared by the decode kernel (one split) and the merge
 // kernel: a sink logit zs (log2 units, -inf for none) joins the normaliser
@@ -509,6 +521,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
     bool ok = true;
     for (int base = 0; base < n_pages && ok; base += 32) {
       // the next chunk's entries, loaded one chunk ahead of their use
+      // this chunk's entries are checked now that they are needed
+      my_block = checked_block(my_block, p.block_limit);
       const int next_block = base + 32 + lane < n_pages ? __ldg(row + base + 32 + lane) : 0;
       const int chunk_pages = min(32, n_pages - base);
       for (int j = 0; j < chunk_pages; j += PPS, ++fill) {
@@ -797,7 +811,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
         if ((j & 31) == 0) {
           // this chunk's entries (loaded one chunk ahead, except the first)
           // and the next chunk's
-          my_block = j == 0 ? ((lane < n_pages) ? __ldg(row + lane) : 0) : next_block;
+          my_block = checked_block(j == 0 ? ((lane < n_pages) ? __ldg(row + lane) : 0) : next_block, p.block_limit);
           next_block = (j + 32 + lane < n_pages) ? __ldg(row + j + 32 + lane) : 0;
         }
         int blk[kMaxPagesPerStage];
