@@ -85,7 +85,9 @@ typedef enum pda_status {
  * (0 returns PDA_OK with no launch); seq_lens[s] <= max_num_blocks_per_seq *
  * block_size and every used block id in [0, num_blocks) are the caller's
  * contract (the kernel never reads past a table row and clamps lengths to
- * the row's capacity; it does not know num_blocks).
+ * the row's capacity; it does not know num_blocks). pda_set_block_check
+ * makes the kernels check block ids against a given pool size;
+ * pda_decode_host checks the table on the host.
  *
  * Ownership: the caller owns every buffer. The library owns an internal
  * per-(device, stream) workspace: the persistent kernel's work-queue words
