@@ -264,7 +264,7 @@ pda_status pda_reshape_and_cache(const void* key, const void* value, void* k_cac
 
 /*
  * pda_decode_noalloc -- pda_decode for callers that cannot allocate device
- * memory. No counterpart in the paper: this is an interface convenience of
+ * memory. No counterpart on the pages: this is an interface convenience of
  * this library.
  *
  * pda_decode keeps its split partials in a workspace it grows with
