@@ -58,7 +58,7 @@ def _case(seed):
 
 
 @pytest.mark.parametrize("seed", range(int(os.environ.get("PDA_FUZZ_FIRST", "0")),
-                                  int(os.environ.get("PDA_FUZZ_FIRST", "0")) + int(os.environ.get("PDA_FUZZ_CASES", "40"))))
+                                  int(os.environ.get("PDA_FUZZ_FIRST", "0")) + int(os.environ.get("PDA_FUZZ_CASES", "100"))))
 def test_random_case(seed):
     c = _case(seed)
     H = c["Hk"] * c["g"]
