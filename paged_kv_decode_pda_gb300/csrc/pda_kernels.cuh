@@ -1072,7 +1072,8 @@ __global__ void __launch_bounds__(kOrderThreads) pda_order_units_kernel(const Or
 }
 
 // Log-sum-exp merge of the per-split partials of one (sequence, head) per
-// 128-thread block (one output dim per thread):
+// 128-thread block (each warp folds every fourth split for all 128 dims,
+// four per lane, then warp 0 combines the four warps' results):
 //   M = max_i m_i,  out = v_scale * sum_i 2^(m_i - M) O_i / sum_i 2^(m_i - M) l_i
 // with a sink logit, if any, added to the denominator (finish()).
 // Splits with no pages were never written and are skipped by the same page
@@ -1093,9 +1094,11 @@ struct MergeParams {
 };
 
 __global__ void __launch_bounds__(kHeadDim) pda_merge_kernel(const MergeParams p) {
+  constexpr int kWarps = kHeadDim / 32;
   const int h = blockIdx.x;
   const int s = blockIdx.y;
-  const int d = threadIdx.x;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
   int L = __ldg(p.seq_lens + s);
   L = max(0, min(L, p.max_blocks * p.block_size));
   const int pages = (L + p.block_size - 1) / p.block_size;
@@ -1108,19 +1111,54 @@ __global__ void __launch_bounds__(kHeadDim) pda_merge_kernel(const MergeParams p
   // Launched as the decode kernel's programmatic dependent: wait until it
   // has finished and its partials are visible (a no-op otherwise).
   grid_dependency_wait();
-  float M = -INFINITY;
-  for (int i = 0; i < active; ++i) M = fmaxf(M, __ldcg(p.part_ml + (prow0 + i) * 2));
-  float acc = 0.f, den = 0.f;
-  if (M != -INFINITY) {
-    for (int i = 0; i < active; ++i) {
-      const float f = fast_exp2(__ldcg(p.part_ml + (prow0 + i) * 2) - M);
-      acc += f * __ldcg(p.part_o + (prow0 + i) * kHeadDim + d);
-      den += f * __ldcg(p.part_ml + (prow0 + i) * 2 + 1);
-    }
+  // Warp w folds splits w, w + kWarps, ... into a running (M, l, O) for dims
+  // 4 lane .. 4 lane + 3, rescaling by 2^(M_old - M_new) as M grows.
+  float M = -INFINITY, den = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = warp; i < active; i += kWarps) {
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + (prow0 + i));
+    const float4 o = __ldcg(reinterpret_cast<const float4*>(p.part_o + (prow0 + i) * kHeadDim) + lane);
+    const float mn = fmaxf(M, ml.x);
+    const float a = fast_exp2(M - mn);  // 0 while M is -inf
+    const float f = fast_exp2(ml.x - mn);
+    acc.x = acc.x * a + f * o.x;
+    acc.y = acc.y * a + f * o.y;
+    acc.z = acc.z * a + f * o.z;
+    acc.w = acc.w * a + f * o.w;
+    den = den * a + f * ml.y;
+    M = mn;
+  }
+  __shared__ float s_m[kWarps], s_l[kWarps];
+  __shared__ float4 s_o[kWarps][32];
+  if (lane == 0) {
+    s_m[warp] = M;
+    s_l[warp] = den;
+  }
+  s_o[warp][lane] = acc;
+  __syncthreads();
+  if (warp != 0) return;
+  float Mt = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) Mt = fmaxf(Mt, s_m[w]);
+  float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+  float D = 0.f;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    if (s_m[w] == -INFINITY) continue;  // a warp that merged no split
+    const float f = fast_exp2(s_m[w] - Mt);
+    const float4 o = s_o[w][lane];
+    A.x += f * o.x;
+    A.y += f * o.y;
+    A.z += f * o.z;
+    A.w += f * o.w;
+    D += f * s_l[w];
   }
   const float zs = p.sinks ? __ldg(p.sinks + h) * 1.4426950408889634f : -INFINITY;
-  const float r = (pages > 0) ? finish(acc, den, M, zs, p.v_scale) : 0.f;
-  store_out(p.out, ((size_t)s * p.num_heads + h) * kHeadDim + d, r, p.out_fp8, p.out_scale);
+  const float r[4] = {A.x, A.y, A.z, A.w};
+  const size_t o0 = ((size_t)s * p.num_heads + h) * kHeadDim + 4 * lane;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    store_out(p.out, o0 + j, pages > 0 ? finish(r[j], D, Mt, zs, p.v_scale) : 0.f, p.out_fp8, p.out_scale);
 }
 
 // One CTA waits on an mbarrier that nothing completes, with a short limit,
