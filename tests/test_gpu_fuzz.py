@@ -114,15 +114,20 @@ def test_random_case(seed):
             ref = oracle.decode(**raw, **kw, sinks=sinks.numpy() if use_sinks else None)
         elif v == "noalloc":
             out = torch.empty_like(batch.q)
+            # Its split count: the override, or the heuristic's at 3 CTAs per
+            # SM, at most the table width. Its partials take 520 bytes per
+            # (sequence, head, split) of a 16 MiB array; more is refused
+            # before any launch.
+            sms = torch.cuda.get_device_properties(0).multi_processor_count
+            n = min(c["splits"] or pda.choose_splits(c["S"], c["Hk"], c["MB"], c["bs"], sms, 3), c["MB"])
+            refuse = n > 1 and c["S"] * H * n * 520 > 16 << 20
             try:
                 pda.decode_noalloc(batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.seq_lens,
                                    cfg.scale, cfg.k_scale, cfg.v_scale, out=out)
             except pda.PdaError as e:
-                # refused before any launch: only a call of two or more splits
-                # needs scratch, 520 bytes per (sequence, head, split)
-                assert e.status == pda.PDA_ERR_NOALLOC_CAPACITY, label
-                assert c["S"] * H * 2 * 520 > 16 << 20, label
+                assert refuse and e.status == pda.PDA_ERR_NOALLOC_CAPACITY, label
                 return
+            assert not refuse, label
             if c["splits"]:
                 # the same split count through the allocating entry point: the
                 # per-unit arithmetic is the same whichever kernel runs it
