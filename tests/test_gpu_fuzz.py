@@ -1,8 +1,9 @@
 """Randomised GPU parity over the supported shape space, against the fp64 oracle.
 
-Each case draws, from a fixed seed: the batch size, kv heads and GQA ratio
-(1-8), the block size (16-128), ragged lengths (zeros included), a table
-wider than needed, a split count (planned or forced) and an entry point
+Each case draws, from a fixed seed: the batch size, kv heads (1-32) and GQA
+ratio (1-8), the block size (16-128), ragged lengths (zeros included), a
+table wider than needed (a quarter of the cases draw it with replacement, so
+blocks are shared and repeated), a split count (planned or forced) and an entry point
 (plain, sinks, shuffled V, token-major, per-slot scales, e4m3 output with
 sinks and either V layout, the no-allocation entry point). Contexts stay
 short so that the oracle is quick; the batch sizes reach both kernel shapes.
@@ -42,7 +43,7 @@ def _lib():
 
 def _case(seed):
     rng = np.random.default_rng(1000 + seed)
-    Hk = int(rng.choice([1, 2, 3, 4, 8]))
+    Hk = int(rng.choice([1, 2, 3, 4, 8, 16, 32]))
     g = int(rng.integers(1, 9))
     bs = int(rng.choice([16, 32, 48, 64, 80, 96, 112, 128]))
     S = int(rng.choice([1, 3, 17, 60, 150, 300]))
@@ -54,7 +55,9 @@ def _case(seed):
     splits = int(rng.choice([0, 0, 1, 2, 3, 7]))
     variant = str(rng.choice(["plain", "sinks", "shuffled_v", "token_major", "slot_scales", "e4m3_out",
                               "noalloc"]))
-    return dict(Hk=Hk, g=g, bs=bs, S=S, lens=lens.tolist(), MB=MB, splits=splits, variant=variant, seed=seed)
+    shared = bool(rng.random() < 0.25)   # tables drawn with replacement: shared and repeated blocks
+    return dict(Hk=Hk, g=g, bs=bs, S=S, lens=lens.tolist(), MB=MB, splits=splits, variant=variant,
+                shared=shared, seed=seed)
 
 
 @pytest.mark.parametrize("seed", range(int(os.environ.get("PDA_FUZZ_FIRST", "0")),
@@ -65,6 +68,12 @@ def test_random_case(seed):
     batch = workloads.make_custom(c["S"], H, c["Hk"], c["lens"], block_size=c["bs"], pool_factor=1.3,
                                   seed=2000 + seed, device=DEV, max_num_blocks_per_seq=c["MB"])
     cfg = batch.cfg
+    if c["shared"]:
+        # prefix-cache style tables: sequences share physical blocks and a
+        # sequence may name one block twice
+        gen = torch.Generator(device=DEV).manual_seed(3000 + seed)
+        batch.block_tables.copy_(torch.randint(0, batch.num_blocks, tuple(batch.block_tables.shape),
+                                               generator=gen, device=DEV, dtype=torch.int32))
     raw = batch.raw()
     kw = dict(scale=cfg.scale, k_scale=cfg.k_scale, v_scale=cfg.v_scale)
     label = "case %d %s" % (seed, c)
