@@ -215,3 +215,20 @@ def test_decode_host_shares_the_size_checks(lib):
     assert host_call(lib, [1, 1], t, NB=0) == pda.PDA_ERR_INVALID_ARG
     assert lib.pda_decode_host(None, None, None, None, None, None, 0, 8, 2, 128, 16, 3, 4, 0.1, 0.05, 0.05,
                                None) == pda.PDA_OK
+
+
+def test_plain_c_caller(lib, tmp_path):
+    # The boundary is C: a C11 program includes the header on its own, links
+    # libpda.so and calls host-side entry points.
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    exe = tmp_path / "abi_c_check"
+    libdir = os.path.dirname(pda.LIB_PATH)
+    subprocess.run([cc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "abi_c_check.c"), "-L", libdir, "-lpda", "-Wl,-rpath," + libdir,
+                    "-o", str(exe)], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stdout, r.stderr)
