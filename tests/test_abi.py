@@ -96,6 +96,12 @@ def test_choose_splits_bounds_and_monotonicity(lib):
     (76, 8, 8, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 1, 1),    # 608 units: exactly one dense wave
     (77, 8, 8, 16, pda.PDA_KERNEL_PERSISTENT, 1, 2),        # 616 units: one more than a dense wave
     (65535, 65535, 2, 16, pda.PDA_KERNEL_PER_UNIT, 1, 1),   # past 2^31 units: per-unit kernel
+    # long contexts: a few sequences split into page ranges up to a dense wave
+    (1, 8, 8192, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 76, 2),   # 1 x 128K tokens: 608 CTAs + merge
+    (4, 8, 2048, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 19, 2),   # 4 x 32K
+    (16, 8, 640, 64, pda.PDA_KERNEL_PERSISTENT, 10, 3),       # 16 x 40,960, 64-token blocks
+    (8, 8, 8192, 16, pda.PDA_KERNEL_PERSISTENT, 32, 3),       # 8 x 128K
+    (64, 8, 2048, 16, pda.PDA_KERNEL_PERSISTENT, 8, 3),       # 64 x 32K: 1 MiB split units
 ])
 def test_choose_kernel_table(lib, S, Hk, MB, bs, kind, splits, launches):
     assert pda.choose_kernel(S, Hk, MB, bs, 152, 3, 4) == (kind, splits, launches)
