@@ -23,6 +23,7 @@ import json
 import math
 import os
 import platform
+import re
 import statistics
 import subprocess
 import sys
@@ -115,13 +116,21 @@ KERNEL_FUNCTION = {"per-unit (3 CTAs/SM)": "pda_split_decode_kernel", "per-unit 
 
 
 def kernel_source_sha() -> str:
-    """Hash of the device sources the decode kernel is compiled from (host code excluded)."""
+    """Hash of the device sources the decode kernel is compiled from (host code excluded).
+
+    Comments and blank lines are left out, so editing a comment keeps the
+    recorded ncu traffic valid; any change to the code itself changes the hash.
+    """
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_pda_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith(".cuh"):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                text = f.read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            text = re.sub(r"//[^\n]*", "", text)
+            text = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+            h.update(name.encode() + b"\0" + text.encode())
     return h.hexdigest()[:16]
 
 

@@ -1,6 +1,12 @@
-// Split-KV fp8 paged decode kernel and log-sum-exp merge kernel (sm_103a).
+// The library's kernels (sm_103a):
+//   pda_split_decode_kernel       one CTA per work unit (below)
+//   pda_persistent_decode_kernel  one CTA per resident slot taking work units
+//                                 from a queue, the same per-unit arithmetic
+//   pda_order_units_kernel        longest-first order of the queued units
+//   pda_merge_kernel              log-sum-exp merge of split partials
+//   pda_reshape_and_cache_kernel  KV-cache write (and a scattered variant)
 //
-// Work unit: one (sequence, kv head, KV split). One CTA per unit:
+// Work unit: one (sequence, kv head, KV split). Per unit:
 //   * warp kConsumerWarps (the producer) gathers the split's pages through
 //     the block table and streams them with 1-D bulk (TMA) copies into a
 //     ring of shared-memory stages, one mbarrier pair per stage;
