@@ -75,6 +75,15 @@ typedef enum pda_status {
  * attention); k_scale and v_scale multiply the e4m3 values on dequantisation
  * (value = e4m3 * scale), i.e. the k/v "descale" of the API page.
  *
+ * Value range: q may hold any finite bf16 values (the whole bf16 range, not
+ * only f16's): each query row is scaled by a power of two before it enters
+ * the f16 tensor-core products and the logit scale by its inverse, which is
+ * exact. The logits scale * k_scale * q . k_t must stay finite in binary32
+ * (|logit| < 2^126 suffices). NaN or infinite inputs give undefined output.
+ * Arithmetic: e4m3 -> f16 and the shifted bf16 q -> f16 are exact; scores,
+ * softmax and accumulation are fp32; the probabilities enter the PV product
+ * as two f16 parts (f16(p) and f16(p - f16(p))), about 2^-22 relative.
+ *
  * max_num_blocks_per_seq is the row stride of block_tables. It is not in the
  * argument list the method states; it is required to index a [S, MB] table
  * and gives the host an upper bound on context length without reading
@@ -97,6 +106,13 @@ typedef enum pda_status {
  * (size the workspace first with pda_reserve), and a one-split call runs the
  * per-unit kernel, which needs none. Calls on one stream run in stream order
  * and share its workspace; calls on different streams have their own.
+ * A CUDA graph that captured a call keeps that call's workspace address: when
+ * a later, larger call grows the workspace, the old buffer is kept allocated
+ * (not reused) until pda_release, so replaying the graph stays valid.
+ * pda_release frees every workspace, old ones included, and so invalidates
+ * every graph that captured a pda_decode* call; re-capture after it. Two
+ * replays of graphs that captured calls on one stream share that stream's
+ * workspace and must not run at the same time.
  *
  * Determinism: for fixed inputs and a fixed split count the result is
  * bitwise reproducible. Which CTA computes a work unit, and when, changes
@@ -287,9 +303,9 @@ pda_status pda_reshape_and_cache(const void* key, const void* value, void* k_cac
  * num_seqs * num_heads * splits * 520 bytes must fit in 16 MiB (splits is
  * the split count above; a call that needs one split uses no scratch at
  * all); larger calls return PDA_ERR_NOALLOC_CAPACITY before
- * launching anything. The first call on each device also looks up the
- * array's device address and the device's properties (no allocation); make
- * that first call outside any stream capture. All calls on a device share
+ * launching anything. The first call on each device (and the first after
+ * pda_release) also looks up the array's device address and the device's
+ * properties (no allocation); make that call outside any stream capture. All calls on a device share
  * the one array: nothing in it needs to start at zero (each call writes the
  * partials it reads), but two calls whose kernels can run at the same time
  * on the GPU (on two streams with no ordering between them, from two host
@@ -444,8 +460,25 @@ void pda_set_block_check(long long num_blocks);
 pda_status pda_reserve(int num_seqs, int num_heads, int num_kv_heads, int max_num_blocks_per_seq,
                        int block_size, cudaStream_t stream);
 
-/* pda_release -- free every workspace the library holds (synchronises each device used). */
+/*
+ * pda_release -- free every workspace and staging buffer the library holds,
+ * the ones that growth retired included (synchronises each device used),
+ * and forget the per-device set-up (SM counts, kernel attributes, the
+ * pda_decode_noalloc array's address), which the next call takes again.
+ * Graphs that captured a pda_decode* or pda_decode_host call refer to freed
+ * memory afterwards and must not be replayed. A cudaDeviceReset destroys
+ * everything the library set up on that device: call pda_release before
+ * resetting a device the library has used.
+ */
 pda_status pda_release(void);
+
+/*
+ * pda_workspace_info -- the workspace of (current device, stream): *bytes
+ * receives its current size (0 when it has none) and *retired the number of
+ * smaller buffers it replaced that are still allocated for graphs that
+ * captured them. Diagnostic; host only, no synchronisation.
+ */
+pda_status pda_workspace_info(cudaStream_t stream, long long* bytes, int* retired);
 
 /*
  * pda_query_device_status -- synchronise `stream`, then read and clear the

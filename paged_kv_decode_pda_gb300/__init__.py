@@ -39,6 +39,7 @@ from ._binding import (  # noqa: F401
     plan_launches,
     plan_splits,
     query_device_status,
+    workspace_info,
     release,
     reserve,
     reshape_and_cache,

@@ -39,6 +39,7 @@ SIGNATURES = {
     "pda_set_block_check": (None, [ctypes.c_longlong]),
     "pda_reserve": (_I, [_I, _I, _I, _I, _I, _P]),
     "pda_release": (_I, []),
+    "pda_workspace_info": (_I, [_P, ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(_I)]),
     "pda_query_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_int)]),
     "pda_set_profile_events": (None, [_P, _P]),
     "pda_test_bounded_wait": (_I, [_I, _P]),
@@ -366,6 +367,16 @@ def reserve(num_seqs, num_heads, num_kv_heads, max_num_blocks_per_seq, block_siz
 
 def release() -> None:
     _check(load().pda_release(), "pda_release")
+
+
+def workspace_info(stream=None) -> tuple[int, int]:
+    """``pda_workspace_info``: (current bytes, retired buffers kept alive) of
+    the current device's workspace for ``stream``."""
+    lib = load()
+    nbytes, retired = ctypes.c_longlong(0), _I(0)
+    _check(lib.pda_workspace_info(_stream_ptr(stream), ctypes.byref(nbytes), ctypes.byref(retired)),
+           "pda_workspace_info")
+    return int(nbytes.value), int(retired.value)
 
 
 def query_device_status(stream=None) -> int:

@@ -11,6 +11,7 @@
 #include <map>
 #include <mutex>
 #include <utility>
+#include <vector>
 
 #include "../../include/pda.h"
 #include "pda_kernels.cuh"
@@ -39,6 +40,9 @@ enum KernelKind {
 };
 bool is_persistent(int k) { return k == kPersistWide || k == kPersistToken; }
 
+// Forgets pda_decode_noalloc's per-device set-up (defined with it below).
+void noalloc_forget_devices();
+
 struct DeviceInfo {
   int sm_count = 0;
   int ctas_per_sm[kNumKinds][9] = {{0}};  // [instance][bs/16 (1..8)]
@@ -50,6 +54,10 @@ std::map<int, DeviceInfo> g_devices;
 struct Workspace {
   void* ptr = nullptr;
   size_t bytes = 0;
+  // Buffers this one replaced when it grew. A CUDA graph captured earlier
+  // keeps their addresses in its kernel parameters, so they stay allocated
+  // until pda_release.
+  std::vector<void*> retired;
 };
 std::mutex g_ws_mu;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
@@ -228,16 +236,38 @@ RingShape ring_for(KernelKind k, int bs) {
   return ring_shape(bs, is_slot(k), is_dense(k) ? pda::kDenseRingBytes : pda::kRingBytes);
 }
 
-const void* kernel_fn(KernelKind k) {
+// Kernel function types of the decode instances.
+using SplitFn = void (*)(const pda::DecodeParams, const CUtensorMap, const CUtensorMap);
+using PersistFn = void (*)(const pda::DecodeParams, unsigned*, int, const CUtensorMap, const CUtensorMap);
+
+// Each decode instance comes in two builds: paired PV columns for GQA groups
+// of at most 4 heads, a second PV MMA for wider groups (see TileWorker).
+bool paired_for(int gqa) { return gqa <= pda::kMaxGqa / 2; }
+
+template <bool kPaired>
+SplitFn split_fn_of(KernelKind k) {
   switch (k) {
-    case kPlainWide: return (const void*)pda::pda_split_decode_kernel<false, false, pda::kWideCtasPerSm>;
-    case kPlainDense: return (const void*)pda::pda_split_decode_kernel<false, false, pda::kDenseCtasPerSm>;
-    case kSlotWide: return (const void*)pda::pda_split_decode_kernel<true, false, pda::kWideCtasPerSm>;
-    case kTokenWide: return (const void*)pda::pda_split_decode_kernel<false, true, pda::kWideCtasPerSm>;
-    case kPersistWide: return (const void*)pda::pda_persistent_decode_kernel<false, pda::kPersistCtasPerSm>;
-    case kPersistToken: return (const void*)pda::pda_persistent_decode_kernel<true, pda::kPersistCtasPerSm>;
-    default: return (const void*)pda::pda_split_decode_kernel<false, true, pda::kDenseCtasPerSm>;
+    case kPlainWide: return pda::pda_split_decode_kernel<false, false, pda::kWideCtasPerSm, kPaired>;
+    case kPlainDense: return pda::pda_split_decode_kernel<false, false, pda::kDenseCtasPerSm, kPaired>;
+    case kSlotWide: return pda::pda_split_decode_kernel<true, false, pda::kWideCtasPerSm, kPaired>;
+    case kTokenWide: return pda::pda_split_decode_kernel<false, true, pda::kWideCtasPerSm, kPaired>;
+    case kTokenDense: return pda::pda_split_decode_kernel<false, true, pda::kDenseCtasPerSm, kPaired>;
+    default: return nullptr;
   }
+}
+SplitFn split_fn(KernelKind k, bool paired) { return paired ? split_fn_of<true>(k) : split_fn_of<false>(k); }
+
+PersistFn persist_fn(bool token_major, bool paired) {
+  if (token_major)
+    return paired ? pda::pda_persistent_decode_kernel<true, pda::kPersistCtasPerSm, true>
+                  : pda::pda_persistent_decode_kernel<true, pda::kPersistCtasPerSm, false>;
+  return paired ? pda::pda_persistent_decode_kernel<false, pda::kPersistCtasPerSm, true>
+                : pda::pda_persistent_decode_kernel<false, pda::kPersistCtasPerSm, false>;
+}
+
+const void* kernel_fn(KernelKind k, bool paired) {
+  if (is_persistent(k)) return (const void*)persist_fn(k == kPersistToken, paired);
+  return (const void*)split_fn(k, paired);
 }
 
 // SM count and resident CTAs per SM of instance `kind` for block size bs.
@@ -259,18 +289,24 @@ pda_status device_info(int dev, int bs, int* sm_count, int* ctas_per_sm, KernelK
         mx = sb > mx ? sb : mx;
       }
     for (int k = 0; k < kNumKinds; ++k)
-      if (cudaFuncSetAttribute(kernel_fn((KernelKind)k), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx) !=
-          cudaSuccess)
-        return PDA_ERR_CUDA;
+      for (bool paired : {false, true})
+        if (cudaFuncSetAttribute(kernel_fn((KernelKind)k, paired), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)mx) != cudaSuccess)
+          return PDA_ERR_CUDA;
     di.smem_attr_set = true;
   }
   int& occ = di.ctas_per_sm[kind][bs / 16];
   if (occ == 0) {
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel_fn(kind), pda::kThreads,
-                                                      ring_for(kind, bs).smem_bytes) != cudaSuccess)
-      return PDA_ERR_CUDA;
-    occ = n > 0 ? n : 1;
+    // the smaller residency of the two builds (the plan does not depend on g)
+    int m = 0;
+    for (bool paired : {false, true}) {
+      int n = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel_fn(kind, paired), pda::kThreads,
+                                                        ring_for(kind, bs).smem_bytes) != cudaSuccess)
+        return PDA_ERR_CUDA;
+      m = (m == 0 || n < m) ? n : m;
+    }
+    occ = m > 0 ? m : 1;
   }
   *sm_count = di.sm_count;
   *ctas_per_sm = occ;
@@ -422,11 +458,36 @@ pda_status get_workspace(int dev, cudaStream_t stream, size_t bytes, void** out)
     cudaFreeAsync(p, stream);
     return PDA_ERR_CUDA;
   }
-  if (ws.ptr) cudaFreeAsync(ws.ptr, stream);
+  if (ws.ptr) ws.retired.push_back(ws.ptr);
   ws.ptr = p;
   ws.bytes = want;
   *out = p;
   return PDA_OK;
+}
+
+// Launch the merge kernel for partials of nsplit splits (one warp per row up
+// to kMergeRowSplits splits, else one block per row), as the programmatic
+// dependent of the kernel before it on `stream` when pdl is set.
+cudaError_t launch_merge(const pda::MergeParams& mp, cudaStream_t stream, bool pdl) {
+  cudaLaunchConfig_t lc = {};
+  if (mp.nsplit <= pda::kMergeRowSplits) {
+    const long long rows = (long long)mp.num_seqs * mp.num_heads;
+    lc.gridDim = dim3((unsigned)((rows + pda::kMergeRowsPerBlock - 1) / pda::kMergeRowsPerBlock));
+  } else {
+    lc.gridDim = dim3((unsigned)mp.num_heads, (unsigned)mp.num_seqs);
+  }
+  lc.blockDim = dim3(kHeadDim);
+  lc.dynamicSmemBytes = 0;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+  }
+  return mp.nsplit <= pda::kMergeRowSplits ? cudaLaunchKernelEx(&lc, pda::pda_merge_kernel, mp)
+                                            : cudaLaunchKernelEx(&lc, pda::pda_merge_wide_kernel, mp);
 }
 
 }  // namespace
@@ -504,73 +565,46 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
   dim3 grid((unsigned)nsplit, (unsigned)num_kv_heads, (unsigned)num_seqs);
   const CUtensorMap& mk = tm ? tm->k : g_no_map;
   const CUtensorMap& mv = tm ? tm->v : g_no_map;
-  switch (pl.kind) {
-    case kPersistWide:
-    case kPersistToken: {
-      const int units = num_seqs * num_kv_heads * nsplit;
-      if (pl.ordered > 0) {
-        // The order kernel, then the decode kernel as its programmatic
-        // dependent: the decode CTAs start on their first units at once and
-        // wait for the order only before taking a second one.
-        pda::OrderParams op;
-        op.seq_lens = seq_lens;
-        op.order = reinterpret_cast<int*>(static_cast<char*>(ws) + wl.order_off);
-        op.first = (int)pl.grid;
-        op.num_units = units;
-        op.num_kv_heads = num_kv_heads;
-        op.nsplit = nsplit;
-        op.block_size = block_size;
-        op.max_blocks = max_num_blocks_per_seq;
-        op.max_split_pages = (max_num_blocks_per_seq + nsplit - 1) / nsplit;
-        pda::pda_order_units_kernel<<<1, pda::kOrderThreads, 0, stream>>>(op);
-        if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
-        p.unit_order = op.order;
-        cudaLaunchConfig_t lc = {};
-        lc.gridDim = dim3(pl.grid);
-        lc.blockDim = dim3(pda::kThreads);
-        lc.dynamicSmemBytes = rs.smem_bytes;
-        lc.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        lc.attrs = attr;
-        lc.numAttrs = 1;
-        const cudaError_t e =
-            pl.kind == kPersistToken
-                ? cudaLaunchKernelEx(&lc, pda::pda_persistent_decode_kernel<true, pda::kPersistCtasPerSm>, p, queue,
-                                     units, mk, mv)
-                : cudaLaunchKernelEx(&lc, pda::pda_persistent_decode_kernel<false, pda::kPersistCtasPerSm>, p, queue,
-                                     units, mk, mv);
-        if (e != cudaSuccess) return PDA_ERR_CUDA;
-      } else if (pl.kind == kPersistToken) {
-        pda::pda_persistent_decode_kernel<true, pda::kPersistCtasPerSm>
-            <<<pl.grid, pda::kThreads, rs.smem_bytes, stream>>>(p, queue, units, mk, mv);
-      } else {
-        pda::pda_persistent_decode_kernel<false, pda::kPersistCtasPerSm>
-            <<<pl.grid, pda::kThreads, rs.smem_bytes, stream>>>(p, queue, units, mk, mv);
-      }
-      break;
+  const bool paired = paired_for(p.gqa);
+  if (is_persistent(pl.kind)) {
+    const int units = num_seqs * num_kv_heads * nsplit;
+    const PersistFn fn = persist_fn(pl.kind == kPersistToken, paired);
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(pl.grid);
+    lc.blockDim = dim3(pda::kThreads);
+    lc.dynamicSmemBytes = rs.smem_bytes;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (pl.ordered > 0) {
+      // The order kernel, then the decode kernel as its programmatic
+      // dependent: the decode CTAs start on their first units at once and
+      // wait for the order only before taking a second one.
+      pda::OrderParams op;
+      op.seq_lens = seq_lens;
+      op.order = reinterpret_cast<int*>(static_cast<char*>(ws) + wl.order_off);
+      op.first = (int)pl.grid;
+      op.num_units = units;
+      op.num_kv_heads = num_kv_heads;
+      op.nsplit = nsplit;
+      op.block_size = block_size;
+      op.max_blocks = max_num_blocks_per_seq;
+      op.max_split_pages = (max_num_blocks_per_seq + nsplit - 1) / nsplit;
+      pda::pda_order_units_kernel<<<1, pda::kOrderThreads, 0, stream>>>(op);
+      if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
+      p.unit_order = op.order;
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      lc.attrs = attr;
+      lc.numAttrs = 1;
     }
-    case kPlainWide:
-      pda::pda_split_decode_kernel<false, false, pda::kWideCtasPerSm><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(
-          p, mk, mv);
-      break;
-    case kPlainDense:
-      pda::pda_split_decode_kernel<false, false, pda::kDenseCtasPerSm><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(
-          p, mk, mv);
-      break;
-    case kSlotWide:
-      pda::pda_split_decode_kernel<true, false, pda::kWideCtasPerSm><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(
-          p, mk, mv);
-      break;
-    case kTokenWide:
-      pda::pda_split_decode_kernel<false, true, pda::kWideCtasPerSm><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(
-          p, mk, mv);
-      break;
-    default:
-      pda::pda_split_decode_kernel<false, true, pda::kDenseCtasPerSm><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(
-          p, mk, mv);
-      break;
+    if (cudaLaunchKernelEx(&lc, fn, p, queue, units, mk, mv) != cudaSuccess) return PDA_ERR_CUDA;
+  } else {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = grid;
+    lc.blockDim = dim3(pda::kThreads);
+    lc.dynamicSmemBytes = rs.smem_bytes;
+    lc.stream = stream;
+    if (cudaLaunchKernelEx(&lc, split_fn(pl.kind, paired), p, mk, mv) != cudaSuccess) return PDA_ERR_CUDA;
   }
   if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
   if (eb && ea && record_profile_event(ea, stream) != cudaSuccess) return PDA_ERR_CUDA;
@@ -581,6 +615,7 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
     mp.part_o = p.part_o;
     mp.part_ml = p.part_ml;
     mp.seq_lens = seq_lens;
+    mp.num_seqs = num_seqs;
     mp.num_heads = num_heads;
     mp.block_size = block_size;
     mp.max_blocks = max_num_blocks_per_seq;
@@ -591,17 +626,7 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
     mp.out_scale = out_scale;
     // Programmatic dependent of the decode kernel: its launch overlaps the
     // decode kernel's last CTAs, and it waits for the partials on the device.
-    cudaLaunchConfig_t lc = {};
-    lc.gridDim = dim3((unsigned)num_heads, (unsigned)num_seqs);
-    lc.blockDim = dim3(kHeadDim);
-    lc.dynamicSmemBytes = 0;
-    lc.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    lc.attrs = attr;
-    lc.numAttrs = 1;
-    if (cudaLaunchKernelEx(&lc, pda::pda_merge_kernel, mp) != cudaSuccess) return PDA_ERR_CUDA;
+    if (launch_merge(mp, stream, true) != cudaSuccess) return PDA_ERR_CUDA;
   }
   return PDA_OK;
 }
@@ -754,15 +779,38 @@ pda_status pda_release(void) {
   for (auto* m : {&g_ws, &g_stage}) {
     for (auto& kv : *m) {
       if (!kv.second.ptr) continue;
-      if (cudaSetDevice(kv.first.first) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess ||
-          cudaFree(kv.second.ptr) != cudaSuccess)
+      if (cudaSetDevice(kv.first.first) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
         st = PDA_ERR_CUDA;
+        continue;
+      }
+      kv.second.retired.push_back(kv.second.ptr);
+      for (void* ptr : kv.second.retired)
+        if (cudaFree(ptr) != cudaSuccess) st = PDA_ERR_CUDA;
     }
   }
   g_ws.clear();
   g_stage.clear();
   cudaSetDevice(prev);
+  // Per-device set-up (SM counts, occupancy, shared-memory opt-ins, the
+  // no-allocation scratch address) is taken again on the next call, so a
+  // device reset between this call and the next does not leave it stale.
+  {
+    std::lock_guard<std::mutex> dk(g_dev_mu);
+    g_devices.clear();
+  }
+  noalloc_forget_devices();
   return st;
+}
+
+pda_status pda_workspace_info(cudaStream_t stream, long long* bytes, int* retired) {
+  if (!bytes || !retired) return PDA_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PDA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_ws_mu);
+  const auto it = g_ws.find({dev, stream});
+  *bytes = it == g_ws.end() ? 0 : (long long)it->second.bytes;
+  *retired = it == g_ws.end() ? 0 : (int)it->second.retired.size();
+  return PDA_OK;
 }
 
 pda_status pda_query_device_status(cudaStream_t stream, int* code) {
@@ -880,7 +928,7 @@ pda_status pda_decode_host(void* out, const void* q, const void* k_cache, const 
       if (cs != cudaStreamCaptureStatusNone) return PDA_ERR_WORKSPACE;
       void* p = nullptr;
       if (cudaMallocAsync(&p, total, stream) != cudaSuccess) return PDA_ERR_CUDA;
-      if (sb.ptr) cudaFreeAsync(sb.ptr, stream);
+      if (sb.ptr) sb.retired.push_back(sb.ptr);
       sb.ptr = p;
       sb.bytes = total;
     }
@@ -967,7 +1015,8 @@ pda_status pda_decode_slot_scales(void* out, const void* q, const void* k_cache,
 
 namespace {
 
-// Room for num_seqs * num_heads * splits <= 32,264 partial rows of 520 bytes.
+// Room for rows * 520 <= 16 MiB, i.e. num_seqs * num_heads * splits <= 32,263
+// partial rows of 520 bytes (128 floats of O plus m and l).
 constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;  // 16 MiB per device
 
 // The partials' storage. Host code may not use this name as an address (on
@@ -1001,23 +1050,33 @@ pda_status noalloc_setup(int dev, int bs, NoAllocDevice* out) {
       const size_t sb = ring_shape(b).smem_bytes;
       mx = sb > mx ? sb : mx;
     }
-    if (cudaFuncSetAttribute(pda::pda_split_decode_kernel<false, false, pda::kWideCtasPerSm>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx) != cudaSuccess)
-      return PDA_ERR_CUDA;
+    for (bool paired : {false, true})
+      if (cudaFuncSetAttribute(split_fn(kPlainWide, paired), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx) !=
+          cudaSuccess)
+        return PDA_ERR_CUDA;
     d.scratch = ptr;
     d.sm_count = sms;
     d.ready = true;
   }
   int& occ = d.occ[bs / 16];
   if (occ == 0) {
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pda::pda_split_decode_kernel<false, false, pda::kWideCtasPerSm>,
-                                                      pda::kThreads, ring_shape(bs).smem_bytes) != cudaSuccess)
-      return PDA_ERR_CUDA;
-    occ = n > 0 ? n : 1;
+    int m = 0;
+    for (bool paired : {false, true}) {
+      int n = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, split_fn(kPlainWide, paired), pda::kThreads,
+                                                        ring_shape(bs).smem_bytes) != cudaSuccess)
+        return PDA_ERR_CUDA;
+      m = (m == 0 || n < m) ? n : m;
+    }
+    occ = m > 0 ? m : 1;
   }
   *out = d;
   return PDA_OK;
+}
+
+void noalloc_forget_devices() {
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  for (auto& d : g_noalloc_dev) d = NoAllocDevice{};
 }
 
 }  // namespace
@@ -1067,8 +1126,15 @@ extern "C" pda_status pda_decode_noalloc(void* out, const void* q, const void* k
   p.logit_scale_log2 = (float)((double)scale * (double)k_scale * 1.4426950408889634);
   p.v_scale = v_scale;
   dim3 grid((unsigned)nsplit, (unsigned)num_kv_heads, (unsigned)num_seqs);
-  pda::pda_split_decode_kernel<false, false, pda::kWideCtasPerSm><<<grid, pda::kThreads, rs.smem_bytes, stream>>>(p, g_no_map, g_no_map);
-  if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
+  {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = grid;
+    lc.blockDim = dim3(pda::kThreads);
+    lc.dynamicSmemBytes = rs.smem_bytes;
+    lc.stream = stream;
+    if (cudaLaunchKernelEx(&lc, split_fn(kPlainWide, paired_for(p.gqa)), p, g_no_map, g_no_map) != cudaSuccess)
+      return PDA_ERR_CUDA;
+  }
   if (nsplit > 1) {
     pda::MergeParams mp;
     mp.out = p.out;
@@ -1080,8 +1146,8 @@ extern "C" pda_status pda_decode_noalloc(void* out, const void* q, const void* k
     mp.max_blocks = max_num_blocks_per_seq;
     mp.nsplit = nsplit;
     mp.v_scale = v_scale;
-    pda::pda_merge_kernel<<<dim3((unsigned)num_heads, (unsigned)num_seqs), kHeadDim, 0, stream>>>(mp);
-    if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
+    mp.num_seqs = num_seqs;
+    if (launch_merge(mp, stream, false) != cudaSuccess) return PDA_ERR_CUDA;
   }
   return PDA_OK;
 }

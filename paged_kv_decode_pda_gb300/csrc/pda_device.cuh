@@ -230,4 +230,13 @@ __device__ __forceinline__ uint2 ld_nc_v2(const void* p) {
 __device__ __forceinline__ float bf16lo_f32(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16hi_f32(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
 
+// f16 pair (x = lo | hi << 16) -> fp32 pair, exact.
+__device__ __forceinline__ float f16lo_f32(uint32_t x) {
+  return __half2float(__ushort_as_half((unsigned short)(x & 0xFFFFu)));
+}
+__device__ __forceinline__ float f16hi_f32(uint32_t x) { return __half2float(__ushort_as_half((unsigned short)(x >> 16))); }
+
+// 2^n as a normal binary32 value, n in [-126, 127] (built from its exponent bits).
+__device__ __forceinline__ float exp2_int(int n) { return __uint_as_float((uint32_t)(n + 127) << 23); }
+
 }  // namespace pda

@@ -107,6 +107,44 @@ struct DecodeParams {
   uint32_t block_limit = 0u;
 };
 
+// Splits of a sequence with `pages` pages that hold at least one page (the
+// others are empty: they write no partial and take no part in the merge).
+__device__ __forceinline__ int active_splits(int pages, int nsplit) {
+  if (pages <= 0) return 0;
+  const int per = (pages + nsplit - 1) / nsplit;
+  return (pages + per - 1) / per;
+}
+
+// One log-sum-exp step: the running (M, den, acc) of 4 dims absorbs a split's
+// (m, l, O). The products and sums are spelled out (no contraction choice
+// left to the compiler), so every merge site gives the same bits.
+__device__ __forceinline__ void lse_fold(float& M, float& den, float4& acc, float m, float l, const float4& o) {
+  const float mn = fmaxf(M, m);
+  const float a = fast_exp2(M - mn);  // 0 while M is -inf
+  const float f = fast_exp2(m - mn);
+  acc.x = __fmaf_rn(acc.x, a, __fmul_rn(f, o.x));
+  acc.y = __fmaf_rn(acc.y, a, __fmul_rn(f, o.y));
+  acc.z = __fmaf_rn(acc.z, a, __fmul_rn(f, o.z));
+  acc.w = __fmaf_rn(acc.w, a, __fmul_rn(f, o.w));
+  den = __fmaf_rn(den, a, __fmul_rn(f, l));
+  M = mn;
+}
+
+// The partials of one (sequence, head) row folded in split order, dims
+// 4 lane .. 4 lane + 3 (one warp per row). Row prow0 + i holds split i.
+__device__ __forceinline__ void lse_fold_row(const float* part_o, const float* part_ml, size_t prow0, int active,
+                                             int lane, float& M, float& den, float4& acc) {
+  M = -INFINITY;
+  den = 0.f;
+  acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int i = 0; i < active; ++i) {
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(part_ml) + (prow0 + i));
+    const float4 o = __ldcg(reinterpret_cast<const float4*>(part_o + (prow0 + i) * kHeadDim) + lane);
+    lse_fold(M, den, acc, ml.x, ml.y, o);
+  }
+}
+
 // A block id the producer is about to read, checked when the block check is on.
 __device__ __forceinline__ int checked_block(int b, uint32_t limit) {
   if (limit != 0u && (uint32_t)b >= limit) {
@@ -177,15 +215,26 @@ __device__ __forceinline__ float warp_sum_over_gid(float v) {
 // One consumer warp's share of a work unit: the GQA group's Q^T fragments
 // and the running softmax state (m, l, O^T) of the unit, updated one
 // 16-token tile at a time (the template flags are those of the kernels).
-template <bool kSlotScales, bool kTokenMajor>
+template <bool kSlotScales, bool kTokenMajor, bool kPaired, bool kLateRemainder = false>
 struct TileWorker {
   int gid, tig;
   uint32_t k_lane_off;   // page-major K: ldmatrix row of this lane
   uint32_t tm_row, tm_xor, tm_hi;  // token-major tiles: row, swizzle and chunk half
   uint32_t v_row, v_lane_off;
   bool low_quad;
-  int tokA, tokB;        // tokens of accumulator rows gid and gid + 8
+  // Paired columns (kPaired, for GQA groups of at most 4 heads): MMA
+  // columns 4..7 repeat heads 0..3, so the lanes that own them (tig >= 2)
+  // compute the same scores, maxima and probabilities as their partners
+  // (lane ^ 2) and feed the PV product the f16 remainder P - f16(P) instead
+  // of f16(P); the two halves of O are added when the warp stores its merge
+  // rows. Wider groups run a second PV MMA on the remainders. The choice is
+  // a template parameter so that each kernel instance holds only its own
+  // PV code (the other path's registers and branches cost the tile loop
+  // time even when not taken).
+  static constexpr bool paired = kPaired;
+  bool hi_lane;          // tig < 2: this lane's P columns carry f16(P)
   uint32_t qf[kChunks][2];
+  float lsc0, lsc1;      // logit scale (log2 units) of columns 2tig, 2tig+1, with the query rows' shifts
   float m0, m1;          // running max (log2 units), heads 2tig, 2tig+1
   float l0, l1;          // running partial sums over this lane's tokens
   float o[kChunks][4];   // O^T: m-tile mt = dims 16mt.. ; cols heads 2tig, 2tig+1
@@ -207,9 +256,13 @@ struct TileWorker {
     v_row = v_shuffled ? 16u : (uint32_t)bs;
     v_lane_off = (uint32_t)lane * v_row;
     low_quad = kTokenMajor ? true : tig < 2;
-    tokA = kTokenMajor ? gid : row_token(gid);
-    tokB = kTokenMajor ? gid + 8 : row_token(gid + 8);
+    hi_lane = tig < 2;
   }
+
+  // Tokens of accumulator rows gid and gid + 8 (computed where needed, not
+  // held in registers through the tile loop).
+  __device__ __forceinline__ int tok_a() const { return kTokenMajor ? gid : row_token(gid); }
+  __device__ __forceinline__ int tok_b() const { return kTokenMajor ? gid + 8 : row_token(gid + 8); }
 
   __device__ __forceinline__ void reset() {
     m0 = m1 = -INFINITY;
@@ -218,29 +271,64 @@ struct TileWorker {
     for (int i = 0; i < kChunks; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   }
 
+  // The query head whose row MMA column `gid` holds: gid itself, or in
+  // paired mode gid mod 4 (columns 4..7 repeat heads 0..3).
+  __device__ __forceinline__ int q_head() const { return paired ? (gid & 3) : gid; }
+
   // Q^T fragments (B operand, 16 dims x 8 heads per chunk) in f16 from the
-  // bf16 query row of head `gid` (zeros when gid is past the group). Chunk c
-  // k-slots (2tig, 2tig+1) <- dims 16c+4tig+{0,1}; (2tig+8, 2tig+9) <- dims
-  // 16c+4tig+{2,3}; this matches how K bytes land in the A fragments below.
-  __device__ __forceinline__ void set_q_chunk(int c, uint2 v) {
-    qf[c][0] = pack_f16x2(bf16lo_f32(v.x), bf16hi_f32(v.x));
-    qf[c][1] = pack_f16x2(bf16lo_f32(v.y), bf16hi_f32(v.y));
-  }
-  __device__ __forceinline__ void load_q_global(const __nv_bfloat16* qrow, bool live) {
+  // bf16 query row of head q_head() (zeros when that head is past the
+  // group). Chunk c k-slots (2tig, 2tig+1) <- dims 16c+4tig+{0,1};
+  // (2tig+8, 2tig+9) <- dims 16c+4tig+{2,3}; this matches how K bytes land
+  // in the A fragments below.
+  //
+  // bf16 reaches 2^127 and f16 only 65504, so each row is first scaled by a
+  // power of two 2^-e that puts its largest |q| in [2^14, 2^15): every bf16
+  // value of the row down to 2^-24 of that maximum is then exact in f16
+  // (smaller ones cannot move a logit by more than 2^-24 of the row's
+  // largest term). The columns' logit scales are multiplied by 2^e, so the
+  // logits are the unshifted ones (both factors are exact powers of two).
+  // `lsc` is scale * k_scale * log2(e) (scale * log2(e) with slot scales).
+  // ld(c) returns the 4 bf16 values of chunk c this lane holds; it is
+  // called twice per chunk (max pass, convert pass), so that the raw row is
+  // never held in registers at once.
+  template <class Ld>
+  __device__ __forceinline__ void set_q(const Ld& ld, float lsc) {
+    uint32_t mx = 0u;
 #pragma unroll
-    for (int c = 0; c < kChunks; ++c) set_q_chunk(c, live ? ld_nc_v2(qrow + 16 * c + 4 * tig) : make_uint2(0u, 0u));
-  }
-  __device__ __forceinline__ void load_q_shared(uint32_t qrow, bool live) {
+    for (int c = 0; c < kChunks; ++c) {
+      const uint2 v = ld(c);
+      mx = __vmaxu2(mx, v.x & 0x7FFF7FFFu);
+      mx = __vmaxu2(mx, v.y & 0x7FFF7FFFu);
+    }
+    mx = max(mx & 0xFFFFu, mx >> 16);  // |q| bits order like |q| (finite q)
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));  // over the row's four lanes
+    const int e = mx == 0u ? 0 : min(max((int)(mx >> 7) - 127 - 14, -100), 113);
+    const float down = exp2_int(-e);
 #pragma unroll
-    for (int c = 0; c < kChunks; ++c)
-      set_q_chunk(c, live ? ld_shared_v2(qrow + (uint32_t)(16 * c + 4 * tig) * 2u) : make_uint2(0u, 0u));
+    for (int c = 0; c < kChunks; ++c) {
+      const uint2 v = ld(c);
+      qf[c][0] = pack_f16x2(bf16lo_f32(v.x) * down, bf16hi_f32(v.x) * down);
+      qf[c][1] = pack_f16x2(bf16lo_f32(v.y) * down, bf16hi_f32(v.y) * down);
+    }
+    // column 2tig's row sits in lanes 8tig..8tig+3, column 2tig+1's in 8tig+4..
+    lsc0 = lsc * exp2_int(__shfl_sync(0xffffffffu, e, 8 * tig));
+    lsc1 = lsc * exp2_int(__shfl_sync(0xffffffffu, e, 8 * tig + 4));
+  }
+  __device__ __forceinline__ void load_q_global(const __nv_bfloat16* qrow, bool live, float lsc) {
+    const int t4 = 4 * tig;
+    set_q([&](int c) { return live ? ld_nc_v2(qrow + 16 * c + t4) : make_uint2(0u, 0u); }, lsc);
+  }
+  __device__ __forceinline__ void load_q_shared(uint32_t qrow, bool live, float lsc) {
+    const uint32_t t8 = (uint32_t)(8 * tig);
+    set_q([&](int c) { return live ? ld_shared_v2(qrow + (uint32_t)(32 * c) + t8) : make_uint2(0u, 0u); }, lsc);
   }
 
   // One 16-token tile: K bytes at kbase, V bytes at vbase (shared), the first
   // n_valid (>= 1) tokens real. Slot scales: ks / vs point at the tile's 16
   // K and V scales, vinv is 1 / (the reference V scale).
-  __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int bs, int n_valid, float lsc,
-                                       const float* ks, const float* vs, float vinv) {
+  __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int bs, int n_valid, const float* ks,
+                                       const float* vs, float vinv) {
     // ---- S^T = K_tile * Q^T (two independent accumulator chains)
     float sc[4] = {0.f, 0.f, 0.f, 0.f};
     float sd[4] = {0.f, 0.f, 0.f, 0.f};
@@ -260,20 +348,28 @@ struct TileWorker {
     for (int i = 0; i < 4; ++i) sc[i] += sd[i];
 
     // ---- online softmax (exp2 domain); tokens >= n_valid are masked
-    const bool vA = tokA < n_valid;
-    const bool vB = tokB < n_valid;
-    float lscA = lsc, lscB = lsc, vsA = 1.f, vsB = 1.f;
+    float lA0 = lsc0, lA1 = lsc1, lB0 = lsc0, lB1 = lsc1, vsA = 1.f, vsB = 1.f;
     if constexpr (kSlotScales) {
       // Scales of slots past the length may hold anything (even NaN).
-      lscA *= vA ? ks[tokA] : 0.f;
-      lscB *= vB ? ks[tokB] : 0.f;
-      vsA = vA ? vs[tokA] * vinv : 0.f;
-      vsB = vB ? vs[tokB] * vinv : 0.f;
+      const int tA = tok_a(), tB = tok_b();
+      const bool vA = tA < n_valid, vB = tB < n_valid;
+      const float kA = vA ? ks[tA] : 0.f;
+      const float kB = vB ? ks[tB] : 0.f;
+      lA0 *= kA;
+      lA1 *= kA;
+      lB0 *= kB;
+      lB1 *= kB;
+      vsA = vA ? vs[tA] * vinv : 0.f;
+      vsB = vB ? vs[tB] * vinv : 0.f;
     }
-    const float s0 = vA ? sc[0] * lscA : -INFINITY;
-    const float s1 = vA ? sc[1] * lscA : -INFINITY;
-    const float s2 = vB ? sc[2] * lscB : -INFINITY;
-    const float s3 = vB ? sc[3] * lscB : -INFINITY;
+    float s0 = sc[0] * lA0;
+    float s1 = sc[1] * lA1;
+    float s2 = sc[2] * lB0;
+    float s3 = sc[3] * lB1;
+    if (n_valid < 16) {  // a tail tile (warp-uniform): its last slots are not tokens
+      if (tok_a() >= n_valid) s0 = s1 = -INFINITY;
+      if (tok_b() >= n_valid) s2 = s3 = -INFINITY;
+    }
     const float mx0 = warp_max_over_gid(fmaxf(s0, s2));
     const float mx1 = warp_max_over_gid(fmaxf(s1, s3));
     const float mn0 = fmaxf(m0, mx0);
@@ -297,19 +393,28 @@ struct TileWorker {
         o[mt][3] *= c1;
       }
     }
+    // P in two f16 parts, f16(P) and f16(P - f16(P)) (the difference is
+    // exact in fp32): together they carry P to about 2^-22 relative (2^-25
+    // absolute below 2^-3), where f16(P) alone would lose 2^-12.
+    float a0 = p0, a1 = p1, a2 = p2, a3 = p3;
+    if constexpr (kSlotScales) {
+      a0 *= vsA;
+      a1 *= vsA;
+      a2 *= vsB;
+      a3 *= vsB;
+    }
+    const uint32_t h0 = pack_f16x2(a0, a1);
+    const uint32_t h1 = pack_f16x2(a2, a3);
+    const uint32_t r0 = pack_f16x2(a0 - f16lo_f32(h0), a1 - f16hi_f32(h0));
+    const uint32_t r1 = pack_f16x2(a2 - f16lo_f32(h1), a3 - f16hi_f32(h1));
     // P^T fragment: transpose (token rows x head cols) to (head rows x token
     // cols). Lane quads 2 and 3 hold their two token pairs in the other
-    // order (row_token), so they swap the two halves of the B fragment.
-    uint32_t x0, x1;
-    if constexpr (kSlotScales) {
-      x0 = pack_f16x2(p0 * vsA, p1 * vsA);
-      x1 = pack_f16x2(p2 * vsB, p3 * vsB);
-    } else {
-      x0 = pack_f16x2(p0, p1);
-      x1 = pack_f16x2(p2, p3);
-    }
-    const uint32_t t0 = movmatrix_trans(x0);
-    const uint32_t t1 = movmatrix_trans(x1);
+    // order (row_token), so they swap the two halves of the B fragment. In
+    // paired mode the remainder columns ride in the same fragment; otherwise
+    // the remainders get a fragment of their own (pl0, pl1).
+    const bool take_hi = !paired || hi_lane;
+    const uint32_t t0 = movmatrix_trans(take_hi ? h0 : r0);
+    const uint32_t t1 = movmatrix_trans(take_hi ? h1 : r1);
     const uint32_t pb0 = low_quad ? t0 : t1;
     const uint32_t pb1 = low_quad ? t1 : t0;
 
@@ -349,42 +454,97 @@ struct TileWorker {
           for (int i = 0; i < 4; ++i) vr[mp][i] &= vmask;
       }
     }
+    // Each instance has one straight block of conversions and MMAs, which the
+    // compiler can interleave freely.
+    if constexpr (kPaired) {
+      pv_mma(vr, pb0, pb1, pb0, pb1, false);
+    } else {
+      const uint32_t u0 = movmatrix_trans(r0);
+      const uint32_t u1 = movmatrix_trans(r1);
+      pv_mma(vr, pb0, pb1, low_quad ? u0 : u1, low_quad ? u1 : u0, true);
+    }
+  }
+
+  // V_tile^T A fragments of m-tile pair mp, half h (16 dims x 16 tokens, f16).
+  __device__ __forceinline__ void v_frag(const uint32_t (&vr)[kChunks / 2][4], int mp, int h, uint32_t (&a)[4]) {
+    if constexpr (kTokenMajor) {
+      // bytes (t,d0) (t,d1) (t',d0) (t',d1) -> (t,d0) (t',d0) | (t,d1) (t',d1)
+      const uint32_t ya = __byte_perm(vr[mp][2 * h], 0, 0x3120);
+      const uint32_t yb = __byte_perm(vr[mp][2 * h + 1], 0, 0x3120);
+      a[0] = e4m3x2_lo_to_f16x2(ya);
+      a[1] = e4m3x2_hi_to_f16x2(ya);
+      a[2] = e4m3x2_lo_to_f16x2(yb);
+      a[3] = e4m3x2_hi_to_f16x2(yb);
+    } else {
+      a[0] = e4m3x2_lo_to_f16x2(vr[mp][2 * h]);
+      a[1] = e4m3x2_lo_to_f16x2(vr[mp][2 * h + 1]);
+      a[2] = e4m3x2_hi_to_f16x2(vr[mp][2 * h]);
+      a[3] = e4m3x2_hi_to_f16x2(vr[mp][2 * h + 1]);
+    }
+  }
+
+  // O^T += V_tile^T * P^T for the 8 m-tiles of 16 dims: B fragment (pb0,
+  // pb1), and with `second` a second B fragment (pl0, pl1). With
+  // kLateRemainder the second pass follows all first-pass MMAs (the V
+  // fragments are converted again), so no MMA waits on its accumulator's
+  // previous one; without it each second MMA reuses the converted
+  // fragments right away (fewer registers, for the 4-CTA instances).
+  __device__ __forceinline__ void pv_mma(const uint32_t (&vr)[kChunks / 2][4], uint32_t pb0, uint32_t pb1,
+                                         uint32_t pl0, uint32_t pl1, bool second) {
 #pragma unroll
     for (int mp = 0; mp < kChunks / 2; ++mp) {
-      if constexpr (kTokenMajor) {
-        // bytes (t,d0) (t,d1) (t',d0) (t',d1) -> (t,d0) (t',d0) | (t,d1) (t',d1)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t a[4];
+        v_frag(vr, mp, h, a);
+        mma_f16(o[2 * mp + h], a[0], a[1], a[2], a[3], pb0, pb1);
+        if (second && !kLateRemainder) mma_f16(o[2 * mp + h], a[0], a[1], a[2], a[3], pl0, pl1);
+      }
+    }
+    if (second && kLateRemainder) {
+#pragma unroll
+      for (int mp = 0; mp < kChunks / 2; ++mp) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const uint32_t ya = __byte_perm(vr[mp][2 * h], 0, 0x3120);
-          const uint32_t yb = __byte_perm(vr[mp][2 * h + 1], 0, 0x3120);
-          mma_f16(o[2 * mp + h], e4m3x2_lo_to_f16x2(ya), e4m3x2_hi_to_f16x2(ya), e4m3x2_lo_to_f16x2(yb),
-                  e4m3x2_hi_to_f16x2(yb), pb0, pb1);
+          uint32_t a[4];
+          v_frag(vr, mp, h, a);
+          mma_f16(o[2 * mp + h], a[0], a[1], a[2], a[3], pl0, pl1);
         }
-      } else {
-        mma_f16(o[2 * mp], e4m3x2_lo_to_f16x2(vr[mp][0]), e4m3x2_lo_to_f16x2(vr[mp][1]),
-                e4m3x2_hi_to_f16x2(vr[mp][0]), e4m3x2_hi_to_f16x2(vr[mp][1]), pb0, pb1);
-        mma_f16(o[2 * mp + 1], e4m3x2_lo_to_f16x2(vr[mp][2]), e4m3x2_lo_to_f16x2(vr[mp][3]),
-                e4m3x2_hi_to_f16x2(vr[mp][2]), e4m3x2_hi_to_f16x2(vr[mp][3]), pb0, pb1);
       }
     }
   }
 
-  // This warp's (m, l, O) into the CTA merge area: mo [w][head][kStride],
-  // mml [w][head][2].
+  // Merge rows a warp stores: the group's heads. Paired instances keep only
+  // heads 0..3 (columns 4..7 are their remainders, folded in below), so
+  // their rows fit the padded stride even where the merge area is one ring
+  // stage of 16 KiB.
+  static constexpr int kMergeRows = kPaired ? kMaxGqa / 2 : kMaxGqa;
+
+  // This warp's (m, l, O) into the CTA merge area: mo [w][kMergeRows][kStride],
+  // mml [w][kMaxGqa][2].
   template <int kStride>
   __device__ __forceinline__ void store_merge(float* mo, float* mml, int warp) {
     l0 = warp_sum_over_gid(l0);
     l1 = warp_sum_over_gid(l1);
-    float* mw = mo + warp * kMaxGqa * kStride;
+    if constexpr (kPaired) {
+      // f16(P) . V (columns 0..3) + remainder . V (columns 4..7)
 #pragma unroll
-    for (int mt = 0; mt < kChunks; ++mt) {
-      // accumulator rows gid / gid + 8 of m-tile mt hold these two dims
-      const int d0 = kTokenMajor ? 16 * mt + 2 * gid : 16 * mt + gid;
-      const int d1 = kTokenMajor ? d0 + 1 : d0 + 8;
-      mw[(2 * tig) * kStride + d0] = o[mt][0];
-      mw[(2 * tig + 1) * kStride + d0] = o[mt][1];
-      mw[(2 * tig) * kStride + d1] = o[mt][2];
-      mw[(2 * tig + 1) * kStride + d1] = o[mt][3];
+      for (int mt = 0; mt < kChunks; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[mt][i] += __shfl_xor_sync(0xffffffffu, o[mt][i], 2);
+    }
+    if (!kPaired || hi_lane) {
+      float* mw = mo + warp * kMergeRows * kStride;
+#pragma unroll
+      for (int mt = 0; mt < kChunks; ++mt) {
+        // accumulator rows gid / gid + 8 of m-tile mt hold these two dims
+        const int d0 = kTokenMajor ? 16 * mt + 2 * gid : 16 * mt + gid;
+        const int d1 = kTokenMajor ? d0 + 1 : d0 + 8;
+        mw[(2 * tig) * kStride + d0] = o[mt][0];
+        mw[(2 * tig + 1) * kStride + d0] = o[mt][1];
+        mw[(2 * tig) * kStride + d1] = o[mt][2];
+        mw[(2 * tig + 1) * kStride + d1] = o[mt][3];
+      }
     }
     if (gid == 0) {
       float* ml = mml + warp * kMaxGqa * 2;
@@ -401,7 +561,7 @@ struct TileWorker {
 // partial (several splits). Consumer thread `tid` of kConsumerThreads.
 // vref: the slot-scale variant's reference V scale (1 otherwise). kStride:
 // the fp32 row stride of mo.
-template <bool kSlotScales, int kStride>
+template <bool kSlotScales, int kStride, int kRows>
 __device__ __forceinline__ void reduce_store(const DecodeParams& p, const float* mo, const float* mml, int tid, int s,
                                              int kvh, int split, float vref) {
   const int g = p.gqa;
@@ -418,7 +578,7 @@ __device__ __forceinline__ void reduce_store(const DecodeParams& p, const float*
       for (int w = 0; w < kConsumerWarps; ++w) {
         const float mw = mml[(w * kMaxGqa + hh) * 2];
         const float f = fast_exp2(mw - M);
-        acc += f * mo[(w * kMaxGqa + hh) * kStride + d];
+        acc += f * mo[(w * kRows + hh) * kStride + d];
         den += f * mml[(w * kMaxGqa + hh) * 2 + 1];
       }
     }
@@ -455,7 +615,7 @@ __device__ __forceinline__ void reduce_store(const DecodeParams& p, const float*
 // 2 tokens x 2 dims per register, split into an even-dim and an odd-dim
 // fragment row by one byte permute. Output row gid of m-tile mt is then dim
 // 16mt + 2gid and row gid + 8 is dim 16mt + 2gid + 1.
-template <bool kSlotScales, bool kTokenMajor, int kMinCtasPerSm>
+template <bool kSlotScales, bool kTokenMajor, int kMinCtasPerSm, bool kPaired>
 __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
     pda_split_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v) {
@@ -610,15 +770,16 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
   }
 
   // -------------------------------------------------------------- consumers
-  TileWorker<kSlotScales, kTokenMajor> w;
+  TileWorker<kSlotScales, kTokenMajor, kPaired, (kMinCtasPerSm < 4)> w;
   w.setup(lane, bs, p.v_shuffled);
   {
-    const bool live = w.gid < g;
-    w.load_q_global(p.q + ((size_t)s * H + (size_t)kvh * g + (live ? w.gid : 0)) * kHeadDim, live);
+    const int qh = w.q_head();
+    const bool live = qh < g;
+    w.load_q_global(p.q + ((size_t)s * H + (size_t)kvh * g + (live ? qh : 0)) * kHeadDim, live,
+                    p.logit_scale_log2);
   }
   w.reset();
 
-  const float lsc = p.logit_scale_log2;
   const int tiles_per_page = bs / 16;
   const uint32_t v_sub = p.v_shuffled ? (uint32_t)(kHeadDim * 16) : 16u;
   // Slot-scale variant: V scales enter P relative to vref (the split's first
@@ -661,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
                                          : sbase + (uint32_t)pg * page_bytes + (uint32_t)(sub * 256);
       const uint32_t vbase = kTokenMajor ? sbase + (uint32_t)(PPS + pg) * page_bytes + (uint32_t)sub * 2048u
                                          : sbase + (uint32_t)(PPS + pg) * page_bytes + (uint32_t)sub * v_sub;
-      w.tile(kbase, vbase, bs, L - tok0, lsc, srow + pg * bs + sub * 16, srow + (PPS + pg) * bs + sub * 16, vinv);
+      w.tile(kbase, vbase, bs, L - tok0, srow + pg * bs + sub * 16, srow + (PPS + pg) * bs + sub * 16, vinv);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8u * stage);
@@ -672,11 +833,12 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
   // barrier; the abort decision is the same for all of them.
   if (named_barrier_or(1, kConsumerThreads, *abort_flag)) return;
 
-  float* mo = reinterpret_cast<float*>(smem);                       // [w][head][kMergeStride]
+  using Worker = decltype(w);
+  float* mo = reinterpret_cast<float*>(smem);                       // [w][row][kMergeStride]
   float* mml = mo + kConsumerWarps * kMaxGqa * kMergeStride;        // [w][head][2]
   w.template store_merge<kMergeStride>(mo, mml, warp);
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
-  reduce_store<kSlotScales, kMergeStride>(p, mo, mml, threadIdx.x, s, kvh, split, vref);
+  reduce_store<kSlotScales, kMergeStride, Worker::kMergeRows>(p, mo, mml, threadIdx.x, s, kvh, split, vref);
 }
 
 // --------------------------------------------------------------------------
@@ -722,8 +884,13 @@ constexpr uint32_t kAuxQ = 0;                                     // query rows,
 constexpr uint32_t kAuxMl = kMaxGqa * kHeadDim * 2;              // merge (m, l) [w][head][2]
 constexpr uint32_t kAuxHdr = kAuxMl + kConsumerWarps * kMaxGqa * 2 * 4;  // StageHeader
 constexpr uint32_t kAuxBytes = kAuxHdr + sizeof(StageHeader);
-constexpr int kPersistMergeStride = kHeadDim;                     // O rows fill 16 KiB exactly
-constexpr uint32_t kPersistMergeBytes = kConsumerWarps * kMaxGqa * kPersistMergeStride * 4;
+// Merge rows in a persistent stage: 8 rows per warp at the unpadded stride
+// fill 16 KiB exactly; paired instances store 4 rows per warp at the padded
+// stride (bank-conflict free).
+template <bool kPaired>
+__host__ __device__ constexpr int persist_merge_stride() { return kPaired ? kMergeStride : kHeadDim; }
+constexpr uint32_t kPersistMergeBytes = kConsumerWarps * kMaxGqa * kHeadDim * 4;
+static_assert(kConsumerWarps * (kMaxGqa / 2) * kMergeStride * 4 <= kPersistMergeBytes, "paired rows fit the stage");
 static_assert(kAuxBytes % 16 == 0, "side entries keep 16-byte alignment");
 
 // Bounded barrier of the consumer warps on an mbarrier (count kConsumerWarps):
@@ -741,7 +908,7 @@ __device__ __forceinline__ bool consumer_sync(uint32_t bar, uint32_t& phase, int
   return ok;
 }
 
-template <bool kTokenMajor, int kMinCtasPerSm>
+template <bool kTokenMajor, int kMinCtasPerSm, bool kPaired>
 __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
     pda_persistent_decode_kernel(const DecodeParams p, unsigned* queue, int num_units,
                                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
@@ -934,10 +1101,9 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
   }
 
   // -------------------------------------------------------------- consumers
-  TileWorker<false, kTokenMajor> w;
+  TileWorker<false, kTokenMajor, kPaired, true> w;
   w.setup(lane, bs, p.v_shuffled);
   w.reset();
-  const float lsc = p.logit_scale_log2;
   const int tiles_per_page = bs / 16;
   const uint32_t v_sub = p.v_shuffled ? (uint32_t)(kHeadDim * 16) : 16u;
   uint32_t cons_phase = 0;
@@ -959,9 +1125,10 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
     if (hd.flags & kHdrFirst) {
       w.reset();
       if (hd.np > 0) {
-        const bool live = w.gid < g;
-        w.load_q_shared(aux_u32 + (uint32_t)stage * kAuxBytes + kAuxQ + (uint32_t)(live ? w.gid : 0) * (kHeadDim * 2),
-                        live);
+        const int qh = w.q_head();
+        const bool live = qh < g;
+        w.load_q_shared(aux_u32 + (uint32_t)stage * kAuxBytes + kAuxQ + (uint32_t)(live ? qh : 0) * (kHeadDim * 2),
+                        live, p.logit_scale_log2);
       }
     }
     const int n_tiles = hd.np * tiles_per_page;
@@ -974,7 +1141,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
                                          : sbase + (uint32_t)pg * page_bytes + (uint32_t)(sub * 256);
       const uint32_t vbase = kTokenMajor ? sbase + (uint32_t)(PPS + pg) * page_bytes + (uint32_t)sub * 2048u
                                          : sbase + (uint32_t)(PPS + pg) * page_bytes + (uint32_t)sub * v_sub;
-      w.tile(kbase, vbase, bs, hd.L - tok0, lsc, nullptr, nullptr, 1.f);
+      w.tile(kbase, vbase, bs, hd.L - tok0, nullptr, nullptr, 1.f);
     }
     if (hd.flags & kHdrLast) {
       // Every consumer warp is done with this stage's pages: its memory
@@ -982,9 +1149,10 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
       if (!consumer_sync(cons_bar, cons_phase, lane, abort_flag)) break;
       float* mo = reinterpret_cast<float*>(ring + (size_t)stage * p.stage_bytes);
       float* mml = reinterpret_cast<float*>(aux + (size_t)stage * kAuxBytes + kAuxMl);
-      w.template store_merge<kPersistMergeStride>(mo, mml, warp);
+      constexpr int kStride = persist_merge_stride<kPaired>();
+      w.template store_merge<kStride>(mo, mml, warp);
       if (!consumer_sync(cons_bar, cons_phase, lane, abort_flag)) break;
-      reduce_store<false, kPersistMergeStride>(p, mo, mml, threadIdx.x, hd.s, hd.kvh, hd.split, 1.f);
+      reduce_store<false, kStride, decltype(w)::kMergeRows>(p, mo, mml, threadIdx.x, hd.s, hd.kvh, hd.split, 1.f);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8u * stage);
@@ -1077,18 +1245,29 @@ __global__ void __launch_bounds__(kOrderThreads) pda_order_units_kernel(const Or
     p.order[atomicAdd(&count[order_key(p, u)], 1u)] = u;
 }
 
-// Log-sum-exp merge of the per-split partials of one (sequence, head) per
-// 128-thread block (each warp folds every fourth split for all 128 dims,
-// four per lane, then warp 0 combines the four warps' results):
+// Log-sum-exp merge of the per-split partials:
 //   M = max_i m_i,  out = v_scale * sum_i 2^(m_i - M) O_i / sum_i 2^(m_i - M) l_i
 // with a sink logit, if any, added to the denominator (finish()).
 // Splits with no pages were never written and are skipped by the same page
 // rule the decode kernel uses; a zero-length sequence gets zeros.
+//
+// pda_merge_kernel: one warp per (sequence, head) row, 4 rows per 128-thread
+// block; each lane folds the splits in order for 4 dims (lse_fold_row). Used
+// up to kMergeRowSplits splits: a quarter of the blocks of one block per row
+// (a batch of 128 x 64 rows at 2 splits went from 3.4 waves of short blocks
+// to less than one).
+// pda_merge_wide_kernel: one 128-thread block per row for more splits (a
+// few very long sequences): warp w folds splits w, w + 4, ... and warp 0
+// combines the four.
+constexpr int kMergeRowSplits = 16;
+constexpr int kMergeRowsPerBlock = kHeadDim / 32;
+
 struct MergeParams {
   void* out;
   const float* part_o;
   const float* part_ml;
   const int32_t* seq_lens;
+  int num_seqs;
   int num_heads;
   int block_size;
   int max_blocks;
@@ -1099,7 +1278,36 @@ struct MergeParams {
   float out_scale = 1.f;
 };
 
+// Store the merged row: lane's 4 dims of row (s, h).
+__device__ __forceinline__ void merge_store(const MergeParams& p, int s, int h, int lane, bool any, float M, float den,
+                                            const float4& acc) {
+  const float zs = p.sinks ? __ldg(p.sinks + h) * 1.4426950408889634f : -INFINITY;
+  const float r[4] = {acc.x, acc.y, acc.z, acc.w};
+  const size_t o0 = ((size_t)s * p.num_heads + h) * kHeadDim + 4 * lane;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    store_out(p.out, o0 + j, any ? finish(r[j], den, M, zs, p.v_scale) : 0.f, p.out_fp8, p.out_scale);
+}
+
 __global__ void __launch_bounds__(kHeadDim) pda_merge_kernel(const MergeParams p) {
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * kMergeRowsPerBlock + (threadIdx.x >> 5);
+  if (row >= (long long)p.num_seqs * p.num_heads) return;
+  const int s = (int)(row / p.num_heads);
+  const int h = (int)(row % p.num_heads);
+  int L = __ldg(p.seq_lens + s);
+  L = max(0, min(L, p.max_blocks * p.block_size));
+  const int active = active_splits((L + p.block_size - 1) / p.block_size, p.nsplit);
+  // Launched as the decode kernel's programmatic dependent: wait until it
+  // has finished and its partials are visible (a no-op otherwise).
+  grid_dependency_wait();
+  float M, den;
+  float4 acc;
+  lse_fold_row(p.part_o, p.part_ml, (size_t)row * p.nsplit, active, lane, M, den, acc);
+  merge_store(p, s, h, lane, active > 0, M, den, acc);
+}
+
+__global__ void __launch_bounds__(kHeadDim) pda_merge_wide_kernel(const MergeParams p) {
   constexpr int kWarps = kHeadDim / 32;
   const int h = blockIdx.x;
   const int s = blockIdx.y;
@@ -1107,15 +1315,8 @@ __global__ void __launch_bounds__(kHeadDim) pda_merge_kernel(const MergeParams p
   const int lane = threadIdx.x & 31;
   int L = __ldg(p.seq_lens + s);
   L = max(0, min(L, p.max_blocks * p.block_size));
-  const int pages = (L + p.block_size - 1) / p.block_size;
-  int active = 0;
-  if (pages > 0) {
-    const int per = (pages + p.nsplit - 1) / p.nsplit;
-    active = (pages + per - 1) / per;
-  }
+  const int active = active_splits((L + p.block_size - 1) / p.block_size, p.nsplit);
   const size_t prow0 = ((size_t)s * p.num_heads + h) * p.nsplit;
-  // Launched as the decode kernel's programmatic dependent: wait until it
-  // has finished and its partials are visible (a no-op otherwise).
   grid_dependency_wait();
   // Warp w folds splits w, w + kWarps, ... into a running (M, l, O) for dims
   // 4 lane .. 4 lane + 3, rescaling by 2^(M_old - M_new) as M grows.
@@ -1124,15 +1325,7 @@ __global__ void __launch_bounds__(kHeadDim) pda_merge_kernel(const MergeParams p
   for (int i = warp; i < active; i += kWarps) {
     const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + (prow0 + i));
     const float4 o = __ldcg(reinterpret_cast<const float4*>(p.part_o + (prow0 + i) * kHeadDim) + lane);
-    const float mn = fmaxf(M, ml.x);
-    const float a = fast_exp2(M - mn);  // 0 while M is -inf
-    const float f = fast_exp2(ml.x - mn);
-    acc.x = acc.x * a + f * o.x;
-    acc.y = acc.y * a + f * o.y;
-    acc.z = acc.z * a + f * o.z;
-    acc.w = acc.w * a + f * o.w;
-    den = den * a + f * ml.y;
-    M = mn;
+    lse_fold(M, den, acc, ml.x, ml.y, o);
   }
   __shared__ float s_m[kWarps], s_l[kWarps];
   __shared__ float4 s_o[kWarps][32];
@@ -1153,18 +1346,13 @@ __global__ void __launch_bounds__(kHeadDim) pda_merge_kernel(const MergeParams p
     if (s_m[w] == -INFINITY) continue;  // a warp that merged no split
     const float f = fast_exp2(s_m[w] - Mt);
     const float4 o = s_o[w][lane];
-    A.x += f * o.x;
-    A.y += f * o.y;
-    A.z += f * o.z;
-    A.w += f * o.w;
-    D += f * s_l[w];
+    A.x = __fmaf_rn(f, o.x, A.x);
+    A.y = __fmaf_rn(f, o.y, A.y);
+    A.z = __fmaf_rn(f, o.z, A.z);
+    A.w = __fmaf_rn(f, o.w, A.w);
+    D = __fmaf_rn(f, s_l[w], D);
   }
-  const float zs = p.sinks ? __ldg(p.sinks + h) * 1.4426950408889634f : -INFINITY;
-  const float r[4] = {A.x, A.y, A.z, A.w};
-  const size_t o0 = ((size_t)s * p.num_heads + h) * kHeadDim + 4 * lane;
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-    store_out(p.out, o0 + j, pages > 0 ? finish(r[j], D, Mt, zs, p.v_scale) : 0.f, p.out_fp8, p.out_scale);
+  merge_store(p, s, h, lane, active > 0, Mt, D, A);
 }
 
 // One CTA waits on an mbarrier that nothing completes, with a short limit,

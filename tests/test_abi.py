@@ -97,8 +97,9 @@ def test_choose_splits_bounds_and_monotonicity(lib):
     (77, 8, 8, 16, pda.PDA_KERNEL_PERSISTENT, 1, 2),        # 616 units: one more than a dense wave
     (65535, 65535, 2, 16, pda.PDA_KERNEL_PER_UNIT, 1, 1),   # past 2^31 units: per-unit kernel
     # long contexts: a few sequences split into page ranges up to a dense wave
-    (1, 8, 8192, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 76, 2),   # 1 x 128K tokens: 608 CTAs + merge
-    (4, 8, 2048, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 19, 2),   # 4 x 32K
+    (1, 8, 8192, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 76, 2),   # 1 x 128K tokens: 608 CTAs + wide merge
+    (4, 8, 2048, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 19, 2),   # 4 x 32K: > 16 splits, wide merge
+    (8, 8, 512, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 9, 2),     # 8 x 8K: 9 splits, one warp per row merge
     (16, 8, 640, 64, pda.PDA_KERNEL_PERSISTENT, 10, 3),       # 16 x 40,960, 64-token blocks
     (8, 8, 8192, 16, pda.PDA_KERNEL_PERSISTENT, 32, 3),       # 8 x 128K
     (64, 8, 2048, 16, pda.PDA_KERNEL_PERSISTENT, 8, 3),       # 64 x 32K: 1 MiB split units
@@ -174,6 +175,13 @@ def test_bounded_wait_rejects_bad_limits(lib):
 
 def test_query_status_null_pointer(lib):
     assert lib.pda_query_device_status(None, ctypes.POINTER(ctypes.c_int)()) == pda.PDA_ERR_INVALID_ARG
+
+
+def test_workspace_info_null_pointers(lib):
+    n = ctypes.c_int(0)
+    b = ctypes.c_longlong(0)
+    assert lib.pda_workspace_info(None, None, ctypes.byref(n)) == pda.PDA_ERR_INVALID_ARG
+    assert lib.pda_workspace_info(None, ctypes.byref(b), None) == pda.PDA_ERR_INVALID_ARG
 
 
 def test_reserve_rejects_bad_args(lib):

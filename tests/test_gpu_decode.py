@@ -40,24 +40,20 @@ def test_config_full_parity(name):
     print(name, stats)
 
 
-@pytest.mark.parametrize("name,n_sample", [
-    ("32q8kv-256seq-ctx4096-bs16", 24),
-    ("40q8kv-256seq-ctx1to4000-bs16", 48),
-    ("64q8kv-128seq-ctx8192-bs64", 12),
-])
-def test_config_full_size_sampled(name, n_sample):
-    """Full-size batch in the benchmark's launch configuration; sampled rows vs the oracle."""
+@pytest.mark.parametrize("name", ["32q8kv-256seq-ctx4096-bs16", "40q8kv-256seq-ctx1to4000-bs16",
+                                  "64q8kv-128seq-ctx8192-bs64"])
+def test_config_full_size_every_sequence(name):
+    """Full-size batch in the benchmark's launch configuration (planned split
+    count and kernel), every element of every sequence against the oracle
+    (the pages' error figures cover every element of 4 head layouts x 3 seeds
+    over 1-4000-token contexts: vLLM pull request lishuoshuo-amd/vllm#3,
+    "Kernel latency, accuracy runs and kernel error")."""
     cfg = workloads.CONFIGS[name]
     batch = workloads.make_batch(cfg, device=DEV)
     out = U.run_cuda(batch)
     torch.cuda.synchronize()
-    rng = np.random.default_rng(123)
-    ids = set(rng.choice(cfg.num_seqs, size=n_sample, replace=False).tolist())
-    lens = batch.seq_lens_host
-    ids |= {int(np.argmin(lens)), int(np.argmax(lens)), 0, cfg.num_seqs - 1}
-    ids = sorted(ids)
-    ref = U.run_oracle(batch, seq_ids=ids)
-    stats = U.compare(out[ids], ref, name, literal=True)
+    ref = U.run_oracle(batch)
+    stats = U.compare(out, ref, name, literal=True)
     print(name, "splits", pda.plan_splits(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads,
                                           cfg.max_num_blocks_per_seq, cfg.block_size), stats)
 
@@ -235,6 +231,44 @@ def test_workspace_growth_during_capture_is_refused():
     assert err is not None and err.status == pda.PDA_ERR_WORKSPACE
 
 
+def test_graph_replay_after_workspace_growth():
+    """A graph captured with a split call keeps its workspace address. A later,
+    larger eager call on the same stream grows the workspace; the old buffer
+    must stay allocated (retired, not freed) so the graph still replays to
+    the eager result."""
+    pda.release()
+    small = workloads.make_custom(4, 32, 8, [900, 1000, 333, 1024], seed=17, device=DEV)
+    big = workloads.make_custom(40, 64, 8, [4096] * 40, seed=18, device=DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    cfg = small.cfg
+    pda.set_split_override(4)
+    try:
+        eager = U.run_cuda(small).clone()
+        pda.reserve(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq, cfg.block_size,
+                    stream=s)
+        bytes0, retired0 = pda.workspace_info(s)
+        assert bytes0 > 0 and retired0 == 0
+        g = torch.cuda.CUDAGraph()
+        out = torch.zeros_like(small.q)
+        with torch.cuda.graph(g, stream=s):
+            U.run_cuda(small, out=out, stream=s)
+        with torch.cuda.stream(s):
+            U.run_cuda(big, stream=s)      # grows the workspace of stream s
+        s.synchronize()
+        bytes1, retired1 = pda.workspace_info(s)
+        assert bytes1 > bytes0 and retired1 == retired0 + 1
+        with torch.cuda.stream(s):
+            g.replay()
+        s.synchronize()
+    finally:
+        pda.set_split_override(0)
+    assert torch.equal(out, eager)
+    del g
+    pda.release()
+    assert pda.workspace_info(s) == (0, 0)
+
+
 def test_bounded_wait_reports_and_context_survives():
     assert pda.query_device_status() == 0
     pda.bounded_wait_check(2000)
@@ -301,3 +335,52 @@ def test_slot_scales_constant_table_matches_per_tensor():
     torch.cuda.synchronize()
     assert (a.float() - b.float()).abs().max().item() <= 4e-3
     U.compare(a, U.run_oracle(batch), "constant tables")
+
+
+# ------------------------------------------------------------ merge kernels
+
+@pytest.mark.parametrize("S,H,Hk,splits", [(8, 32, 8, 2), (8, 32, 8, 4), (4, 40, 8, 16), (4, 64, 8, 17),
+                                            (2, 8, 1, 40)])
+def test_merge_kernels_match_across_kernels(S, H, Hk, splits):
+    """Up to 16 splits the merge runs one warp per row, beyond that four
+    warps per row. The per-unit kernel (pda_decode on one-wave batches) and
+    pda_decode_noalloc run the same tiles and the same merge: same split
+    count, same bits, call after call and from a graph replayed twice;
+    zero-length sequences give zeros."""
+    lens = [1024, 0, 517, 16, 33, 1000, 0, 257][:S]
+    batch = workloads.make_custom(S, H, Hk, lens, seed=H + splits, device=DEV, max_num_blocks_per_seq=64)
+    cfg = batch.cfg
+    pda.set_split_override(splits)
+    try:
+        assert pda.plan_kernel(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq,
+                               cfg.block_size) == pda.PDA_KERNEL_PER_UNIT_DENSE
+        assert pda.plan_launches(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq,
+                                 cfg.block_size) == 2
+        ref = torch.empty_like(batch.q)
+        pda.decode_noalloc(batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.seq_lens, cfg.scale,
+                           cfg.k_scale, cfg.v_scale, out=ref)
+        outs = [U.run_cuda(batch).clone() for _ in range(3)]
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        pda.reserve(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq, cfg.block_size,
+                    stream=s)
+        g = torch.cuda.CUDAGraph()
+        gout = torch.zeros_like(batch.q)
+        with torch.cuda.graph(g, stream=s):
+            U.run_cuda(batch, out=gout, stream=s)
+        for _ in range(2):
+            gout.zero_()
+            with torch.cuda.stream(s):
+                g.replay()
+            s.synchronize()
+            outs.append(gout.clone())
+        torch.cuda.synchronize()
+    finally:
+        pda.set_split_override(0)
+    for o in outs:
+        assert torch.equal(o, ref)
+    for i, L in enumerate(lens):
+        if L == 0:
+            assert torch.all(outs[0][i] == 0)
+    U.compare(outs[0], U.run_oracle(batch), "merge H=%d splits=%d" % (H, splits))
+    assert pda.query_device_status() == 0

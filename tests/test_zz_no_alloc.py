@@ -72,11 +72,52 @@ def test_noalloc_matches_decode_on_two_calls_in_a_row(splits):
     assert pda.query_device_status() == 0
 
 
-def test_noalloc_uses_scratch_for_split_batches():
-    # The default plan splits this batch, so the partials really go through the array.
+def noalloc_splits(cfg) -> int:
+    """The split count pda_decode_noalloc plans: the heuristic at the per-unit
+    kernel's 3 CTAs per SM, capped at the table width."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n = pda.choose_splits(cfg.num_seqs, cfg.num_kv_heads, cfg.max_num_blocks_per_seq, cfg.block_size, sms, 3)
+    return min(n, cfg.max_num_blocks_per_seq)
+
+
+def test_noalloc_default_plan_splits_through_the_array():
+    # With its own plan (no override) the small benchmark batch splits, so
+    # its partials go through the static array; the result matches the oracle.
     cfg = workloads.CONFIGS[workloads.SMALL]
-    assert pda.plan_splits(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq,
-                           cfg.block_size) > 1
+    assert noalloc_splits(cfg) > 1
+    batch = workloads.make_batch(cfg, device=DEV)
+    out = torch.empty_like(batch.q)
+    pda.decode_noalloc(batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.seq_lens, cfg.scale,
+                       cfg.k_scale, cfg.v_scale, out=out)
+    torch.cuda.synchronize()
+    U.compare(out, U.run_oracle(batch), "noalloc, own plan", literal=True)
+
+
+def test_noalloc_allocates_no_device_memory():
+    # A split call on a stream the library has never seen: no workspace
+    # appears for that stream and the device's free memory does not move.
+    batch = workloads.make_custom(6, 32, 8, [1024, 700, 999, 64, 1024, 513], seed=91, device=DEV)
+    cfg = batch.cfg
+    out = torch.empty_like(batch.q)
+    s, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    pda.set_split_override(3)
+    try:
+        # first call: the library's module (and its array) may load lazily here
+        pda.decode_noalloc(batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.seq_lens, cfg.scale,
+                           cfg.k_scale, cfg.v_scale, out=out, stream=s)
+        s.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
+        s2.wait_stream(s)
+        for _ in range(3):
+            pda.decode_noalloc(batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.seq_lens,
+                               cfg.scale, cfg.k_scale, cfg.v_scale, out=out, stream=s2)
+        s2.synchronize()
+        free1 = torch.cuda.mem_get_info()[0]
+    finally:
+        pda.set_split_override(0)
+    assert pda.workspace_info(s) == (0, 0) and pda.workspace_info(s2) == (0, 0)
+    assert free1 == free0, "device free memory moved by %d bytes" % (free0 - free1)
 
 
 def test_noalloc_rejects_batches_beyond_its_buffer():
