@@ -2,6 +2,9 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config NAME]
 
+``--gpus N`` runs N replicas, one process per GPU: under torchrun its
+WORLD_SIZE must equal N; without a launcher, N > 1 starts torchrun itself.
+
 A step is one ``pda_decode`` call (split plan, page gather, dequant, QK^T,
 online softmax, PV, CTA merge, partial store / LSE merge) over one batch of
 synthetic input already resident in HBM. Steps are captured in CUDA graphs
@@ -107,8 +110,10 @@ def peaks():
 # Clock event reasons that void a timed region (sw_power_cap is kept and noted).
 REJECT_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
 
-# One call in this many inside the timed region carries kernel events.
-EVENT_STRIDE = 10
+# Calls in the roofline graph, each bracketed by kernel events (independent
+# of --steps). It runs right after the timed region, inside the same clock
+# sampling window; the timed region itself carries no event nodes.
+ROOFLINE_CALLS = 24
 
 # Kernel function behind each decode instance name the library reports.
 KERNEL_FUNCTION = {"per-unit (3 CTAs/SM)": "pda_split_decode_kernel", "per-unit dense (4 CTAs/SM)":
@@ -304,20 +309,21 @@ def run_ours(args, ws, rank, local):
     stream.synchronize()
     assert pda.query_device_status(stream) == 0
 
-    # Graphs: one of `chunk` calls, every EVENT_STRIDE-th of them bracketed by
-    # kernel events (an event node costs microseconds, too much to put around
-    # every call of a small batch), and one graph for the remainder.
+    # Graphs: the timed region replays graphs of `chunk` plain calls (and one
+    # for the remainder); the roofline graph holds ROOFLINE_CALLS calls, each
+    # bracketed by kernel events (an event node costs the bracketed call its
+    # overlap with its neighbours, so these calls stay out of the timed region).
     K = args.steps
     chunk = min(K, 100)
-    n_ev = (chunk + EVENT_STRIDE - 1) // EVENT_STRIDE
-    ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
+    ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(ROOFLINE_CALLS)]
 
     def capture(n, with_events):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for i in range(n):
-                if with_events and i % EVENT_STRIDE == 0:
-                    pda.set_profile_events(*ev_pairs[i // EVENT_STRIDE])
+                if with_events:
+                    pda.set_profile_events(*ev_pairs[i])
                 call(i)
                 pda.set_profile_events(None, None)
         return g
@@ -335,11 +341,13 @@ def run_ours(args, ws, rank, local):
         mode = "eager"
         torch.cuda.synchronize()
     if mode == "graph":
-        g_main = capture(chunk, True)
+        g_main = capture(chunk, False)
         rem = K % chunk
         g_rem = capture(rem, False) if rem else None
+        g_roof = capture(ROOFLINE_CALLS, True)
         with torch.cuda.stream(stream):
             g_main.replay()
+            g_roof.replay()
         stream.synchronize()
 
     def timed_region():
@@ -357,20 +365,25 @@ def run_ours(args, ws, rank, local):
                 if g_rem is not None:
                     g_rem.replay()
             else:
-                # host enqueue (~10 us) stays far below the kernel time, so the
-                # stream never drains; every EVENT_STRIDE-th of the last `chunk`
-                # calls carries kernel events
+                # host enqueue (~10 us) stays far below the kernel time
                 for i in range(K):
-                    j = i - (K - chunk)
-                    if j >= 0 and j % EVENT_STRIDE == 0:
-                        pda.set_profile_events(*ev_pairs[j // EVENT_STRIDE])
                     call(i)
-                    pda.set_profile_events(None, None)
             t_end.record(stream)
         stream.synchronize()
         torch.cuda.synchronize()
         if ws > 1:
             torch.distributed.barrier()
+        # roofline calls: the same calls, each with kernel events around the
+        # decode kernel, right after the timed region
+        with torch.cuda.stream(stream):
+            if mode == "graph":
+                g_roof.replay()
+            else:
+                for i in range(ROOFLINE_CALLS):
+                    pda.set_profile_events(*ev_pairs[i])
+                    call(i)
+                    pda.set_profile_events(None, None)
+        stream.synchronize()
         clocks = sampler.stop()
         return t_start, t_end, clocks
 
@@ -382,7 +395,7 @@ def run_ours(args, ws, rank, local):
         t_start, t_end, clocks = timed_region()
         remeasured = True
     elapsed_ms = t_start.elapsed_time(t_end)
-    kern_ms = [a.elapsed_time(b) for a, b in ev_pairs]
+    kern_ms = sorted(a.elapsed_time(b) for a, b in ev_pairs)
     assert pda.query_device_status(stream) == 0
 
     value, elapsed_ms = aggregate_throughput(bytes_per_call, K, elapsed_ms, ws, dev)
@@ -565,8 +578,8 @@ def run_ours(args, ws, rank, local):
         return
 
     peak, peak_kind = peaks()
-    kern_mean_ms = statistics.fmean(kern_ms)
-    achieved = bytes_per_call / (kern_mean_ms * 1e-3) / 1e9
+    kern_median_ms = statistics.median(kern_ms)
+    achieved = bytes_per_call / (kern_median_ms * 1e-3) / 1e9
     traffic = ncu_traffic(cfg.name) if args.variant == "plain" else None
     us_per_call = elapsed_ms * 1e3 / K
 
@@ -609,10 +622,14 @@ def run_ours(args, ws, rank, local):
                      "kernel": KERNEL_FUNCTION[kernel_kind] if args.variant != "slot_scales"
                      else "pda_split_decode_kernel",
                      "timed_span": "profile events around the decode kernel (with the unit-order kernel that "
-                                   "precedes the persistent kernel) of every %dth call in the timed region"
-                                   % EVENT_STRIDE,
-                     "kernel_us_mean": kern_mean_ms * 1e3,
-                     "kernel_launches_timed": len(kern_ms), "algorithmic_bytes_per_launch": bytes_per_call},
+                                   "precedes the persistent kernel) of each of %d calls replayed as one graph "
+                                   "right after the timed region, in the same clock window; achieved uses the "
+                                   "median" % ROOFLINE_CALLS,
+                     "kernel_us_median": kern_median_ms * 1e3,
+                     "kernel_us_min": kern_ms[0] * 1e3, "kernel_us_max": kern_ms[-1] * 1e3,
+                     "kernel_us_mean": statistics.fmean(kern_ms) * 1e3,
+                     "kernel_launches_timed": len(kern_ms), "algorithmic_bytes_per_launch": bytes_per_call,
+                     "call_frac": bytes_per_call / (us_per_call * 1e-6) / 1e9 / peak},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "e2e_serving_step": e2e_step_line,
@@ -823,9 +840,29 @@ def run_cache_write(args):
                                    "frac": nbytes / us / 1e3 / peak, "peak_source": kind}}), flush=True)
 
 
+def spawn_replicas(n: int) -> int:
+    """--gpus N > 1 without a launcher: run this command as N ranks under
+    torchrun (one process per GPU, rendezvous on 127.0.0.1), rank 0 printing
+    the JSON line; returns torchrun's exit status."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", str(n),
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.run(cmd).returncode
+
+
 def main():
     args = parse()
+    if args.gpus < 1:
+        raise SystemExit("bench.py: --gpus must be >= 1")
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        sys.exit(spawn_replicas(args.gpus))
     ws, rank, local = dist_env()
+    if ws != args.gpus:
+        raise SystemExit("bench.py: --gpus %d but the launcher started %d rank(s) (WORLD_SIZE); "
+                         "they must agree" % (args.gpus, ws))
     if args.profile:
         run_profile(args)
         return
