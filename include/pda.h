@@ -79,7 +79,10 @@ typedef enum pda_status {
  * only f16's): each query row is scaled by a power of two before it enters
  * the f16 tensor-core products and the logit scale by its inverse, which is
  * exact. The logits scale * k_scale * q . k_t must stay finite in binary32
- * (|logit| < 2^126 suffices). NaN or infinite inputs give undefined output.
+ * (|logit| < 2^126 suffices), and they carry binary32's relative precision:
+ * with logits of magnitude X, tokens whose logits differ by less than about
+ * X * 2^-22 are weighted only that precisely (at X ~ 1e5, a few tenths of a
+ * percent). NaN or infinite inputs give undefined output.
  * Arithmetic: e4m3 -> f16 and the shifted bf16 q -> f16 are exact; scores,
  * softmax and accumulation are fp32; the probabilities enter the PV product
  * as two f16 parts (f16(p) and f16(p - f16(p))), about 2^-22 relative.

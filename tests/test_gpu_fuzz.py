@@ -5,8 +5,16 @@ ratio (1-8), the block size (16-128), ragged lengths (zeros included), a
 table wider than needed (a quarter of the cases draw it with replacement, so
 blocks are shared and repeated), a split count (planned or forced) and an entry point
 (plain, sinks, shuffled V, token-major, per-slot scales, e4m3 output with
-sinks and either V layout, the no-allocation entry point). Contexts stay
-short so that the oracle is quick; the batch sizes reach both kernel shapes.
+sinks and either V layout, the no-allocation entry point); a third of the
+cases scale the query rows by powers of two from 2^-40 to 2^4, and a third
+draw V three times larger. Contexts stay short so that the oracle is quick;
+the batch sizes reach both kernel shapes.
+
+Upward scaling stops at 2^4: logits of magnitude X carry an fp32 rounding
+of about X 2^-24, so once X reaches ~10^5 two tokens whose logits lie that
+close are weighted a few tenths of a percent apart from the exact result.
+Any fp32 softmax does that; tests/test_gpu_accuracy.py covers rows past
+f16's range on fixed inputs.
 """
 
 from __future__ import annotations
@@ -56,8 +64,13 @@ def _case(seed):
     variant = str(rng.choice(["plain", "sinks", "shuffled_v", "token_major", "slot_scales", "e4m3_out",
                               "noalloc"]))
     shared = bool(rng.random() < 0.25)   # tables drawn with replacement: shared and repeated blocks
+    # a third of the cases scale query rows by powers of two past f16's range
+    # either way, and a third draw V three times larger (few-token outputs
+    # then often land in [2, 4), where the bar is tight)
+    q_exps = rng.choice([0, 4, -4, -8, -16, -40], size=(S, Hk * g)).tolist() if rng.random() < 1 / 3 else None
+    v_gain = 3.0 if rng.random() < 1 / 3 else 1.0
     return dict(Hk=Hk, g=g, bs=bs, S=S, lens=lens.tolist(), MB=MB, splits=splits, variant=variant,
-                shared=shared, seed=seed)
+                shared=shared, seed=seed, q_exps=q_exps, v_gain=v_gain)
 
 
 @pytest.mark.parametrize("seed", range(int(os.environ.get("PDA_FUZZ_FIRST", "0")),
@@ -66,7 +79,12 @@ def test_random_case(seed):
     c = _case(seed)
     H = c["Hk"] * c["g"]
     batch = workloads.make_custom(c["S"], H, c["Hk"], c["lens"], block_size=c["bs"], pool_factor=1.3,
-                                  seed=2000 + seed, device=DEV, max_num_blocks_per_seq=c["MB"])
+                                  seed=2000 + seed, device=DEV, max_num_blocks_per_seq=c["MB"],
+                                  v_scale=0.05 / c["v_gain"])
+    batch.cfg = batch.cfg.with_(v_scale=0.05)
+    if c["q_exps"] is not None:
+        mult = torch.tensor(np.ldexp(1.0, np.array(c["q_exps"], dtype=np.int64)), dtype=torch.float32, device=DEV)
+        batch.q = (batch.q.float() * mult[:, :, None]).to(torch.bfloat16)
     cfg = batch.cfg
     if c["shared"]:
         # prefix-cache style tables: sequences share physical blocks and a
