@@ -240,8 +240,9 @@ pda_status pda_decode_strided(void* out, const void* q, const void* k_cache, con
  * one value give pda_decode's result for that per-tensor scale (up to fp32
  * rounding order). Entries of slots past a sequence's length are never used
  * (they may hold anything). Within one KV split, the largest ratio between
- * two V scales must stay below 2^15 (probabilities are carried in f16
- * relative to the split's first V scale).
+ * two V scales must stay below 2^15 (each probability, times its slot's V
+ * scale relative to the split's first one, enters the PV product in f16
+ * parts, whose range ends at 65504); the tests cover ratios of 2^14.
  */
 pda_status pda_decode_slot_scales(void* out, const void* q, const void* k_cache, const void* v_cache,
                                   const float* k_scales, const float* v_scales, const int32_t* block_tables,

@@ -3,7 +3,9 @@
 //   pda_persistent_decode_kernel  one CTA per resident slot taking work units
 //                                 from a queue, the same per-unit arithmetic
 //   pda_order_units_kernel        longest-first order of the queued units
-//   pda_merge_kernel              log-sum-exp merge of split partials
+//   pda_merge_kernel              log-sum-exp merge of split partials (one
+//                                 warp per row; pda_merge_wide_kernel past
+//                                 16 splits)
 //   pda_reshape_and_cache_kernel  KV-cache write (and a scattered variant)
 //
 // Work unit: one (sequence, kv head, KV split). Per unit:
@@ -16,7 +18,8 @@
 //       online softmax over tokens in fp32 (exp2 domain)
 //       O^T += V_tile^T (128 x 16 tok) * P^T (16 tok x 8 heads)
 //     with K and V dequantised exactly from e4m3 to f16 in registers, once
-//     per tile for every head of the group;
+//     per tile for every head of the group, the query rows shifted by a
+//     power of two into f16's range, and P carried as two f16 parts;
 //   * the consumers merge their (m, l, O) through shared memory and either
 //     write bf16 output (one split) or an fp32 partial (several splits) that
 //     the merge kernel combines by log-sum-exp.

@@ -301,7 +301,7 @@ def test_slot_scales_parity(bs, splits):
     NB, Hk = batch.num_blocks, 8
     # Per-slot scales within +-20 % of the scale the codes were made with (the
     # spread per-token quantisation of N(0,1) data gives), so values keep the
-    # configs' range; P is carried in f16, so the error scales with |v|.
+    # configs' range (tests/test_gpu_accuracy.py spreads them over 2^14).
     g = torch.Generator(device=DEV).manual_seed(5)
     ks = (torch.rand(NB, Hk, bs, generator=g, device=DEV) * 0.02 + 0.04).float()
     vs = (torch.rand(NB, Hk, bs, generator=g, device=DEV) * 0.02 + 0.04).float()
