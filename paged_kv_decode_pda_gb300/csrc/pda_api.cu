@@ -197,6 +197,35 @@ pda_status make_token_major_map(const void* base, long long nb, int hk, int bs, 
   return PDA_OK;
 }
 
+// Native V pages [NB][Hk][128][bs] of 32-, 64- or 128-token blocks through a
+// tensor map with the TMA swizzle whose span is one page row (bs bytes): the
+// box is one page (bs x 128 rows of one kv head of one block). The block
+// extent is the int32 id range (the entry points are not told the pool
+// size; reads stay where the table points, as with 1-D copies). Returns the
+// kernel's swizzle mode, or kVSwizzleNone (then *map is unused) for other
+// block sizes or when the driver entry point is missing.
+int make_v_swizzle_map(const void* v_cache, int hk, int bs, CUtensorMap* map) {
+  CUtensorMapSwizzle sw;
+  int mode;
+  switch (bs) {
+    case 32: sw = CU_TENSOR_MAP_SWIZZLE_32B; mode = pda::kVSwizzle32; break;
+    case 64: sw = CU_TENSOR_MAP_SWIZZLE_64B; mode = pda::kVSwizzle64; break;
+    case 128: sw = CU_TENSOR_MAP_SWIZZLE_128B; mode = pda::kVSwizzle128; break;
+    default: return pda::kVSwizzleNone;
+  }
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return pda::kVSwizzleNone;
+  const cuuint64_t dims[4] = {(cuuint64_t)bs, (cuuint64_t)kHeadDim, (cuuint64_t)hk, (cuuint64_t)INT32_MAX};
+  const cuuint64_t strides[3] = {(cuuint64_t)bs, (cuuint64_t)kHeadDim * bs, (cuuint64_t)hk * kHeadDim * bs};
+  const cuuint32_t box[4] = {(cuuint32_t)bs, (cuuint32_t)kHeadDim, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  if (enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(v_cache), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+      CUDA_SUCCESS)
+    return pda::kVSwizzleNone;
+  return mode;
+}
+
 // The checks of sizes and scalars every decode entry point makes.
 pda_status validate_sizes(int num_seqs, int num_heads, int num_kv_heads, int head_size, int block_size,
                           int max_blocks, float scale, float k_scale, float v_scale) {
@@ -563,8 +592,13 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
   cudaEvent_t eb = g_prof_before.load(), ea = g_prof_after.load();
   if (eb && ea && record_profile_event(eb, stream) != cudaSuccess) return PDA_ERR_CUDA;
   dim3 grid((unsigned)nsplit, (unsigned)num_kv_heads, (unsigned)num_seqs);
+  // Native V pages of 32-, 64- and 128-token blocks load through a swizzled
+  // tensor map (no ldmatrix bank conflicts); the per-slot-scale instance's
+  // stages carry scale rows and are not aligned for it.
+  CUtensorMap vmap;
+  if (!slot && !tm && !v_shuffled) p.v_swizzle = make_v_swizzle_map(v_cache, num_kv_heads, block_size, &vmap);
   const CUtensorMap& mk = tm ? tm->k : g_no_map;
-  const CUtensorMap& mv = tm ? tm->v : g_no_map;
+  const CUtensorMap& mv = tm ? tm->v : (p.v_swizzle ? vmap : g_no_map);
   const bool paired = paired_for(p.gqa);
   if (is_persistent(pl.kind)) {
     const int units = num_seqs * num_kv_heads * nsplit;

@@ -70,6 +70,26 @@ static_assert(32 % kMaxPagesPerStage == 0, "stage pages must tile a 32-entry tab
 constexpr int kMaxGqa = 8;                   // MMA N dimension: query heads of a group
 constexpr int kMergeStride = kHeadDim + 4;   // padded fp32 row of the CTA merge area
 
+// Swizzled native V pages ([128 dims][bs tokens], rows bs bytes apart): an
+// ldmatrix reads the 8 rows of dims 8j..8j+7 at one 16-byte token chunk,
+// which at 32-, 64- and 128-byte rows falls on 2, 2 and 1 bank groups
+// (4- to 8-way conflicts). Loaded through a tensor map with the 32-, 64- or
+// 128-byte TMA swizzle, chunk c of row d lands at chunk c ^ f(d):
+//   32 B rows:  f(d) = (d >> 2) & 1      (address bit 4 ^= bit 7)
+//   64 B rows:  f(d) = (d >> 1) & 3      (bits 4-5 ^= bits 7-8)
+//   128 B rows: f(d) = d & 7             (bits 4-6 ^= bits 7-9)
+// and the 8 rows of one ldmatrix fall on 8 distinct bank groups. Since the
+// ldmatrix rows are dims 32mp + 8j + (lane & 7), f depends on the lane only.
+enum : int { kVSwizzleNone = 0, kVSwizzle32 = 1, kVSwizzle64 = 2, kVSwizzle128 = 3 };
+__device__ __forceinline__ uint32_t v_swizzle_xor(int mode, int lane) {
+  switch (mode) {
+    case kVSwizzle32: return (uint32_t)((lane >> 2) & 1);
+    case kVSwizzle64: return (uint32_t)((lane >> 1) & 3);
+    case kVSwizzle128: return (uint32_t)(lane & 7);
+    default: return 0u;
+  }
+}
+
 struct DecodeParams {
   void* out;                    // [S][H][D] bf16, or e4m3 bytes when out_fp8
   const __nv_bfloat16* q;       // [S][H][D]
@@ -94,6 +114,10 @@ struct DecodeParams {
   float logit_scale_log2;       // scale * k_scale * log2(e)  (scale * log2(e) with slot scales)
   float v_scale;                // per-tensor V scale (unused with slot scales)
   int v_shuffled = 0;           // 1: V pages are [bs/16][D][16] (AITER shuffled), else [D][bs]
+  // Native V pages of 32-, 64- or 128-token blocks arrive through a tensor
+  // map (tm_v) with the TMA swizzle whose span is one page row (kVSwizzle*),
+  // else (0) as one 1-D bulk copy.
+  int v_swizzle = 0;
   // Token-major variant: position (1..3) of the token, kv-head and block
   // dimensions in the 4-D tensor maps (dimension 0 is the 128 bytes of a row).
   int tm_dim_token = 1;
@@ -224,6 +248,7 @@ struct TileWorker {
   uint32_t k_lane_off;   // page-major K: ldmatrix row of this lane
   uint32_t tm_row, tm_xor, tm_hi;  // token-major tiles: row, swizzle and chunk half
   uint32_t v_row, v_lane_off;
+  uint32_t v_xor;        // swizzled native V: this lane's chunk XOR (0 otherwise)
   bool low_quad;
   // Paired columns (kPaired, for GQA groups of at most 4 heads): MMA
   // columns 4..7 repeat heads 0..3, so the lanes that own them (tig >= 2)
@@ -242,7 +267,7 @@ struct TileWorker {
   float l0, l1;          // running partial sums over this lane's tokens
   float o[kChunks][4];   // O^T: m-tile mt = dims 16mt.. ; cols heads 2tig, 2tig+1
 
-  __device__ __forceinline__ void setup(int lane, int bs, int v_shuffled) {
+  __device__ __forceinline__ void setup(int lane, int bs, int v_shuffled, int v_swizzle) {
     gid = lane >> 2;
     tig = lane & 3;
     // ldmatrix row assignment. K: lane l supplies token row_token(l & 15) of
@@ -258,6 +283,7 @@ struct TileWorker {
     // contiguous and so bank-conflict free for any block size).
     v_row = v_shuffled ? 16u : (uint32_t)bs;
     v_lane_off = (uint32_t)lane * v_row;
+    v_xor = v_swizzle_xor(v_swizzle, lane);
     low_quad = kTokenMajor ? true : tig < 2;
     hi_lane = tig < 2;
   }
@@ -728,7 +754,10 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
               } else {
                 const size_t off = (size_t)blk[t] * block_stride + (size_t)kvh * head_stride;
                 bulk_g2s(sbase + (uint32_t)t * page_bytes, p.k_cache + off, page_bytes, bar);
-                bulk_g2s(sbase + (uint32_t)(PPS + t) * page_bytes, p.v_cache + off, page_bytes, bar);
+                if (p.v_swizzle)  // coordinates: row bytes, dim, kv head, block
+                  tma_load_4d(sbase + (uint32_t)(PPS + t) * page_bytes, &tm_v, 0, 0, kvh, blk[t], bar);
+                else
+                  bulk_g2s(sbase + (uint32_t)(PPS + t) * page_bytes, p.v_cache + off, page_bytes, bar);
               }
             }
           }
@@ -774,7 +803,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
 
   // -------------------------------------------------------------- consumers
   TileWorker<kSlotScales, kTokenMajor, kPaired, (kMinCtasPerSm < 4)> w;
-  w.setup(lane, bs, p.v_shuffled);
+  w.setup(lane, bs, p.v_shuffled, p.v_swizzle);
   {
     const int qh = w.q_head();
     const bool live = qh < g;
@@ -824,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
       const uint32_t kbase = kTokenMajor ? sbase + (uint32_t)pg * page_bytes + (uint32_t)sub * 2048u
                                          : sbase + (uint32_t)pg * page_bytes + (uint32_t)(sub * 256);
       const uint32_t vbase = kTokenMajor ? sbase + (uint32_t)(PPS + pg) * page_bytes + (uint32_t)sub * 2048u
-                                         : sbase + (uint32_t)(PPS + pg) * page_bytes + (uint32_t)sub * v_sub;
+                                         : sbase + (uint32_t)(PPS + pg) * page_bytes + ((uint32_t)sub ^ w.v_xor) * v_sub;
       w.tile(kbase, vbase, bs, L - tok0, srow + pg * bs + sub * 16, srow + (PPS + pg) * bs + sub * 16, vinv);
     }
     __syncwarp();
@@ -1045,7 +1074,10 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
                 } else {
                   const size_t off = (size_t)blk[u] * block_stride + (size_t)kvh * head_stride;
                   bulk_g2s(sbase + (uint32_t)u * page_bytes, p.k_cache + off, page_bytes, bar);
-                  bulk_g2s(sbase + (uint32_t)(PPS + u) * page_bytes, p.v_cache + off, page_bytes, bar);
+                  if (p.v_swizzle)  // coordinates: row bytes, dim, kv head, block
+                    tma_load_4d(sbase + (uint32_t)(PPS + u) * page_bytes, &tm_v, 0, 0, kvh, blk[u], bar);
+                  else
+                    bulk_g2s(sbase + (uint32_t)(PPS + u) * page_bytes, p.v_cache + off, page_bytes, bar);
                 }
               }
             }
@@ -1105,7 +1137,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
 
   // -------------------------------------------------------------- consumers
   TileWorker<false, kTokenMajor, kPaired, true> w;
-  w.setup(lane, bs, p.v_shuffled);
+  w.setup(lane, bs, p.v_shuffled, p.v_swizzle);
   w.reset();
   const int tiles_per_page = bs / 16;
   const uint32_t v_sub = p.v_shuffled ? (uint32_t)(kHeadDim * 16) : 16u;
@@ -1143,7 +1175,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
       const uint32_t kbase = kTokenMajor ? sbase + (uint32_t)pg * page_bytes + (uint32_t)sub * 2048u
                                          : sbase + (uint32_t)pg * page_bytes + (uint32_t)(sub * 256);
       const uint32_t vbase = kTokenMajor ? sbase + (uint32_t)(PPS + pg) * page_bytes + (uint32_t)sub * 2048u
-                                         : sbase + (uint32_t)(PPS + pg) * page_bytes + (uint32_t)sub * v_sub;
+                                         : sbase + (uint32_t)(PPS + pg) * page_bytes + ((uint32_t)sub ^ w.v_xor) * v_sub;
       w.tile(kbase, vbase, bs, hd.L - tok0, nullptr, nullptr, 1.f);
     }
     if (hd.flags & kHdrLast) {
