@@ -746,10 +746,10 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
           const uint32_t sbase = ring_u32 + (uint32_t)stage * p.stage_bytes;
           const uint32_t bar = full0 + 8u * stage;
           mbar_arrive_expect_tx(bar, 2u * page_bytes * (uint32_t)np);
+          if constexpr (kTokenMajor) {
 #pragma unroll
-          for (int t = 0; t < kMaxPagesPerStage; ++t) {
-            if (t < np) {
-              if constexpr (kTokenMajor) {
+            for (int t = 0; t < kMaxPagesPerStage; ++t) {
+              if (t < np) {
                 // coordinates: 0 for the row bytes and the token dim, kvh and
                 // the block id in the head and block dims
                 const int c1 = p.tm_dim_head == 1 ? kvh : (p.tm_dim_block == 1 ? blk[t] : 0);
@@ -757,16 +757,29 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
                 const int c3 = p.tm_dim_head == 3 ? kvh : (p.tm_dim_block == 3 ? blk[t] : 0);
                 tma_load_4d(sbase + (uint32_t)t * page_bytes, &tm_k, 0, c1, c2, c3, bar);
                 tma_load_4d(sbase + (uint32_t)(PPS + t) * page_bytes, &tm_v, 0, c1, c2, c3, bar);
-              } else {
+              }
+            }
+          } else if (!kSlotScales && p.v_swizzle) {
+            // Swizzled V (32- to 128-token blocks: at most 2 pages a stage).
+            // One branch per stage, not per page: the slot-scale instance's
+            // busy producer lost 2.5 % of a 2.15 GB batch to a per-page one
+            // (that instance never swizzles: its stages carry scale rows).
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (t < np) {
                 const size_t off = (size_t)blk[t] * block_stride + (size_t)kvh * head_stride;
                 bulk_g2s(sbase + (uint32_t)t * page_bytes, p.k_cache + off, page_bytes, bar);
-                // (the slot-scale instance never swizzles: its stages carry
-                // scale rows and are not aligned for it, and the branch alone
-                // cost its busy producer 2.5 % on the 2.15 GB batch)
-                if (!kSlotScales && p.v_swizzle)  // coordinates: row bytes, dim, kv head, block
-                  tma_load_4d(sbase + (uint32_t)(PPS + t) * page_bytes, &tm_v, 0, 0, kvh, blk[t], bar);
-                else
-                  bulk_g2s(sbase + (uint32_t)(PPS + t) * page_bytes, p.v_cache + off, page_bytes, bar);
+                // coordinates: row bytes, dim, kv head, block
+                tma_load_4d(sbase + (uint32_t)(PPS + t) * page_bytes, &tm_v, 0, 0, kvh, blk[t], bar);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int t = 0; t < kMaxPagesPerStage; ++t) {
+              if (t < np) {
+                const size_t off = (size_t)blk[t] * block_stride + (size_t)kvh * head_stride;
+                bulk_g2s(sbase + (uint32_t)t * page_bytes, p.k_cache + off, page_bytes, bar);
+                bulk_g2s(sbase + (uint32_t)(PPS + t) * page_bytes, p.v_cache + off, page_bytes, bar);
               }
             }
           }
@@ -1069,10 +1082,10 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
             if (with_q)
               bulk_g2s(aux_u32 + (uint32_t)stage * kAuxBytes + kAuxQ,
                        p.q + ((size_t)s * p.num_heads + (size_t)kvh * g) * kHeadDim, q_bytes, bar);
+            if constexpr (kTokenMajor) {
 #pragma unroll
-            for (int u = 0; u < kMaxPagesPerStage; ++u) {
-              if (u < np) {
-                if constexpr (kTokenMajor) {
+              for (int u = 0; u < kMaxPagesPerStage; ++u) {
+                if (u < np) {
                   // coordinates: 0 for the row bytes and the token dim, kvh
                   // and the block id in the head and block dims
                   const int c1 = p.tm_dim_head == 1 ? kvh : (p.tm_dim_block == 1 ? blk[u] : 0);
@@ -1080,13 +1093,27 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
                   const int c3 = p.tm_dim_head == 3 ? kvh : (p.tm_dim_block == 3 ? blk[u] : 0);
                   tma_load_4d(sbase + (uint32_t)u * page_bytes, &tm_k, 0, c1, c2, c3, bar);
                   tma_load_4d(sbase + (uint32_t)(PPS + u) * page_bytes, &tm_v, 0, c1, c2, c3, bar);
-                } else {
+                }
+              }
+            } else if (p.v_swizzle) {
+              // swizzled V (32- to 128-token blocks: at most 2 pages a stage);
+              // one branch per stage, not per page
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                if (u < np) {
                   const size_t off = (size_t)blk[u] * block_stride + (size_t)kvh * head_stride;
                   bulk_g2s(sbase + (uint32_t)u * page_bytes, p.k_cache + off, page_bytes, bar);
-                  if (p.v_swizzle)  // coordinates: row bytes, dim, kv head, block
-                    tma_load_4d(sbase + (uint32_t)(PPS + u) * page_bytes, &tm_v, 0, 0, kvh, blk[u], bar);
-                  else
-                    bulk_g2s(sbase + (uint32_t)(PPS + u) * page_bytes, p.v_cache + off, page_bytes, bar);
+                  // coordinates: row bytes, dim, kv head, block
+                  tma_load_4d(sbase + (uint32_t)(PPS + u) * page_bytes, &tm_v, 0, 0, kvh, blk[u], bar);
+                }
+              }
+            } else {
+#pragma unroll
+              for (int u = 0; u < kMaxPagesPerStage; ++u) {
+                if (u < np) {
+                  const size_t off = (size_t)blk[u] * block_stride + (size_t)kvh * head_stride;
+                  bulk_g2s(sbase + (uint32_t)u * page_bytes, p.k_cache + off, page_bytes, bar);
+                  bulk_g2s(sbase + (uint32_t)(PPS + u) * page_bytes, p.v_cache + off, page_bytes, bar);
                 }
               }
             }
