@@ -605,8 +605,9 @@ def run_ours(args, ws, rank, local):
         "vs_baseline": value / ws / PAGES_GBS_SAME_WORKLOAD,
         "vs_baseline_note": "pages' asm kernel on AMD MI355X, 362.53 us/call for this workload (context only)",
         "dtype": "f16",
-        "dtype_detail": "e4m3 KV and bf16 q converted exactly to f16 for the MMAs, fp32 accumulation and "
-                        "softmax, bf16 out",
+        "dtype_detail": "f16 MMA operands: e4m3 KV converted exactly, each bf16 q row shifted by a power of two "
+                        "into f16's range (exact within 2^24 of the row's largest), probabilities as two f16 parts; "
+                        "fp32 accumulation and softmax, bf16 out",
         "data": "synthetic (seeded N(0,1) q; K/V N(0,1) quantised to e4m3 with scale 0.05; shuffled block tables)",
         "config": {"workload": cfg.name, "variant": args.variant, "num_seqs": cfg.num_seqs, "num_heads": cfg.num_heads,
                    "num_kv_heads": cfg.num_kv_heads, "head_size": cfg.head_size, "block_size": cfg.block_size,

@@ -83,9 +83,11 @@ typedef enum pda_status {
  * with logits of magnitude X, tokens whose logits differ by less than about
  * X * 2^-22 are weighted only that precisely (at X ~ 1e5, a few tenths of a
  * percent). NaN or infinite inputs give undefined output.
- * Arithmetic: e4m3 -> f16 and the shifted bf16 q -> f16 are exact; scores,
- * softmax and accumulation are fp32; the probabilities enter the PV product
- * as two f16 parts (f16(p) and f16(p - f16(p))), about 2^-22 relative.
+ * Arithmetic: e4m3 -> f16 is exact, and so is the shifted bf16 q -> f16 for
+ * every value within 2^24 of its row's largest (smaller ones round to f16's
+ * subnormal grid); scores, softmax and accumulation are fp32; the
+ * probabilities enter the PV product as two f16 parts (f16(p) and
+ * f16(p - f16(p))), about 2^-22 relative.
  *
  * max_num_blocks_per_seq is the row stride of block_tables. It is not in the
  * argument list the method states; it is required to index a [S, MB] table
