@@ -46,11 +46,12 @@ def _run_host(batch, h, pinned, stream=None):
     return out
 
 
-@pytest.mark.parametrize("S,max_len,pinned", [(8, 900, True), (200, 700, True), (60, 300, False)])
-def test_host_call_equals_device_call(S, max_len, pinned):
+@pytest.mark.parametrize("S,max_len,pinned,bs", [(8, 900, True, 16), (200, 700, True, 16), (60, 300, False, 16),
+                                                  (40, 700, True, 64), (300, 500, True, 32)])
+def test_host_call_equals_device_call(S, max_len, pinned, bs):
     lens = np.random.default_rng(S).integers(0, max_len + 1, S)
     lens[0] = 0
-    batch = workloads.make_custom(S, 32, 8, lens.tolist(), pool_factor=1.3, seed=S, device=DEV)
+    batch = workloads.make_custom(S, 32, 8, lens.tolist(), block_size=bs, pool_factor=1.3, seed=S, device=DEV)
     dev_out = U.run_cuda(batch)
     torch.cuda.synchronize()
     h = _host(batch, pinned)
@@ -58,7 +59,7 @@ def test_host_call_equals_device_call(S, max_len, pinned):
     host_out = _run_host(batch, h, pinned, stream=s)
     assert torch.equal(host_out, dev_out.cpu())
     if S <= 60:
-        U.compare(host_out, U.run_oracle(batch), "decode_host")
+        U.compare(host_out, U.run_oracle(batch), "decode_host bs=%d" % bs)
 
 
 def test_host_call_rejects_a_bad_table_and_runs_nothing():
