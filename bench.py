@@ -217,9 +217,16 @@ class ClockSampler:
                 "power_w_max": max(pw) if pw else None, "samples": len(rows), "reasons": sorted(reasons)}
 
 
+# Arm Ltd. (implementer 0x41) part numbers of server cores, as /proc/cpuinfo
+# reports them on Arm hosts that give no model name.
+ARM_PARTS = {"0xd0c": "Neoverse-N1", "0xd40": "Neoverse-V1", "0xd49": "Neoverse-N2", "0xd4f": "Neoverse-V2",
+             "0xd84": "Neoverse-V3", "0xd8e": "Neoverse-N3"}
+
+
 def host_cpu_name() -> str:
     """The host CPU model as the OS reports it (x86 'model name'; on Arm the
-    implementer/part codes when no name is given), with the online core count."""
+    core's name from its part number when no name is given), with the online
+    core count."""
     name = ""
     try:
         with open("/proc/cpuinfo") as f:
@@ -230,6 +237,8 @@ def host_cpu_name() -> str:
                     name = line.split(":", 1)[1].strip()
                     break
             if name:
+                if key == "CPU part":
+                    name = "Arm %s (part %s)" % (ARM_PARTS[name], name) if name in ARM_PARTS else "Arm part " + name
                 break
     except OSError:
         pass
