@@ -45,8 +45,16 @@ void noalloc_forget_devices();
 
 struct DeviceInfo {
   int sm_count = 0;
+  int cluster_launch = -1;                // cudaDevAttrClusterLaunch (-1: not read yet)
   int ctas_per_sm[kNumKinds][9] = {{0}};  // [instance][bs/16 (1..8)]
   bool smem_attr_set = false;
+  // co-resident clusters of n split CTAs: [instance][bs/16][n] (-1: not asked yet)
+  int max_clusters[kNumKinds][9][17];
+  DeviceInfo() {
+    for (auto& a : max_clusters)
+      for (auto& b : a)
+        for (int& c : b) c = -1;
+  }
 };
 std::mutex g_dev_mu;
 std::map<int, DeviceInfo> g_devices;
@@ -82,7 +90,8 @@ RingShape ring_shape(int bs, bool slot_scales = false, int ring_bytes = pda::kRi
   r.num_stages = (int)((uint32_t)ring_bytes / r.scale_off);  // scale rows ride on top
   if (r.num_stages < 2) r.num_stages = 2;
   size_t ring = (size_t)r.num_stages * r.stage_bytes;
-  size_t merge = (size_t)pda::kConsumerWarps * pda::kMaxGqa * (pda::kMergeStride + 2) * sizeof(float);
+  // the CTA merge area, then the cluster merge's partial
+  size_t merge = (size_t)pda::kClusterPartOff + pda::kClusterPartBytes;
   if (ring < merge) ring = merge;
   // + 1 KiB so the kernel can align the ring to 1024 bytes (128-byte swizzle).
   r.smem_bytes = ring + 2 * 8 * (size_t)r.num_stages + 16 + 1024;
@@ -276,15 +285,30 @@ bool paired_for(int gqa) { return gqa <= pda::kMaxGqa / 2; }
 template <bool kPaired>
 SplitFn split_fn_of(KernelKind k) {
   switch (k) {
-    case kPlainWide: return pda::pda_split_decode_kernel<false, false, pda::kWideCtasPerSm, kPaired>;
-    case kPlainDense: return pda::pda_split_decode_kernel<false, false, pda::kDenseCtasPerSm, kPaired>;
-    case kSlotWide: return pda::pda_split_decode_kernel<true, false, pda::kWideCtasPerSm, kPaired>;
-    case kTokenWide: return pda::pda_split_decode_kernel<false, true, pda::kWideCtasPerSm, kPaired>;
-    case kTokenDense: return pda::pda_split_decode_kernel<false, true, pda::kDenseCtasPerSm, kPaired>;
+    case kPlainWide: return pda::pda_split_decode_kernel<false, false, pda::kWideCtasPerSm, kPaired, false>;
+    case kPlainDense: return pda::pda_split_decode_kernel<false, false, pda::kDenseCtasPerSm, kPaired, false>;
+    case kSlotWide: return pda::pda_split_decode_kernel<true, false, pda::kWideCtasPerSm, kPaired, false>;
+    case kTokenWide: return pda::pda_split_decode_kernel<false, true, pda::kWideCtasPerSm, kPaired, false>;
+    case kTokenDense: return pda::pda_split_decode_kernel<false, true, pda::kDenseCtasPerSm, kPaired, false>;
     default: return nullptr;
   }
 }
-SplitFn split_fn(KernelKind k, bool paired) { return paired ? split_fn_of<true>(k) : split_fn_of<false>(k); }
+// Cluster-merging builds of the instances that run one-wave split grids
+// (none for the wide plain and token-major instances: those run only
+// multi-wave grids).
+template <bool kPaired>
+SplitFn cluster_fn_of(KernelKind k) {
+  switch (k) {
+    case kPlainDense: return pda::pda_split_decode_kernel<false, false, pda::kDenseCtasPerSm, kPaired, true>;
+    case kSlotWide: return pda::pda_split_decode_kernel<true, false, pda::kWideCtasPerSm, kPaired, true>;
+    case kTokenDense: return pda::pda_split_decode_kernel<false, true, pda::kDenseCtasPerSm, kPaired, true>;
+    default: return nullptr;
+  }
+}
+SplitFn split_fn(KernelKind k, bool paired, bool cluster = false) {
+  if (cluster) return paired ? cluster_fn_of<true>(k) : cluster_fn_of<false>(k);
+  return paired ? split_fn_of<true>(k) : split_fn_of<false>(k);
+}
 
 PersistFn persist_fn(bool token_major, bool paired) {
   if (token_major)
@@ -309,6 +333,11 @@ pda_status device_info(int dev, int bs, int* sm_count, int* ctas_per_sm, KernelK
       return PDA_ERR_CUDA;
     }
   }
+  if (di.cluster_launch < 0) {
+    int c = 0;
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrClusterLaunch, dev) != cudaSuccess) return PDA_ERR_CUDA;
+    di.cluster_launch = c ? 1 : 0;
+  }
   if (!di.smem_attr_set) {
     // Opt every instance in to the largest ring any block size uses.
     size_t mx = 0;
@@ -318,10 +347,16 @@ pda_status device_info(int dev, int bs, int* sm_count, int* ctas_per_sm, KernelK
         mx = sb > mx ? sb : mx;
       }
     for (int k = 0; k < kNumKinds; ++k)
-      for (bool paired : {false, true})
+      for (bool paired : {false, true}) {
         if (cudaFuncSetAttribute(kernel_fn((KernelKind)k, paired), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)mx) != cudaSuccess)
           return PDA_ERR_CUDA;
+        const SplitFn cf = split_fn((KernelKind)k, paired, true);
+        // clusters of up to 16 split CTAs (8 is the portable limit)
+        if (cf && (cudaFuncSetAttribute(cf, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx) != cudaSuccess ||
+                   cudaFuncSetAttribute(cf, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess))
+          return PDA_ERR_CUDA;
+      }
     di.smem_attr_set = true;
   }
   int& occ = di.ctas_per_sm[kind][bs / 16];
@@ -372,6 +407,7 @@ struct Plan {
   int nsplit;
   unsigned grid = 0;         // persistent kernel: CTAs (resident slots, at most one per unit)
   long long ordered = 0;     // persistent kernel: units handed out longest first (0: ticket order)
+  bool cluster = false;      // per-unit kernel: the splits merge inside their cluster (no merge kernel)
 };
 
 // Largest batch (in work units) whose units the persistent kernel takes in
@@ -407,12 +443,70 @@ Plan plan_from(int num_seqs, int num_kv_heads, int max_blocks, int bs, int sms, 
     const long long slots = (long long)sms * occ;
     pl.grid = (unsigned)(units < slots ? units : slots);
     pl.ordered = (units > slots && units <= kMaxOrderedUnits) ? units - slots : 0;
+  } else if (pl.nsplit >= 2 && pl.nsplit <= pda::kMaxClusterSplits) {
+    // A one-wave grid of the per-unit kernel merges each unit's splits in
+    // a cluster of nsplit CTAs, with no merge launch and no fp32 partials
+    // (GB300, us per call against the merge kernel: 19 x 4 units of 4K
+    // tokens in 8 splits 20.1 vs 21.3, 4 x 8 units of 4K in 16 splits 14.0
+    // vs 14.9, 16 x 8 units of 1K in 4 splits 12.7 vs 12.7).
+    const long long ctas = (long long)num_seqs * num_kv_heads * pl.nsplit;
+    pl.cluster = ctas <= (long long)sms * (pl.kind == wide ? occ : occ_d);
   }
   return pl;
 }
 
+// Launch attributes of a cluster-merged per-unit grid: the nsplit CTAs of
+// each unit (grid x) form one cluster. Under the default scheduling policy a
+// full wave of clusters of 8 did not fit at once (a 608-CTA batch took
+// 30.0 us instead of 21.4 us with the merge kernel); letting the hardware
+// balance the clusters' CTAs over the SMs fits them (20.1 us, GB300).
+int cluster_attrs(cudaLaunchAttribute* attr, int nsplit) {
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)nsplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
+  attr[1].val.clusterSchedulingPolicyPreference = cudaClusterSchedulingPolicyLoadBalancing;
+  return 2;
+}
+
+// Clusters of nsplit CTAs of instance kind that the device holds at once (0
+// when it cannot launch them), cached per device.
+pda_status max_active_clusters(int dev, KernelKind kind, int bs, int nsplit, int* out) {
+  *out = 0;
+  if (nsplit < 2 || nsplit > pda::kMaxClusterSplits || !split_fn(kind, false, true)) return PDA_OK;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& di = g_devices[dev];
+  int& n = di.max_clusters[kind][bs / 16][nsplit];
+  if (n < 0) {
+    n = 0;
+    if (di.cluster_launch == 1) {
+      cudaLaunchConfig_t lc = {};
+      lc.gridDim = dim3((unsigned)nsplit, 1, 1);
+      lc.blockDim = dim3(pda::kThreads);
+      lc.dynamicSmemBytes = ring_for(kind, bs).smem_bytes;
+      cudaLaunchAttribute attr[2];
+      lc.attrs = attr;
+      lc.numAttrs = (unsigned)cluster_attrs(attr, nsplit);
+      // the smaller count of the two builds
+      for (bool paired : {false, true}) {
+        int c = 0;
+        if (cudaOccupancyMaxActiveClusters(&c, split_fn(kind, paired, true), &lc) != cudaSuccess) {
+          (void)cudaGetLastError();  // not launchable this way: no clusters
+          c = 0;
+        }
+        n = paired ? (c < n ? c : n) : c;
+      }
+    }
+  }
+  *out = n;
+  return PDA_OK;
+}
+
 // Kernels one call launches under plan pl.
-int plan_launches(const Plan& pl) { return 1 + (pl.ordered > 0 ? 1 : 0) + (pl.nsplit > 1 ? 1 : 0); }
+int plan_launches(const Plan& pl) {
+  return 1 + (pl.ordered > 0 ? 1 : 0) + (pl.nsplit > 1 && !pl.cluster ? 1 : 0);
+}
 
 pda_status plan_call(int dev, int num_seqs, int num_kv_heads, int max_blocks, int bs, KernelKind wide,
                      KernelKind dense, Plan* out) {
@@ -424,6 +518,14 @@ pda_status plan_call(int dev, int num_seqs, int num_kv_heads, int max_blocks, in
     if (st != PDA_OK) return st;
   }
   *out = plan_from(num_seqs, num_kv_heads, max_blocks, bs, sms, occ, occ_d, wide, dense, g_split_override.load());
+  if (out->cluster) {
+    // Only when the device runs every cluster of the grid at once.
+    const long long ctas = (long long)num_seqs * num_kv_heads * out->nsplit;
+    int n = 0;
+    st = max_active_clusters(dev, out->kind, bs, out->nsplit, &n);
+    if (st != PDA_OK) return st;
+    out->cluster = n > 0 && (long long)n * out->nsplit >= ctas;
+  }
   return PDA_OK;
 }
 
@@ -457,7 +559,7 @@ struct WsLayout {
 
 WsLayout ws_layout(int num_seqs, int num_heads, const Plan& pl) {
   WsLayout w;
-  const size_t part = partial_bytes(num_seqs, num_heads, pl.nsplit);
+  const size_t part = pl.cluster ? 0 : partial_bytes(num_seqs, num_heads, pl.nsplit);
   if (!is_persistent(pl.kind) && part == 0) return w;
   w.order_off = kQueueBytes;
   w.part_off = w.order_off + (((size_t)pl.ordered * sizeof(int) + 255) & ~(size_t)255);
@@ -556,6 +658,7 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
   const RingShape rs = ring_for(pl.kind, block_size);
   pda::DecodeParams p;
   p.block_limit = g_block_limit.load();
+  p.cluster_merge = pl.cluster ? 1 : 0;
   p.out = out;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k_cache = static_cast<const uint8_t*>(k_cache);
@@ -563,8 +666,9 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
   p.block_tables = block_tables;
   p.seq_lens = seq_lens;
   unsigned* queue = static_cast<unsigned*>(ws);
-  p.part_o = nsplit > 1 ? reinterpret_cast<float*>(static_cast<char*>(ws) + wl.part_off) : nullptr;
-  p.part_ml = nsplit > 1 ? p.part_o + (size_t)num_seqs * num_heads * nsplit * kHeadDim : nullptr;
+  const bool partials = nsplit > 1 && !pl.cluster;
+  p.part_o = partials ? reinterpret_cast<float*>(static_cast<char*>(ws) + wl.part_off) : nullptr;
+  p.part_ml = partials ? p.part_o + (size_t)num_seqs * num_heads * nsplit * kHeadDim : nullptr;
   p.num_heads = num_heads;
   p.num_kv_heads = num_kv_heads;
   p.gqa = num_heads / num_kv_heads;
@@ -638,12 +742,18 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
     lc.blockDim = dim3(pda::kThreads);
     lc.dynamicSmemBytes = rs.smem_bytes;
     lc.stream = stream;
-    if (cudaLaunchKernelEx(&lc, split_fn(pl.kind, paired), p, mk, mv) != cudaSuccess) return PDA_ERR_CUDA;
+    cudaLaunchAttribute attr[2];
+    if (pl.cluster) {
+      lc.attrs = attr;
+      lc.numAttrs = (unsigned)cluster_attrs(attr, nsplit);
+    }
+    if (cudaLaunchKernelEx(&lc, split_fn(pl.kind, paired, pl.cluster), p, mk, mv) != cudaSuccess)
+      return PDA_ERR_CUDA;
   }
   if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
   if (eb && ea && record_profile_event(ea, stream) != cudaSuccess) return PDA_ERR_CUDA;
 
-  if (nsplit > 1) {
+  if (partials) {
     pda::MergeParams mp;
     mp.out = p.out;
     mp.part_o = p.part_o;

@@ -69,6 +69,12 @@ constexpr int kMaxPagesPerStage = kStageTokensMin / 16;  // 16-token pages; divi
 static_assert(32 % kMaxPagesPerStage == 0, "stage pages must tile a 32-entry table chunk");
 constexpr int kMaxGqa = 8;                   // MMA N dimension: query heads of a group
 constexpr int kMergeStride = kHeadDim + 4;   // padded fp32 row of the CTA merge area
+// Cluster merge (per-unit kernel, one wave, 2..kMaxClusterSplits splits):
+// each CTA keeps its merged rows [kMaxGqa][kHeadDim] and (m, l) pairs
+// [kMaxGqa][2] in shared memory right after the CTA merge area.
+constexpr int kMaxClusterSplits = 16;
+constexpr int kClusterPartOff = kConsumerWarps * kMaxGqa * (kMergeStride + 2) * 4;  // bytes
+constexpr int kClusterPartBytes = (kMaxGqa * kHeadDim + kMaxGqa * 2) * 4;
 
 // Swizzled native V pages ([128 dims][bs tokens], rows bs bytes apart): an
 // ldmatrix reads the 8 rows of dims 8j..8j+7 at one 16-byte token chunk,
@@ -132,6 +138,9 @@ struct DecodeParams {
   // Block check: nonzero = the pool size; a block id outside [0, block_limit)
   // is recorded in the status word and read as block 0.
   uint32_t block_limit = 0u;
+  // 1 when the per-unit kernel's cluster build runs with clusters of nsplit
+  // CTAs (read only by that build).
+  int cluster_merge = 0;
 };
 
 // Splits of a sequence with `pages` pages that hold at least one page (the
@@ -202,6 +211,18 @@ __device__ __forceinline__ void store_out(void* out, size_t idx, float x, int ou
   } else {
     static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(x);
   }
+}
+
+// Store lane's 4 dims of the merged row (s, h): zeros when no split held a
+// page (any == false).
+__device__ __forceinline__ void store_merged(void* out, const float* sinks, int out_fp8, float out_scale,
+                                             float v_scale, int num_heads, int s, int h, int lane, bool any, float M,
+                                             float den, const float4& acc) {
+  const float zs = sinks ? __ldg(sinks + h) * 1.4426950408889634f : -INFINITY;
+  const float r[4] = {acc.x, acc.y, acc.z, acc.w};
+  const size_t o0 = ((size_t)s * num_heads + h) * kHeadDim + 4 * lane;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) store_out(out, o0 + j, any ? finish(r[j], den, M, zs, v_scale) : 0.f, out_fp8, out_scale);
 }
 
 // Token order of the 16 MMA rows of a K tile. Row r of the QK accumulator
@@ -596,9 +617,11 @@ struct TileWorker {
 // partial (several splits). Consumer thread `tid` of kConsumerThreads.
 // vref: the slot-scale variant's reference V scale (1 otherwise). kStride:
 // the fp32 row stride of mo.
+// cpart: the cluster merge's shared-memory partial (rows, then (m, l)
+// pairs), or nullptr for fp32 partials in global memory.
 template <bool kSlotScales, int kStride, int kRows>
 __device__ __forceinline__ void reduce_store(const DecodeParams& p, const float* mo, const float* mml, int tid, int s,
-                                             int kvh, int split, float vref) {
+                                             int kvh, int split, float vref, float* cpart = nullptr) {
   const int g = p.gqa;
   const int H = p.num_heads;
   for (int i = tid; i < g * kHeadDim; i += kConsumerThreads) {
@@ -622,6 +645,13 @@ __device__ __forceinline__ void reduce_store(const DecodeParams& p, const float*
       const float zs = p.sinks ? __ldg(p.sinks + h) * 1.4426950408889634f : -INFINITY;
       const float r = finish(acc, den, M, zs, kSlotScales ? vref : p.v_scale);
       store_out(p.out, ((size_t)s * H + h) * kHeadDim + d, r, p.out_fp8, p.out_scale);
+    } else if (cpart) {
+      // The same values the global partial would hold, kept in this CTA.
+      cpart[hh * kHeadDim + d] = kSlotScales ? acc * vref : acc;
+      if (d == 0) {
+        cpart[kMaxGqa * kHeadDim + hh * 2 + 0] = M;
+        cpart[kMaxGqa * kHeadDim + hh * 2 + 1] = den;
+      }
     } else {
       // Slot-scale partials carry their own V reference (the merge then uses 1).
       const size_t prow = ((size_t)s * H + h) * p.nsplit + split;
@@ -631,6 +661,44 @@ __device__ __forceinline__ void reduce_store(const DecodeParams& p, const float*
         p.part_ml[prow * 2 + 1] = den;
       }
     }
+  }
+}
+
+// Cluster merge of a one-wave split batch. The nsplit CTAs of one (sequence,
+// kv head) unit form one thread-block cluster along x, so CTA rank = split.
+// Each has left its merged (O, m, l) rows in its own shared memory at byte
+// offset kClusterPartOff (reduce_store with cpart). After a cluster barrier,
+// consumer warp w of CTA r folds head row r + nsplit * w (nsplit >= 2 and
+// g <= 8: at most one row per warp) over the splits that hold pages, in
+// split order, with lse_fold and the merge kernel's final step, reading the
+// other CTAs' rows through distributed shared memory: the same operations on
+// the same values as the merge kernel, so the same bits. The caller's second
+// cluster barrier keeps every CTA's shared memory alive until all reads end.
+template <bool kSlotScales>
+__device__ __forceinline__ void cluster_merge_rows(const DecodeParams& p, uint32_t cpart, int s, int kvh, int split,
+                                                   int L, int warp, int lane) {
+  const int active = active_splits((L + p.block_size - 1) / p.block_size, p.nsplit);
+  constexpr int kBatch = 4;  // splits whose remote loads are in flight together
+  for (int hh = split + p.nsplit * warp; hh < p.gqa; hh += p.nsplit * kConsumerWarps) {
+    float M = -INFINITY, den = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i0 = 0; i0 < active; i0 += kBatch) {
+      float2 ml[kBatch];
+      float4 o[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        if (i0 + j < active) {
+          const uint32_t base = mapa_cluster(cpart, i0 + j);
+          ml[j] = ld_cluster_f2(base + (uint32_t)((kMaxGqa * kHeadDim + hh * 2) * 4));
+          o[j] = ld_cluster_f4(base + (uint32_t)((hh * kHeadDim + 4 * lane) * 4));
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j)
+        if (i0 + j < active) lse_fold(M, den, acc, ml[j].x, ml[j].y, o[j]);
+    }
+    store_merged(p.out, p.sinks, p.out_fp8, p.out_scale, kSlotScales ? 1.f : p.v_scale, p.num_heads, s,
+                 kvh * p.gqa + hh, lane, active > 0, M, den, acc);
   }
 }
 
@@ -650,7 +718,15 @@ __device__ __forceinline__ void reduce_store(const DecodeParams& p, const float*
 // 2 tokens x 2 dims per register, split into an even-dim and an odd-dim
 // fragment row by one byte permute. Output row gid of m-tile mt is then dim
 // 16mt + 2gid and row gid + 8 is dim 16mt + 2gid + 1.
-template <bool kSlotScales, bool kTokenMajor, int kMinCtasPerSm, bool kPaired>
+//
+// kCluster: the build launched with clusters of nsplit CTAs along x (the
+// splits of one unit, 2..kMaxClusterSplits, p.cluster_merge = 1); the splits
+// merge through distributed shared memory (cluster_merge_rows) instead of
+// fp32 partials and the merge kernel. That build reads the flag at run time:
+// with the branches folded at compile time it ran 1-3 % slower on GB300
+// (608 CTAs in clusters of 8: 20.6 against 20.0 us). The other builds fold
+// the flag to false and compile exactly as without clusters.
+template <bool kSlotScales, bool kTokenMajor, int kMinCtasPerSm, bool kPaired, bool kCluster>
 __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
     pda_split_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v) {
@@ -667,6 +743,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
   const int H = p.num_heads;
   const int g = p.gqa;
 
+  const bool cluster = kCluster && p.cluster_merge != 0;
+
   int L = __ldg(p.seq_lens + s);
   L = max(0, min(L, p.max_blocks * bs));
   const int pages = (L + bs - 1) / bs;
@@ -675,14 +753,18 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
 
   if (pg_first >= pg_end) {
     // No tokens for this split. With one split the row is all-zero output;
-    // with several, the merge kernel skips empty splits by the same rule.
+    // with several, the merge skips empty splits by the same rule. In a
+    // cluster the CTA runs on with no pages: it still merges its share of
+    // rows, and every thread takes part in both cluster barriers (its own
+    // partial is never read).
     if (p.nsplit == 1) {
       for (int i = threadIdx.x; i < g * kHeadDim; i += blockDim.x) {
         const int h = kvh * g + i / kHeadDim;
         store_out(p.out, ((size_t)s * H + h) * kHeadDim + (i % kHeadDim), 0.f, p.out_fp8, p.out_scale);
       }
     }
-    return;
+    if (!cluster) return;
+    pg_end = pg_first;
   }
 
   const int n_pages = pg_end - pg_first;
@@ -820,6 +902,11 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
         break;
       }
     }
+    if (cluster) {
+      // the producer warp's arrivals at the consumers' two cluster barriers
+      cluster_sync();
+      cluster_sync();
+    }
     return;
   }
 
@@ -885,14 +972,28 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
   // ------------------------------------------------ merge the consumer warps
   // All consumer warps are past their last ring read once they pass this
   // barrier; the abort decision is the same for all of them.
-  if (named_barrier_or(1, kConsumerThreads, *abort_flag)) return;
+  if (named_barrier_or(1, kConsumerThreads, *abort_flag)) {
+    if (cluster) {
+      // still at both cluster barriers (the merged rows are undefined then)
+      cluster_sync();
+      cluster_sync();
+    }
+    return;
+  }
 
   using Worker = decltype(w);
   float* mo = reinterpret_cast<float*>(smem);                       // [w][row][kMergeStride]
   float* mml = mo + kConsumerWarps * kMaxGqa * kMergeStride;        // [w][head][2]
   w.template store_merge<kMergeStride>(mo, mml, warp);
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
-  reduce_store<kSlotScales, kMergeStride, Worker::kMergeRows>(p, mo, mml, threadIdx.x, s, kvh, split, vref);
+  reduce_store<kSlotScales, kMergeStride, Worker::kMergeRows>(
+      p, mo, mml, threadIdx.x, s, kvh, split, vref,
+      cluster ? reinterpret_cast<float*>(smem + kClusterPartOff) : nullptr);
+  if (cluster) {
+    cluster_sync();
+    cluster_merge_rows<kSlotScales>(p, smem_u32(smem + kClusterPartOff), s, kvh, split, L, warp, lane);
+    cluster_sync();
+  }
 }
 
 // --------------------------------------------------------------------------
@@ -1352,12 +1453,7 @@ struct MergeParams {
 // Store the merged row: lane's 4 dims of row (s, h).
 __device__ __forceinline__ void merge_store(const MergeParams& p, int s, int h, int lane, bool any, float M, float den,
                                             const float4& acc) {
-  const float zs = p.sinks ? __ldg(p.sinks + h) * 1.4426950408889634f : -INFINITY;
-  const float r[4] = {acc.x, acc.y, acc.z, acc.w};
-  const size_t o0 = ((size_t)s * p.num_heads + h) * kHeadDim + 4 * lane;
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-    store_out(p.out, o0 + j, any ? finish(r[j], den, M, zs, p.v_scale) : 0.f, p.out_fp8, p.out_scale);
+  store_merged(p.out, p.sinks, p.out_fp8, p.out_scale, p.v_scale, p.num_heads, s, h, lane, any, M, den, acc);
 }
 
 __global__ void __launch_bounds__(kHeadDim) pda_merge_kernel(const MergeParams p) {

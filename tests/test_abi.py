@@ -87,7 +87,7 @@ def test_choose_splits_bounds_and_monotonicity(lib):
 
 # GB300: 152 SMs, 3 per-unit / persistent CTAs or 4 dense per-unit CTAs per SM
 @pytest.mark.parametrize("S,Hk,MB,bs,kind,splits,launches", [
-    (16, 8, 64, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 4, 2),   # 16 x 1024: one wave of 4/SM, 4 splits + merge
+    (16, 8, 64, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 4, 1),   # 16 x 1024: one wave of 4/SM, 4 splits merged in clusters
     (64, 8, 64, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 1, 1),   # 64 x 1024: 512 CTAs fit 608 slots
     (256, 8, 256, 16, pda.PDA_KERNEL_PERSISTENT, 1, 2),     # headline: order kernel + persistent
     (256, 8, 250, 16, pda.PDA_KERNEL_PERSISTENT, 1, 2),     # ragged up to 4000 tokens
@@ -98,8 +98,11 @@ def test_choose_splits_bounds_and_monotonicity(lib):
     (65535, 65535, 2, 16, pda.PDA_KERNEL_PER_UNIT, 1, 1),   # past 2^31 units: per-unit kernel
     # long contexts: a few sequences split into page ranges up to a dense wave
     (1, 8, 8192, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 76, 2),   # 1 x 128K tokens: 608 CTAs + wide merge
-    (4, 8, 2048, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 19, 2),   # 4 x 32K: > 16 splits, wide merge
-    (8, 8, 512, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 9, 2),     # 8 x 8K: 9 splits, one warp per row merge
+    (4, 8, 2048, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 19, 2),   # 4 x 32K: 19 splits (> 16 for a cluster), wide merge
+    (8, 8, 512, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 9, 1),     # 8 x 8K: 9 splits merged in clusters
+    (8, 8, 256, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 9, 1),     # 8 x 4K: the same split count
+    (19, 4, 256, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 8, 1),    # 76 units x 8 splits fill one wave: clusters of 8
+    (1, 1, 64, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 4, 1),      # 1 x 1K, one kv head: 4 splits (256 tokens each)
     (16, 8, 640, 64, pda.PDA_KERNEL_PERSISTENT, 10, 3),       # 16 x 40,960, 64-token blocks
     (8, 8, 8192, 16, pda.PDA_KERNEL_PERSISTENT, 32, 3),       # 8 x 128K
     (64, 8, 2048, 16, pda.PDA_KERNEL_PERSISTENT, 8, 3),       # 64 x 32K: 1 MiB split units

@@ -216,7 +216,11 @@ def test_side_stream_and_graph_capture():
 
 def test_workspace_growth_during_capture_is_refused():
     pda.release()
-    batch = workloads.make_custom(2, 8, 2, [2048, 2048], seed=14, device=DEV)
+    # 4 units x 32 splits: more splits than a cluster merges, so fp32 partials
+    batch = workloads.make_custom(2, 8, 2, [8192, 8192], seed=14, device=DEV)
+    cfg = batch.cfg
+    assert pda.plan_splits(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq,
+                           cfg.block_size) > 16
     s = torch.cuda.Stream()
     g = torch.cuda.CUDAGraph()
     err = None
@@ -231,6 +235,29 @@ def test_workspace_growth_during_capture_is_refused():
     assert err is not None and err.status == pda.PDA_ERR_WORKSPACE
 
 
+def test_cluster_merged_split_call_needs_no_workspace():
+    # 2 to 16 splits in one wave merge inside their clusters: no partials, so
+    # the call captures without pda_reserve and replays to the eager result.
+    pda.release()
+    batch = workloads.make_custom(2, 8, 2, [2048, 1500], seed=14, device=DEV)
+    cfg = batch.cfg
+    assert 2 <= pda.plan_splits(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq,
+                                cfg.block_size) <= 16
+    eager = U.run_cuda(batch).clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    out = torch.zeros_like(batch.q)
+    with torch.cuda.graph(g, stream=s):
+        U.run_cuda(batch, out=out, stream=s)
+    with torch.cuda.stream(s):
+        g.replay()
+    s.synchronize()
+    assert pda.workspace_info(s) == (0, 0)
+    assert torch.equal(out, eager)
+    U.compare(eager, U.run_oracle(batch), "cluster merge, no workspace")
+
+
 def test_graph_replay_after_workspace_growth():
     """A graph captured with a split call keeps its workspace address. A later,
     larger eager call on the same stream grows the workspace; the old buffer
@@ -242,7 +269,9 @@ def test_graph_replay_after_workspace_growth():
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     cfg = small.cfg
-    pda.set_split_override(4)
+    # 17 splits: more than a cluster merges, so the call keeps fp32 partials
+    # in the workspace (and so does the big batch, persistent with 17 splits)
+    pda.set_split_override(17)
     try:
         eager = U.run_cuda(small).clone()
         pda.reserve(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq, cfg.block_size,
@@ -339,14 +368,17 @@ def test_slot_scales_constant_table_matches_per_tensor():
 
 # ------------------------------------------------------------ merge kernels
 
-@pytest.mark.parametrize("S,H,Hk,splits", [(8, 32, 8, 2), (8, 32, 8, 4), (4, 40, 8, 16), (4, 64, 8, 17),
-                                            (2, 8, 1, 40)])
+@pytest.mark.parametrize("S,H,Hk,splits", [(8, 32, 8, 2), (8, 32, 8, 4), (8, 40, 8, 3), (6, 32, 8, 6), (8, 8, 8, 5),
+                                            (8, 64, 8, 8), (8, 8, 1, 7), (4, 40, 8, 9), (4, 32, 8, 13),
+                                            (4, 40, 8, 16), (4, 64, 8, 17), (2, 8, 1, 40)])
 def test_merge_kernels_match_across_kernels(S, H, Hk, splits):
-    """Up to 16 splits the merge runs one warp per row, beyond that four
-    warps per row. The per-unit kernel (pda_decode on one-wave batches) and
-    pda_decode_noalloc run the same tiles and the same merge: same split
-    count, same bits, call after call and from a graph replayed twice;
-    zero-length sequences give zeros."""
+    """One-wave batches of 2 to 16 splits merge inside each unit's cluster
+    of CTAs (one launch); more splits go through fp32 partials and the merge
+    kernel, one warp per row up to 16 splits, four warps per row beyond.
+    pda_decode_noalloc always uses the merge kernel. Both run the same tiles
+    and the same fold: same split count, same bits, call after call and
+    from a graph replayed twice; zero-length sequences, and splits left
+    without pages by short sequences, give what the oracle gives."""
     lens = [1024, 0, 517, 16, 33, 1000, 0, 257][:S]
     batch = workloads.make_custom(S, H, Hk, lens, seed=H + splits, device=DEV, max_num_blocks_per_seq=64)
     cfg = batch.cfg
@@ -355,7 +387,7 @@ def test_merge_kernels_match_across_kernels(S, H, Hk, splits):
         assert pda.plan_kernel(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq,
                                cfg.block_size) == pda.PDA_KERNEL_PER_UNIT_DENSE
         assert pda.plan_launches(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq,
-                                 cfg.block_size) == 2
+                                 cfg.block_size) == (1 if splits <= 16 else 2)
         ref = torch.empty_like(batch.q)
         pda.decode_noalloc(batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.seq_lens, cfg.scale,
                            cfg.k_scale, cfg.v_scale, out=ref)
