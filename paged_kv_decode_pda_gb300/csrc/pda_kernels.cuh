@@ -619,9 +619,67 @@ struct TileWorker {
 // the fp32 row stride of mo.
 // cpart: the cluster merge's shared-memory partial (rows, then (m, l)
 // pairs), or nullptr for fp32 partials in global memory.
-template <bool kSlotScales, int kStride, int kRows>
+template <bool kSlotScales, int kStride, int kRows, bool kUnrollRows = false>
 __device__ __forceinline__ void reduce_store(const DecodeParams& p, const float* mo, const float* mml, int tid, int s,
                                              int kvh, int split, float vref, float* cpart = nullptr) {
+  if constexpr (kUnrollRows && kRows <= kMaxGqa / 2) {
+    static_assert(kConsumerThreads == kHeadDim, "one consumer thread per dim");
+    const int g = p.gqa;
+    const int H = p.num_heads;
+    const int d = tid;
+    // Thread tid folds dim tid of head hh over the consumer warps and stores
+    // it (live: hh is a head of the group).
+    auto fold_store = [&](int hh, bool live) {
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mml[(w * kMaxGqa + hh) * 2]);
+      float acc = 0.f, den = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float mw = mml[(w * kMaxGqa + hh) * 2];
+          const float f = fast_exp2(mw - M);
+          acc += f * mo[(w * kRows + hh) * kStride + d];
+          den += f * mml[(w * kMaxGqa + hh) * 2 + 1];
+        }
+      }
+      if (!live) return;
+      const int h = kvh * g + hh;
+      if (p.nsplit == 1) {
+        const float zs = p.sinks ? __ldg(p.sinks + h) * 1.4426950408889634f : -INFINITY;
+        const float r = finish(acc, den, M, zs, kSlotScales ? vref : p.v_scale);
+        store_out(p.out, ((size_t)s * H + h) * kHeadDim + d, r, p.out_fp8, p.out_scale);
+      } else if (cpart) {
+        // The same values the global partial would hold, kept in this CTA.
+        cpart[hh * kHeadDim + d] = kSlotScales ? acc * vref : acc;
+        if (d == 0) {
+          cpart[kMaxGqa * kHeadDim + hh * 2 + 0] = M;
+          cpart[kMaxGqa * kHeadDim + hh * 2 + 1] = den;
+        }
+      } else {
+        // Slot-scale partials carry their own V reference (the merge then uses 1).
+        const size_t prow = ((size_t)s * H + h) * p.nsplit + split;
+        p.part_o[prow * kHeadDim + d] = kSlotScales ? acc * vref : acc;
+        if (d == 0) {
+          p.part_ml[prow * 2 + 0] = M;
+          p.part_ml[prow * 2 + 1] = den;
+        }
+      }
+    };
+    // Groups of at most 4 heads (paired builds) in the per-unit kernel: all
+    // 4 rows unrolled and folded unconditionally (rows past the group are
+    // merge-area memory too), so that the heads' independent load / exp2 /
+    // divide chains overlap; only the stores are guarded. The CTA merge
+    // took 0.6-1.0 us of a 16 x 1024 call (a timer trace); unrolled, GB300
+    // runs 4 x 8 units of 4K tokens in 16 splits in 13.7 against 14.1 us
+    // and 8 x 8 units of 2K in 9 splits in 12.9 against 13.2 us. Folding
+    // all 8 rows of wider groups cost the g = 5 batches 1-1.5 %, and the
+    // persistent kernel's per-unit merge lost 0.3 % on the 256 x 4096
+    // batch, so those keep the loop over the group's heads.
+#pragma unroll
+    for (int hh = 0; hh < kRows; ++hh) fold_store(hh, hh < g);
+    return;
+  }
   const int g = p.gqa;
   const int H = p.num_heads;
   for (int i = tid; i < g * kHeadDim; i += kConsumerThreads) {
@@ -986,7 +1044,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
   float* mml = mo + kConsumerWarps * kMaxGqa * kMergeStride;        // [w][head][2]
   w.template store_merge<kMergeStride>(mo, mml, warp);
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
-  reduce_store<kSlotScales, kMergeStride, Worker::kMergeRows>(
+  reduce_store<kSlotScales, kMergeStride, Worker::kMergeRows, true>(
       p, mo, mml, threadIdx.x, s, kvh, split, vref,
       cluster ? reinterpret_cast<float*>(smem + kClusterPartOff) : nullptr);
   if (cluster) {
