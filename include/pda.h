@@ -445,6 +445,20 @@ int pda_plan_launches(int num_seqs, int num_heads, int num_kv_heads, int max_num
 void pda_set_split_override(int num_splits);
 
 /*
+ * pda_set_tail_split -- tail pieces of the persistent kernel (process-wide;
+ * on by default). When a multi-wave batch hands out its units in
+ * longest-first order, the units of the last, partial round (units modulo
+ * resident CTAs, at most 1024) are cut into pieces of at least 256 tokens,
+ * at most 8 per unit, that the CTAs done with their whole units share. The
+ * last piece of a unit to finish folds the pieces' (O, m, l) in piece order
+ * and stores the unit's result, so the result of such a unit is not bitwise
+ * the whole unit's (it is the same softmax, within rounding). 0 turns the
+ * pieces off for later calls (tests that compare kernels bit for bit,
+ * measurements).
+ */
+void pda_set_tail_split(int enable);
+
+/*
  * pda_set_block_check -- device-side check of block ids for later decode
  * calls (process-wide). pda_decode, pda_decode_ex, pda_decode_slot_scales
  * and pda_decode_noalloc are not given the pool size, so a table entry

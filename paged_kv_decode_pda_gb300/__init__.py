@@ -46,6 +46,7 @@ from ._binding import (  # noqa: F401
     set_block_check,
     set_profile_events,
     set_split_override,
+    set_tail_split,
     status_string,
     bounded_wait_check,
 )

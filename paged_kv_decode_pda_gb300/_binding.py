@@ -36,6 +36,7 @@ SIGNATURES = {
     "pda_plan_launches": (_I, [_I, _I, _I, _I, _I]),
     "pda_choose_kernel": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "pda_set_split_override": (None, [_I]),
+    "pda_set_tail_split": (None, [_I]),
     "pda_set_block_check": (None, [ctypes.c_longlong]),
     "pda_reserve": (_I, [_I, _I, _I, _I, _I, _P]),
     "pda_release": (_I, []),
@@ -353,6 +354,11 @@ def plan_launches(num_seqs, num_heads, num_kv_heads, max_num_blocks_per_seq, blo
 
 def set_split_override(n: int) -> None:
     load().pda_set_split_override(int(n))
+
+
+def set_tail_split(enable: bool) -> None:
+    """``pda_set_tail_split``: tail pieces of the persistent kernel on (default) or off."""
+    load().pda_set_tail_split(1 if enable else 0)
 
 
 def set_block_check(num_blocks: int) -> None:

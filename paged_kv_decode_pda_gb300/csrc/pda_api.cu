@@ -21,6 +21,8 @@ namespace {
 using pda::kHeadDim;
 
 std::atomic<int> g_split_override{0};
+// Tail pieces of the persistent kernel (pda_set_tail_split); on by default.
+std::atomic<int> g_tail_split{1};
 // pda_set_block_check: the pool size the decode kernels check block ids
 // against (0 = no check), clamped to 2^31 (every int32 id below it).
 std::atomic<uint32_t> g_block_limit{0u};
@@ -408,12 +410,19 @@ struct Plan {
   unsigned grid = 0;         // persistent kernel: CTAs (resident slots, at most one per unit)
   long long ordered = 0;     // persistent kernel: units handed out longest first (0: ticket order)
   bool cluster = false;      // per-unit kernel: the splits merge inside their cluster (no merge kernel)
+  // persistent kernel, tail pieces (0 units: none): the last tail_units
+  // units handed out are cut into at most max_pieces pieces of at least
+  // min_piece_pages pages
+  int tail_units = 0;
+  int max_pieces = 1;
+  int min_piece_pages = 1;
 };
 
 // Largest batch (in work units) whose units the persistent kernel takes in
 // longest-first order: the order kernel is one CTA, so its time grows with
 // the units, and it must finish while the CTAs work on their first units.
 constexpr long long kMaxOrderedUnits = 16384;
+
 
 // The plan from sizes and residency alone (host only): split count with
 // the wide instance's CTAs per SM; the dense instance when that grid fits
@@ -443,6 +452,21 @@ Plan plan_from(int num_seqs, int num_kv_heads, int max_blocks, int bs, int sms, 
     const long long slots = (long long)sms * occ;
     pl.grid = (unsigned)(units < slots ? units : slots);
     pl.ordered = (units > slots && units <= kMaxOrderedUnits) ? units - slots : 0;
+    if (pl.ordered > 0 && pl.nsplit == 1) {
+      // The units of the last, partial round of hand-outs are cut into
+      // pieces that the CTAs done with their whole units share, about two
+      // pieces per CTA (GB300, 256 x 4096 tokens: the last 224 units of
+      // 2048 over 456 CTAs left half the CTAs idle for the call's last
+      // 50 us). A piece holds at least 256 tokens; the tail merge kernel
+      // folds them.
+      const long long k = units % (long long)pl.grid;
+      if (k > 0) {
+        pl.tail_units = (int)(k < pda::kOrderThreads ? k : pda::kOrderThreads);
+        const long long per = (2 * (long long)pl.grid + pl.tail_units - 1) / pl.tail_units;
+        pl.max_pieces = (int)(per < pda::kMaxTailPieces ? per : pda::kMaxTailPieces);
+        pl.min_piece_pages = (256 + bs - 1) / bs;
+      }
+    }
   } else if (pl.nsplit >= 2 && pl.nsplit <= pda::kMaxClusterSplits) {
     // A one-wave grid of the per-unit kernel merges each unit's splits in
     // a cluster of nsplit CTAs, with no merge launch and no fp32 partials
@@ -505,7 +529,7 @@ pda_status max_active_clusters(int dev, KernelKind kind, int bs, int nsplit, int
 
 // Kernels one call launches under plan pl.
 int plan_launches(const Plan& pl) {
-  return 1 + (pl.ordered > 0 ? 1 : 0) + (pl.nsplit > 1 && !pl.cluster ? 1 : 0);
+  return 1 + (pl.ordered > 0 ? 1 : 0) + (pl.nsplit > 1 && !pl.cluster ? 1 : 0) + (pl.tail_units > 0 ? 1 : 0);
 }
 
 pda_status plan_call(int dev, int num_seqs, int num_kv_heads, int max_blocks, int bs, KernelKind wide,
@@ -518,6 +542,7 @@ pda_status plan_call(int dev, int num_seqs, int num_kv_heads, int max_blocks, in
     if (st != PDA_OK) return st;
   }
   *out = plan_from(num_seqs, num_kv_heads, max_blocks, bs, sms, occ, occ_d, wide, dense, g_split_override.load());
+  if (!g_tail_split.load()) out->tail_units = 0;
   if (out->cluster) {
     // Only when the device runs every cluster of the grid at once.
     const long long ctas = (long long)num_seqs * num_kv_heads * out->nsplit;
@@ -553,16 +578,25 @@ size_t partial_bytes(int num_seqs, int num_heads, int nsplit) {
 
 struct WsLayout {
   size_t order_off = 0;
+  size_t piece_off = 0;  // tail pieces: piece table (int4 entries)
+  size_t info_off = 0;   // tail pieces: {unit, first entry, pieces} per tail unit
+  size_t rows_off = 0;   // tail pieces: (O, m, l) rows of each piece
   size_t part_off = 0;
   size_t bytes = 0;
 };
+
+size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
 
 WsLayout ws_layout(int num_seqs, int num_heads, const Plan& pl) {
   WsLayout w;
   const size_t part = pl.cluster ? 0 : partial_bytes(num_seqs, num_heads, pl.nsplit);
   if (!is_persistent(pl.kind) && part == 0) return w;
+  const size_t pieces = (size_t)pl.tail_units * (size_t)pl.max_pieces;
   w.order_off = kQueueBytes;
-  w.part_off = w.order_off + (((size_t)pl.ordered * sizeof(int) + 255) & ~(size_t)255);
+  w.piece_off = w.order_off + align256((size_t)pl.ordered * sizeof(int));
+  w.info_off = w.piece_off + align256(pieces * 4 * sizeof(int));
+  w.rows_off = w.info_off + align256((size_t)pl.tail_units * 4 * sizeof(int));
+  w.part_off = w.rows_off + align256(pieces * pda::kTailRowFloats * sizeof(float));
   w.bytes = w.part_off + part;
   return w;
 }
@@ -727,6 +761,18 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
       op.block_size = block_size;
       op.max_blocks = max_num_blocks_per_seq;
       op.max_split_pages = (max_num_blocks_per_seq + nsplit - 1) / nsplit;
+      if (pl.tail_units > 0) {
+        op.tail_units = pl.tail_units;
+        op.max_pieces = pl.max_pieces;
+        op.min_piece_pages = pl.min_piece_pages;
+        op.piece_table = reinterpret_cast<int4*>(static_cast<char*>(ws) + wl.piece_off);
+        op.tail_info = reinterpret_cast<int4*>(static_cast<char*>(ws) + wl.info_off);
+        op.num_tickets = reinterpret_cast<int*>(queue + 2);
+        p.tail_first = (unsigned)(units - pl.tail_units);
+        p.piece_table = op.piece_table;
+        p.num_tickets = op.num_tickets;
+        p.tail_rows = reinterpret_cast<float*>(static_cast<char*>(ws) + wl.rows_off);
+      }
       pda::pda_order_units_kernel<<<1, pda::kOrderThreads, 0, stream>>>(op);
       if (cudaGetLastError() != cudaSuccess) return PDA_ERR_CUDA;
       p.unit_order = op.order;
@@ -736,6 +782,31 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
       lc.numAttrs = 1;
     }
     if (cudaLaunchKernelEx(&lc, fn, p, queue, units, mk, mv) != cudaSuccess) return PDA_ERR_CUDA;
+    if (pl.tail_units > 0) {
+      // the tail merge, as the decode kernel's programmatic dependent
+      pda::TailMergeParams tp;
+      tp.m.out = out;
+      tp.m.num_heads = num_heads;
+      tp.m.v_scale = v_scale;
+      tp.m.sinks = sinks;
+      tp.m.out_fp8 = out_fp8;
+      tp.m.out_scale = out_scale;
+      tp.tail_info = reinterpret_cast<const int4*>(static_cast<char*>(ws) + wl.info_off);
+      tp.tail_rows = p.tail_rows;
+      tp.tail_units = pl.tail_units;
+      tp.num_kv_heads = num_kv_heads;
+      tp.gqa = p.gqa;
+      cudaLaunchConfig_t tc = {};
+      tc.gridDim = dim3((unsigned)((pl.tail_units * p.gqa + pda::kMergeRowsPerBlock - 1) / pda::kMergeRowsPerBlock));
+      tc.blockDim = dim3(kHeadDim);
+      tc.stream = stream;
+      cudaLaunchAttribute ta[1];
+      ta[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      ta[0].val.programmaticStreamSerializationAllowed = 1;
+      tc.attrs = ta;
+      tc.numAttrs = 1;
+      if (cudaLaunchKernelEx(&tc, pda::pda_tail_merge_kernel, tp) != cudaSuccess) return PDA_ERR_CUDA;
+    }
   } else {
     cudaLaunchConfig_t lc = {};
     lc.gridDim = grid;
@@ -838,6 +909,8 @@ int pda_choose_kernel(int num_seqs, int num_kv_heads, int max_num_blocks_per_seq
 }
 
 void pda_set_split_override(int num_splits) { g_split_override.store(num_splits > 0 ? num_splits : 0); }
+
+void pda_set_tail_split(int enable) { g_tail_split.store(enable ? 1 : 0); }
 
 void pda_set_block_check(long long num_blocks) {
   g_block_limit.store(num_blocks <= 0 ? 0u : (num_blocks >= (1LL << 31) ? (1u << 31) : (uint32_t)num_blocks));

@@ -141,7 +141,18 @@ struct DecodeParams {
   // 1 when the per-unit kernel's cluster build runs with clusters of nsplit
   // CTAs (read only by that build).
   int cluster_merge = 0;
+  // Persistent kernel, tail pieces: tickets from tail_first on take the
+  // entries {unit, piece, pieces, tail unit j} of piece_table, which the
+  // order kernel writes each call along with the ticket count (*num_tickets).
+  // A piece stores its (O, m, l) rows in tail_rows (kTailRowFloats per
+  // entry); the tail merge kernel folds each unit's pieces.
+  unsigned tail_first = 0xFFFFFFFFu;
+  const int4* piece_table = nullptr;
+  const int* num_tickets = nullptr;
+  float* tail_rows = nullptr;
 };
+constexpr int kTailRowFloats = kMaxGqa * (kHeadDim + 2);
+constexpr int kMaxTailPieces = 8;  // most pieces a tail unit is cut into
 
 // Splits of a sequence with `pages` pages that hold at least one page (the
 // others are empty: they write no partial and take no part in the merge).
@@ -1088,7 +1099,7 @@ struct StageHeader {
   int first_page;  // page index (in the sequence) of the stage's first page
   int np;          // pages in the stage (0: a zero-length sequence)
   int flags;       // kHdrFirst / kHdrLast / kHdrEnd
-  int pad;
+  int slot;        // tail piece: its piece_table entry (and tail_rows slot); -1 for a whole unit
 };
 constexpr int kHdrFirst = 1;
 constexpr int kHdrLast = 2;
@@ -1121,14 +1132,47 @@ __device__ __forceinline__ bool consumer_sync(uint32_t bar, uint32_t& phase, int
   return ok;
 }
 
+// Tail pieces (persistent kernel). tail_piece_rows: consumer thread tid
+// folds dim tid of every head of the group over the consumer warps, as
+// reduce_store does, and leaves the piece's (O, m, l) in its tail_rows slot:
+// O rows [kMaxGqa][kHeadDim], then (m, l) pairs.
+template <int kStride, int kRows>
+__device__ __forceinline__ void tail_piece_rows(const DecodeParams& p, const float* mo, const float* mml, int tid,
+                                                int slot) {
+  float* rows = p.tail_rows + (size_t)slot * kTailRowFloats;
+  const int d = tid;
+  for (int hh = 0; hh < p.gqa; ++hh) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mml[(w * kMaxGqa + hh) * 2]);
+    float acc = 0.f, den = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float mw = mml[(w * kMaxGqa + hh) * 2];
+        const float f = fast_exp2(mw - M);
+        acc += f * mo[(w * kRows + hh) * kStride + d];
+        den += f * mml[(w * kMaxGqa + hh) * 2 + 1];
+      }
+    }
+    __stcg(rows + hh * kHeadDim + d, acc);
+    if (d == 0) {
+      __stcg(rows + kMaxGqa * kHeadDim + hh * 2 + 0, M);
+      __stcg(rows + kMaxGqa * kHeadDim + hh * 2 + 1, den);
+    }
+  }
+}
+
 template <bool kTokenMajor, int kMinCtasPerSm, bool kPaired>
 __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
     pda_persistent_decode_kernel(const DecodeParams p, unsigned* queue, int num_units,
                                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   extern __shared__ __align__(128) uint8_t smem[];
   // A merge kernel launched as this grid's programmatic dependent may start
-  // its launch now; it waits for this grid's results before reading them.
-  grid_dependents_launch();
+  // its launch now (with the order kernel: once this CTA has waited for
+  // it, so that a dependent may read what the order kernel wrote); it waits
+  // for this grid's results before reading them.
+  if (p.unit_order == nullptr) grid_dependents_launch();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int bs = p.block_size;
@@ -1168,8 +1212,12 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
     bool ok = true;
     unsigned t = blockIdx.x;  // ticket
     unsigned unit = t;
+    // Tickets past the whole units (tail pieces) exist once the order
+    // kernel has counted them.
+    unsigned n_tickets = (unsigned)num_units;
+    int piece = 0, pieces = 1, slot = -1;
     bool order_ready = false;
-    while (ok && t < (unsigned)num_units) {
+    while (ok && t < n_tickets) {
       const int s = (int)(unit / (unsigned)per_seq);
       const int kvh = (int)((unit / (unsigned)p.nsplit) % (unsigned)p.num_kv_heads);
       const int split = (int)(unit % (unsigned)p.nsplit);
@@ -1178,6 +1226,14 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
       const int pages = (L + bs - 1) / bs;
       int pg_first, pg_end;
       split_range(pages, p.nsplit, split, pg_first, pg_end);
+      if (pieces > 1) {
+        // a tail piece: its share of the split's pages (never empty: the
+        // order kernel cuts only splits of at least 16 pages per piece)
+        int a, b;
+        split_range(pg_end - pg_first, pieces, piece, a, b);
+        pg_end = pg_first + b;
+        pg_first += a;
+      }
       bool skip = false;
       if (pg_first >= pg_end) {
         // An empty split writes nothing (the merge kernel skips it); a
@@ -1231,6 +1287,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
           hd->first_page = pg_first + j;
           hd->np = np;
           hd->flags = (k == 0 ? kHdrFirst : 0) | (k == n_st - 1 ? kHdrLast : 0);
+          hd->slot = slot;
           const bool with_q = (k == 0) && (np > 0);
           const uint32_t q_bytes = with_q ? (uint32_t)g * kHeadDim * 2u : 0u;
           const uint32_t bytes = 2u * page_bytes * (uint32_t)np + q_bytes;
@@ -1284,14 +1341,32 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
       if (!fetched && lane == 0) t_next = gridDim.x + atomicAdd(queue, 1u);
       t = __shfl_sync(0xffffffffu, t_next, 0);
       unit = t;
-      if (p.unit_order != nullptr && t < (unsigned)num_units) {
+      piece = 0;
+      pieces = 1;
+      slot = -1;
+      if (p.unit_order != nullptr) {
         if (!order_ready) {
           grid_dependency_wait();  // the order kernel has finished and its writes are visible
+          grid_dependents_launch();
           order_ready = true;
+          if (p.num_tickets != nullptr) {
+            unsigned n = 0;
+            if (lane == 0) n = (unsigned)__ldcg(p.num_tickets);
+            n_tickets = __shfl_sync(0xffffffffu, n, 0);
+          }
         }
-        unsigned u = 0;
-        if (lane == 0) u = (unsigned)__ldcg(p.unit_order + (t - gridDim.x));
-        unit = __shfl_sync(0xffffffffu, u, 0);
+        if (t >= p.tail_first && t < n_tickets) {
+          int4 e = make_int4(0, 0, 1, -1);
+          if (lane == 0) e = __ldcg(p.piece_table + (t - p.tail_first));
+          unit = (unsigned)__shfl_sync(0xffffffffu, e.x, 0);
+          piece = __shfl_sync(0xffffffffu, e.y, 0);
+          pieces = __shfl_sync(0xffffffffu, e.z, 0);
+          slot = pieces > 1 ? (int)(t - p.tail_first) : -1;
+        } else if (t < (unsigned)num_units) {
+          unsigned u = 0;
+          if (lane == 0) u = (unsigned)__ldcg(p.unit_order + (t - gridDim.x));
+          unit = __shfl_sync(0xffffffffu, u, 0);
+        }
       }
     }
     if (ok) {
@@ -1382,7 +1457,12 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
       constexpr int kStride = persist_merge_stride<kPaired>();
       w.template store_merge<kStride>(mo, mml, warp);
       if (!consumer_sync(cons_bar, cons_phase, lane, abort_flag)) break;
-      reduce_store<false, kStride, decltype(w)::kMergeRows>(p, mo, mml, threadIdx.x, hd.s, hd.kvh, hd.split, 1.f);
+      if (hd.slot < 0) {
+        reduce_store<false, kStride, decltype(w)::kMergeRows>(p, mo, mml, threadIdx.x, hd.s, hd.kvh, hd.split, 1.f);
+      } else {
+        // a tail piece: its (O, m, l) rows for the tail merge kernel
+        tail_piece_rows<kStride, decltype(w)::kMergeRows>(p, mo, mml, threadIdx.x, hd.slot);
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8u * stage);
@@ -1411,6 +1491,17 @@ struct OrderParams {
   int block_size;
   int max_blocks;
   int max_split_pages;  // ceil(max_blocks / nsplit): largest page count of a split
+  // Tail pieces: the last tail_units units of the order (at most
+  // kOrderThreads) are cut into pieces of at least min_piece_pages pages,
+  // at most max_pieces each, listed in piece_table (entries {unit, piece,
+  // pieces, j}); tail_info[j] = {unit, first entry, pieces};
+  // *num_tickets = units before the tail + the entries.
+  int tail_units = 0;
+  int max_pieces = 1;
+  int min_piece_pages = 1;
+  int4* piece_table = nullptr;
+  int4* tail_info = nullptr;
+  int* num_tickets = nullptr;
 };
 
 __device__ __forceinline__ int order_key(const OrderParams& p, int u) {
@@ -1464,15 +1555,127 @@ __global__ void __launch_bounds__(kOrderThreads) pda_order_units_kernel(const Or
     warp_sum[lane] = w - warp_sum[lane];  // exclusive over warps
   }
   __syncthreads();
+  const int n_order = p.num_units - p.first;
+  const int K = p.tail_units;
+  // Tail pieces: the tail is the last K positions of the order. The bucket
+  // where it starts (tb) holds units of equal page count; which of them are
+  // in the tail must not depend on the scatter's atomic order (a pieced
+  // unit's result differs in the last bits from the whole unit's), so the
+  // tail takes that bucket's units of the largest indices.
+  __shared__ int s_tb, s_tb_start, s_tb_count, s_tb_tail;
   unsigned base = warp_sum[warp] + incl - sum;
 #pragma unroll
   for (int j = 0; j < kPer; ++j) {
     count[kPer * tid + j] = base;
+    const unsigned t0 = (unsigned)(n_order - K);
+    if (K > 0 && own[j] > 0 && base <= t0 && t0 < base + own[j]) {
+      s_tb = kPer * tid + j;
+      s_tb_start = (int)base;
+      s_tb_count = (int)own[j];
+      s_tb_tail = (int)(base + own[j] - t0);
+    }
     base += own[j];
   }
   __syncthreads();
-  for (int u = p.first + tid; u < p.num_units; u += kOrderThreads)
-    p.order[atomicAdd(&count[order_key(p, u)], 1u)] = u;
+  if (K <= 0) {
+    for (int u = p.first + tid; u < p.num_units; u += kOrderThreads)
+      p.order[atomicAdd(&count[order_key(p, u)], 1u)] = u;
+    return;
+  }
+  {
+    // Units are visited in a fixed scrambled order v -> first + (v A mod n),
+    // A coprime with n: the tail takes bucket tb's last units in that order,
+    // a set spread over the sequences (tb's units in plain index order would
+    // be whole sequences, whose kv heads then run side by side: 1 % slower).
+    __shared__ int s_mult;
+    if (tid == 0) {
+      int a = n_order > 1 ? (int)(2654435761u % (unsigned)n_order) : 1;
+      for (;; ++a) {
+        if (a >= n_order) a = 1;
+        int x = a, y = n_order;
+        while (y != 0) {
+          const int r = x % y;
+          x = y;
+          y = r;
+        }
+        if (x == 1) break;
+      }
+      s_mult = a;
+    }
+    __syncthreads();
+    const int mult = s_mult;
+    const int tb = s_tb, tb_start = s_tb_start, tb_keep = s_tb_count - s_tb_tail;
+    int running = 0;  // units of bucket tb in earlier chunks (scrambled order)
+    for (int base_v = 0; base_v < n_order; base_v += kOrderThreads) {
+      const int v = base_v + tid;
+      const int u = v < n_order ? p.first + (int)(((long long)v * mult) % n_order) : p.num_units;
+      const int key = u < p.num_units ? order_key(p, u) : -1;
+      const bool in_tb = key == tb;
+      const unsigned m = __ballot_sync(0xffffffffu, in_tb);
+      if (lane == 0) warp_sum[warp] = (unsigned)__popc(m);
+      __syncthreads();
+      if (warp == 0) {
+        const unsigned c = warp_sum[lane];
+        unsigned w = c;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const unsigned v = __shfl_up_sync(0xffffffffu, w, d);
+          if (lane >= d) w += v;
+        }
+        warp_sum[lane] = w - c;  // exclusive over warps
+        if (lane == 31) s_tb_count = (int)w;  // this chunk's units of tb (s_tb_count no longer needed)
+      }
+      __syncthreads();
+      const int rank = running + (int)(warp_sum[warp] + __popc(m & ((1u << lane) - 1u)));
+      running += s_tb_count;
+      if (u < p.num_units) {
+        // tb's units past tb_keep (in index order) take the tail's start
+        const unsigned pos = (in_tb && rank >= tb_keep) ? (unsigned)(tb_start + rank)
+                                                        : atomicAdd(&count[key], 1u);
+        p.order[pos] = u;
+      }
+      __syncthreads();  // warp_sum and s_tb_count are reused by the next chunk
+    }
+  }
+
+  // ---- tail pieces: unit j of the last tail_units in the order is cut into
+  // pieces(j) = clamp(pages / min_piece_pages, 1, max_pieces); an exclusive
+  // scan places each unit's pieces side by side in piece_table, and
+  // tail_info[j] tells the tail merge kernel where they are.
+  __syncthreads();  // the order entries written above are visible to the block
+  int u = 0, pieces = 0;
+  if (tid < K) {
+    u = p.order[n_order - K + tid];
+    const int sq = u / (p.num_kv_heads * p.nsplit);
+    int L = __ldg(p.seq_lens + sq);
+    L = max(0, min(L, p.max_blocks * p.block_size));
+    int first, end;
+    split_range((L + p.block_size - 1) / p.block_size, p.nsplit, u % p.nsplit, first, end);
+    pieces = min(max(max(0, end - first) / p.min_piece_pages, 1), p.max_pieces);
+  }
+  int incl2 = pieces;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl2, d);
+    if (lane >= d) incl2 += v;
+  }
+  __shared__ int warp_pieces[kOrderThreads / 32];
+  if (lane == 31) warp_pieces[warp] = incl2;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_pieces[lane];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, w, d);
+      if (lane >= d) w += v;
+    }
+    warp_pieces[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const int before = (warp > 0 ? warp_pieces[warp - 1] : 0) + incl2 - pieces;
+  for (int i = 0; i < pieces; ++i) p.piece_table[before + i] = make_int4(u, i, pieces, tid);
+  if (tid < K) p.tail_info[tid] = make_int4(u, before, pieces, 0);
+  if (tid == 0) *p.num_tickets = p.num_units - K + warp_pieces[kOrderThreads / 32 - 1];
 }
 
 // Log-sum-exp merge of the per-split partials:
@@ -1578,6 +1781,54 @@ __global__ void __launch_bounds__(kHeadDim) pda_merge_wide_kernel(const MergePar
     D = __fmaf_rn(f, s_l[w], D);
   }
   merge_store(p, s, h, lane, active > 0, Mt, D, A);
+}
+
+// Tail merge (persistent kernel with tail pieces, one split per unit): one
+// warp per (tail unit, head) row, 4 rows per 128-thread block, launched as
+// the decode kernel's programmatic dependent. Lane l folds dims 4l .. 4l+3
+// of the unit's pieces (tail_info[j] = {unit, first entry, pieces}) in
+// piece order with lse_fold, then stores the row as the merge kernel does.
+// A unit of one piece was stored whole by the decode kernel. The decode
+// kernel lets this grid launch only after its CTAs have waited for the
+// order kernel, so tail_info can be read before waiting for the decode
+// grid itself, and rows with nothing to fold leave at once.
+struct TailMergeParams {
+  MergeParams m;         // out, sinks, output format, v_scale, num_heads
+  const int4* tail_info;
+  const float* tail_rows;
+  int tail_units;
+  int num_kv_heads;
+  int gqa;
+};
+
+__global__ void __launch_bounds__(kHeadDim) pda_tail_merge_kernel(const TailMergeParams p) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kMergeRowsPerBlock + (threadIdx.x >> 5);
+  if (row >= p.tail_units * p.gqa) return;
+  const int j = row / p.gqa;
+  const int hh = row % p.gqa;
+  const int4 e = __ldcg(p.tail_info + j);
+  if (e.z <= 1) return;
+  grid_dependency_wait();  // the decode kernel's pieces are stored and visible
+  const int s = e.x / p.num_kv_heads;
+  const int kvh = e.x % p.num_kv_heads;
+  // every piece's values first, so the loads overlap, then the fold
+  float2 ml[kMaxTailPieces];
+  float4 o[kMaxTailPieces];
+#pragma unroll
+  for (int i = 0; i < kMaxTailPieces; ++i) {
+    if (i < e.z) {
+      const float* rows = p.tail_rows + (size_t)(e.y + i) * kTailRowFloats;
+      ml[i] = __ldcg(reinterpret_cast<const float2*>(rows + kMaxGqa * kHeadDim) + hh);
+      o[i] = __ldcg(reinterpret_cast<const float4*>(rows + hh * kHeadDim) + lane);
+    }
+  }
+  float M = -INFINITY, den = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < kMaxTailPieces; ++i)
+    if (i < e.z) lse_fold(M, den, acc, ml[i].x, ml[i].y, o[i]);
+  merge_store(p.m, s, kvh * p.gqa + hh, lane, true, M, den, acc);
 }
 
 // One CTA waits on an mbarrier that nothing completes, with a short limit,

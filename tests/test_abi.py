@@ -89,12 +89,12 @@ def test_choose_splits_bounds_and_monotonicity(lib):
 @pytest.mark.parametrize("S,Hk,MB,bs,kind,splits,launches", [
     (16, 8, 64, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 4, 1),   # 16 x 1024: one wave of 4/SM, 4 splits merged in clusters
     (64, 8, 64, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 1, 1),   # 64 x 1024: 512 CTAs fit 608 slots
-    (256, 8, 256, 16, pda.PDA_KERNEL_PERSISTENT, 1, 2),     # headline: order kernel + persistent
-    (256, 8, 250, 16, pda.PDA_KERNEL_PERSISTENT, 1, 2),     # ragged up to 4000 tokens
+    (256, 8, 256, 16, pda.PDA_KERNEL_PERSISTENT, 1, 3),     # headline: order kernel + persistent + tail merge
+    (256, 8, 250, 16, pda.PDA_KERNEL_PERSISTENT, 1, 3),     # ragged up to 4000 tokens
     (128, 8, 128, 64, pda.PDA_KERNEL_PERSISTENT, 2, 3),     # 64-token blocks: + merge
     (2200, 8, 8, 16, pda.PDA_KERNEL_PERSISTENT, 1, 1),      # 17,600 units: ticket order, no order kernel
     (76, 8, 8, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 1, 1),    # 608 units: exactly one dense wave
-    (77, 8, 8, 16, pda.PDA_KERNEL_PERSISTENT, 1, 2),        # 616 units: one more than a dense wave
+    (77, 8, 8, 16, pda.PDA_KERNEL_PERSISTENT, 1, 3),        # 616 units: one more than a dense wave
     (65535, 65535, 2, 16, pda.PDA_KERNEL_PER_UNIT, 1, 1),   # past 2^31 units: per-unit kernel
     # long contexts: a few sequences split into page ranges up to a dense wave
     (1, 8, 8192, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 76, 2),   # 1 x 128K tokens: 608 CTAs + wide merge

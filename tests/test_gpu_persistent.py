@@ -73,10 +73,12 @@ def test_persistent_parity(bs, splits):
 @pytest.mark.parametrize("splits", [1, 3])
 def test_persistent_bitwise_equals_per_unit_kernel(splits):
     # pda_decode_noalloc always runs the per-unit kernel; with the same split
-    # count the per-unit arithmetic (stages, tiles, warp merge) is identical.
+    # count the per-unit arithmetic (stages, tiles, warp merge) is identical
+    # (tail pieces off: a pieced unit folds its pieces instead).
     batch = _many(200, 16, seed=7, max_len=700)
     cfg = batch.cfg
     pda.set_split_override(splits)
+    pda.set_tail_split(False)
     try:
         assert _kernel(batch) == pda.PDA_KERNEL_PERSISTENT
         a = U.run_cuda(batch)
@@ -86,6 +88,7 @@ def test_persistent_bitwise_equals_per_unit_kernel(splits):
         torch.cuda.synchronize()
     finally:
         pda.set_split_override(0)
+        pda.set_tail_split(True)
     assert torch.equal(a, b)
 
 
@@ -104,11 +107,18 @@ def test_device_plan_matches_the_pure_planner(S, Hk, MB, bs):
 
 def test_launch_counts():
     # units beyond the resident slots are handed out longest first (one more
-    # launch, up to 16384 units); a split adds the merge launch
+    # launch, up to 16384 units) and the units of the last partial round
+    # are cut into pieces that the tail merge kernel folds (one more); a
+    # split adds the merge launch instead (no pieces then)
     batch = _many(160, 16, seed=3)
     cfg = batch.cfg
     args = (cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq, cfg.block_size)
-    assert pda.plan_launches(*args) == 2
+    assert pda.plan_launches(*args) == 3
+    pda.set_tail_split(False)
+    try:
+        assert pda.plan_launches(*args) == 2
+    finally:
+        pda.set_tail_split(True)
     pda.set_split_override(3)
     try:
         assert pda.plan_launches(*args) == 3
@@ -270,3 +280,66 @@ def test_persistent_sinks_fp8_and_shuffled_v():
                           sinks=sinks.numpy())
     U.compare(a, exact, "persistent with sinks")
     U.compare_e4m3(c, exact, out_scale, "persistent e4m3 output")
+
+
+# ------------------------------------------------------------- tail pieces
+
+def _uniform(S, H, Hk, ctx, bs=16, seed=0):
+    return workloads.make_custom(S, H, Hk, [ctx] * S, block_size=bs, seed=seed, device=DEV)
+
+
+@pytest.mark.parametrize("S,H,Hk,ctx,bs,splits", [
+    (80, 32, 8, 2048, 16, 0),     # 640 units over 456 CTAs: the last 184 in 5 pieces each
+    (80, 40, 8, 1024, 16, 0),     # g = 5 (two PV passes): 64-page units in 4 pieces
+    (40, 64, 8, 2048, 64, 2),     # g = 8, 64-token blocks, 2 splits: no pieces (the merge kernel folds splits)
+    (120, 32, 8, 700, 16, 0),     # 44-page units: 2 pieces each
+    (700, 8, 1, 3000, 32, 0),     # one kv head (g = 8), 32-token blocks: 244 tail units in 4 pieces
+])
+def test_tail_pieces_parity(S, H, Hk, ctx, bs, splits):
+    """Units of the last, partial round are cut into pieces; the last piece
+    of each folds them. Parity with the oracle, agreement with the same call
+    without pieces, and the same bits call after call (the arrival counters
+    start from zero every call)."""
+    batch = _uniform(S, H, Hk, ctx, bs=bs, seed=S + H + bs)
+    cfg = batch.cfg
+    pda.set_split_override(splits)
+    try:
+        kind = _kernel(batch)
+        assert kind == pda.PDA_KERNEL_PERSISTENT
+        a = U.run_cuda(batch).clone()
+        b = U.run_cuda(batch).clone()
+        pda.set_tail_split(False)
+        c = U.run_cuda(batch).clone()
+        torch.cuda.synchronize()
+    finally:
+        pda.set_split_override(0)
+        pda.set_tail_split(True)
+    assert torch.equal(a, b), "tail pieces must be deterministic"
+    assert (a.float() - c.float()).abs().max().item() <= 4e-3
+    U.compare(a, U.run_oracle(batch), "tail pieces S=%d H=%d bs=%d splits=%d (%s)" % (S, H, bs, splits, kind))
+    assert pda.query_device_status() == 0
+
+
+def test_tail_pieces_with_sinks_e4m3_output_and_strided_caches():
+    # every persistent entry point takes the same pieces
+    batch = _uniform(80, 32, 8, 2048, seed=11)
+    assert _kernel(batch) == pda.PDA_KERNEL_PERSISTENT
+    cfg = batch.cfg
+    NB, Hk, bs = batch.num_blocks, cfg.num_kv_heads, cfg.block_size
+    g = torch.Generator().manual_seed(3)
+    sinks = (torch.randn(cfg.num_heads, generator=g) * 2).float()
+    out_scale = 0.0075
+    ex = pda.decode_ex(batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.seq_lens, cfg.scale,
+                       cfg.k_scale, cfg.v_scale, sinks=sinks.to(DEV), output_scale=out_scale)
+    kt = batch.k_cache.view(torch.uint8).permute(0, 3, 1, 2, 4).reshape(NB, bs, Hk, 128).contiguous()
+    vt = batch.v_cache.view(torch.uint8).permute(0, 3, 1, 2).contiguous()
+    st = (bs * Hk * 128, Hk * 128, 128)
+    tm = pda.decode_strided(batch.q, kt.data_ptr(), vt.data_ptr(), batch.block_tables, batch.seq_lens, cfg.scale,
+                            cfg.k_scale, cfg.v_scale, num_kv_heads=Hk, block_size=bs, num_blocks=NB,
+                            k_strides=st, v_strides=st)
+    torch.cuda.synchronize()
+    raw = batch.raw()
+    exact = oracle.decode(**raw, scale=cfg.scale, k_scale=cfg.k_scale, v_scale=cfg.v_scale, sinks=sinks.numpy())
+    U.compare_e4m3(ex, exact, out_scale, "tail pieces, sinks + e4m3 out")
+    U.compare(tm, U.run_oracle(batch), "tail pieces, token-major caches")
+    assert pda.query_device_status() == 0
