@@ -452,13 +452,13 @@ Plan plan_from(int num_seqs, int num_kv_heads, int max_blocks, int bs, int sms, 
     const long long slots = (long long)sms * occ;
     pl.grid = (unsigned)(units < slots ? units : slots);
     pl.ordered = (units > slots && units <= kMaxOrderedUnits) ? units - slots : 0;
-    if (pl.ordered > 0 && pl.nsplit == 1) {
+    if (pl.ordered > 0) {
       // The units of the last, partial round of hand-outs are cut into
       // pieces that the CTAs done with their whole units share, about two
       // pieces per CTA (GB300, 256 x 4096 tokens: the last 224 units of
       // 2048 over 456 CTAs left half the CTAs idle for the call's last
       // 50 us). A piece holds at least 256 tokens; the tail merge kernel
-      // folds them.
+      // folds them (into the split's partial with several splits).
       const long long k = units % (long long)pl.grid;
       if (k > 0) {
         pl.tail_units = (int)(k < pda::kOrderThreads ? k : pda::kOrderThreads);
@@ -791,6 +791,9 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
       tp.m.sinks = sinks;
       tp.m.out_fp8 = out_fp8;
       tp.m.out_scale = out_scale;
+      tp.m.nsplit = nsplit;
+      tp.part_o = p.part_o;
+      tp.part_ml = p.part_ml;
       tp.tail_info = reinterpret_cast<const int4*>(static_cast<char*>(ws) + wl.info_off);
       tp.tail_rows = p.tail_rows;
       tp.tail_units = pl.tail_units;

@@ -1783,17 +1783,22 @@ __global__ void __launch_bounds__(kHeadDim) pda_merge_wide_kernel(const MergePar
   merge_store(p, s, h, lane, active > 0, Mt, D, A);
 }
 
-// Tail merge (persistent kernel with tail pieces, one split per unit): one
-// warp per (tail unit, head) row, 4 rows per 128-thread block, launched as
-// the decode kernel's programmatic dependent. Lane l folds dims 4l .. 4l+3
-// of the unit's pieces (tail_info[j] = {unit, first entry, pieces}) in
-// piece order with lse_fold, then stores the row as the merge kernel does.
-// A unit of one piece was stored whole by the decode kernel. The decode
-// kernel lets this grid launch only after its CTAs have waited for the
-// order kernel, so tail_info can be read before waiting for the decode
-// grid itself, and rows with nothing to fold leave at once.
+// Tail merge (persistent kernel with tail pieces): one warp per (tail unit,
+// head) row, 4 rows per 128-thread block, launched as the decode kernel's
+// programmatic dependent. Lane l folds dims 4l .. 4l+3 of the unit's pieces
+// (tail_info[j] = {unit, first entry, pieces}) in piece order with
+// lse_fold, then stores the row as the merge kernel does (one split per
+// unit) or as the unit's split partial for the merge kernel, which is then
+// launched as this grid's dependent. A unit of one piece was stored whole
+// by the decode kernel. The decode kernel lets this grid launch only after
+// its CTAs have waited for the order kernel, so tail_info can be read
+// before waiting for the decode grid; with one split, rows with nothing to
+// fold leave at once (with several, every row waits, so that this grid
+// ends after the decode grid and the merge kernel after both).
 struct TailMergeParams {
-  MergeParams m;         // out, sinks, output format, v_scale, num_heads
+  MergeParams m;         // out, sinks, output format, v_scale, num_heads, nsplit
+  float* part_o;         // several splits: the split partials the merge kernel folds
+  float* part_ml;
   const int4* tail_info;
   const float* tail_rows;
   int tail_units;
@@ -1802,16 +1807,23 @@ struct TailMergeParams {
 };
 
 __global__ void __launch_bounds__(kHeadDim) pda_tail_merge_kernel(const TailMergeParams p) {
+  grid_dependents_launch();  // the merge kernel, if any, waits for this grid before reading
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * kMergeRowsPerBlock + (threadIdx.x >> 5);
-  if (row >= p.tail_units * p.gqa) return;
+  const int nsplit = p.m.nsplit;
+  if (row >= p.tail_units * p.gqa) {
+    if (nsplit > 1) grid_dependency_wait();
+    return;
+  }
   const int j = row / p.gqa;
   const int hh = row % p.gqa;
   const int4 e = __ldcg(p.tail_info + j);
-  if (e.z <= 1) return;
+  if (e.z <= 1 && nsplit == 1) return;
   grid_dependency_wait();  // the decode kernel's pieces are stored and visible
-  const int s = e.x / p.num_kv_heads;
-  const int kvh = e.x % p.num_kv_heads;
+  if (e.z <= 1) return;
+  const int s = e.x / (p.num_kv_heads * nsplit);
+  const int kvh = (e.x / nsplit) % p.num_kv_heads;
+  const int split = e.x % nsplit;
   // every piece's values first, so the loads overlap, then the fold
   float2 ml[kMaxTailPieces];
   float4 o[kMaxTailPieces];
@@ -1828,7 +1840,15 @@ __global__ void __launch_bounds__(kHeadDim) pda_tail_merge_kernel(const TailMerg
 #pragma unroll
   for (int i = 0; i < kMaxTailPieces; ++i)
     if (i < e.z) lse_fold(M, den, acc, ml[i].x, ml[i].y, o[i]);
-  merge_store(p.m, s, kvh * p.gqa + hh, lane, true, M, den, acc);
+  const int h = kvh * p.gqa + hh;
+  if (nsplit == 1) {
+    merge_store(p.m, s, h, lane, true, M, den, acc);
+  } else {
+    // the split's partial, as the decode kernel stores a whole split's
+    const size_t prow = ((size_t)s * p.m.num_heads + h) * nsplit + split;
+    reinterpret_cast<float4*>(p.part_o + prow * kHeadDim)[lane] = acc;
+    if (lane == 0) reinterpret_cast<float2*>(p.part_ml)[prow] = make_float2(M, den);
+  }
 }
 
 // One CTA waits on an mbarrier that nothing completes, with a short limit,

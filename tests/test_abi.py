@@ -91,7 +91,7 @@ def test_choose_splits_bounds_and_monotonicity(lib):
     (64, 8, 64, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 1, 1),   # 64 x 1024: 512 CTAs fit 608 slots
     (256, 8, 256, 16, pda.PDA_KERNEL_PERSISTENT, 1, 3),     # headline: order kernel + persistent + tail merge
     (256, 8, 250, 16, pda.PDA_KERNEL_PERSISTENT, 1, 3),     # ragged up to 4000 tokens
-    (128, 8, 128, 64, pda.PDA_KERNEL_PERSISTENT, 2, 3),     # 64-token blocks: + merge
+    (128, 8, 128, 64, pda.PDA_KERNEL_PERSISTENT, 2, 4),     # 64-token blocks: + tail merge + merge
     (2200, 8, 8, 16, pda.PDA_KERNEL_PERSISTENT, 1, 1),      # 17,600 units: ticket order, no order kernel
     (76, 8, 8, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 1, 1),    # 608 units: exactly one dense wave
     (77, 8, 8, 16, pda.PDA_KERNEL_PERSISTENT, 1, 3),        # 616 units: one more than a dense wave
@@ -103,9 +103,9 @@ def test_choose_splits_bounds_and_monotonicity(lib):
     (8, 8, 256, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 9, 1),     # 8 x 4K: the same split count
     (19, 4, 256, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 8, 1),    # 76 units x 8 splits fill one wave: clusters of 8
     (1, 1, 64, 16, pda.PDA_KERNEL_PER_UNIT_DENSE, 4, 1),      # 1 x 1K, one kv head: 4 splits (256 tokens each)
-    (16, 8, 640, 64, pda.PDA_KERNEL_PERSISTENT, 10, 3),       # 16 x 40,960, 64-token blocks
-    (8, 8, 8192, 16, pda.PDA_KERNEL_PERSISTENT, 32, 3),       # 8 x 128K
-    (64, 8, 2048, 16, pda.PDA_KERNEL_PERSISTENT, 8, 3),       # 64 x 32K: 1 MiB split units
+    (16, 8, 640, 64, pda.PDA_KERNEL_PERSISTENT, 10, 4),       # 16 x 40,960, 64-token blocks
+    (8, 8, 8192, 16, pda.PDA_KERNEL_PERSISTENT, 32, 4),       # 8 x 128K
+    (64, 8, 2048, 16, pda.PDA_KERNEL_PERSISTENT, 8, 4),       # 64 x 32K: 1 MiB split units
 ])
 def test_choose_kernel_table(lib, S, Hk, MB, bs, kind, splits, launches):
     assert pda.choose_kernel(S, Hk, MB, bs, 152, 3, 4) == (kind, splits, launches)

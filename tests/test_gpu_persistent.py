@@ -109,7 +109,7 @@ def test_launch_counts():
     # units beyond the resident slots are handed out longest first (one more
     # launch, up to 16384 units) and the units of the last partial round
     # are cut into pieces that the tail merge kernel folds (one more); a
-    # split adds the merge launch instead (no pieces then)
+    # split adds the merge launch
     batch = _many(160, 16, seed=3)
     cfg = batch.cfg
     args = (cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq, cfg.block_size)
@@ -121,7 +121,7 @@ def test_launch_counts():
         pda.set_tail_split(True)
     pda.set_split_override(3)
     try:
-        assert pda.plan_launches(*args) == 3
+        assert pda.plan_launches(*args) == 4
     finally:
         pda.set_split_override(0)
     assert pda.plan_launches(2200, 32, 8, 8, 16) == 1   # 17600 units: ticket order
@@ -214,14 +214,14 @@ def test_queue_resets_between_calls_and_graph_replays():
 
 @pytest.mark.parametrize("splits", [2, 3])
 def test_split_batch_in_a_graph_matches_eager(splits):
-    # Order kernel, persistent kernel and the merge kernel (a programmatic
-    # dependent) captured together and replayed.
+    # Order kernel, persistent kernel, the tail merge and the merge kernel
+    # (programmatic dependents) captured together and replayed.
     b = _many(180, 16, seed=90 + splits, max_len=600)
     cfg = b.cfg
     pda.set_split_override(splits)
     try:
         assert pda.plan_launches(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq,
-                                 cfg.block_size) == 3
+                                 cfg.block_size) == 4
         eager = U.run_cuda(b).clone()
         s = torch.cuda.Stream()
         pda.reserve(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq, cfg.block_size,
@@ -291,7 +291,7 @@ def _uniform(S, H, Hk, ctx, bs=16, seed=0):
 @pytest.mark.parametrize("S,H,Hk,ctx,bs,splits", [
     (80, 32, 8, 2048, 16, 0),     # 640 units over 456 CTAs: the last 184 in 5 pieces each
     (80, 40, 8, 1024, 16, 0),     # g = 5 (two PV passes): 64-page units in 4 pieces
-    (40, 64, 8, 2048, 64, 2),     # g = 8, 64-token blocks, 2 splits: no pieces (the merge kernel folds splits)
+    (40, 64, 8, 2048, 64, 2),     # g = 8, 64-token blocks, 2 splits: pieces of splits, then the merge kernel
     (120, 32, 8, 700, 16, 0),     # 44-page units: 2 pieces each
     (700, 8, 1, 3000, 32, 0),     # one kv head (g = 8), 32-token blocks: 244 tail units in 4 pieces
 ])
