@@ -448,10 +448,12 @@ void pda_set_split_override(int num_splits);
  * pda_set_tail_split -- tail pieces of the persistent kernel (process-wide;
  * on by default). When a multi-wave batch hands out its units in
  * longest-first order, the units of the last, partial round (units modulo
- * resident CTAs, at most 1024) are cut into pieces of at least 256 tokens,
- * at most 8 per unit, that the CTAs done with their whole units share. The
- * last piece of a unit to finish folds the pieces' (O, m, l) in piece order
- * and stores the unit's result, so the result of such a unit is not bitwise
+ * resident CTAs, at most 1024) that hold at least 1024 tokens are cut into
+ * pieces of at least 256 tokens, at most 8 per unit, that the CTAs done with
+ * their whole units share. A tail merge kernel, launched as the decode
+ * kernel's programmatic dependent, folds the pieces' (O, m, l) in piece
+ * order and stores the unit's result (or the split's partial, which the
+ * merge kernel then folds), so the result of such a unit is not bitwise
  * the whole unit's (it is the same softmax, within rounding). 0 turns the
  * pieces off for later calls (tests that compare kernels bit for bit,
  * measurements).

@@ -457,8 +457,9 @@ Plan plan_from(int num_seqs, int num_kv_heads, int max_blocks, int bs, int sms, 
       // pieces that the CTAs done with their whole units share, about two
       // pieces per CTA (GB300, 256 x 4096 tokens: the last 224 units of
       // 2048 over 456 CTAs left half the CTAs idle for the call's last
-      // 50 us). A piece holds at least 256 tokens; the tail merge kernel
-      // folds them (into the split's partial with several splits).
+      // 50 us). A piece holds at least 256 tokens, and units under 1024
+      // tokens stay whole; the tail merge kernel folds the pieces (into the
+      // split's partial with several splits).
       const long long k = units % (long long)pl.grid;
       if (k > 0) {
         pl.tail_units = (int)(k < pda::kOrderThreads ? k : pda::kOrderThreads);

@@ -153,6 +153,12 @@ struct DecodeParams {
 };
 constexpr int kTailRowFloats = kMaxGqa * (kHeadDim + 2);
 constexpr int kMaxTailPieces = 8;  // most pieces a tail unit is cut into
+// A tail unit is cut only when it holds at least kMinCutPieces pieces of
+// the minimum size: the tail merge kernel's fold costs about as much as a
+// CTA spends on 1024 tokens alone (GB300, 256 sequences of 1 to 4000
+// tokens: its shortest units in 2 pieces took 161.2 us per call, left
+// whole 159.0 us).
+constexpr int kMinCutPieces = 4;
 
 // Splits of a sequence with `pages` pages that hold at least one page (the
 // others are empty: they write no partial and take no part in the merge).
@@ -1492,8 +1498,8 @@ struct OrderParams {
   int max_blocks;
   int max_split_pages;  // ceil(max_blocks / nsplit): largest page count of a split
   // Tail pieces: the last tail_units units of the order (at most
-  // kOrderThreads) are cut into pieces of at least min_piece_pages pages,
-  // at most max_pieces each, listed in piece_table (entries {unit, piece,
+  // kOrderThreads) of at least kMinCutPieces * min_piece_pages pages are cut
+  // into pieces of at least min_piece_pages pages, at most max_pieces each, listed in piece_table (entries {unit, piece,
   // pieces, j}); tail_info[j] = {unit, first entry, pieces};
   // *num_tickets = units before the tail + the entries.
   int tail_units = 0;
@@ -1639,9 +1645,10 @@ __global__ void __launch_bounds__(kOrderThreads) pda_order_units_kernel(const Or
   }
 
   // ---- tail pieces: unit j of the last tail_units in the order is cut into
-  // pieces(j) = clamp(pages / min_piece_pages, 1, max_pieces); an exclusive
-  // scan places each unit's pieces side by side in piece_table, and
-  // tail_info[j] tells the tail merge kernel where they are.
+  // pieces(j) = min(pages / min_piece_pages, max_pieces) when it holds at
+  // least kMinCutPieces * min_piece_pages pages, else left whole; an
+  // exclusive scan places each unit's pieces side by side in piece_table,
+  // and tail_info[j] tells the tail merge kernel where they are.
   __syncthreads();  // the order entries written above are visible to the block
   int u = 0, pieces = 0;
   if (tid < K) {
@@ -1651,7 +1658,8 @@ __global__ void __launch_bounds__(kOrderThreads) pda_order_units_kernel(const Or
     L = max(0, min(L, p.max_blocks * p.block_size));
     int first, end;
     split_range((L + p.block_size - 1) / p.block_size, p.nsplit, u % p.nsplit, first, end);
-    pieces = min(max(max(0, end - first) / p.min_piece_pages, 1), p.max_pieces);
+    const int pages = max(0, end - first);
+    pieces = pages < kMinCutPieces * p.min_piece_pages ? 1 : min(pages / p.min_piece_pages, p.max_pieces);
   }
   int incl2 = pieces;
 #pragma unroll
