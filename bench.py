@@ -640,7 +640,8 @@ def run_ours(args, ws, rank, local):
                      "timed_span": ("the timed region's CUDA events over its %d launches of the decode kernel "
                                     "(one launch per call)" % K) if single_launch else
                                    ("profile events around the decode kernel (with the unit-order kernel that "
-                                    "precedes the persistent kernel) of each of %d calls replayed as one graph "
+                                    "precedes the persistent kernel and the tail merge kernel that follows it) "
+                                    "of each of %d calls replayed as one graph "
                                     "right after the timed region, in the same clock window; achieved uses the "
                                     "median" % ROOFLINE_CALLS),
                      "kernel_us": kern_used_us,

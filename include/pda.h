@@ -522,7 +522,9 @@ pda_status pda_query_device_status(cudaStream_t stream, int* code);
  * calls record `before` immediately before and `after` immediately after the
  * split-KV decode kernel on their stream (capturable); with the persistent
  * kernel's unit-order kernel, `before` precedes that one too (the two run
- * overlapped). NULL, NULL turns it off. Process-wide; for measurement only.
+ * overlapped), and with its tail merge kernel, `after` follows that one too
+ * (a programmatic dependent of the decode kernel). The split merge kernel
+ * stays outside. NULL, NULL turns it off. Process-wide; for measurement only.
  */
 void pda_set_profile_events(cudaEvent_t before, cudaEvent_t after);
 

@@ -419,9 +419,8 @@ struct Plan {
 };
 
 // Largest batch (in work units) whose units the persistent kernel takes in
-// longest-first order: the order kernel is one CTA, so its time grows with
-// the units, and it must finish while the CTAs work on their first units.
-constexpr long long kMaxOrderedUnits = 16384;
+// longest-first order.
+constexpr long long kMaxOrderedUnits = pda::kMaxOrderedUnits;
 
 
 // The plan from sizes and residency alone (host only): split count with
