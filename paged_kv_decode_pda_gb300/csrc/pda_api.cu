@@ -453,16 +453,21 @@ Plan plan_from(int num_seqs, int num_kv_heads, int max_blocks, int bs, int sms, 
     pl.ordered = (units > slots && units <= kMaxOrderedUnits) ? units - slots : 0;
     if (pl.ordered > 0) {
       // The units of the last, partial round of hand-outs are cut into
-      // pieces that the CTAs done with their whole units share, about two
-      // pieces per CTA (GB300, 256 x 4096 tokens: the last 224 units of
-      // 2048 over 456 CTAs left half the CTAs idle for the call's last
-      // 50 us). A piece holds at least 256 tokens, and units under 1024
-      // tokens stay whole; the tail merge kernel folds the pieces (into the
-      // split's partial with several splits).
+      // pieces that the CTAs done with their whole units share (GB300,
+      // 256 x 4096 tokens: the last 224 units of 2048 over 456 CTAs left
+      // half the CTAs idle for the call's last 50 us). A piece holds at
+      // least 256 tokens, and units under 1024 tokens stay whole; the tail
+      // merge kernel folds the pieces (into the split's partial with several
+      // splits). A tail of a third of the CTAs or more is cut into pieces
+      // that shrink toward the end (up to kMaxTailPieces), a smaller one
+      // into equal pieces, about two per CTA (the order kernel's
+      // tail_piece_count).
       const long long k = units % (long long)pl.grid;
       if (k > 0) {
         pl.tail_units = (int)(k < pda::kOrderThreads ? k : pda::kOrderThreads);
-        const long long per = (2 * (long long)pl.grid + pl.tail_units - 1) / pl.tail_units;
+        const long long per = 3LL * pl.tail_units >= (long long)pl.grid
+                                  ? pda::kMaxTailPieces
+                                  : (2 * (long long)pl.grid + pl.tail_units - 1) / pl.tail_units;
         pl.max_pieces = (int)(per < pda::kMaxTailPieces ? per : pda::kMaxTailPieces);
         pl.min_piece_pages = (256 + bs - 1) / bs;
       }

@@ -142,10 +142,11 @@ struct DecodeParams {
   // CTAs (read only by that build).
   int cluster_merge = 0;
   // Persistent kernel, tail pieces: tickets from tail_first on take the
-  // entries {unit, piece, pieces, tail unit j} of piece_table, which the
-  // order kernel writes each call along with the ticket count (*num_tickets).
-  // A piece stores its (O, m, l) rows in tail_rows (kTailRowFloats per
-  // entry); the tail merge kernel folds each unit's pieces.
+  // entries {unit, first page, end page, slot} of piece_table (pages of the
+  // unit's split; slot -1 for a whole unit), which the order kernel writes
+  // each call along with the ticket count (*num_tickets). A piece stores
+  // its (O, m, l) rows in tail_rows (kTailRowFloats per slot); the tail
+  // merge kernel folds each unit's pieces.
   unsigned tail_first = 0xFFFFFFFFu;
   const int4* piece_table = nullptr;
   const int* num_tickets = nullptr;
@@ -1105,7 +1106,7 @@ struct StageHeader {
   int first_page;  // page index (in the sequence) of the stage's first page
   int np;          // pages in the stage (0: a zero-length sequence)
   int flags;       // kHdrFirst / kHdrLast / kHdrEnd
-  int slot;        // tail piece: its piece_table entry (and tail_rows slot); -1 for a whole unit
+  int slot;        // tail piece: its tail_rows slot; -1 for a whole unit
 };
 constexpr int kHdrFirst = 1;
 constexpr int kHdrLast = 2;
@@ -1221,7 +1222,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
     // Tickets past the whole units (tail pieces) exist once the order
     // kernel has counted them.
     unsigned n_tickets = (unsigned)num_units;
-    int piece = 0, pieces = 1, slot = -1;
+    int piece_a = 0, piece_b = 0, slot = -1;
     bool order_ready = false;
     while (ok && t < n_tickets) {
       const int s = (int)(unit / (unsigned)per_seq);
@@ -1232,13 +1233,10 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
       const int pages = (L + bs - 1) / bs;
       int pg_first, pg_end;
       split_range(pages, p.nsplit, split, pg_first, pg_end);
-      if (pieces > 1) {
-        // a tail piece: its share of the split's pages (never empty: the
-        // order kernel cuts only splits of at least 16 pages per piece)
-        int a, b;
-        split_range(pg_end - pg_first, pieces, piece, a, b);
-        pg_end = pg_first + b;
-        pg_first += a;
+      if (slot >= 0) {
+        // a tail piece: pages [piece_a, piece_b) of the split (never empty)
+        pg_end = pg_first + piece_b;
+        pg_first += piece_a;
       }
       bool skip = false;
       if (pg_first >= pg_end) {
@@ -1347,8 +1345,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
       if (!fetched && lane == 0) t_next = gridDim.x + atomicAdd(queue, 1u);
       t = __shfl_sync(0xffffffffu, t_next, 0);
       unit = t;
-      piece = 0;
-      pieces = 1;
+      piece_a = piece_b = 0;
       slot = -1;
       if (p.unit_order != nullptr) {
         if (!order_ready) {
@@ -1362,12 +1359,12 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
           }
         }
         if (t >= p.tail_first && t < n_tickets) {
-          int4 e = make_int4(0, 0, 1, -1);
+          int4 e = make_int4(0, 0, 0, -1);
           if (lane == 0) e = __ldcg(p.piece_table + (t - p.tail_first));
           unit = (unsigned)__shfl_sync(0xffffffffu, e.x, 0);
-          piece = __shfl_sync(0xffffffffu, e.y, 0);
-          pieces = __shfl_sync(0xffffffffu, e.z, 0);
-          slot = pieces > 1 ? (int)(t - p.tail_first) : -1;
+          piece_a = __shfl_sync(0xffffffffu, e.y, 0);
+          piece_b = __shfl_sync(0xffffffffu, e.z, 0);
+          slot = __shfl_sync(0xffffffffu, e.w, 0);
         } else if (t < (unsigned)num_units) {
           unsigned u = 0;
           if (lane == 0) u = (unsigned)__ldcg(p.unit_order + (t - gridDim.x));
@@ -1503,9 +1500,10 @@ struct OrderParams {
   int max_split_pages;  // ceil(max_blocks / nsplit): largest page count of a split
   // Tail pieces: the last tail_units units of the order (at most
   // kOrderThreads) of at least kMinCutPieces * min_piece_pages pages are cut
-  // into pieces of at least min_piece_pages pages, at most max_pieces each, listed in piece_table (entries {unit, piece,
-  // pieces, j}); tail_info[j] = {unit, first entry, pieces};
-  // *num_tickets = units before the tail + the entries.
+  // into pieces of at least min_piece_pages pages, at most max_pieces each
+  // (tail_piece_count); piece_table lists the tickets ({unit, first page,
+  // end page, slot}, slot -1 for a whole unit), tail_info[j] = {unit, first
+  // slot, pieces}, *num_tickets = units before the tail + the entries.
   int tail_units = 0;
   int max_pieces = 1;
   int min_piece_pages = 1;
@@ -1513,6 +1511,78 @@ struct OrderParams {
   int4* tail_info = nullptr;
   int* num_tickets = nullptr;
 };
+
+// Tail pieces of a split of n pages, with K tail units on C CTAs and
+// pieces of at least m pages (at most cap; splits under kMinCutPieces * m
+// pages stay whole). When the tail fills a third of the CTAs or more, piece
+// r holds about K / C of what is left of the split and the last piece the
+// rest, so the pieces get smaller toward the end of the hand-out (tickets go
+// out piece index by piece index, over all tail units) and the CTAs finish
+// close together: GB300, 256 x 4096 tokens (K = 224 on 456 CTAs, pieces of
+// 126, 64, 32, 17 and 17 pages) took 307.9 us per call against 310.5 us
+// with 5 equal pieces, its CTAs ending within 7 us instead of 15 us. A
+// smaller tail is cut into equal pieces.
+__device__ __forceinline__ bool tail_geometric(int K, int C) { return 3 * K >= C; }
+
+__device__ __forceinline__ int tail_piece_size(int rem, int K, int C, int m) {
+  return max((int)(((long long)K * rem + C / 2) / C), m);
+}
+
+__device__ inline int tail_piece_count(int n, int K, int C, int m, int cap) {
+  if (n < kMinCutPieces * m) return 1;
+  if (!tail_geometric(K, C)) return min(n / m, cap);
+  int rem = n, P = 1;
+  while (P < cap) {
+    const int sz = tail_piece_size(rem, K, C, m);
+    if (rem - sz < m) break;
+    rem -= sz;
+    ++P;
+  }
+  return P;
+}
+
+// Pages [a, b) of piece r of the P that tail_piece_count gave.
+__device__ inline void tail_piece_range(int n, int K, int C, int m, int P, int r, int& a, int& b) {
+  if (!tail_geometric(K, C)) {
+    split_range(n, P, r, a, b);
+    return;
+  }
+  int rem = n, sz = 0;
+  for (int i = 0; i <= r; ++i) {
+    sz = i == P - 1 ? rem : tail_piece_size(rem, K, C, m);
+    if (i < r) rem -= sz;
+  }
+  a = n - rem;
+  b = a + sz;
+}
+
+// Exclusive prefix sum of v over the order kernel's block (kOrderThreads
+// threads, 32 warps); *total receives the block's sum. Uses wsum[32].
+__device__ __forceinline__ int order_block_scan(int v, int* wsum, int* total) {
+  static_assert(kOrderThreads == 32 * 32, "one warp's lanes cover the warp sums");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int x = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += x;
+  }
+  __syncthreads();  // wsum's previous readers are done
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = wsum[lane];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, w, d);
+      if (lane >= d) w += x;
+    }
+    wsum[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  *total = wsum[31];
+  return (warp > 0 ? wsum[warp - 1] : 0) + incl - v;
+}
 
 __device__ __forceinline__ int order_key(const OrderParams& p, int u) {
   const int s = u / (p.num_kv_heads * p.nsplit);
@@ -1657,12 +1727,14 @@ __global__ void __launch_bounds__(kOrderThreads) pda_order_units_kernel(const Or
   if (K <= 0) return;
 
   // ---- tail pieces: unit j of the last tail_units in the order is cut into
-  // pieces(j) = min(pages / min_piece_pages, max_pieces) when it holds at
-  // least kMinCutPieces * min_piece_pages pages, else left whole; an
-  // exclusive scan places each unit's pieces side by side in piece_table,
-  // and tail_info[j] tells the tail merge kernel where they are.
+  // tail_piece_count pieces; their rows slots sit side by side (tail_info[j]
+  // tells the tail merge kernel where), and their tickets go out piece index
+  // by piece index over the tail units, so the last tickets are the last
+  // (smallest) pieces.
   __syncthreads();  // the order entries written above are visible to the block
-  int u = 0, pieces = 0;
+  const int C = p.first;  // the persistent grid: one CTA per unit of the first round
+  const int m = p.min_piece_pages;
+  int u = 0, n = 0, P = 0;
   if (tid < K) {
     u = p.order[n_order - K + tid];
     const int sq = u / (p.num_kv_heads * p.nsplit);
@@ -1670,32 +1742,30 @@ __global__ void __launch_bounds__(kOrderThreads) pda_order_units_kernel(const Or
     L = max(0, min(L, p.max_blocks * p.block_size));
     int first, end;
     split_range((L + p.block_size - 1) / p.block_size, p.nsplit, u % p.nsplit, first, end);
-    const int pages = max(0, end - first);
-    pieces = pages < kMinCutPieces * p.min_piece_pages ? 1 : min(pages / p.min_piece_pages, p.max_pieces);
+    n = max(0, end - first);
+    P = tail_piece_count(n, K, C, m, p.max_pieces);
   }
-  int incl2 = pieces;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl2, d);
-    if (lane >= d) incl2 += v;
-  }
-  __shared__ int warp_pieces[kOrderThreads / 32];
-  if (lane == 31) warp_pieces[warp] = incl2;
-  __syncthreads();
-  if (warp == 0) {
-    int w = warp_pieces[lane];
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, w, d);
-      if (lane >= d) w += v;
+  __shared__ int scan_buf[32];
+  int total = 0;
+  const int slot0 = order_block_scan(P, scan_buf, &total);
+  if (tid < K) p.tail_info[tid] = make_int4(u, slot0, P, 0);
+  int issued = 0;  // tickets of the earlier piece indices
+  for (int r = 0; r < p.max_pieces; ++r) {
+    const int f = P > r ? 1 : 0;
+    int cnt = 0;
+    const int rank = order_block_scan(f, scan_buf, &cnt);
+    if (f) {
+      int4 e = make_int4(u, 0, 0, -1);
+      if (P > 1) {
+        tail_piece_range(n, K, C, m, P, r, e.y, e.z);
+        e.w = slot0 + r;
+      }
+      p.piece_table[issued + rank] = e;
     }
-    warp_pieces[lane] = w;  // inclusive over warps
+    issued += cnt;
+    if (cnt == 0) break;  // block-uniform
   }
-  __syncthreads();
-  const int before = (warp > 0 ? warp_pieces[warp - 1] : 0) + incl2 - pieces;
-  for (int i = 0; i < pieces; ++i) p.piece_table[before + i] = make_int4(u, i, pieces, tid);
-  if (tid < K) p.tail_info[tid] = make_int4(u, before, pieces, 0);
-  if (tid == 0) *p.num_tickets = p.num_units - K + warp_pieces[kOrderThreads / 32 - 1];
+  if (tid == 0) *p.num_tickets = p.num_units - K + issued;
 }
 
 // Log-sum-exp merge of the per-split partials:

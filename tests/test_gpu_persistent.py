@@ -289,13 +289,14 @@ def _uniform(S, H, Hk, ctx, bs=16, seed=0):
 
 
 @pytest.mark.parametrize("S,H,Hk,ctx,bs,splits,spread", [
-    (80, 32, 8, 2048, 16, 0, 0),     # 640 units over 456 CTAs: the last 184 in 5 pieces each
-    (80, 40, 8, 1024, 16, 0, 0),     # g = 5 (two PV passes): 64-page units in 4 pieces
+    (80, 32, 8, 2048, 16, 0, 0),     # 640 units over 456 CTAs: the last 184 in shrinking pieces
+    (80, 40, 8, 1024, 16, 0, 0),     # g = 5 (two PV passes): 64-page units in pieces of 26, 16 and 22 pages
     (40, 64, 8, 2048, 64, 2, 0),     # g = 8, 64-token blocks, 2 splits: pieces of splits, then the merge kernel
-    (120, 32, 8, 1100, 16, 0, 0),    # 69-page units: pieces of 18, 17, 17 and 17 pages
+    (120, 32, 8, 1100, 16, 0, 0),    # a tail of 48 units: equal pieces of 18, 17, 17 and 17 pages
+    (130, 32, 8, 2048, 16, 0, 0),    # a tail of 128 units: 8 equal pieces of 16 pages
     (120, 32, 8, 700, 16, 0, 0),     # 44-page units stay whole: the tail merge has nothing to fold
     (160, 32, 8, 900, 16, 0, 400),   # 900 to 1299 tokens: tail units on both sides of the 1024-token cut
-    (700, 8, 1, 3000, 32, 0, 0),     # one kv head (g = 8), 32-token blocks: 244 tail units in 4 pieces
+    (700, 8, 1, 3000, 32, 0, 0),     # one kv head (g = 8), 32-token blocks: 244 tail units in shrinking pieces
 ])
 def test_tail_pieces_parity(S, H, Hk, ctx, bs, splits, spread):
     """Units of the last, partial round are cut into pieces; the tail merge
