@@ -237,6 +237,23 @@ int make_v_swizzle_map(const void* v_cache, int hk, int bs, CUtensorMap* map) {
   return mode;
 }
 
+// A per-slot scale table [NB][Hk][bs] (fp32) as a 2-D tensor map of rows
+// b * Hk + h, bs floats each, for four-row gathers (box: one row). The row
+// extent is the int32 range, as the entry points are not told the pool
+// size; rows are read only where the block table points. False when the
+// driver entry point is missing or refuses the map.
+bool make_scale_row_map(const float* table, int bs, CUtensorMap* map) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)bs, (cuuint64_t)INT32_MAX};
+  const cuuint64_t strides[1] = {(cuuint64_t)bs * sizeof(float)};
+  const cuuint32_t box[2] = {(cuuint32_t)bs, 1};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(table), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The checks of sizes and scalars every decode entry point makes.
 pda_status validate_sizes(int num_seqs, int num_heads, int num_kv_heads, int head_size, int block_size,
                           int max_blocks, float scale, float k_scale, float v_scale) {
@@ -740,8 +757,19 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
   // stages carry scale rows and are not aligned for it.
   CUtensorMap vmap;
   if (!slot && !tm && !v_shuffled) p.v_swizzle = make_v_swizzle_map(v_cache, num_kv_heads, block_size, &vmap);
-  const CUtensorMap& mk = tm ? tm->k : g_no_map;
-  const CUtensorMap& mv = tm ? tm->v : (p.v_swizzle ? vmap : g_no_map);
+  // Per-slot scale rows: at 4 pages a stage each table's 4 rows in one
+  // gather, else one bulk copy per row (rows of at least 128 bytes).
+  CUtensorMap kscale_map, vscale_map;
+  if (slot) {
+    if (rs.pages_per_stage != 4)
+      p.scale_rows = pda::kScaleRowsBulk;
+    else if (make_scale_row_map(k_scales, block_size, &kscale_map) &&
+             make_scale_row_map(v_scales, block_size, &vscale_map))
+      p.scale_rows = pda::kScaleRowsGather4;
+  }
+  const bool gather = p.scale_rows == pda::kScaleRowsGather4;
+  const CUtensorMap& mk = tm ? tm->k : (gather ? kscale_map : g_no_map);
+  const CUtensorMap& mv = tm ? tm->v : (gather ? vscale_map : (p.v_swizzle ? vmap : g_no_map));
   const bool paired = paired_for(p.gqa);
   if (is_persistent(pl.kind)) {
     const int units = num_seqs * num_kv_heads * nsplit;

@@ -117,6 +117,12 @@ struct DecodeParams {
   uint32_t scale_off;           // per-slot scale rows inside a stage (slot-scale variant)
   const float* k_scales;        // [NB][Hk][bs] fp32 (slot-scale variant)
   const float* v_scales;        // [NB][Hk][bs] fp32 (slot-scale variant)
+  // Slot-scale variant: how a stage's K and V scale rows arrive.
+  // kScaleRowsGather4 (4 pages a stage): one four-row gather per table
+  // through tm_k / tm_v (2-D maps over the tables as [NB * Hk][bs] rows);
+  // kScaleRowsBulk: one bulk copy per row; kScaleRowsPieces: 16-byte
+  // cp.async pieces spread over the producer warp.
+  int scale_rows = 0;
   float logit_scale_log2;       // scale * k_scale * log2(e)  (scale * log2(e) with slot scales)
   float v_scale;                // per-tensor V scale (unused with slot scales)
   int v_shuffled = 0;           // 1: V pages are [bs/16][D][16] (AITER shuffled), else [D][bs]
@@ -153,6 +159,9 @@ struct DecodeParams {
   float* tail_rows = nullptr;
 };
 constexpr int kTailRowFloats = kMaxGqa * (kHeadDim + 2);
+constexpr int kScaleRowsPieces = 0;
+constexpr int kScaleRowsGather4 = 1;
+constexpr int kScaleRowsBulk = 2;
 constexpr int kMaxTailPieces = 8;  // most pieces a tail unit is cut into
 // A tail unit is cut only when it holds at least kMinCutPieces pieces of
 // the minimum size: the tail merge kernel's fold costs about as much as a
@@ -860,8 +869,9 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
-      // slot scales: one more arrival per producer lane (its scale copies)
-      mbar_init(full0 + 8u * i, kSlotScales ? 33u : 1u);
+      // slot scales by cp.async: one more arrival per producer lane (its
+      // scale copies)
+      mbar_init(full0 + 8u * i, (kSlotScales && p.scale_rows == kScaleRowsPieces) ? 33u : 1u);
       mbar_init(empty0 + 8u * i, kConsumerWarps);
     }
     *abort_flag = 0;
@@ -903,7 +913,36 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
         if (lane == 0) {
           const uint32_t sbase = ring_u32 + (uint32_t)stage * p.stage_bytes;
           const uint32_t bar = full0 + 8u * stage;
-          mbar_arrive_expect_tx(bar, 2u * page_bytes * (uint32_t)np);
+          const uint32_t row_bytes = (uint32_t)bs * 4u;
+          uint32_t scale_tx = 0u;
+          if (kSlotScales && p.scale_rows == kScaleRowsGather4) scale_tx = 2u * 4u * row_bytes;
+          if (kSlotScales && p.scale_rows == kScaleRowsBulk) scale_tx = 2u * (uint32_t)np * row_bytes;
+          mbar_arrive_expect_tx(bar, 2u * page_bytes * (uint32_t)np + scale_tx);
+          if constexpr (kSlotScales) {
+            // K rows at scale_off, V rows PPS rows further; row of page t:
+            // b * Hk + kvh of its table
+            const int Hk = p.num_kv_heads;
+            const uint32_t sc = sbase + p.scale_off;
+            if (p.scale_rows == kScaleRowsGather4) {
+              // a stage of fewer than 4 pages repeats its first row (the
+              // extra rows go unread)
+              const int r0 = blk[0] * Hk + kvh;
+              const int r1 = np > 1 ? blk[1] * Hk + kvh : r0;
+              const int r2 = np > 2 ? blk[2] * Hk + kvh : r0;
+              const int r3 = np > 3 ? blk[3] * Hk + kvh : r0;
+              tma_gather4_rows(sc, &tm_k, r0, r1, r2, r3, bar);
+              tma_gather4_rows(sc + 4u * row_bytes, &tm_v, r0, r1, r2, r3, bar);
+            } else if (p.scale_rows == kScaleRowsBulk) {
+#pragma unroll
+              for (int t = 0; t < kMaxPagesPerStage; ++t) {
+                if (t < np) {
+                  const size_t off = ((size_t)blk[t] * Hk + kvh) * (size_t)bs;
+                  bulk_g2s(sc + (uint32_t)t * row_bytes, p.k_scales + off, row_bytes, bar);
+                  bulk_g2s(sc + (uint32_t)(PPS + t) * row_bytes, p.v_scales + off, row_bytes, bar);
+                }
+              }
+            }
+          }
           if constexpr (kTokenMajor) {
 #pragma unroll
             for (int t = 0; t < kMaxPagesPerStage; ++t) {
@@ -942,7 +981,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
             }
           }
         }
-        if constexpr (kSlotScales) {
+        if (kSlotScales && p.scale_rows == kScaleRowsPieces) {
           // The stage's K and V scale rows (np pages x bs floats each) as
           // 16-byte cp.async pieces spread over the warp: tiny rows would
           // cost a bulk-copy operation each. Every lane then arrives once on
