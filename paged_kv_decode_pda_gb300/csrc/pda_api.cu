@@ -254,6 +254,21 @@ bool make_scale_row_map(const float* table, int bs, CUtensorMap* map) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A page-major cache of 16-token pages ([NB][Hk] pages of 2 KiB) as a 2-D
+// tensor map of rows b * Hk + h, one page each (256 8-byte elements), for
+// four-page gathers (box: one row). Row extent as in make_scale_row_map.
+bool make_page_row_map(const void* cache, CUtensorMap* map) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)(kHeadDim * 16 / 8), (cuuint64_t)INT32_MAX};
+  const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 16};
+  const cuuint32_t box[2] = {(cuuint32_t)(kHeadDim * 16 / 8), 1};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(cache), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The checks of sizes and scalars every decode entry point makes.
 pda_status validate_sizes(int num_seqs, int num_heads, int num_kv_heads, int head_size, int block_size,
                           int max_blocks, float scale, float k_scale, float v_scale) {
@@ -767,9 +782,23 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
              make_scale_row_map(v_scales, block_size, &vscale_map))
       p.scale_rows = pda::kScaleRowsGather4;
   }
-  const bool gather = p.scale_rows == pda::kScaleRowsGather4;
-  const CUtensorMap& mk = tm ? tm->k : (gather ? kscale_map : g_no_map);
-  const CUtensorMap& mv = tm ? tm->v : (gather ? vscale_map : (p.v_swizzle ? vmap : g_no_map));
+  // Persistent kernel, page-major 16-token pages: a stage's 4 pages of
+  // each cache in one gather.
+  CUtensorMap kpage_map, vpage_map;
+  if (is_persistent(pl.kind) && !slot && !tm && rs.pages_per_stage == 4 && block_size == 16 &&
+      make_page_row_map(k_cache, &kpage_map) && make_page_row_map(v_cache, &vpage_map))
+    p.page_gather = 1;
+  const CUtensorMap* maps_k = &g_no_map;
+  const CUtensorMap* maps_v = p.v_swizzle ? &vmap : &g_no_map;
+  if (p.scale_rows == pda::kScaleRowsGather4) {
+    maps_k = &kscale_map;
+    maps_v = &vscale_map;
+  } else if (p.page_gather) {
+    maps_k = &kpage_map;
+    maps_v = &vpage_map;
+  }
+  const CUtensorMap& mk = tm ? tm->k : *maps_k;
+  const CUtensorMap& mv = tm ? tm->v : *maps_v;
   const bool paired = paired_for(p.gqa);
   if (is_persistent(pl.kind)) {
     const int units = num_seqs * num_kv_heads * nsplit;

@@ -123,6 +123,11 @@ struct DecodeParams {
   // kScaleRowsBulk: one bulk copy per row; kScaleRowsPieces: 16-byte
   // cp.async pieces spread over the producer warp.
   int scale_rows = 0;
+  // Persistent kernel, page-major 16-token pages (4 a stage): 1 = a stage's
+  // 4 K pages and 4 V pages arrive as one four-row gather each through
+  // tm_k / tm_v (2-D maps over the caches as [NB * Hk] rows of one 2 KiB
+  // page); 0 = one bulk copy per page.
+  int page_gather = 0;
   float logit_scale_log2;       // scale * k_scale * log2(e)  (scale * log2(e) with slot scales)
   float v_scale;                // per-tensor V scale (unused with slot scales)
   int v_shuffled = 0;           // 1: V pages are [bs/16][D][16] (AITER shuffled), else [D][bs]
@@ -162,6 +167,15 @@ constexpr int kTailRowFloats = kMaxGqa * (kHeadDim + 2);
 constexpr int kScaleRowsPieces = 0;
 constexpr int kScaleRowsGather4 = 1;
 constexpr int kScaleRowsBulk = 2;
+
+// The rows b * Hk + kvh of a stage's np (1..4) pages in a table or cache
+// viewed as [NB * Hk] rows, for a four-row gather; rows past np repeat the
+// first (the gather lands them in the stage's unused page slots).
+__device__ __forceinline__ int4 stage_rows(const int* blk, int np, int Hk, int kvh) {
+  const int r0 = blk[0] * Hk + kvh;
+  return make_int4(r0, np > 1 ? blk[1] * Hk + kvh : r0, np > 2 ? blk[2] * Hk + kvh : r0,
+                   np > 3 ? blk[3] * Hk + kvh : r0);
+}
 constexpr int kMaxTailPieces = 8;  // most pieces a tail unit is cut into
 // A tail unit is cut only when it holds at least kMinCutPieces pieces of
 // the minimum size: the tail merge kernel's fold costs about as much as a
@@ -924,14 +938,9 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
             const int Hk = p.num_kv_heads;
             const uint32_t sc = sbase + p.scale_off;
             if (p.scale_rows == kScaleRowsGather4) {
-              // a stage of fewer than 4 pages repeats its first row (the
-              // extra rows go unread)
-              const int r0 = blk[0] * Hk + kvh;
-              const int r1 = np > 1 ? blk[1] * Hk + kvh : r0;
-              const int r2 = np > 2 ? blk[2] * Hk + kvh : r0;
-              const int r3 = np > 3 ? blk[3] * Hk + kvh : r0;
-              tma_gather4_rows(sc, &tm_k, r0, r1, r2, r3, bar);
-              tma_gather4_rows(sc + 4u * row_bytes, &tm_v, r0, r1, r2, r3, bar);
+              const int4 r = stage_rows(blk, np, Hk, kvh);
+              tma_gather4_rows(sc, &tm_k, r.x, r.y, r.z, r.w, bar);
+              tma_gather4_rows(sc + 4u * row_bytes, &tm_v, r.x, r.y, r.z, r.w, bar);
             } else if (p.scale_rows == kScaleRowsBulk) {
 #pragma unroll
               for (int t = 0; t < kMaxPagesPerStage; ++t) {
@@ -1333,7 +1342,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
           hd->slot = slot;
           const bool with_q = (k == 0) && (np > 0);
           const uint32_t q_bytes = with_q ? (uint32_t)g * kHeadDim * 2u : 0u;
-          const uint32_t bytes = 2u * page_bytes * (uint32_t)np + q_bytes;
+          // a four-row gather always lands 4 pages per table
+          const uint32_t bytes = 2u * page_bytes * (uint32_t)(p.page_gather && np > 0 ? 4 : np) + q_bytes;
           if (bytes == 0) {
             mbar_arrive(bar);  // release-orders the header for the consumers
           } else {
@@ -1365,6 +1375,17 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
                   // coordinates: row bytes, dim, kv head, block
                   tma_load_4d(sbase + (uint32_t)(PPS + u) * page_bytes, &tm_v, 0, 0, kvh, blk[u], bar);
                 }
+              }
+            } else if (p.page_gather) {
+              // 16-token pages: two copies a stage instead of eight (GB300,
+              // us per call: 256 x 4096 tokens 309.1 against 311.4, 256 x
+              // 1-4000 tokens 155.6 against 158.3; the one-wave per-unit
+              // kernel gained nothing from it: 16 x 1024 tokens 12.77
+              // against 12.64)
+              if (np > 0) {
+                const int4 r = stage_rows(blk, np, p.num_kv_heads, kvh);
+                tma_gather4_rows(sbase, &tm_k, r.x, r.y, r.z, r.w, bar);
+                tma_gather4_rows(sbase + (uint32_t)PPS * page_bytes, &tm_v, r.x, r.y, r.z, r.w, bar);
               }
             } else {
 #pragma unroll
