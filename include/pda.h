@@ -461,6 +461,20 @@ void pda_set_split_override(int num_splits);
 void pda_set_tail_split(int enable);
 
 /*
+ * pda_set_tma_gather -- four-row TMA gathers (process-wide; on by default).
+ * With 16-token blocks the persistent decode kernel copies a stage's four
+ * K pages and four V pages as one tile::gather4 copy per cache, and the
+ * per-slot-scale entry point (pda_decode_slot_scales) a stage's four K and
+ * four V scale rows as one gather per table (larger blocks: one bulk copy
+ * per scale row). 0 copies pages one bulk copy each and scale rows as
+ * 16-byte cp.async pieces, for later calls. The same bytes arrive either
+ * way, so results are bitwise equal; for tests and measurements. No
+ * counterpart in the pages (a copy strategy, not part of what the
+ * operation computes).
+ */
+void pda_set_tma_gather(int enable);
+
+/*
  * pda_set_block_check -- device-side check of block ids for later decode
  * calls (process-wide). pda_decode, pda_decode_ex, pda_decode_slot_scales
  * and pda_decode_noalloc are not given the pool size, so a table entry

@@ -47,6 +47,7 @@ from ._binding import (  # noqa: F401
     set_profile_events,
     set_split_override,
     set_tail_split,
+    set_tma_gather,
     status_string,
     bounded_wait_check,
 )

@@ -37,6 +37,7 @@ SIGNATURES = {
     "pda_choose_kernel": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "pda_set_split_override": (None, [_I]),
     "pda_set_tail_split": (None, [_I]),
+    "pda_set_tma_gather": (None, [_I]),
     "pda_set_block_check": (None, [ctypes.c_longlong]),
     "pda_reserve": (_I, [_I, _I, _I, _I, _I, _P]),
     "pda_release": (_I, []),
@@ -359,6 +360,11 @@ def set_split_override(n: int) -> None:
 def set_tail_split(enable: bool) -> None:
     """``pda_set_tail_split``: tail pieces of the persistent kernel on (default) or off."""
     load().pda_set_tail_split(1 if enable else 0)
+
+
+def set_tma_gather(enable: bool) -> None:
+    """``pda_set_tma_gather``: four-row TMA gathers of pages and scale rows on (default) or off."""
+    load().pda_set_tma_gather(1 if enable else 0)
 
 
 def set_block_check(num_blocks: int) -> None:

@@ -23,6 +23,9 @@ using pda::kHeadDim;
 std::atomic<int> g_split_override{0};
 // Tail pieces of the persistent kernel (pda_set_tail_split); on by default.
 std::atomic<int> g_tail_split{1};
+// Four-row TMA gathers of scale rows and 16-token pages (pda_set_tma_gather);
+// on by default.
+std::atomic<int> g_tma_gather{1};
 // pda_set_block_check: the pool size the decode kernels check block ids
 // against (0 = no check), clamped to 2^31 (every int32 id below it).
 std::atomic<uint32_t> g_block_limit{0u};
@@ -775,7 +778,8 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
   // Per-slot scale rows: at 4 pages a stage each table's 4 rows in one
   // gather, else one bulk copy per row (rows of at least 128 bytes).
   CUtensorMap kscale_map, vscale_map;
-  if (slot) {
+  const bool gathers = g_tma_gather.load() != 0;
+  if (slot && gathers) {
     if (rs.pages_per_stage != 4)
       p.scale_rows = pda::kScaleRowsBulk;
     else if (make_scale_row_map(k_scales, block_size, &kscale_map) &&
@@ -785,7 +789,7 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
   // Persistent kernel, page-major 16-token pages: a stage's 4 pages of
   // each cache in one gather.
   CUtensorMap kpage_map, vpage_map;
-  if (is_persistent(pl.kind) && !slot && !tm && rs.pages_per_stage == 4 && block_size == 16 &&
+  if (gathers && is_persistent(pl.kind) && !slot && !tm && rs.pages_per_stage == 4 && block_size == 16 &&
       make_page_row_map(k_cache, &kpage_map) && make_page_row_map(v_cache, &vpage_map))
     p.page_gather = 1;
   const CUtensorMap* maps_k = &g_no_map;
@@ -976,6 +980,8 @@ int pda_choose_kernel(int num_seqs, int num_kv_heads, int max_num_blocks_per_seq
 void pda_set_split_override(int num_splits) { g_split_override.store(num_splits > 0 ? num_splits : 0); }
 
 void pda_set_tail_split(int enable) { g_tail_split.store(enable ? 1 : 0); }
+
+void pda_set_tma_gather(int enable) { g_tma_gather.store(enable ? 1 : 0); }
 
 void pda_set_block_check(long long num_blocks) {
   g_block_limit.store(num_blocks <= 0 ? 0u : (num_blocks >= (1LL << 31) ? (1u << 31) : (uint32_t)num_blocks));

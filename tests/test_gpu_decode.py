@@ -353,6 +353,34 @@ def test_slot_scales_parity(bs, splits):
     U.compare(out, ref, "slot scales bs=%d" % bs)
 
 
+@pytest.mark.parametrize("bs", [16, 32, 64, 128])
+def test_slot_scale_row_gathers_bitwise_equal_to_pieces(bs):
+    """Scale rows arrive as four-row gathers (16-token blocks) or one bulk
+    copy per row (larger blocks), or, with the gathers off, as 16-byte
+    cp.async pieces: the same bytes, so the same bits. Ragged lengths give
+    last stages of fewer pages than a stage holds."""
+    lens = [1, 15, 17, 63, 65, 200, 333, 1000, 0, 48]
+    batch = workloads.make_custom(len(lens), 32, 8, lens, block_size=bs, pool_factor=1.3, seed=40 + bs, device=DEV)
+    NB, Hk = batch.num_blocks, 8
+    g = torch.Generator(device=DEV).manual_seed(6)
+    ks = (torch.rand(NB, Hk, bs, generator=g, device=DEV) * 0.02 + 0.04).float()
+    vs = (torch.rand(NB, Hk, bs, generator=g, device=DEV) * 0.02 + 0.04).float()
+
+    def call():
+        return pda.decode_slot_scales(batch.q, batch.k_cache, batch.v_cache, ks, vs, batch.block_tables,
+                                      batch.seq_lens, batch.cfg.scale)
+
+    a = call().clone()
+    pda.set_tma_gather(False)
+    try:
+        b = call().clone()
+        torch.cuda.synchronize()
+    finally:
+        pda.set_tma_gather(True)
+    assert torch.equal(a, b)
+    assert pda.query_device_status() == 0
+
+
 def test_slot_scales_constant_table_matches_per_tensor():
     batch = workloads.make_custom(4, 40, 8, [100, 1000, 7, 513], seed=33, device=DEV)
     NB, Hk, bs = batch.num_blocks, 8, 16

@@ -326,6 +326,38 @@ def test_tail_pieces_parity(S, H, Hk, ctx, bs, splits, spread):
     assert pda.query_device_status() == 0
 
 
+@pytest.mark.parametrize("S,splits,shuffled", [(160, 0, False), (160, 2, False), (700, 0, True)])
+def test_page_gathers_bitwise_equal_to_page_copies(S, splits, shuffled):
+    """16-token pages reach the persistent kernel's stages as four-page
+    gathers or as one bulk copy per page: the same bytes, so the same bits.
+    Ragged lengths give last stages of 1 to 3 pages (the gather repeats the
+    first row into the unused slots), empty and one-token sequences."""
+    batch = _many(S, 16, seed=300 + S + splits, max_len=700)
+    cfg = batch.cfg
+    assert _kernel(batch) == pda.PDA_KERNEL_PERSISTENT
+    v = batch.v_cache
+    if shuffled:  # [NB, Hk, bs/16, 128, 16]: the same values (bitwise the same outputs)
+        NB, Hk, D, bs = v.shape
+        v = v.reshape(NB, Hk, D, bs // 16, 16).permute(0, 1, 3, 2, 4).contiguous()
+
+    def call():
+        return pda.decode_ex(batch.q, batch.k_cache, v, batch.block_tables, batch.seq_lens, cfg.scale,
+                             cfg.k_scale, cfg.v_scale, v_shuffled=shuffled)
+
+    pda.set_split_override(splits)
+    try:
+        a = call().clone()
+        pda.set_tma_gather(False)
+        b = call().clone()
+        torch.cuda.synchronize()
+    finally:
+        pda.set_tma_gather(True)
+        pda.set_split_override(0)
+    assert torch.equal(a, b)
+    U.compare(a, U.run_oracle(batch), "page gathers S=%d splits=%d shuffled=%d" % (S, splits, shuffled))
+    assert pda.query_device_status() == 0
+
+
 def test_tail_pieces_with_sinks_e4m3_output_and_strided_caches():
     # every persistent entry point takes the same pieces
     batch = _uniform(80, 32, 8, 2048, seed=11)
