@@ -301,10 +301,12 @@ def run_ours(args, ws, rank, local):
     if args.variant != "slot_scales":   # token-major caches plan like page-major ones
         kernels_per_call = pda.plan_launches(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads,
                                              cfg.max_num_blocks_per_seq, cfg.block_size)
-    else:   # per-unit kernel (+ merge)
-        kernels_per_call = 1 + (1 if nsplit > 1 else 0)
-    kernel_kind = pda.KERNEL_NAMES[pda.plan_kernel(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads,
-                                                   cfg.max_num_blocks_per_seq, cfg.block_size)]
+        kernel_id = pda.plan_kernel(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq,
+                                    cfg.block_size)
+    else:   # the per-slot-scale entry point plans for itself
+        kernel_id, nsplit, kernels_per_call = pda.plan_slot_scales(
+            cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq, cfg.block_size)
+    kernel_kind = pda.KERNEL_NAMES[kernel_id]
     stream = torch.cuda.Stream(device=dev)
     out = torch.empty_like(batch.q)
     pda.reserve(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.max_num_blocks_per_seq, cfg.block_size,
@@ -626,7 +628,7 @@ def run_ours(args, ws, rank, local):
         "data": "synthetic (seeded N(0,1) q; K/V N(0,1) quantised to e4m3 with scale 0.05; shuffled block tables)",
         "config": {"workload": cfg.name, "variant": args.variant, "num_seqs": cfg.num_seqs, "num_heads": cfg.num_heads,
                    "num_kv_heads": cfg.num_kv_heads, "head_size": cfg.head_size, "block_size": cfg.block_size,
-                   "ctx": cfg.ctx if cfg.ctx else list(cfg.ctx_range), "kv_splits": nsplit, "decode_kernel": kernel_kind if args.variant != "slot_scales" else None,
+                   "ctx": cfg.ctx if cfg.ctx else list(cfg.ctx_range), "kv_splits": nsplit, "decode_kernel": kernel_kind,
                    "bytes_per_call": bytes_per_call,
                    "l2": "KV pool %.2f GB x %d replica(s) >= 3x L2 (%d MB); no flush needed" % (
                        kv_bytes / 1e9, replicas, l2 >> 20),
@@ -635,8 +637,7 @@ def run_ours(args, ws, rank, local):
                    "parallelism": "replicas x%d" % ws},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
-                     "kernel": KERNEL_FUNCTION[kernel_kind] if args.variant != "slot_scales"
-                     else "pda_split_decode_kernel",
+                     "kernel": KERNEL_FUNCTION[kernel_kind],
                      "timed_span": ("the timed region's CUDA events over its %d launches of the decode kernel "
                                     "(one launch per call)" % K) if single_launch else
                                    ("profile events around the decode kernel (with the unit-order kernel that "

@@ -438,6 +438,20 @@ int pda_choose_kernel(int num_seqs, int num_kv_heads, int max_num_blocks_per_seq
 int pda_plan_launches(int num_seqs, int num_heads, int num_kv_heads, int max_num_blocks_per_seq, int block_size);
 
 /*
+ * pda_plan_slot_scales -- the plan pda_decode_slot_scales makes for these
+ * sizes on the current device. *kernel receives PDA_KERNEL_PERSISTENT when
+ * the grid is past one wave of 3 CTAs per SM and the GQA group's query rows
+ * leave room for a stage's scale rows in the persistent kernel's side
+ * entries (g <= 6 at 16- to 64-token blocks, g <= 4 at 128), else
+ * PDA_KERNEL_PER_UNIT; *num_splits the split count; *launches the kernels
+ * one call launches (the unit-order, tail merge and merge kernels as for
+ * pda_decode). Any out pointer may be NULL. Returns 0, or -1 for invalid
+ * sizes or a CUDA error. Diagnostic.
+ */
+int pda_plan_slot_scales(int num_seqs, int num_heads, int num_kv_heads, int max_num_blocks_per_seq, int block_size,
+                         int* kernel, int* num_splits, int* launches);
+
+/*
  * pda_set_split_override -- force the split count of later pda_decode calls
  * (process-wide; 0 restores the heuristic). For tests and measurements.
  * Values above the table row length are clamped at call time.

@@ -37,6 +37,7 @@ from ._binding import (  # noqa: F401
     load,
     plan_kernel,
     plan_launches,
+    plan_slot_scales,
     plan_splits,
     query_device_status,
     workspace_info,

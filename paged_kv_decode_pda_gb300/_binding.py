@@ -34,6 +34,7 @@ SIGNATURES = {
     "pda_plan_splits": (_I, [_I, _I, _I, _I, _I]),
     "pda_plan_kernel": (_I, [_I, _I, _I, _I, _I]),
     "pda_plan_launches": (_I, [_I, _I, _I, _I, _I]),
+    "pda_plan_slot_scales": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "pda_choose_kernel": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "pda_set_split_override": (None, [_I]),
     "pda_set_tail_split": (None, [_I]),
@@ -351,6 +352,15 @@ def plan_launches(num_seqs, num_heads, num_kv_heads, max_num_blocks_per_seq, blo
     if n < 0:
         raise PdaError(PDA_ERR_CUDA, "pda_plan_launches")
     return n
+
+
+def plan_slot_scales(num_seqs, num_heads, num_kv_heads, max_num_blocks_per_seq, block_size) -> tuple[int, int, int]:
+    """The plan of a pda_decode_slot_scales call: (PDA_KERNEL_* instance, split count, launches per call)."""
+    k, ns, nl = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    if load().pda_plan_slot_scales(num_seqs, num_heads, num_kv_heads, max_num_blocks_per_seq, block_size,
+                                   ctypes.byref(k), ctypes.byref(ns), ctypes.byref(nl)) != 0:
+        raise PdaError(PDA_ERR_CUDA, "pda_plan_slot_scales")
+    return k.value, ns.value, nl.value
 
 
 def set_split_override(n: int) -> None:

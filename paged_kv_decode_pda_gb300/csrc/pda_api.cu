@@ -41,9 +41,15 @@ enum KernelKind {
   kTokenDense,
   kPersistWide,   // persistent, page-major pages
   kPersistToken,  // persistent, token-major pages through tensor maps
+  kPersistSlot,   // persistent, page-major pages with per-slot scale tables
   kNumKinds
 };
-bool is_persistent(int k) { return k == kPersistWide || k == kPersistToken; }
+bool is_persistent(int k) { return k == kPersistWide || k == kPersistToken || k == kPersistSlot; }
+// The per-unit instance that takes a persistent instance's calls when the
+// persistent kernel cannot (past 2^31 units, or captured without a workspace).
+KernelKind per_unit_of(KernelKind k) {
+  return k == kPersistToken ? kTokenWide : (k == kPersistSlot ? kSlotWide : kPlainWide);
+}
 
 // Forgets pda_decode_noalloc's per-device set-up (defined with it below).
 void noalloc_forget_devices();
@@ -107,7 +113,10 @@ RingShape ring_shape(int bs, bool slot_scales = false, int ring_bytes = pda::kRi
 // (swizzled tensor-map pages need 1 KiB alignment) and at least the merge
 // rows; then one side entry per stage (query rows, merge (m, l), header);
 // then full and empty barriers per stage plus one consumer barrier.
-RingShape persistent_ring_shape(int bs) {
+// With per-slot scales the side entries are kAuxBytesSlot long and a
+// stage's scale rows (2 x pages x bs floats) sit at the end of the entry's
+// query-row area: scale_off is that offset within the entry.
+RingShape persistent_ring_shape(int bs, bool slot_scales = false) {
   RingShape r = ring_shape(bs);
   const uint32_t kv = r.scale_off;
   uint32_t st = kv > pda::kPersistMergeBytes ? kv : pda::kPersistMergeBytes;
@@ -115,8 +124,17 @@ RingShape persistent_ring_shape(int bs) {
   r.stage_bytes = st;
   r.num_stages = (int)((uint32_t)pda::kPersistRingBytes / st);
   if (r.num_stages < 2) r.num_stages = 2;
-  r.smem_bytes = (size_t)r.num_stages * (st + pda::kAuxBytes) + 8 * (2 * (size_t)r.num_stages + 1) + 16 + 1024;
+  const uint32_t aux = slot_scales ? pda::kAuxBytesSlot : pda::kAuxBytes;
+  r.scale_off = slot_scales ? pda::kAuxMl - 2u * (uint32_t)r.pages_per_stage * (uint32_t)bs * 4u : 0u;
+  r.smem_bytes = (size_t)r.num_stages * (st + aux) + 8 * (2 * (size_t)r.num_stages + 1) + 16 + 1024;
   return r;
+}
+
+// The persistent slot-scale instance fits a GQA group whose query rows
+// (g x 256 bytes) leave room in the side entry for a stage's scale rows.
+bool slot_persistent_fits(int gqa, int bs) {
+  const RingShape r = persistent_ring_shape(bs, true);
+  return (uint32_t)gqa * kHeadDim * 2u <= r.scale_off;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -304,10 +322,10 @@ pda_status validate(const void* out, const void* q, const void* k_cache, const v
 }
 
 bool is_dense(KernelKind k) { return k == kPlainDense || k == kTokenDense; }
-bool is_slot(KernelKind k) { return k == kSlotWide; }
+bool is_slot(KernelKind k) { return k == kSlotWide || k == kPersistSlot; }
 
 RingShape ring_for(KernelKind k, int bs) {
-  if (is_persistent(k)) return persistent_ring_shape(bs);
+  if (is_persistent(k)) return persistent_ring_shape(bs, k == kPersistSlot);
   return ring_shape(bs, is_slot(k), is_dense(k) ? pda::kDenseRingBytes : pda::kRingBytes);
 }
 
@@ -347,16 +365,19 @@ SplitFn split_fn(KernelKind k, bool paired, bool cluster = false) {
   return paired ? split_fn_of<true>(k) : split_fn_of<false>(k);
 }
 
-PersistFn persist_fn(bool token_major, bool paired) {
-  if (token_major)
-    return paired ? pda::pda_persistent_decode_kernel<true, pda::kPersistCtasPerSm, true>
-                  : pda::pda_persistent_decode_kernel<true, pda::kPersistCtasPerSm, false>;
-  return paired ? pda::pda_persistent_decode_kernel<false, pda::kPersistCtasPerSm, true>
-                : pda::pda_persistent_decode_kernel<false, pda::kPersistCtasPerSm, false>;
+PersistFn persist_fn(KernelKind k, bool paired) {
+  if (k == kPersistToken)
+    return paired ? pda::pda_persistent_decode_kernel<false, true, pda::kPersistCtasPerSm, true>
+                  : pda::pda_persistent_decode_kernel<false, true, pda::kPersistCtasPerSm, false>;
+  if (k == kPersistSlot)
+    return paired ? pda::pda_persistent_decode_kernel<true, false, pda::kPersistCtasPerSm, true>
+                  : pda::pda_persistent_decode_kernel<true, false, pda::kPersistCtasPerSm, false>;
+  return paired ? pda::pda_persistent_decode_kernel<false, false, pda::kPersistCtasPerSm, true>
+                : pda::pda_persistent_decode_kernel<false, false, pda::kPersistCtasPerSm, false>;
 }
 
 const void* kernel_fn(KernelKind k, bool paired) {
-  if (is_persistent(k)) return (const void*)persist_fn(k == kPersistToken, paired);
+  if (is_persistent(k)) return (const void*)persist_fn(k, paired);
   return (const void*)split_fn(k, paired);
 }
 
@@ -429,10 +450,20 @@ int resolve_splits(int num_seqs, int num_kv_heads, int max_blocks, int bs, int s
 #ifdef PDA_DISABLE_PERSISTENT
 constexpr KernelKind kWidePlain = kPlainWide;
 constexpr KernelKind kWideToken = kTokenWide;
+constexpr bool kPersistentSlot = false;
 #else
 constexpr KernelKind kWidePlain = kPersistWide;
 constexpr KernelKind kWideToken = kPersistToken;
+constexpr bool kPersistentSlot = true;
 #endif
+
+// The wide instance of per-slot-scale calls: the persistent kernel when the
+// group's query rows leave room for the scale rows (g <= 6 at 16- to 64-token
+// blocks), else the per-unit kernel. Its one-wave grids run the per-unit
+// kernel (plan_from).
+KernelKind slot_wide_kind(int gqa, int bs) {
+  return (kPersistentSlot && slot_persistent_fits(gqa, bs)) ? kPersistSlot : kSlotWide;
+}
 
 // Split count and kernel instance for a call: the wide instance (3 CTAs per
 // SM, 64 KiB ring) unless its planned grid fits one wave of the dense
@@ -471,7 +502,10 @@ Plan plan_from(int num_seqs, int num_kv_heads, int max_blocks, int bs, int sms, 
   pl.nsplit = resolve_splits(num_seqs, num_kv_heads, MB, bs, sms, occ, override_splits);
   if (dense != wide) {
     const long long ctas = (long long)num_seqs * num_kv_heads * pl.nsplit;
-    if (occ_d > occ && ctas <= (long long)sms * occ_d) {
+    // per-slot scales: the per-unit kernel for one wave (its splits can
+    // merge in clusters), the persistent one past it
+    const bool one_wave_slot = wide == kPersistSlot && ctas <= (long long)sms * occ;
+    if ((occ_d > occ && ctas <= (long long)sms * occ_d) || one_wave_slot) {
       pl.kind = dense;
       pl.nsplit = resolve_splits(num_seqs, num_kv_heads, MB, bs, sms, occ_d, override_splits);
     }
@@ -479,7 +513,7 @@ Plan plan_from(int num_seqs, int num_kv_heads, int max_blocks, int bs, int sms, 
   if (is_persistent(pl.kind) && (long long)num_seqs * num_kv_heads * pl.nsplit > INT32_MAX) {
     // The persistent kernel counts units in 32-bit tickets; the per-unit
     // kernel's grid (splits, kv heads, sequences) has no such bound.
-    pl.kind = pl.kind == kPersistToken ? kTokenWide : kPlainWide;
+    pl.kind = per_unit_of(pl.kind);
   }
   if (is_persistent(pl.kind)) {
     const long long units = (long long)num_seqs * num_kv_heads * pl.nsplit;
@@ -712,7 +746,7 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PDA_ERR_CUDA;
-  const KernelKind wide = slot ? kSlotWide : (tm ? kWideToken : kWidePlain);
+  const KernelKind wide = slot ? slot_wide_kind(num_heads / num_kv_heads, block_size) : (tm ? kWideToken : kWidePlain);
   const KernelKind dense = slot ? kSlotWide : (tm ? kTokenDense : kPlainDense);
   Plan pl;
   st = plan_call(dev, num_seqs, num_kv_heads, max_num_blocks_per_seq, block_size, wide, dense, &pl);
@@ -723,7 +757,7 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
   st = get_workspace(dev, stream, wl.bytes, &ws);
   if (st == PDA_ERR_WORKSPACE && is_persistent(pl.kind) && nsplit == 1) {
     // Captured without pda_reserve: the per-unit kernel needs no workspace.
-    pl.kind = pl.kind == kPersistToken ? kTokenWide : kPlainWide;
+    pl.kind = per_unit_of(pl.kind);
     wl = WsLayout();
     st = PDA_OK;
   }
@@ -779,12 +813,14 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
   // gather, else one bulk copy per row (rows of at least 128 bytes).
   CUtensorMap kscale_map, vscale_map;
   const bool gathers = g_tma_gather.load() != 0;
-  if (slot && gathers) {
-    if (rs.pages_per_stage != 4)
+  if (slot) {
+    if (gathers && rs.pages_per_stage != 4)
       p.scale_rows = pda::kScaleRowsBulk;
-    else if (make_scale_row_map(k_scales, block_size, &kscale_map) &&
+    else if (gathers && make_scale_row_map(k_scales, block_size, &kscale_map) &&
              make_scale_row_map(v_scales, block_size, &vscale_map))
       p.scale_rows = pda::kScaleRowsGather4;
+    // the persistent kernel's stages take no cp.async pieces
+    if (p.scale_rows == pda::kScaleRowsPieces && is_persistent(pl.kind)) p.scale_rows = pda::kScaleRowsBulk;
   }
   // Persistent kernel, page-major 16-token pages: a stage's 4 pages of
   // each cache in one gather.
@@ -806,7 +842,7 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
   const bool paired = paired_for(p.gqa);
   if (is_persistent(pl.kind)) {
     const int units = num_seqs * num_kv_heads * nsplit;
-    const PersistFn fn = persist_fn(pl.kind == kPersistToken, paired);
+    const PersistFn fn = persist_fn(pl.kind, paired);
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(pl.grid);
     lc.blockDim = dim3(pda::kThreads);
@@ -853,7 +889,7 @@ static pda_status launch_decode(bool slot, void* out, const void* q, const void*
       pda::TailMergeParams tp;
       tp.m.out = out;
       tp.m.num_heads = num_heads;
-      tp.m.v_scale = v_scale;
+      tp.m.v_scale = slot ? 1.f : v_scale;  // slot scales: the pieces carry their V reference
       tp.m.sinks = sinks;
       tp.m.out_fp8 = out_fp8;
       tp.m.out_scale = out_scale;
@@ -1028,6 +1064,23 @@ int pda_plan_launches(int num_seqs, int num_heads, int num_kv_heads, int max_num
   return plan_launches(pl);
 }
 
+int pda_plan_slot_scales(int num_seqs, int num_heads, int num_kv_heads, int max_num_blocks_per_seq, int block_size,
+                         int* kernel, int* num_splits, int* launches) {
+  if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 ||
+      max_num_blocks_per_seq < 0 || block_size <= 0 || block_size % 16 != 0 || block_size > 128)
+    return -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  Plan pl;
+  if (plan_call(dev, num_seqs, num_kv_heads, max_num_blocks_per_seq, block_size,
+                slot_wide_kind(num_heads / num_kv_heads, block_size), kSlotWide, &pl) != PDA_OK)
+    return -1;
+  if (kernel) *kernel = is_persistent(pl.kind) ? PDA_KERNEL_PERSISTENT : PDA_KERNEL_PER_UNIT;
+  if (num_splits) *num_splits = pl.nsplit;
+  if (launches) *launches = num_seqs == 0 ? 0 : plan_launches(pl);
+  return 0;
+}
+
 void pda_set_profile_events(cudaEvent_t before, cudaEvent_t after) {
   if (before && after) {
     g_prof_before.store(before);
@@ -1047,7 +1100,9 @@ pda_status pda_reserve(int num_seqs, int num_heads, int num_kv_heads, int max_nu
   if (cudaGetDevice(&dev) != cudaSuccess) return PDA_ERR_CUDA;
   // Size for the largest plan any entry point makes for these sizes.
   size_t bytes = 0;
-  const KernelKind pairs[3][2] = {{kWidePlain, kPlainDense}, {kSlotWide, kSlotWide}, {kWideToken, kTokenDense}};
+  const KernelKind pairs[3][2] = {{kWidePlain, kPlainDense},
+                                  {slot_wide_kind(num_heads / num_kv_heads, block_size), kSlotWide},
+                                  {kWideToken, kTokenDense}};
   for (const auto& pr : pairs) {
     Plan pl;
     pda_status st = plan_call(dev, num_seqs, num_kv_heads, max_num_blocks_per_seq, block_size, pr[0], pr[1], &pl);

@@ -1163,6 +1163,12 @@ constexpr uint32_t kAuxQ = 0;                                     // query rows,
 constexpr uint32_t kAuxMl = kMaxGqa * kHeadDim * 2;              // merge (m, l) [w][head][2]
 constexpr uint32_t kAuxHdr = kAuxMl + kConsumerWarps * kMaxGqa * 2 * 4;  // StageHeader
 constexpr uint32_t kAuxBytes = kAuxHdr + sizeof(StageHeader);
+// Side entries of the per-slot-scale instance: 128-byte multiples, so that
+// the scale rows a TMA gather lands in the query-row area (at p.scale_off,
+// past the group's query rows) start on a 128-byte boundary.
+constexpr uint32_t kAuxBytesSlot = (kAuxBytes + 127u) & ~127u;
+template <bool kSlotScales>
+__host__ __device__ constexpr uint32_t aux_bytes() { return kSlotScales ? kAuxBytesSlot : kAuxBytes; }
 // Merge rows in a persistent stage: 8 rows per warp at the unpadded stride
 // fill 16 KiB exactly; paired instances store 4 rows per warp at the padded
 // stride (bank-conflict free).
@@ -1193,7 +1199,7 @@ __device__ __forceinline__ bool consumer_sync(uint32_t bar, uint32_t& phase, int
 // O rows [kMaxGqa][kHeadDim], then (m, l) pairs.
 template <int kStride, int kRows>
 __device__ __forceinline__ void tail_piece_rows(const DecodeParams& p, const float* mo, const float* mml, int tid,
-                                                int slot) {
+                                                int slot, float vref) {
   float* rows = p.tail_rows + (size_t)slot * kTailRowFloats;
   const int d = tid;
   for (int hh = 0; hh < p.gqa; ++hh) {
@@ -1210,7 +1216,9 @@ __device__ __forceinline__ void tail_piece_rows(const DecodeParams& p, const flo
         den += f * mml[(w * kMaxGqa + hh) * 2 + 1];
       }
     }
-    __stcg(rows + hh * kHeadDim + d, acc);
+    // slot scales: the piece's own V reference goes into its O rows (the
+    // tail merge then scales by 1)
+    __stcg(rows + hh * kHeadDim + d, acc * vref);
     if (d == 0) {
       __stcg(rows + kMaxGqa * kHeadDim + hh * 2 + 0, M);
       __stcg(rows + kMaxGqa * kHeadDim + hh * 2 + 1, den);
@@ -1218,7 +1226,12 @@ __device__ __forceinline__ void tail_piece_rows(const DecodeParams& p, const flo
   }
 }
 
-template <bool kTokenMajor, int kMinCtasPerSm, bool kPaired>
+// kSlotScales: per-slot scale tables (page-major pages only). Each stage's
+// K and V scale rows land in its side entry at p.scale_off, by one TMA
+// gather per table (p.scale_rows == kScaleRowsGather4) or one bulk copy per
+// row; a unit's (or piece's) V reference is the first V scale of its first
+// stage, as in the per-unit kernel.
+template <bool kSlotScales, bool kTokenMajor, int kMinCtasPerSm, bool kPaired>
 __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
     pda_persistent_decode_kernel(const DecodeParams p, unsigned* queue, int num_units,
                                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
@@ -1235,9 +1248,11 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
   const int NS = p.num_stages;
   const int PPS = p.pages_per_stage;
 
+  static_assert(!(kSlotScales && kTokenMajor), "per-slot scales come with page-major pages");
+  constexpr uint32_t kAux = aux_bytes<kSlotScales>();
   uint8_t* ring = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);
   uint8_t* aux = ring + (size_t)NS * p.stage_bytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(aux + (size_t)NS * kAuxBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(aux + (size_t)NS * kAux);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * NS + 1);
   const uint32_t ring_u32 = smem_u32(ring);
   const uint32_t aux_u32 = smem_u32(aux);
@@ -1331,7 +1346,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
         if (lane == 0) {
           const uint32_t sbase = ring_u32 + (uint32_t)stage * p.stage_bytes;
           const uint32_t bar = full0 + 8u * stage;
-          StageHeader* hd = reinterpret_cast<StageHeader*>(aux + (size_t)stage * kAuxBytes + kAuxHdr);
+          StageHeader* hd = reinterpret_cast<StageHeader*>(aux + (size_t)stage * kAux + kAuxHdr);
           hd->s = s;
           hd->kvh = kvh;
           hd->split = split;
@@ -1342,15 +1357,40 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
           hd->slot = slot;
           const bool with_q = (k == 0) && (np > 0);
           const uint32_t q_bytes = with_q ? (uint32_t)g * kHeadDim * 2u : 0u;
-          // a four-row gather always lands 4 pages per table
-          const uint32_t bytes = 2u * page_bytes * (uint32_t)(p.page_gather && np > 0 ? 4 : np) + q_bytes;
+          // a four-row gather always lands 4 pages (or scale rows) per table
+          const uint32_t row_bytes = (uint32_t)bs * 4u;
+          uint32_t scale_tx = 0u;
+          if (kSlotScales && np > 0)
+            scale_tx = 2u * row_bytes * (uint32_t)(p.scale_rows == kScaleRowsGather4 ? 4 : np);
+          const uint32_t bytes =
+              2u * page_bytes * (uint32_t)(p.page_gather && np > 0 ? 4 : np) + q_bytes + scale_tx;
           if (bytes == 0) {
             mbar_arrive(bar);  // release-orders the header for the consumers
           } else {
             mbar_arrive_expect_tx(bar, bytes);
             if (with_q)
-              bulk_g2s(aux_u32 + (uint32_t)stage * kAuxBytes + kAuxQ,
+              bulk_g2s(aux_u32 + (uint32_t)stage * kAux + kAuxQ,
                        p.q + ((size_t)s * p.num_heads + (size_t)kvh * g) * kHeadDim, q_bytes, bar);
+            if constexpr (kSlotScales) {
+              // the stage's K scale rows, then its V rows (PPS rows further)
+              const uint32_t sc = aux_u32 + (uint32_t)stage * kAux + p.scale_off;
+              if (p.scale_rows == kScaleRowsGather4) {
+                if (np > 0) {
+                  const int4 r = stage_rows(blk, np, p.num_kv_heads, kvh);
+                  tma_gather4_rows(sc, &tm_k, r.x, r.y, r.z, r.w, bar);
+                  tma_gather4_rows(sc + 4u * row_bytes, &tm_v, r.x, r.y, r.z, r.w, bar);
+                }
+              } else {
+#pragma unroll
+                for (int u = 0; u < kMaxPagesPerStage; ++u) {
+                  if (u < np) {
+                    const size_t off = ((size_t)blk[u] * p.num_kv_heads + kvh) * (size_t)bs;
+                    bulk_g2s(sc + (uint32_t)u * row_bytes, p.k_scales + off, row_bytes, bar);
+                    bulk_g2s(sc + (uint32_t)(PPS + u) * row_bytes, p.v_scales + off, row_bytes, bar);
+                  }
+                }
+              }
+            }
             if constexpr (kTokenMajor) {
 #pragma unroll
               for (int u = 0; u < kMaxPagesPerStage; ++u) {
@@ -1439,7 +1479,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
       const bool got = mbar_wait_bounded(empty0 + 8u * stage, (round & 1u) ^ 1u, abort_flag, kWaitLimitNs);
       if (__all_sync(0xffffffffu, got)) {
         if (lane == 0) {
-          StageHeader* hd = reinterpret_cast<StageHeader*>(aux + (size_t)stage * kAuxBytes + kAuxHdr);
+          StageHeader* hd = reinterpret_cast<StageHeader*>(aux + (size_t)stage * kAux + kAuxHdr);
           hd->flags = kHdrEnd;
           mbar_arrive(full0 + 8u * stage);
         }
@@ -1469,12 +1509,15 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
   }
 
   // -------------------------------------------------------------- consumers
-  TileWorker<false, kTokenMajor, kPaired, true> w;
+  TileWorker<kSlotScales, kTokenMajor, kPaired, true> w;
   w.setup(lane, bs, p.v_shuffled, p.v_swizzle);
   w.reset();
   const int tiles_per_page = bs / 16;
   const uint32_t v_sub = p.v_shuffled ? (uint32_t)(kHeadDim * 16) : 16u;
   uint32_t cons_phase = 0;
+  // Slot-scale variant: V scales enter P relative to vref (the first slot
+  // of the unit or piece), and vref multiplies the result back at the end.
+  float vref = 1.f, vinv = 1.f;
 
   for (int fill = 0;; ++fill) {
     const int stage = fill % NS;
@@ -1487,15 +1530,29 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
       }
       break;
     }
-    const StageHeader hd = *reinterpret_cast<const StageHeader*>(aux + (size_t)stage * kAuxBytes + kAuxHdr);
+    const StageHeader hd = *reinterpret_cast<const StageHeader*>(aux + (size_t)stage * kAux + kAuxHdr);
     if (hd.flags & kHdrEnd) break;
     const uint32_t sbase = ring_u32 + (uint32_t)stage * p.stage_bytes;
+    // slot scales of the stage: K rows of its pages, then V rows
+    const float* srow = kSlotScales ? reinterpret_cast<const float*>(aux + (size_t)stage * kAux + p.scale_off)
+                                    : nullptr;
     if (hd.flags & kHdrFirst) {
       w.reset();
+      if constexpr (kSlotScales) {
+        vref = 1.f;
+        vinv = 1.f;
+        if (hd.np > 0) {
+          const float v0 = srow[PPS * bs];
+          if (isfinite(v0) && v0 != 0.f) {
+            vref = v0;
+            vinv = 1.f / v0;
+          }
+        }
+      }
       if (hd.np > 0) {
         const int qh = w.q_head();
         const bool live = qh < g;
-        w.load_q_shared(aux_u32 + (uint32_t)stage * kAuxBytes + kAuxQ + (uint32_t)(live ? qh : 0) * (kHeadDim * 2),
+        w.load_q_shared(aux_u32 + (uint32_t)stage * kAux + kAuxQ + (uint32_t)(live ? qh : 0) * (kHeadDim * 2),
                         live, p.logit_scale_log2);
       }
     }
@@ -1509,22 +1566,26 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
                                          : sbase + (uint32_t)pg * page_bytes + (uint32_t)(sub * 256);
       const uint32_t vbase = kTokenMajor ? sbase + (uint32_t)(PPS + pg) * page_bytes + (uint32_t)sub * 2048u
                                          : sbase + (uint32_t)(PPS + pg) * page_bytes + ((uint32_t)sub ^ w.v_xor) * v_sub;
-      w.tile(kbase, vbase, bs, hd.L - tok0, nullptr, nullptr, 1.f);
+      if constexpr (kSlotScales)
+        w.tile(kbase, vbase, bs, hd.L - tok0, srow + pg * bs + sub * 16, srow + (PPS + pg) * bs + sub * 16, vinv);
+      else
+        w.tile(kbase, vbase, bs, hd.L - tok0, nullptr, nullptr, 1.f);
     }
     if (hd.flags & kHdrLast) {
       // Every consumer warp is done with this stage's pages: its memory
       // becomes the merge area until the stage is released below.
       if (!consumer_sync(cons_bar, cons_phase, lane, abort_flag)) break;
       float* mo = reinterpret_cast<float*>(ring + (size_t)stage * p.stage_bytes);
-      float* mml = reinterpret_cast<float*>(aux + (size_t)stage * kAuxBytes + kAuxMl);
+      float* mml = reinterpret_cast<float*>(aux + (size_t)stage * kAux + kAuxMl);
       constexpr int kStride = persist_merge_stride<kPaired>();
       w.template store_merge<kStride>(mo, mml, warp);
       if (!consumer_sync(cons_bar, cons_phase, lane, abort_flag)) break;
       if (hd.slot < 0) {
-        reduce_store<false, kStride, decltype(w)::kMergeRows>(p, mo, mml, threadIdx.x, hd.s, hd.kvh, hd.split, 1.f);
+        reduce_store<kSlotScales, kStride, decltype(w)::kMergeRows>(p, mo, mml, threadIdx.x, hd.s, hd.kvh, hd.split,
+                                                                     vref);
       } else {
         // a tail piece: its (O, m, l) rows for the tail merge kernel
-        tail_piece_rows<kStride, decltype(w)::kMergeRows>(p, mo, mml, threadIdx.x, hd.slot);
+        tail_piece_rows<kStride, decltype(w)::kMergeRows>(p, mo, mml, threadIdx.x, hd.slot, kSlotScales ? vref : 1.f);
       }
     }
     __syncwarp();

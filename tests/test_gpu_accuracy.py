@@ -109,8 +109,10 @@ def test_outputs_between_2_and_4_on_every_entry_point(bs):
         assert stats["n_out_2_to_4"] >= 1000, (name, stats)
 
 
-def test_outputs_between_2_and_4_with_slot_scales():
-    batch = large_v_batch(48, 40, 8, 40, seed=7)
+@pytest.mark.parametrize("S", [48, 80])
+def test_outputs_between_2_and_4_with_slot_scales(S):
+    # 48 sequences: the per-unit kernel; 80: the persistent kernel
+    batch = large_v_batch(S, 40, 8, 40, seed=7)
     NB, Hk, bs = batch.num_blocks, 8, 16
     g = torch.Generator(device=DEV).manual_seed(8)
     ks = (torch.rand(NB, Hk, bs, generator=g, device=DEV) * 0.02 + 0.04).float()
@@ -180,13 +182,14 @@ def test_query_shift_keeps_normal_rows_bitwise():
 
 # ------------------------------------------------------ slot-scale V ratios
 
-@pytest.mark.parametrize("splits", [1, 2])
-def test_slot_scales_v_ratio_2_pow_14_within_a_split(splits):
+@pytest.mark.parametrize("splits,S", [(1, 4), (2, 4), (1, 80)])
+def test_slot_scales_v_ratio_2_pow_14_within_a_split(splits, S):
     """V scales spread over 2^-7 .. 2^7 times 0.05 inside one split: the
     probabilities times V-scale ratios stay inside f16's range up to the
-    documented 2^15 limit."""
-    lens = [64, 200, 1000, 37]
-    batch = workloads.make_custom(4, 32, 8, lens, pool_factor=1.2, seed=51, device=DEV)
+    documented 2^15 limit (80 sequences: the persistent kernel, whose tail
+    pieces each take their own reference)."""
+    lens = ([64, 200, 1000, 37] * 20)[:S]
+    batch = workloads.make_custom(S, 32, 8, lens, pool_factor=1.2, seed=51, device=DEV)
     NB, Hk, bs = batch.num_blocks, 8, 16
     g = torch.Generator(device=DEV).manual_seed(52)
     ks = (torch.rand(NB, Hk, bs, generator=g, device=DEV) * 0.02 + 0.04).float()
@@ -194,7 +197,7 @@ def test_slot_scales_v_ratio_2_pow_14_within_a_split(splits):
     vs = (0.05 * torch.exp2(r)).float()
     # the first slot of every sequence sets the split's reference scale:
     # make the widest spread reachable from it within the split
-    for s in range(4):
+    for s in range(S):
         b0 = int(batch.block_tables[s, 0])
         vs[b0, :, 0] = 0.05 * 2.0 ** -7
     ratio = (vs.max() / vs.min()).item()

@@ -358,6 +358,94 @@ def test_page_gathers_bitwise_equal_to_page_copies(S, splits, shuffled):
     assert pda.query_device_status() == 0
 
 
+def _slot_tables(batch, seed, junk=True):
+    """Per-slot scales within +-20 % of the codes' scale; slots past each
+    length hold NaN, which the kernels must never use."""
+    cfg = batch.cfg
+    NB, Hk, bs = batch.num_blocks, cfg.num_kv_heads, cfg.block_size
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    ks = (torch.rand(NB, Hk, bs, generator=g, device=DEV) * 0.02 + 0.04).float()
+    vs = (torch.rand(NB, Hk, bs, generator=g, device=DEV) * 0.02 + 0.04).float()
+    if junk:
+        for s, L in enumerate(batch.seq_lens_host):
+            L = int(L)
+            if L == 0:
+                continue
+            P = (L + bs - 1) // bs
+            b = int(batch.block_tables[s, P - 1])
+            n = L - (P - 1) * bs
+            ks[b, :, n:] = float("nan")
+            vs[b, :, n:] = float("nan")
+    return ks, vs
+
+
+@pytest.mark.parametrize("S,H,bs,splits,ctx", [
+    (80, 32, 16, 0, 2048),    # 640 units: scale-row gathers, shrinking tail pieces
+    (120, 40, 16, 0, 0),      # g = 5, ragged lengths: last stages of 1 to 3 pages
+    (40, 32, 64, 2, 2048),    # 64-token blocks, 2 splits: a bulk copy per scale row, pieces of splits
+    (100, 48, 32, 0, 0),      # g = 6, the widest group whose query rows leave room for the scale rows
+])
+def test_slot_scales_on_the_persistent_kernel(S, H, bs, splits, ctx):
+    """Multi-wave per-slot-scale calls run on the persistent kernel, scale
+    rows in the stages' side entries: oracle parity, the same bits call after
+    call and with the gathers off, and the uncut call within rounding."""
+    if ctx:
+        batch = _uniform(S, H, 8, ctx, bs=bs, seed=S + H + bs)
+    else:
+        batch = _many(S, bs, seed=S + H + bs, max_len=2000, H=H)
+    cfg = batch.cfg
+    ks, vs = _slot_tables(batch, seed=S + bs)
+    pda.set_split_override(splits)
+    try:
+        kind, nsplit, launches = pda.plan_slot_scales(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads,
+                                                      cfg.max_num_blocks_per_seq, bs)
+        assert kind == pda.PDA_KERNEL_PERSISTENT and nsplit == max(splits, 1)
+
+        def call():
+            return pda.decode_slot_scales(batch.q, batch.k_cache, batch.v_cache, ks, vs, batch.block_tables,
+                                          batch.seq_lens, cfg.scale).clone()
+
+        a, b = call(), call()
+        pda.set_tma_gather(False)
+        c = call()
+        pda.set_tma_gather(True)
+        pda.set_tail_split(False)
+        d = call()
+        torch.cuda.synchronize()
+    finally:
+        pda.set_tma_gather(True)
+        pda.set_tail_split(True)
+        pda.set_split_override(0)
+    assert torch.equal(a, b), "deterministic"
+    assert torch.equal(a, c), "gathers and bulk copies bring the same rows"
+    assert (a.float() - d.float()).abs().max().item() <= 4e-3
+    ref = oracle.decode(**batch.raw(), scale=cfg.scale, k_scales=ks.cpu().numpy(), v_scales=vs.cpu().numpy())
+    U.compare(a, ref, "slot scales, persistent S=%d H=%d bs=%d splits=%d" % (S, H, bs, splits))
+    assert pda.query_device_status() == 0
+
+
+@pytest.mark.parametrize("S,H,Hk,bs,want", [
+    (80, 64, 8, 16, pda.PDA_KERNEL_PER_UNIT),      # g = 8: no room beside the query rows
+    (80, 40, 8, 128, pda.PDA_KERNEL_PER_UNIT),     # g = 5 at 128-token blocks (1 KiB of scale rows)
+    (80, 32, 8, 128, pda.PDA_KERNEL_PERSISTENT),   # g = 4 at 128-token blocks
+    (40, 32, 8, 16, pda.PDA_KERNEL_PER_UNIT),      # one wave: the per-unit kernel (cluster merges)
+])
+def test_slot_scale_kernel_choice(S, H, Hk, bs, want):
+    kind, _, launches = pda.plan_slot_scales(S, H, Hk, 4096 // bs, bs)
+    assert kind == want
+    assert launches >= 1
+    if want == pda.PDA_KERNEL_PER_UNIT:
+        # still oracle parity on the per-unit kernel
+        batch = _uniform(S, H, Hk, 300, bs=bs, seed=S + H)
+        ks, vs = _slot_tables(batch, seed=H)
+        out = pda.decode_slot_scales(batch.q, batch.k_cache, batch.v_cache, ks, vs, batch.block_tables,
+                                     batch.seq_lens, batch.cfg.scale)
+        torch.cuda.synchronize()
+        ref = oracle.decode(**batch.raw(), scale=batch.cfg.scale, k_scales=ks.cpu().numpy(),
+                            v_scales=vs.cpu().numpy())
+        U.compare(out, ref, "slot scales, per-unit S=%d H=%d bs=%d" % (S, H, bs))
+
+
 def test_tail_pieces_with_sinks_e4m3_output_and_strided_caches():
     # every persistent entry point takes the same pieces
     batch = _uniform(80, 32, 8, 2048, seed=11)
