@@ -245,6 +245,10 @@ pda_status pda_decode_strided(void* out, const void* q, const void* k_cache, con
  * two V scales must stay below 2^15 (each probability, times its slot's V
  * scale relative to the split's first one, enters the PV product in f16
  * parts, whose range ends at 65504); the tests cover ratios of 2^14.
+ * Multi-wave calls of GQA groups of at most 6 heads (4 at 128-token blocks)
+ * run on the persistent kernel, whose tail pieces each take their own first
+ * slot as the reference (a subset of the split: the same bound holds);
+ * pda_plan_slot_scales tells which kernel a call takes.
  */
 pda_status pda_decode_slot_scales(void* out, const void* q, const void* k_cache, const void* v_cache,
                                   const float* k_scales, const float* v_scales, const int32_t* block_tables,
