@@ -2,7 +2,9 @@
 //   pda_split_decode_kernel       one CTA per work unit (below)
 //   pda_persistent_decode_kernel  one CTA per resident slot taking work units
 //                                 from a queue, the same per-unit arithmetic
-//   pda_order_units_kernel        longest-first order of the queued units
+//   pda_order_units_kernel        longest-first order of the queued units,
+//                                 and the pieces of the last partial round
+//   pda_tail_merge_kernel         log-sum-exp fold of those pieces
 //   pda_merge_kernel              log-sum-exp merge of split partials (one
 //                                 warp per row; pda_merge_wide_kernel past
 //                                 16 splits)
@@ -10,8 +12,9 @@
 //
 // Work unit: one (sequence, kv head, KV split). Per unit:
 //   * warp kConsumerWarps (the producer) gathers the split's pages through
-//     the block table and streams them with 1-D bulk (TMA) copies into a
-//     ring of shared-memory stages, one mbarrier pair per stage;
+//     the block table and streams them with bulk (TMA) copies into a ring
+//     of shared-memory stages, one mbarrier pair per stage (16-token pages
+//     in the persistent kernel: four at a time by a TMA gather);
 //   * warps 0..kConsumerWarps-1 (the consumers) each take 16-token tiles of
 //     a stage and run, for all query heads of the GQA group at once,
 //       S^T = K_tile (16 tok x 128) * Q^T (128 x 8 heads)     (warp MMA)
