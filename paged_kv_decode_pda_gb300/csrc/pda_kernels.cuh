@@ -1665,10 +1665,14 @@ __device__ inline int tail_piece_count(int n, int K, int C, int m, int cap) {
   return P;
 }
 
-// Pages [a, b) of piece r of the P that tail_piece_count gave.
+// Pages [a, b) of piece r of the P that tail_piece_count gave. Equal
+// pieces differ by at most a page and are never empty (n >= P): split_range's
+// rounding would leave the last pieces empty when n / P is small (11 pages in
+// 5 pieces: 3, 3, 3, 2 and none), and an empty piece stores no rows.
 __device__ inline void tail_piece_range(int n, int K, int C, int m, int P, int r, int& a, int& b) {
   if (!tail_geometric(K, C)) {
-    split_range(n, P, r, a, b);
+    a = (int)((long long)r * n / P);
+    b = (int)((long long)(r + 1) * n / P);
     return;
   }
   int rem = n, sz = 0;

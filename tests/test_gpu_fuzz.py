@@ -73,10 +73,39 @@ def _case(seed):
                 shared=shared, seed=seed, q_exps=q_exps, v_gain=v_gain)
 
 
+def _tail_case(seed):
+    """A multi-wave batch of long ragged contexts: the persistent kernel with
+    longest-first order, tail pieces of both shapes (shrinking or equal) and
+    units on both sides of the 1024-token cut."""
+    rng = np.random.default_rng(5000 + seed)
+    Hk = int(rng.choice([1, 2, 4, 8]))
+    g = int(rng.integers(1, 9))
+    bs = int(rng.choice([16, 16, 16, 32, 64, 128]))
+    splits = int(rng.choice([0, 0, 2, 3])) if Hk >= 4 else int(rng.choice([2, 3, 4]))
+    units_goal = int(rng.integers(500, 1600))
+    S = max(1, units_goal // (Hk * max(splits, 1)))
+    lo = int(rng.choice([1, 300, 900]))
+    lens = rng.integers(lo, 3001, S)
+    lens[rng.random(S) < 0.05] = 0
+    pages = max(1, int((lens.max() + bs - 1) // bs))
+    MB = pages + int(rng.integers(0, 3))
+    variant = str(rng.choice(["plain", "sinks", "shuffled_v", "token_major", "slot_scales", "e4m3_out"]))
+    return dict(Hk=Hk, g=g, bs=bs, S=S, lens=lens.tolist(), MB=MB, splits=splits, variant=variant,
+                shared=False, seed=seed, q_exps=None, v_gain=1.0)
+
+
 @pytest.mark.parametrize("seed", range(int(os.environ.get("PDA_FUZZ_FIRST", "0")),
                                   int(os.environ.get("PDA_FUZZ_FIRST", "0")) + int(os.environ.get("PDA_FUZZ_CASES", "100"))))
 def test_random_case(seed):
-    c = _case(seed)
+    _run_case(seed, _case(seed))
+
+
+@pytest.mark.parametrize("seed", range(int(os.environ.get("PDA_FUZZ_TAIL_CASES", "24"))))
+def test_random_multi_wave_case(seed):
+    _run_case(10000 + seed, _tail_case(seed))
+
+
+def _run_case(seed, c):
     H = c["Hk"] * c["g"]
     batch = workloads.make_custom(c["S"], H, c["Hk"], c["lens"], block_size=c["bs"], pool_factor=1.3,
                                   seed=2000 + seed, device=DEV, max_num_blocks_per_seq=c["MB"],

@@ -297,6 +297,8 @@ def _uniform(S, H, Hk, ctx, bs=16, seed=0):
     (120, 32, 8, 700, 16, 0, 0),     # 44-page units stay whole: the tail merge has nothing to fold
     (160, 32, 8, 900, 16, 0, 400),   # 900 to 1299 tokens: tail units on both sides of the 1024-token cut
     (700, 8, 1, 3000, 32, 0, 0),     # one kv head (g = 8), 32-token blocks: 244 tail units in shrinking pieces
+    (128, 6, 2, 2766, 128, 2, 0),    # 128-token blocks, 2 splits of 11 pages in 5 equal pieces (2-3 pages)
+    (33, 24, 8, 2735, 128, 2, 0),    # g = 3, 8 kv heads, the same cut on a 2-stage ring
 ])
 def test_tail_pieces_parity(S, H, Hk, ctx, bs, splits, spread):
     """Units of the last, partial round are cut into pieces; the tail merge
