@@ -90,8 +90,11 @@ def _tail_case(seed):
     pages = max(1, int((lens.max() + bs - 1) // bs))
     MB = pages + int(rng.integers(0, 3))
     variant = str(rng.choice(["plain", "sinks", "shuffled_v", "token_major", "slot_scales", "e4m3_out"]))
+    # as in _case: a third with query rows past f16's range, a third with larger V
+    q_exps = rng.choice([0, 4, -4, -8, -16, -40], size=(S, Hk * g)).tolist() if rng.random() < 1 / 3 else None
+    v_gain = 3.0 if rng.random() < 1 / 3 else 1.0
     return dict(Hk=Hk, g=g, bs=bs, S=S, lens=lens.tolist(), MB=MB, splits=splits, variant=variant,
-                shared=False, seed=seed, q_exps=None, v_gain=1.0)
+                shared=bool(rng.random() < 0.25), seed=seed, q_exps=q_exps, v_gain=v_gain)
 
 
 @pytest.mark.parametrize("seed", range(int(os.environ.get("PDA_FUZZ_FIRST", "0")),
