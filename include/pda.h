@@ -442,6 +442,21 @@ int pda_choose_kernel(int num_seqs, int num_kv_heads, int max_num_blocks_per_seq
 int pda_plan_launches(int num_seqs, int num_heads, int num_kv_heads, int max_num_blocks_per_seq, int block_size);
 
 /*
+ * pda_tail_pieces -- the tail-piece cut the persistent kernel makes (host
+ * only; no device is needed). A call whose units overrun the resident CTAs
+ * (`ctas`) by a partial last round of `tail_units` units (0 < tail_units <
+ * ctas) cuts each of those units of `pages` pages (of its split) into
+ * pieces: at least 256 tokens each, units under 1024 tokens whole, pieces
+ * that shrink toward the end of the hand-out when tail_units >= ctas / 3,
+ * else equal ones. Writes the first min(pieces, max_sizes) piece sizes in
+ * pages to `sizes` (in hand-out order within the unit) and returns the
+ * piece count; -1 for invalid arguments. Diagnostic (tests, tuning); no
+ * counterpart in the pages (a scheduling choice, not part of what the
+ * operation computes).
+ */
+int pda_tail_pieces(int pages, int tail_units, int ctas, int block_size, int* sizes, int max_sizes);
+
+/*
  * pda_plan_slot_scales -- the plan pda_decode_slot_scales makes for these
  * sizes on the current device. *kernel receives PDA_KERNEL_PERSISTENT when
  * the grid is past one wave of 3 CTAs per SM and the GQA group's query rows

@@ -38,6 +38,7 @@ from ._binding import (  # noqa: F401
     plan_kernel,
     plan_launches,
     plan_slot_scales,
+    tail_pieces,
     plan_splits,
     query_device_status,
     workspace_info,

@@ -35,6 +35,7 @@ SIGNATURES = {
     "pda_plan_kernel": (_I, [_I, _I, _I, _I, _I]),
     "pda_plan_launches": (_I, [_I, _I, _I, _I, _I]),
     "pda_plan_slot_scales": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)]),
+    "pda_tail_pieces": (_I, [_I, _I, _I, _I, ctypes.POINTER(_I), _I]),
     "pda_choose_kernel": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "pda_set_split_override": (None, [_I]),
     "pda_set_tail_split": (None, [_I]),
@@ -361,6 +362,15 @@ def plan_slot_scales(num_seqs, num_heads, num_kv_heads, max_num_blocks_per_seq, 
                                    ctypes.byref(k), ctypes.byref(ns), ctypes.byref(nl)) != 0:
         raise PdaError(PDA_ERR_CUDA, "pda_plan_slot_scales")
     return k.value, ns.value, nl.value
+
+
+def tail_pieces(pages: int, tail_units: int, ctas: int, block_size: int) -> list[int]:
+    """``pda_tail_pieces``: the piece sizes (pages) a tail unit of ``pages`` pages is cut into."""
+    buf = (_I * 8)()
+    n = load().pda_tail_pieces(pages, tail_units, ctas, block_size, buf, 8)
+    if n < 0:
+        raise PdaError(PDA_ERR_INVALID_ARG, "pda_tail_pieces")
+    return [buf[i] for i in range(n)]
 
 
 def set_split_override(n: int) -> None:

@@ -484,6 +484,9 @@ struct Plan {
   int min_piece_pages = 1;
 };
 
+// Smallest tail piece: 256 tokens.
+int tail_min_piece_pages(int bs) { return (256 + bs - 1) / bs; }
+
 // Largest batch (in work units) whose units the persistent kernel takes in
 // longest-first order.
 constexpr long long kMaxOrderedUnits = pda::kMaxOrderedUnits;
@@ -534,11 +537,8 @@ Plan plan_from(int num_seqs, int num_kv_heads, int max_blocks, int bs, int sms, 
       const long long k = units % (long long)pl.grid;
       if (k > 0) {
         pl.tail_units = (int)(k < pda::kOrderThreads ? k : pda::kOrderThreads);
-        const long long per = 3LL * pl.tail_units >= (long long)pl.grid
-                                  ? pda::kMaxTailPieces
-                                  : (2 * (long long)pl.grid + pl.tail_units - 1) / pl.tail_units;
-        pl.max_pieces = (int)(per < pda::kMaxTailPieces ? per : pda::kMaxTailPieces);
-        pl.min_piece_pages = (256 + bs - 1) / bs;
+        pl.max_pieces = pda::tail_piece_cap(pl.tail_units, (int)pl.grid);
+        pl.min_piece_pages = tail_min_piece_pages(bs);
       }
     }
   } else if (pl.nsplit >= 2 && pl.nsplit <= pda::kMaxClusterSplits) {
@@ -1062,6 +1062,21 @@ int pda_plan_launches(int num_seqs, int num_heads, int num_kv_heads, int max_num
       PDA_OK)
     return -1;
   return plan_launches(pl);
+}
+
+int pda_tail_pieces(int pages, int tail_units, int ctas, int block_size, int* sizes, int max_sizes) {
+  if (pages < 0 || tail_units <= 0 || ctas <= 0 || tail_units >= ctas || block_size <= 0 || block_size % 16 != 0 ||
+      block_size > 128 || max_sizes < 0 || (max_sizes > 0 && !sizes))
+    return -1;
+  const int m = tail_min_piece_pages(block_size);
+  const int cap = pda::tail_piece_cap(tail_units, ctas);
+  const int P = pda::tail_piece_count(pages, tail_units, ctas, m, cap);
+  for (int r = 0; r < P && r < max_sizes; ++r) {
+    int a = 0, b = pages;
+    if (P > 1) pda::tail_piece_range(pages, tail_units, ctas, m, P, cap, r, a, b);
+    sizes[r] = b - a;
+  }
+  return P;
 }
 
 int pda_plan_slot_scales(int num_seqs, int num_heads, int num_kv_heads, int max_num_blocks_per_seq, int block_size,

@@ -1646,18 +1646,34 @@ struct OrderParams {
 // 126, 64, 32, 17 and 17 pages) took 307.9 us per call against 310.5 us
 // with 5 equal pieces, its CTAs ending within 7 us instead of 15 us. A
 // smaller tail is cut into equal pieces.
-__device__ __forceinline__ bool tail_geometric(int K, int C) { return 3 * K >= C; }
+// (Host and device: the planner and a host-side check use the same rules.)
+__host__ __device__ inline bool tail_geometric(int K, int C) { return 3 * K >= C; }
 
-__device__ __forceinline__ int tail_piece_size(int rem, int K, int C, int m) {
-  return max((int)(((long long)K * rem + C / 2) / C), m);
+// Most pieces a tail unit is cut into: kMaxTailPieces for shrinking pieces,
+// else about two equal pieces per CTA.
+__host__ __device__ inline int tail_piece_cap(int K, int C) {
+  if (tail_geometric(K, C)) return kMaxTailPieces;
+  const long long per = (2LL * C + K - 1) / K;
+  return per < kMaxTailPieces ? (int)per : kMaxTailPieces;
 }
 
-__device__ inline int tail_piece_count(int n, int K, int C, int m, int cap) {
+// The next shrinking piece cut from the rem pages left when `cut` pieces are
+// already cut: about K / C of them, at least m. The cut that reaches the
+// cap takes at least half, so that the last piece (the rest) is never the
+// larger of the two.
+__host__ __device__ inline int tail_piece_size(int rem, int K, int C, int m, int cut, int cap) {
+  int sz = (int)(((long long)K * rem + C / 2) / C);
+  if (sz < m) sz = m;
+  if (cut == cap - 2 && sz < rem - rem / 2) sz = rem - rem / 2;
+  return sz;
+}
+
+__host__ __device__ inline int tail_piece_count(int n, int K, int C, int m, int cap) {
   if (n < kMinCutPieces * m) return 1;
-  if (!tail_geometric(K, C)) return min(n / m, cap);
+  if (!tail_geometric(K, C)) return n / m < cap ? n / m : cap;
   int rem = n, P = 1;
   while (P < cap) {
-    const int sz = tail_piece_size(rem, K, C, m);
+    const int sz = tail_piece_size(rem, K, C, m, P - 1, cap);
     if (rem - sz < m) break;
     rem -= sz;
     ++P;
@@ -1669,7 +1685,7 @@ __device__ inline int tail_piece_count(int n, int K, int C, int m, int cap) {
 // pieces differ by at most a page and are never empty (n >= P): split_range's
 // rounding would leave the last pieces empty when n / P is small (11 pages in
 // 5 pieces: 3, 3, 3, 2 and none), and an empty piece stores no rows.
-__device__ inline void tail_piece_range(int n, int K, int C, int m, int P, int r, int& a, int& b) {
+__host__ __device__ inline void tail_piece_range(int n, int K, int C, int m, int P, int cap, int r, int& a, int& b) {
   if (!tail_geometric(K, C)) {
     a = (int)((long long)r * n / P);
     b = (int)((long long)(r + 1) * n / P);
@@ -1677,7 +1693,7 @@ __device__ inline void tail_piece_range(int n, int K, int C, int m, int P, int r
   }
   int rem = n, sz = 0;
   for (int i = 0; i <= r; ++i) {
-    sz = i == P - 1 ? rem : tail_piece_size(rem, K, C, m);
+    sz = i == P - 1 ? rem : tail_piece_size(rem, K, C, m, i, cap);
     if (i < r) rem -= sz;
   }
   a = n - rem;
@@ -1885,7 +1901,7 @@ __global__ void __launch_bounds__(kOrderThreads) pda_order_units_kernel(const Or
     if (f) {
       int4 e = make_int4(u, 0, 0, -1);
       if (P > 1) {
-        tail_piece_range(n, K, C, m, P, r, e.y, e.z);
+        tail_piece_range(n, K, C, m, P, p.max_pieces, r, e.y, e.z);
         e.w = slot0 + r;
       }
       p.piece_table[issued + rank] = e;

@@ -111,6 +111,51 @@ def test_choose_kernel_table(lib, S, Hk, MB, bs, kind, splits, launches):
     assert pda.choose_kernel(S, Hk, MB, bs, 152, 3, 4) == (kind, splits, launches)
 
 
+# ----------------------------------------------------------- tail pieces
+
+@pytest.mark.parametrize("pages,K,C,bs,want", [
+    (256, 224, 456, 16, [126, 64, 32, 17, 17]),   # 256 x 4096 tokens: 224 tail units shrink
+    (64, 224, 456, 64, [31, 16, 8, 4, 5]),        # 128 x 8192, 64-token blocks, 2 splits
+    (11, 56, 456, 128, [2, 2, 2, 2, 3]),          # a short tail: equal pieces, none empty
+    (69, 48, 456, 16, [17, 17, 17, 18]),          # equal pieces of a 69-page unit
+    (128, 128, 456, 16, [16] * 8),                # equal pieces at the cap of 8
+    (63, 224, 456, 16, [63]),                     # under 1024 tokens: whole
+    (0, 224, 456, 16, [0]),                       # an empty split stays whole
+])
+def test_tail_piece_table(lib, pages, K, C, bs, want):
+    assert pda.tail_pieces(pages, K, C, bs) == want
+
+
+def test_tail_piece_invariants(lib):
+    # every cut covers the unit, pieces are never empty, hold at least 256
+    # tokens (the last shrinking piece may hold fewer only when the rest is
+    # smaller than that), stay within the cap, and shrinking pieces never grow
+    # by more than the minimum piece
+    for bs in (16, 32, 48, 64, 128):
+        m = -(-256 // bs)
+        for C in (152, 456, 608):
+            for K in (1, 7, C // 4, C // 3, C // 3 + 1, C // 2, C - 1):
+                for pages in range(0, 300, 7):
+                    sizes = pda.tail_pieces(pages, K, C, bs)
+                    assert sum(sizes) == pages, (bs, C, K, pages, sizes)
+                    assert 1 <= len(sizes) <= 8
+                    if len(sizes) == 1:
+                        continue
+                    assert pages >= 4 * m
+                    assert min(sizes) >= m, (bs, C, K, pages, sizes)
+                    if 3 * K < C:
+                        assert max(sizes) - min(sizes) <= 1
+                        assert len(sizes) <= -(-2 * C // K)
+                    else:
+                        assert all(b <= a + m for a, b in zip(sizes, sizes[1:])), (bs, C, K, pages, sizes)
+
+
+def test_tail_pieces_rejects_bad_arguments(lib):
+    for args in [(-1, 10, 456, 16), (10, 0, 456, 16), (10, 456, 456, 16), (10, 10, 456, 24), (10, 10, 0, 16)]:
+        with pytest.raises(pda.PdaError):
+            pda.tail_pieces(*args)
+
+
 def test_choose_kernel_rejects_bad_sizes(lib):
     for args in [(0, 8, 64, 16, 152, 3, 4), (16, 0, 64, 16, 152, 3, 4), (16, 8, 0, 16, 152, 3, 4),
                  (16, 8, 64, 16, 0, 3, 4), (16, 8, 64, 16, 152, 0, 4), (16, 8, 64, 16, 152, 3, 0)]:
