@@ -1,7 +1,7 @@
 /* A plain C11 caller of the C ABI (include/pda.h): compiled and run by
  * tests/test_abi.py. Only host-side paths are used, so no GPU is needed:
- * the pure planner, status strings, and argument checks that return before
- * any CUDA call. */
+ * the pure planner, the tail-piece cut, status strings, and argument checks
+ * that return before any CUDA call. */
 #include <stdio.h>
 #include <string.h>
 
@@ -24,6 +24,10 @@ int main(void) {
   if (pda_decode_host(out, q, k, v, table, lens, 1, 8, 2, 128, 16, 2, 4, 0.1f, 0.05f, 0.05f, NULL) !=
       PDA_ERR_INVALID_ARG)
     return 5;
+  /* the tail-piece cut of the 256 x 4096-token batch: 5 shrinking pieces */
+  int sizes[8] = {0};
+  if (pda_tail_pieces(256, 224, 456, 16, sizes, 8) != 5 || sizes[0] != 126 || sizes[4] != 17) return 6;
+  if (pda_tail_pieces(256, 456, 456, 16, sizes, 8) != -1) return 7;
   puts("ok");
   return 0;
 }
