@@ -433,7 +433,10 @@ int pda_choose_kernel(int num_seqs, int num_kv_heads, int max_num_blocks_per_seq
  * pda_plan_launches -- kernels one pda_decode call launches for these sizes
  * on the current device: the decode kernel, plus the unit-order kernel when
  * the persistent kernel has more units than resident CTAs (up to 16384
- * units), plus the merge kernel when the call splits. A one-wave per-unit
+ * units), plus the tail merge kernel when those units leave a partial last
+ * round (units modulo resident CTAs > 0; it runs even when no unit of that
+ * round is long enough to cut), plus the merge kernel when the call splits
+ * (with pda_set_tail_split(0): no tail merge kernel). A one-wave per-unit
  * call of 2 to 16 splits has no merge launch: the splits of each (sequence,
  * kv head) run as one thread-block cluster and combine their results
  * through distributed shared memory. 0 for num_seqs == 0;
