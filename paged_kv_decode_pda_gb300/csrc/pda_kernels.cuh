@@ -167,18 +167,6 @@ struct DecodeParams {
   float* tail_rows = nullptr;
 };
 constexpr int kTailRowFloats = kMaxGqa * (kHeadDim + 2);
-constexpr int kScaleRowsPieces = 0;
-constexpr int kScaleRowsGather4 = 1;
-constexpr int kScaleRowsBulk = 2;
-
-// The rows b * Hk + kvh of a stage's np (1..4) pages in a table or cache
-// viewed as [NB * Hk] rows, for a four-row gather; rows past np repeat the
-// first (the gather lands them in the stage's unused page slots).
-__device__ __forceinline__ int4 stage_rows(const int* blk, int np, int Hk, int kvh) {
-  const int r0 = blk[0] * Hk + kvh;
-  return make_int4(r0, np > 1 ? blk[1] * Hk + kvh : r0, np > 2 ? blk[2] * Hk + kvh : r0,
-                   np > 3 ? blk[3] * Hk + kvh : r0);
-}
 constexpr int kMaxTailPieces = 8;  // most pieces a tail unit is cut into
 // A tail unit is cut only when it holds at least kMinCutPieces pieces of
 // the minimum size: the tail merge kernel's fold costs about as much as a
@@ -186,6 +174,20 @@ constexpr int kMaxTailPieces = 8;  // most pieces a tail unit is cut into
 // tokens: its shortest units in 2 pieces took 161.2 us per call, left
 // whole 159.0 us).
 constexpr int kMinCutPieces = 4;
+
+// DecodeParams::scale_rows: how a stage's per-slot scale rows arrive.
+constexpr int kScaleRowsPieces = 0;
+constexpr int kScaleRowsGather4 = 1;
+constexpr int kScaleRowsBulk = 2;
+
+// The rows b * Hk + kvh of a stage's np (1..4) pages in a table or cache
+// viewed as [NB * Hk] rows, for a four-row gather; rows past np repeat the
+// first (the gather lands them in the stage's unused slots).
+__device__ __forceinline__ int4 stage_rows(const int* blk, int np, int Hk, int kvh) {
+  const int r0 = blk[0] * Hk + kvh;
+  return make_int4(r0, np > 1 ? blk[1] * Hk + kvh : r0, np > 2 ? blk[2] * Hk + kvh : r0,
+                   np > 3 ? blk[3] * Hk + kvh : r0);
+}
 
 // Splits of a sequence with `pages` pages that hold at least one page (the
 // others are empty: they write no partial and take no part in the merge).
@@ -1890,7 +1892,7 @@ __global__ void __launch_bounds__(kOrderThreads) pda_order_units_kernel(const Or
     P = tail_piece_count(n, K, C, m, p.max_pieces);
   }
   __shared__ int scan_buf[32];
-  int total = 0;
+  int total = 0;  // rows slots in all (sized by the host: at most K * max_pieces)
   const int slot0 = order_block_scan(P, scan_buf, &total);
   if (tid < K) p.tail_info[tid] = make_int4(u, slot0, P, 0);
   int issued = 0;  // tickets of the earlier piece indices
