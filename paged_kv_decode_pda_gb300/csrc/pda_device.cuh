@@ -149,6 +149,11 @@ __device__ __forceinline__ void tma_gather4_rows(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// Fetch a kernel-parameter tensor map's descriptor ahead of its first copy.
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 // --------------------------------------------------------- warp fragments
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {

@@ -126,10 +126,10 @@ struct DecodeParams {
   // kScaleRowsBulk: one bulk copy per row; kScaleRowsPieces: 16-byte
   // cp.async pieces spread over the producer warp.
   int scale_rows = 0;
-  // Persistent kernel, page-major 16-token pages (4 a stage): 1 = a stage's
-  // 4 K pages and 4 V pages arrive as one four-row gather each through
-  // tm_k / tm_v (2-D maps over the caches as [NB * Hk] rows of one 2 KiB
-  // page); 0 = one bulk copy per page.
+  // Page-major 16-token pages (4 a stage), not per-slot scales nor cluster
+  // merges: 1 = a stage's 4 K pages and 4 V pages arrive as one four-row
+  // gather each through tm_k / tm_v (2-D maps over the caches as [NB * Hk]
+  // rows of one 2 KiB page); 0 = one bulk copy per page.
   int page_gather = 0;
   float logit_scale_log2;       // scale * k_scale * log2(e)  (scale * log2(e) with slot scales)
   float v_scale;                // per-tensor V scale (unused with slot scales)
@@ -848,6 +848,11 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
   const int g = p.gqa;
 
   const bool cluster = kCluster && p.cluster_merge != 0;
+  if (!kSlotScales && !kTokenMajor && p.page_gather && threadIdx.x == kConsumerWarps * 32) {
+    // the producer's descriptors, fetched while the table loads below run
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+  }
 
   int L = __ldg(p.seq_lens + s);
   L = max(0, min(L, p.max_blocks * bs));
@@ -936,7 +941,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
           uint32_t scale_tx = 0u;
           if (kSlotScales && p.scale_rows == kScaleRowsGather4) scale_tx = 2u * 4u * row_bytes;
           if (kSlotScales && p.scale_rows == kScaleRowsBulk) scale_tx = 2u * (uint32_t)np * row_bytes;
-          mbar_arrive_expect_tx(bar, 2u * page_bytes * (uint32_t)np + scale_tx);
+          const bool gather = !kSlotScales && !kTokenMajor && p.page_gather;
+          mbar_arrive_expect_tx(bar, 2u * page_bytes * (uint32_t)(gather ? 4 : np) + scale_tx);
           if constexpr (kSlotScales) {
             // K rows at scale_off, V rows PPS rows further; row of page t:
             // b * Hk + kvh of its table
@@ -984,6 +990,12 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
                 tma_load_4d(sbase + (uint32_t)(PPS + t) * page_bytes, &tm_v, 0, 0, kvh, blk[t], bar);
               }
             }
+          } else if (gather) {
+            // 16-token pages: two copies a stage instead of eight (GB300,
+            // 64 x 1024 tokens in one wave: 27.38 against 27.76 us per call)
+            const int4 r = stage_rows(blk, np, p.num_kv_heads, kvh);
+            tma_gather4_rows(sbase, &tm_k, r.x, r.y, r.z, r.w, bar);
+            tma_gather4_rows(sbase + (uint32_t)PPS * page_bytes, &tm_v, r.x, r.y, r.z, r.w, bar);
           } else {
 #pragma unroll
             for (int t = 0; t < kMaxPagesPerStage; ++t) {
@@ -1424,9 +1436,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
             } else if (p.page_gather) {
               // 16-token pages: two copies a stage instead of eight (GB300,
               // us per call: 256 x 4096 tokens 309.1 against 311.4, 256 x
-              // 1-4000 tokens 155.6 against 158.3; the one-wave per-unit
-              // kernel gained nothing from it: 16 x 1024 tokens 12.77
-              // against 12.64)
+              // 1-4000 tokens 155.6 against 158.3)
               if (np > 0) {
                 const int4 r = stage_rows(blk, np, p.num_kv_heads, kvh);
                 tma_gather4_rows(sbase, &tm_k, r.x, r.y, r.z, r.w, bar);

@@ -328,15 +328,26 @@ def test_tail_pieces_parity(S, H, Hk, ctx, bs, splits, spread):
     assert pda.query_device_status() == 0
 
 
-@pytest.mark.parametrize("S,splits,shuffled", [(160, 0, False), (160, 2, False), (700, 0, True)])
-def test_page_gathers_bitwise_equal_to_page_copies(S, splits, shuffled):
-    """16-token pages reach the persistent kernel's stages as four-page
-    gathers or as one bulk copy per page: the same bytes, so the same bits.
-    Ragged lengths give last stages of 1 to 3 pages (the gather repeats the
-    first row into the unused slots), empty and one-token sequences."""
+@pytest.mark.parametrize("S,splits,shuffled,kind", [
+    (160, 0, False, pda.PDA_KERNEL_PERSISTENT),
+    (160, 2, False, pda.PDA_KERNEL_PERSISTENT),
+    (700, 0, True, pda.PDA_KERNEL_PERSISTENT),
+    (60, 0, False, pda.PDA_KERNEL_PER_UNIT_DENSE),   # one wave, no split
+    (2, 20, True, pda.PDA_KERNEL_PER_UNIT_DENSE),    # one wave, 20 splits: the merge kernel, no clusters
+])
+def test_page_gathers_bitwise_equal_to_page_copies(S, splits, shuffled, kind):
+    """16-token pages reach the stages as four-page gathers or as one bulk
+    copy per page: the same bytes, so the same bits, on the persistent
+    kernel and on per-unit grids that do not merge in clusters. Ragged
+    lengths give last stages of 1 to 3 pages (the gather repeats the first
+    row into the unused slots), empty and one-token sequences."""
     batch = _many(S, 16, seed=300 + S + splits, max_len=700)
     cfg = batch.cfg
-    assert _kernel(batch) == pda.PDA_KERNEL_PERSISTENT
+    pda.set_split_override(splits)
+    try:
+        assert _kernel(batch) == kind
+    finally:
+        pda.set_split_override(0)
     v = batch.v_cache
     if shuffled:  # [NB, Hk, bs/16, 128, 16]: the same values (bitwise the same outputs)
         NB, Hk, D, bs = v.shape
